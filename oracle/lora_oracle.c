@@ -1,0 +1,236 @@
+/*
+ * CPU oracle for the batched multi-adapter LoRA side branch.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the library's product path may link,
+ * load or call this file; only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header or constant with the CUDA
+ * library: it is a plain, slow restatement of what the pages define, in double
+ * precision, with no blocking, fusion or reordering.
+ *
+ * Notation (PEFT orientation, vLLM LoRA deep-dive page, §1 "LoRA 数学原理" and
+ * §4 "完整推理流程": lora_a is (r, k), lora_b is (d, r)):
+ *   x     [T, k]      input rows, one per token
+ *   A_s,i [r_s, k]    down projection of slot s, output slice i
+ *   B_s,i [d_i, r_s]  up projection of slot s, output slice i
+ *   y     [T, d]      output rows; slice i occupies columns [o_i, o_i + d_i)
+ *
+ * Branch (llama.cpp LoRA adapter page, §"为什么低秩增量可以「后加」" and
+ * §"真正的核心:建图时如何把低秩分支拼进去"; vLLM book ch. 16, §16.1.3
+ * "推理时的叠加式计算"; TensorRT-LLM LoRA serving page, §"与基座并行:
+ * forward_with_base", add_lora_result): for every token t whose slot
+ * s = slot_ids[t] is in [0, S) with r_s > 0, for every slice i and column m:
+ *     y[t, o_i + m] = y_in[t, o_i + m]
+ *                     + scale_s * sum_j ( sum_c x[t,c] * A_s,i[j,c] ) * B_s,i[m,j]
+ * Every other row is left as it was.  Slot -1 means "no adapter" (vLLM book
+ * ch. 16, §16.4.2, token_lora_mapping).
+ *
+ * Index (TensorRT-LLM LoRA serving page, §"一次 decode 批次的路由", steps 2
+ * and 4: sorted ids, bincount, cumsum with one extra entry holding the total;
+ * vLLM book ch. 16, §16.4.3, the five LoRAKernelMeta tensors):
+ *   key(t) = slot_ids[t] if 0 <= slot_ids[t] < S, else S (the "no adapter"
+ *            bucket, placed last like TensorRT-LLM's sentinel slot);
+ *   sorted_ids = tokens 0..T-1 in ascending key order, ties in ascending token
+ *                index;
+ *   seg_offsets[b] = #{t : key(t) < b} for b = 0..S+1;
+ *   active = [count, s_1 < s_2 < ...] for slots with >= 1 token and r_s > 0.
+ * A slot id outside [-1, S) is an error; the token goes to the last bucket and
+ * is left unchanged by the branch.
+ *
+ * parity: pinned by tests/test_oracle_pins.py (library matmul, merged-weight
+ * identity, closed forms, brute force over all permutations of tiny inputs).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_SLOT_RANGE 1
+
+/* bf16 is the upper half of an IEEE binary32; widening is exact. */
+static double bf16_value(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+double oracle_bf16_to_double(uint16_t bits) { return bf16_value(bits); }
+
+/*
+ * Round a double to the nearest bf16 (8 significant bits, binary32 exponent
+ * range), ties to even, written from the format's definition: split off the
+ * exponent, scale the significand to an integer grid, round half-to-even.
+ */
+uint16_t oracle_round_bf16(double v)
+{
+    if (isnan(v)) return 0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    int e;
+    (void)frexp(a, &e);                 /* a = m * 2^e, 0.5 <= m < 1 */
+    int q_exp = e - 8;                  /* quantum of an 8-bit significand */
+    if (q_exp < -133) q_exp = -133;     /* subnormal quantum 2^(-126-7) */
+    double scaled = ldexp(a, -q_exp);   /* exact: only the exponent changes */
+    double fl = floor(scaled);
+    double frac = scaled - fl;
+    double q;
+    if (frac > 0.5) q = fl + 1.0;
+    else if (frac < 0.5) q = fl;
+    else q = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+    double r = ldexp(q, q_exp);
+    if (r >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80); /* overflow to inf */
+    float f = (float)r;                 /* exact: r has <= 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | (uint16_t)(u >> 16));
+}
+
+/*
+ * Per-slot scale.  llama.cpp's get_scale (llama.cpp LoRA adapter page,
+ * §"缩放系数到底乘在哪"): alpha ? adapter_scale * alpha / rank : adapter_scale.
+ * rsLoRA (vLLM LoRA deep-dive page, §1, "rsLoRA 变体"): alpha / sqrt(rank).
+ * The runtime strength multiplies either rule; alpha == 0 means "alpha/r is 1".
+ */
+double oracle_scale(double alpha, int32_t rank, int32_t rslora, double adapter_scale)
+{
+    if (alpha == 0.0 || rank <= 0) return adapter_scale;
+    if (rslora) return adapter_scale * alpha / sqrt((double)rank);
+    return adapter_scale * alpha / (double)rank;
+}
+
+/* Fold a scale into B (vLLM LoRA deep-dive page, §1 "推理优化:预合并 scaling",
+ * LoRALayerWeights.optimize: lora_b *= scaling): bf16(s * B), nearest-even. */
+void oracle_premultiply(const uint16_t *b, int64_t n, double s, uint16_t *out)
+{
+    for (int64_t e = 0; e < n; ++e) out[e] = oracle_round_bf16(s * bf16_value(b[e]));
+}
+
+typedef struct { int32_t key; int32_t t; } key_token_t;
+
+static int cmp_key_token(const void *pa, const void *pb)
+{
+    const key_token_t *a = (const key_token_t *)pa, *b = (const key_token_t *)pb;
+    if (a->key != b->key) return a->key < b->key ? -1 : 1;
+    return a->t < b->t ? -1 : (a->t > b->t ? 1 : 0);
+}
+
+/* Returns ORACLE_OK or ORACLE_ERR_SLOT_RANGE (first error); outputs are always
+ * written.  A comparison sort on unique (key, token) pairs gives the stable
+ * order; the offsets are counted straight from their definition. */
+int oracle_build_index(const int32_t *slot_ids, int32_t T, int32_t S, const int32_t *ranks,
+                       int32_t *sorted_ids, int32_t *seg_offsets, int32_t *active)
+{
+    int status = ORACLE_OK;
+    key_token_t *pairs = (key_token_t *)malloc(sizeof(key_token_t) * (size_t)(T > 0 ? T : 1));
+    int32_t *key = (int32_t *)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
+    for (int32_t t = 0; t < T; ++t) {
+        int32_t s = slot_ids[t];
+        if (s >= 0 && s < S) {
+            key[t] = s;
+        } else {
+            key[t] = S;
+            if (s != -1) status = ORACLE_ERR_SLOT_RANGE;
+        }
+        pairs[t].key = key[t];
+        pairs[t].t = t;
+    }
+    qsort(pairs, (size_t)T, sizeof(key_token_t), cmp_key_token);
+    for (int32_t p = 0; p < T; ++p) sorted_ids[p] = pairs[p].t;
+    for (int32_t b = 0; b <= S + 1; ++b) {
+        int32_t c = 0;
+        for (int32_t t = 0; t < T; ++t) c += (key[t] < b);
+        seg_offsets[b] = c;
+    }
+    int32_t n_active = 0;
+    for (int32_t s = 0; s < S; ++s) {
+        int32_t count = 0;
+        for (int32_t t = 0; t < T; ++t) count += (key[t] == s);
+        if (count > 0 && ranks[s] > 0) active[1 + n_active++] = s;
+    }
+    active[0] = n_active;
+    free(pairs);
+    free(key);
+    return status;
+}
+
+/*
+ * Shrink for a list of rows: xa[q][i][j] = sum_c x[t,c] * A_s,i[j,c] with
+ * t = rows[q], s = slot_ids[t], j < r_s; entries j >= r_s and rows without an
+ * active slot are left as they were.  A is indexed [s * n_slices + i].
+ * *macs is increased by the multiply-adds performed.
+ */
+void oracle_shrink(const uint16_t *x, int64_t ldx, int32_t k, int32_t n_slices,
+                   const int32_t *slot_ids, int32_t S, const int32_t *ranks,
+                   const uint16_t *const *A, const int32_t *rows, int32_t n_rows,
+                   int32_t r_max, double *xa, int64_t *macs)
+{
+    for (int32_t q = 0; q < n_rows; ++q) {
+        int32_t t = rows[q];
+        int32_t s = slot_ids[t];
+        if (s < 0 || s >= S || ranks[s] <= 0) continue;
+        const uint16_t *xt = x + (int64_t)t * ldx;
+        for (int32_t i = 0; i < n_slices; ++i) {
+            const uint16_t *a = A[(int64_t)s * n_slices + i];
+            for (int32_t j = 0; j < ranks[s]; ++j) {
+                double acc = 0.0;
+                for (int32_t c = 0; c < k; ++c) acc += bf16_value(xt[c]) * bf16_value(a[(int64_t)j * k + c]);
+                xa[((int64_t)q * n_slices + i) * r_max + j] = acc;
+                *macs += k;
+            }
+        }
+    }
+}
+
+/*
+ * Full branch for a list of rows: y_out[q][:] is row rows[q] of the result, in
+ * double, before any rounding to bf16.  y_in may be NULL (zeros).  scales are
+ * per slot.  B is indexed [s * n_slices + i].  Returns ORACLE_ERR_SLOT_RANGE if
+ * a listed row carries a slot id outside [-1, S).
+ */
+int oracle_apply(const uint16_t *x, int64_t ldx, const uint16_t *y_in, int64_t ldy,
+                 int32_t k, int32_t n_slices, const int32_t *slice_offsets,
+                 const int32_t *slot_ids, int32_t S, const int32_t *ranks, const double *scales,
+                 const uint16_t *const *A, const uint16_t *const *B,
+                 const int32_t *rows, int32_t n_rows, double *y_out, int64_t *macs)
+{
+    int status = ORACLE_OK;
+    int32_t d = slice_offsets[n_slices];
+    double *xa = (double *)malloc(sizeof(double) * 512);
+    for (int32_t q = 0; q < n_rows; ++q) {
+        int32_t t = rows[q];
+        double *yo = y_out + (int64_t)q * d;
+        for (int32_t m = 0; m < d; ++m) yo[m] = y_in ? bf16_value(y_in[(int64_t)t * ldy + m]) : 0.0;
+        int32_t s = slot_ids[t];
+        if (s != -1 && (s < 0 || s >= S)) { status = ORACLE_ERR_SLOT_RANGE; continue; }
+        if (s < 0 || ranks[s] <= 0) continue;
+        int32_t r = ranks[s];
+        if (r > 512) { free(xa); xa = (double *)malloc(sizeof(double) * (size_t)r); }
+        const uint16_t *xt = x + (int64_t)t * ldx;
+        for (int32_t i = 0; i < n_slices; ++i) {
+            const uint16_t *a = A[(int64_t)s * n_slices + i];
+            const uint16_t *b = B[(int64_t)s * n_slices + i];
+            /* shrink: xa_j = x_t . A_j */
+            for (int32_t j = 0; j < r; ++j) {
+                double acc = 0.0;
+                for (int32_t c = 0; c < k; ++c) acc += bf16_value(xt[c]) * bf16_value(a[(int64_t)j * k + c]);
+                xa[j] = acc;
+                *macs += k;
+            }
+            /* expand: y += scale * B xa over this slice's columns */
+            int32_t o = slice_offsets[i];
+            int32_t di = slice_offsets[i + 1] - slice_offsets[i];
+            for (int32_t m = 0; m < di; ++m) {
+                double acc = 0.0;
+                for (int32_t j = 0; j < r; ++j) acc += xa[j] * bf16_value(b[(int64_t)m * r + j]);
+                yo[o + m] += scales[s] * acc;
+                *macs += r;
+            }
+        }
+        if (r > 512) { free(xa); xa = (double *)malloc(sizeof(double) * 512); }
+    }
+    free(xa);
+    return status;
+}

@@ -1,0 +1,73 @@
+"""Plant plausible mistakes in a copy of the oracle and check the pins catch them.
+
+Each mutant is the oracle's C source with one edit (a dropped term, a wrong sign
+or index, a transposed operand, a wrong tie order ...), compiled with gcc into a
+temporary directory.  The pins of test_oracle_pins.py are then run against it;
+at least one must fail.  This runs on the CPU only.
+"""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "lora_oracle.c")
+
+MUTANTS = {
+    "drop_scale": ("yo[o + m] += scales[s] * acc;", "yo[o + m] += acc;"),
+    "wrong_sign": ("yo[o + m] += scales[s] * acc;", "yo[o + m] -= scales[s] * acc;"),
+    "drop_slice_offset": ("yo[o + m] += scales[s] * acc;", "yo[m] += scales[s] * acc;"),
+    "transposed_B": ("bf16_value(b[(int64_t)m * r + j])", "bf16_value(b[(int64_t)j * di + m])"),
+    "reversed_x": ("for (int32_t c = 0; c < k; ++c) acc += bf16_value(xt[c]) * bf16_value(a[(int64_t)j * k + c]);\n                xa[j] = acc;",
+                   "for (int32_t c = 0; c < k; ++c) acc += bf16_value(xt[k - 1 - c]) * bf16_value(a[(int64_t)j * k + c]);\n                xa[j] = acc;"),
+    "drop_y_in": ("yo[m] = y_in ? bf16_value(y_in[(int64_t)t * ldy + m]) : 0.0;", "yo[m] = 0.0;"),
+    "unstable_ties": ("return a->t < b->t ? -1 : (a->t > b->t ? 1 : 0);", "return a->t > b->t ? -1 : (a->t < b->t ? 1 : 0);"),
+    "offsets_off_by_one": ("c += (key[t] < b);", "c += (key[t] <= b);"),
+    "no_adapter_bucket_first": ("key[t] = S;\n            if (s != -1)", "key[t] = -1;\n            if (s != -1)"),
+    "active_keeps_rank0": ("if (count > 0 && ranks[s] > 0) active", "if (count > 0) active"),
+    "rslora_without_sqrt": ("adapter_scale * alpha / sqrt((double)rank)", "adapter_scale * alpha / (double)rank"),
+    "alpha_zero_not_special": ("if (alpha == 0.0 || rank <= 0) return adapter_scale;", "if (rank <= 0) return adapter_scale;"),
+    "ties_away_from_zero": ("q = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;", "q = fl + 1.0;"),
+    "rank_loop_short": ("for (int32_t j = 0; j < r; ++j) {\n                double acc = 0.0;", "for (int32_t j = 0; j + 1 < r; ++j) {\n                double acc = 0.0;"),
+}
+
+PINS = [
+    lambda: pins.test_index_brute_force_all_tiny_inputs((8, 8)),
+    lambda: pins.test_index_brute_force_all_tiny_inputs((0, 16)),
+    lambda: pins.test_index_matches_library_stable_sort(1),
+    pins.test_branch_matches_library_matmul,
+    pins.test_merged_weight_identity,
+    pins.test_orientation_matches_printed_shapes,
+    pins.test_closed_form_one_hot_rank1,
+    pins.test_zero_B_and_no_adapter_rows_are_unchanged,
+    pins.test_rslora_versus_standard_scale,
+    pins.test_scale_values_printed_on_pages,
+    pins.test_premultiplied_scale_equals_runtime_scale,
+    pins.test_rank_concatenation_identity,
+    pins.test_mac_count_matches_pages,
+    pins.test_rank0_slot_and_out_of_range_slot,
+    pins.test_round_bf16_against_brute_force,
+]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path, monkeypatch):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mutated = src.replace(old, new, 1)
+    c_path = tmp_path / "mutant.c"
+    c_path.write_text(mutated)
+    so_path = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", str(so_path), str(c_path), "-lm"])
+    monkeypatch.setattr(oracle, "_lib", oracle.configure(ctypes.CDLL(str(so_path))))
+    failures = 0
+    for pin in PINS:
+        try:
+            pin()
+        except AssertionError:
+            failures += 1
+    assert failures > 0, f"no pin caught mutant {name}"
