@@ -1,0 +1,506 @@
+#!/usr/bin/env python
+"""Benchmark of the batched multi-adapter LoRA branch on GB300.
+
+Workload (default): the Llama-3-8B packed QKV projection at decode, T=256 tokens
+(one per request), k=4096, output slices 4096/1024/1024, 32 resident adapters
+with ranks drawn from {8, 16, 32, 64}, Zipf(1.1) slot popularity, alpha = 2r.
+All inputs are seeded and synthetic (workloads.config(2)).
+
+A step is one pass of the whole hot path over one batch: re-upload one slot
+table (what a slot change costs), build the token index, then run the branch on
+the QKV projection of each of ``--layers`` (32) layers, each with its own
+adapter weights, x and y buffers, so the working set (about 1.3 GB) is far
+larger than the 129 MB L2 and every call streams from HBM.  The step is
+captured once in a CUDA graph and replayed; CUDA events on the launching stream
+time exactly K replays after W warm-up replays.
+
+Metric: LoRA-branch tokens/s (tokens through one projection call per second:
+T * layers / step time) and achieved HBM GB/s of the algorithmic bytes of each
+call against the measured copy bandwidth.  One JSON line on rank 0.
+
+``--impl reference`` times the CPU oracle (plain C, fp64) on the host cores
+instead, on the same workload; under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+CONFIG_INDEX = {name: i for i, name in enumerate(W.CONFIG_NAMES)}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default="decode_qkv", choices=list(CONFIG_INDEX))
+    p.add_argument("--layers", type=int, default=32)
+    p.add_argument("--path", default="auto", choices=["auto", "decode_fused", "decode_split", "prefill"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-baseline sample")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# Accounting (measurement, not the method): bytes and flops a call must move
+# ---------------------------------------------------------------------------
+def algorithmic_bytes(slot_ids, ranks, k, widths) -> int:
+    """Each active slot's A and B once (bf16), x rows of LoRA tokens once, their
+    y rows read and written (bf16).  Workspace, index and no-adapter rows excluded."""
+    S, n, d = len(ranks), len(widths), int(sum(widths))
+    ids = np.asarray(slot_ids)
+    valid = (ids >= 0) & (ids < S)
+    lora = np.zeros(len(ids), dtype=bool)
+    lora[valid] = np.asarray(ranks)[ids[valid]] > 0
+    n_l = int(lora.sum())
+    weights = sum(2 * int(ranks[s]) * (n * k + d) for s in np.unique(ids[lora]))
+    return int(weights + 2 * k * n_l + 4 * d * n_l)
+
+
+def algorithmic_flops(slot_ids, ranks, k, widths) -> int:
+    S, n, d = len(ranks), len(widths), int(sum(widths))
+    return int(sum(2 * int(ranks[s]) * (n * k + d) for s in slot_ids if 0 <= s < S and ranks[s] > 0))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", FALLBACK_BF16_TFLOPS)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (replicas: each rank runs the same workload on its GPU)
+# ---------------------------------------------------------------------------
+def dist_info():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def dist_init(backend):
+    import torch.distributed as dist
+    rank, world, _ = dist_info()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        os.environ.setdefault("MASTER_PORT", "29511")
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return rank, world
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest value over ranks (the slowest replica sets the job's time)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, elapsed_per_rank: float, world: int, device=None) -> float:
+    """Whole-job rate: the units all ranks processed over the slowest rank's time."""
+    return units_per_rank * world / max_over_ranks(elapsed_per_rank, device)
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 20):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.interval_ms = interval_ms
+        self._thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(self.interval_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self._thread = threading.Thread(target=self._read, daemon=True)
+        self._thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        def flag(v):
+            return v.lower() in ("active", "1", "yes", "true") or v.startswith("0x") and int(v, 16) != 0
+
+        window = [s for (t, s) in self.samples if t0 <= t <= t1 and len(s) >= 9]
+        if not window:  # the timed region was shorter than the sampling period: nearest samples
+            window = sorted((abs(t - (t0 + t1) / 2), s) for (t, s) in self.samples if len(s) >= 9)[:3]
+            window = [s for _, s in window]
+        if not window:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sm = [float(s[1]) for s in window if s[1].replace(".", "").isdigit()]
+        smax = [float(s[2]) for s in window if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for s in window for j in range(4) if flag(s[5 + j])})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(window)}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+def _workload(name):
+    idx = CONFIG_INDEX[name]
+    return W.config(idx, y_init="normal")
+
+
+def run_ours(args):
+    import torch
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import ResidentProjection
+
+    rank, world = dist_init("nccl")
+    _, _, local = dist_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    wl = _workload(args.config)
+    mods = list(range(len(wl.modules)))
+    # layer l uses projection mods[l % len(mods)] in its own buffers
+    base = [ResidentProjection.from_workload(wl, m, device=dev) for m in mods]
+    layers = []
+    for l in range(args.layers):
+        src = base[l % len(base)]
+        layers.append(src if l < len(base) else src.clone(device=dev))
+    T, S = wl.T, wl.S
+    counts = np.bincount(wl.slot_ids[wl.slot_ids >= 0], minlength=S)
+    max_seg = int(counts.max()) if counts.size else 0
+    slot_dev = torch.from_numpy(wl.slot_ids).to(dev)
+    index = L.TokenIndex(T, S, device=dev)
+    ws = [L.Workspace(T, lay.shape, device=dev) for lay in layers[:len(base)]]
+    ws_of = [ws[l % len(ws)].buf for l in range(len(layers))]
+
+    def apply_layer(l):
+        lay = layers[l]
+        L.lora_apply(lay.x, lay.y, lay.shape, lay.table.dev, index.sorted_ids, index.seg_offsets, index.active,
+                     ws_of[l], index.err, max_seg_hint=max_seg, path=args.path)
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def index_part():
+        layers[0].refresh_table()
+        index.build(slot_dev, layers[0].table)
+
+    def apply_part():
+        for l in range(len(layers)):
+            apply_layer(l)
+
+    # eager warm-up (sets kernel attributes), then capture the two parts of a step
+    with torch.cuda.stream(stream):
+        index_part()
+        apply_part()
+    torch.cuda.synchronize()
+    g_index, g_apply = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_index, stream=stream):
+        index_part()
+    with torch.cuda.graph(g_apply, stream=stream):
+        apply_part()
+    torch.cuda.synchronize()
+
+    def replay(events=None):
+        if events is None:
+            g_index.replay()
+            g_apply.replay()
+        else:
+            g_index.replay()
+            events[0].record()
+            g_apply.replay()
+            events[1].record()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            replay()
+    torch.cuda.synchronize()
+
+    peak_gbs, peak_tf, peak_src = measured_peaks()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    w0 = time.time()
+    with torch.cuda.stream(stream):
+        t_start.record()
+        for k in range(args.steps):
+            replay(marks[k])
+        t_end.record()
+    torch.cuda.synchronize()
+    w1 = time.time()
+    barrier()
+    time.sleep(0.1)
+    sampler.stop()
+    elapsed_s = t_start.elapsed_time(t_end) / 1e3
+    apply_ms = [a.elapsed_time(b) for a, b in marks]          # the L calls of every step
+    apply_ms_mean = float(np.mean(apply_ms))
+    index_ms_mean = (elapsed_s * 1e3 - float(np.sum(apply_ms))) / args.steps
+    err = int(index.err.item())
+
+    units = T * len(layers) * args.steps
+    value = job_throughput(units, elapsed_s, world, dev)
+    ms_per_step = max_over_ranks(elapsed_s, dev) / args.steps * 1e3
+
+    bytes_per_call = [algorithmic_bytes(wl.slot_ids, wl.ranks, wl.modules[m].k, wl.modules[m].slice_widths)
+                      for m in mods]
+    flops_per_call = [algorithmic_flops(wl.slot_ids, wl.ranks, wl.modules[m].k, wl.modules[m].slice_widths)
+                      for m in mods]
+    per_layer_bytes = [bytes_per_call[l % len(mods)] for l in range(len(layers))]
+    per_layer_flops = [flops_per_call[l % len(mods)] for l in range(len(layers))]
+    call_s = apply_ms_mean / 1e3 / len(layers)
+    achieved_gbs = sum(per_layer_bytes) / len(layers) / call_s / 1e9
+    resolved, launches_per_apply = L.lora_resolve_path(args.path, T, max_seg)
+    gpu_launches = args.steps * (1 + len(layers) * launches_per_apply)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, wl, layers, index, slot_dev, ws_of, max_seg, dev, world)
+
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        cpu = cpu_baseline(wl, args.cpu_seconds)
+
+    clocks = sampler.summary(w0, w1)
+    out = {
+        "metric": "LoRA-branch tokens/s (Llama-3-8B packed QKV decode)",
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded: workloads.config)",
+        "config": {
+            "workload": wl.description if args.config != "decode_qkv" else
+            "decode packed QKV, Llama-3-8B shapes: T=256, k=4096, slices 4096/1024/1024, S=32, "
+            "r in {8,16,32,64} (r_max 64), Zipf(1.1) slot popularity, alpha=2r",
+            "config": args.config,
+            "layers_per_step": len(layers),
+            "calls_per_step": len(layers),
+            "path": resolved,
+            "l2": f"inputs larger than L2: {len(layers)} distinct layer buffer sets, "
+                  f"{sum(per_layer_bytes) / 1e9:.2f} GB of algorithmic bytes per step",
+            "parallelism": f"replicas x{world}",
+        },
+        "gbs": achieved_gbs,
+        "roofline": {
+            "bound": "hbm",
+            "achieved": achieved_gbs,
+            "peak": peak_gbs,
+            "unit": "GB/s",
+            "frac": achieved_gbs / peak_gbs,
+            "traffic": None,
+            "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
+            "kernel": "lora_apply (shrink + expand) per projection call",
+            "bytes_per_call": sum(per_layer_bytes) / len(layers),
+            "flops_per_call": sum(per_layer_flops) / len(layers),
+            "us_per_call": call_s * 1e6,
+            "index_and_table_us": index_ms_mean * 1e3,
+            "frac_of_8000": achieved_gbs / 8000.0,
+        },
+        "gpu_launches": gpu_launches,
+        "clocks": clocks,
+        "device_error": err,
+    }
+    if e2e is not None:
+        out["e2e"] = e2e
+    if cpu is not None:
+        out["cpu_baseline"] = cpu
+    return out, rank
+
+
+def run_e2e(args, wl, layers, index, slot_dev, ws_of, max_seg, dev, world):
+    """Same metric with host buffers: every step copies slot ids and each layer's
+    x and y from pinned host memory, runs the step, and reads every y back."""
+    import torch
+    import rank_adapter_gemm_gb300 as L
+    T = wl.T
+    h_slots = torch.from_numpy(wl.slot_ids).pin_memory()
+    h_x = [lay.x.cpu().pin_memory() for lay in layers]
+    h_y = [lay.y.cpu().pin_memory() for lay in layers]
+    h_out = [torch.empty_like(h).pin_memory() for h in h_y]
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        slot_dev.copy_(h_slots, non_blocking=True)
+        for lay, hx, hy in zip(layers, h_x, h_y):
+            lay.x.copy_(hx, non_blocking=True)
+            lay.y.copy_(hy, non_blocking=True)
+        index.build(slot_dev, layers[0].table)
+        for l, lay in enumerate(layers):
+            L.lora_apply(lay.x, lay.y, lay.shape, lay.table.dev, index.sorted_ids, index.seg_offsets,
+                         index.active, ws_of[l], index.err, max_seg_hint=max_seg, path=args.path)
+        for lay, ho in zip(layers, h_out):
+            ho.copy_(lay.y, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, 200))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with torch.cuda.stream(stream):
+        e0.record()
+        for _ in range(steps):
+            graph.replay()
+        e1.record()
+    torch.cuda.synchronize()
+    elapsed = e0.elapsed_time(e1) / 1e3
+    value = job_throughput(T * len(layers) * steps, elapsed, world, dev)
+    h2d = h_slots.numel() * 4 + sum(h.numel() * 2 for h in h_x) + sum(h.numel() * 2 for h in h_y)
+    d2h = sum(h.numel() * 2 for h in h_out)
+    return {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": steps}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+def _oracle_call(wl, rows):
+    import oracle
+    m = wl.modules[0]
+    rule = oracle.slot_scales(wl.ranks, wl.alphas, wl.scale_rule, False)
+    if wl.premultiplied:
+        B = [[(oracle.premultiply(b, rule[s]) if b is not None else None) for b in row] for s, row in enumerate(m.B)]
+        scales = np.ones(wl.S)
+    else:
+        B, scales = m.B, rule
+    t0 = time.perf_counter()
+    oracle.apply(m.x, m.y_in, m.slice_widths, wl.slot_ids, wl.ranks, scales, m.A, B, rows=rows)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wl, seconds: float):
+    """The oracle as it stands, single-threaded, on repeated passes over the
+    batch's rows until about ``seconds`` of CPU work (at least one pass)."""
+    rows = np.arange(wl.T, dtype=np.int32)
+    done, spent, passes = 0, 0.0, 0
+    while passes == 0 or spent < seconds:
+        spent += _oracle_call(wl, rows)
+        done += len(rows)
+        passes += 1
+    return {"value": done / spent, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{passes} passes of the first projection over all {wl.T} tokens "
+                      f"({done} token-calls, {spent:.1f} s, fp64 C oracle, one thread)"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return None, rank
+    wl = _workload(args.config)
+    rows = np.arange(wl.T, dtype=np.int32)
+    for _ in range(max(args.warmup, 0)):
+        _oracle_call(wl, rows[:max(1, len(rows) // 8)])
+    # each step: the branch for one projection call over a bounded sample of rows
+    budget_s = 150.0
+    per_row = _oracle_call(wl, rows[:8]) / 8
+    n_rows = int(max(1, min(len(rows), budget_s / max(args.steps, 1) / max(per_row, 1e-9))))
+    sample = rows[:n_rows]
+    t = 0.0
+    for _ in range(args.steps):
+        t += _oracle_call(wl, sample)
+    value = n_rows * args.steps / t
+    out = {
+        "metric": "LoRA-branch tokens/s (Llama-3-8B packed QKV decode)",
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded: workloads.config)",
+        "config": {"workload": wl.description, "config": args.config},
+        "impl": "reference",
+        "cpu_baseline": {"kind": "oracle", "cores": 1, "value": value,
+                         "sample": f"{n_rows} of {wl.T} tokens of the first projection per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return out, rank
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        out, rank = run_reference(args)
+    else:
+        out, rank = run_ours(args)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    try:
+        import torch.distributed as dist
+        if dist.is_available() and dist.is_initialized():
+            dist.destroy_process_group()
+    except Exception:
+        pass
+
+
+if __name__ == "__main__":
+    main()

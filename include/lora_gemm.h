@@ -1,0 +1,246 @@
+/*
+ * lora_gemm.h - C ABI of the GB300 (sm_103a) batched multi-adapter LoRA branch.
+ *
+ * The library computes, for a batch of T tokens where token t carries an adapter
+ * slot id slot_ids[t] (-1 = no adapter):
+ *
+ *     y[t, o_i + m] += scale_s * sum_j ( sum_c x[t, c] * A_s,i[j, c] ) * B_s,i[m, j]
+ *
+ * for s = slot_ids[t], every output slice i and column m < d_i.  This is the
+ * unmerged LoRA side branch h = W0 x + (alpha/r) B A x (llama.cpp LoRA adapter
+ * page, section "why the low-rank increment can be added afterwards"; vLLM book
+ * ch. 16, section 16.1.3, Y = xW + s (xA)B), batched over tokens that use
+ * different adapters (vLLM book ch. 16, section 16.4.2, token_lora_mapping with
+ * -1 = no LoRA), with packed projections (QKV, gate_up) as output slices
+ * (vLLM LoRA deep-dive page, section 5.4 packed modules).
+ *
+ * Layouts (PEFT orientation, vLLM LoRA deep-dive page section 4: lora_a is
+ * (r, k), lora_b is (d, r)); all matrices row-major, bf16 unless stated:
+ *   x        [T, ldx]       input rows, first k columns used
+ *   y        [T, ldy]       output rows, first d = slice_offsets[n] columns used
+ *   A_s,i    [r_s, k]       contiguous, one per slot s and slice i
+ *   B_s,i    [d_i, r_s]     contiguous, one per slot s and slice i
+ *   ws       float32        caller-owned workspace, see lora_workspace_bytes()
+ *
+ * Conventions for every call:
+ *   - Asynchronous on the caller's stream.  The library allocates nothing,
+ *     never synchronises the device and never reads device memory back, so a
+ *     step of calls can be captured in a CUDA graph.  (lora_set_slot_table
+ *     copies from host memory; see its notes.)
+ *   - Host-side argument checks return a lora_status_t before anything is
+ *     enqueued.  Errors found in device data (a slot id outside [-1, S), a
+ *     timed-out wait) are written to the caller's device word `err` as the first
+ *     error code (compare-and-swap from 0); the library never clears it.  Zero
+ *     it before a step and read it after synchronising.
+ *   - Device pointers to bf16 data and leading dimensions must be 16-byte
+ *     aligned / multiples of 8 elements; k and every slice width must be
+ *     multiples of 8.  Ranks are 0 or multiples of 8 up to LORA_MAX_RANK
+ *     (TensorRT-LLM pads ranks below 8 for the same alignment reason: TensorRT-LLM
+ *     LoRA serving page, "path 1: CUDA Graph mode", min_kn).  A rank-0 slot is an
+ *     empty slot; its pointers may be null and it contributes nothing
+ *     (TensorRT-LLM's base sentinel slot has rank 0: same page, "adapter pool").
+ *   - Nothing is thread-safe beyond what the stream order gives: calls that run
+ *     concurrently on different streams must not share ws, err or y.
+ */
+#ifndef LORA_GEMM_H
+#define LORA_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; a null stream is the legacy default stream. */
+typedef struct CUstream_st *lora_stream_t;
+
+#define LORA_ABI_VERSION 1
+#define LORA_MAX_SLICES 4
+#define LORA_MAX_RANK 256
+#define LORA_MAX_SLOTS 1024
+
+typedef enum {
+    LORA_OK = 0,
+    LORA_ERR_INVALID_ARG = 1,   /* null pointer with nonzero size, negative size, bad shape */
+    LORA_ERR_ALIGNMENT = 2,     /* pointer / leading dimension / width not 16-byte aligned */
+    LORA_ERR_RANK = 3,          /* rank not 0 or a multiple of 8, or above r_max / LORA_MAX_RANK */
+    LORA_ERR_SLOT_RANGE = 4,    /* device: a slot id outside [-1, S) (token left unchanged) */
+    LORA_ERR_NULL_WEIGHT = 5,   /* a slot with rank > 0 has a null A or B pointer */
+    LORA_ERR_WORKSPACE = 6,     /* workspace missing or smaller than lora_workspace_bytes() */
+    LORA_ERR_TIMEOUT = 7,       /* device: a bounded wait between thread blocks gave up */
+    LORA_ERR_CUDA = 8,          /* a CUDA runtime call failed (e.g. launch) */
+    LORA_ERR_UNSUPPORTED = 9    /* no kernel for this device or configuration */
+} lora_status_t;
+
+/* Kernel path of lora_apply_ex. */
+typedef enum {
+    LORA_PATH_AUTO = 0,          /* decode kernels if max_seg_hint <= LORA_DECODE_MAX_SEG, else prefill */
+    LORA_PATH_DECODE_FUSED = 1,  /* one launch: shrink, per-segment wait, expand */
+    LORA_PATH_DECODE_SPLIT = 2,  /* two launches: shrink then expand (programmatic dependent launch) */
+    LORA_PATH_PREFILL = 3        /* tcgen05/TMEM tensor-core shrink and expand */
+} lora_path_t;
+
+#define LORA_DECODE_MAX_SEG 256
+
+/*
+ * Shape of one packed projection, passed by the host to every branch call.
+ *   S              number of resident slots in the slot table (1..LORA_MAX_SLOTS)
+ *   r_max          upper bound on every slot's rank (multiple of 8, <= LORA_MAX_RANK);
+ *                  it sets the workspace row stride
+ *   k              input width (multiple of 8)
+ *   n_slices       number of output slices (1..LORA_MAX_SLICES)
+ *   slice_offsets  slice i owns y columns [slice_offsets[i], slice_offsets[i+1]);
+ *                  slice_offsets[0] = 0, strictly increasing, widths multiples of 8
+ */
+typedef struct {
+    int32_t S;
+    int32_t r_max;
+    int32_t k;
+    int32_t n_slices;
+    int32_t slice_offsets[LORA_MAX_SLICES + 1];
+} lora_shape_t;
+
+/* Library ABI version (LORA_ABI_VERSION of the build). */
+int32_t lora_abi_version(void);
+
+/* Human-readable name of a status code; never null. */
+const char *lora_status_string(lora_status_t status);
+
+/*
+ * Per-slot scale rule (host).  llama.cpp's get_scale (llama.cpp LoRA adapter
+ * page, section "where the scale is applied"): adapter_scale * alpha / rank, or
+ * adapter_scale alone when alpha == 0 (a file without alpha).  With rslora != 0
+ * the rank enters as sqrt(rank) (vLLM LoRA deep-dive page, section 1, rsLoRA).
+ * Returns adapter_scale for rank <= 0.
+ */
+double lora_scale(double alpha, int32_t rank, int32_t rslora, double adapter_scale);
+
+/*
+ * Fold a scale into B on load, in place on the device: w[e] = bf16(scale * w[e])
+ * with the product in fp32 and round-to-nearest-even (vLLM LoRA deep-dive page,
+ * section 1, LoRALayerWeights.optimize(): lora_b *= scaling, scaling = 1).  The
+ * slot is then used with scale 1.  w: device bf16, n elements, 2-byte aligned.
+ */
+lora_status_t lora_premultiply(void *w, int64_t n, float scale, lora_stream_t stream);
+
+/*
+ * Slot table: per slot s its rank r_s, runtime scale s_s and, per slice i, the
+ * device addresses of A_s,i and B_s,i as 64-bit integers (TensorRT-LLM LoRA
+ * serving page, "a decode batch's route", step 3: one row per slot, int64
+ * pointers, refreshed only when slot ownership changes).  The packed table lives
+ * in caller-owned device memory of lora_slot_table_bytes(S, n_slices) bytes
+ * (16-byte aligned).  Ranks of one slot are shared by all its slices.
+ */
+size_t lora_slot_table_bytes(int32_t S, int32_t n_slices);
+
+/*
+ * Validate the host arrays and pack them into host_buf (lora_slot_table_bytes
+ * bytes).  ranks[S], scales[S], A_ptrs[S * n_slices] and B_ptrs[S * n_slices]
+ * are host arrays; entry s * n_slices + i is slot s, slice i.  Checks: 1 <= S <=
+ * LORA_MAX_SLOTS, 1 <= n_slices <= LORA_MAX_SLICES, r_max a multiple of 8 in
+ * [8, LORA_MAX_RANK], every rank 0 or a multiple of 8 <= r_max (LORA_ERR_RANK),
+ * every pointer of a rank>0 slot non-null (LORA_ERR_NULL_WEIGHT) and 16-byte
+ * aligned (LORA_ERR_ALIGNMENT).  Pure host code; usable without a GPU.
+ */
+lora_status_t lora_pack_slot_table(void *host_buf, int32_t S, int32_t n_slices, int32_t r_max,
+                                   const int32_t *ranks, const float *scales,
+                                   const uint64_t *A_ptrs, const uint64_t *B_ptrs);
+
+/*
+ * lora_pack_slot_table into host_staging, then an asynchronous host-to-device
+ * copy of the packed bytes into dev_table on `stream`.  host_staging must stay
+ * unchanged until the copy has executed (pinned memory recommended; with
+ * pageable memory the CUDA runtime stages the bytes before returning).  Call it
+ * only when the slot-to-adapter assignment changes.
+ */
+lora_status_t lora_set_slot_table(void *dev_table, void *host_staging, int32_t S, int32_t n_slices,
+                                  int32_t r_max, const int32_t *ranks, const float *scales,
+                                  const uint64_t *A_ptrs, const uint64_t *B_ptrs,
+                                  lora_stream_t stream);
+
+/*
+ * Per-step token index (TensorRT-LLM LoRA serving page, "a decode batch's
+ * route", steps 2 and 4: sorted ids, bincount, cumsum with a final total; vLLM
+ * book ch. 16, section 16.4.3, the LoRAKernelMeta tensors).  Device arrays:
+ *   slot_ids    int32 [T]      input; -1 = no adapter
+ *   sorted_ids  int32 [T]      tokens ordered by key = slot (no-adapter and
+ *                              out-of-range ids keyed S, i.e. last), ties in
+ *                              ascending token index (a stable sort)
+ *   seg_offsets int32 [S + 2]  seg_offsets[b] = number of tokens with key < b;
+ *                              slot s owns sorted positions [seg_offsets[s],
+ *                              seg_offsets[s+1]); seg_offsets[S+1] = T
+ *   active      int32 [S + 1]  active[0] = number of slots with at least one
+ *                              token and rank > 0; active[1..] those slots, ascending
+ *   err         int32 [1]      first error; LORA_ERR_SLOT_RANGE for ids outside [-1, S)
+ * Ranks come from dev_table (any module's table: ranks are per slot).  Built once
+ * per step and shared by every projection of the step.  T may be 0.
+ */
+lora_status_t lora_build_index(const int32_t *slot_ids, int32_t T, int32_t S, const void *dev_table,
+                               int32_t *sorted_ids, int32_t *seg_offsets, int32_t *active,
+                               int32_t *err, lora_stream_t stream);
+
+/*
+ * Workspace size for T tokens of a projection: an fp32 buffer xa[n_slices][T][r_max]
+ * (the shrink output, row t = token t) after a control block of per-slot
+ * counters.  The control block must be zero before the first call that uses the
+ * workspace (e.g. cudaMemsetAsync of the whole buffer once); every call leaves
+ * it zero again when it returns without LORA_ERR_TIMEOUT.
+ */
+lora_status_t lora_workspace_bytes(int32_t T, const lora_shape_t *shape, size_t *bytes);
+
+/*
+ * Shrink: xa[i][t][j] = sum_c x[t, c] * A_s,i[j, c] for tokens t of active slots s,
+ * j < r_s, accumulated in fp32 (vLLM book ch. 16, section 16.4.2: lora_shrink
+ * writes buffer[num_tokens, r] from lora_a).  Other rows of xa are not written.
+ */
+lora_status_t lora_shrink(const void *x, int64_t ldx, int32_t T, const lora_shape_t *shape,
+                          const void *dev_table, const int32_t *sorted_ids,
+                          const int32_t *seg_offsets, const int32_t *active,
+                          float *ws, size_t ws_bytes, int32_t *err, lora_stream_t stream);
+
+/*
+ * Expand: y[t, o_i + m] = bf16( y[t, o_i + m] + scale_s * sum_j xa[i][t][j] * B_s,i[m, j] ),
+ * the sum in fp32, one round-to-nearest-even per element (vLLM book ch. 16,
+ * section 16.4.2: lora_expand accumulates into the output slices; TensorRT-LLM
+ * LoRA serving page, add_lora_result: output.add_(lora_result)).  Rows of tokens
+ * without an active slot are neither read nor written.
+ */
+lora_status_t lora_expand(const float *ws, size_t ws_bytes, void *y, int64_t ldy, int32_t T,
+                          const lora_shape_t *shape, const void *dev_table,
+                          const int32_t *sorted_ids, const int32_t *seg_offsets,
+                          const int32_t *active, int32_t *err, lora_stream_t stream);
+
+/*
+ * Shrink followed by expand on the same workspace: the whole branch for one
+ * projection.  max_seg_hint is a host-known upper bound on the tokens of any one
+ * slot in this step (T is always valid); LORA_PATH_AUTO picks the decode kernels
+ * when it is <= LORA_DECODE_MAX_SEG and the tensor-core prefill kernels
+ * otherwise.  When no token has an active slot the kernels exit early on the
+ * device (the no-LoRA step).
+ */
+lora_status_t lora_apply(const void *x, int64_t ldx, void *y, int64_t ldy, int32_t T,
+                         const lora_shape_t *shape, const void *dev_table,
+                         const int32_t *sorted_ids, const int32_t *seg_offsets,
+                         const int32_t *active, int32_t max_seg_hint,
+                         float *ws, size_t ws_bytes, int32_t *err, lora_stream_t stream);
+
+/*
+ * The path lora_apply takes for this max_seg_hint (and T) on this build:
+ * requested itself unless it is LORA_PATH_AUTO.  *launches receives the number
+ * of kernel launches the path makes per call (may be null).  Host only.
+ */
+lora_path_t lora_resolve_path(lora_path_t requested, int32_t T, int32_t max_seg_hint, int32_t *launches);
+
+/* lora_apply with an explicit kernel path. */
+lora_status_t lora_apply_ex(const void *x, int64_t ldx, void *y, int64_t ldy, int32_t T,
+                            const lora_shape_t *shape, const void *dev_table,
+                            const int32_t *sorted_ids, const int32_t *seg_offsets,
+                            const int32_t *active, int32_t max_seg_hint, lora_path_t path,
+                            float *ws, size_t ws_bytes, int32_t *err, lora_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_GEMM_H */

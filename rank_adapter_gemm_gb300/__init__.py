@@ -1,0 +1,223 @@
+"""Batched multi-adapter LoRA branch for GB300 (sm_103a): Python binding.
+
+Thin marshalling over the C ABI of include/lora_gemm.h: each ``lora_*``
+function below has the C function's name, takes torch tensors (device memory
+owned by the caller) and passes their addresses, leading dimensions and the
+current CUDA stream.  All arithmetic runs in the library's CUDA kernels; there
+is no CPU path.  A non-OK status raises :class:`LoraError`.
+
+The helper classes at the end (``SlotTable``, ``TokenIndex``, ``Workspace``)
+only allocate the caller-owned buffers the calls need.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import numpy as np
+
+from ._lib import (LORA_ABI_VERSION, LORA_DECODE_MAX_SEG, LORA_MAX_RANK, LORA_MAX_SLICES, LORA_MAX_SLOTS,
+                   PATHS, LoraError, check, load, lora_shape_t, status_string)
+
+__all__ = [
+    "LORA_ABI_VERSION", "LORA_MAX_RANK", "LORA_MAX_SLICES", "LORA_MAX_SLOTS", "LORA_DECODE_MAX_SEG",
+    "LoraError", "lora_shape_t", "make_shape", "lora_abi_version", "lora_status_string", "lora_scale",
+    "lora_premultiply", "lora_slot_table_bytes", "lora_pack_slot_table", "lora_set_slot_table",
+    "lora_build_index", "lora_workspace_bytes", "lora_shrink", "lora_expand", "lora_apply", "lora_resolve_path",
+    "SlotTable", "TokenIndex", "Workspace",
+]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _p(t) -> Optional[ctypes.c_void_p]:
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        return ctypes.c_void_p(t.ctypes.data)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t, name, dtype=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _rows(t, name):
+    torch = _torch()
+    _dev(t, name, torch.bfloat16)
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D bf16 tensor with unit column stride")
+    return t.stride(0)
+
+
+def make_shape(S: int, r_max: int, k: int, slice_widths: Sequence[int]) -> lora_shape_t:
+    """Shape of one packed projection (lora_shape_t)."""
+    widths = [int(w) for w in slice_widths]
+    if not 1 <= len(widths) <= LORA_MAX_SLICES:
+        raise ValueError("between 1 and LORA_MAX_SLICES output slices")
+    sh = lora_shape_t()
+    sh.S, sh.r_max, sh.k, sh.n_slices = int(S), int(r_max), int(k), len(widths)
+    off = 0
+    sh.slice_offsets[0] = 0
+    for i, w in enumerate(widths):
+        off += w
+        sh.slice_offsets[i + 1] = off
+    for i in range(len(widths) + 1, LORA_MAX_SLICES + 1):
+        sh.slice_offsets[i] = off
+    return sh
+
+
+# ---------------------------------------------------------------------------
+# C ABI, one wrapper per entry point
+# ---------------------------------------------------------------------------
+def lora_abi_version() -> int:
+    return int(load().lora_abi_version())
+
+
+def lora_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def lora_scale(alpha: float, rank: int, rslora: bool = False, adapter_scale: float = 1.0) -> float:
+    return float(load().lora_scale(float(alpha), int(rank), int(bool(rslora)), float(adapter_scale)))
+
+
+def lora_premultiply(w, scale: float, stream=None) -> None:
+    _dev(w, "w", _torch().bfloat16)
+    if not w.is_contiguous():
+        raise ValueError("w must be contiguous")
+    check(load().lora_premultiply(_p(w), w.numel(), float(scale), _stream(stream)), "lora_premultiply")
+
+
+def lora_slot_table_bytes(S: int, n_slices: int) -> int:
+    return int(load().lora_slot_table_bytes(int(S), int(n_slices)))
+
+
+def lora_pack_slot_table(host_buf, S, n_slices, r_max, ranks, scales, A_ptrs, B_ptrs) -> None:
+    ranks = np.ascontiguousarray(ranks, dtype=np.int32)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    A_ptrs = np.ascontiguousarray(A_ptrs, dtype=np.uint64)
+    B_ptrs = np.ascontiguousarray(B_ptrs, dtype=np.uint64)
+    check(load().lora_pack_slot_table(_p(host_buf), int(S), int(n_slices), int(r_max), _p(ranks), _p(scales),
+                                      _p(A_ptrs), _p(B_ptrs)), "lora_pack_slot_table")
+
+
+def lora_set_slot_table(dev_table, host_staging, S, n_slices, r_max, ranks, scales, A_ptrs, B_ptrs,
+                        stream=None) -> None:
+    ranks = np.ascontiguousarray(ranks, dtype=np.int32)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    A_ptrs = np.ascontiguousarray(A_ptrs, dtype=np.uint64)
+    B_ptrs = np.ascontiguousarray(B_ptrs, dtype=np.uint64)
+    _dev(dev_table, "dev_table")
+    check(load().lora_set_slot_table(_p(dev_table), _p(host_staging), int(S), int(n_slices), int(r_max),
+                                     _p(ranks), _p(scales), _p(A_ptrs), _p(B_ptrs), _stream(stream)),
+          "lora_set_slot_table")
+
+
+def lora_build_index(slot_ids, S, dev_table, sorted_ids, seg_offsets, active, err, stream=None) -> None:
+    torch = _torch()
+    _dev(slot_ids, "slot_ids", torch.int32)
+    T = int(slot_ids.numel())
+    check(load().lora_build_index(_p(slot_ids), T, int(S), _p(dev_table), _p(sorted_ids), _p(seg_offsets),
+                                  _p(active), _p(err), _stream(stream)), "lora_build_index")
+
+
+def lora_workspace_bytes(T: int, shape: lora_shape_t) -> int:
+    out = ctypes.c_size_t(0)
+    check(load().lora_workspace_bytes(int(T), ctypes.byref(shape), ctypes.byref(out)), "lora_workspace_bytes")
+    return int(out.value)
+
+
+def lora_shrink(x, shape, dev_table, sorted_ids, seg_offsets, active, ws, err, stream=None) -> None:
+    ldx = _rows(x, "x")
+    check(load().lora_shrink(_p(x), ldx, int(x.shape[0]), ctypes.byref(shape), _p(dev_table), _p(sorted_ids),
+                             _p(seg_offsets), _p(active), _p(ws), ws.numel() * ws.element_size(), _p(err),
+                             _stream(stream)), "lora_shrink")
+
+
+def lora_expand(ws, y, shape, dev_table, sorted_ids, seg_offsets, active, err, stream=None) -> None:
+    ldy = _rows(y, "y")
+    check(load().lora_expand(_p(ws), ws.numel() * ws.element_size(), _p(y), ldy, int(y.shape[0]),
+                             ctypes.byref(shape), _p(dev_table), _p(sorted_ids), _p(seg_offsets), _p(active),
+                             _p(err), _stream(stream)), "lora_expand")
+
+
+def lora_apply(x, y, shape, dev_table, sorted_ids, seg_offsets, active, ws, err, max_seg_hint: int = 0,
+               path: str = "auto", stream=None) -> None:
+    ldx = _rows(x, "x")
+    ldy = _rows(y, "y")
+    if x.shape[0] != y.shape[0]:
+        raise ValueError("x and y must have the same number of rows")
+    args = (_p(x), ldx, _p(y), ldy, int(x.shape[0]), ctypes.byref(shape), _p(dev_table), _p(sorted_ids),
+            _p(seg_offsets), _p(active), int(max_seg_hint))
+    tail = (_p(ws), ws.numel() * ws.element_size(), _p(err), _stream(stream))
+    if path == "auto":
+        check(load().lora_apply(*args, *tail), "lora_apply")
+    else:
+        check(load().lora_apply_ex(*args, PATHS[path], *tail), "lora_apply_ex")
+
+
+def lora_resolve_path(path: str, T: int, max_seg_hint: int = 0):
+    """(path name lora_apply takes, kernel launches per call)."""
+    launches = ctypes.c_int32(0)
+    code = load().lora_resolve_path(PATHS[path], int(T), int(max_seg_hint), ctypes.byref(launches))
+    name = {v: k for k, v in PATHS.items()}[int(code)]
+    return name, int(launches.value)
+
+
+# ---------------------------------------------------------------------------
+# Caller-owned buffers (allocation only)
+# ---------------------------------------------------------------------------
+class SlotTable:
+    """Device slot table plus the pinned staging buffer its upload copies from."""
+
+    def __init__(self, S: int, n_slices: int, r_max: int, device="cuda"):
+        torch = _torch()
+        self.S, self.n_slices, self.r_max = int(S), int(n_slices), int(r_max)
+        nbytes = lora_slot_table_bytes(S, n_slices)
+        self.dev = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+        self.staging = torch.zeros(nbytes, dtype=torch.uint8).pin_memory()
+
+    def set(self, ranks, scales, A_ptrs, B_ptrs, stream=None) -> None:
+        lora_set_slot_table(self.dev, self.staging, self.S, self.n_slices, self.r_max, ranks, scales,
+                            A_ptrs, B_ptrs, stream)
+
+
+class TokenIndex:
+    """sorted_ids[T], seg_offsets[S+2], active[S+1] and the error word."""
+
+    def __init__(self, T: int, S: int, device="cuda"):
+        torch = _torch()
+        self.T, self.S = int(T), int(S)
+        self.sorted_ids = torch.zeros(max(T, 1), dtype=torch.int32, device=device)
+        self.seg_offsets = torch.zeros(S + 2, dtype=torch.int32, device=device)
+        self.active = torch.zeros(S + 1, dtype=torch.int32, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def build(self, slot_ids, table: SlotTable, stream=None) -> None:
+        lora_build_index(slot_ids, self.S, table.dev, self.sorted_ids, self.seg_offsets, self.active, self.err,
+                         stream)
+
+
+class Workspace:
+    """fp32 workspace of lora_workspace_bytes(T, shape) bytes, zeroed once."""
+
+    def __init__(self, T: int, shape: lora_shape_t, device="cuda"):
+        torch = _torch()
+        nbytes = lora_workspace_bytes(T, shape)
+        self.buf = torch.zeros((nbytes + 3) // 4, dtype=torch.float32, device=device)

@@ -1,0 +1,132 @@
+// Per-step token index: a stable counting sort of tokens by adapter slot.
+//
+// TensorRT-LLM LoRA serving page, section "一次 decode 批次的路由" (steps 2 and 4:
+// sorted ids, bincount over slots, cumsum with one extra entry holding the
+// total) and vLLM book ch. 16, section 16.4.3 (LoRAKernelMeta: tokens sorted by
+// slot, tokens per slot, segment starts, active slots).  No-adapter tokens
+// (slot -1) and out-of-range ids are keyed S, i.e. placed last, like
+// TensorRT-LLM's sentinel slot after the real ones.
+//
+// One thread block does the whole sort: histogram in shared memory, an
+// exclusive scan into the segment offsets, then a pass over the tokens in
+// blockDim-sized chunks in token order.  Inside a chunk, a token's place among
+// equal keys is its rank within its warp (__match_any_sync + popc) plus the
+// counts of the same key in lower warps; the running per-key cursor carries
+// the order across chunks, so ties stay in ascending token index.
+#include "common.cuh"
+
+namespace lora {
+
+namespace {
+
+__global__ void build_index_kernel(const int32_t *__restrict__ slot_ids, int32_t T, int32_t S,
+                                   const void *table, int32_t *__restrict__ sorted_ids,
+                                   int32_t *__restrict__ seg_offsets, int32_t *__restrict__ active,
+                                   int32_t *err) {
+    extern __shared__ int32_t smem[];
+    const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nw = nt >> 5;
+    const int bins = S + 1;
+    int32_t *cursor = smem;              // [bins]   histogram, then running cursor
+    int32_t *flag = cursor + bins;       // [S]      active flags, then positions
+    int32_t *wcnt = flag + S;            // [bins * nw] per-chunk per-warp counts
+    int32_t *scratch = wcnt + bins * nw; // [33]
+
+    const TableView tab(table, S, 1);
+    const int32_t *hdr = static_cast<const int32_t *>(table);
+    const bool table_ok = hdr[0] == kTableMagic && hdr[1] == S;  // else ranks are not read at all
+    if (tid == 0 && !table_ok) report_error(err, LORA_ERR_INVALID_ARG);
+    for (int b = tid; b < bins; b += nt) cursor[b] = 0;
+    for (int e = tid; e < bins * nw; e += nt) wcnt[e] = 0;
+    __syncthreads();
+
+    // 1. histogram
+    bool bad = false;
+    for (int t = tid; t < T; t += nt) {
+        int32_t s = slot_ids[t];
+        int32_t key = (s >= 0 && s < S) ? s : S;
+        bad |= (s < -1 || s >= S);
+        atomicAdd(&cursor[key], 1);
+    }
+    if (bad) report_error(err, LORA_ERR_SLOT_RANGE);
+    __syncthreads();
+
+    // 2. active slots: tokens present and rank > 0, ascending
+    for (int s = tid; s < S; s += nt) flag[s] = (table_ok && cursor[s] > 0 && tab.rank[s] > 0) ? 1 : 0;
+    __syncthreads();
+    {
+        // the scan turns flags into positions; activity is re-derived from the counts
+        int32_t n_active = block_exclusive_scan(flag, S, scratch);
+        for (int s = tid; s < S; s += nt) {
+            const bool is_active = table_ok && cursor[s] > 0 && tab.rank[s] > 0;
+            if (is_active) active[1 + flag[s]] = s;
+        }
+        if (tid == 0) active[0] = n_active;
+    }
+
+    // 3. segment offsets
+    block_exclusive_scan(cursor, bins, scratch);
+    for (int b = tid; b < bins; b += nt) seg_offsets[b] = cursor[b];
+    if (tid == 0) seg_offsets[S + 1] = T;
+    __syncthreads();
+
+    // 4. stable scatter, chunk by chunk in token order
+    for (int base = 0; base < T; base += nt) {
+        const int t = base + tid;
+        const bool valid = t < T;
+        int32_t key = -1 - lane;  // unique per lane for invalid tokens: never matches
+        if (valid) {
+            int32_t s = slot_ids[t];
+            key = (s >= 0 && s < S) ? s : S;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        const unsigned lower = peers & ((1u << lane) - 1u);
+        const int in_warp = __popc(lower);
+        const bool leader = lower == 0;
+        if (valid && leader) wcnt[key * nw + warp] = __popc(peers);
+        __syncthreads();
+        if (valid) {
+            int32_t before = 0;
+            for (int w = 0; w < warp; ++w) before += wcnt[key * nw + w];
+            sorted_ids[cursor[key] + before + in_warp] = t;
+        }
+        __syncthreads();
+        if (valid && leader) {
+            atomicAdd(&cursor[key], __popc(peers));
+            wcnt[key * nw + warp] = 0;
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+size_t index_smem_bytes(int32_t S, int threads) {
+    const int nw = threads / 32;
+    return sizeof(int32_t) * (size_t(S + 1) + size_t(S) + size_t(S + 1) * nw + 33);
+}
+
+cudaError_t launch_build_index(const int32_t *slot_ids, int32_t T, int32_t S, const void *table,
+                               int32_t *sorted_ids, int32_t *seg_offsets, int32_t *active, int32_t *err,
+                               cudaStream_t stream) {
+    int threads = 1024;
+    if (T < 1024) threads = ((T + 31) / 32) * 32;
+    if (threads < 128) threads = 128;
+    size_t smem = index_smem_bytes(S, threads);
+    while (smem > 200 * 1024 && threads > 128) {
+        threads /= 2;
+        smem = index_smem_bytes(S, threads);
+    }
+    static bool attr_set = false;  // once, outside any stream capture (the first call)
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(build_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             200 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    build_index_kernel<<<1, threads, smem, stream>>>(slot_ids, T, S, table, sorted_ids, seg_offsets,
+                                                     active, err);
+    return cudaGetLastError();
+}
+
+}  // namespace lora

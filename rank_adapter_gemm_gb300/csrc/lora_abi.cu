@@ -1,0 +1,284 @@
+// extern "C" entry points of the LoRA branch library: argument checks, slot
+// table packing, workspace sizing and kernel dispatch.  Declarations and the
+// contract of every call are in include/lora_gemm.h.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace lora {
+cudaError_t launch_build_index(const int32_t *slot_ids, int32_t T, int32_t S, const void *table,
+                               int32_t *sorted_ids, int32_t *seg_offsets, int32_t *active, int32_t *err,
+                               cudaStream_t stream);
+cudaError_t launch_shrink(const uint16_t *x, int64_t ldx, const Shape &sh, const void *table,
+                          const int32_t *sorted_ids, const int32_t *seg, float *xa, int32_t T, int32_t *err,
+                          bool trigger_dependents, cudaStream_t stream);
+cudaError_t launch_expand(const float *xa, uint16_t *y, int64_t ldy, const Shape &sh, const void *table,
+                          const int32_t *sorted_ids, const int32_t *seg, int32_t T, int32_t *err,
+                          bool programmatic, cudaStream_t stream);
+cudaError_t launch_fused_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
+                                const void *table, const int32_t *sorted_ids, const int32_t *seg,
+                                float *ws, int32_t T, int32_t *err, cudaStream_t stream);
+cudaError_t launch_premultiply(uint16_t *w, int64_t n, float scale, cudaStream_t stream);
+bool prefill_available();
+bool fused_decode_available();
+cudaError_t launch_prefill(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
+                           const void *table, const int32_t *sorted_ids, const int32_t *seg, float *ws,
+                           int32_t T, int32_t *err, cudaStream_t stream);
+}  // namespace lora
+
+using lora::Shape;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+lora_status_t check_shape(const lora_shape_t *shape, Shape *out) {
+    if (shape == nullptr) return LORA_ERR_INVALID_ARG;
+    const lora_shape_t &s = *shape;
+    if (s.S < 1 || s.S > LORA_MAX_SLOTS) return LORA_ERR_INVALID_ARG;
+    if (s.n_slices < 1 || s.n_slices > LORA_MAX_SLICES) return LORA_ERR_INVALID_ARG;
+    if (s.k < 8) return LORA_ERR_INVALID_ARG;
+    if (s.k % 8 != 0) return LORA_ERR_ALIGNMENT;
+    if (s.r_max < 8 || s.r_max > LORA_MAX_RANK || s.r_max % 8 != 0) return LORA_ERR_RANK;
+    if (s.slice_offsets[0] != 0) return LORA_ERR_INVALID_ARG;
+    for (int i = 0; i < s.n_slices; ++i) {
+        const int32_t w = s.slice_offsets[i + 1] - s.slice_offsets[i];
+        if (w <= 0) return LORA_ERR_INVALID_ARG;
+        if (w % 8 != 0) return LORA_ERR_ALIGNMENT;
+    }
+    out->S = s.S;
+    out->r_max = s.r_max;
+    out->k = s.k;
+    out->n = s.n_slices;
+    for (int i = 0; i <= LORA_MAX_SLICES; ++i)
+        out->off[i] = i <= s.n_slices ? s.slice_offsets[i] : s.slice_offsets[s.n_slices];
+    return LORA_OK;
+}
+
+lora_status_t check_index_ptrs(const void *table, const int32_t *sorted_ids, const int32_t *seg,
+                               const int32_t *active, int32_t T) {
+    if (table == nullptr || seg == nullptr || active == nullptr) return LORA_ERR_INVALID_ARG;
+    if (T > 0 && sorted_ids == nullptr) return LORA_ERR_INVALID_ARG;
+    if (!aligned16(table)) return LORA_ERR_ALIGNMENT;
+    return LORA_OK;
+}
+
+lora_status_t check_rows(const void *p, int64_t ld, int32_t T, int32_t width) {
+    if (T > 0 && p == nullptr) return LORA_ERR_INVALID_ARG;
+    if (ld < width) return LORA_ERR_INVALID_ARG;
+    if (!aligned16(p) || ld % 8 != 0) return LORA_ERR_ALIGNMENT;
+    return LORA_OK;
+}
+
+lora_status_t check_ws(const float *ws, size_t ws_bytes, int32_t T, const Shape &sh) {
+    const lora::WorkspaceLayout L(T, sh.n, sh.r_max, sh.S);
+    if (ws == nullptr || ws_bytes < L.bytes) return LORA_ERR_WORKSPACE;
+    if (!aligned16(ws)) return LORA_ERR_ALIGNMENT;
+    return LORA_OK;
+}
+
+lora_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA; }
+
+float *xa_of(float *ws, int32_t T, const Shape &sh) {
+    const lora::WorkspaceLayout L(T, sh.n, sh.r_max, sh.S);
+    return reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + L.xa_off);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t lora_abi_version(void) { return LORA_ABI_VERSION; }
+
+const char *lora_status_string(lora_status_t status) {
+    switch (status) {
+    case LORA_OK: return "LORA_OK";
+    case LORA_ERR_INVALID_ARG: return "LORA_ERR_INVALID_ARG: invalid argument (null pointer, size or shape)";
+    case LORA_ERR_ALIGNMENT: return "LORA_ERR_ALIGNMENT: pointer, leading dimension or width not 16-byte aligned";
+    case LORA_ERR_RANK: return "LORA_ERR_RANK: rank not 0 or a multiple of 8, or above r_max / LORA_MAX_RANK";
+    case LORA_ERR_SLOT_RANGE: return "LORA_ERR_SLOT_RANGE: a slot id outside [-1, S)";
+    case LORA_ERR_NULL_WEIGHT: return "LORA_ERR_NULL_WEIGHT: a slot with rank > 0 has a null A or B pointer";
+    case LORA_ERR_WORKSPACE: return "LORA_ERR_WORKSPACE: workspace missing or too small";
+    case LORA_ERR_TIMEOUT: return "LORA_ERR_TIMEOUT: a bounded wait between thread blocks gave up";
+    case LORA_ERR_CUDA: return "LORA_ERR_CUDA: a CUDA runtime call failed";
+    case LORA_ERR_UNSUPPORTED: return "LORA_ERR_UNSUPPORTED: no kernel for this device or configuration";
+    }
+    return "LORA_ERR_UNKNOWN";
+}
+
+double lora_scale(double alpha, int32_t rank, int32_t rslora, double adapter_scale) {
+    if (rank <= 0 || alpha == 0.0) return adapter_scale;
+    const double denom = rslora ? std::sqrt(static_cast<double>(rank)) : static_cast<double>(rank);
+    return adapter_scale * alpha / denom;
+}
+
+lora_status_t lora_premultiply(void *w, int64_t n, float scale, lora_stream_t stream) {
+    if (n < 0 || (n > 0 && w == nullptr)) return LORA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(w) & 1u) != 0) return LORA_ERR_ALIGNMENT;
+    return from_cuda(lora::launch_premultiply(static_cast<uint16_t *>(w), n, scale,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t lora_slot_table_bytes(int32_t S, int32_t n_slices) {
+    if (S < 1 || n_slices < 1) return 0;
+    return lora::TableLayout(S, n_slices).bytes;
+}
+
+lora_status_t lora_pack_slot_table(void *host_buf, int32_t S, int32_t n_slices, int32_t r_max,
+                                   const int32_t *ranks, const float *scales, const uint64_t *A_ptrs,
+                                   const uint64_t *B_ptrs) {
+    if (host_buf == nullptr || ranks == nullptr || scales == nullptr || A_ptrs == nullptr || B_ptrs == nullptr)
+        return LORA_ERR_INVALID_ARG;
+    if (S < 1 || S > LORA_MAX_SLOTS || n_slices < 1 || n_slices > LORA_MAX_SLICES) return LORA_ERR_INVALID_ARG;
+    if (r_max < 8 || r_max > LORA_MAX_RANK || r_max % 8 != 0) return LORA_ERR_RANK;
+    for (int32_t s = 0; s < S; ++s) {
+        const int32_t r = ranks[s];
+        if (r < 0 || r % 8 != 0 || r > r_max) return LORA_ERR_RANK;
+        if (!std::isfinite(scales[s])) return LORA_ERR_INVALID_ARG;
+        if (r == 0) continue;
+        for (int32_t i = 0; i < n_slices; ++i) {
+            const uint64_t a = A_ptrs[s * n_slices + i], b = B_ptrs[s * n_slices + i];
+            if (a == 0 || b == 0) return LORA_ERR_NULL_WEIGHT;
+            if ((a & 15u) != 0 || (b & 15u) != 0) return LORA_ERR_ALIGNMENT;
+        }
+    }
+    const lora::TableLayout L(S, n_slices);
+    char *p = static_cast<char *>(host_buf);
+    std::memset(p, 0, L.bytes);
+    const int32_t hdr[4] = {lora::kTableMagic, S, n_slices, r_max};
+    std::memcpy(p, hdr, sizeof hdr);
+    std::memcpy(p + L.rank_off, ranks, sizeof(int32_t) * size_t(S));
+    std::memcpy(p + L.scale_off, scales, sizeof(float) * size_t(S));
+    uint64_t *a = reinterpret_cast<uint64_t *>(p + L.a_off);
+    uint64_t *b = reinterpret_cast<uint64_t *>(p + L.b_off);
+    for (int32_t e = 0; e < S * n_slices; ++e) {
+        const bool used = ranks[e / n_slices] > 0;  // empty slots carry null pointers
+        a[e] = used ? A_ptrs[e] : 0;
+        b[e] = used ? B_ptrs[e] : 0;
+    }
+    return LORA_OK;
+}
+
+lora_status_t lora_set_slot_table(void *dev_table, void *host_staging, int32_t S, int32_t n_slices,
+                                  int32_t r_max, const int32_t *ranks, const float *scales,
+                                  const uint64_t *A_ptrs, const uint64_t *B_ptrs, lora_stream_t stream) {
+    if (dev_table == nullptr || host_staging == nullptr) return LORA_ERR_INVALID_ARG;
+    if (!aligned16(dev_table)) return LORA_ERR_ALIGNMENT;
+    const lora_status_t st = lora_pack_slot_table(host_staging, S, n_slices, r_max, ranks, scales, A_ptrs, B_ptrs);
+    if (st != LORA_OK) return st;
+    return from_cuda(cudaMemcpyAsync(dev_table, host_staging, lora::TableLayout(S, n_slices).bytes,
+                                     cudaMemcpyHostToDevice, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_build_index(const int32_t *slot_ids, int32_t T, int32_t S, const void *dev_table,
+                               int32_t *sorted_ids, int32_t *seg_offsets, int32_t *active, int32_t *err,
+                               lora_stream_t stream) {
+    if (T < 0 || S < 1 || S > LORA_MAX_SLOTS) return LORA_ERR_INVALID_ARG;
+    if (T > 0 && (slot_ids == nullptr || sorted_ids == nullptr)) return LORA_ERR_INVALID_ARG;
+    if (dev_table == nullptr || seg_offsets == nullptr || active == nullptr) return LORA_ERR_INVALID_ARG;
+    if (!aligned16(dev_table)) return LORA_ERR_ALIGNMENT;
+    return from_cuda(lora::launch_build_index(slot_ids, T, S, dev_table, sorted_ids, seg_offsets, active, err,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_workspace_bytes(int32_t T, const lora_shape_t *shape, size_t *bytes) {
+    Shape sh;
+    if (bytes == nullptr || T < 0) return LORA_ERR_INVALID_ARG;
+    const lora_status_t st = check_shape(shape, &sh);
+    if (st != LORA_OK) return st;
+    *bytes = lora::WorkspaceLayout(T, sh.n, sh.r_max, sh.S).bytes;
+    return LORA_OK;
+}
+
+lora_status_t lora_shrink(const void *x, int64_t ldx, int32_t T, const lora_shape_t *shape, const void *dev_table,
+                          const int32_t *sorted_ids, const int32_t *seg_offsets, const int32_t *active,
+                          float *ws, size_t ws_bytes, int32_t *err, lora_stream_t stream) {
+    Shape sh;
+    lora_status_t st;
+    if (T < 0) return LORA_ERR_INVALID_ARG;
+    if ((st = check_shape(shape, &sh)) != LORA_OK) return st;
+    if ((st = check_index_ptrs(dev_table, sorted_ids, seg_offsets, active, T)) != LORA_OK) return st;
+    if ((st = check_rows(x, ldx, T, sh.k)) != LORA_OK) return st;
+    if ((st = check_ws(ws, ws_bytes, T, sh)) != LORA_OK) return st;
+    if (T == 0) return LORA_OK;
+    return from_cuda(lora::launch_shrink(static_cast<const uint16_t *>(x), ldx, sh, dev_table, sorted_ids,
+                                         seg_offsets, xa_of(ws, T, sh), T, err, false,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_expand(const float *ws, size_t ws_bytes, void *y, int64_t ldy, int32_t T,
+                          const lora_shape_t *shape, const void *dev_table, const int32_t *sorted_ids,
+                          const int32_t *seg_offsets, const int32_t *active, int32_t *err, lora_stream_t stream) {
+    Shape sh;
+    lora_status_t st;
+    if (T < 0) return LORA_ERR_INVALID_ARG;
+    if ((st = check_shape(shape, &sh)) != LORA_OK) return st;
+    if ((st = check_index_ptrs(dev_table, sorted_ids, seg_offsets, active, T)) != LORA_OK) return st;
+    if ((st = check_rows(y, ldy, T, sh.off[sh.n])) != LORA_OK) return st;
+    if ((st = check_ws(ws, ws_bytes, T, sh)) != LORA_OK) return st;
+    if (T == 0) return LORA_OK;
+    return from_cuda(lora::launch_expand(xa_of(const_cast<float *>(ws), T, sh), static_cast<uint16_t *>(y), ldy,
+                                         sh, dev_table, sorted_ids, seg_offsets, T, err, false,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+lora_path_t lora_resolve_path(lora_path_t requested, int32_t T, int32_t max_seg_hint, int32_t *launches) {
+    lora_path_t path = requested;
+    if (max_seg_hint <= 0 || max_seg_hint > T) max_seg_hint = T;
+    if (path == LORA_PATH_AUTO) {
+        if (max_seg_hint > LORA_DECODE_MAX_SEG && lora::prefill_available()) path = LORA_PATH_PREFILL;
+        else if (lora::fused_decode_available()) path = LORA_PATH_DECODE_FUSED;
+        else path = LORA_PATH_DECODE_SPLIT;
+    }
+    if (launches != nullptr) *launches = path == LORA_PATH_DECODE_FUSED ? 1 : 2;
+    return path;
+}
+
+lora_status_t lora_apply_ex(const void *x, int64_t ldx, void *y, int64_t ldy, int32_t T, const lora_shape_t *shape,
+                            const void *dev_table, const int32_t *sorted_ids, const int32_t *seg_offsets,
+                            const int32_t *active, int32_t max_seg_hint, lora_path_t path, float *ws,
+                            size_t ws_bytes, int32_t *err, lora_stream_t stream) {
+    Shape sh;
+    lora_status_t st;
+    if (T < 0) return LORA_ERR_INVALID_ARG;
+    if ((st = check_shape(shape, &sh)) != LORA_OK) return st;
+    if ((st = check_index_ptrs(dev_table, sorted_ids, seg_offsets, active, T)) != LORA_OK) return st;
+    if ((st = check_rows(x, ldx, T, sh.k)) != LORA_OK) return st;
+    if ((st = check_rows(y, ldy, T, sh.off[sh.n])) != LORA_OK) return st;
+    if ((st = check_ws(ws, ws_bytes, T, sh)) != LORA_OK) return st;
+    if (T == 0) return LORA_OK;
+    if (max_seg_hint <= 0 || max_seg_hint > T) max_seg_hint = T;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const uint16_t *xb = static_cast<const uint16_t *>(x);
+    uint16_t *yb = static_cast<uint16_t *>(y);
+    path = lora_resolve_path(path, T, max_seg_hint, nullptr);
+    switch (path) {
+    case LORA_PATH_DECODE_FUSED:
+        if (!lora::fused_decode_available()) return LORA_ERR_UNSUPPORTED;
+        return from_cuda(lora::launch_fused_decode(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws, T,
+                                                   err, s));
+    case LORA_PATH_DECODE_SPLIT: {
+        float *xa = xa_of(ws, T, sh);
+        cudaError_t e = lora::launch_shrink(xb, ldx, sh, dev_table, sorted_ids, seg_offsets, xa, T, err, true, s);
+        if (e != cudaSuccess) return LORA_ERR_CUDA;
+        return from_cuda(lora::launch_expand(xa, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, T, err, true, s));
+    }
+    case LORA_PATH_PREFILL:
+        if (!lora::prefill_available()) return LORA_ERR_UNSUPPORTED;
+        return from_cuda(lora::launch_prefill(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws, T, err, s));
+    default:
+        return LORA_ERR_INVALID_ARG;
+    }
+}
+
+lora_status_t lora_apply(const void *x, int64_t ldx, void *y, int64_t ldy, int32_t T, const lora_shape_t *shape,
+                         const void *dev_table, const int32_t *sorted_ids, const int32_t *seg_offsets,
+                         const int32_t *active, int32_t max_seg_hint, float *ws, size_t ws_bytes, int32_t *err,
+                         lora_stream_t stream) {
+    return lora_apply_ex(x, ldx, y, ldy, T, shape, dev_table, sorted_ids, seg_offsets, active, max_seg_hint,
+                         LORA_PATH_AUTO, ws, ws_bytes, err, stream);
+}
+
+}  // extern "C"

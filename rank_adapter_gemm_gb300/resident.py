@@ -1,0 +1,112 @@
+"""Put one packed projection's adapters, activations and slot table on the device.
+
+Marshalling only: numpy bf16 bit patterns become torch bf16 device tensors,
+per-slot scales come from the library's lora_scale, a pre-multiplied scale is
+folded into B by the library's lora_premultiply kernel, and the pointer table
+is uploaded with lora_set_slot_table.
+"""
+from __future__ import annotations
+
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+from . import SlotTable, lora_premultiply, lora_scale, make_shape
+
+
+def _to_dev(bits: np.ndarray, device):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16))
+    return t.to(device).view(torch.bfloat16)
+
+
+class ResidentProjection:
+    """Adapter weights of S slots for one projection plus its x and y rows.
+
+    A[s][i] is [r_s, k], B[s][i] is [d_i, r_s] (bf16 bit patterns); rank-0
+    slots have None.  ``scale_rule`` is "alpha_over_r" or "alpha_over_sqrt_r";
+    with ``premultiplied`` the rule's scale is folded into B and the table
+    carries scale 1.
+    """
+
+    def __init__(self, *, S: int, r_max: int, ranks: Sequence[int], alphas: Sequence[float], scale_rule: str,
+                 premultiplied: bool, k: int, slice_widths: Sequence[int],
+                 A: Sequence[Sequence[Optional[np.ndarray]]], B: Sequence[Sequence[Optional[np.ndarray]]],
+                 x: Optional[np.ndarray] = None, y_in: Optional[np.ndarray] = None, device="cuda"):
+        self.S, self.r_max, self.k = int(S), int(r_max), int(k)
+        self.slice_widths = [int(w) for w in slice_widths]
+        self.n = len(self.slice_widths)
+        self.d = sum(self.slice_widths)
+        self.ranks = np.asarray(ranks, dtype=np.int32)
+        rslora = scale_rule == "alpha_over_sqrt_r"
+        rule_scales = np.array([lora_scale(alphas[s], int(self.ranks[s]), rslora) for s in range(S)])
+        self.A: List[List] = []
+        self.B: List[List] = []
+        a_ptrs = np.zeros(S * self.n, dtype=np.uint64)
+        b_ptrs = np.zeros(S * self.n, dtype=np.uint64)
+        for s in range(S):
+            rowA, rowB = [], []
+            for i in range(self.n):
+                if self.ranks[s] > 0:
+                    ta = _to_dev(A[s][i], device)
+                    tb = _to_dev(B[s][i], device)
+                    if premultiplied:
+                        lora_premultiply(tb, float(rule_scales[s]))
+                    a_ptrs[s * self.n + i] = ta.data_ptr()
+                    b_ptrs[s * self.n + i] = tb.data_ptr()
+                else:
+                    ta = tb = None
+                rowA.append(ta)
+                rowB.append(tb)
+            self.A.append(rowA)
+            self.B.append(rowB)
+        self.scales = np.ones(S, dtype=np.float32) if premultiplied else rule_scales.astype(np.float32)
+        self.table = SlotTable(S, self.n, r_max, device=device)
+        self.table.set(self.ranks, self.scales, a_ptrs, b_ptrs)
+        self._ptrs = (a_ptrs, b_ptrs)
+        self.shape = make_shape(S, r_max, k, self.slice_widths)
+        self.x = _to_dev(x, device) if x is not None else None
+        self.y = _to_dev(y_in, device) if y_in is not None else None
+
+    def clone(self, device="cuda") -> "ResidentProjection":
+        """Same values in fresh device buffers (weights, rows and slot table)."""
+        import copy
+        other = copy.copy(self)
+        n = self.n
+        a_ptrs = np.zeros(self.S * n, dtype=np.uint64)
+        b_ptrs = np.zeros(self.S * n, dtype=np.uint64)
+        other.A = [[(t.clone() if t is not None else None) for t in row] for row in self.A]
+        other.B = [[(t.clone() if t is not None else None) for t in row] for row in self.B]
+        for s in range(self.S):
+            for i in range(n):
+                if other.A[s][i] is not None:
+                    a_ptrs[s * n + i] = other.A[s][i].data_ptr()
+                    b_ptrs[s * n + i] = other.B[s][i].data_ptr()
+        other.table = SlotTable(self.S, n, self.r_max, device=device)
+        other.table.set(self.ranks, self.scales, a_ptrs, b_ptrs)
+        other._ptrs = (a_ptrs, b_ptrs)
+        other.x = self.x.clone() if self.x is not None else None
+        other.y = self.y.clone() if self.y is not None else None
+        return other
+
+    def refresh_table(self, stream=None) -> None:
+        """Re-upload the slot table (what a change of slot ownership costs)."""
+        self.table.set(self.ranks, self.scales, *self._ptrs, stream=stream)
+
+    @classmethod
+    def from_workload(cls, wl, module_index: int = 0, device="cuda", with_rows: bool = True):
+        m = wl.modules[module_index]
+        return cls(S=wl.S, r_max=wl.r_max, ranks=wl.ranks, alphas=wl.alphas, scale_rule=wl.scale_rule,
+                   premultiplied=wl.premultiplied, k=m.k, slice_widths=m.slice_widths, A=m.A, B=m.B,
+                   x=m.x if with_rows else None, y_in=m.y_in if with_rows else None, device=device)
+
+
+def to_device_bf16(bits: np.ndarray, device="cuda"):
+    """uint16 bf16 bit patterns -> torch bf16 tensor on the device."""
+    return _to_dev(bits, device)
+
+
+def to_host_bits(t) -> np.ndarray:
+    """torch bf16 tensor -> numpy uint16 bit patterns."""
+    import torch
+    return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)

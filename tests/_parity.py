@@ -1,0 +1,71 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path and the oracle on
+the same seeded inputs and compare them element by element."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import workloads as W
+
+# spec tolerance for bf16 y with fp32 accumulation: |gpu - ref| <= ATOL + RTOL |ref|,
+# ref = the fp64 oracle value before rounding to bf16
+ATOL = 1e-2
+RTOL = 2e-2
+
+
+def oracle_y(wl, mod_idx=0, rows=None, y_in="module"):
+    """fp64 reference rows of projection mod_idx (pre-multiplied B handled as the pages say)."""
+    m = wl.modules[mod_idx]
+    rule = oracle.slot_scales(wl.ranks, wl.alphas, wl.scale_rule, False)
+    if wl.premultiplied:
+        scales = np.ones(wl.S)
+        B = [[(oracle.premultiply(b, rule[s]) if b is not None else None) for b in row]
+             for s, row in enumerate(m.B)]
+    else:
+        scales = rule
+        B = m.B
+    yi = m.y_in if isinstance(y_in, str) else y_in
+    y, macs, st = oracle.apply(m.x, yi, m.slice_widths, wl.slot_ids, wl.ranks, scales, m.A, B, rows=rows)
+    return y, st
+
+
+def gpu_apply(wl, mod_idx=0, path="auto", max_seg_hint=0, repeat=1):
+    import torch
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import ResidentProjection, to_host_bits
+    rp = ResidentProjection.from_workload(wl, mod_idx)
+    slot_dev = torch.from_numpy(np.ascontiguousarray(wl.slot_ids, dtype=np.int32)).cuda()
+    idx = L.TokenIndex(wl.T, wl.S)
+    idx.build(slot_dev, rp.table)
+    ws = L.Workspace(wl.T, rp.shape)
+    y0 = rp.y.clone()
+    outs = []
+    for _ in range(repeat):
+        rp.y.copy_(y0)
+        L.lora_apply(rp.x, rp.y, rp.shape, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active, ws.buf,
+                     idx.err, max_seg_hint=max_seg_hint, path=path)
+        torch.cuda.synchronize()
+        outs.append(to_host_bits(rp.y))
+    err = int(idx.err.cpu().item())
+    return outs if repeat > 1 else outs[0], err, idx, rp, ws
+
+
+def untouched_rows(wl):
+    s = wl.slot_ids
+    bad = (s < 0) | (s >= wl.S)
+    rank0 = np.zeros_like(bad)
+    ok = ~bad
+    rank0[ok] = wl.ranks[s[ok]] == 0
+    return bad | rank0
+
+
+def assert_y_close(y_gpu_bits, y_ref, what=""):
+    g = W.bf16_bits_to_f32(y_gpu_bits).astype(np.float64)
+    diff = np.abs(g - y_ref)
+    tol = ATOL + RTOL * np.abs(y_ref)
+    bad = diff > tol
+    if bad.any():
+        idx = np.unravel_index(np.argmax(diff - tol), diff.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements outside tolerance; worst at {idx}: "
+                             f"gpu {g[idx]!r} ref {y_ref[idx]!r}")
+    return float(diff.max()) if diff.size else 0.0

@@ -1,0 +1,95 @@
+"""The C-ABI library loads, exports every symbol include/lora_gemm.h declares,
+and its host-only entry points behave as documented (no GPU needed)."""
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lora_gemm.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from rank_adapter_gemm_gb300 import build
+    build.build()
+    import rank_adapter_gemm_gb300 as lib
+    return lib
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lora_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declarations_are_exported(L):
+    from rank_adapter_gemm_gb300 import _lib
+    declared = _declared()
+    assert set(declared) == set(_lib.EXPORTED)
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.library_path()], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (lora_[a-z_]+)$", out, flags=re.M))
+    for name in declared:
+        assert name in exported, name
+    lib = _lib.load()
+    for name in declared:
+        assert hasattr(lib, name)
+
+
+def test_abi_version_and_status_strings(L):
+    assert L.lora_abi_version() == L.LORA_ABI_VERSION
+    from rank_adapter_gemm_gb300 import _lib
+    for code, name in _lib.STATUS.items():
+        assert L.lora_status_string(code).startswith(name)
+    assert L.lora_status_string(999) == "LORA_ERR_UNKNOWN"
+
+
+def test_scale_rule_matches_oracle(L):
+    for alpha, r, rs, a_s in [(16, 64, False, 1.0), (32, 16, True, 1.0), (0, 16, False, 0.5), (32, 16, False, 0.7),
+                              (8, 8, True, 2.0), (16, 0, False, 1.0)]:
+        assert L.lora_scale(alpha, r, rs, a_s) == oracle.scale(alpha, r, rs, a_s)
+
+
+def test_pack_slot_table_layout_and_checks(L):
+    S, n, r_max = 3, 2, 32
+    buf = np.zeros(L.lora_slot_table_bytes(S, n), np.uint8)
+    ranks = np.array([16, 0, 32], np.int32)
+    scales = np.array([2.0, 1.0, 0.5], np.float32)
+    A = np.array([0x1000, 0x1010, 0, 0, 0x2000, 0x2010], np.uint64)
+    B = np.array([0x3000, 0x3010, 0, 0, 0x4000, 0x4010], np.uint64)
+    L.lora_pack_slot_table(buf, S, n, r_max, ranks, scales, A, B)
+    w = buf.view(np.int32)
+    assert list(w[:4]) == [0x41526F4C, S, n, r_max]
+    assert list(w[4:7]) == [16, 0, 32]
+    assert list(buf[32:44].view(np.float32)) == [2.0, 1.0, 0.5]
+    ptrs = buf[48:].view(np.uint64)
+    assert list(ptrs[:6]) == list(A) and list(ptrs[6:12]) == list(B)
+    bad = [
+        (dict(ranks=np.array([12, 0, 32], np.int32)), 3),          # not a multiple of 8
+        (dict(ranks=np.array([16, 0, 40], np.int32)), 3),          # above r_max
+        (dict(A=np.array([0, 0x1010, 0, 0, 0x2000, 0x2010], np.uint64)), 5),   # null on a used slot
+        (dict(B=np.array([0x3008, 0x3010, 0, 0, 0x4000, 0x4010], np.uint64)), 2),  # misaligned
+    ]
+    for kw, status in bad:
+        args = dict(ranks=ranks, scales=scales, A=A, B=B)
+        args.update(kw)
+        with pytest.raises(L.LoraError) as e:
+            L.lora_pack_slot_table(buf, S, n, r_max, args["ranks"], args["scales"], args["A"], args["B"])
+        assert e.value.status == status
+
+
+def test_workspace_bytes(L):
+    sh = L.make_shape(32, 64, 4096, [4096, 1024, 1024])
+    nbytes = L.lora_workspace_bytes(256, sh)
+    assert nbytes >= 3 * 256 * 64 * 4
+    assert nbytes - 3 * 256 * 64 * 4 < 4 * (2 * 32 * 4 + 64) + 256
+    with pytest.raises(L.LoraError) as e:
+        L.lora_workspace_bytes(10, L.make_shape(0, 64, 4096, [4096]))
+    assert e.value.status == 1
+    with pytest.raises(L.LoraError) as e:
+        L.lora_workspace_bytes(10, L.make_shape(4, 64, 4095, [4096]))
+    assert e.value.status == 2

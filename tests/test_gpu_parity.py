@@ -1,0 +1,332 @@
+"""GPU parity: the CUDA library against the CPU oracle on the same seeded inputs.
+
+Index outputs must match bit for bit; y must lie within the north-star
+tolerance |gpu - ref| <= 1e-2 + 2e-2 |ref| of the fp64 oracle; rows of tokens
+without an active slot must keep their exact input bits.  Every call goes
+through the C ABI (via the ctypes binding).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from _parity import assert_y_close, gpu_apply, oracle_y, untouched_rows
+
+pytestmark = pytest.mark.gpu
+
+DECODE_PATHS = ["decode_split"]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _small(seed, T, k, widths, S, ranks, frac_none=0.1, slot_dist="uniform", y_init="normal",
+           scale_rule="alpha_over_r", premultiplied=False):
+    wl = W.generate(name="case", seed=seed, T=T, S=S, rank=8, modules=[{"name": "m", "k": k, "slices": widths}],
+                    slot_dist=slot_dist, frac_none=frac_none, alpha=16.0, y_init=y_init,
+                    scale_rule=scale_rule, premultiplied=premultiplied)
+    # per-slot ranks drawn with the same generator rules
+    rng = np.random.Generator(np.random.PCG64(seed + 7))
+    wl.ranks = np.asarray(ranks, dtype=np.int32)
+    wl.r_max = max(8, int(max(ranks)))
+    m = wl.modules[0]
+    m.A = [[(W._normal_bf16(rng, (r, k), k ** -0.5) if r > 0 else None) for _ in widths] for r in wl.ranks]
+    m.B = [[(W._normal_bf16(rng, (w, r), 0.02) if r > 0 else None) for w in widths] for r in wl.ranks]
+    wl.alphas = np.full(S, 16.0)
+    return wl
+
+
+# ---------------------------------------------------------------------------
+# Index
+# ---------------------------------------------------------------------------
+def _gpu_index(slot_ids, S, ranks):
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    T = len(slot_ids)
+    tab = L.SlotTable(S, 1, 256)
+    dummy = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
+    ptrs = np.full(S, dummy.data_ptr(), dtype=np.uint64)
+    tab.set(np.asarray(ranks, np.int32), np.ones(S, np.float32), ptrs, ptrs)
+    idx = L.TokenIndex(T, S)
+    sid = torch.from_numpy(np.ascontiguousarray(slot_ids, dtype=np.int32)).cuda()
+    idx.build(sid, tab)
+    torch.cuda.synchronize()
+    return (idx.sorted_ids.cpu().numpy()[:T], idx.seg_offsets.cpu().numpy(), idx.active.cpu().numpy(),
+            int(idx.err.cpu().item()))
+
+
+def _check_index(slot_ids, S, ranks):
+    so, seg, act, err = _gpu_index(slot_ids, S, ranks)
+    so_r, seg_r, act_r, st_r = oracle.build_index(slot_ids, S, ranks)
+    np.testing.assert_array_equal(so, so_r)
+    np.testing.assert_array_equal(seg, seg_r)
+    np.testing.assert_array_equal(act[:1 + act_r[0]], act_r[:1 + act_r[0]])
+    assert (err == 4) == (st_r == oracle.ERR_SLOT_RANGE)
+    assert err in (0, 4)
+
+
+@pytest.mark.parametrize("cfg", range(5))
+def test_index_bit_exact_on_configs(cfg):
+    wl = W.config(cfg, y_init="zeros") if cfg != 3 else None
+    if cfg == 3:  # the prefill config's slot ids only (avoid drawing 1 GB of y here)
+        rng_wl = W.generate(name="ids", seed=1003, T=None, S=16, rank=16,
+                            modules=[{"name": "m", "k": 8, "slices": [8]}],
+                            requests={"n": 16, "min_len": 128, "max_len": 2048, "n_adapters": 16},
+                            alpha=32.0)
+        slot_ids, S, ranks = rng_wl.slot_ids, 16, rng_wl.ranks
+    else:
+        slot_ids, S, ranks = wl.slot_ids, wl.S, wl.ranks
+    _check_index(slot_ids, S, ranks)
+
+
+@pytest.mark.parametrize("T,S,seed", [(0, 1, 0), (1, 1, 1), (7, 3, 2), (33, 5, 3), (1024, 128, 4),
+                                      (1025, 1, 5), (5000, 1024, 6), (40000, 17, 7), (100000, 300, 8)])
+def test_index_fuzz(T, S, seed):
+    rng = np.random.default_rng(seed)
+    slot_ids = rng.integers(-1, S, size=T).astype(np.int32)
+    ranks = rng.choice([0, 8, 16, 64], size=S).astype(np.int32)
+    _check_index(slot_ids, S, ranks)
+
+
+def test_index_all_none_and_out_of_range():
+    S = 4
+    ranks = np.array([8, 8, 0, 16], np.int32)
+    _check_index(np.full(50, -1, np.int32), S, ranks)
+    ids = np.array([0, 5, -1, 3, -2, 2, 4, 1, 1, 0], np.int32)
+    _check_index(ids, S, ranks)
+
+
+def test_index_deterministic_over_runs():
+    rng = np.random.default_rng(11)
+    ids = rng.integers(-1, 64, size=3000).astype(np.int32)
+    ranks = np.full(64, 16, np.int32)
+    first = _gpu_index(ids, 64, ranks)
+    for _ in range(20):
+        again = _gpu_index(ids, 64, ranks)
+        for a, b in zip(first[:3], again[:3]):
+            np.testing.assert_array_equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# Branch on the named configs
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("path", DECODE_PATHS)
+@pytest.mark.parametrize("cfg", [0, 1, 2])
+@pytest.mark.parametrize("y_init", ["zeros", "normal"])
+def test_apply_configs_full(cfg, y_init, path):
+    wl = W.config(cfg, y_init=y_init)
+    y, err, *_ = gpu_apply(wl, path=path)
+    assert err == 0
+    ref, st = oracle_y(wl)
+    assert st == 0
+    assert_y_close(y, ref, f"config {cfg}")
+    keep = untouched_rows(wl)
+    np.testing.assert_array_equal(y[keep], wl.modules[0].y_in[keep])
+
+
+@pytest.mark.parametrize("path", DECODE_PATHS)
+def test_apply_large_decode_sampled(path):
+    """T=1024, k=d=8192, r=64, S=128: all rows checked (the oracle takes seconds)."""
+    wl = W.config(4)
+    y, err, *_ = gpu_apply(wl, path=path)
+    assert err == 0
+    rows = np.arange(wl.T, dtype=np.int32)
+    ref, _ = oracle_y(wl, rows=rows)
+    assert_y_close(y[rows], ref, "large decode")
+
+
+@pytest.mark.parametrize("mod_idx", [0, 1, 2, 3])
+def test_apply_layer_sweep_sampled(mod_idx):
+    """The four packed projections of one Llama-3-8B layer at T=1024, r=64."""
+    wl = W.config(4, sweep=True)
+    y, err, *_ = gpu_apply(wl, mod_idx=mod_idx)
+    assert err == 0
+    rng = np.random.default_rng(mod_idx)
+    rows = np.sort(rng.choice(wl.T, size=96, replace=False)).astype(np.int32)
+    ref, _ = oracle_y(wl, mod_idx=mod_idx, rows=rows)
+    assert_y_close(y[rows], ref, wl.modules[mod_idx].name)
+    keep = untouched_rows(wl)
+    np.testing.assert_array_equal(y[keep], wl.modules[mod_idx].y_in[keep])
+
+
+@pytest.mark.parametrize("mod_idx", [0, 1])
+def test_apply_prefill_sampled(mod_idx):
+    """Prefill MLP (about 17k tokens): sampled rows from every request, plus the
+    first and last token of the batch."""
+    wl = W.config(3)
+    y, err, *_ = gpu_apply(wl, mod_idx=mod_idx)
+    assert err == 0
+    rng = np.random.default_rng(100 + mod_idx)
+    rows = np.unique(np.concatenate([[0, wl.T - 1], rng.choice(wl.T, size=62, replace=False)])).astype(np.int32)
+    ref, _ = oracle_y(wl, mod_idx=mod_idx, rows=rows)
+    assert_y_close(y[rows], ref, wl.modules[mod_idx].name)
+
+
+# ---------------------------------------------------------------------------
+# Ragged shapes and edge cases
+# ---------------------------------------------------------------------------
+RAGGED = [
+    # seed, T, k, widths, S, ranks
+    (1, 33, 40, [8, 24], 5, [8, 24, 0, 72, 8]),
+    (2, 1, 8, [8], 1, [8]),
+    (3, 70, 264, [136, 8, 520], 3, [16, 256, 40]),
+    (4, 300, 1000, [1000], 2, [64, 8]),
+    (5, 129, 520, [512, 16, 8, 24], 7, [8, 16, 24, 32, 40, 48, 56]),
+    (6, 257, 4096, [1024], 1, [128]),
+]
+
+
+@pytest.mark.parametrize("path", DECODE_PATHS)
+@pytest.mark.parametrize("case", RAGGED, ids=[f"ragged{c[0]}" for c in RAGGED])
+def test_apply_ragged(case, path):
+    seed, T, k, widths, S, ranks = case
+    wl = _small(seed, T, k, widths, S, ranks)
+    y, err, *_ = gpu_apply(wl, path=path)
+    assert err == 0
+    ref, _ = oracle_y(wl)
+    assert_y_close(y, ref, f"ragged {seed}")
+    keep = untouched_rows(wl)
+    np.testing.assert_array_equal(y[keep], wl.modules[0].y_in[keep])
+
+
+def test_apply_all_tokens_without_adapter():
+    wl = _small(9, 64, 256, [256], 4, [16, 16, 16, 16], frac_none=1.0)
+    y, err, *_ = gpu_apply(wl)
+    assert err == 0
+    np.testing.assert_array_equal(y, wl.modules[0].y_in)
+
+
+def test_apply_zero_B_leaves_y_unchanged():
+    wl = _small(10, 48, 512, [256, 128], 3, [16, 32, 8], frac_none=0.0)
+    m = wl.modules[0]
+    m.B = [[(np.zeros_like(b) if b is not None else None) for b in row] for row in m.B]
+    y, err, *_ = gpu_apply(wl)
+    assert err == 0
+    np.testing.assert_array_equal(W.bf16_bits_to_f32(y), W.bf16_bits_to_f32(m.y_in))
+
+
+def test_apply_out_of_range_slots_flag_error_and_skip_rows():
+    wl = _small(12, 40, 256, [128], 3, [8, 16, 8], frac_none=0.0)
+    wl.slot_ids[[0, 5, 9]] = [3, 100, -4]
+    y, err, *_ = gpu_apply(wl)
+    assert err == 4  # LORA_ERR_SLOT_RANGE
+    ref, _ = oracle_y(wl)
+    assert_y_close(y, ref, "out of range")
+    np.testing.assert_array_equal(y[[0, 5, 9]], wl.modules[0].y_in[[0, 5, 9]])
+
+
+def test_apply_rslora_and_premultiplied_configs():
+    for rule, pre in [("alpha_over_sqrt_r", False), ("alpha_over_r", True), ("alpha_over_sqrt_r", True)]:
+        wl = _small(13, 64, 512, [256, 256], 4, [16, 64, 8, 32], scale_rule=rule, premultiplied=pre)
+        y, err, *_ = gpu_apply(wl)
+        assert err == 0
+        ref, _ = oracle_y(wl)
+        assert_y_close(y, ref, f"{rule} premultiplied={pre}")
+
+
+def test_apply_is_deterministic():
+    wl = W.config(2)
+    ys, err, *_ = gpu_apply(wl, repeat=5)
+    for y in ys[1:]:
+        np.testing.assert_array_equal(y, ys[0])
+
+
+# ---------------------------------------------------------------------------
+# Shrink and expand entry points on their own
+# ---------------------------------------------------------------------------
+def test_shrink_then_expand_entry_points():
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import ResidentProjection, to_host_bits
+    wl = W.config(2)
+    rp = ResidentProjection.from_workload(wl)
+    idx = L.TokenIndex(wl.T, wl.S)
+    idx.build(torch.from_numpy(wl.slot_ids).cuda(), rp.table)
+    ws = L.Workspace(wl.T, rp.shape)
+    L.lora_shrink(rp.x, rp.shape, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active, ws.buf, idx.err)
+    torch.cuda.synchronize()
+    # xa follows the control block; compare it with the oracle's shrink
+    nbytes_ctrl = ws.buf.numel() * 4 - 4 * wl.modules[0].n_slices * wl.T * wl.r_max
+    xa = ws.buf[nbytes_ctrl // 4:].view(wl.modules[0].n_slices, wl.T, wl.r_max).cpu().numpy().astype(np.float64)
+    ref, _ = oracle.shrink(wl.modules[0].x, wl.slot_ids, wl.ranks, wl.modules[0].A, wl.r_max)
+    for t in range(wl.T):
+        r = wl.ranks[wl.slot_ids[t]]
+        got = xa[:, t, :r]
+        want = ref[t, :, :r]
+        np.testing.assert_allclose(got, want, rtol=1e-4, atol=1e-4)
+    L.lora_expand(ws.buf, rp.y, rp.shape, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active, idx.err)
+    torch.cuda.synchronize()
+    assert int(idx.err.cpu().item()) == 0
+    y_ref, _ = oracle_y(wl)
+    assert_y_close(to_host_bits(rp.y), y_ref, "shrink+expand")
+
+
+def test_premultiply_kernel_matches_oracle():
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import to_device_bf16, to_host_bits
+    rng = np.random.default_rng(3)
+    b = W.f32_to_bf16_bits(rng.standard_normal(100000, dtype=np.float32))
+    for s in (2.0, 0.25, 8.0):
+        t = to_device_bf16(b)
+        L.lora_premultiply(t, s)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(to_host_bits(t), oracle.premultiply(b, s))
+    t = to_device_bf16(b)
+    L.lora_premultiply(t, 0.3)
+    torch.cuda.synchronize()
+    got = W.bf16_bits_to_f32(to_host_bits(t)).astype(np.float64)
+    want = W.bf16_bits_to_f32(oracle.premultiply(b, 0.3)).astype(np.float64)
+    # fp32 product then one rounding vs the exact product rounded: at most one bf16 step apart
+    np.testing.assert_allclose(got, want, rtol=2 ** -7, atol=0)
+
+
+# ---------------------------------------------------------------------------
+# Host-side argument checks (no kernel runs)
+# ---------------------------------------------------------------------------
+def test_host_validation_errors():
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    wl = _small(14, 16, 64, [64], 2, [8, 8])
+    from rank_adapter_gemm_gb300.resident import ResidentProjection
+    rp = ResidentProjection.from_workload(wl)
+    idx = L.TokenIndex(wl.T, wl.S)
+    idx.build(torch.from_numpy(wl.slot_ids).cuda(), rp.table)
+    ws = L.Workspace(wl.T, rp.shape)
+    args = (rp.shape, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active)
+    with pytest.raises(L.LoraError) as e:
+        L.lora_apply(rp.x, rp.y, *args, ws.buf[:4], idx.err)
+    assert e.value.status == 6
+    bad_x = torch.zeros(wl.T, 72, dtype=torch.bfloat16, device="cuda")[:, 1:65]
+    with pytest.raises(L.LoraError) as e:
+        L.lora_apply(bad_x, rp.y, *args, ws.buf, idx.err)
+    assert e.value.status == 2
+    bad_shape = L.make_shape(2, 8, 60, [64])
+    with pytest.raises(L.LoraError) as e:
+        L.lora_apply(rp.x, rp.y, bad_shape, *args[1:], ws.buf, idx.err)
+    assert e.value.status == 2
+    with pytest.raises(L.LoraError) as e:
+        L.lora_apply(rp.x, rp.y, L.make_shape(2, 12, 64, [64]), *args[1:], ws.buf, idx.err)
+    assert e.value.status == 3
+
+
+def test_rank_above_r_max_is_rejected_on_device():
+    """A table whose rank exceeds the shape's r_max (the workspace stride) is an
+    error and the slot is skipped, never an out-of-bounds write."""
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import ResidentProjection, to_host_bits
+    wl = _small(15, 32, 128, [128], 2, [32, 8], frac_none=0.0)
+    rp = ResidentProjection.from_workload(wl)
+    idx = L.TokenIndex(wl.T, wl.S)
+    idx.build(torch.from_numpy(wl.slot_ids).cuda(), rp.table)
+    small = L.make_shape(2, 16, 128, [128])
+    ws = L.Workspace(wl.T, small)
+    L.lora_apply(rp.x, rp.y, small, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active, ws.buf, idx.err)
+    torch.cuda.synchronize()
+    assert int(idx.err.cpu().item()) == 3
+    y = to_host_bits(rp.y)
+    rows0 = wl.slot_ids == 0
+    np.testing.assert_array_equal(y[rows0], wl.modules[0].y_in[rows0])
