@@ -239,6 +239,37 @@ lora_status_t lora_apply_ex(const void *x, int64_t ldx, void *y, int64_t ldy, in
                             const int32_t *active, int32_t max_seg_hint, lora_path_t path,
                             float *ws, size_t ws_bytes, int32_t *err, lora_stream_t stream);
 
+/*
+ * lora_apply without a workspace argument, for callers that cannot allocate
+ * device memory where they run the branch: for example a plug-in inside a host
+ * engine that owns all device memory through its own pool and gives plug-ins no
+ * allocator, or code that must not call cudaMalloc because it synchronises the
+ * device.  The pages describe no counterpart of this call; it is a service of
+ * this library.
+ *
+ * It runs the same shrink and expand kernels as LORA_PATH_DECODE_SPLIT, with the
+ * fp32 shrink output kept in a fixed array inside the library's device image:
+ * LORA_NOALLOC_WS_BYTES (4 MiB) on every device that loads the library, held
+ * until the process exits.  It calls no allocating routine.
+ *   - Limit: n_slices * T * r_max * 4 bytes must fit in LORA_NOALLOC_WS_BYTES,
+ *     else the call returns LORA_ERR_WORKSPACE and enqueues nothing.
+ *   - Set-up: the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Sharing: every call on a device uses the same array, and the array keeps
+ *     the last call's contents.  Calls whose kernels overlap on the GPU (calls
+ *     on different streams, or from threads that do not order their streams)
+ *     race on it and give wrong results; issue them on one stream.  Nothing in
+ *     the array has to start at zero: the shrink writes every entry the expand
+ *     reads.
+ * Other arguments, checks and errors are those of lora_apply.
+ */
+#define LORA_NOALLOC_WS_BYTES (4u << 20)
+lora_status_t lora_apply_noalloc(const void *x, int64_t ldx, void *y, int64_t ldy, int32_t T,
+                                 const lora_shape_t *shape, const void *dev_table,
+                                 const int32_t *sorted_ids, const int32_t *seg_offsets,
+                                 const int32_t *active, int32_t *err, lora_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

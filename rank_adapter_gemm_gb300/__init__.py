@@ -17,14 +17,15 @@ from typing import Optional, Sequence
 import numpy as np
 
 from ._lib import (LORA_ABI_VERSION, LORA_DECODE_MAX_SEG, LORA_MAX_RANK, LORA_MAX_SLICES, LORA_MAX_SLOTS,
-                   PATHS, LoraError, check, load, lora_shape_t, status_string)
+                   LORA_NOALLOC_WS_BYTES, PATHS, LoraError, check, load, lora_shape_t, status_string)
 
 __all__ = [
     "LORA_ABI_VERSION", "LORA_MAX_RANK", "LORA_MAX_SLICES", "LORA_MAX_SLOTS", "LORA_DECODE_MAX_SEG",
+    "LORA_NOALLOC_WS_BYTES",
     "LoraError", "lora_shape_t", "make_shape", "lora_abi_version", "lora_status_string", "lora_scale",
     "lora_premultiply", "lora_slot_table_bytes", "lora_pack_slot_table", "lora_set_slot_table",
     "lora_build_index", "lora_workspace_bytes", "lora_shrink", "lora_expand", "lora_apply", "lora_resolve_path",
-    "SlotTable", "TokenIndex", "Workspace",
+    "lora_apply_noalloc", "SlotTable", "TokenIndex", "Workspace",
 ]
 
 
@@ -170,6 +171,19 @@ def lora_apply(x, y, shape, dev_table, sorted_ids, seg_offsets, active, ws, err,
         check(load().lora_apply(*args, *tail), "lora_apply")
     else:
         check(load().lora_apply_ex(*args, PATHS[path], *tail), "lora_apply_ex")
+
+
+def lora_apply_noalloc(x, y, shape, dev_table, sorted_ids, seg_offsets, active, err, stream=None) -> None:
+    """lora_apply with the library's built-in scratch instead of a workspace:
+    for callers that cannot allocate device memory where they run the branch.
+    Calls on one device share that scratch, so keep them on one stream."""
+    ldx = _rows(x, "x")
+    ldy = _rows(y, "y")
+    if x.shape[0] != y.shape[0]:
+        raise ValueError("x and y must have the same number of rows")
+    check(load().lora_apply_noalloc(_p(x), ldx, _p(y), ldy, int(x.shape[0]), ctypes.byref(shape), _p(dev_table),
+                                    _p(sorted_ids), _p(seg_offsets), _p(active), _p(err), _stream(stream)),
+          "lora_apply_noalloc")
 
 
 def lora_resolve_path(path: str, T: int, max_seg_hint: int = 0):

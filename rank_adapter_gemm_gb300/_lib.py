@@ -16,6 +16,7 @@ LORA_MAX_SLICES = 4
 LORA_MAX_RANK = 256
 LORA_MAX_SLOTS = 1024
 LORA_DECODE_MAX_SEG = 256
+LORA_NOALLOC_WS_BYTES = 4 << 20
 
 STATUS = {
     0: "LORA_OK",
@@ -38,7 +39,7 @@ EXPORTED = (
     "lora_abi_version", "lora_status_string", "lora_scale", "lora_premultiply",
     "lora_slot_table_bytes", "lora_pack_slot_table", "lora_set_slot_table", "lora_build_index",
     "lora_workspace_bytes", "lora_shrink", "lora_expand", "lora_apply", "lora_apply_ex",
-    "lora_resolve_path",
+    "lora_resolve_path", "lora_apply_noalloc",
 )
 
 
@@ -94,6 +95,7 @@ def load() -> ctypes.CDLL:
         "lora_apply": (ST, [P, I64, P, I64, I32, SH, P, P, P, P, I32, P, SZ, P, P]),
         "lora_apply_ex": (ST, [P, I64, P, I64, I32, SH, P, P, P, P, I32, ST, P, SZ, P, P]),
         "lora_resolve_path": (ST, [ST, I32, I32, ctypes.POINTER(I32)]),
+        "lora_apply_noalloc": (ST, [P, I64, P, I64, I32, SH, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
