@@ -75,8 +75,12 @@ typedef enum {
 
 /* Kernel path of lora_apply_ex. */
 typedef enum {
-    LORA_PATH_AUTO = 0,          /* decode kernels if max_seg_hint <= LORA_DECODE_MAX_SEG, else prefill */
-    LORA_PATH_DECODE_FUSED = 1,  /* one launch: shrink, per-segment wait, expand */
+    LORA_PATH_AUTO = 0,          /* decode kernels if max_seg_hint <= LORA_DECODE_MAX_SEG, else prefill;
+                                    the fused decode kernel when T <= 2048, r_max <= 128
+                                    and k % 16 == 0 */
+    LORA_PATH_DECODE_FUSED = 1,  /* one launch: shrink, per-(slot, slice) wait, expand; needs
+                                    T <= 2048, r_max <= 128 and k % 16 == 0
+                                    (else LORA_ERR_UNSUPPORTED) */
     LORA_PATH_DECODE_SPLIT = 2,  /* two launches: shrink then expand (programmatic dependent launch) */
     LORA_PATH_PREFILL = 3        /* tcgen05/TMEM tensor-core shrink and expand */
 } lora_path_t;
@@ -190,6 +194,12 @@ lora_status_t lora_build_index(const int32_t *slot_ids, int32_t T, int32_t S, co
 lora_status_t lora_workspace_bytes(int32_t T, const lora_shape_t *shape, size_t *bytes);
 
 /*
+ * Byte offset of xa inside the workspace (xa is float32 [n_slices][T][r_max]);
+ * 0 if the shape is invalid.  Host only.
+ */
+size_t lora_workspace_xa_offset(const lora_shape_t *shape);
+
+/*
  * Shrink: xa[i][t][j] = sum_c x[t, c] * A_s,i[j, c] for tokens t of active slots s,
  * j < r_s, accumulated in fp32 (vLLM book ch. 16, section 16.4.2: lora_shrink
  * writes buffer[num_tokens, r] from lora_a).  Other rows of xa are not written.
@@ -226,8 +236,8 @@ lora_status_t lora_apply(const void *x, int64_t ldx, void *y, int64_t ldy, int32
                          float *ws, size_t ws_bytes, int32_t *err, lora_stream_t stream);
 
 /*
- * The path lora_apply takes for this max_seg_hint (and T) on this build:
- * requested itself unless it is LORA_PATH_AUTO.  *launches receives the number
+ * The path lora_apply takes for this max_seg_hint (and T) on this build, for
+ * r_max <= 128: requested itself unless it is LORA_PATH_AUTO.  *launches receives the number
  * of kernel launches the path makes per call (may be null).  Host only.
  */
 lora_path_t lora_resolve_path(lora_path_t requested, int32_t T, int32_t max_seg_hint, int32_t *launches);

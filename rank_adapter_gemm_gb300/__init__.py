@@ -24,7 +24,7 @@ __all__ = [
     "LORA_NOALLOC_WS_BYTES",
     "LoraError", "lora_shape_t", "make_shape", "lora_abi_version", "lora_status_string", "lora_scale",
     "lora_premultiply", "lora_slot_table_bytes", "lora_pack_slot_table", "lora_set_slot_table",
-    "lora_build_index", "lora_workspace_bytes", "lora_shrink", "lora_expand", "lora_apply", "lora_resolve_path",
+    "lora_build_index", "lora_workspace_bytes", "lora_workspace_xa_offset", "lora_shrink", "lora_expand", "lora_apply", "lora_resolve_path",
     "lora_apply_noalloc", "SlotTable", "TokenIndex", "Workspace",
 ]
 
@@ -142,6 +142,11 @@ def lora_workspace_bytes(T: int, shape: lora_shape_t) -> int:
     out = ctypes.c_size_t(0)
     check(load().lora_workspace_bytes(int(T), ctypes.byref(shape), ctypes.byref(out)), "lora_workspace_bytes")
     return int(out.value)
+
+
+def lora_workspace_xa_offset(shape: lora_shape_t) -> int:
+    """Byte offset of xa (float32 [n_slices][T][r_max]) inside the workspace."""
+    return int(load().lora_workspace_xa_offset(ctypes.byref(shape)))
 
 
 def lora_shrink(x, shape, dev_table, sorted_ids, seg_offsets, active, ws, err, stream=None) -> None:

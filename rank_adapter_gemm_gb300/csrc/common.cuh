@@ -140,9 +140,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 //   B (16x8,  col-major): b0 = (k 2q..2q+1, col g), b1 = (k 2q+8.., col g)
 //   C/D (16x8, fp32):     d0,d1 = (row g, cols 2q, 2q+1), d2,d3 = (row g+8, cols 2q, 2q+1)
 // ---------------------------------------------------------------------------
+// Not volatile: a pure register operation, so the compiler may interleave
+// independent MMAs and loads.
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])

@@ -22,7 +22,7 @@ cudaError_t launch_fused_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int
                                 float *ws, int32_t T, int32_t *err, cudaStream_t stream);
 cudaError_t launch_premultiply(uint16_t *w, int64_t n, float scale, cudaStream_t stream);
 bool prefill_available();
-bool fused_decode_available();
+bool fused_decode_supported(int32_t T, int32_t r_max, int32_t k);
 cudaError_t launch_prefill(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                            const void *table, const int32_t *sorted_ids, const int32_t *seg, float *ws,
                            int32_t T, int32_t *err, cudaStream_t stream);
@@ -80,6 +80,17 @@ lora_status_t check_ws(const float *ws, size_t ws_bytes, int32_t T, const Shape 
 }
 
 lora_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA; }
+
+lora_path_t resolve(lora_path_t path, int32_t T, int32_t max_seg_hint, int32_t r_max, int32_t k, int32_t *launches) {
+    if (max_seg_hint <= 0 || max_seg_hint > T) max_seg_hint = T;
+    if (path == LORA_PATH_AUTO) {
+        if (max_seg_hint > LORA_DECODE_MAX_SEG && lora::prefill_available()) path = LORA_PATH_PREFILL;
+        else if (lora::fused_decode_supported(T, r_max, k)) path = LORA_PATH_DECODE_FUSED;
+        else path = LORA_PATH_DECODE_SPLIT;
+    }
+    if (launches != nullptr) *launches = path == LORA_PATH_DECODE_FUSED ? 1 : 2;
+    return path;
+}
 
 float *xa_of(float *ws, int32_t T, const Shape &sh) {
     const lora::WorkspaceLayout L(T, sh.n, sh.r_max, sh.S);
@@ -192,6 +203,12 @@ lora_status_t lora_workspace_bytes(int32_t T, const lora_shape_t *shape, size_t 
     return LORA_OK;
 }
 
+size_t lora_workspace_xa_offset(const lora_shape_t *shape) {
+    Shape sh;
+    if (check_shape(shape, &sh) != LORA_OK) return 0;
+    return lora::WorkspaceLayout(0, sh.n, sh.r_max, sh.S).xa_off;
+}
+
 lora_status_t lora_shrink(const void *x, int64_t ldx, int32_t T, const lora_shape_t *shape, const void *dev_table,
                           const int32_t *sorted_ids, const int32_t *seg_offsets, const int32_t *active,
                           float *ws, size_t ws_bytes, int32_t *err, lora_stream_t stream) {
@@ -225,15 +242,9 @@ lora_status_t lora_expand(const float *ws, size_t ws_bytes, void *y, int64_t ldy
 }
 
 lora_path_t lora_resolve_path(lora_path_t requested, int32_t T, int32_t max_seg_hint, int32_t *launches) {
-    lora_path_t path = requested;
-    if (max_seg_hint <= 0 || max_seg_hint > T) max_seg_hint = T;
-    if (path == LORA_PATH_AUTO) {
-        if (max_seg_hint > LORA_DECODE_MAX_SEG && lora::prefill_available()) path = LORA_PATH_PREFILL;
-        else if (lora::fused_decode_available()) path = LORA_PATH_DECODE_FUSED;
-        else path = LORA_PATH_DECODE_SPLIT;
-    }
-    if (launches != nullptr) *launches = path == LORA_PATH_DECODE_FUSED ? 1 : 2;
-    return path;
+    // without a shape the rank bound is unknown here: report the choice for the
+    // largest rank the fused kernel takes; lora_apply_ex re-resolves with r_max
+    return resolve(requested, T, max_seg_hint, 128, 4096, launches);
 }
 
 lora_status_t lora_apply_ex(const void *x, int64_t ldx, void *y, int64_t ldy, int32_t T, const lora_shape_t *shape,
@@ -253,10 +264,10 @@ lora_status_t lora_apply_ex(const void *x, int64_t ldx, void *y, int64_t ldy, in
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint16_t *xb = static_cast<const uint16_t *>(x);
     uint16_t *yb = static_cast<uint16_t *>(y);
-    path = lora_resolve_path(path, T, max_seg_hint, nullptr);
+    path = resolve(path, T, max_seg_hint, sh.r_max, sh.k, nullptr);
     switch (path) {
     case LORA_PATH_DECODE_FUSED:
-        if (!lora::fused_decode_available()) return LORA_ERR_UNSUPPORTED;
+        if (!lora::fused_decode_supported(T, sh.r_max, sh.k)) return LORA_ERR_UNSUPPORTED;
         return from_cuda(lora::launch_fused_decode(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws, T,
                                                    err, s));
     case LORA_PATH_DECODE_SPLIT: {

@@ -14,7 +14,7 @@ from _parity import assert_y_close, gpu_apply, oracle_y, untouched_rows
 
 pytestmark = pytest.mark.gpu
 
-DECODE_PATHS = ["decode_split"]
+DECODE_PATHS = ["decode_split", "decode_fused"]
 
 
 def _torch():
@@ -137,11 +137,12 @@ def test_apply_large_decode_sampled(path):
     assert_y_close(y[rows], ref, "large decode")
 
 
+@pytest.mark.parametrize("path", DECODE_PATHS)
 @pytest.mark.parametrize("mod_idx", [0, 1, 2, 3])
-def test_apply_layer_sweep_sampled(mod_idx):
+def test_apply_layer_sweep_sampled(mod_idx, path):
     """The four packed projections of one Llama-3-8B layer at T=1024, r=64."""
     wl = W.config(4, sweep=True)
-    y, err, *_ = gpu_apply(wl, mod_idx=mod_idx)
+    y, err, *_ = gpu_apply(wl, mod_idx=mod_idx, path=path)
     assert err == 0
     rng = np.random.default_rng(mod_idx)
     rows = np.sort(rng.choice(wl.T, size=96, replace=False)).astype(np.int32)
@@ -175,6 +176,8 @@ RAGGED = [
     (4, 300, 1000, [1000], 2, [64, 8]),
     (5, 129, 520, [512, 16, 8, 24], 7, [8, 16, 24, 32, 40, 48, 56]),
     (6, 257, 4096, [1024], 1, [128]),
+    (7, 90, 272, [136, 8, 528], 5, [16, 128, 40, 0, 24]),
+    (8, 200, 1040, [1040, 16], 9, [8, 8, 16, 32, 64, 120, 8, 16, 24]),
 ]
 
 
@@ -183,6 +186,12 @@ RAGGED = [
 def test_apply_ragged(case, path):
     seed, T, k, widths, S, ranks = case
     wl = _small(seed, T, k, widths, S, ranks)
+    if path == "decode_fused" and (wl.r_max > 128 or k % 16 != 0):
+        import rank_adapter_gemm_gb300 as L
+        with pytest.raises(L.LoraError) as e:  # the fused kernel takes ranks up to 128 and k % 16 == 0
+            gpu_apply(wl, path=path)
+        assert e.value.status == 9
+        return
     y, err, *_ = gpu_apply(wl, path=path)
     assert err == 0
     ref, _ = oracle_y(wl)
@@ -227,10 +236,51 @@ def test_apply_rslora_and_premultiplied_configs():
 
 
 def test_apply_is_deterministic():
+    """The split path reduces in a fixed order: bit-identical over runs."""
     wl = W.config(2)
-    ys, err, *_ = gpu_apply(wl, repeat=5)
+    ys, err, *_ = gpu_apply(wl, repeat=5, path="decode_split")
     for y in ys[1:]:
         np.testing.assert_array_equal(y, ys[0])
+
+
+def test_fused_repeat_stays_within_tolerance():
+    """The fused path adds split-k partials with fp32 reductions, whose order
+    varies; every repetition must still match the oracle."""
+    wl = W.config(2)
+    ys, err, *_ = gpu_apply(wl, repeat=5, path="decode_fused")
+    assert err == 0
+    ref, _ = oracle_y(wl)
+    for y in ys:
+        assert_y_close(y, ref, "fused repeat")
+
+
+def test_fused_leaves_workspace_clean():
+    """Each fused call clears its accumulator rows and counters, so the
+    workspace can serve the next call (another projection, other shapes)
+    without a clearing launch."""
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import ResidentProjection, to_host_bits
+    wl = W.config(2)
+    rp = ResidentProjection.from_workload(wl)
+    idx = L.TokenIndex(wl.T, wl.S)
+    idx.build(torch.from_numpy(wl.slot_ids).cuda(), rp.table)
+    ws = L.Workspace(wl.T, rp.shape)
+    ref, _ = oracle_y(wl)
+    y0 = rp.y.clone()
+    n, T, r_max = wl.modules[0].n_slices, wl.T, wl.r_max
+    xa_floats = n * T * r_max
+    for _ in range(3):
+        rp.y.copy_(y0)
+        L.lora_apply(rp.x, rp.y, rp.shape, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active, ws.buf,
+                     idx.err, path="decode_fused")
+        torch.cuda.synchronize()
+        assert int(idx.err.item()) == 0
+        assert_y_close(to_host_bits(rp.y), ref, "fused")
+        buf = ws.buf.cpu().numpy()
+        ctrl_floats = (len(buf) - 2 * xa_floats) - ((len(buf) - 2 * xa_floats) % 64)
+        assert not buf[:ctrl_floats].view(np.int32).any(), "counters not reset"
+        assert not buf[-xa_floats:].any(), "accumulator not cleared"
 
 
 # ---------------------------------------------------------------------------
@@ -247,9 +297,10 @@ def test_shrink_then_expand_entry_points():
     ws = L.Workspace(wl.T, rp.shape)
     L.lora_shrink(rp.x, rp.shape, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active, ws.buf, idx.err)
     torch.cuda.synchronize()
-    # xa follows the control block; compare it with the oracle's shrink
-    nbytes_ctrl = ws.buf.numel() * 4 - 4 * wl.modules[0].n_slices * wl.T * wl.r_max
-    xa = ws.buf[nbytes_ctrl // 4:].view(wl.modules[0].n_slices, wl.T, wl.r_max).cpu().numpy().astype(np.float64)
+    # compare xa (float32 [n][T][r_max] in the workspace) with the oracle's shrink
+    off = L.lora_workspace_xa_offset(rp.shape) // 4
+    nxa = wl.modules[0].n_slices * wl.T * wl.r_max
+    xa = ws.buf[off:off + nxa].view(wl.modules[0].n_slices, wl.T, wl.r_max).cpu().numpy().astype(np.float64)
     ref, _ = oracle.shrink(wl.modules[0].x, wl.slot_ids, wl.ranks, wl.modules[0].A, wl.r_max)
     for t in range(wl.T):
         r = wl.ranks[wl.slot_ids[t]]
