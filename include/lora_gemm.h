@@ -75,14 +75,18 @@ typedef enum {
 
 /* Kernel path of lora_apply_ex. */
 typedef enum {
-    LORA_PATH_AUTO = 0,          /* decode kernels if max_seg_hint <= LORA_DECODE_MAX_SEG, else prefill;
-                                    the fused decode kernel when T <= 2048, r_max <= 128
-                                    and k % 16 == 0 */
+    LORA_PATH_AUTO = 0,          /* the prefill kernels if max_seg_hint > LORA_DECODE_MAX_SEG and
+                                    r_max <= 64; otherwise the fused decode kernel when
+                                    T <= 2048, r_max <= 128 and k % 16 == 0, else the
+                                    split decode kernels */
     LORA_PATH_DECODE_FUSED = 1,  /* one launch: shrink, per-(slot, slice) wait, expand; needs
                                     T <= 2048, r_max <= 128 and k % 16 == 0
                                     (else LORA_ERR_UNSUPPORTED) */
     LORA_PATH_DECODE_SPLIT = 2,  /* two launches: shrink then expand (programmatic dependent launch) */
-    LORA_PATH_PREFILL = 3        /* tcgen05/TMEM tensor-core shrink and expand */
+    LORA_PATH_PREFILL = 3        /* two launches: tcgen05/TMEM tensor-core shrink (split-K over a
+                                    thread-block cluster) and expand, on 128-token tiles of
+                                    one slot's segment; needs r_max <= 64
+                                    (else LORA_ERR_UNSUPPORTED) */
 } lora_path_t;
 
 #define LORA_DECODE_MAX_SEG 256
@@ -185,11 +189,15 @@ lora_status_t lora_build_index(const int32_t *slot_ids, int32_t T, int32_t S, co
                                int32_t *err, lora_stream_t stream);
 
 /*
- * Workspace size for T tokens of a projection: an fp32 buffer xa[n_slices][T][r_max]
- * (the shrink output, row t = token t) after a control block of per-slot
- * counters.  The control block must be zero before the first call that uses the
- * workspace (e.g. cudaMemsetAsync of the whole buffer once); every call leaves
- * it zero again when it returns without LORA_ERR_TIMEOUT.
+ * Workspace size for T tokens of a projection, in order: a control block of
+ * per-slot counters; the fp32 shrink output xa[n_slices][T][r_max] (row t =
+ * token t); the fused decode kernel's fp32 accumulator (same size); and, when
+ * r_max <= 64, the prefill kernels' xa as two bf16 parts hi + lo, each
+ * [n_slices][T][RP] in sorted-token order (RP = 16, 32 or 64, the rank padded
+ * up).  Regions start on 256-byte boundaries.  The whole buffer must be zero
+ * before the first call that uses it (e.g. one cudaMemsetAsync); every call
+ * leaves the control block and the accumulator zero again when it returns
+ * without LORA_ERR_TIMEOUT.
  */
 lora_status_t lora_workspace_bytes(int32_t T, const lora_shape_t *shape, size_t *bytes);
 
@@ -237,7 +245,7 @@ lora_status_t lora_apply(const void *x, int64_t ldx, void *y, int64_t ldy, int32
 
 /*
  * The path lora_apply takes for this max_seg_hint (and T) on this build, for
- * r_max <= 128: requested itself unless it is LORA_PATH_AUTO.  *launches receives the number
+ * r_max <= 64 and k % 16 == 0: requested itself unless it is LORA_PATH_AUTO.  *launches receives the number
  * of kernel launches the path makes per call (may be null).  Host only.
  */
 lora_path_t lora_resolve_path(lora_path_t requested, int32_t T, int32_t max_seg_hint, int32_t *launches);

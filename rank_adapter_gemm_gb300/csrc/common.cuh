@@ -47,18 +47,28 @@ struct TableView {
     }
 };
 
+// Rank padding of the tensor-core prefill path: 16, 32 or 64 columns (rows of
+// 32, 64 or 128 bytes, one swizzle span).
+__host__ __device__ inline int32_t tc_rank_pad(int32_t r_max) { return r_max <= 16 ? 16 : (r_max <= 32 ? 32 : 64); }
+
 // Workspace: a control block of per-(slot, slice) counters, the fp32 xa that
-// lora_shrink writes (and lora_expand reads), and the fp32 accumulator of the
-// fused decode kernel, which every call leaves zeroed for the next one.
+// lora_shrink writes (and lora_expand reads), the fp32 accumulator of the
+// fused decode kernel, which every call leaves zeroed for the next one, and
+// (r_max <= 64) the prefill path's xa as bf16 hi and lo parts, [n][T][RP] each
+// in sorted-token order.
 struct WorkspaceLayout {
-    size_t ctrl_bytes, xa_off, acc_off, bytes;
+    size_t ctrl_bytes, xa_off, acc_off, hi_off, lo_off, bytes;
     __host__ __device__ WorkspaceLayout(int32_t T, int32_t n_slices, int32_t r_max, int32_t S) {
         // two int32 counters per (slot, slice) + a few global words, rounded to 256 B
         ctrl_bytes = (sizeof(int32_t) * (2 * size_t(S) * LORA_MAX_SLICES + 64) + 255) & ~size_t(255);
-        const size_t xa_bytes = sizeof(float) * size_t(n_slices) * size_t(T > 0 ? T : 0) * size_t(r_max);
+        const size_t tt = size_t(T > 0 ? T : 0);
+        const size_t xa_bytes = sizeof(float) * size_t(n_slices) * tt * size_t(r_max);
+        const size_t hl_bytes = r_max <= 64 ? sizeof(uint16_t) * size_t(n_slices) * tt * size_t(tc_rank_pad(r_max)) : 0;
         xa_off = ctrl_bytes;
         acc_off = xa_off + ((xa_bytes + 255) & ~size_t(255));
-        bytes = acc_off + xa_bytes;
+        hi_off = acc_off + ((xa_bytes + 255) & ~size_t(255));
+        lo_off = hi_off + ((hl_bytes + 255) & ~size_t(255));
+        bytes = lo_off + hl_bytes;
     }
 };
 
@@ -192,6 +202,86 @@ static __device__ __noinline__ int32_t block_exclusive_scan(int32_t *data, int32
     int32_t total = scratch[32];
     __syncthreads();
     return total;
+}
+
+
+// ---------------------------------------------------------------------------
+// Thread-block clusters and distributed shared memory
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// Work items over slots
+// ---------------------------------------------------------------------------
+// Per-slot work items, computed by the whole block: s_pref[s] becomes the
+// exclusive prefix of items(n_s, r_s) over slots with tokens and rank > 0.
+// Guards: the table header must match the shape, the index must cover exactly
+// T tokens and no rank may exceed r_max (the workspace row stride); otherwise
+// the offending work is dropped and the error word set.
+template <class F>
+__device__ int32_t slot_item_prefix(const void *table, const Shape &sh, const int32_t *seg, int32_t T,
+                                    int32_t *s_pref, int32_t *s_scr, int32_t *err, F items) {
+    const int32_t *hdr = static_cast<const int32_t *>(table);
+    const TableView tab(table, sh.S, sh.n);
+    const bool ok = hdr[0] == kTableMagic && hdr[1] == sh.S && hdr[2] == sh.n && seg[sh.S + 1] == T;
+    if (!ok && threadIdx.x == 0 && blockIdx.x == 0) report_error(err, LORA_ERR_INVALID_ARG);
+    for (int s = threadIdx.x; s < sh.S; s += blockDim.x) {
+        const int32_t n = ok ? seg[s + 1] - seg[s] : 0;
+        const int32_t r = ok ? tab.rank[s] : 0;
+        const bool rank_ok = r <= sh.r_max;
+        if (!rank_ok && blockIdx.x == 0) report_error(err, LORA_ERR_RANK);
+        s_pref[s] = (ok && rank_ok && n > 0 && r > 0) ? items(n, r) : 0;
+    }
+    __syncthreads();
+    return block_exclusive_scan(s_pref, sh.S, s_scr);
+}
+
+// Slot owning item u: the last slot whose exclusive prefix is <= u.
+__device__ __forceinline__ int32_t find_slot(const int32_t *s_pref, int32_t S, int32_t u) {
+    int32_t lo = 0, hi = S;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi) >> 1;
+        if (s_pref[mid] <= u) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo - 1;
+}
+
+// fp32 pair -> bf16 hi part and bf16 remainder (v = hi + lo to ~2^-17 relative).
+__device__ __forceinline__ void split_bf16x2(float v0, float v1, uint32_t &hi, uint32_t &lo) {
+    hi = pack_bf16x2(v0, v1);
+    lo = pack_bf16x2(v0 - bf16lo_to_f32(hi), v1 - bf16hi_to_f32(hi));
 }
 
 }  // namespace lora

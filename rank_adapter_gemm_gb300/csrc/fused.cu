@@ -163,12 +163,6 @@ __device__ __forceinline__ void stg_u2(void *p, uint32_t a, uint32_t b) {
     asm volatile("st.global.v2.u32 [%0], {%1,%2};" :: "l"(p), "r"(a), "r"(b) : "memory");
 }
 
-// fp32 pair -> bf16 pair plus the bf16 remainder (v = hi + lo to ~2^-17 relative)
-__device__ __forceinline__ void split_bf16x2(float v0, float v1, uint32_t &hi, uint32_t &lo) {
-    hi = pack_bf16x2(v0, v1);
-    lo = pack_bf16x2(v0 - bf16lo_to_f32(hi), v1 - bf16hi_to_f32(hi));
-}
-
 // ---------------------------------------------------------------------------
 // Work units (everything read from the prologue's shared-memory tables)
 // ---------------------------------------------------------------------------
@@ -194,15 +188,6 @@ struct Tables {
     const int32_t *tok;     // [T] sorted_ids
 };
 
-__device__ __forceinline__ int32_t find_slot(const int32_t *pref, int32_t S, int32_t u) {
-    int32_t lo = 0, hi = S;
-    while (lo < hi) {
-        const int32_t mid = (lo + hi) >> 1;
-        if (pref[mid] <= u) lo = mid + 1;
-        else hi = mid;
-    }
-    return lo - 1;
-}
 
 __device__ __forceinline__ int slice_width_max(const Shape &sh) {
     int d = 0;

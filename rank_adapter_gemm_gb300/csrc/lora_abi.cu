@@ -21,7 +21,7 @@ cudaError_t launch_fused_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int
                                 const void *table, const int32_t *sorted_ids, const int32_t *seg,
                                 float *ws, int32_t T, int32_t *err, cudaStream_t stream);
 cudaError_t launch_premultiply(uint16_t *w, int64_t n, float scale, cudaStream_t stream);
-bool prefill_available();
+bool prefill_supported(int32_t r_max);
 bool fused_decode_supported(int32_t T, int32_t r_max, int32_t k);
 cudaError_t launch_prefill(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                            const void *table, const int32_t *sorted_ids, const int32_t *seg, float *ws,
@@ -84,7 +84,7 @@ lora_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LOR
 lora_path_t resolve(lora_path_t path, int32_t T, int32_t max_seg_hint, int32_t r_max, int32_t k, int32_t *launches) {
     if (max_seg_hint <= 0 || max_seg_hint > T) max_seg_hint = T;
     if (path == LORA_PATH_AUTO) {
-        if (max_seg_hint > LORA_DECODE_MAX_SEG && lora::prefill_available()) path = LORA_PATH_PREFILL;
+        if (max_seg_hint > LORA_DECODE_MAX_SEG && lora::prefill_supported(r_max)) path = LORA_PATH_PREFILL;
         else if (lora::fused_decode_supported(T, r_max, k)) path = LORA_PATH_DECODE_FUSED;
         else path = LORA_PATH_DECODE_SPLIT;
     }
@@ -242,9 +242,9 @@ lora_status_t lora_expand(const float *ws, size_t ws_bytes, void *y, int64_t ldy
 }
 
 lora_path_t lora_resolve_path(lora_path_t requested, int32_t T, int32_t max_seg_hint, int32_t *launches) {
-    // without a shape the rank bound is unknown here: report the choice for the
-    // largest rank the fused kernel takes; lora_apply_ex re-resolves with r_max
-    return resolve(requested, T, max_seg_hint, 128, 4096, launches);
+    // without a shape the rank bound is unknown here: report the choice for
+    // r_max <= 64 and k % 16 == 0; lora_apply_ex re-resolves with the shape
+    return resolve(requested, T, max_seg_hint, 64, 4096, launches);
 }
 
 lora_status_t lora_apply_ex(const void *x, int64_t ldx, void *y, int64_t ldy, int32_t T, const lora_shape_t *shape,
@@ -277,7 +277,7 @@ lora_status_t lora_apply_ex(const void *x, int64_t ldx, void *y, int64_t ldy, in
         return from_cuda(lora::launch_expand(xa, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, T, err, true, s));
     }
     case LORA_PATH_PREFILL:
-        if (!lora::prefill_available()) return LORA_ERR_UNSUPPORTED;
+        if (!lora::prefill_supported(sh.r_max)) return LORA_ERR_UNSUPPORTED;
         return from_cuda(lora::launch_prefill(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws, T, err, s));
     default:
         return LORA_ERR_INVALID_ARG;

@@ -86,9 +86,14 @@ def test_workspace_bytes(L):
     sh = L.make_shape(32, 64, 4096, [4096, 1024, 1024])
     nbytes = L.lora_workspace_bytes(256, sh)
     xa = 3 * 256 * 64 * 4
-    # control block, the shrink output xa, and the fused kernel's accumulator (same size as xa)
-    assert nbytes >= 2 * xa
-    assert nbytes - 2 * xa < 4 * (2 * 32 * 4 + 64) + 2 * 256
+    hl = 3 * 256 * 64 * 2  # prefill xa as bf16 hi and lo, rank padded to 64
+    # control block, the shrink output xa, the fused kernel's accumulator (same
+    # size as xa) and the prefill path's hi/lo parts
+    assert nbytes >= 2 * xa + 2 * hl
+    assert nbytes - 2 * xa - 2 * hl < 4 * (2 * 32 * 4 + 64) + 4 * 256
+    # ranks above 64 have no prefill region
+    big = L.lora_workspace_bytes(256, L.make_shape(32, 128, 4096, [4096]))
+    assert 2 * 256 * 128 * 4 <= big < 2 * 256 * 128 * 4 + 4 * (2 * 32 * 4 + 64) + 4 * 256
     with pytest.raises(L.LoraError) as e:
         L.lora_workspace_bytes(10, L.make_shape(0, 64, 4096, [4096]))
     assert e.value.status == 1

@@ -152,17 +152,34 @@ def test_apply_layer_sweep_sampled(mod_idx, path):
     np.testing.assert_array_equal(y[keep], wl.modules[mod_idx].y_in[keep])
 
 
+@pytest.mark.parametrize("path", ["auto", "decode_split"])
 @pytest.mark.parametrize("mod_idx", [0, 1])
-def test_apply_prefill_sampled(mod_idx):
+def test_apply_prefill_sampled(mod_idx, path):
     """Prefill MLP (about 17k tokens): sampled rows from every request, plus the
-    first and last token of the batch."""
+    first and last token of the batch.  "auto" takes the tensor-core prefill
+    kernels here (segments far above LORA_DECODE_MAX_SEG)."""
+    import rank_adapter_gemm_gb300 as L
     wl = W.config(3)
-    y, err, *_ = gpu_apply(wl, mod_idx=mod_idx)
+    if path == "auto":
+        assert L.lora_resolve_path("auto", wl.T, wl.T)[0] == "prefill"
+    y, err, *_ = gpu_apply(wl, mod_idx=mod_idx, path=path)
     assert err == 0
     rng = np.random.default_rng(100 + mod_idx)
-    rows = np.unique(np.concatenate([[0, wl.T - 1], rng.choice(wl.T, size=62, replace=False)])).astype(np.int32)
+    rows = np.unique(np.concatenate([[0, wl.T - 1], rng.choice(wl.T, size=190, replace=False)])).astype(np.int32)
     ref, _ = oracle_y(wl, mod_idx=mod_idx, rows=rows)
     assert_y_close(y[rows], ref, wl.modules[mod_idx].name)
+    keep = untouched_rows(wl)
+    np.testing.assert_array_equal(y[keep], wl.modules[mod_idx].y_in[keep])
+
+
+def test_prefill_is_deterministic():
+    """The prefill shrink reduces its split-K partials in cluster-rank order and
+    the expand adds each product once: bit-identical over runs."""
+    wl = _small(21, 1500, 2048, [1024, 512], 3, [16, 16, 8], frac_none=0.05)
+    ys, err, *_ = gpu_apply(wl, repeat=3, path="prefill")
+    assert err == 0
+    for y in ys[1:]:
+        np.testing.assert_array_equal(y, ys[0])
 
 
 # ---------------------------------------------------------------------------
@@ -181,11 +198,17 @@ RAGGED = [
 ]
 
 
-@pytest.mark.parametrize("path", DECODE_PATHS)
+@pytest.mark.parametrize("path", DECODE_PATHS + ["prefill"])
 @pytest.mark.parametrize("case", RAGGED, ids=[f"ragged{c[0]}" for c in RAGGED])
 def test_apply_ragged(case, path):
     seed, T, k, widths, S, ranks = case
     wl = _small(seed, T, k, widths, S, ranks)
+    if path == "prefill" and wl.r_max > 64:
+        import rank_adapter_gemm_gb300 as L
+        with pytest.raises(L.LoraError) as e:  # the tensor-core path pads ranks to at most 64
+            gpu_apply(wl, path=path)
+        assert e.value.status == 9
+        return
     if path == "decode_fused" and (wl.r_max > 128 or k % 16 != 0):
         import rank_adapter_gemm_gb300 as L
         with pytest.raises(L.LoraError) as e:  # the fused kernel takes ranks up to 128 and k % 16 == 0
@@ -198,6 +221,46 @@ def test_apply_ragged(case, path):
     assert_y_close(y, ref, f"ragged {seed}")
     keep = untouched_rows(wl)
     np.testing.assert_array_equal(y[keep], wl.modules[0].y_in[keep])
+
+
+# Long segments for the tensor-core path: several 128-token tiles per slot with
+# ragged tails, gathered (non-contiguous) rows, k not a multiple of 64, slice
+# widths not multiples of 256 or 64, and every rank padding (16, 32, 64).
+PREFILL = [
+    # seed, T, k, widths, S, ranks, slot_dist
+    (31, 700, 4096, [4096], 2, [16, 16], "uniform"),
+    (32, 1000, 520, [264, 8, 1000], 4, [32, 8, 0, 24], "uniform"),
+    (33, 2100, 1024, [1536, 512], 6, [64, 16, 8, 64, 48, 32], "zipf"),
+    (34, 513, 64, [72], 1, [16], "uniform"),
+    (35, 3000, 8192, [512, 512, 512, 512], 5, [16, 8, 16, 0, 8], "uniform"),
+    (36, 400, 4104, [4104], 3, [64, 64, 56], "uniform"),
+]
+
+
+@pytest.mark.parametrize("case", PREFILL, ids=[f"prefill{c[0]}" for c in PREFILL])
+@pytest.mark.parametrize("y_init", ["zeros", "normal"])
+def test_apply_prefill_long_segments(case, y_init):
+    seed, T, k, widths, S, ranks, dist = case
+    wl = _small(seed, T, k, widths, S, ranks, slot_dist=dist, y_init=y_init, frac_none=0.05)
+    y, err, *_ = gpu_apply(wl, path="prefill")
+    assert err == 0
+    ref, _ = oracle_y(wl)
+    assert_y_close(y, ref, f"prefill {seed}")
+    keep = untouched_rows(wl)
+    np.testing.assert_array_equal(y[keep], wl.modules[0].y_in[keep])
+
+
+def test_prefill_request_major_batch():
+    """Requests of 128..2048 tokens laid out one after another, each with one
+    adapter (the prefill batch shape), reduced to k = 1024 so every row is checked."""
+    wl = W.generate(name="req", seed=41, T=None, S=8, rank=16,
+                    modules=[{"name": "m", "k": 1024, "slices": [2048, 2048]}],
+                    requests={"n": 6, "min_len": 128, "max_len": 2048, "n_adapters": 8},
+                    alpha=32.0, scale_rule="alpha_over_sqrt_r", y_init="normal")
+    y, err, *_ = gpu_apply(wl, path="prefill")
+    assert err == 0
+    ref, _ = oracle_y(wl)
+    assert_y_close(y, ref, "request-major prefill")
 
 
 def test_apply_all_tokens_without_adapter():
@@ -270,6 +333,8 @@ def test_fused_leaves_workspace_clean():
     y0 = rp.y.clone()
     n, T, r_max = wl.modules[0].n_slices, wl.T, wl.r_max
     xa_floats = n * T * r_max
+    xa_off = L.lora_workspace_xa_offset(rp.shape) // 4
+    acc_off = xa_off + (xa_floats + 63) // 64 * 64  # regions start on 256-byte boundaries
     for _ in range(3):
         rp.y.copy_(y0)
         L.lora_apply(rp.x, rp.y, rp.shape, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active, ws.buf,
@@ -278,9 +343,8 @@ def test_fused_leaves_workspace_clean():
         assert int(idx.err.item()) == 0
         assert_y_close(to_host_bits(rp.y), ref, "fused")
         buf = ws.buf.cpu().numpy()
-        ctrl_floats = (len(buf) - 2 * xa_floats) - ((len(buf) - 2 * xa_floats) % 64)
-        assert not buf[:ctrl_floats].view(np.int32).any(), "counters not reset"
-        assert not buf[-xa_floats:].any(), "accumulator not cleared"
+        assert not buf[:xa_off].view(np.int32).any(), "counters not reset"
+        assert not buf[acc_off:acc_off + xa_floats].any(), "accumulator not cleared"
 
 
 # ---------------------------------------------------------------------------
