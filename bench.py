@@ -53,6 +53,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="decode_qkv", choices=list(CONFIG_INDEX))
     p.add_argument("--layers", type=int, default=32)
+    p.add_argument("--requests", type=int, default=16, help="prefill_mlp only: requests in the batch")
     p.add_argument("--path", default="auto", choices=["auto", "decode_fused", "decode_split", "prefill"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -192,9 +193,17 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
-def _workload(name):
+def _workload(name, n_requests=16):
     idx = CONFIG_INDEX[name]
-    return W.config(idx, y_init="normal")
+    return W.config(idx, y_init="normal", n_requests=n_requests)
+
+
+HEADLINE = "LoRA-branch tokens/sec and achieved HBM GB/s (% of peak), Llama-3-8B QKV decode"
+
+
+def metric_name(config):
+    return HEADLINE if config == "decode_qkv" else \
+        f"LoRA-branch tokens/sec and achieved HBM GB/s (% of peak), {config}"
 
 
 def run_ours(args):
@@ -207,7 +216,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    wl = _workload(args.config)
+    wl = _workload(args.config, args.requests)
     mods = list(range(len(wl.modules)))
     # layer l uses projection mods[l % len(mods)] in its own buffers
     base = [ResidentProjection.from_workload(wl, m, device=dev) for m in mods]
@@ -315,7 +324,7 @@ def run_ours(args):
 
     clocks = sampler.summary(w0, w1)
     out = {
-        "metric": "LoRA-branch tokens/s (Llama-3-8B packed QKV decode)",
+        "metric": metric_name(args.config),
         "value": value,
         "unit": "tokens/s",
         "n_gpus": world,
@@ -451,7 +460,7 @@ def run_reference(args):
     rank, world, _ = dist_info()
     if rank != 0:
         return None, rank
-    wl = _workload(args.config)
+    wl = _workload(args.config, args.requests)
     rows = np.arange(wl.T, dtype=np.int32)
     for _ in range(max(args.warmup, 0)):
         _oracle_call(wl, rows[:max(1, len(rows) // 8)])
@@ -465,7 +474,7 @@ def run_reference(args):
         t += _oracle_call(wl, sample)
     value = n_rows * args.steps / t
     out = {
-        "metric": "LoRA-branch tokens/s (Llama-3-8B packed QKV decode)",
+        "metric": metric_name(args.config),
         "value": value,
         "unit": "tokens/s",
         "n_gpus": world,

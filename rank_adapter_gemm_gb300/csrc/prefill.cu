@@ -18,7 +18,7 @@
 //
 // Shrink: one cluster of KS CTAs per tile splits k (split-K, TensorRT-LLM LoRA
 // serving page, "path 2: split-K tuning": M small against K gives too few
-// blocks).  Each CTA runs a 4-stage copy pipeline feeding one MMA thread, the
+// blocks).  Each CTA runs a 4- to 8-stage copy pipeline feeding one MMA thread, the
 // partial [128 x n*RP] sums meet through distributed shared memory in rank order
 // (deterministic), and xa is written as two bf16 parts, hi + lo (xa to about
 // 2^-17 relative), in sorted order: [n][T][RP].
@@ -26,9 +26,10 @@
 // Expand: a persistent CTA per SM walks units (tile, slice, 256 output columns).
 // One warp stages the unit's xa hi/lo and B tiles, one thread issues
 // D = xa_hi B^T + xa_lo B^T into one of two tensor-memory accumulators, two
-// warps stream the unit's y rows into a ring of 16 KB buffers, and four warps
-// read the accumulator (one token row per thread), add it to y in fp32, round
-// once to bf16 and write the rows back with coalesced stores.
+// warps stream the unit's y rows into a ring of 16 KB buffers, and eight warps
+// (two groups taking alternate buffers) read the accumulator (one token row per
+// thread), add it to y in fp32, round once to bf16 and write the rows back with
+// coalesced stores.
 #include <algorithm>
 
 #include "common.cuh"
@@ -46,7 +47,8 @@ constexpr int kSub = 64;                        // output columns per y buffer
 constexpr int kYBuf = kTile * kSub * 2;         // 16 KB
 constexpr uint64_t kWaitNs = 2000000000ull;     // bound on every wait: 2 s
 constexpr int kShrinkThreads = 160;             // warps 0-3 copy + epilogue, warp 4 MMA
-constexpr int kExpandThreads = 256;             // warp 0 MMA, 1 operands, 2-3 y, 4-7 epilogue
+constexpr int kEpiWarps = 8;                    // expand epilogue: two groups of four warps
+constexpr int kExpandThreads = 128 + 32 * kEpiWarps;  // warp 0 MMA, 1 operands, 2-3 y, 4-11 epilogue
 constexpr int kSmemLimit = 227 * 1024;
 
 struct PrefillArgs {
@@ -184,6 +186,7 @@ __global__ void __launch_bounds__(kShrinkThreads) tc_shrink_kernel(PrefillArgs a
     if (warp < 4) {
         // ---- producers: x rows (gathered) and the A rows of every slice ----
         const int tid = threadIdx.x;
+        const int depth = stages - 1;
         for (int32_t it = 0; it < nloc; ++it) {
             const int st = it % stages;
             if (it >= stages && !tc::mbar_wait(&empty[st], ((it / stages) - 1) & 1, abort_flag, kWaitNs)) {
@@ -208,15 +211,18 @@ __global__ void __launch_bounds__(kShrinkThreads) tc_shrink_kernel(PrefillArgs a
                      v ? A + static_cast<int64_t>(j) * sh.k + col : a.x, v);
             }
             tc::cp_commit();
-            if (it >= 2) {
-                tc::cp_wait_group<2>();
+            // stage it - depth has landed (this thread's part): publish it to
+            // the MMA thread.  The slot refilled next was published one
+            // iteration ago, so depth = stages - 1 keeps the ring full.
+            if (it >= depth) {
+                tc::cp_wait_group_n(depth);
                 tc::fence_async_smem();
-                tc::mbar_arrive(&full[(it - 2) % stages]);
+                tc::mbar_arrive(&full[(it - depth) % stages]);
             }
         }
         tc::cp_wait_all();
         tc::fence_async_smem();
-        for (int32_t it = max(0, nloc - 2); it < nloc; ++it) tc::mbar_arrive(&full[it % stages]);
+        for (int32_t it = max(0, nloc - depth); it < nloc; ++it) tc::mbar_arrive(&full[it % stages]);
     } else {
         // ---- MMA issuer: D[:, i*RP .. +RP) += x_tile A_i^T over this CTA's k range ----
         if (lane == 0) {
@@ -328,8 +334,8 @@ __device__ __forceinline__ Unit unit_info(int64_t u, int32_t per_tile, const Chu
 
 // Shared memory (base rounded up to 1024 bytes): two operand stages of
 // [xa_hi 128xRP | xa_lo 128xRP | B 256xRP] (rows of RP*2 bytes, swizzled to that
-// width), `ystages` y buffers of 128 rows x 128 bytes (128-byte swizzle), then
-// barriers and the tile table.
+// width), `ystages` (even) y buffers of 128 rows x 128 bytes (128-byte swizzle),
+// then barriers, the tile table and the segment offsets.
 template <int RP>
 __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(PrefillArgs a, Shape sh, const void *table,
                                                                       int32_t ystages) {
@@ -349,12 +355,14 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(PrefillArg
     uint64_t *y_empty = y_full + ystages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(y_empty + ystages);
     volatile int32_t *abort_flag = reinterpret_cast<int32_t *>(tmem_slot + 1);
-    int32_t *s_pref = reinterpret_cast<int32_t *>(tmem_slot + 2);
-    int32_t *s_scr = s_pref + sh.S;
+    int32_t *s_pref = reinterpret_cast<int32_t *>(tmem_slot + 2);  // [S]
+    int32_t *s_scr = s_pref + sh.S;                                // [40]
+    int32_t *s_seg = s_scr + 40;                                   // [S + 1]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const TableView tab(table, sh.S, sh.n);
     const int32_t ntiles = slot_item_prefix(table, sh, a.seg, a.T, s_pref, s_scr, a.err, tiles_of);
+    for (int i = threadIdx.x; i <= sh.S; i += blockDim.x) s_seg[i] = a.seg[i];
     ChunkPrefix cp;
     cp.pre[0] = 0;
     for (int i = 0; i < LORA_MAX_SLICES; ++i)
@@ -370,7 +378,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(PrefillArg
                 tc::mbar_init(&op_full[b], 32);
                 tc::mbar_init(&op_empty[b], 1);
                 tc::mbar_init(&acc_full[b], 1);
-                tc::mbar_init(&acc_empty[b], 4);
+                tc::mbar_init(&acc_empty[b], kEpiWarps);
             }
             tc::mbar_init(drain, 1);
             for (int b = 0; b < ystages; ++b) {
@@ -421,12 +429,13 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(PrefillArg
         // ---- operands: xa hi/lo rows of the tile and the B rows of the chunk ----
         for (int64_t u = u_lo; u < u_hi; ++u) {
             const int32_t it = static_cast<int32_t>(u - u_lo), b = it & 1;
+            const Unit un = unit_info(u, per_tile, cp, sh, s_pref, s_seg);
+            const int32_t r_s = tab.rank[un.s];
+            const uint16_t *B = reinterpret_cast<const uint16_t *>(tab.b_ptr[un.s * sh.n + un.i]);
             if (it >= 2 && !tc::mbar_wait(&op_empty[b], ((it >> 1) - 1) & 1, abort_flag, kWaitNs)) {
                 give_up(a.err, abort_flag);
                 break;
             }
-            const Unit un = unit_info(u, per_tile, cp, sh, s_pref, a.seg);
-            const int32_t r_s = tab.rank[un.s];
             const uint32_t ob = sbase + b * op_bytes;
             constexpr int cpr = rowb / 16;  // 16-byte chunks per row
             const size_t xrow = static_cast<size_t>(un.i) * a.T + un.p0;
@@ -438,12 +447,11 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(PrefillArg
                 tc::cp16(ob + d, v ? a.xa_hi + o : a.xa_hi, v);
                 tc::cp16(ob + xa_bytes + d, v ? a.xa_lo + o : a.xa_lo, v);
             }
-            const uint16_t *B = reinterpret_cast<const uint16_t *>(tab.b_ptr[un.s * sh.n + un.i]);
             for (int q = lane; q < kCols * cpr; q += 32) {
                 const int m = q / cpr, c = q % cpr;
                 const bool v = m < un.width && 8 * c < r_s;
                 tc::cp16(ob + 2 * xa_bytes + tc::swz_offset(m, c, rowb),
-                     v ? B + static_cast<int64_t>(un.c0 + m) * r_s + 8 * c : a.xa_hi, v);
+                         v ? B + static_cast<int64_t>(un.c0 + m) * r_s + 8 * c : a.xa_hi, v);
             }
             tc::cp_wait_all();
             tc::fence_async_smem();
@@ -451,19 +459,29 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(PrefillArg
         }
         tc::cp_wait_all();
     } else if (warp < 4) {
-        // ---- y rows of the unit, 64 columns per buffer ----
+        // ---- y rows of the unit, 64 columns per buffer; the next unit's token
+        // ids are fetched while this unit's copies are issued ----
         const int yt = threadIdx.x - 64;  // 0..63
         int32_t yit = 0;
         bool stop = false;
-        for (int64_t u = u_lo; u < u_hi && !stop; ++u) {
-            const Unit un = unit_info(u, per_tile, cp, sh, s_pref, a.seg);
-            int32_t tok[16];
+        int32_t tok[16], tok_next[16];
+        Unit un_next = unit_info(u_lo, per_tile, cp, sh, s_pref, s_seg);
+        auto fetch = [&](const Unit &un, int32_t (&dst)[16]) {
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
                 const int row = (yt >> 3) + 8 * m;
-                int32_t t = row < un.len ? a.sorted_ids[un.p0 + row] : -1;
-                if (t >= a.T) t = -1;
-                tok[m] = t;
+                const int32_t t = row < un.len ? a.sorted_ids[un.p0 + row] : -1;
+                dst[m] = t < a.T ? t : -1;
+            }
+        };
+        fetch(un_next, tok_next);
+        for (int64_t u = u_lo; u < u_hi && !stop; ++u) {
+            const Unit un = un_next;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) tok[m] = tok_next[m];
+            if (u + 1 < u_hi) {
+                un_next = unit_info(u + 1, per_tile, cp, sh, s_pref, s_seg);
+                fetch(un_next, tok_next);
             }
             const int nsub = (un.width + kSub - 1) / kSub;
             for (int q = 0; q < nsub; ++q, ++yit) {
@@ -487,25 +505,33 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(PrefillArg
         }
         tc::cp_wait_all();
     } else {
-        // ---- epilogue: one token row per thread ----
-        const int eq = warp & 3, row = 32 * eq + lane;
+        // ---- epilogue: two groups of four warps take alternate y buffers; in
+        // each group a warp owns 32 token rows (its tensor-memory lane quarter)
+        // and a thread one row ----
+        const int eq = warp & 3, grp = (warp - 4) >> 2, row = 32 * eq + lane;
         int32_t yit = 0;
         bool stop = false;
+        Unit un_next = unit_info(u_lo, per_tile, cp, sh, s_pref, s_seg);
+        int32_t t_next = row < un_next.len ? a.sorted_ids[un_next.p0 + row] : -1;
         for (int64_t u = u_lo; u < u_hi && !stop; ++u) {
             const int32_t it = static_cast<int32_t>(u - u_lo), b = it & 1;
-            const Unit un = unit_info(u, per_tile, cp, sh, s_pref, a.seg);
+            const Unit un = un_next;
+            const int32_t t = t_next < a.T ? t_next : -1;
+            if (u + 1 < u_hi) {
+                un_next = unit_info(u + 1, per_tile, cp, sh, s_pref, s_seg);
+                t_next = row < un_next.len ? a.sorted_ids[un_next.p0 + row] : -1;
+            }
             if (!__all_sync(0xffffffffu, tc::mbar_wait(&acc_full[b], (it >> 1) & 1, abort_flag, kWaitNs))) {
                 give_up(a.err, abort_flag);
                 break;
             }
             tc::fence_after_sync();
-            int32_t t = row < un.len ? a.sorted_ids[un.p0 + row] : -1;
-            if (t >= a.T) t = -1;
             const float sc = tab.scale[un.s];
             const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * eq) << 16) + b * kCols;
             uint16_t *yrow = a.y + sh.off[un.i] + un.c0;
             const int nsub = (un.width + kSub - 1) / kSub;
             for (int q = 0; q < nsub; ++q, ++yit) {
+                if ((yit & 1) != grp) continue;
                 const int yb = yit % ystages;
                 if (!__all_sync(0xffffffffu, tc::mbar_wait(&y_full[yb], (yit / ystages) & 1, abort_flag, kWaitNs))) {
                     give_up(a.err, abort_flag);
@@ -513,18 +539,16 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(PrefillArg
                     break;
                 }
                 const uint32_t ys = ybase + yb * kYBuf;
+                uint32_t acc[64];
 #pragma unroll
-                for (int h = 0; h < kSub / 16; ++h) {
-                    uint32_t acc[16];
-                    tc::tmem_ld16(tbase + q * kSub + 16 * h, acc);
-                    if (t >= 0) {
+                for (int h = 0; h < kSub / 16; ++h) tc::tmem_ld16_async(tbase + q * kSub + 16 * h, acc + 16 * h);
+                tc::tmem_wait_ld64(acc);
+                if (t >= 0) {
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int c = 2 * h + e;
-                            if (q * kSub + 8 * c < un.width) {
-                                const uint32_t addr = ys + tc::swz_offset(row, c, 128);
-                                sts_u4(addr, add_scaled(lds_u4(addr), acc + 8 * e, sc));
-                            }
+                    for (int c = 0; c < kSub / 8; ++c) {
+                        if (q * kSub + 8 * c < un.width) {
+                            const uint32_t addr = ys + tc::swz_offset(row, c, 128);
+                            sts_u4(addr, add_scaled(lds_u4(addr), acc + 8 * c, sc));
                         }
                     }
                 }
@@ -543,6 +567,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(PrefillArg
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&y_empty[yb]);
             }
+            if (stop) break;
             tc::fence_before_sync();
             if (lane == 0) tc::mbar_arrive(&acc_empty[b]);
         }
@@ -557,15 +582,18 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(PrefillArg
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-size_t table_words(int32_t S) { return sizeof(int32_t) * (static_cast<size_t>(S) + 40); }
+size_t table_words(int32_t S) { return sizeof(int32_t) * (2 * static_cast<size_t>(S) + 48); }
 
 size_t shrink_smem(int RP, int n, int stages, int32_t S) {
     return 1024 + static_cast<size_t>(stages) * (kXStage + n * RP * kKB * 2) + 8 * (2 * stages + 1) + 8 +
            sizeof(int32_t) * kTile + table_words(S);
 }
 
+// About 100 KB of stages (two CTAs per SM where they fit), at least 4.
 int shrink_stages(int RP, int n, int32_t S) {
-    for (int st = 4; st >= 3; --st)
+    const int stage = kXStage + n * RP * kKB * 2;
+    int st = std::min(8, std::max(4, (100 * 1024) / stage));
+    for (; st >= 3; --st)
         if (shrink_smem(RP, n, st, S) <= static_cast<size_t>(kSmemLimit)) return st;
     return 0;
 }
@@ -575,8 +603,9 @@ size_t expand_smem(int RP, int ystages, int32_t S) {
            8 * (9 + 2 * ystages) + 8 + table_words(S);
 }
 
+// An even number of y buffers (the two epilogue groups take alternate ones).
 int expand_ystages(int RP, int32_t S) {
-    for (int ys = 8; ys >= 2; --ys)
+    for (int ys = 8; ys >= 2; ys -= 2)
         if (expand_smem(RP, ys, S) <= static_cast<size_t>(kSmemLimit)) return ys;
     return 0;
 }

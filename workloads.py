@@ -215,7 +215,7 @@ LLAMA3_8B_LAYER = [
 CONFIG_NAMES = ("tiny", "decode_q_proj", "decode_qkv", "prefill_mlp", "large_decode")
 
 
-def config(index: int, y_init: str = "normal", sweep: bool = False) -> Workload:
+def config(index: int, y_init: str = "normal", sweep: bool = False, n_requests: int = 16) -> Workload:
     """Config ``index`` (0..4) of the benchmark suite, drawn at seed 1000+index.
 
     0 tiny: T=8, k=d=256, one slice, S=2, r=8, slot ids uniform over {-1,0,1},
@@ -225,7 +225,8 @@ def config(index: int, y_init: str = "normal", sweep: bool = False) -> Workload:
     2 decode packed QKV (Llama-3-8B shapes): T=256, k=4096, slices 4096/1024/1024,
       S=32, ranks drawn from {8,16,32,64} (r_max 64), Zipf(1.1) slot popularity,
       alpha=2r.
-    3 prefill MLP: 16 requests of uniform length in [128, 2048], request-major,
+    3 prefill MLP: 16 requests (``n_requests``, a smaller batch of the same
+      recipe for profiling) of uniform length in [128, 2048], request-major,
       adapter per request uniform over 16 slots; gate_up (k=4096, 14336+14336)
       then down (k=14336, d=4096); r=16; rsLoRA alpha/sqrt(r) with alpha=32.
     4 large multi-tenant decode: T=1024, k=d=8192, r=64, S=128, Zipf(1.1) with 5%
@@ -255,9 +256,9 @@ def config(index: int, y_init: str = "normal", sweep: bool = False) -> Workload:
         return generate(name="prefill_mlp", seed=seed, T=None, S=16, rank=16,
                         modules=[{"name": "gate_up", "k": 4096, "slices": [14336, 14336]},
                                  {"name": "down", "k": 14336, "slices": [4096]}],
-                        requests={"n": 16, "min_len": 128, "max_len": 2048, "n_adapters": 16},
+                        requests={"n": n_requests, "min_len": 128, "max_len": 2048, "n_adapters": 16},
                         alpha=32.0, scale_rule="alpha_over_sqrt_r", y_init=y_init,
-                        description="16 requests, lengths U[128,2048], gate_up 4096->2x14336, "
+                        description=f"{n_requests} requests, lengths U[128,2048], gate_up 4096->2x14336, "
                                     "down 14336->4096, r=16, rsLoRA")
     if index == 4:
         mods = LLAMA3_8B_LAYER if sweep else [{"name": "qo_8192", "k": 8192, "slices": [8192]}]
