@@ -76,17 +76,22 @@ typedef enum {
 /* Kernel path of lora_apply_ex. */
 typedef enum {
     LORA_PATH_AUTO = 0,          /* the prefill kernels if max_seg_hint > LORA_DECODE_MAX_SEG and
-                                    r_max <= 64; otherwise the fused decode kernel when
-                                    T <= 2048, r_max <= 128 and k % 16 == 0, else the
+                                    r_max <= 64; otherwise the fused decode path when it takes
+                                    the shape (the faster of its kernels for the shape), else the
                                     split decode kernels */
-    LORA_PATH_DECODE_FUSED = 1,  /* one launch: shrink, per-(slot, slice) wait, expand; needs
-                                    T <= 2048, r_max <= 128 and k % 16 == 0
-                                    (else LORA_ERR_UNSUPPORTED) */
+    LORA_PATH_DECODE_FUSED = 1,  /* one launch: shrink, per-(slot, slice) wait, expand, on warp-level
+                                    MMA; needs T <= 2048, r_max <= 128 and k % 16 == 0, else the
+                                    tensor-core fused kernel when it applies (LORA_PATH_DECODE_TC),
+                                    else LORA_ERR_UNSUPPORTED */
     LORA_PATH_DECODE_SPLIT = 2,  /* two launches: shrink then expand (programmatic dependent launch) */
-    LORA_PATH_PREFILL = 3        /* two launches: tcgen05/TMEM tensor-core shrink (split-K over a
+    LORA_PATH_PREFILL = 3,       /* two launches: tcgen05/TMEM tensor-core shrink (split-K over a
                                     thread-block cluster) and expand, on 128-token tiles of
                                     one slot's segment; needs r_max <= 64
                                     (else LORA_ERR_UNSUPPORTED) */
+    LORA_PATH_DECODE_TC = 4      /* one launch, tcgen05/TMEM tensor cores: split-K shrink with
+                                    per-(slot, slice) completion counters, then a transposed
+                                    expand; needs T <= 2048, r_max <= 64 and tables that fit in
+                                    shared memory (else LORA_ERR_UNSUPPORTED) */
 } lora_path_t;
 
 #define LORA_DECODE_MAX_SEG 256

@@ -22,6 +22,10 @@ cudaError_t launch_fused_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int
                                 float *ws, int32_t T, int32_t *err, cudaStream_t stream);
 cudaError_t launch_premultiply(uint16_t *w, int64_t n, float scale, cudaStream_t stream);
 bool prefill_supported(int32_t r_max);
+bool fused_tc_supported(int32_t T, const Shape &sh);
+cudaError_t launch_fused_tc(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
+                            const void *table, const int32_t *sorted_ids, const int32_t *seg, float *ws, int32_t T,
+                            int32_t *err, cudaStream_t stream);
 bool fused_decode_supported(int32_t T, int32_t r_max, int32_t k);
 cudaError_t launch_prefill(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                            const void *table, const int32_t *sorted_ids, const int32_t *seg, float *ws,
@@ -81,14 +85,20 @@ lora_status_t check_ws(const float *ws, size_t ws_bytes, int32_t T, const Shape 
 
 lora_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA; }
 
-lora_path_t resolve(lora_path_t path, int32_t T, int32_t max_seg_hint, int32_t r_max, int32_t k, int32_t *launches) {
+// The fused decode path: the warp-level MMA kernel where it applies (faster
+// today on the decode shapes measured), else the tensor-core (tcgen05) one.
+bool fused_ok(int32_t T, const Shape &sh) {
+    return lora::fused_decode_supported(T, sh.r_max, sh.k) || lora::fused_tc_supported(T, sh);
+}
+
+lora_path_t resolve(lora_path_t path, int32_t T, int32_t max_seg_hint, const Shape &sh, int32_t *launches) {
     if (max_seg_hint <= 0 || max_seg_hint > T) max_seg_hint = T;
     if (path == LORA_PATH_AUTO) {
-        if (max_seg_hint > LORA_DECODE_MAX_SEG && lora::prefill_supported(r_max)) path = LORA_PATH_PREFILL;
-        else if (lora::fused_decode_supported(T, r_max, k)) path = LORA_PATH_DECODE_FUSED;
+        if (max_seg_hint > LORA_DECODE_MAX_SEG && lora::prefill_supported(sh.r_max)) path = LORA_PATH_PREFILL;
+        else if (fused_ok(T, sh)) path = LORA_PATH_DECODE_FUSED;
         else path = LORA_PATH_DECODE_SPLIT;
     }
-    if (launches != nullptr) *launches = path == LORA_PATH_DECODE_FUSED ? 1 : 2;
+    if (launches != nullptr) *launches = (path == LORA_PATH_DECODE_FUSED || path == LORA_PATH_DECODE_TC) ? 1 : 2;
     return path;
 }
 
@@ -242,9 +252,15 @@ lora_status_t lora_expand(const float *ws, size_t ws_bytes, void *y, int64_t ldy
 }
 
 lora_path_t lora_resolve_path(lora_path_t requested, int32_t T, int32_t max_seg_hint, int32_t *launches) {
-    // without a shape the rank bound is unknown here: report the choice for
-    // r_max <= 64 and k % 16 == 0; lora_apply_ex re-resolves with the shape
-    return resolve(requested, T, max_seg_hint, 64, 4096, launches);
+    // without a shape the rank bound is unknown here: report the choice for one
+    // 4096 -> 4096 slice with r_max 64; lora_apply_ex re-resolves with the shape
+    Shape sh{};
+    sh.S = 1;
+    sh.r_max = 64;
+    sh.k = 4096;
+    sh.n = 1;
+    for (int i = 1; i <= LORA_MAX_SLICES; ++i) sh.off[i] = 4096;
+    return resolve(requested, T, max_seg_hint, sh, launches);
 }
 
 lora_status_t lora_apply_ex(const void *x, int64_t ldx, void *y, int64_t ldy, int32_t T, const lora_shape_t *shape,
@@ -264,12 +280,19 @@ lora_status_t lora_apply_ex(const void *x, int64_t ldx, void *y, int64_t ldy, in
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint16_t *xb = static_cast<const uint16_t *>(x);
     uint16_t *yb = static_cast<uint16_t *>(y);
-    path = resolve(path, T, max_seg_hint, sh.r_max, sh.k, nullptr);
+    path = resolve(path, T, max_seg_hint, sh, nullptr);
     switch (path) {
     case LORA_PATH_DECODE_FUSED:
-        if (!lora::fused_decode_supported(T, sh.r_max, sh.k)) return LORA_ERR_UNSUPPORTED;
-        return from_cuda(lora::launch_fused_decode(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws, T,
-                                                   err, s));
+        if (lora::fused_decode_supported(T, sh.r_max, sh.k))
+            return from_cuda(lora::launch_fused_decode(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws,
+                                                       T, err, s));
+        if (!lora::fused_tc_supported(T, sh)) return LORA_ERR_UNSUPPORTED;
+        return from_cuda(lora::launch_fused_tc(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws, T, err,
+                                               s));
+    case LORA_PATH_DECODE_TC:
+        if (!lora::fused_tc_supported(T, sh)) return LORA_ERR_UNSUPPORTED;
+        return from_cuda(lora::launch_fused_tc(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws, T, err,
+                                               s));
     case LORA_PATH_DECODE_SPLIT: {
         float *xa = xa_of(ws, T, sh);
         cudaError_t e = lora::launch_shrink(xb, ldx, sh, dev_table, sorted_ids, seg_offsets, xa, T, err, true, s);

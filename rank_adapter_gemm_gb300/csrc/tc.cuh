@@ -40,15 +40,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the thread for up to `hint_ns` while
+// the phase is incomplete, instead of spinning (the waiting warp then takes no
+// issue slots from the warps that do the work).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns) : "memory");
+    return ok != 0;
+}
+
 // Bounded wait on a phase: false after `limit_ns` or when *abort_flag is set.
-// The timer and the flag are read every 256 polls.
+// Each poll may suspend the thread for up to a microsecond; the timer and the
+// flag are read every 16 polls.
 __device__ inline bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int32_t *abort_flag,
                                  uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        for (int spin = 0; spin < 256; ++spin)
-            if (mbar_try_wait(bar, parity)) return true;
+        for (int spin = 0; spin < 16; ++spin)
+            if (mbar_try_wait_sleep(bar, parity, 1000)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
@@ -197,6 +211,19 @@ __device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t *r) {
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
+}
+
+// Waits for this thread's outstanding tensor-memory loads; names the 32
+// registers they fill so that no use moves above the wait.
+__device__ __forceinline__ void tmem_wait_ld32(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
 }
 
 // Waits for this thread's outstanding tensor-memory loads; names the 64

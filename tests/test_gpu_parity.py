@@ -14,7 +14,7 @@ from _parity import assert_y_close, gpu_apply, oracle_y, untouched_rows
 
 pytestmark = pytest.mark.gpu
 
-DECODE_PATHS = ["decode_split", "decode_fused"]
+DECODE_PATHS = ["decode_split", "decode_fused", "decode_tc"]
 
 
 def _torch():
@@ -209,9 +209,11 @@ def test_apply_ragged(case, path):
             gpu_apply(wl, path=path)
         assert e.value.status == 9
         return
-    if path == "decode_fused" and (wl.r_max > 128 or k % 16 != 0):
+    mma_ok = wl.r_max <= 128 and k % 16 == 0  # warp-MMA fused kernel
+    tc_ok = wl.r_max <= 64                     # tensor-core fused kernel
+    if (path == "decode_fused" and not (mma_ok or tc_ok)) or (path == "decode_tc" and not tc_ok):
         import rank_adapter_gemm_gb300 as L
-        with pytest.raises(L.LoraError) as e:  # the fused kernel takes ranks up to 128 and k % 16 == 0
+        with pytest.raises(L.LoraError) as e:
             gpu_apply(wl, path=path)
         assert e.value.status == 9
         return
@@ -306,18 +308,20 @@ def test_apply_is_deterministic():
         np.testing.assert_array_equal(y, ys[0])
 
 
-def test_fused_repeat_stays_within_tolerance():
-    """The fused path adds split-k partials with fp32 reductions, whose order
+@pytest.mark.parametrize("path", ["decode_fused", "decode_tc"])
+def test_fused_repeat_stays_within_tolerance(path):
+    """The fused kernels add split-k partials with fp32 reductions, whose order
     varies; every repetition must still match the oracle."""
     wl = W.config(2)
-    ys, err, *_ = gpu_apply(wl, repeat=5, path="decode_fused")
+    ys, err, *_ = gpu_apply(wl, repeat=5, path=path)
     assert err == 0
     ref, _ = oracle_y(wl)
     for y in ys:
         assert_y_close(y, ref, "fused repeat")
 
 
-def test_fused_leaves_workspace_clean():
+@pytest.mark.parametrize("path", ["decode_fused", "decode_tc"])
+def test_fused_leaves_workspace_clean(path):
     """Each fused call clears its accumulator rows and counters, so the
     workspace can serve the next call (another projection, other shapes)
     without a clearing launch."""
@@ -338,13 +342,45 @@ def test_fused_leaves_workspace_clean():
     for _ in range(3):
         rp.y.copy_(y0)
         L.lora_apply(rp.x, rp.y, rp.shape, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active, ws.buf,
-                     idx.err, path="decode_fused")
+                     idx.err, path=path)
         torch.cuda.synchronize()
         assert int(idx.err.item()) == 0
-        assert_y_close(to_host_bits(rp.y), ref, "fused")
+        assert_y_close(to_host_bits(rp.y), ref, path)
         buf = ws.buf.cpu().numpy()
         assert not buf[:xa_off].view(np.int32).any(), "counters not reset"
         assert not buf[acc_off:acc_off + xa_floats].any(), "accumulator not cleared"
+
+
+@pytest.mark.parametrize("path", ["decode_fused", "decode_tc"])
+def test_fused_wait_timeout_reports_error_and_device_stays_usable(path):
+    """Counters that can never reach their targets (a poisoned workspace) make the
+    fused kernel's bounded cross-CTA wait give up: the call ends with
+    LORA_ERR_TIMEOUT in the error word instead of hanging, and the next call on a
+    clean workspace is correct."""
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import ResidentProjection, to_host_bits
+    wl = W.config(2)
+    rp = ResidentProjection.from_workload(wl)
+    idx = L.TokenIndex(wl.T, wl.S)
+    idx.build(torch.from_numpy(wl.slot_ids).cuda(), rp.table)
+    ws = L.Workspace(wl.T, rp.shape)
+    y0 = rp.y.clone()
+    xa_off = L.lora_workspace_xa_offset(rp.shape) // 4
+    ws.buf[:xa_off].view(torch.int32).fill_(-(1 << 30))
+    L.lora_apply(rp.x, rp.y, rp.shape, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active, ws.buf,
+                 idx.err, path=path)
+    torch.cuda.synchronize()
+    assert int(idx.err.item()) == 7  # LORA_ERR_TIMEOUT
+    ws.buf.zero_()
+    idx.err.zero_()
+    rp.y.copy_(y0)
+    L.lora_apply(rp.x, rp.y, rp.shape, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active, ws.buf,
+                 idx.err, path=path)
+    torch.cuda.synchronize()
+    assert int(idx.err.item()) == 0
+    ref, _ = oracle_y(wl)
+    assert_y_close(to_host_bits(rp.y), ref, path + " after a timed-out call")
 
 
 # ---------------------------------------------------------------------------
