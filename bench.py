@@ -82,6 +82,27 @@ def algorithmic_flops(slot_ids, ranks, k, widths) -> int:
     return int(sum(2 * int(ranks[s]) * (n * k + d) for s in slot_ids if 0 <= s < S and ranks[s] > 0))
 
 
+def captured_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, or None when
+    the kernel's sources changed since the capture (the counters no longer apply)."""
+    import hashlib
+    here = os.path.dirname(os.path.abspath(__file__))
+    try:
+        with open(os.path.join(here, "profiles", "ncu_traffic.json")) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    m = hashlib.sha256()
+    for name in rec["sources"]:
+        with open(os.path.join(here, "rank_adapter_gemm_gb300", "csrc", name), "rb") as f:
+            m.update(f.read())
+    if m.hexdigest()[:16] != rec["source_sha256_16"]:
+        return None
+    return rec["dram_read_bytes"] + rec["dram_write_bytes"]
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -355,7 +376,8 @@ def run_ours(args):
             "peak": peak_gbs,
             "unit": "GB/s",
             "frac": achieved_gbs / peak_gbs,
-            "traffic": None,
+            "traffic": (captured_traffic("fused_decode_kernel")
+                        if args.config == "decode_qkv" and resolved == "decode_fused" else None),
             "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
             "kernel": "lora_apply (shrink + expand) per projection call",
             "bytes_per_call": sum(per_layer_bytes) / len(layers),
