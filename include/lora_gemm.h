@@ -81,17 +81,18 @@ typedef enum {
                                     split decode kernels */
     LORA_PATH_DECODE_FUSED = 1,  /* one launch: shrink, per-(slot, slice) wait, expand, on warp-level
                                     MMA; needs T <= 2048, r_max <= 128 and k % 16 == 0, else the
-                                    tensor-core fused kernel when it applies (LORA_PATH_DECODE_TC),
+                                    tensor-core decode kernels when they apply (LORA_PATH_DECODE_TC),
                                     else LORA_ERR_UNSUPPORTED */
     LORA_PATH_DECODE_SPLIT = 2,  /* two launches: shrink then expand (programmatic dependent launch) */
     LORA_PATH_PREFILL = 3,       /* two launches: tcgen05/TMEM tensor-core shrink (split-K over a
                                     thread-block cluster) and expand, on 128-token tiles of
                                     one slot's segment; needs r_max <= 64
                                     (else LORA_ERR_UNSUPPORTED) */
-    LORA_PATH_DECODE_TC = 4      /* one launch, tcgen05/TMEM tensor cores: split-K shrink with
-                                    per-(slot, slice) completion counters, then a transposed
-                                    expand; needs T <= 2048, r_max <= 64 and tables that fit in
-                                    shared memory (else LORA_ERR_UNSUPPORTED) */
+    LORA_PATH_DECODE_TC = 4      /* two launches, tcgen05/TMEM tensor cores: a split-K streaming
+                                    shrink adding into an fp32 accumulator, then a transposed
+                                    expand launched as its programmatic dependent; needs
+                                    T <= 2048, r_max <= 64 and tables that fit in shared memory
+                                    (else LORA_ERR_UNSUPPORTED) */
 } lora_path_t;
 
 #define LORA_DECODE_MAX_SEG 256
@@ -195,14 +196,18 @@ lora_status_t lora_build_index(const int32_t *slot_ids, int32_t T, int32_t S, co
 
 /*
  * Workspace size for T tokens of a projection, in order: a control block of
- * per-slot counters; the fp32 shrink output xa[n_slices][T][r_max] (row t =
- * token t); the fused decode kernel's fp32 accumulator (same size); and, when
- * r_max <= 64, the prefill kernels' xa as two bf16 parts hi + lo, each
- * [n_slices][T][RP] in sorted-token order (RP = 16, 32 or 64, the rank padded
- * up).  Regions start on 256-byte boundaries.  The whole buffer must be zero
- * before the first call that uses it (e.g. one cudaMemsetAsync); every call
- * leaves the control block and the accumulator zero again when it returns
- * without LORA_ERR_TIMEOUT.
+ * per-slot counters and a call counter; the fp32 shrink output
+ * xa[n_slices][T][r_max] (row t = token t); the fused decode kernel's fp32
+ * accumulator (same size); and, when r_max <= 64, the prefill kernels' xa as two
+ * bf16 parts hi + lo, each [n_slices][T][RP] in sorted-token order (RP = 16, 32
+ * or 64, the rank padded up), then two more fp32 accumulators the size of xa
+ * that LORA_PATH_DECODE_TC uses in turn (a call adds into one and clears the
+ * other).  Regions start on 256-byte boundaries.  The whole buffer must be zero
+ * before the first call that uses it (e.g. one cudaMemsetAsync), and again after
+ * a call whose error word reads LORA_ERR_TIMEOUT.  Otherwise every call leaves
+ * what the next call of any path needs: the per-slot counters and the fused
+ * accumulator zero, the call counter matching the clear LORA_PATH_DECODE_TC
+ * accumulator.
  */
 lora_status_t lora_workspace_bytes(int32_t T, const lora_shape_t *shape, size_t *bytes);
 

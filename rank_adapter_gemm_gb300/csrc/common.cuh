@@ -57,18 +57,23 @@ __host__ __device__ inline int32_t tc_rank_pad(int32_t r_max) { return r_max <= 
 // (r_max <= 64) the prefill path's xa as bf16 hi and lo parts, [n][T][RP] each
 // in sorted-token order.
 struct WorkspaceLayout {
-    size_t ctrl_bytes, xa_off, acc_off, hi_off, lo_off, bytes;
+    size_t ctrl_bytes, xa_off, acc_off, hi_off, lo_off, acc2_off, acc3_off, bytes;
     __host__ __device__ WorkspaceLayout(int32_t T, int32_t n_slices, int32_t r_max, int32_t S) {
         // two int32 counters per (slot, slice) + a few global words, rounded to 256 B
         ctrl_bytes = (sizeof(int32_t) * (2 * size_t(S) * LORA_MAX_SLICES + 64) + 255) & ~size_t(255);
         const size_t tt = size_t(T > 0 ? T : 0);
         const size_t xa_bytes = sizeof(float) * size_t(n_slices) * tt * size_t(r_max);
-        const size_t hl_bytes = r_max <= 64 ? sizeof(uint16_t) * size_t(n_slices) * tt * size_t(tc_rank_pad(r_max)) : 0;
+        const bool tc = r_max <= 64;  // the tensor-core paths' extra regions
+        const size_t hl_bytes = tc ? sizeof(uint16_t) * size_t(n_slices) * tt * size_t(tc_rank_pad(r_max)) : 0;
         xa_off = ctrl_bytes;
         acc_off = xa_off + ((xa_bytes + 255) & ~size_t(255));
         hi_off = acc_off + ((xa_bytes + 255) & ~size_t(255));
         lo_off = hi_off + ((hl_bytes + 255) & ~size_t(255));
-        bytes = lo_off + hl_bytes;
+        // two more fp32 accumulators, used in turn by the two-kernel decode
+        const size_t acc_tc = tc ? ((xa_bytes + 255) & ~size_t(255)) : 0;
+        acc2_off = lo_off + ((hl_bytes + 255) & ~size_t(255));
+        acc3_off = acc2_off + acc_tc;
+        bytes = acc3_off + acc_tc;
     }
 };
 

@@ -22,8 +22,8 @@ cudaError_t launch_fused_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int
                                 float *ws, int32_t T, int32_t *err, cudaStream_t stream);
 cudaError_t launch_premultiply(uint16_t *w, int64_t n, float scale, cudaStream_t stream);
 bool prefill_supported(int32_t r_max);
-bool fused_tc_supported(int32_t T, const Shape &sh);
-cudaError_t launch_fused_tc(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
+bool decode_tc_supported(int32_t T, const Shape &sh);
+cudaError_t launch_decode_tc(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                             const void *table, const int32_t *sorted_ids, const int32_t *seg, float *ws, int32_t T,
                             int32_t *err, cudaStream_t stream);
 bool fused_decode_supported(int32_t T, int32_t r_max, int32_t k);
@@ -88,7 +88,7 @@ lora_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LOR
 // The fused decode path: the warp-level MMA kernel where it applies (faster
 // today on the decode shapes measured), else the tensor-core (tcgen05) one.
 bool fused_ok(int32_t T, const Shape &sh) {
-    return lora::fused_decode_supported(T, sh.r_max, sh.k) || lora::fused_tc_supported(T, sh);
+    return lora::fused_decode_supported(T, sh.r_max, sh.k) || lora::decode_tc_supported(T, sh);
 }
 
 lora_path_t resolve(lora_path_t path, int32_t T, int32_t max_seg_hint, const Shape &sh, int32_t *launches) {
@@ -98,7 +98,8 @@ lora_path_t resolve(lora_path_t path, int32_t T, int32_t max_seg_hint, const Sha
         else if (fused_ok(T, sh)) path = LORA_PATH_DECODE_FUSED;
         else path = LORA_PATH_DECODE_SPLIT;
     }
-    if (launches != nullptr) *launches = (path == LORA_PATH_DECODE_FUSED || path == LORA_PATH_DECODE_TC) ? 1 : 2;
+    if (launches != nullptr)
+        *launches = (path == LORA_PATH_DECODE_FUSED && lora::fused_decode_supported(T, sh.r_max, sh.k)) ? 1 : 2;
     return path;
 }
 
@@ -286,12 +287,12 @@ lora_status_t lora_apply_ex(const void *x, int64_t ldx, void *y, int64_t ldy, in
         if (lora::fused_decode_supported(T, sh.r_max, sh.k))
             return from_cuda(lora::launch_fused_decode(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws,
                                                        T, err, s));
-        if (!lora::fused_tc_supported(T, sh)) return LORA_ERR_UNSUPPORTED;
-        return from_cuda(lora::launch_fused_tc(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws, T, err,
+        if (!lora::decode_tc_supported(T, sh)) return LORA_ERR_UNSUPPORTED;
+        return from_cuda(lora::launch_decode_tc(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws, T, err,
                                                s));
     case LORA_PATH_DECODE_TC:
-        if (!lora::fused_tc_supported(T, sh)) return LORA_ERR_UNSUPPORTED;
-        return from_cuda(lora::launch_fused_tc(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws, T, err,
+        if (!lora::decode_tc_supported(T, sh)) return LORA_ERR_UNSUPPORTED;
+        return from_cuda(lora::launch_decode_tc(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws, T, err,
                                                s));
     case LORA_PATH_DECODE_SPLIT: {
         float *xa = xa_of(ws, T, sh);

@@ -88,10 +88,11 @@ def test_workspace_bytes(L):
     xa = 3 * 256 * 64 * 4
     hl = 3 * 256 * 64 * 2  # prefill xa as bf16 hi and lo, rank padded to 64
     # control block, the shrink output xa, the fused kernel's accumulator (same
-    # size as xa) and the prefill path's hi/lo parts
-    assert nbytes >= 2 * xa + 2 * hl
-    assert nbytes - 2 * xa - 2 * hl < 4 * (2 * 32 * 4 + 64) + 4 * 256
-    # ranks above 64 have no prefill region
+    # size as xa), the prefill path's hi/lo parts and the two accumulators the
+    # tensor-core decode kernels use in turn
+    assert nbytes >= 4 * xa + 2 * hl
+    assert nbytes - 4 * xa - 2 * hl < 4 * (2 * 32 * 4 + 64) + 6 * 256
+    # ranks above 64 have no tensor-core regions
     big = L.lora_workspace_bytes(256, L.make_shape(32, 128, 4096, [4096]))
     assert 2 * 256 * 128 * 4 <= big < 2 * 256 * 128 * 4 + 4 * (2 * 32 * 4 + 64) + 4 * 256
     with pytest.raises(L.LoraError) as e:

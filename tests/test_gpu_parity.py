@@ -321,10 +321,12 @@ def test_fused_repeat_stays_within_tolerance(path):
 
 
 @pytest.mark.parametrize("path", ["decode_fused", "decode_tc"])
-def test_fused_leaves_workspace_clean(path):
-    """Each fused call clears its accumulator rows and counters, so the
-    workspace can serve the next call (another projection, other shapes)
-    without a clearing launch."""
+def test_decode_leaves_workspace_ready(path):
+    """Each call leaves the workspace ready for the next one without a clearing
+    launch: the fused kernel clears its accumulator rows and counters; the
+    two-kernel tensor-core path adds into one of its two accumulators, clears
+    the other and advances the call counter g (the control word after the 8 S
+    per-slot counters), so accumulator g & 1 is zero after every call."""
     torch = _torch()
     import rank_adapter_gemm_gb300 as L
     from rank_adapter_gemm_gb300.resident import ResidentProjection, to_host_bits
@@ -335,11 +337,15 @@ def test_fused_leaves_workspace_clean(path):
     ws = L.Workspace(wl.T, rp.shape)
     ref, _ = oracle_y(wl)
     y0 = rp.y.clone()
-    n, T, r_max = wl.modules[0].n_slices, wl.T, wl.r_max
+    n, T, r_max, S = wl.modules[0].n_slices, wl.T, wl.r_max, wl.S
     xa_floats = n * T * r_max
+    region = (xa_floats + 63) // 64 * 64  # regions start on 256-byte boundaries
+    hl_region = (n * T * 64 * 2 // 4 + 63) // 64 * 64  # bf16 hi or lo, rank padded to 64
     xa_off = L.lora_workspace_xa_offset(rp.shape) // 4
-    acc_off = xa_off + (xa_floats + 63) // 64 * 64  # regions start on 256-byte boundaries
-    for _ in range(3):
+    acc_off = xa_off + region
+    acc2_off = acc_off + region + 2 * hl_region
+    gen_word = 2 * 4 * S
+    for call in range(1, 4):
         rp.y.copy_(y0)
         L.lora_apply(rp.x, rp.y, rp.shape, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active, ws.buf,
                      idx.err, path=path)
@@ -347,11 +353,17 @@ def test_fused_leaves_workspace_clean(path):
         assert int(idx.err.item()) == 0
         assert_y_close(to_host_bits(rp.y), ref, path)
         buf = ws.buf.cpu().numpy()
-        assert not buf[:xa_off].view(np.int32).any(), "counters not reset"
-        assert not buf[acc_off:acc_off + xa_floats].any(), "accumulator not cleared"
+        ctrl = buf[:xa_off].view(np.int32).copy()
+        assert not buf[acc_off:acc_off + xa_floats].any(), "fused accumulator not cleared"
+        if path == "decode_tc":
+            assert ctrl[gen_word] == call, "call counter not advanced"
+            ctrl[gen_word] = 0
+            nxt = acc2_off + (call & 1) * region
+            assert not buf[nxt:nxt + xa_floats].any(), "next accumulator not cleared"
+        assert not ctrl.any(), "counters not reset"
 
 
-@pytest.mark.parametrize("path", ["decode_fused", "decode_tc"])
+@pytest.mark.parametrize("path", ["decode_fused"])
 def test_fused_wait_timeout_reports_error_and_device_stays_usable(path):
     """Counters that can never reach their targets (a poisoned workspace) make the
     fused kernel's bounded cross-CTA wait give up: the call ends with
