@@ -88,11 +88,17 @@ typedef enum {
                                     thread-block cluster) and expand, on 128-token tiles of
                                     one slot's segment; needs r_max <= 64
                                     (else LORA_ERR_UNSUPPORTED) */
-    LORA_PATH_DECODE_TC = 4      /* two launches, tcgen05/TMEM tensor cores: a split-K streaming
+    LORA_PATH_DECODE_TC = 4,     /* two launches, tcgen05/TMEM tensor cores: a split-K streaming
                                     shrink adding into an fp32 accumulator, then a transposed
                                     expand launched as its programmatic dependent; needs
                                     T <= 2048, r_max <= 64 and tables that fit in shared memory
                                     (else LORA_ERR_UNSUPPORTED) */
+    LORA_PATH_DECODE_STREAM = 5  /* two launches on warp-level MMA fed by bulk copies: a split-K
+                                    streaming shrink adding into an fp32 accumulator, then an
+                                    expand launched as its programmatic dependent, one CTA of each
+                                    sharing every SM; needs T <= 2048, r_max <= 128, k % 16 == 0
+                                    and tables that fit in shared memory (else
+                                    LORA_ERR_UNSUPPORTED) */
 } lora_path_t;
 
 #define LORA_DECODE_MAX_SEG 256
@@ -200,14 +206,15 @@ lora_status_t lora_build_index(const int32_t *slot_ids, int32_t T, int32_t S, co
  * xa[n_slices][T][r_max] (row t = token t); the fused decode kernel's fp32
  * accumulator (same size); and, when r_max <= 64, the prefill kernels' xa as two
  * bf16 parts hi + lo, each [n_slices][T][RP] in sorted-token order (RP = 16, 32
- * or 64, the rank padded up), then two more fp32 accumulators the size of xa
- * that LORA_PATH_DECODE_TC uses in turn (a call adds into one and clears the
+ * or 64, the rank padded up); then, when r_max <= 128, two more fp32
+ * accumulators the size of xa that LORA_PATH_DECODE_TC and
+ * LORA_PATH_DECODE_STREAM use in turn (a call adds into one and clears the
  * other).  Regions start on 256-byte boundaries.  The whole buffer must be zero
  * before the first call that uses it (e.g. one cudaMemsetAsync), and again after
  * a call whose error word reads LORA_ERR_TIMEOUT.  Otherwise every call leaves
  * what the next call of any path needs: the per-slot counters and the fused
- * accumulator zero, the call counter matching the clear LORA_PATH_DECODE_TC
- * accumulator.
+ * accumulator zero, the call counter matching the clear accumulator of the
+ * two-kernel decode paths.
  */
 lora_status_t lora_workspace_bytes(int32_t T, const lora_shape_t *shape, size_t *bytes);
 

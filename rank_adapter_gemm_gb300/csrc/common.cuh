@@ -69,8 +69,8 @@ struct WorkspaceLayout {
         acc_off = xa_off + ((xa_bytes + 255) & ~size_t(255));
         hi_off = acc_off + ((xa_bytes + 255) & ~size_t(255));
         lo_off = hi_off + ((hl_bytes + 255) & ~size_t(255));
-        // two more fp32 accumulators, used in turn by the two-kernel decode
-        const size_t acc_tc = tc ? ((xa_bytes + 255) & ~size_t(255)) : 0;
+        // two more fp32 accumulators, used in turn by the two-kernel decode paths
+        const size_t acc_tc = r_max <= 128 ? ((xa_bytes + 255) & ~size_t(255)) : 0;
         acc2_off = lo_off + ((hl_bytes + 255) & ~size_t(255));
         acc3_off = acc2_off + acc_tc;
         bytes = acc3_off + acc_tc;

@@ -23,6 +23,10 @@ cudaError_t launch_fused_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int
 cudaError_t launch_premultiply(uint16_t *w, int64_t n, float scale, cudaStream_t stream);
 bool prefill_supported(int32_t r_max);
 bool decode_tc_supported(int32_t T, const Shape &sh);
+bool decode_stream_supported(int32_t T, const Shape &sh);
+cudaError_t launch_decode_stream(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
+                                 const void *table, const int32_t *sorted_ids, const int32_t *seg, float *ws,
+                                 int32_t T, int32_t *err, cudaStream_t stream);
 cudaError_t launch_decode_tc(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                             const void *table, const int32_t *sorted_ids, const int32_t *seg, float *ws, int32_t T,
                             int32_t *err, cudaStream_t stream);
@@ -294,6 +298,10 @@ lora_status_t lora_apply_ex(const void *x, int64_t ldx, void *y, int64_t ldy, in
         if (!lora::decode_tc_supported(T, sh)) return LORA_ERR_UNSUPPORTED;
         return from_cuda(lora::launch_decode_tc(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws, T, err,
                                                s));
+    case LORA_PATH_DECODE_STREAM:
+        if (!lora::decode_stream_supported(T, sh)) return LORA_ERR_UNSUPPORTED;
+        return from_cuda(lora::launch_decode_stream(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws, T,
+                                                    err, s));
     case LORA_PATH_DECODE_SPLIT: {
         float *xa = xa_of(ws, T, sh);
         cudaError_t e = lora::launch_shrink(xb, ldx, sh, dev_table, sorted_ids, seg_offsets, xa, T, err, true, s);

@@ -92,9 +92,12 @@ def test_workspace_bytes(L):
     # tensor-core decode kernels use in turn
     assert nbytes >= 4 * xa + 2 * hl
     assert nbytes - 4 * xa - 2 * hl < 4 * (2 * 32 * 4 + 64) + 6 * 256
-    # ranks above 64 have no tensor-core regions
+    # ranks above 64 have no bf16 hi/lo regions; up to 128 they keep the two
+    # accumulators of the two-kernel decode paths
     big = L.lora_workspace_bytes(256, L.make_shape(32, 128, 4096, [4096]))
-    assert 2 * 256 * 128 * 4 <= big < 2 * 256 * 128 * 4 + 4 * (2 * 32 * 4 + 64) + 4 * 256
+    assert 4 * 256 * 128 * 4 <= big < 4 * 256 * 128 * 4 + 4 * (2 * 32 * 4 + 64) + 6 * 256
+    huge = L.lora_workspace_bytes(256, L.make_shape(32, 256, 4096, [4096]))
+    assert 2 * 256 * 256 * 4 <= huge < 2 * 256 * 256 * 4 + 4 * (2 * 32 * 4 + 64) + 6 * 256
     with pytest.raises(L.LoraError) as e:
         L.lora_workspace_bytes(10, L.make_shape(0, 64, 4096, [4096]))
     assert e.value.status == 1

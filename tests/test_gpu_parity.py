@@ -14,7 +14,7 @@ from _parity import assert_y_close, gpu_apply, oracle_y, untouched_rows
 
 pytestmark = pytest.mark.gpu
 
-DECODE_PATHS = ["decode_split", "decode_fused", "decode_tc"]
+DECODE_PATHS = ["decode_split", "decode_fused", "decode_tc", "decode_stream"]
 
 
 def _torch():
@@ -209,9 +209,10 @@ def test_apply_ragged(case, path):
             gpu_apply(wl, path=path)
         assert e.value.status == 9
         return
-    mma_ok = wl.r_max <= 128 and k % 16 == 0  # warp-MMA fused kernel
-    tc_ok = wl.r_max <= 64                     # tensor-core fused kernel
-    if (path == "decode_fused" and not (mma_ok or tc_ok)) or (path == "decode_tc" and not tc_ok):
+    mma_ok = wl.r_max <= 128 and k % 16 == 0  # warp-MMA kernels (fused and streaming)
+    tc_ok = wl.r_max <= 64                     # tcgen05 decode kernels
+    if ((path == "decode_fused" and not (mma_ok or tc_ok)) or (path == "decode_tc" and not tc_ok)
+            or (path == "decode_stream" and not mma_ok)):
         import rank_adapter_gemm_gb300 as L
         with pytest.raises(L.LoraError) as e:
             gpu_apply(wl, path=path)
@@ -308,7 +309,7 @@ def test_apply_is_deterministic():
         np.testing.assert_array_equal(y, ys[0])
 
 
-@pytest.mark.parametrize("path", ["decode_fused", "decode_tc"])
+@pytest.mark.parametrize("path", ["decode_fused", "decode_tc", "decode_stream"])
 def test_fused_repeat_stays_within_tolerance(path):
     """The fused kernels add split-k partials with fp32 reductions, whose order
     varies; every repetition must still match the oracle."""
@@ -320,12 +321,12 @@ def test_fused_repeat_stays_within_tolerance(path):
         assert_y_close(y, ref, "fused repeat")
 
 
-@pytest.mark.parametrize("path", ["decode_fused", "decode_tc"])
+@pytest.mark.parametrize("path", ["decode_fused", "decode_tc", "decode_stream"])
 def test_decode_leaves_workspace_ready(path):
     """Each call leaves the workspace ready for the next one without a clearing
     launch: the fused kernel clears its accumulator rows and counters; the
-    two-kernel tensor-core path adds into one of its two accumulators, clears
-    the other and advances the call counter g (the control word after the 8 S
+    two-kernel paths add into one of their two accumulators, clear the other
+    and advance the call counter g (the control word after the 8 S
     per-slot counters), so accumulator g & 1 is zero after every call."""
     torch = _torch()
     import rank_adapter_gemm_gb300 as L
@@ -355,7 +356,7 @@ def test_decode_leaves_workspace_ready(path):
         buf = ws.buf.cpu().numpy()
         ctrl = buf[:xa_off].view(np.int32).copy()
         assert not buf[acc_off:acc_off + xa_floats].any(), "fused accumulator not cleared"
-        if path == "decode_tc":
+        if path in ("decode_tc", "decode_stream"):
             assert ctrl[gen_word] == call, "call counter not advanced"
             ctrl[gen_word] = 0
             nxt = acc2_off + (call & 1) * region
