@@ -54,7 +54,7 @@ def parse_args(argv=None):
     p.add_argument("--config", default="decode_qkv", choices=list(CONFIG_INDEX))
     p.add_argument("--layers", type=int, default=32)
     p.add_argument("--requests", type=int, default=16, help="prefill_mlp only: requests in the batch")
-    p.add_argument("--path", default="auto", choices=["auto", "decode_fused", "decode_split", "prefill", "decode_tc", "decode_stream"])
+    p.add_argument("--path", default="auto", choices=["auto", "decode_fused", "decode_split", "prefill", "decode_tc", "decode_stream", "decode_direct"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-baseline sample")

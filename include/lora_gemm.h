@@ -93,12 +93,18 @@ typedef enum {
                                     expand launched as its programmatic dependent; needs
                                     T <= 2048, r_max <= 64 and tables that fit in shared memory
                                     (else LORA_ERR_UNSUPPORTED) */
-    LORA_PATH_DECODE_STREAM = 5  /* two launches on warp-level MMA fed by bulk copies: a split-K
+    LORA_PATH_DECODE_STREAM = 5, /* two launches on warp-level MMA fed by bulk copies: a split-K
                                     streaming shrink adding into an fp32 accumulator, then an
                                     expand launched as its programmatic dependent, one CTA of each
                                     sharing every SM; needs T <= 2048, r_max <= 128, k % 16 == 0
                                     and tables that fit in shared memory (else
                                     LORA_ERR_UNSUPPORTED) */
+    LORA_PATH_DECODE_DIRECT = 6  /* two launches on warp-level MMA in which every warp streams its
+                                    own byte-balanced share through a private cp.async ring (no
+                                    barriers between warps): a split-K shrink adding into an fp32
+                                    accumulator, then an expand launched as its programmatic
+                                    dependent; needs T <= 2048, r_max <= 64, S <= 512 and
+                                    S * n_slices <= 512 (else LORA_ERR_UNSUPPORTED) */
 } lora_path_t;
 
 #define LORA_DECODE_MAX_SEG 256

@@ -1,0 +1,895 @@
+// Decode-size LoRA branch as two kernels in which every warp is its own
+// streaming engine (LORA_PATH_DECODE_DIRECT).
+//
+// At decode the branch reads each active adapter's A and B once while x and y
+// are small (llama.cpp LoRA adapter page, section "为什么低秩增量可以「后加」":
+// the low-rank branch is bandwidth-bound at decode), so the kernels are built
+// to keep many bytes in flight on every SM with as little per-byte work as
+// possible:
+//
+//   * Lane-private staging.  Each warp owns a ring of stages in shared memory.
+//     A stage is a list of 512-byte chunks; lane l copies 16 bytes into bytes
+//     [16 l, 16 l + 16) of a chunk (cp.async, zero-filled where a row or column
+//     is out of range) and later reads back exactly those bytes as one of its
+//     MMA fragments.  No lane ever reads another lane's bytes, so a stage needs
+//     no barrier, no mbarrier and no ldmatrix: cp.async.wait_group is the only
+//     synchronisation, and the warps of a CTA never wait for one another.
+//   * Fragment order instead of data order.  mma.m16n8k16 sums over k, so any
+//     fixed permutation of k that both operands share is allowed: lane 4g + q
+//     reads the 16 contiguous bytes at columns 8q..8q+7 of a 32-column block of
+//     its row and feeds columns 8q..8q+3 to the first k16 MMA, 8q+4..8q+7 to the
+//     second.  Rows are permuted the same way, so that a lane's accumulators
+//     cover 2 or 4 adjacent ranks (shrink: one red.v2/red.v4 per token) or 8
+//     adjacent output columns (expand: one 16-byte load and store of y).
+//   * Byte-balanced split.  The work is a list of units (shrink: slot, slice,
+//     32-rank block, 32-column blocks of k; expand: slot, slice, 64 output
+//     columns, 16 tokens) with a weight of about the HBM bytes they move; warp
+//     w of W takes the pieces whose weight offset lies in its W-th of the
+//     total, so big slots are split over k across many warps (split-K,
+//     TensorRT-LLM LoRA serving page, "路径二:split-K 调优") and every warp of
+//     the GPU moves about the same bytes.
+//   * Shrink partial sums go to an fp32 buffer with vector reductions
+//     (red.global.add.v4.f32).  The expand is launched as a programmatic
+//     dependent of the shrink: it builds its tables and copies its first
+//     stages of B and y (which the shrink does not write) before
+//     griddepcontrol.wait, and reads the sums only after it.  x·A enters the
+//     expand MMA as bf16 hi + lo parts (about 2^-17 relative), and
+//     y = bf16(y + s · xa B^T) is rounded once.
+//   * The workspace holds two sum buffers and a call counter g: call g adds
+//     into buffer g & 1 and clears buffer (g + 1) & 1, which the previous call
+//     used; the last expand CTA to finish advances g.  No CTA waits on another.
+//
+// Limits (the host routes other cases elsewhere): T <= 2048, r_max <= 64,
+// S * n_slices <= 512, S <= 512.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace lora {
+
+namespace {
+
+constexpr int kSWarps = 16;          // shrink: 4 warps per SM sub-partition
+constexpr int kEWarps = 8;           // expand
+constexpr int kChunk = 512;          // 16 bytes per lane
+constexpr int kSChunks = 12;         // shrink stage: 12 chunks (6 KB)
+constexpr int kSStages = 2;          // shrink ring depth per warp
+constexpr int kEChunks = 20;         // expand stage: B (<= 16 chunks) + y (<= 4 chunks)
+constexpr int kEStages = 2;          // expand ring depth per warp
+constexpr int kMaxTokens = 2048;
+constexpr int kMaxRank = 64;
+constexpr int kMaxSlots = 512;
+constexpr int kMaxPtrs = 512;        // S * n_slices
+constexpr int kRB = 32;              // shrink rank block
+constexpr int kTGs = 32;             // shrink token group
+constexpr int kCB = 64;              // expand output columns per unit
+constexpr int kTGe = 16;             // expand token group
+
+struct DArgs {
+    const uint16_t *x;
+    int64_t ldx;
+    uint16_t *y;
+    int64_t ldy;
+    const int32_t *sorted_ids;
+    const int32_t *seg;
+    const int32_t *active;
+    float *acc0, *acc1;  // [n][T][r_max] fp32 sums: buffer g & 1 this call
+    int32_t *gen;        // call counter g
+    int32_t *exits;      // expand CTAs that finished this call
+    int32_t *err;
+    int32_t T;
+};
+
+__host__ __device__ inline int32_t cdiv(int32_t a, int32_t b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t sa(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+// 16 bytes global -> shared through L1 (re-read weights hit there), or 16 zero
+// bytes when !valid (src is not read then).
+__device__ __forceinline__ void cp16_ca(uint32_t dst, const void *src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+// Same through L2 only (activations and y).
+__device__ __forceinline__ void cp16_cg(uint32_t dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+
+__device__ __forceinline__ uint4 lds16(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void red_v4(float *p, float a, float b, float c, float d) {
+    asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1,%2,%3,%4};" :: "l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void red_v2(float *p, float a, float b) {
+    asm volatile("red.relaxed.gpu.global.add.v2.f32 [%0], {%1,%2};" :: "l"(p), "f"(a), "f"(b) : "memory");
+}
+
+__device__ __forceinline__ float4 ldg_f4(const float *p) {
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+
+// ---------------------------------------------------------------------------
+// Tables: one copy per CTA in shared memory, built by the prologue.
+// ---------------------------------------------------------------------------
+struct Tabs {
+    int32_t *misc;     // [0] active count NA, [1] call counter, [3..5] table header
+    int32_t *soff;     // [LORA_MAX_SLICES + 1] slice offsets
+    int32_t *scb;      // [LORA_MAX_SLICES + 1] exclusive prefix of 64-column blocks per slice
+    int32_t *tok;      // [T] sorted token ids (-1 where invalid)
+    int32_t *act;      // [S + 1] active list as loaded
+    int32_t *seg;      // [S + 2]
+    int32_t *rank;     // [S]
+    float *scale;      // [S]
+    uint64_t *aptr;    // [S * n]
+    uint64_t *bptr;    // [S * n]
+    int32_t *a_slot;   // [S] per active slot: slot id
+    int32_t *a_p0;     // [S] first sorted position
+    int32_t *a_len;    // [S] tokens
+    int32_t *a_r;      // [S] rank (0: no work)
+    long long *a_pre;  // [S + 1] exclusive prefix of slot weights
+};
+
+constexpr int kMiscInts = 8 + 2 * (LORA_MAX_SLICES + 1) + 2;
+
+__host__ __device__ inline size_t tabs_bytes(int32_t S, int32_t n, int32_t T) {
+    size_t b = 4 * (kMiscInts + size_t(T) + (S + 1) + (S + 2) + 2 * size_t(S));
+    b = (b + 15) & ~size_t(15);
+    b += 16 * size_t(S) * n;                    // aptr, bptr
+    b += 4 * 4 * size_t(S);                     // a_slot, a_p0, a_len, a_r
+    b = (b + 15) & ~size_t(15);
+    b += 8 * (size_t(S) + 1);                   // a_pre
+    return (b + 15) & ~size_t(15);
+}
+
+__device__ Tabs carve(unsigned char *base, int32_t S, int32_t n, int32_t T) {
+    Tabs t;
+    int32_t *p = reinterpret_cast<int32_t *>(base);
+    t.misc = p;
+    t.soff = p + 8;
+    t.scb = t.soff + LORA_MAX_SLICES + 1;
+    t.tok = p + kMiscInts;
+    t.act = t.tok + T;
+    t.seg = t.act + S + 1;
+    t.rank = t.seg + S + 2;
+    t.scale = reinterpret_cast<float *>(t.rank + S);
+    size_t off = 4 * (kMiscInts + size_t(T) + (S + 1) + (S + 2) + 2 * size_t(S));
+    off = (off + 15) & ~size_t(15);
+    t.aptr = reinterpret_cast<uint64_t *>(base + off);
+    t.bptr = t.aptr + size_t(S) * n;
+    t.a_slot = reinterpret_cast<int32_t *>(t.bptr + size_t(S) * n);
+    t.a_p0 = t.a_slot + S;
+    t.a_len = t.a_p0 + S;
+    t.a_r = t.a_len + S;
+    off += 16 * size_t(S) * n + 16 * size_t(S);
+    off = (off + 15) & ~size_t(15);
+    t.a_pre = reinterpret_cast<long long *>(base + off);
+    return t;
+}
+
+// ---------------------------------------------------------------------------
+// Unit weights (about the HBM bytes a unit moves; re-reads that hit L2 and
+// activation rows count a quarter).
+// ---------------------------------------------------------------------------
+// Shrink: rank block rb of a slot of rank r with L tokens, per 32-column block
+// of k: the block's A rows (padded to 16 or 32), re-read once per extra token
+// group of 32, plus the x rows.
+__device__ __forceinline__ int32_t s_mt(int32_t r, int32_t rb) { return r - kRB * rb > 16 ? 2 : 1; }
+__device__ __forceinline__ int32_t s_block_w(int32_t r, int32_t L, int32_t rb) {
+    const int32_t rp = 16 * s_mt(r, rb), ng = cdiv(L, kTGs);
+    return 64 * rp + 16 * (rp * (ng - 1) + L);
+}
+__device__ __forceinline__ long long s_slot_w(int32_t r, int32_t L, int32_t n, int32_t nkb) {
+    long long w = 0;
+    for (int32_t rb = 0; kRB * rb < r; ++rb) w += s_block_w(r, L, rb);
+    return w * nkb * n;
+}
+// Expand: token group tg (16 tokens) of 64 output columns: the B rows (64 x
+// r, padded to 32 ranks; L2 re-reads after the first group), y read and
+// written, the sums read from L2.
+__device__ __forceinline__ int32_t e_unit_w(int32_t r, int32_t L, int32_t tg) {
+    const int32_t rpad = 32 * cdiv(r, 32), Lg = min(kTGe, L - kTGe * tg);
+    return (tg == 0 ? 128 : 32) * rpad + (256 + r) * Lg;
+}
+__device__ __forceinline__ int32_t e_cb_w(int32_t r, int32_t L) {
+    const int32_t rpad = 32 * cdiv(r, 32), ng = cdiv(L, kTGe);
+    return 128 * rpad + 32 * rpad * (ng - 1) + (256 + r) * L;
+}
+
+__device__ __forceinline__ void cp4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(sa(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp8(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" :: "r"(sa(dst)), "l"(src) : "memory");
+}
+
+// Prologue: every table load of the CTA in flight at once, then the checks,
+// the per-active-slot records and their weight prefix.  Ends with a barrier.
+template <bool kExpand>
+__device__ void build_tabs(const DArgs &a, const Shape &sh, const void *table, const Tabs &t) {
+    const int32_t S = sh.S, n = sh.n, T = a.T;
+    const int tid = threadIdx.x, nthr = blockDim.x, warp = tid >> 5, lane = tid & 31;
+    const TableView tab(table, S, n);
+    const int32_t *hdr = static_cast<const int32_t *>(table);
+    if (tid == 0) {
+        cp4(t.misc + 3, hdr);
+        cp4(t.misc + 4, hdr + 1);
+        cp4(t.misc + 5, hdr + 2);
+        cp4(t.misc + 1, a.gen);
+        int32_t c = 0, o = 0;
+#pragma unroll
+        for (int i = 0; i <= LORA_MAX_SLICES; ++i) {
+            if (i <= sh.n) o = sh.off[i];  // compile-time index: the shape stays in parameter space
+            t.soff[i] = o;
+            t.scb[i] = c;
+            if (i < LORA_MAX_SLICES && i < sh.n) c += cdiv(sh.off[i + 1] - o, kCB);
+        }
+    }
+    for (int i = tid; i < T; i += nthr) cp4(t.tok + i, a.sorted_ids + i);
+    for (int s = tid; s <= S; s += nthr) cp4(t.act + s, a.active + s);
+    for (int s = tid; s < S + 2; s += nthr) cp4(t.seg + s, a.seg + s);
+    for (int s = tid; s < S; s += nthr) {
+        cp4(t.rank + s, tab.rank + s);
+        cp4(t.scale + s, tab.scale + s);
+    }
+    for (int e = tid; e < S * n; e += nthr) {
+        cp8(t.aptr + e, tab.a_ptr + e);
+        cp8(t.bptr + e, tab.b_ptr + e);
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    for (int i = tid; i < T; i += nthr) {
+        const int32_t v = t.tok[i];
+        if (v < 0 || v >= T) {
+            if (blockIdx.x == 0) report_error(a.err, LORA_ERR_INVALID_ARG);
+            t.tok[i] = -1;
+        }
+    }
+    const bool ok = t.misc[3] == kTableMagic && t.misc[4] == S && t.misc[5] == n && t.seg[S + 1] == T;
+    if (!ok && tid == 0 && blockIdx.x == 0) report_error(a.err, LORA_ERR_INVALID_ARG);
+    const int32_t NA = ok ? min(max(t.act[0], 0), S) : 0;
+    const int32_t nkb = cdiv(sh.k, 32), ncb = t.scb[LORA_MAX_SLICES];
+    for (int j = tid; j < NA; j += nthr) {
+        const int32_t s = t.act[1 + j];
+        int32_t r = 0, L = 0, p0 = 0;
+        if (s >= 0 && s < S) {
+            p0 = t.seg[s];
+            L = t.seg[s + 1] - p0;
+            r = t.rank[s];
+            if (p0 < 0 || L < 0 || p0 + L > T) {
+                if (blockIdx.x == 0) report_error(a.err, LORA_ERR_INVALID_ARG);
+                r = 0;
+            }
+            if (r > sh.r_max || r > kMaxRank) {
+                if (blockIdx.x == 0) report_error(a.err, LORA_ERR_RANK);
+                r = 0;
+            }
+        } else if (blockIdx.x == 0) {
+            report_error(a.err, LORA_ERR_INVALID_ARG);
+        }
+        if (r <= 0 || L <= 0) r = L = 0;
+        t.a_slot[j] = max(s, 0);
+        t.a_p0[j] = p0;
+        t.a_len[j] = L;
+        t.a_r[j] = r;
+        t.a_pre[j] = r == 0 ? 0 : (kExpand ? static_cast<long long>(ncb) * e_cb_w(r, L) : s_slot_w(r, L, n, nkb));
+    }
+    __syncthreads();
+    if (warp == 0) {
+        long long carry = 0;
+        for (int32_t base = 0; base < NA; base += 32) {
+            const int32_t j = base + lane;
+            const long long v = j < NA ? t.a_pre[j] : 0;
+            long long incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const long long w = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += w;
+            }
+            if (j < NA) t.a_pre[j] = carry + incl - v;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            t.a_pre[NA] = carry;
+            t.misc[0] = NA;
+        }
+    }
+    __syncthreads();
+}
+
+// Last active slot j in [0, NA) with a_pre[j] <= v.
+__device__ __forceinline__ int32_t find_active(const long long *pre, int32_t NA, long long v) {
+    int32_t lo = 0, hi = NA;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi) >> 1;
+        if (pre[mid] <= v) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo - 1;
+}
+
+// This warp's share [R0, R1) of the total weight W.
+template <int kWarpsPerCta>
+__device__ __forceinline__ void warp_share(long long W, long long &R0, long long &R1) {
+    const long long NW = static_cast<long long>(gridDim.x) * kWarpsPerCta;
+    const long long gw = static_cast<long long>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+    R0 = (W * gw + NW - 1) / NW;
+    R1 = (W * (gw + 1) + NW - 1) / NW;
+}
+
+// ---------------------------------------------------------------------------
+// Shrink: xa[i][p][j] += sum over a block range of k of x[tok(p), c] A_{s,i}[j, c]
+// ---------------------------------------------------------------------------
+// A segment: the warp's blocks [bs, be) of unit (active slot ja, slice i,
+// rank block rb) for token group g.  The warp walks its blocks of a unit once
+// per token group; a segment's sums stay in registers and are reduced into the
+// buffer after its last block.  Two walkers follow the same segments: the
+// copy walker runs one stage ahead of the compute walker.
+struct SGen {
+    int32_t ja, i, rb, g, bs, be, w;
+    long long start, R1;
+    bool live;
+};
+
+__device__ __forceinline__ int32_t s_nt8(int32_t L, int32_t g) { return min(4, cdiv(L - kTGs * g, 8)); }
+
+// Blocks of the current unit whose weight start is below R1.
+__device__ __forceinline__ void s_range(SGen &c, int32_t nkb) {
+    const long long lim = c.R1 - c.start;
+    c.be = lim <= 0 ? 0 : static_cast<int32_t>(min(static_cast<long long>(nkb), (lim + c.w - 1) / c.w));
+    c.g = 0;
+    if (c.be <= c.bs) c.live = false;
+}
+
+__device__ __forceinline__ void s_next_unit(SGen &c, const Tabs &t, int32_t n, int32_t nkb) {
+    c.start += static_cast<long long>(nkb) * c.w;
+    if (kRB * (++c.rb) >= t.a_r[c.ja]) {
+        c.rb = 0;
+        if (++c.i == n) {
+            c.i = 0;
+            const int32_t NA = t.misc[0];
+            do {
+                ++c.ja;
+            } while (c.ja < NA && t.a_r[c.ja] == 0);
+            if (c.ja >= NA) {
+                c.live = false;
+                return;
+            }
+        }
+    }
+    c.w = s_block_w(t.a_r[c.ja], t.a_len[c.ja], c.rb);
+    c.bs = 0;
+    s_range(c, nkb);
+}
+
+__device__ __forceinline__ void s_next_seg(SGen &c, const Tabs &t, int32_t n, int32_t nkb) {
+    if (kTGs * (++c.g) >= t.a_len[c.ja]) s_next_unit(c, t, n, nkb);
+}
+
+__device__ __forceinline__ void s_first(SGen &c, const Tabs &t, int32_t n, int32_t nkb) {
+    const int32_t NA = t.misc[0];
+    long long R0;
+    warp_share<kSWarps>(t.a_pre[NA], R0, c.R1);
+    c.live = R0 < c.R1;
+    if (!c.live) return;
+    c.ja = find_active(t.a_pre, NA, R0);
+    const int32_t r = t.a_r[c.ja], L = t.a_len[c.ja];
+    long long o = R0 - t.a_pre[c.ja];
+    const long long wslice = s_slot_w(r, L, 1, nkb);
+    c.i = static_cast<int32_t>(o / wslice);
+    o -= c.i * wslice;
+    c.start = t.a_pre[c.ja] + c.i * wslice;
+    c.rb = 0;
+    while (true) {
+        const long long wu = static_cast<long long>(nkb) * s_block_w(r, L, c.rb);
+        if (o < wu) break;
+        o -= wu;
+        c.start += wu;
+        ++c.rb;
+    }
+    c.w = s_block_w(r, L, c.rb);
+    c.bs = static_cast<int32_t>((o + c.w - 1) / c.w);
+    if (c.bs >= nkb) {
+        s_next_unit(c, t, n, nkb);  // the share starts after this unit's last block start
+        return;
+    }
+    s_range(c, nkb);
+}
+
+// Copy walker: per-segment lane pointers at block 0, so a block costs one
+// 64-bit add per 16-byte copy.  Chunk c < 2 MT of a block is A row
+// 2 MT gq + c of the rank block; chunk 2 MT + nt is the x row of token
+// 32 g + 8 nt + gq; lane 4 gq + q copies columns 8q..8q+7 of each.
+struct SCopy {
+    SGen gen;
+    int32_t b, kb, cpb, mt, nt;
+    uint32_t vm;
+    const unsigned char *pa[4], *px[4];
+};
+
+__device__ __forceinline__ void s_copy_seg(SCopy &s, const Tabs &t, const Shape &sh, const DArgs &a, int lane) {
+    const int32_t gq = lane >> 2, q = lane & 3;
+    const int32_t ja = s.gen.ja, r = t.a_r[ja], L = t.a_len[ja], p0 = t.a_p0[ja];
+    s.mt = s_mt(r, s.gen.rb);
+    s.nt = s_nt8(L, s.gen.g);
+    s.cpb = 2 * s.mt + s.nt;
+    s.kb = kSChunks / s.cpb;
+    s.b = s.gen.bs;
+    const int32_t rows = min(kRB, r - kRB * s.gen.rb);
+    const unsigned char *A = reinterpret_cast<const unsigned char *>(t.aptr[t.a_slot[ja] * sh.n + s.gen.i]) +
+                             2 * (static_cast<int64_t>(kRB * s.gen.rb) * sh.k + 8 * q);
+    uint32_t vm = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int32_t row = 2 * s.mt * gq + c;
+        const bool v = c < 2 * s.mt && row < rows;
+        s.pa[c] = A + (v ? 2 * static_cast<int64_t>(row) * sh.k : 0);
+        vm |= v ? (1u << c) : 0u;
+    }
+    const unsigned char *X = reinterpret_cast<const unsigned char *>(a.x) + 16 * q;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+        const int32_t jt = kTGs * s.gen.g + 8 * nt + gq;
+        const int32_t tok = (nt < s.nt && jt < L) ? t.tok[p0 + jt] : -1;
+        s.px[nt] = X + (tok >= 0 ? 2 * static_cast<int64_t>(tok) * a.ldx : 0);
+        vm |= tok >= 0 ? (1u << (4 + nt)) : 0u;
+    }
+    s.vm = vm;
+}
+
+// Issue the next stage of copies into `slot` (this lane's bytes) and commit
+// a group (an empty one once the walk is over).
+__device__ __forceinline__ void s_copy_stage(SCopy &s, uint32_t slot, int32_t kq, const Tabs &t, const Shape &sh,
+                                             const DArgs &a, int lane, int32_t nkb) {
+    if (s.gen.live) {
+        const int32_t nb = min(s.kb, s.gen.be - s.b);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j < nb) {
+                const int32_t blk = s.b + j;
+                const bool cv = 32 * blk < kq;
+                const uint32_t dst = slot + j * s.cpb * kChunk;
+                const int64_t off = 64 * static_cast<int64_t>(blk);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (c < 2 * s.mt) cp16_ca(dst + c * kChunk, s.pa[c] + off, cv && ((s.vm >> c) & 1u));
+                const uint32_t dx = dst + 2 * s.mt * kChunk;
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt)
+                    if (nt < s.nt) cp16_cg(dx + nt * kChunk, s.px[nt] + off, cv && ((s.vm >> (4 + nt)) & 1u));
+            }
+        }
+        s.b += nb;
+        if (s.b >= s.gen.be) {
+            s_next_seg(s.gen, t, sh.n, nkb);
+            if (s.gen.live) s_copy_seg(s, t, sh, a, lane);
+        }
+    }
+    cp_commit();
+}
+
+// Lane 4 gq + q holds, for tokens 8 nt + 2q + e, the ranks 2 MT gq .. + 2 MT - 1
+// of the block: acc[mt][nt][e] is rank 2 MT gq + 2 mt, acc[mt][nt][2 + e] the next.
+__device__ __forceinline__ void s_reduce(const SGen &c, float *buf, const Tabs &t, const Shape &sh, int32_t T,
+                                      int lane, const float (&acc)[2][4][4]) {
+    const int32_t gq = lane >> 2, q = lane & 3;
+    const int32_t r = t.a_r[c.ja], L = t.a_len[c.ja], p0 = t.a_p0[c.ja];
+    const int32_t MT = s_mt(r, c.rb), NT8 = s_nt8(L, c.g);
+    const int32_t rows = min(kRB, r - kRB * c.rb);
+    float *base = buf + (static_cast<int64_t>(c.i) * T + p0 + kTGs * c.g) * sh.r_max + kRB * c.rb;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+        if (nt >= NT8) continue;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int32_t jt = 8 * nt + 2 * q + e;
+            if (kTGs * c.g + jt >= L) continue;
+            float *p = base + static_cast<int64_t>(jt) * sh.r_max;
+            if (MT == 2) {
+                if (4 * gq < rows) red_v4(p + 4 * gq, acc[0][nt][e], acc[0][nt][2 + e], acc[1][nt][e], acc[1][nt][2 + e]);
+            } else {
+                if (2 * gq < rows) red_v2(p + 2 * gq, acc[0][nt][e], acc[0][nt][2 + e]);
+            }
+        }
+    }
+}
+
+size_t direct_shrink_smem(int32_t S, int32_t n, int32_t T) {
+    return static_cast<size_t>(kSWarps) * kSStages * kSChunks * kChunk + tabs_bytes(S, n, T);
+}
+
+__global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a, Shape sh, const void *table) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    // the expand may start its prologue as soon as every CTA of this grid runs
+    pdl_launch_dependents();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const Tabs t = carve(smem + static_cast<size_t>(kSWarps) * kSStages * kSChunks * kChunk, sh.S, sh.n, a.T);
+    build_tabs<false>(a, sh, table, t);
+    const int32_t gen = t.misc[1];
+    float *buf = (gen & 1) ? a.acc1 : a.acc0;
+    {
+        // clear the buffer the previous call used: the next call adds into it
+        float4 *other = reinterpret_cast<float4 *>((gen & 1) ? a.acc0 : a.acc1);
+        const int64_t n4 = static_cast<int64_t>(sh.n) * a.T * sh.r_max / 4;
+        for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid; e < n4;
+             e += static_cast<int64_t>(gridDim.x) * blockDim.x)
+            other[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const int32_t nkb = cdiv(sh.k, 32), kq = sh.k - 8 * (lane & 3);
+    const uint32_t ring = sa(smem) + warp * (kSStages * kSChunks * kChunk) + 16 * lane;
+    constexpr uint32_t kSlot = kSChunks * kChunk;
+
+    SCopy cw;
+    s_first(cw.gen, t, sh.n, nkb);
+    if (cw.gen.live) s_copy_seg(cw, t, sh, a, lane);
+    SGen cg = cw.gen;  // compute walker
+#pragma unroll
+    for (int s = 0; s < kSStages - 1; ++s) s_copy_stage(cw, ring + s * kSlot, kq, t, sh, a, lane, nkb);
+
+    float acc[2][4][4];
+    int32_t sc = 0, si = kSStages - 1;
+    int32_t b = cg.bs, kb = 1, cpb = 1, MT = 1, NT = 1;
+    if (cg.live) {
+        MT = s_mt(t.a_r[cg.ja], cg.rb);
+        NT = s_nt8(t.a_len[cg.ja], cg.g);
+        cpb = 2 * MT + NT;
+        kb = kSChunks / cpb;
+    }
+    while (cg.live) {
+        s_copy_stage(cw, ring + si * kSlot, kq, t, sh, a, lane, nkb);
+        si = si + 1 == kSStages ? 0 : si + 1;
+        cp_wait<kSStages - 1>();
+        if (b == cg.bs) {
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
+        }
+        const int32_t nb = min(kb, cg.be - b);
+        const uint32_t slot = ring + sc * kSlot;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j >= nb) continue;
+            const uint32_t src = slot + j * cpb * kChunk;
+            uint4 av[4], xv[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) av[c] = c < 2 * MT ? lds16(src + c * kChunk) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+                xv[nt] = nt < NT ? lds16(src + (2 * MT + nt) * kChunk) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                if (mt >= MT) continue;
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    if (nt >= NT) continue;
+                    mma_bf16_16816(acc[mt][nt], av[2 * mt].x, av[2 * mt + 1].x, av[2 * mt].y, av[2 * mt + 1].y,
+                                   xv[nt].x, xv[nt].y);
+                    mma_bf16_16816(acc[mt][nt], av[2 * mt].z, av[2 * mt + 1].z, av[2 * mt].w, av[2 * mt + 1].w,
+                                   xv[nt].z, xv[nt].w);
+                }
+            }
+        }
+        sc = sc + 1 == kSStages ? 0 : sc + 1;
+        b += nb;
+        if (b >= cg.be) {
+            s_reduce(cg, buf, t, sh, a.T, lane, acc);
+            s_next_seg(cg, t, sh.n, nkb);
+            if (cg.live) {
+                b = cg.bs;
+                MT = s_mt(t.a_r[cg.ja], cg.rb);
+                NT = s_nt8(t.a_len[cg.ja], cg.g);
+                cpb = 2 * MT + NT;
+                kb = kSChunks / cpb;
+            }
+        }
+    }
+    cp_wait<0>();
+}
+
+// ---------------------------------------------------------------------------
+// Expand: y[tok(p), o_i + c] = bf16(y + s * sum_j xa[i][p][j] B_{s,i}[c, j])
+// ---------------------------------------------------------------------------
+// A unit: active slot ja, column block cb of the slot's concatenated slices
+// (slice i, block ci of 64 columns), token group tg of 16.  MMA rows are the
+// 64 output columns (4 tiles of 16), MMA columns the tokens, k the rank.  One
+// stage holds one unit: chunk 8 kb + 2 mt + h is B row 64 ci + 8 gq + 2 mt + h
+// at ranks 32 kb + 8q..; chunk 16 + 2 nt + e the y row of token
+// 16 tg + 8 nt + 2q + e at columns 64 ci + 8 gq...
+struct EGen {
+    int32_t ja, cb, i, ci, tg;
+    long long start, R1;
+    bool live;
+};
+
+__device__ __forceinline__ void e_advance(EGen &c, const Tabs &t, int32_t ncb) {
+    const int32_t r = t.a_r[c.ja], L = t.a_len[c.ja];
+    c.start += e_unit_w(r, L, c.tg);
+    if (kTGe * (++c.tg) >= L) {
+        c.tg = 0;
+        ++c.cb;
+        if (t.scb[c.i] + (++c.ci) == t.scb[c.i + 1]) {
+            c.ci = 0;
+            ++c.i;
+        }
+        if (c.cb == ncb) {
+            c.cb = c.i = c.ci = 0;
+            const int32_t NA = t.misc[0];
+            do {
+                ++c.ja;
+            } while (c.ja < NA && t.a_r[c.ja] == 0);
+            if (c.ja >= NA) c.live = false;
+        }
+    }
+    if (c.start >= c.R1) c.live = false;
+}
+
+__device__ __forceinline__ void e_first(EGen &c, const Tabs &t, int32_t ncb) {
+    const int32_t NA = t.misc[0];
+    long long R0;
+    warp_share<kEWarps>(t.a_pre[NA], R0, c.R1);
+    c.live = R0 < c.R1;
+    if (!c.live) return;
+    c.ja = find_active(t.a_pre, NA, R0);
+    const int32_t r = t.a_r[c.ja], L = t.a_len[c.ja];
+    long long o = R0 - t.a_pre[c.ja];
+    const int32_t wcb = e_cb_w(r, L);
+    c.cb = static_cast<int32_t>(o / wcb);
+    o -= static_cast<long long>(c.cb) * wcb;
+    c.start = t.a_pre[c.ja] + static_cast<long long>(c.cb) * wcb;
+    c.i = 0;
+    while (t.scb[c.i + 1] <= c.cb) ++c.i;
+    c.ci = c.cb - t.scb[c.i];
+    c.tg = 0;
+    // the first unit whose start is >= R0
+    while (o > 0 && c.live) {
+        o -= e_unit_w(r, L, c.tg);
+        e_advance(c, t, ncb);
+    }
+    if (c.start >= c.R1) c.live = false;
+}
+
+__device__ __forceinline__ void e_copy_stage(EGen &g, uint32_t slot, const Tabs &t, const Shape &sh,
+                                             const DArgs &a, int lane, int32_t ncb) {
+    if (g.live) {
+        const int32_t gq = lane >> 2, q = lane & 3;
+        const int32_t ja = g.ja, r = t.a_r[ja], L = t.a_len[ja], p0 = t.a_p0[ja];
+        const int32_t o0 = t.soff[g.i], d = t.soff[g.i + 1] - o0;
+        const int32_t col0 = kCB * g.ci + 8 * gq;
+        const unsigned char *Bb = reinterpret_cast<const unsigned char *>(t.bptr[t.a_slot[ja] * sh.n + g.i]) +
+                                  2 * (static_cast<int64_t>(col0) * r + 8 * q);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+            if (32 * kb >= r) break;
+            const bool vk = 32 * kb + 8 * q < r;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const bool v = vk && col0 + c < d;
+                cp16_ca(slot + (8 * kb + c) * kChunk, Bb + (v ? 2 * (c * r + 32 * kb) : 0), v);
+            }
+        }
+        const unsigned char *Y = reinterpret_cast<const unsigned char *>(a.y) + 2 * static_cast<int64_t>(o0 + col0);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            if (kTGe * g.tg + 8 * nt >= L) break;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int32_t jt = kTGe * g.tg + 8 * nt + 2 * q + e;
+                const int32_t tok = jt < L ? t.tok[p0 + jt] : -1;
+                const bool v = tok >= 0 && col0 < d;
+                cp16_cg(slot + (16 + 2 * nt + e) * kChunk, Y + (v ? 2 * static_cast<int64_t>(tok) * a.ldy : 0), v);
+            }
+        }
+        e_advance(g, t, ncb);
+    }
+    cp_commit();
+}
+
+// The sums of a unit's tokens 16 tg + 8 nt + gq at ranks 32 kb + 8q .. + 7.
+__device__ __forceinline__ void e_load_xa(const EGen &g, const float *buf, const Tabs &t, const Shape &sh,
+                                          int32_t T, int lane, float4 (&X)[2][2][2]) {
+    const int32_t gq = lane >> 2, q = lane & 3;
+    const int32_t ja = g.ja, r = t.a_r[ja], L = t.a_len[ja], p0 = t.a_p0[ja];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int32_t jt = kTGe * g.tg + 8 * nt + gq;
+        const float *row = buf + (static_cast<int64_t>(g.i) * T + p0 + jt) * sh.r_max + 8 * q;
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+            const bool v = g.live && jt < L && 32 * kb + 8 * q < r;
+            X[nt][kb][0] = v ? ldg_f4(row + 32 * kb) : make_float4(0.f, 0.f, 0.f, 0.f);
+            X[nt][kb][1] = v ? ldg_f4(row + 32 * kb + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+}
+
+__device__ __forceinline__ void e_compute(const EGen &g, uint32_t slot, const float4 (&X)[2][2][2], const Tabs &t,
+                                          const DArgs &a, int lane) {
+    const int32_t gq = lane >> 2, q = lane & 3;
+    const int32_t ja = g.ja, r = t.a_r[ja], L = t.a_len[ja], p0 = t.a_p0[ja];
+    const int32_t NT8 = min(2, cdiv(L - kTGe * g.tg, 8));
+    float acc[4][2][4];
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb) {
+        if (32 * kb >= r) break;
+        uint32_t bh[2][2][2], bl[2][2][2];  // [nt][half][pair]
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                split_bf16x2(X[nt][kb][h].x, X[nt][kb][h].y, bh[nt][h][0], bl[nt][h][0]);
+                split_bf16x2(X[nt][kb][h].z, X[nt][kb][h].w, bh[nt][h][1], bl[nt][h][1]);
+            }
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+            const uint4 c0 = lds16(slot + (8 * kb + 2 * mt) * kChunk);
+            const uint4 c1 = lds16(slot + (8 * kb + 2 * mt + 1) * kChunk);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                if (nt >= NT8) continue;
+                mma_bf16_16816(acc[mt][nt], c0.x, c1.x, c0.y, c1.y, bh[nt][0][0], bh[nt][0][1]);
+                mma_bf16_16816(acc[mt][nt], c0.x, c1.x, c0.y, c1.y, bl[nt][0][0], bl[nt][0][1]);
+                mma_bf16_16816(acc[mt][nt], c0.z, c1.z, c0.w, c1.w, bh[nt][1][0], bh[nt][1][1]);
+                mma_bf16_16816(acc[mt][nt], c0.z, c1.z, c0.w, c1.w, bl[nt][1][0], bl[nt][1][1]);
+            }
+        }
+    }
+    const float s = t.scale[t.a_slot[ja]];
+    const int32_t o0 = t.soff[g.i], d = t.soff[g.i + 1] - o0;
+    const int32_t col0 = kCB * g.ci + 8 * gq;
+    if (col0 >= d) return;
+    uint16_t *Y = a.y + o0 + col0;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        if (nt >= NT8) continue;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int32_t jt = kTGe * g.tg + 8 * nt + 2 * q + e;
+            const int32_t tok = jt < L ? t.tok[p0 + jt] : -1;
+            if (tok < 0) continue;
+            const uint4 yv = lds16(slot + (16 + 2 * nt + e) * kChunk);
+            uint4 o;
+            o.x = pack_bf16x2(fmaf(s, acc[0][nt][e], bf16lo_to_f32(yv.x)), fmaf(s, acc[0][nt][2 + e], bf16hi_to_f32(yv.x)));
+            o.y = pack_bf16x2(fmaf(s, acc[1][nt][e], bf16lo_to_f32(yv.y)), fmaf(s, acc[1][nt][2 + e], bf16hi_to_f32(yv.y)));
+            o.z = pack_bf16x2(fmaf(s, acc[2][nt][e], bf16lo_to_f32(yv.z)), fmaf(s, acc[2][nt][2 + e], bf16hi_to_f32(yv.z)));
+            o.w = pack_bf16x2(fmaf(s, acc[3][nt][e], bf16lo_to_f32(yv.w)), fmaf(s, acc[3][nt][2 + e], bf16hi_to_f32(yv.w)));
+            stg_u4(Y + static_cast<int64_t>(tok) * a.ldy, o);
+        }
+    }
+}
+
+size_t direct_expand_smem(int32_t S, int32_t n, int32_t T) {
+    return static_cast<size_t>(kEWarps) * kEStages * kEChunks * kChunk + tabs_bytes(S, n, T);
+}
+
+__global__ void __launch_bounds__(32 * kEWarps, 1) direct_expand_kernel(DArgs a, Shape sh, const void *table) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const Tabs t = carve(smem + static_cast<size_t>(kEWarps) * kEStages * kEChunks * kChunk, sh.S, sh.n, a.T);
+    // tables, B and y are not written by the shrink: read them before the wait
+    build_tabs<true>(a, sh, table, t);
+    const float *buf = (t.misc[1] & 1) ? a.acc1 : a.acc0;
+    const int32_t ncb = t.scb[LORA_MAX_SLICES];
+    const uint32_t ring = sa(smem) + warp * (kEStages * kEChunks * kChunk) + 16 * lane;
+    constexpr uint32_t kSlot = kEChunks * kChunk;
+    EGen gi;
+    e_first(gi, t, ncb);
+    EGen gc = gi;
+#pragma unroll
+    for (int s = 0; s < kEStages - 1; ++s) e_copy_stage(gi, ring + s * kSlot, t, sh, a, lane, ncb);
+    pdl_wait();
+    float4 X[2][2][2];
+    e_load_xa(gc, buf, t, sh, a.T, lane, X);
+    int32_t sc = 0, si = kEStages - 1;
+    while (gc.live) {
+        e_copy_stage(gi, ring + si * kSlot, t, sh, a, lane, ncb);
+        si = si + 1 == kEStages ? 0 : si + 1;
+        EGen gn = gc;
+        e_advance(gn, t, ncb);
+        float4 Xn[2][2][2];
+        e_load_xa(gn, buf, t, sh, a.T, lane, Xn);
+        cp_wait<kEStages - 1>();
+        e_compute(gc, ring + sc * kSlot, X, t, a, lane);
+        sc = sc + 1 == kEStages ? 0 : sc + 1;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+                X[nt][kb][0] = Xn[nt][kb][0];
+                X[nt][kb][1] = Xn[nt][kb][1];
+            }
+        gc = gn;
+    }
+    cp_wait<0>();
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(a.exits, 1) == static_cast<int32_t>(gridDim.x) - 1) {
+            *a.exits = 0;
+            atomicAdd(a.gen, 1);
+        }
+    }
+}
+
+}  // namespace
+
+bool decode_direct_supported(int32_t T, const Shape &sh) {
+    return T >= 1 && T <= kMaxTokens && sh.r_max <= kMaxRank && sh.S <= kMaxSlots && sh.S * sh.n <= kMaxPtrs &&
+           direct_shrink_smem(sh.S, sh.n, T) <= 227 * 1024 && direct_expand_smem(sh.S, sh.n, T) <= 227 * 1024;
+}
+
+cudaError_t launch_decode_direct(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
+                                 const void *table, const int32_t *sorted_ids, const int32_t *seg,
+                                 const int32_t *active, float *ws, int32_t T, int32_t *err, cudaStream_t stream) {
+    if (!decode_direct_supported(T, sh)) return cudaErrorNotSupported;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int num_sms = 0;
+    e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const size_t s_smem = direct_shrink_smem(sh.S, sh.n, T), e_smem = direct_expand_smem(sh.S, sh.n, T);
+    e = cudaFuncSetAttribute(direct_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s_smem));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(direct_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(e_smem));
+    if (e != cudaSuccess) return e;
+    const WorkspaceLayout W(T, sh.n, sh.r_max, sh.S);
+    char *base = reinterpret_cast<char *>(ws);
+    int32_t *ctrl = reinterpret_cast<int32_t *>(base);
+    DArgs a;
+    a.x = x;
+    a.ldx = ldx;
+    a.y = y;
+    a.ldy = ldy;
+    a.sorted_ids = sorted_ids;
+    a.seg = seg;
+    a.active = active;
+    a.acc0 = reinterpret_cast<float *>(base + W.acc2_off);
+    a.acc1 = reinterpret_cast<float *>(base + W.acc3_off);
+    a.gen = ctrl + 2 * LORA_MAX_SLICES * static_cast<size_t>(sh.S);
+    a.exits = a.gen + 1;
+    a.err = err;
+    a.T = T;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(num_sms));
+    cfg.blockDim = dim3(32 * kSWarps);
+    cfg.dynamicSmemBytes = s_smem;
+    cfg.stream = stream;
+    cfg.numAttrs = 0;
+    e = cudaLaunchKernelEx(&cfg, direct_shrink_kernel, a, sh, table);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg2 = {};
+    cfg2.gridDim = dim3(static_cast<unsigned>(num_sms));
+    cfg2.blockDim = dim3(32 * kEWarps);
+    cfg2.dynamicSmemBytes = e_smem;
+    cfg2.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg2.attrs = attr;
+    cfg2.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg2, direct_expand_kernel, a, sh, table);
+}
+
+}  // namespace lora

@@ -31,6 +31,10 @@ cudaError_t launch_decode_tc(const uint16_t *x, int64_t ldx, uint16_t *y, int64_
                             const void *table, const int32_t *sorted_ids, const int32_t *seg, float *ws, int32_t T,
                             int32_t *err, cudaStream_t stream);
 bool fused_decode_supported(int32_t T, int32_t r_max, int32_t k);
+bool decode_direct_supported(int32_t T, const Shape &sh);
+cudaError_t launch_decode_direct(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
+                                 const void *table, const int32_t *sorted_ids, const int32_t *seg,
+                                 const int32_t *active, float *ws, int32_t T, int32_t *err, cudaStream_t stream);
 cudaError_t launch_prefill(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                            const void *table, const int32_t *sorted_ids, const int32_t *seg, float *ws,
                            int32_t T, int32_t *err, cudaStream_t stream);
@@ -302,6 +306,10 @@ lora_status_t lora_apply_ex(const void *x, int64_t ldx, void *y, int64_t ldy, in
         if (!lora::decode_stream_supported(T, sh)) return LORA_ERR_UNSUPPORTED;
         return from_cuda(lora::launch_decode_stream(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws, T,
                                                     err, s));
+    case LORA_PATH_DECODE_DIRECT:
+        if (!lora::decode_direct_supported(T, sh)) return LORA_ERR_UNSUPPORTED;
+        return from_cuda(lora::launch_decode_direct(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, active,
+                                                    ws, T, err, s));
     case LORA_PATH_DECODE_SPLIT: {
         float *xa = xa_of(ws, T, sh);
         cudaError_t e = lora::launch_shrink(xb, ldx, sh, dev_table, sorted_ids, seg_offsets, xa, T, err, true, s);

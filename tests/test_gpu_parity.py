@@ -14,7 +14,7 @@ from _parity import assert_y_close, gpu_apply, oracle_y, untouched_rows
 
 pytestmark = pytest.mark.gpu
 
-DECODE_PATHS = ["decode_split", "decode_fused", "decode_tc", "decode_stream"]
+DECODE_PATHS = ["decode_split", "decode_fused", "decode_tc", "decode_stream", "decode_direct"]
 
 
 def _torch():
@@ -212,7 +212,7 @@ def test_apply_ragged(case, path):
     mma_ok = wl.r_max <= 128 and k % 16 == 0  # warp-MMA kernels (fused and streaming)
     tc_ok = wl.r_max <= 64                     # tcgen05 decode kernels
     if ((path == "decode_fused" and not (mma_ok or tc_ok)) or (path == "decode_tc" and not tc_ok)
-            or (path == "decode_stream" and not mma_ok)):
+            or (path == "decode_stream" and not mma_ok) or (path == "decode_direct" and not tc_ok)):
         import rank_adapter_gemm_gb300 as L
         with pytest.raises(L.LoraError) as e:
             gpu_apply(wl, path=path)
@@ -309,7 +309,7 @@ def test_apply_is_deterministic():
         np.testing.assert_array_equal(y, ys[0])
 
 
-@pytest.mark.parametrize("path", ["decode_fused", "decode_tc", "decode_stream"])
+@pytest.mark.parametrize("path", ["decode_fused", "decode_tc", "decode_stream", "decode_direct"])
 def test_fused_repeat_stays_within_tolerance(path):
     """The fused kernels add split-k partials with fp32 reductions, whose order
     varies; every repetition must still match the oracle."""
@@ -321,7 +321,7 @@ def test_fused_repeat_stays_within_tolerance(path):
         assert_y_close(y, ref, "fused repeat")
 
 
-@pytest.mark.parametrize("path", ["decode_fused", "decode_tc", "decode_stream"])
+@pytest.mark.parametrize("path", ["decode_fused", "decode_tc", "decode_stream", "decode_direct"])
 def test_decode_leaves_workspace_ready(path):
     """Each call leaves the workspace ready for the next one without a clearing
     launch: the fused kernel clears its accumulator rows and counters; the
@@ -356,7 +356,7 @@ def test_decode_leaves_workspace_ready(path):
         buf = ws.buf.cpu().numpy()
         ctrl = buf[:xa_off].view(np.int32).copy()
         assert not buf[acc_off:acc_off + xa_floats].any(), "fused accumulator not cleared"
-        if path in ("decode_tc", "decode_stream"):
+        if path in ("decode_tc", "decode_stream", "decode_direct"):
             assert ctrl[gen_word] == call, "call counter not advanced"
             ctrl[gen_word] = 0
             nxt = acc2_off + (call & 1) * region
