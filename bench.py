@@ -103,6 +103,22 @@ def captured_traffic(kernel: str):
     return rec["dram_read_bytes"] + rec["dram_write_bytes"]
 
 
+# Kernels of one lora_apply call whose DRAM traffic was captured with ncu on the
+# bench workload (per call: the sum over the call's launches).
+TRAFFIC_KERNELS = {
+    ("decode_qkv", "decode_fused"): ("fused_decode_kernel",),
+    ("decode_qkv", "decode_direct"): ("direct_shrink_kernel", "direct_expand_kernel"),
+}
+
+
+def call_traffic(config: str, path: str):
+    names = TRAFFIC_KERNELS.get((config, path))
+    if not names:
+        return None
+    parts = [captured_traffic(k) for k in names]
+    return None if any(p is None for p in parts) else sum(parts)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -376,8 +392,7 @@ def run_ours(args):
             "peak": peak_gbs,
             "unit": "GB/s",
             "frac": achieved_gbs / peak_gbs,
-            "traffic": (captured_traffic("fused_decode_kernel")
-                        if args.config == "decode_qkv" and resolved == "decode_fused" else None),
+            "traffic": call_traffic(args.config, resolved),
             "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
             "kernel": "lora_apply (shrink + expand) per projection call",
             "bytes_per_call": sum(per_layer_bytes) / len(layers),

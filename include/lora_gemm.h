@@ -76,9 +76,10 @@ typedef enum {
 /* Kernel path of lora_apply_ex. */
 typedef enum {
     LORA_PATH_AUTO = 0,          /* the prefill kernels if max_seg_hint > LORA_DECODE_MAX_SEG and
-                                    r_max <= 64; otherwise the fused decode path when it takes
-                                    the shape (the faster of its kernels for the shape), else the
-                                    split decode kernels */
+                                    r_max <= 64; otherwise, above 64 tokens, the warp-streaming
+                                    decode kernels (LORA_PATH_DECODE_DIRECT) when they take the
+                                    shape, else the fused decode path when it does; otherwise
+                                    the split decode kernels */
     LORA_PATH_DECODE_FUSED = 1,  /* one launch: shrink, per-(slot, slice) wait, expand, on warp-level
                                     MMA; needs T <= 2048, r_max <= 128 and k % 16 == 0, else the
                                     tensor-core decode kernels when they apply (LORA_PATH_DECODE_TC),

@@ -95,6 +95,8 @@ lora_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LOR
 
 // The fused decode path: the warp-level MMA kernel where it applies (faster
 // today on the decode shapes measured), else the tensor-core (tcgen05) one.
+constexpr int32_t kSmallDecodeT = 64;
+
 bool fused_ok(int32_t T, const Shape &sh) {
     return lora::fused_decode_supported(T, sh.r_max, sh.k) || lora::decode_tc_supported(T, sh);
 }
@@ -102,8 +104,11 @@ bool fused_ok(int32_t T, const Shape &sh) {
 lora_path_t resolve(lora_path_t path, int32_t T, int32_t max_seg_hint, const Shape &sh, int32_t *launches) {
     if (max_seg_hint <= 0 || max_seg_hint > T) max_seg_hint = T;
     if (path == LORA_PATH_AUTO) {
+        // measured on GB300: the warp-streaming kernels lead from a few hundred
+        // tokens up; at 64 tokens and fewer the split kernels' shorter prologue wins
         if (max_seg_hint > LORA_DECODE_MAX_SEG && lora::prefill_supported(sh.r_max)) path = LORA_PATH_PREFILL;
-        else if (fused_ok(T, sh)) path = LORA_PATH_DECODE_FUSED;
+        else if (T > kSmallDecodeT && lora::decode_direct_supported(T, sh)) path = LORA_PATH_DECODE_DIRECT;
+        else if (T > kSmallDecodeT && fused_ok(T, sh)) path = LORA_PATH_DECODE_FUSED;
         else path = LORA_PATH_DECODE_SPLIT;
     }
     if (launches != nullptr)
