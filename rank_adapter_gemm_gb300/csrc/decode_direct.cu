@@ -185,32 +185,31 @@ __device__ Tabs carve(unsigned char *base, int32_t S, int32_t n, int32_t T) {
 }
 
 // ---------------------------------------------------------------------------
-// Unit weights (about the HBM bytes a unit moves; re-reads that hit L2 and
-// activation rows count a quarter).
+// Unit weights: the 512-byte chunks a unit brings into the SM (what bounds a
+// warp's time), the A rows re-read once per token group included.
 // ---------------------------------------------------------------------------
 // Shrink: rank block rb of a slot of rank r with L tokens, per 32-column block
-// of k: the block's A rows (padded to 16 or 32), re-read once per extra token
-// group of 32, plus the x rows.
+// of k: 2 MT chunks of A rows per token group of 32, one chunk of x rows per 8
+// tokens, and a fixed cost.
 __device__ __forceinline__ int32_t s_mt(int32_t r, int32_t rb) { return r - kRB * rb > 16 ? 2 : 1; }
 __device__ __forceinline__ int32_t s_block_w(int32_t r, int32_t L, int32_t rb) {
-    const int32_t rp = 16 * s_mt(r, rb), ng = cdiv(L, kTGs);
-    return 64 * rp + 16 * (rp * (ng - 1) + L);
+    return 2 * s_mt(r, rb) * cdiv(L, kTGs) + cdiv(L, 8) + 1;
 }
 __device__ __forceinline__ long long s_slot_w(int32_t r, int32_t L, int32_t n, int32_t nkb) {
     long long w = 0;
     for (int32_t rb = 0; kRB * rb < r; ++rb) w += s_block_w(r, L, rb);
     return w * nkb * n;
 }
-// Expand: token group tg (16 tokens) of 64 output columns: the B rows (64 x
-// r, padded to 32 ranks; L2 re-reads after the first group), y read and
-// written, the sums read from L2.
+// Expand: token group tg (16 tokens) of 64 output columns: 8 chunks of B rows
+// per 32 ranks, two chunks of y and 2 nkb chunks of sums per 8 tokens, and a
+// fixed cost.
 __device__ __forceinline__ int32_t e_unit_w(int32_t r, int32_t L, int32_t tg) {
-    const int32_t rpad = 32 * cdiv(r, 32), Lg = min(kTGe, L - kTGe * tg);
-    return (tg == 0 ? 128 : 32) * rpad + (256 + r) * Lg;
+    const int32_t nt8 = min(2, cdiv(L - kTGe * tg, 8)), nkb = cdiv(r, 32);
+    return 8 * nkb + 2 * nt8 * (1 + nkb) + 2;
 }
 __device__ __forceinline__ int32_t e_cb_w(int32_t r, int32_t L) {
-    const int32_t rpad = 32 * cdiv(r, 32), ng = cdiv(L, kTGe);
-    return 128 * rpad + 32 * rpad * (ng - 1) + (256 + r) * L;
+    const int32_t nkb = cdiv(r, 32);
+    return cdiv(L, kTGe) * (8 * nkb + 2) + 2 * cdiv(L, 8) * (1 + nkb);
 }
 
 __device__ __forceinline__ void cp4(void *dst, const void *src) {
@@ -385,6 +384,9 @@ __device__ __forceinline__ void s_next_seg(SGen &c, const Tabs &t, int32_t n, in
 
 __device__ __forceinline__ void s_first(SGen &c, const Tabs &t, int32_t n, int32_t nkb) {
     const int32_t NA = t.misc[0];
+    c.ja = c.i = c.rb = c.g = c.bs = c.be = 0;  // defined fields for a warp without work
+    c.w = 1;
+    c.start = 0;
     long long R0;
     warp_share<kSWarps>(t.a_pre[NA], R0, c.R1);
     c.live = R0 < c.R1;
@@ -643,6 +645,8 @@ __device__ __forceinline__ void e_advance(EGen &c, const Tabs &t, int32_t ncb) {
 
 __device__ __forceinline__ void e_first(EGen &c, const Tabs &t, int32_t ncb) {
     const int32_t NA = t.misc[0];
+    c.ja = c.cb = c.i = c.ci = c.tg = 0;  // defined fields for a warp without work
+    c.start = 0;
     long long R0;
     warp_share<kEWarps>(t.a_pre[NA], R0, c.R1);
     c.live = R0 < c.R1;
@@ -706,6 +710,14 @@ __device__ __forceinline__ void e_copy_stage(EGen &g, uint32_t slot, const Tabs 
 __device__ __forceinline__ void e_load_xa(const EGen &g, const float *buf, const Tabs &t, const Shape &sh,
                                           int32_t T, int lane, float4 (&X)[2][2][2]) {
     const int32_t gq = lane >> 2, q = lane & 3;
+    if (!g.live) {
+        // past the warp's last unit: the tables are not indexed with its fields
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) X[nt][kb][0] = X[nt][kb][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        return;
+    }
     const int32_t ja = g.ja, r = t.a_r[ja], L = t.a_len[ja], p0 = t.a_p0[ja];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
@@ -713,7 +725,7 @@ __device__ __forceinline__ void e_load_xa(const EGen &g, const float *buf, const
         const float *row = buf + (static_cast<int64_t>(g.i) * T + p0 + jt) * sh.r_max + 8 * q;
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
-            const bool v = g.live && jt < L && 32 * kb + 8 * q < r;
+            const bool v = jt < L && 32 * kb + 8 * q < r;
             X[nt][kb][0] = v ? ldg_f4(row + 32 * kb) : make_float4(0.f, 0.f, 0.f, 0.f);
             X[nt][kb][1] = v ? ldg_f4(row + 32 * kb + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
