@@ -54,7 +54,6 @@ constexpr int kEWarps = 8;           // expand
 constexpr int kChunk = 512;          // 16 bytes per lane
 constexpr int kSChunks = 12;         // shrink stage: 12 chunks (6 KB)
 constexpr int kSStages = 2;          // shrink ring depth per warp
-constexpr int kEChunks = 20;         // expand stage: B (<= 16 chunks) + y (<= 4 chunks)
 constexpr int kEStages = 2;          // expand ring depth per warp
 constexpr int kMaxTokens = 2048;
 constexpr int kMaxRank = 64;
@@ -120,6 +119,45 @@ __device__ __forceinline__ float4 ldg_f4(const float *p) {
     float4 v;
     asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
     return v;
+}
+
+// Bulk (TMA) copies and L2 prefetches of contiguous byte ranges (16-byte
+// aligned, sizes multiples of 16), completion of copies counted on an mbarrier.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+// Bounded wait on an mbarrier phase (a bulk copy of this warp): false after
+// 200 ms, which only a broken memory system can cause.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    while (true) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        uint64_t t1;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+        if (t1 - t0 > 200ull * 1000 * 1000) return false;
+    }
 }
 
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -524,6 +562,26 @@ __global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a,
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Tabs t = carve(smem + static_cast<size_t>(kSWarps) * kSStages * kSChunks * kChunk, sh.S, sh.n, a.T);
     build_tabs<false>(a, sh, table, t);
+    {
+        // Bring what the expand reads into L2 while this grid streams A: the B
+        // matrix of every (active slot, slice) in 64 KB pieces, and the y row of
+        // every token with an adapter.  DRAM then stays busy through this
+        // kernel's ramp and tail, and the expand reads L2.
+        const int32_t NA = t.misc[0], G = gridDim.x;
+        for (int32_t e = blockIdx.x + G * tid; e < NA * sh.n; e += G * static_cast<int32_t>(blockDim.x)) {
+            const int32_t ja = e / sh.n, i = e - ja * sh.n, r = t.a_r[ja];
+            if (r == 0) continue;
+            const unsigned char *B = reinterpret_cast<const unsigned char *>(t.bptr[t.a_slot[ja] * sh.n + i]);
+            const uint32_t bytes = 2u * static_cast<uint32_t>(t.soff[i + 1] - t.soff[i]) * r;
+            for (uint32_t o = 0; o < bytes; o += 65536u) bulk_prefetch_l2(B + o, min(65536u, bytes - o));
+        }
+        const uint32_t ybytes = 2u * static_cast<uint32_t>(t.soff[LORA_MAX_SLICES]);
+        const int32_t npos = min(max(t.seg[sh.S], 0), a.T);
+        for (int32_t p = blockIdx.x + G * tid; p < npos; p += G * static_cast<int32_t>(blockDim.x)) {
+            const int32_t tok = t.tok[p];
+            if (tok >= 0) bulk_prefetch_l2(a.y + static_cast<int64_t>(tok) * a.ldy, ybytes);
+        }
+    }
     const int32_t gen = t.misc[1];
     float *buf = (gen & 1) ? a.acc1 : a.acc0;
     {
@@ -609,43 +667,49 @@ __global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a,
 // ---------------------------------------------------------------------------
 // Expand: y[tok(p), o_i + c] = bf16(y + s * sum_j xa[i][p][j] B_{s,i}[c, j])
 // ---------------------------------------------------------------------------
-// A unit: active slot ja, column block cb of the slot's concatenated slices
-// (slice i, block ci of 64 columns), token group tg of 16.  MMA rows are the
+// A unit: active slot ja, slice i, token group tg of 16, block ci of 64 output
+// columns.  MMA rows are the
 // 64 output columns (4 tiles of 16), MMA columns the tokens, k the rank.  One
-// stage holds one unit: chunk 8 kb + 2 mt + h is B row 64 ci + 8 gq + 2 mt + h
-// at ranks 32 kb + 8q..; chunk 16 + 2 nt + e the y row of token
-// 16 tg + 8 nt + 2q + e at columns 64 ci + 8 gq...
+// stage holds one unit: bytes [0, 8 KB) the unit's B rows 64 ci .. + 63 as
+// stored ([64][r] bf16, one bulk copy, completion on the slot's mbarrier);
+// then chunk c < 4 (lane-private cp.async) the y row of token
+// 16 tg + 8 nt + 2q + e (c = 2 nt + e) at columns 64 ci + 8 gq...
+// Lane 4 gq + q feeds MMA row m of tile mt from B row 8 (m % 8) + 2 mt + m / 8,
+// so that its accumulators cover the 8 adjacent columns 8 gq .. 8 gq + 7.
+constexpr uint32_t kEBTile = 8192;
+constexpr uint32_t kESlot = kEBTile + 4 * kChunk;
+
 struct EGen {
-    int32_t ja, cb, i, ci, tg;
+    int32_t ja, i, tg, ci;
     long long start, R1;
     bool live;
 };
 
-__device__ __forceinline__ void e_advance(EGen &c, const Tabs &t, int32_t ncb) {
+// Units of a slot in the order (slice, token group, column block): consecutive
+// units of a warp mostly share their tokens' sums, which stay in registers.
+__device__ __forceinline__ void e_advance(EGen &c, const Tabs &t, int32_t n) {
     const int32_t r = t.a_r[c.ja], L = t.a_len[c.ja];
     c.start += e_unit_w(r, L, c.tg);
-    if (kTGe * (++c.tg) >= L) {
-        c.tg = 0;
-        ++c.cb;
-        if (t.scb[c.i] + (++c.ci) == t.scb[c.i + 1]) {
-            c.ci = 0;
-            ++c.i;
-        }
-        if (c.cb == ncb) {
-            c.cb = c.i = c.ci = 0;
-            const int32_t NA = t.misc[0];
-            do {
-                ++c.ja;
-            } while (c.ja < NA && t.a_r[c.ja] == 0);
-            if (c.ja >= NA) c.live = false;
+    if (t.scb[c.i] + (++c.ci) == t.scb[c.i + 1]) {
+        c.ci = 0;
+        if (kTGe * (++c.tg) >= L) {
+            c.tg = 0;
+            if (++c.i == n) {
+                c.i = 0;
+                const int32_t NA = t.misc[0];
+                do {
+                    ++c.ja;
+                } while (c.ja < NA && t.a_r[c.ja] == 0);
+                if (c.ja >= NA) c.live = false;
+            }
         }
     }
     if (c.start >= c.R1) c.live = false;
 }
 
-__device__ __forceinline__ void e_first(EGen &c, const Tabs &t, int32_t ncb) {
+__device__ __forceinline__ void e_first(EGen &c, const Tabs &t, int32_t n) {
     const int32_t NA = t.misc[0];
-    c.ja = c.cb = c.i = c.ci = c.tg = 0;  // defined fields for a warp without work
+    c.ja = c.i = c.tg = c.ci = 0;  // defined fields for a warp without work
     c.start = 0;
     long long R0;
     warp_share<kEWarps>(t.a_pre[NA], R0, c.R1);
@@ -654,42 +718,49 @@ __device__ __forceinline__ void e_first(EGen &c, const Tabs &t, int32_t ncb) {
     c.ja = find_active(t.a_pre, NA, R0);
     const int32_t r = t.a_r[c.ja], L = t.a_len[c.ja];
     long long o = R0 - t.a_pre[c.ja];
-    const int32_t wcb = e_cb_w(r, L);
-    c.cb = static_cast<int32_t>(o / wcb);
-    o -= static_cast<long long>(c.cb) * wcb;
-    c.start = t.a_pre[c.ja] + static_cast<long long>(c.cb) * wcb;
-    c.i = 0;
-    while (t.scb[c.i + 1] <= c.cb) ++c.i;
-    c.ci = c.cb - t.scb[c.i];
-    c.tg = 0;
-    // the first unit whose start is >= R0
-    while (o > 0 && c.live) {
-        o -= e_unit_w(r, L, c.tg);
-        e_advance(c, t, ncb);
+    const long long wcb = e_cb_w(r, L);
+    c.start = t.a_pre[c.ja];
+    while (o >= (t.scb[c.i + 1] - t.scb[c.i]) * wcb) {
+        const long long ws = (t.scb[c.i + 1] - t.scb[c.i]) * wcb;
+        o -= ws;
+        c.start += ws;
+        ++c.i;
     }
+    const int32_t nci = t.scb[c.i + 1] - t.scb[c.i];
+    while (true) {
+        const long long wt = static_cast<long long>(nci) * e_unit_w(r, L, c.tg);
+        if (o < wt) break;
+        o -= wt;
+        c.start += wt;
+        ++c.tg;
+    }
+    const int32_t w = e_unit_w(r, L, c.tg);
+    c.ci = static_cast<int32_t>(o / w);
+    c.start += static_cast<long long>(c.ci) * w;
+    // the first unit whose start is >= R0
+    if (c.start < R0) e_advance(c, t, n);
     if (c.start >= c.R1) c.live = false;
 }
 
-__device__ __forceinline__ void e_copy_stage(EGen &g, uint32_t slot, const Tabs &t, const Shape &sh,
-                                             const DArgs &a, int lane, int32_t ncb) {
+// Copies of the next unit into slot `slot` of this warp's ring (base `wslot`),
+// then a commit (an empty group once the walk is over).
+__device__ __forceinline__ void e_copy_stage(EGen &g, uint32_t wslot, uint32_t bar, const Tabs &t, const Shape &sh,
+                                             const DArgs &a, int lane, int32_t n) {
     if (g.live) {
         const int32_t gq = lane >> 2, q = lane & 3;
         const int32_t ja = g.ja, r = t.a_r[ja], L = t.a_len[ja], p0 = t.a_p0[ja];
         const int32_t o0 = t.soff[g.i], d = t.soff[g.i + 1] - o0;
-        const int32_t col0 = kCB * g.ci + 8 * gq;
-        const unsigned char *Bb = reinterpret_cast<const unsigned char *>(t.bptr[t.a_slot[ja] * sh.n + g.i]) +
-                                  2 * (static_cast<int64_t>(col0) * r + 8 * q);
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-            if (32 * kb >= r) break;
-            const bool vk = 32 * kb + 8 * q < r;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const bool v = vk && col0 + c < d;
-                cp16_ca(slot + (8 * kb + c) * kChunk, Bb + (v ? 2 * (c * r + 32 * kb) : 0), v);
-            }
+        if (lane == 0) {
+            const int32_t rows = min(kCB, d - kCB * g.ci);
+            const uint32_t bytes = 2u * static_cast<uint32_t>(rows * r);
+            const unsigned char *src = reinterpret_cast<const unsigned char *>(t.bptr[t.a_slot[ja] * sh.n + g.i]) +
+                                       2 * static_cast<int64_t>(kCB * g.ci) * r;
+            mbar_expect_tx(bar, bytes);
+            bulk_copy(wslot, src, bytes, bar);
         }
+        const int32_t col0 = kCB * g.ci + 8 * gq;
         const unsigned char *Y = reinterpret_cast<const unsigned char *>(a.y) + 2 * static_cast<int64_t>(o0 + col0);
+        const uint32_t ydst = wslot + kEBTile + 16 * lane;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             if (kTGe * g.tg + 8 * nt >= L) break;
@@ -698,10 +769,10 @@ __device__ __forceinline__ void e_copy_stage(EGen &g, uint32_t slot, const Tabs 
                 const int32_t jt = kTGe * g.tg + 8 * nt + 2 * q + e;
                 const int32_t tok = jt < L ? t.tok[p0 + jt] : -1;
                 const bool v = tok >= 0 && col0 < d;
-                cp16_cg(slot + (16 + 2 * nt + e) * kChunk, Y + (v ? 2 * static_cast<int64_t>(tok) * a.ldy : 0), v);
+                cp16_cg(ydst + (2 * nt + e) * kChunk, Y + (v ? 2 * static_cast<int64_t>(tok) * a.ldy : 0), v);
             }
         }
-        e_advance(g, t, ncb);
+        e_advance(g, t, n);
     }
     cp_commit();
 }
@@ -732,7 +803,7 @@ __device__ __forceinline__ void e_load_xa(const EGen &g, const float *buf, const
     }
 }
 
-__device__ __forceinline__ void e_compute(const EGen &g, uint32_t slot, const float4 (&X)[2][2][2], const Tabs &t,
+__device__ __forceinline__ void e_compute(const EGen &g, uint32_t wslot, const float4 (&X)[2][2][2], const Tabs &t,
                                           const DArgs &a, int lane) {
     const int32_t gq = lane >> 2, q = lane & 3;
     const int32_t ja = g.ja, r = t.a_r[ja], L = t.a_len[ja], p0 = t.a_p0[ja];
@@ -753,10 +824,14 @@ __device__ __forceinline__ void e_compute(const EGen &g, uint32_t slot, const fl
                 split_bf16x2(X[nt][kb][h].x, X[nt][kb][h].y, bh[nt][h][0], bl[nt][h][0]);
                 split_bf16x2(X[nt][kb][h].z, X[nt][kb][h].w, bh[nt][h][1], bl[nt][h][1]);
             }
+        const int32_t rc = 32 * kb + 8 * q;
+        const bool vk = rc < r;
+        // B row 8 gq + 2 mt (+1) at ranks rc..rc+7: byte 2 (row r + rc) of the tile
+        const uint32_t brow = wslot + 2u * static_cast<uint32_t>(8 * gq * r + rc);
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
-            const uint4 c0 = lds16(slot + (8 * kb + 2 * mt) * kChunk);
-            const uint4 c1 = lds16(slot + (8 * kb + 2 * mt + 1) * kChunk);
+            const uint4 c0 = vk ? lds16(brow + 2u * static_cast<uint32_t>(2 * mt * r)) : make_uint4(0, 0, 0, 0);
+            const uint4 c1 = vk ? lds16(brow + 2u * static_cast<uint32_t>((2 * mt + 1) * r)) : make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 if (nt >= NT8) continue;
@@ -772,6 +847,7 @@ __device__ __forceinline__ void e_compute(const EGen &g, uint32_t slot, const fl
     const int32_t col0 = kCB * g.ci + 8 * gq;
     if (col0 >= d) return;
     uint16_t *Y = a.y + o0 + col0;
+    const uint32_t ysrc = wslot + kEBTile + 16 * lane;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
         if (nt >= NT8) continue;
@@ -780,7 +856,7 @@ __device__ __forceinline__ void e_compute(const EGen &g, uint32_t slot, const fl
             const int32_t jt = kTGe * g.tg + 8 * nt + 2 * q + e;
             const int32_t tok = jt < L ? t.tok[p0 + jt] : -1;
             if (tok < 0) continue;
-            const uint4 yv = lds16(slot + (16 + 2 * nt + e) * kChunk);
+            const uint4 yv = lds16(ysrc + (2 * nt + e) * kChunk);
             uint4 o;
             o.x = pack_bf16x2(fmaf(s, acc[0][nt][e], bf16lo_to_f32(yv.x)), fmaf(s, acc[0][nt][2 + e], bf16hi_to_f32(yv.x)));
             o.y = pack_bf16x2(fmaf(s, acc[1][nt][e], bf16lo_to_f32(yv.y)), fmaf(s, acc[1][nt][2 + e], bf16hi_to_f32(yv.y)));
@@ -792,46 +868,59 @@ __device__ __forceinline__ void e_compute(const EGen &g, uint32_t slot, const fl
 }
 
 size_t direct_expand_smem(int32_t S, int32_t n, int32_t T) {
-    return static_cast<size_t>(kEWarps) * kEStages * kEChunks * kChunk + tabs_bytes(S, n, T);
+    return static_cast<size_t>(kEWarps) * kEStages * kESlot + tabs_bytes(S, n, T);
 }
 
 __global__ void __launch_bounds__(32 * kEWarps, 1) direct_expand_kernel(DArgs a, Shape sh, const void *table) {
     extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t bars[kEWarps][kEStages];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const Tabs t = carve(smem + static_cast<size_t>(kEWarps) * kEStages * kEChunks * kChunk, sh.S, sh.n, a.T);
+    if (lane == 0) {
+        for (int s = 0; s < kEStages; ++s) mbar_init(sa(&bars[warp][s]), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    const Tabs t = carve(smem + static_cast<size_t>(kEWarps) * kEStages * kESlot, sh.S, sh.n, a.T);
     // tables, B and y are not written by the shrink: read them before the wait
     build_tabs<true>(a, sh, table, t);
     const float *buf = (t.misc[1] & 1) ? a.acc1 : a.acc0;
-    const int32_t ncb = t.scb[LORA_MAX_SLICES];
-    const uint32_t ring = sa(smem) + warp * (kEStages * kEChunks * kChunk) + 16 * lane;
-    constexpr uint32_t kSlot = kEChunks * kChunk;
+    const uint32_t wring = sa(smem) + warp * (kEStages * kESlot);
     EGen gi;
-    e_first(gi, t, ncb);
+    e_first(gi, t, sh.n);
     EGen gc = gi;
 #pragma unroll
-    for (int s = 0; s < kEStages - 1; ++s) e_copy_stage(gi, ring + s * kSlot, t, sh, a, lane, ncb);
+    for (int s = 0; s < kEStages - 1; ++s) e_copy_stage(gi, wring + s * kESlot, sa(&bars[warp][s]), t, sh, a, lane, sh.n);
     pdl_wait();
     float4 X[2][2][2];
     e_load_xa(gc, buf, t, sh, a.T, lane, X);
-    int32_t sc = 0, si = kEStages - 1;
+    int32_t it = 0;
+    bool timed_out = false;
     while (gc.live) {
-        e_copy_stage(gi, ring + si * kSlot, t, sh, a, lane, ncb);
-        si = si + 1 == kEStages ? 0 : si + 1;
+        const int32_t sn = (it + kEStages - 1) % kEStages, sc = it % kEStages;
+        __syncwarp();  // every lane's reads of the slot refilled next are done
+        e_copy_stage(gi, wring + sn * kESlot, sa(&bars[warp][sn]), t, sh, a, lane, sh.n);
         EGen gn = gc;
-        e_advance(gn, t, ncb);
+        e_advance(gn, t, sh.n);
+        // the next unit's sums: the same registers while (slot, slice, token group) holds
+        const bool same = gn.live && gn.ja == gc.ja && gn.i == gc.i && gn.tg == gc.tg;
         float4 Xn[2][2][2];
-        e_load_xa(gn, buf, t, sh, a.T, lane, Xn);
+        if (!same) e_load_xa(gn, buf, t, sh, a.T, lane, Xn);
         cp_wait<kEStages - 1>();
-        e_compute(gc, ring + sc * kSlot, X, t, a, lane);
-        sc = sc + 1 == kEStages ? 0 : sc + 1;
+        if (!mbar_wait(sa(&bars[warp][sc]), static_cast<uint32_t>(it / kEStages) & 1u) && !timed_out) {
+            timed_out = true;
+            if (lane == 0) report_error(a.err, LORA_ERR_TIMEOUT);
+        }
+        e_compute(gc, wring + sc * kESlot, X, t, a, lane);
+        if (!same) {
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int kb = 0; kb < 2; ++kb) {
-                X[nt][kb][0] = Xn[nt][kb][0];
-                X[nt][kb][1] = Xn[nt][kb][1];
-            }
+                for (int kb = 0; kb < 2; ++kb) {
+                    X[nt][kb][0] = Xn[nt][kb][0];
+                    X[nt][kb][1] = Xn[nt][kb][1];
+                }
+        }
         gc = gn;
+        ++it;
     }
     cp_wait<0>();
     __syncthreads();
