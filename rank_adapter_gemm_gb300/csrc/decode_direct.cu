@@ -32,8 +32,9 @@
 //     (red.global.add.v4.f32).  The expand is launched as a programmatic
 //     dependent of the shrink: it builds its tables and copies its first
 //     stages of B and y (which the shrink does not write) before
-//     griddepcontrol.wait, and reads the sums only after it.  x·A enters the
-//     expand MMA as bf16 hi + lo parts (about 2^-17 relative), and
+//     griddepcontrol.wait, and reads the sums only after it.  The fp32 sums
+//     enter the expand MMA rounded once to bf16 (2^-9 relative, as serving
+//     engines feed their expand), accumulation stays fp32, and
 //     y = bf16(y + s · xa B^T) is rounded once.
 //   * The workspace holds two sum buffers and a call counter g: call g adds
 //     into buffer g & 1 and clears buffer (g + 1) & 1, which the previous call
@@ -551,6 +552,28 @@ __device__ __forceinline__ void s_reduce(const SGen &c, float *buf, const Tabs &
     }
 }
 
+// Brings what the expand reads into L2 while the shrink streams A: the B
+// matrix of every (active slot, slice) in 64 KB pieces and the y row of every
+// token with an adapter, spread over all threads of the grid.  A warp issues
+// its share once its first stage has landed: the prefetches then fill the DRAM
+// time after the first burst of A instead of delaying it.
+__device__ __forceinline__ void prefetch_expand_inputs(const Tabs &t, const Shape &sh, const DArgs &a) {
+    const int32_t NA = t.misc[0], G = gridDim.x, tid = threadIdx.x;
+    for (int32_t e = blockIdx.x + G * tid; e < NA * sh.n; e += G * static_cast<int32_t>(blockDim.x)) {
+        const int32_t ja = e / sh.n, i = e - ja * sh.n, r = t.a_r[ja];
+        if (r == 0) continue;
+        const unsigned char *B = reinterpret_cast<const unsigned char *>(t.bptr[t.a_slot[ja] * sh.n + i]);
+        const uint32_t bytes = 2u * static_cast<uint32_t>(t.soff[i + 1] - t.soff[i]) * r;
+        for (uint32_t o = 0; o < bytes; o += 65536u) bulk_prefetch_l2(B + o, min(65536u, bytes - o));
+    }
+    const uint32_t ybytes = 2u * static_cast<uint32_t>(t.soff[LORA_MAX_SLICES]);
+    const int32_t npos = min(max(t.seg[sh.S], 0), a.T);
+    for (int32_t p = blockIdx.x + G * tid; p < npos; p += G * static_cast<int32_t>(blockDim.x)) {
+        const int32_t tok = t.tok[p];
+        if (tok >= 0) bulk_prefetch_l2(a.y + static_cast<int64_t>(tok) * a.ldy, ybytes);
+    }
+}
+
 size_t direct_shrink_smem(int32_t S, int32_t n, int32_t T) {
     return static_cast<size_t>(kSWarps) * kSStages * kSChunks * kChunk + tabs_bytes(S, n, T);
 }
@@ -562,26 +585,6 @@ __global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a,
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Tabs t = carve(smem + static_cast<size_t>(kSWarps) * kSStages * kSChunks * kChunk, sh.S, sh.n, a.T);
     build_tabs<false>(a, sh, table, t);
-    {
-        // Bring what the expand reads into L2 while this grid streams A: the B
-        // matrix of every (active slot, slice) in 64 KB pieces, and the y row of
-        // every token with an adapter.  DRAM then stays busy through this
-        // kernel's ramp and tail, and the expand reads L2.
-        const int32_t NA = t.misc[0], G = gridDim.x;
-        for (int32_t e = blockIdx.x + G * tid; e < NA * sh.n; e += G * static_cast<int32_t>(blockDim.x)) {
-            const int32_t ja = e / sh.n, i = e - ja * sh.n, r = t.a_r[ja];
-            if (r == 0) continue;
-            const unsigned char *B = reinterpret_cast<const unsigned char *>(t.bptr[t.a_slot[ja] * sh.n + i]);
-            const uint32_t bytes = 2u * static_cast<uint32_t>(t.soff[i + 1] - t.soff[i]) * r;
-            for (uint32_t o = 0; o < bytes; o += 65536u) bulk_prefetch_l2(B + o, min(65536u, bytes - o));
-        }
-        const uint32_t ybytes = 2u * static_cast<uint32_t>(t.soff[LORA_MAX_SLICES]);
-        const int32_t npos = min(max(t.seg[sh.S], 0), a.T);
-        for (int32_t p = blockIdx.x + G * tid; p < npos; p += G * static_cast<int32_t>(blockDim.x)) {
-            const int32_t tok = t.tok[p];
-            if (tok >= 0) bulk_prefetch_l2(a.y + static_cast<int64_t>(tok) * a.ldy, ybytes);
-        }
-    }
     const int32_t gen = t.misc[1];
     float *buf = (gen & 1) ? a.acc1 : a.acc0;
     {
@@ -603,6 +606,8 @@ __global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a,
 #pragma unroll
     for (int s = 0; s < kSStages - 1; ++s) s_copy_stage(cw, ring + s * kSlot, kq, t, sh, a, lane, nkb);
 
+    if (!cg.live) prefetch_expand_inputs(t, sh, a);
+    bool prefetched = !cg.live;
     float acc[2][4][4];
     int32_t sc = 0, si = kSStages - 1;
     int32_t b = cg.bs, kb = 1, cpb = 1, MT = 1, NT = 1;
@@ -616,6 +621,10 @@ __global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a,
         s_copy_stage(cw, ring + si * kSlot, kq, t, sh, a, lane, nkb);
         si = si + 1 == kSStages ? 0 : si + 1;
         cp_wait<kSStages - 1>();
+        if (!prefetched) {
+            prefetch_expand_inputs(t, sh, a);
+            prefetched = true;
+        }
         if (b == cg.bs) {
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt)
@@ -816,13 +825,13 @@ __device__ __forceinline__ void e_compute(const EGen &g, uint32_t wslot, const f
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
         if (32 * kb >= r) break;
-        uint32_t bh[2][2][2], bl[2][2][2];  // [nt][half][pair]
+        uint32_t bh[2][2][2];  // [nt][half][pair]: the sums rounded to bf16 once
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                split_bf16x2(X[nt][kb][h].x, X[nt][kb][h].y, bh[nt][h][0], bl[nt][h][0]);
-                split_bf16x2(X[nt][kb][h].z, X[nt][kb][h].w, bh[nt][h][1], bl[nt][h][1]);
+                bh[nt][h][0] = pack_bf16x2(X[nt][kb][h].x, X[nt][kb][h].y);
+                bh[nt][h][1] = pack_bf16x2(X[nt][kb][h].z, X[nt][kb][h].w);
             }
         const int32_t rc = 32 * kb + 8 * q;
         const bool vk = rc < r;
@@ -836,9 +845,7 @@ __device__ __forceinline__ void e_compute(const EGen &g, uint32_t wslot, const f
             for (int nt = 0; nt < 2; ++nt) {
                 if (nt >= NT8) continue;
                 mma_bf16_16816(acc[mt][nt], c0.x, c1.x, c0.y, c1.y, bh[nt][0][0], bh[nt][0][1]);
-                mma_bf16_16816(acc[mt][nt], c0.x, c1.x, c0.y, c1.y, bl[nt][0][0], bl[nt][0][1]);
                 mma_bf16_16816(acc[mt][nt], c0.z, c1.z, c0.w, c1.w, bh[nt][1][0], bh[nt][1][1]);
-                mma_bf16_16816(acc[mt][nt], c0.z, c1.z, c0.w, c1.w, bl[nt][1][0], bl[nt][1][1]);
             }
         }
     }
