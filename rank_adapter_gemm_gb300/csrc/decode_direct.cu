@@ -617,7 +617,14 @@ __global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a,
         cpb = 2 * MT + NT;
         kb = kSChunks / cpb;
     }
+    bool first = true;
     while (cg.live) {
+        if (first) {
+            // the first stage of every warp lands before any second stage is asked
+            // for: the opening burst is half as long
+            cp_wait<0>();
+            first = false;
+        }
         s_copy_stage(cw, ring + si * kSlot, kq, t, sh, a, lane, nkb);
         si = si + 1 == kSStages ? 0 : si + 1;
         cp_wait<kSStages - 1>();
