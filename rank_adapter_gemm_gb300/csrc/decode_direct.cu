@@ -50,11 +50,11 @@ namespace lora {
 
 namespace {
 
-constexpr int kSWarps = 16;          // shrink: 4 warps per SM sub-partition
+constexpr int kSWarps = 12;          // shrink: 3 warps per SM sub-partition
 constexpr int kEWarps = 8;           // expand
 constexpr int kChunk = 512;          // 16 bytes per lane
-constexpr int kSChunks = 12;         // shrink stage: 12 chunks (6 KB)
-constexpr int kSStages = 2;          // shrink ring depth per warp
+constexpr int kSChunks = 11;         // shrink stage: 11 chunks (5.5 KB)
+constexpr int kSStages = 3;          // shrink ring depth per warp
 constexpr int kEStages = 2;          // expand ring depth per warp
 constexpr int kMaxTokens = 2048;
 constexpr int kMaxRank = 64;
