@@ -243,6 +243,19 @@ def metric_name(config):
         f"LoRA-branch tokens/sec and achieved HBM GB/s (% of peak), {config}"
 
 
+def _index_ids(wl):
+    """Slot ids the step uploads: one per token, or one per sequence of
+    tokens_per_seq tokens (speculative decode, sequence-major)."""
+    return np.ascontiguousarray(wl.slot_ids[::wl.tokens_per_seq])
+
+
+def _build_index(index, slot_dev, table, tokens_per_seq):
+    if tokens_per_seq > 1:
+        index.build_seq(slot_dev, tokens_per_seq, table)
+    else:
+        index.build(slot_dev, table)
+
+
 def run_ours(args):
     import torch
     import rank_adapter_gemm_gb300 as L
@@ -264,7 +277,7 @@ def run_ours(args):
     T, S = wl.T, wl.S
     counts = np.bincount(wl.slot_ids[wl.slot_ids >= 0], minlength=S)
     max_seg = int(counts.max()) if counts.size else 0
-    slot_dev = torch.from_numpy(wl.slot_ids).to(dev)
+    slot_dev = torch.from_numpy(_index_ids(wl)).to(dev)
     index = L.TokenIndex(T, S, device=dev)
     ws = [L.Workspace(T, lay.shape, device=dev) for lay in layers[:len(base)]]
     ws_of = [ws[l % len(ws)].buf for l in range(len(layers))]
@@ -278,7 +291,7 @@ def run_ours(args):
 
     def index_part():
         layers[0].refresh_table()
-        index.build(slot_dev, layers[0].table)
+        _build_index(index, slot_dev, layers[0].table, wl.tokens_per_seq)
 
     def apply_part():
         for l in range(len(layers)):
@@ -418,7 +431,7 @@ def run_e2e(args, wl, layers, index, slot_dev, ws_of, max_seg, dev, world):
     import torch
     import rank_adapter_gemm_gb300 as L
     T = wl.T
-    h_slots = torch.from_numpy(wl.slot_ids).pin_memory()
+    h_slots = torch.from_numpy(_index_ids(wl)).pin_memory()
     h_x = [lay.x.cpu().pin_memory() for lay in layers]
     h_y = [lay.y.cpu().pin_memory() for lay in layers]
     h_out = [torch.empty_like(h).pin_memory() for h in h_y]
@@ -429,7 +442,7 @@ def run_e2e(args, wl, layers, index, slot_dev, ws_of, max_seg, dev, world):
         for lay, hx, hy in zip(layers, h_x, h_y):
             lay.x.copy_(hx, non_blocking=True)
             lay.y.copy_(hy, non_blocking=True)
-        index.build(slot_dev, layers[0].table)
+        _build_index(index, slot_dev, layers[0].table, wl.tokens_per_seq)
         for l, lay in enumerate(layers):
             L.lora_apply(lay.x, lay.y, lay.shape, lay.table.dev, index.sorted_ids, index.seg_offsets,
                          index.active, ws_of[l], index.err, max_seg_hint=max_seg, path=args.path)

@@ -208,6 +208,27 @@ lora_status_t lora_build_index(const int32_t *slot_ids, int32_t T, int32_t S, co
                                int32_t *err, lora_stream_t stream);
 
 /*
+ * Token index for speculative decoding, where every sequence carries the same
+ * number of tokens (TensorRT-LLM LoRA serving page, section "一次 decode 批次的
+ * 路由": with tokens_per_seq > 1 the sequence order is expanded to the token
+ * order as sorted * tokens_per_seq + arange(tokens_per_seq)).
+ *   seq_slot_ids   device int32[n_seq], the slot of each sequence (-1: none)
+ *   tokens_per_seq >= 1; sequence b owns tokens b*tokens_per_seq ..
+ *                  b*tokens_per_seq + tokens_per_seq - 1 of x and y (T =
+ *                  n_seq * tokens_per_seq tokens, at most INT32_MAX)
+ * The outputs are exactly lora_build_index's for the token-level slot ids
+ * (each sequence's slot repeated tokens_per_seq times): sorted_ids int32[T],
+ * seg_offsets int32[S + 2] (seg_offsets[S + 1] = T), active int32[S + 1],
+ * the same error reporting.  One launch; nothing is allocated.  Host checks:
+ * LORA_ERR_INVALID_ARG for n_seq < 0, tokens_per_seq < 1, T above INT32_MAX,
+ * S outside [1, LORA_MAX_SLOTS] or missing pointers, LORA_ERR_ALIGNMENT for an
+ * unaligned table.
+ */
+lora_status_t lora_build_index_seq(const int32_t *seq_slot_ids, int32_t n_seq, int32_t tokens_per_seq, int32_t S,
+                                   const void *dev_table, int32_t *sorted_ids, int32_t *seg_offsets,
+                                   int32_t *active, int32_t *err, lora_stream_t stream);
+
+/*
  * Workspace size for T tokens of a projection, in order: a control block of
  * per-slot counters and a call counter; the fp32 shrink output
  * xa[n_slices][T][r_max] (row t = token t); the fused decode kernel's fp32

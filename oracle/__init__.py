@@ -139,6 +139,17 @@ def build_index(slot_ids: np.ndarray, S: int, ranks: np.ndarray):
     return sorted_ids[:T], seg, active, int(st)
 
 
+def build_index_seq(seq_slot_ids: np.ndarray, tokens_per_seq: int, S: int, ranks: np.ndarray):
+    """Token index of sequences of tokens_per_seq tokens each (speculative decode).
+
+    The definition: sequence b owns tokens b*tps .. b*tps + tps - 1, every one of
+    them carrying the sequence's slot, so the index is the token index of the
+    slot ids repeated tps times (TensorRT-LLM LoRA serving page, "一次 decode 批次
+    的路由").  Returns (sorted_ids[n_seq*tps], seg_offsets[S+2], active[S+1], status)."""
+    tok = np.repeat(np.ascontiguousarray(seq_slot_ids, dtype=np.int32), int(tokens_per_seq))
+    return build_index(tok, S, ranks)
+
+
 # ----------------------------------------------------------------------------
 # Branch
 # ----------------------------------------------------------------------------

@@ -24,7 +24,7 @@ __all__ = [
     "LORA_NOALLOC_WS_BYTES",
     "LoraError", "lora_shape_t", "make_shape", "lora_abi_version", "lora_status_string", "lora_scale",
     "lora_premultiply", "lora_slot_table_bytes", "lora_pack_slot_table", "lora_set_slot_table",
-    "lora_build_index", "lora_workspace_bytes", "lora_workspace_xa_offset", "lora_shrink", "lora_expand", "lora_apply", "lora_resolve_path",
+    "lora_build_index", "lora_build_index_seq", "lora_workspace_bytes", "lora_workspace_xa_offset", "lora_shrink", "lora_expand", "lora_apply", "lora_resolve_path",
     "lora_apply_noalloc", "SlotTable", "TokenIndex", "Workspace",
 ]
 
@@ -202,6 +202,17 @@ def lora_resolve_path(path: str, T: int, max_seg_hint: int = 0):
 # ---------------------------------------------------------------------------
 # Caller-owned buffers (allocation only)
 # ---------------------------------------------------------------------------
+def lora_build_index_seq(seq_slot_ids, tokens_per_seq, S, dev_table, sorted_ids, seg_offsets, active, err,
+                         stream=None) -> None:
+    """Token index of n_seq sequences of tokens_per_seq tokens each (speculative decode)."""
+    torch = _torch()
+    _dev(seq_slot_ids, "seq_slot_ids", torch.int32)
+    n_seq = int(seq_slot_ids.numel())
+    check(load().lora_build_index_seq(_p(seq_slot_ids), n_seq, int(tokens_per_seq), int(S), _p(dev_table),
+                                      _p(sorted_ids), _p(seg_offsets), _p(active), _p(err), _stream(stream)),
+          "lora_build_index_seq")
+
+
 class SlotTable:
     """Device slot table plus the pinned staging buffer its upload copies from."""
 
@@ -231,6 +242,12 @@ class TokenIndex:
     def build(self, slot_ids, table: SlotTable, stream=None) -> None:
         lora_build_index(slot_ids, self.S, table.dev, self.sorted_ids, self.seg_offsets, self.active, self.err,
                          stream)
+
+    def build_seq(self, seq_slot_ids, tokens_per_seq: int, table: SlotTable, stream=None) -> None:
+        """Index for T = len(seq_slot_ids) * tokens_per_seq tokens, sequence-major."""
+        assert int(seq_slot_ids.numel()) * int(tokens_per_seq) == self.T
+        lora_build_index_seq(seq_slot_ids, tokens_per_seq, self.S, table.dev, self.sorted_ids, self.seg_offsets,
+                             self.active, self.err, stream)
 
 
 class Workspace:

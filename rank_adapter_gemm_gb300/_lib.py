@@ -40,7 +40,7 @@ EXPORTED = (
     "lora_abi_version", "lora_status_string", "lora_scale", "lora_premultiply",
     "lora_slot_table_bytes", "lora_pack_slot_table", "lora_set_slot_table", "lora_build_index",
     "lora_workspace_bytes", "lora_shrink", "lora_expand", "lora_apply", "lora_apply_ex",
-    "lora_resolve_path", "lora_apply_noalloc", "lora_workspace_xa_offset",
+    "lora_resolve_path", "lora_apply_noalloc", "lora_workspace_xa_offset", "lora_build_index_seq",
 )
 
 
@@ -90,6 +90,7 @@ def load() -> ctypes.CDLL:
         "lora_pack_slot_table": (ST, [P, I32, I32, I32, P, P, P, P]),
         "lora_set_slot_table": (ST, [P, P, I32, I32, I32, P, P, P, P, P]),
         "lora_build_index": (ST, [P, I32, I32, P, P, P, P, P, P]),
+        "lora_build_index_seq": (ST, [P, I32, I32, I32, P, P, P, P, P, P]),
         "lora_workspace_bytes": (ST, [I32, SH, ctypes.POINTER(SZ)]),
         "lora_workspace_xa_offset": (SZ, [SH]),
         "lora_shrink": (ST, [P, I64, I32, SH, P, P, P, P, P, SZ, P, P]),

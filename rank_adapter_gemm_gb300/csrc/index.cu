@@ -7,6 +7,13 @@
 // (slot -1) and out-of-range ids are keyed S, i.e. placed last, like
 // TensorRT-LLM's sentinel slot after the real ones.
 //
+// Speculative decoding (TensorRT-LLM LoRA serving page, "一次 decode 批次的路由":
+// tokens_per_seq > 1 expands the sequence order to the token order as
+// sorted * tokens_per_seq + arange(tokens_per_seq)): the keys are one per
+// sequence, sequence b owning tokens b tps .. b tps + tps - 1; the counts are
+// multiplied by tps and each sequence writes its tps token ids in a row.  With
+// tps = 1 this is the token-level sort.
+//
 // One thread block does the whole sort: histogram in shared memory, an
 // exclusive scan into the segment offsets, then a pass over the tokens in
 // blockDim-sized chunks in token order.  Inside a chunk, a token's place among
@@ -19,7 +26,7 @@ namespace lora {
 
 namespace {
 
-__global__ void build_index_kernel(const int32_t *__restrict__ slot_ids, int32_t T, int32_t S,
+__global__ void build_index_kernel(const int32_t *__restrict__ slot_ids, int32_t T, int32_t tps, int32_t S,
                                    const void *table, int32_t *__restrict__ sorted_ids,
                                    int32_t *__restrict__ seg_offsets, int32_t *__restrict__ active,
                                    int32_t *err) {
@@ -46,7 +53,7 @@ __global__ void build_index_kernel(const int32_t *__restrict__ slot_ids, int32_t
         int32_t s = slot_ids[t];
         int32_t key = (s >= 0 && s < S) ? s : S;
         bad |= (s < -1 || s >= S);
-        atomicAdd(&cursor[key], 1);
+        atomicAdd(&cursor[key], tps);
     }
     if (bad) report_error(err, LORA_ERR_SLOT_RANGE);
     __syncthreads();
@@ -67,7 +74,7 @@ __global__ void build_index_kernel(const int32_t *__restrict__ slot_ids, int32_t
     // 3. segment offsets
     block_exclusive_scan(cursor, bins, scratch);
     for (int b = tid; b < bins; b += nt) seg_offsets[b] = cursor[b];
-    if (tid == 0) seg_offsets[S + 1] = T;
+    if (tid == 0) seg_offsets[S + 1] = T * tps;
     __syncthreads();
 
     // 4. stable scatter, chunk by chunk in token order
@@ -88,11 +95,12 @@ __global__ void build_index_kernel(const int32_t *__restrict__ slot_ids, int32_t
         if (valid) {
             int32_t before = 0;
             for (int w = 0; w < warp; ++w) before += wcnt[key * nw + w];
-            sorted_ids[cursor[key] + before + in_warp] = t;
+            int32_t *dst = sorted_ids + cursor[key] + (before + in_warp) * tps;
+            for (int32_t j = 0; j < tps; ++j) dst[j] = t * tps + j;
         }
         __syncthreads();
         if (valid && leader) {
-            atomicAdd(&cursor[key], __popc(peers));
+            atomicAdd(&cursor[key], __popc(peers) * tps);
             wcnt[key * nw + warp] = 0;
         }
         __syncthreads();
@@ -106,7 +114,8 @@ size_t index_smem_bytes(int32_t S, int threads) {
     return sizeof(int32_t) * (size_t(S + 1) + size_t(S) + size_t(S + 1) * nw + 33);
 }
 
-cudaError_t launch_build_index(const int32_t *slot_ids, int32_t T, int32_t S, const void *table,
+// T keys (tokens, or sequences of tps tokens each).
+cudaError_t launch_build_index(const int32_t *slot_ids, int32_t T, int32_t tps, int32_t S, const void *table,
                                int32_t *sorted_ids, int32_t *seg_offsets, int32_t *active, int32_t *err,
                                cudaStream_t stream) {
     int threads = 1024;
@@ -124,7 +133,7 @@ cudaError_t launch_build_index(const int32_t *slot_ids, int32_t T, int32_t S, co
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    build_index_kernel<<<1, threads, smem, stream>>>(slot_ids, T, S, table, sorted_ids, seg_offsets,
+    build_index_kernel<<<1, threads, smem, stream>>>(slot_ids, T, tps, S, table, sorted_ids, seg_offsets,
                                                      active, err);
     return cudaGetLastError();
 }

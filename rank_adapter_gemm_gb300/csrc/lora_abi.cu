@@ -8,7 +8,7 @@
 #include "common.cuh"
 
 namespace lora {
-cudaError_t launch_build_index(const int32_t *slot_ids, int32_t T, int32_t S, const void *table,
+cudaError_t launch_build_index(const int32_t *slot_ids, int32_t T, int32_t tps, int32_t S, const void *table,
                                int32_t *sorted_ids, int32_t *seg_offsets, int32_t *active, int32_t *err,
                                cudaStream_t stream);
 cudaError_t launch_shrink(const uint16_t *x, int64_t ldx, const Shape &sh, const void *table,
@@ -214,8 +214,20 @@ lora_status_t lora_build_index(const int32_t *slot_ids, int32_t T, int32_t S, co
     if (T > 0 && (slot_ids == nullptr || sorted_ids == nullptr)) return LORA_ERR_INVALID_ARG;
     if (dev_table == nullptr || seg_offsets == nullptr || active == nullptr) return LORA_ERR_INVALID_ARG;
     if (!aligned16(dev_table)) return LORA_ERR_ALIGNMENT;
-    return from_cuda(lora::launch_build_index(slot_ids, T, S, dev_table, sorted_ids, seg_offsets, active, err,
+    return from_cuda(lora::launch_build_index(slot_ids, T, 1, S, dev_table, sorted_ids, seg_offsets, active, err,
                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_build_index_seq(const int32_t *seq_slot_ids, int32_t n_seq, int32_t tokens_per_seq, int32_t S,
+                                   const void *dev_table, int32_t *sorted_ids, int32_t *seg_offsets,
+                                   int32_t *active, int32_t *err, lora_stream_t stream) {
+    if (n_seq < 0 || tokens_per_seq < 1 || S < 1 || S > LORA_MAX_SLOTS) return LORA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(n_seq) * tokens_per_seq > INT32_MAX) return LORA_ERR_INVALID_ARG;
+    if (n_seq > 0 && (seq_slot_ids == nullptr || sorted_ids == nullptr)) return LORA_ERR_INVALID_ARG;
+    if (dev_table == nullptr || seg_offsets == nullptr || active == nullptr) return LORA_ERR_INVALID_ARG;
+    if (!aligned16(dev_table)) return LORA_ERR_ALIGNMENT;
+    return from_cuda(lora::launch_build_index(seq_slot_ids, n_seq, tokens_per_seq, S, dev_table, sorted_ids,
+                                              seg_offsets, active, err, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 lora_status_t lora_workspace_bytes(int32_t T, const lora_shape_t *shape, size_t *bytes) {

@@ -90,6 +90,64 @@ def test_index_fuzz(T, S, seed):
     _check_index(slot_ids, S, ranks)
 
 
+def _gpu_index_seq(seq_ids, tps, S, ranks):
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    T = len(seq_ids) * tps
+    tab = L.SlotTable(S, 1, 256)
+    dummy = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
+    ptrs = np.full(S, dummy.data_ptr(), dtype=np.uint64)
+    tab.set(np.asarray(ranks, np.int32), np.ones(S, np.float32), ptrs, ptrs)
+    idx = L.TokenIndex(T, S)
+    sid = torch.from_numpy(np.ascontiguousarray(seq_ids, dtype=np.int32)).cuda()
+    idx.build_seq(sid, tps, tab)
+    torch.cuda.synchronize()
+    return (idx.sorted_ids.cpu().numpy()[:T], idx.seg_offsets.cpu().numpy(), idx.active.cpu().numpy(),
+            int(idx.err.cpu().item()))
+
+
+@pytest.mark.parametrize("n_seq,tps,S,seed", [(0, 4, 3, 0), (1, 1, 1, 1), (64, 4, 32, 2), (37, 3, 5, 3),
+                                              (300, 8, 128, 4), (1024, 2, 17, 5), (5000, 3, 1024, 6)])
+def test_speculative_index_bit_exact(n_seq, tps, S, seed):
+    """Sequences of tps tokens (speculative decode): bit-exact against the oracle's
+    token index of the repeated slot ids, out-of-range ids included."""
+    rng = np.random.default_rng(seed)
+    seq = rng.integers(-1, S, size=n_seq).astype(np.int32)
+    if n_seq > 4:
+        seq[3] = S + 2  # out of range: keyed with the no-adapter bucket, error reported
+    ranks = rng.choice([0, 8, 16, 64], size=S).astype(np.int32)
+    so, seg, act, err = _gpu_index_seq(seq, tps, S, ranks)
+    so_r, seg_r, act_r, st_r = oracle.build_index_seq(seq, tps, S, ranks)
+    np.testing.assert_array_equal(so, so_r)
+    np.testing.assert_array_equal(seg, seg_r)
+    np.testing.assert_array_equal(act[:1 + act_r[0]], act_r[:1 + act_r[0]])
+    assert (err == 4) == (st_r == oracle.ERR_SLOT_RANGE)
+
+
+@pytest.mark.parametrize("path", ["auto", "decode_direct", "decode_split"])
+def test_apply_speculative_decode(path):
+    """Packed QKV (Llama-3-8B shapes) for 64 sequences of 4 draft tokens each:
+    index from the per-sequence slots, y against the oracle on the per-token slots."""
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import ResidentProjection, to_host_bits
+    wl = W.config(5)
+    tps = wl.tokens_per_seq
+    seq = np.ascontiguousarray(wl.slot_ids[::tps])
+    np.testing.assert_array_equal(np.repeat(seq, tps), wl.slot_ids)
+    rp = ResidentProjection.from_workload(wl)
+    idx = L.TokenIndex(wl.T, wl.S)
+    idx.build_seq(torch.from_numpy(seq).cuda(), tps, rp.table)
+    ws = L.Workspace(wl.T, rp.shape)
+    counts = np.bincount(seq[seq >= 0], minlength=wl.S) * tps
+    L.lora_apply(rp.x, rp.y, rp.shape, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active, ws.buf,
+                 idx.err, max_seg_hint=int(counts.max()), path=path)
+    torch.cuda.synchronize()
+    assert int(idx.err.item()) == 0
+    ref, _ = oracle_y(wl)
+    assert_y_close(to_host_bits(rp.y), ref, "speculative decode")
+
+
 def test_index_all_none_and_out_of_range():
     S = 4
     ranks = np.array([8, 8, 0, 16], np.int32)

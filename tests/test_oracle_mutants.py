@@ -9,6 +9,7 @@ import ctypes
 import os
 import subprocess
 
+import numpy as np
 import pytest
 
 import oracle
@@ -71,3 +72,21 @@ def test_pins_catch_planted_mistake(name, tmp_path, monkeypatch):
         except AssertionError:
             failures += 1
     assert failures > 0, f"no pin caught mutant {name}"
+
+
+# The speculative-decode index is a thin rule in oracle/__init__.py (token order
+# of sequences of tps tokens); plant the two plausible slips in that rule.
+SEQ_MUTANTS = {
+    # tokens interleaved across sequences instead of sequence-major
+    "tiled_tokens": lambda seq, tps, S, ranks: oracle.build_index(
+        np.tile(np.asarray(seq, np.int32), int(tps)), S, ranks),
+    # the sequence index reused without expanding it to tokens
+    "not_expanded": lambda seq, tps, S, ranks: oracle.build_index(np.asarray(seq, np.int32), S, ranks),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SEQ_MUTANTS))
+def test_pins_catch_planted_speculative_index_mistake(name, monkeypatch):
+    monkeypatch.setattr(oracle, "build_index_seq", SEQ_MUTANTS[name])
+    with pytest.raises(AssertionError):
+        pins.test_speculative_index_matches_pages_expansion(2, 4)

@@ -122,6 +122,35 @@ def test_index_layout_matches_pages():
         assert rows["active"][1] == "S+1" and len(active) == S + 1
 
 
+@pytest.mark.parametrize("seed,tps", [(0, 1), (1, 2), (2, 4), (3, 5), (4, 8)])
+def test_speculative_index_matches_pages_expansion(seed, tps):
+    """TensorRT-LLM LoRA serving page, "一次 decode 批次的路由": with tokens_per_seq
+    > 1 the sequence-level order is expanded to tokens as sorted * tps +
+    arange(tps), and the per-slot counts scale by tps.  The oracle's speculative
+    index (the token index of the repeated slot ids) must equal that expansion of
+    its sequence-level index."""
+    rng = np.random.default_rng(100 + seed)
+    S = int(rng.integers(1, 40))
+    n_seq = int(rng.integers(0, 300))
+    seq = rng.integers(-1, S, size=n_seq).astype(np.int32)
+    ranks = rng.choice([0, 8, 16, 64], size=S).astype(np.int32)
+    so_s, seg_s, act_s, st_s = oracle.build_index(seq, S, ranks)
+    so_t, seg_t, act_t, st_t = oracle.build_index_seq(seq, tps, S, ranks)
+    assert st_s == st_t == oracle.ERR_OK
+    want = (so_s.astype(np.int64)[:, None] * tps + np.arange(tps)).ravel()
+    np.testing.assert_array_equal(so_t, want)
+    np.testing.assert_array_equal(seg_t, seg_s * tps)
+    np.testing.assert_array_equal(act_t, act_s)
+
+
+def test_speculative_index_one_token_per_sequence_is_the_token_index():
+    rng = np.random.default_rng(7)
+    ids = rng.integers(-1, 16, size=500).astype(np.int32)
+    ranks = np.full(16, 8, np.int32)
+    for a, b in zip(oracle.build_index(ids, 16, ranks), oracle.build_index_seq(ids, 1, 16, ranks)):
+        np.testing.assert_array_equal(a, b)
+
+
 # ---------------------------------------------------------------------------
 # Branch value
 # ---------------------------------------------------------------------------

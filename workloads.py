@@ -109,6 +109,7 @@ class Workload:
     modules: List[Module]
     seed: int
     description: str = ""
+    tokens_per_seq: int = 1       # speculative decode: sequences of this many tokens, sequence-major
 
 
 # ----------------------------------------------------------------------------
@@ -148,7 +149,7 @@ def generate(*, name: str, seed: int, T: Optional[int], S: int,
              zipf_exponent: float = 1.1, alpha: Optional[float] = None,
              alpha_times_rank: Optional[float] = None, scale_rule: str = "alpha_over_r",
              premultiplied: bool = False, requests: Optional[Dict] = None,
-             y_init: str = "normal", description: str = "") -> Workload:
+             y_init: str = "normal", description: str = "", tokens_per_seq: int = 1) -> Workload:
     """Draw one workload.
 
     ``modules`` is a list of ``{"name", "k", "slices"}`` dicts.  Slots get either
@@ -156,7 +157,8 @@ def generate(*, name: str, seed: int, T: Optional[int], S: int,
     alpha of a slot is ``alpha`` or ``alpha_times_rank * r_s``.  ``requests``
     (``{"n", "min_len", "max_len", "n_adapters"}``) makes a request-major
     prefill batch: lengths uniform in [min_len, max_len], one adapter per request
-    drawn uniformly.
+    drawn uniformly.  ``tokens_per_seq`` > 1 draws one slot per sequence of that
+    many consecutive tokens (speculative decode; T must be a multiple).
     """
     rng = np.random.Generator(np.random.PCG64(seed))
     # 1. slot ids
@@ -166,8 +168,9 @@ def generate(*, name: str, seed: int, T: Optional[int], S: int,
         slot_ids = np.repeat(adapters, lens).astype(np.int32)
         T = int(slot_ids.shape[0])
     else:
-        assert T is not None
-        slot_ids = _draw_slot_ids(rng, T, S, slot_dist, frac_none, zipf_exponent)
+        assert T is not None and T % tokens_per_seq == 0
+        seq_ids = _draw_slot_ids(rng, T // tokens_per_seq, S, slot_dist, frac_none, zipf_exponent)
+        slot_ids = np.repeat(seq_ids, tokens_per_seq).astype(np.int32)
     # 2. ranks
     if rank_choices is not None:
         ranks = rng.choice(np.asarray(rank_choices), size=S).astype(np.int32)
@@ -199,7 +202,7 @@ def generate(*, name: str, seed: int, T: Optional[int], S: int,
         mods.append(Module(name=m["name"], k=k, slice_widths=widths, x=x, y_in=y_in, A=A, B=B))
     return Workload(name=name, T=int(T), S=S, r_max=int(r_max), slot_ids=slot_ids, ranks=ranks,
                     alphas=alphas, scale_rule=scale_rule, premultiplied=premultiplied,
-                    modules=mods, seed=seed, description=description)
+                    modules=mods, seed=seed, description=description, tokens_per_seq=int(tokens_per_seq))
 
 
 # ----------------------------------------------------------------------------
@@ -212,11 +215,11 @@ LLAMA3_8B_LAYER = [
     {"name": "down", "k": 14336, "slices": [4096]},
 ]
 
-CONFIG_NAMES = ("tiny", "decode_q_proj", "decode_qkv", "prefill_mlp", "large_decode")
+CONFIG_NAMES = ("tiny", "decode_q_proj", "decode_qkv", "prefill_mlp", "large_decode", "decode_qkv_spec")
 
 
 def config(index: int, y_init: str = "normal", sweep: bool = False, n_requests: int = 16) -> Workload:
-    """Config ``index`` (0..4) of the benchmark suite, drawn at seed 1000+index.
+    """Config ``index`` (0..5) of the benchmark suite, drawn at seed 1000+index.
 
     0 tiny: T=8, k=d=256, one slice, S=2, r=8, slot ids uniform over {-1,0,1},
       alpha=16 (scale alpha/r applied at run time).
@@ -233,6 +236,9 @@ def config(index: int, y_init: str = "normal", sweep: bool = False, n_requests: 
       of tokens at -1, alpha=2r.  ``sweep=True`` instead draws the four packed
       projections of one Llama-3-8B layer (qkv, o, gate_up, down) on the same
       slot draw.
+    5 speculative decode, packed QKV (Llama-3-8B shapes): 64 sequences of 4
+      tokens (one verified plus three draft tokens, T=256), one slot per sequence
+      with Zipf(1.1) popularity over S=32, ranks from {8,16,32,64}, alpha=2r.
     """
     seed = 1000 + index
     if index == 0:
@@ -266,4 +272,10 @@ def config(index: int, y_init: str = "normal", sweep: bool = False, n_requests: 
                         T=1024, S=128, rank=64, modules=mods, slot_dist="zipf",
                         frac_none=0.05, alpha_times_rank=2.0, y_init=y_init,
                         description="T=1024, r=64, S=128, Zipf(1.1), 5% at -1")
+    if index == 5:
+        return generate(name="decode_qkv_spec", seed=seed, T=256, S=32, rank_choices=RANK_CHOICES,
+                        r_max=64, modules=[LLAMA3_8B_LAYER[0]], slot_dist="zipf",
+                        alpha_times_rank=2.0, y_init=y_init, tokens_per_seq=4,
+                        description="64 sequences x 4 tokens (speculative decode), k=4096, "
+                                    "slices 4096/1024/1024, S=32, r in {8,16,32,64}, Zipf(1.1) per sequence")
     raise IndexError(index)
