@@ -57,6 +57,9 @@ def parse_args(argv=None):
     p.add_argument("--path", default="auto", choices=["auto", "decode_fused", "decode_split", "prefill", "decode_tc", "decode_stream", "decode_direct"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--with-base", default="none", choices=["none", "serial", "overlap"],
+                   help="time the base projection y = x W0^T (bf16 library GEMM) with the branch: one after the "
+                        "other on one stream, or the branch on an aux stream overlapping the GEMM")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-baseline sample")
     return p.parse_args(argv)
 
@@ -282,8 +285,22 @@ def run_ours(args):
     ws = [L.Workspace(T, lay.shape, device=dev) for lay in layers[:len(base)]]
     ws_of = [ws[l % len(ws)].buf for l in range(len(layers))]
 
+    w0 = []
+    if args.with_base != "none":
+        g = torch.Generator(device=dev).manual_seed(1234)
+        for lay in layers:
+            d = int(sum(lay.widths)) if hasattr(lay, "widths") else int(lay.y.shape[1])
+            w0.append((torch.randn(d, lay.x.shape[1], device=dev, generator=g) * 0.02).to(torch.bfloat16))
+    aux = torch.cuda.Stream(device=dev)
+
     def apply_layer(l):
         lay = layers[l]
+        if args.with_base == "overlap":
+            L.apply_with_base(lay.x, w0[l], lay.y, lay.shape, lay.table.dev, index, ws_of[l], aux,
+                              max_seg_hint=max_seg, path=args.path)
+            return
+        if args.with_base == "serial":
+            torch.matmul(lay.x, w0[l].t(), out=lay.y)
         L.lora_apply(lay.x, lay.y, lay.shape, lay.table.dev, index.sorted_ids, index.seg_offsets, index.active,
                      ws_of[l], index.err, max_seg_hint=max_seg, path=args.path)
 
@@ -357,6 +374,10 @@ def run_ours(args):
                       for m in mods]
     flops_per_call = [algorithmic_flops(wl.slot_ids, wl.ranks, wl.modules[m].k, wl.modules[m].slice_widths)
                       for m in mods]
+    if args.with_base != "none":  # the base GEMM's W0, x and y bytes too
+        bytes_per_call = [b + 2 * wl.modules[m].k * sum(wl.modules[m].slice_widths)
+                          + 2 * T * (wl.modules[m].k + sum(wl.modules[m].slice_widths))
+                          for b, m in zip(bytes_per_call, mods)]
     per_layer_bytes = [bytes_per_call[l % len(mods)] for l in range(len(layers))]
     per_layer_flops = [flops_per_call[l % len(mods)] for l in range(len(layers))]
     call_s = apply_ms_mean / 1e3 / len(layers)
@@ -365,7 +386,7 @@ def run_ours(args):
     gpu_launches = args.steps * (1 + len(layers) * launches_per_apply)
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.with_base == "none":
         e2e = run_e2e(args, wl, layers, index, slot_dev, ws_of, max_seg, dev, world)
 
     cpu = None
@@ -397,6 +418,10 @@ def run_ours(args):
             "l2": f"inputs larger than L2: {len(layers)} distinct layer buffer sets, "
                   f"{sum(per_layer_bytes) / 1e9:.2f} GB of algorithmic bytes per step",
             "parallelism": f"replicas x{world}",
+            **({"base": "bf16 library GEMM y = x W0^T, then the branch on the same stream"
+                if args.with_base == "serial" else
+                "bf16 library GEMM y = x W0^T, the branch on an aux stream: its shrink overlaps the GEMM"}
+               if args.with_base != "none" else {}),
         },
         "gbs": achieved_gbs,
         "roofline": {
@@ -407,7 +432,8 @@ def run_ours(args):
             "frac": achieved_gbs / peak_gbs,
             "traffic": call_traffic(args.config, resolved),
             "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
-            "kernel": "lora_apply (shrink + expand) per projection call",
+            "kernel": ("lora_apply (shrink + expand) per projection call" if args.with_base == "none" else
+                       "base GEMM + lora_apply per projection call"),
             "bytes_per_call": sum(per_layer_bytes) / len(layers),
             "flops_per_call": sum(per_layer_flops) / len(layers),
             "us_per_call": call_s * 1e6,

@@ -303,6 +303,32 @@ lora_status_t lora_apply_ex(const void *x, int64_t ldx, void *y, int64_t ldy, in
                             float *ws, size_t ws_bytes, int32_t *err, lora_stream_t stream);
 
 /*
+ * The branch overlapped with the producer of y (TensorRT-LLM LoRA serving page,
+ * section "与基座并行:forward_with_base": the LoRA branch runs on an auxiliary
+ * stream next to the base projection y = x W0^T and the two join on events).
+ * Same arguments and result as lora_apply_ex, plus:
+ *   y_ready   a CUDA event (cudaEvent_t) the caller records once y holds its
+ *             input values (e.g. after the base GEMM on another stream), or
+ *             null when y is already ready on `stream`.
+ * On `stream`, the x-only half of the branch (the shrink: reads x, A and the
+ * index, writes the workspace) is launched first, then the stream waits for
+ * y_ready, then the half that reads and writes y (the expand).  So the shrink
+ * runs while the other stream computes y, and y is touched only after it is
+ * ready.  The two-kernel decode paths (LORA_PATH_DECODE_DIRECT,
+ * LORA_PATH_DECODE_SPLIT, and LORA_PATH_AUTO where it picks them) split this
+ * way; on the other paths the stream waits for y_ready before the whole call.
+ * The caller joins `stream` back (an event) before using y.  Nothing is
+ * allocated; host checks and errors as lora_apply_ex.  The event must stay
+ * valid until the call's work has run.
+ */
+typedef void *lora_event_t;
+lora_status_t lora_apply_overlap(const void *x, int64_t ldx, void *y, int64_t ldy, int32_t T,
+                                 const lora_shape_t *shape, const void *dev_table, const int32_t *sorted_ids,
+                                 const int32_t *seg_offsets, const int32_t *active, int32_t max_seg_hint,
+                                 lora_path_t path, float *ws, size_t ws_bytes, int32_t *err, lora_stream_t stream,
+                                 lora_event_t y_ready);
+
+/*
  * lora_apply without a workspace argument, for callers that cannot allocate
  * device memory where they run the branch: for example a plug-in inside a host
  * engine that owns all device memory through its own pool and gives plug-ins no

@@ -25,7 +25,7 @@ __all__ = [
     "LoraError", "lora_shape_t", "make_shape", "lora_abi_version", "lora_status_string", "lora_scale",
     "lora_premultiply", "lora_slot_table_bytes", "lora_pack_slot_table", "lora_set_slot_table",
     "lora_build_index", "lora_build_index_seq", "lora_workspace_bytes", "lora_workspace_xa_offset", "lora_shrink", "lora_expand", "lora_apply", "lora_resolve_path",
-    "lora_apply_noalloc", "SlotTable", "TokenIndex", "Workspace",
+    "lora_apply_noalloc", "lora_apply_overlap", "apply_with_base", "SlotTable", "TokenIndex", "Workspace",
 ]
 
 
@@ -176,6 +176,42 @@ def lora_apply(x, y, shape, dev_table, sorted_ids, seg_offsets, active, ws, err,
         check(load().lora_apply(*args, *tail), "lora_apply")
     else:
         check(load().lora_apply_ex(*args, PATHS[path], *tail), "lora_apply_ex")
+
+
+def lora_apply_overlap(x, y, shape, dev_table, sorted_ids, seg_offsets, active, ws, err, y_ready=None,
+                       max_seg_hint: int = 0, path: str = "auto", stream=None) -> None:
+    """lora_apply on `stream` whose y half waits for the event `y_ready`
+    (a torch.cuda.Event recorded once y holds its input values)."""
+    ldx = _rows(x, "x")
+    ldy = _rows(y, "y")
+    if x.shape[0] != y.shape[0]:
+        raise ValueError("x and y must have the same number of rows")
+    ev = ctypes.c_void_p(y_ready.cuda_event) if y_ready is not None else None
+    check(load().lora_apply_overlap(_p(x), ldx, _p(y), ldy, int(x.shape[0]), ctypes.byref(shape), _p(dev_table),
+                                    _p(sorted_ids), _p(seg_offsets), _p(active), int(max_seg_hint), PATHS[path],
+                                    _p(ws), ws.numel() * ws.element_size(), _p(err), _stream(stream), ev),
+          "lora_apply_overlap")
+
+
+def apply_with_base(x, w0, y, shape, dev_table, index, ws, aux_stream, max_seg_hint: int = 0,
+                    path: str = "auto") -> None:
+    """y = x w0^T + branch, the base projection (a bf16 library GEMM) on the
+    current stream and the branch on `aux_stream`: the branch's x-only half
+    overlaps the GEMM, its y half runs once the GEMM has written y, and the
+    current stream waits for the branch before it goes on."""
+    torch = _torch()
+    main = torch.cuda.current_stream()
+    x_ready = torch.cuda.Event()
+    x_ready.record(main)
+    aux_stream.wait_event(x_ready)
+    torch.matmul(x, w0.t(), out=y)
+    y_ready = torch.cuda.Event()
+    y_ready.record(main)
+    lora_apply_overlap(x, y, shape, dev_table, index.sorted_ids, index.seg_offsets, index.active, ws, index.err,
+                       y_ready=y_ready, max_seg_hint=max_seg_hint, path=path, stream=aux_stream)
+    done = torch.cuda.Event()
+    done.record(aux_stream)
+    main.wait_event(done)
 
 
 def lora_apply_noalloc(x, y, shape, dev_table, sorted_ids, seg_offsets, active, err, stream=None) -> None:

@@ -41,6 +41,7 @@ EXPORTED = (
     "lora_slot_table_bytes", "lora_pack_slot_table", "lora_set_slot_table", "lora_build_index",
     "lora_workspace_bytes", "lora_shrink", "lora_expand", "lora_apply", "lora_apply_ex",
     "lora_resolve_path", "lora_apply_noalloc", "lora_workspace_xa_offset", "lora_build_index_seq",
+    "lora_apply_overlap",
 )
 
 
@@ -97,6 +98,7 @@ def load() -> ctypes.CDLL:
         "lora_expand": (ST, [P, SZ, P, I64, I32, SH, P, P, P, P, P, P]),
         "lora_apply": (ST, [P, I64, P, I64, I32, SH, P, P, P, P, I32, P, SZ, P, P]),
         "lora_apply_ex": (ST, [P, I64, P, I64, I32, SH, P, P, P, P, I32, ST, P, SZ, P, P]),
+        "lora_apply_overlap": (ST, [P, I64, P, I64, I32, SH, P, P, P, P, I32, ST, P, SZ, P, P, P]),
         "lora_resolve_path": (ST, [ST, I32, I32, ctypes.POINTER(I32)]),
         "lora_apply_noalloc": (ST, [P, I64, P, I64, I32, SH, P, P, P, P, P, P]),
     }

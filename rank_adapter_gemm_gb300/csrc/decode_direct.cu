@@ -954,25 +954,20 @@ bool decode_direct_supported(int32_t T, const Shape &sh) {
            direct_shrink_smem(sh.S, sh.n, T) <= 227 * 1024 && direct_expand_smem(sh.S, sh.n, T) <= 227 * 1024;
 }
 
-cudaError_t launch_decode_direct(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
-                                 const void *table, const int32_t *sorted_ids, const int32_t *seg,
-                                 const int32_t *active, float *ws, int32_t T, int32_t *err, cudaStream_t stream) {
+namespace {
+
+cudaError_t direct_args(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
+                        const int32_t *sorted_ids, const int32_t *seg, const int32_t *active, float *ws, int32_t T,
+                        int32_t *err, DArgs &a, int &num_sms) {
     if (!decode_direct_supported(T, sh)) return cudaErrorNotSupported;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    int num_sms = 0;
     e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    const size_t s_smem = direct_shrink_smem(sh.S, sh.n, T), e_smem = direct_expand_smem(sh.S, sh.n, T);
-    e = cudaFuncSetAttribute(direct_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s_smem));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(direct_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(e_smem));
     if (e != cudaSuccess) return e;
     const WorkspaceLayout W(T, sh.n, sh.r_max, sh.S);
     char *base = reinterpret_cast<char *>(ws);
     int32_t *ctrl = reinterpret_cast<int32_t *>(base);
-    DArgs a;
     a.x = x;
     a.ldx = ldx;
     a.y = y;
@@ -986,25 +981,65 @@ cudaError_t launch_decode_direct(const uint16_t *x, int64_t ldx, uint16_t *y, in
     a.exits = a.gen + 1;
     a.err = err;
     a.T = T;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+// The x-only half: sums of x A^T into the call's buffer (reads x, A; writes the
+// workspace only).
+cudaError_t launch_direct_shrink(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
+                                 const void *table, const int32_t *sorted_ids, const int32_t *seg,
+                                 const int32_t *active, float *ws, int32_t T, int32_t *err, cudaStream_t stream) {
+    DArgs a;
+    int num_sms = 0;
+    cudaError_t e = direct_args(x, ldx, y, ldy, sh, sorted_ids, seg, active, ws, T, err, a, num_sms);
+    if (e != cudaSuccess) return e;
+    const size_t s_smem = direct_shrink_smem(sh.S, sh.n, T);
+    e = cudaFuncSetAttribute(direct_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s_smem));
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(num_sms));
     cfg.blockDim = dim3(32 * kSWarps);
     cfg.dynamicSmemBytes = s_smem;
     cfg.stream = stream;
     cfg.numAttrs = 0;
-    e = cudaLaunchKernelEx(&cfg, direct_shrink_kernel, a, sh, table);
+    return cudaLaunchKernelEx(&cfg, direct_shrink_kernel, a, sh, table);
+}
+
+// The y half: y += s (x A^T) B^T from the buffer the shrink of this call filled.
+// `programmatic`: launched as a programmatic dependent of that shrink (it must
+// then directly follow it on the stream).
+cudaError_t launch_direct_expand(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
+                                 const void *table, const int32_t *sorted_ids, const int32_t *seg,
+                                 const int32_t *active, float *ws, int32_t T, int32_t *err, bool programmatic,
+                                 cudaStream_t stream) {
+    DArgs a;
+    int num_sms = 0;
+    cudaError_t e = direct_args(x, ldx, y, ldy, sh, sorted_ids, seg, active, ws, T, err, a, num_sms);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg2 = {};
-    cfg2.gridDim = dim3(static_cast<unsigned>(num_sms));
-    cfg2.blockDim = dim3(32 * kEWarps);
-    cfg2.dynamicSmemBytes = e_smem;
-    cfg2.stream = stream;
+    const size_t e_smem = direct_expand_smem(sh.S, sh.n, T);
+    e = cudaFuncSetAttribute(direct_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(e_smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(num_sms));
+    cfg.blockDim = dim3(32 * kEWarps);
+    cfg.dynamicSmemBytes = e_smem;
+    cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg2.attrs = attr;
-    cfg2.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg2, direct_expand_kernel, a, sh, table);
+    cfg.attrs = attr;
+    cfg.numAttrs = programmatic ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, direct_expand_kernel, a, sh, table);
+}
+
+cudaError_t launch_decode_direct(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
+                                 const void *table, const int32_t *sorted_ids, const int32_t *seg,
+                                 const int32_t *active, float *ws, int32_t T, int32_t *err, cudaStream_t stream) {
+    cudaError_t e = launch_direct_shrink(x, ldx, y, ldy, sh, table, sorted_ids, seg, active, ws, T, err, stream);
+    if (e != cudaSuccess) return e;
+    return launch_direct_expand(x, ldx, y, ldy, sh, table, sorted_ids, seg, active, ws, T, err, true, stream);
 }
 
 }  // namespace lora

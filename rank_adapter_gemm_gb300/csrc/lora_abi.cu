@@ -32,6 +32,13 @@ cudaError_t launch_decode_tc(const uint16_t *x, int64_t ldx, uint16_t *y, int64_
                             int32_t *err, cudaStream_t stream);
 bool fused_decode_supported(int32_t T, int32_t r_max, int32_t k);
 bool decode_direct_supported(int32_t T, const Shape &sh);
+cudaError_t launch_direct_shrink(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
+                                 const void *table, const int32_t *sorted_ids, const int32_t *seg,
+                                 const int32_t *active, float *ws, int32_t T, int32_t *err, cudaStream_t stream);
+cudaError_t launch_direct_expand(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
+                                 const void *table, const int32_t *sorted_ids, const int32_t *seg,
+                                 const int32_t *active, float *ws, int32_t T, int32_t *err, bool programmatic,
+                                 cudaStream_t stream);
 cudaError_t launch_decode_direct(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                  const void *table, const int32_t *sorted_ids, const int32_t *seg,
                                  const int32_t *active, float *ws, int32_t T, int32_t *err, cudaStream_t stream);
@@ -339,6 +346,46 @@ lora_status_t lora_apply_ex(const void *x, int64_t ldx, void *y, int64_t ldy, in
     default:
         return LORA_ERR_INVALID_ARG;
     }
+}
+
+lora_status_t lora_apply_overlap(const void *x, int64_t ldx, void *y, int64_t ldy, int32_t T,
+                                 const lora_shape_t *shape, const void *dev_table, const int32_t *sorted_ids,
+                                 const int32_t *seg_offsets, const int32_t *active, int32_t max_seg_hint,
+                                 lora_path_t path, float *ws, size_t ws_bytes, int32_t *err, lora_stream_t stream,
+                                 lora_event_t y_ready) {
+    Shape sh;
+    lora_status_t st;
+    if (T < 0) return LORA_ERR_INVALID_ARG;
+    if ((st = check_shape(shape, &sh)) != LORA_OK) return st;
+    if ((st = check_index_ptrs(dev_table, sorted_ids, seg_offsets, active, T)) != LORA_OK) return st;
+    if ((st = check_rows(x, ldx, T, sh.k)) != LORA_OK) return st;
+    if ((st = check_rows(y, ldy, T, sh.off[sh.n])) != LORA_OK) return st;
+    if ((st = check_ws(ws, ws_bytes, T, sh)) != LORA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaEvent_t ev = reinterpret_cast<cudaEvent_t>(y_ready);
+    if (max_seg_hint <= 0 || max_seg_hint > T) max_seg_hint = T;
+    const lora_path_t p = T == 0 ? LORA_PATH_DECODE_SPLIT : resolve(path, T, max_seg_hint, sh, nullptr);
+    const uint16_t *xb = static_cast<const uint16_t *>(x);
+    uint16_t *yb = static_cast<uint16_t *>(y);
+    if (T > 0 && p == LORA_PATH_DECODE_DIRECT && lora::decode_direct_supported(T, sh)) {
+        if (lora::launch_direct_shrink(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, active, ws, T, err,
+                                       s) != cudaSuccess)
+            return LORA_ERR_CUDA;
+        if (ev != nullptr && cudaStreamWaitEvent(s, ev, 0) != cudaSuccess) return LORA_ERR_CUDA;
+        return from_cuda(lora::launch_direct_expand(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, active,
+                                                    ws, T, err, false, s));
+    }
+    if (T > 0 && p == LORA_PATH_DECODE_SPLIT) {
+        float *xa = xa_of(ws, T, sh);
+        if (lora::launch_shrink(xb, ldx, sh, dev_table, sorted_ids, seg_offsets, xa, T, err, false, s) != cudaSuccess)
+            return LORA_ERR_CUDA;
+        if (ev != nullptr && cudaStreamWaitEvent(s, ev, 0) != cudaSuccess) return LORA_ERR_CUDA;
+        return from_cuda(lora::launch_expand(xa, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, T, err, false, s));
+    }
+    // one-launch and tensor-core paths: y is ready before any of their work
+    if (ev != nullptr && cudaStreamWaitEvent(s, ev, 0) != cudaSuccess) return LORA_ERR_CUDA;
+    return lora_apply_ex(x, ldx, y, ldy, T, shape, dev_table, sorted_ids, seg_offsets, active, max_seg_hint, p, ws,
+                         ws_bytes, err, stream);
 }
 
 lora_status_t lora_apply(const void *x, int64_t ldx, void *y, int64_t ldy, int32_t T, const lora_shape_t *shape,

@@ -552,3 +552,35 @@ def test_rank_above_r_max_is_rejected_on_device():
     y = to_host_bits(rp.y)
     rows0 = wl.slot_ids == 0
     np.testing.assert_array_equal(y[rows0], wl.modules[0].y_in[rows0])
+
+
+@pytest.mark.parametrize("path", ["auto", "decode_split", "decode_fused"])
+def test_apply_with_base_on_aux_stream(path):
+    """y = x W0^T + branch with the branch on an auxiliary stream next to the base
+    GEMM (TensorRT-LLM LoRA serving page, "与基座并行:forward_with_base"): the
+    branch's x-only half overlaps the GEMM and its y half waits for the GEMM's
+    event.  Reference: the oracle on top of the GPU's own base-GEMM output."""
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import ResidentProjection, to_host_bits
+    wl = W.config(2)
+    rp = ResidentProjection.from_workload(wl)
+    d = sum(wl.modules[0].slice_widths)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    w0 = (torch.randn(d, wl.modules[0].k, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+    idx = L.TokenIndex(wl.T, wl.S)
+    idx.build(torch.from_numpy(wl.slot_ids).cuda(), rp.table)
+    ws = L.Workspace(wl.T, rp.shape)
+    counts = np.bincount(wl.slot_ids[wl.slot_ids >= 0], minlength=wl.S)
+    x = rp.x.view(torch.bfloat16)
+    y = rp.y.view(torch.bfloat16)
+    base = torch.matmul(x, w0.t())
+    torch.cuda.synchronize()
+    base_bits = to_host_bits(base)
+    aux = torch.cuda.Stream()
+    y.fill_(7.0)  # overwritten by the base GEMM before the branch touches it
+    L.apply_with_base(x, w0, y, rp.shape, rp.table.dev, idx, ws.buf, aux, max_seg_hint=int(counts.max()), path=path)
+    torch.cuda.synchronize()
+    assert int(idx.err.item()) == 0
+    ref, _ = oracle_y(wl, y_in=base_bits)
+    assert_y_close(to_host_bits(rp.y), ref, f"with base ({path})")
