@@ -59,6 +59,14 @@ def configure(lib):
     lib.oracle_shrink.argtypes = [P, i64, i32, i32, P, i32, P, P, P, i32, i32, P, P]
     lib.oracle_apply.restype = ctypes.c_int
     lib.oracle_apply.argtypes = [P, i64, P, i64, i32, i32, P, P, i32, P, P, P, P, P, i32, P, P]
+    lib.oracle_e4m3_to_double.restype = f64
+    lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_round.restype = ctypes.c_uint8
+    lib.oracle_e4m3_round.argtypes = [f64]
+    lib.oracle_premultiply_e4m3.restype = None
+    lib.oracle_premultiply_e4m3.argtypes = [P, i64, f64, P]
+    lib.oracle_apply_e4m3.restype = ctypes.c_int
+    lib.oracle_apply_e4m3.argtypes = [P, i64, P, i64, i32, i32, P, P, i32, P, P, P, P, P, i32, P]
     return lib
 
 
@@ -73,10 +81,10 @@ def _ptr(a: Optional[np.ndarray]):
     return None if a is None else ctypes.c_void_p(a.ctypes.data)
 
 
-def _ptr_table(mats: Sequence[Sequence[Optional[np.ndarray]]]):
+def _ptr_table(mats: Sequence[Sequence[Optional[np.ndarray]]], dtype=np.uint16):
     """[S][n] arrays -> (ctypes array of S*n pointers, keep-alive list)."""
     flat = [m for row in mats for m in row]
-    keep = [np.ascontiguousarray(m, dtype=np.uint16) if m is not None else None for m in flat]
+    keep = [np.ascontiguousarray(m, dtype=dtype) if m is not None else None for m in flat]
     arr = (ctypes.c_void_p * max(1, len(keep)))()
     for e, m in enumerate(keep):
         arr[e] = None if m is None else m.ctypes.data
@@ -121,6 +129,57 @@ def premultiply(b_bits: np.ndarray, s: float) -> np.ndarray:
     out = np.empty_like(src)
     _load().oracle_premultiply(_ptr(src), int(src.size), float(s), _ptr(out))
     return out
+
+
+# ----------------------------------------------------------------------------
+# FP8 (float8_e4m3fn) adapters
+# ----------------------------------------------------------------------------
+def e4m3_to_double(codes: np.ndarray) -> np.ndarray:
+    lib = _load()
+    flat = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib.oracle_e4m3_to_double(int(c)) for c in flat], dtype=np.float64).reshape(np.shape(codes))
+
+
+def e4m3_round(values: np.ndarray) -> np.ndarray:
+    """v.clamp(-448, 448).to(float8_e4m3fn) codes (nearest, ties to even)."""
+    lib = _load()
+    flat = np.asarray(values, dtype=np.float64).ravel()
+    return np.array([lib.oracle_e4m3_round(float(v)) for v in flat], dtype=np.uint8).reshape(np.shape(values))
+
+
+def premultiply_e4m3(b_codes: np.ndarray, s: float) -> np.ndarray:
+    """The pages' load-time scale of FP8 B: (b.to(bf16) * s).clamp(+-448).to(fp8)."""
+    src = np.ascontiguousarray(b_codes, dtype=np.uint8)
+    out = np.empty_like(src)
+    _load().oracle_premultiply_e4m3(_ptr(src), int(src.size), float(s), _ptr(out))
+    return out
+
+
+def apply_e4m3(x: np.ndarray, y_in: Optional[np.ndarray], slice_widths: Sequence[int],
+               slot_ids: np.ndarray, ranks: np.ndarray, scales: np.ndarray,
+               A: Sequence[Sequence[Optional[np.ndarray]]], B: Sequence[Sequence[Optional[np.ndarray]]],
+               rows: Optional[np.ndarray] = None):
+    """Branch rows (fp64) with x rounded to e4m3 and A, B given as e4m3 codes;
+    returns (y[len(rows), d], status)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    slot_ids = np.ascontiguousarray(slot_ids, dtype=np.int32)
+    ranks = np.ascontiguousarray(ranks, dtype=np.int32)
+    scales = np.ascontiguousarray(scales, dtype=np.float64)
+    T, k = x.shape
+    widths = [int(w) for w in slice_widths]
+    offs = np.zeros(len(widths) + 1, dtype=np.int32)
+    offs[1:] = np.cumsum(widths)
+    d = int(offs[-1])
+    if y_in is not None:
+        y_in = np.ascontiguousarray(y_in, dtype=np.uint16)
+    rows = np.arange(T, dtype=np.int32) if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+    out = np.zeros((len(rows), d), dtype=np.float64)
+    ta, ka = _ptr_table(A, np.uint8)
+    tb, kb = _ptr_table(B, np.uint8)
+    st = _load().oracle_apply_e4m3(_ptr(x), k, _ptr(y_in), d, k, len(widths), _ptr(offs), _ptr(slot_ids),
+                                   len(ranks), _ptr(ranks), _ptr(scales), ta, tb, _ptr(rows), len(rows), _ptr(out))
+    del ka, kb
+    return out, int(st)
 
 
 # ----------------------------------------------------------------------------

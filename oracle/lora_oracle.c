@@ -234,3 +234,97 @@ int oracle_apply(const uint16_t *x, int64_t ldx, const uint16_t *y_in, int64_t l
     free(xa);
     return status;
 }
+
+/*
+ * FP8 adapters (TensorRT-LLM LoRA serving page, §"第五步:FP8 特判" and the
+ * "data_type" check at the start of the forward pass): the adapter weights stay
+ * in float8_e4m3fn, the runtime activation x is clamped to the FP8 range and
+ * converted to it, and the branch then multiplies FP8 values.
+ *
+ * float8_e4m3fn: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; no
+ * infinities; S.1111.111 is NaN; exponent 0 holds the subnormals m * 2^-9; the
+ * largest finite value is 448.
+ */
+double oracle_e4m3_to_double(uint8_t code)
+{
+    int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = m * ldexp(1.0, -9);
+    else v = (1.0 + m / 8.0) * ldexp(1.0, e - 7);
+    return sign ? -v : v;
+}
+
+/*
+ * x.clamp(-448, 448).to(float8_e4m3fn): the finite code nearest to the clamped
+ * value, ties to the code with an even mantissa; found by comparing against
+ * every non-negative finite code (0x00 .. 0x7E).
+ */
+uint8_t oracle_e4m3_round(double v)
+{
+    if (isnan(v)) return 0x7F;
+    int neg = signbit(v) != 0;
+    double a = fabs(v);
+    if (a > 448.0) a = 448.0;
+    int best = 0;
+    double best_d = a;
+    for (int c = 1; c <= 0x7E; ++c) {
+        double d = fabs(oracle_e4m3_to_double((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) { best = c; best_d = d; }
+    }
+    return (uint8_t)(best | (neg ? 0x80 : 0));
+}
+
+/* The pages' load-time scale for FP8 B: (b.to(bf16) * s).clamp(-448, 448).to(fp8),
+ * the product rounded to bf16 first. */
+void oracle_premultiply_e4m3(const uint8_t *b, int64_t n, double s, uint8_t *out)
+{
+    for (int64_t e = 0; e < n; ++e)
+        out[e] = oracle_e4m3_round(bf16_value(oracle_round_bf16(oracle_e4m3_to_double(b[e]) * s)));
+}
+
+/*
+ * oracle_apply with FP8 operands: every x value is rounded to e4m3 as above
+ * before the shrink; A and B hold e4m3 codes.  Sums and y as in oracle_apply.
+ */
+int oracle_apply_e4m3(const uint16_t *x, int64_t ldx, const uint16_t *y_in, int64_t ldy,
+                      int32_t k, int32_t n_slices, const int32_t *slice_offsets,
+                      const int32_t *slot_ids, int32_t S, const int32_t *ranks, const double *scales,
+                      const uint8_t *const *A, const uint8_t *const *B,
+                      const int32_t *rows, int32_t n_rows, double *y_out)
+{
+    int status = ORACLE_OK;
+    int32_t d = slice_offsets[n_slices];
+    double *xq = (double *)malloc(sizeof(double) * (size_t)k);
+    for (int32_t q = 0; q < n_rows; ++q) {
+        int32_t t = rows[q];
+        double *yo = y_out + (int64_t)q * d;
+        for (int32_t m = 0; m < d; ++m) yo[m] = y_in ? bf16_value(y_in[(int64_t)t * ldy + m]) : 0.0;
+        int32_t s = slot_ids[t];
+        if (s != -1 && (s < 0 || s >= S)) { status = ORACLE_ERR_SLOT_RANGE; continue; }
+        if (s < 0 || ranks[s] <= 0) continue;
+        int32_t r = ranks[s];
+        for (int32_t c = 0; c < k; ++c)
+            xq[c] = oracle_e4m3_to_double(oracle_e4m3_round(bf16_value(x[(int64_t)t * ldx + c])));
+        double *xa = (double *)malloc(sizeof(double) * (size_t)r);
+        for (int32_t i = 0; i < n_slices; ++i) {
+            const uint8_t *a = A[(int64_t)s * n_slices + i];
+            const uint8_t *b = B[(int64_t)s * n_slices + i];
+            for (int32_t j = 0; j < r; ++j) {
+                double acc = 0.0;
+                for (int32_t c = 0; c < k; ++c) acc += xq[c] * oracle_e4m3_to_double(a[(int64_t)j * k + c]);
+                xa[j] = acc;
+            }
+            int32_t o = slice_offsets[i];
+            int32_t di = slice_offsets[i + 1] - slice_offsets[i];
+            for (int32_t m = 0; m < di; ++m) {
+                double acc = 0.0;
+                for (int32_t j = 0; j < r; ++j) acc += xa[j] * oracle_e4m3_to_double(b[(int64_t)m * r + j]);
+                yo[o + m] += scales[s] * acc;
+            }
+        }
+        free(xa);
+    }
+    free(xq);
+    return status;
+}

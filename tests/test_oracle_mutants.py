@@ -33,6 +33,11 @@ MUTANTS = {
     "alpha_zero_not_special": ("if (alpha == 0.0 || rank <= 0) return adapter_scale;", "if (rank <= 0) return adapter_scale;"),
     "ties_away_from_zero": ("q = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;", "q = fl + 1.0;"),
     "rank_loop_short": ("for (int32_t j = 0; j < r; ++j) {\n                double acc = 0.0;", "for (int32_t j = 0; j + 1 < r; ++j) {\n                double acc = 0.0;"),
+    "e4m3_wrong_bias": ("v = (1.0 + m / 8.0) * ldexp(1.0, e - 7);", "v = (1.0 + m / 8.0) * ldexp(1.0, e - 8);"),
+    "e4m3_no_subnormals": ("if (e == 0) v = m * ldexp(1.0, -9);", "if (e == 0) v = (1.0 + m / 8.0) * ldexp(1.0, -7);"),
+    "fp8_x_not_quantized": ("xq[c] = oracle_e4m3_to_double(oracle_e4m3_round(bf16_value(x[(int64_t)t * ldx + c])));",
+                            "xq[c] = bf16_value(x[(int64_t)t * ldx + c]);"),
+    "e4m3_ties_to_odd": ("(c & 1) == 0 && (best & 1) == 1", "(c & 1) == 1 && (best & 1) == 0"),
 }
 
 PINS = [
@@ -51,6 +56,10 @@ PINS = [
     pins.test_mac_count_matches_pages,
     pins.test_rank0_slot_and_out_of_range_slot,
     pins.test_round_bf16_against_brute_force,
+    pins.test_e4m3_decode_matches_library_on_every_code,
+    pins.test_e4m3_round_matches_library_clamp_and_convert,
+    pins.test_e4m3_premultiply_matches_pages_expression,
+    pins.test_fp8_branch_equals_bf16_branch_on_decoded_values,
 ]
 
 

@@ -456,3 +456,69 @@ def test_round_bf16_agrees_with_input_rounding_on_float32_values():
     want = W.f32_to_bf16_bits(v)
     got = np.array([oracle.round_bf16(float(a)) for a in v], dtype=np.uint16)
     np.testing.assert_array_equal(got, want)
+
+
+# ---------------------------------------------------------------------------
+# FP8 adapters (TensorRT-LLM LoRA serving page, "第五步:FP8 特判" and the
+# forward-pass data_type check: weights stay float8_e4m3fn, x is clamped to the
+# FP8 range and converted)
+# ---------------------------------------------------------------------------
+def test_e4m3_decode_matches_library_on_every_code():
+    torch = pytest.importorskip("torch")
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_to_double(codes)
+    lib = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    np.testing.assert_array_equal(np.isnan(ours), np.isnan(lib))
+    np.testing.assert_array_equal(ours[~np.isnan(ours)], lib[~np.isnan(lib)])
+    assert oracle.e4m3_to_double(np.array([0x7E], np.uint8))[0] == 448.0  # fp8_max on the page
+
+
+def test_e4m3_round_matches_library_clamp_and_convert():
+    """x.clamp(-fp8_max, fp8_max).to(float8_e4m3fn), including ties and the clamp."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(3)
+    v = rng.standard_normal(4000) * np.exp(rng.uniform(-12, 8, 4000))
+    pos = oracle.e4m3_to_double(np.arange(0x7F, dtype=np.uint8))
+    mids = (pos[:-1] + pos[1:]) / 2  # exact ties between neighbouring codes
+    v = np.concatenate([v, mids, -mids, [500.0, -1e6, 448.0, 0.0]])
+    ours = oracle.e4m3_round(v)
+    lib = torch.from_numpy(v).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(ours, lib)
+
+
+def test_e4m3_premultiply_matches_pages_expression():
+    """(t_out.to(bf16) * scale).clamp(-fp8_max, fp8_max).to(t_out.dtype)."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(4)
+    codes = rng.integers(0, 256, size=3000).astype(np.uint8)
+    codes = codes[(codes & 0x7F) != 0x7F]  # no NaN codes
+    for s in (0.25, 2.0, 1.0 / 3.0, 8.0):
+        ours = oracle.premultiply_e4m3(codes, s)
+        t = torch.from_numpy(codes).view(torch.float8_e4m3fn)
+        lib = (t.to(torch.bfloat16) * s).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        np.testing.assert_array_equal(ours, lib)
+
+
+def test_fp8_branch_equals_bf16_branch_on_decoded_values():
+    """Every e4m3 value is a bf16 value, so the FP8 branch is the bf16 branch run
+    on x rounded through e4m3 and on the decoded weights."""
+    rng = np.random.default_rng(5)
+    T, k, widths, S = 12, 64, [24, 8], 3
+    ranks = np.array([8, 0, 16], np.int32)
+    x = W.f32_to_bf16_bits(rng.standard_normal((T, k)).astype(np.float32))
+    y_in = W.f32_to_bf16_bits(rng.standard_normal((T, sum(widths))).astype(np.float32))
+    ids = np.array([0, 2, -1, 1, 2, 0, 0, 2, -1, 2, 1, 0], np.int32)
+    A8 = [[(rng.integers(0, 256, size=(r, k)).astype(np.uint8) & 0xF7 if r else None) for _ in widths] for r in ranks]
+    B8 = [[(rng.integers(0, 256, size=(w, r)).astype(np.uint8) & 0xF7 if r else None) for w in widths] for r in ranks]
+    scales = np.array([0.5, 1.0, 2.0])
+    got, st = oracle.apply_e4m3(x, y_in, widths, ids, ranks, scales, A8, B8)
+    assert st == oracle.ERR_OK
+
+    def bf16_of(codes):
+        return W.f32_to_bf16_bits(oracle.e4m3_to_double(codes).astype(np.float32))
+
+    xq = bf16_of(oracle.e4m3_round(W.bf16_bits_to_f32(x).astype(np.float64)))
+    A = [[bf16_of(a) if a is not None else None for a in row] for row in A8]
+    B = [[bf16_of(b) if b is not None else None for b in row] for row in B8]
+    ref, _, _ = oracle.apply(xq, y_in, widths, ids, ranks, scales, A, B)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
