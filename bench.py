@@ -54,7 +54,9 @@ def parse_args(argv=None):
     p.add_argument("--config", default="decode_qkv", choices=list(CONFIG_INDEX))
     p.add_argument("--layers", type=int, default=32)
     p.add_argument("--requests", type=int, default=16, help="prefill_mlp only: requests in the batch")
-    p.add_argument("--path", default="auto", choices=["auto", "decode_fused", "decode_split", "prefill", "decode_tc", "decode_stream", "decode_direct"])
+    p.add_argument("--path", default="auto", choices=["auto", "decode_fused", "decode_split", "prefill", "decode_tc", "decode_stream", "decode_direct",
+                            "decode_direct_fp8"],
+                   help="auto takes decode_direct_fp8 for a workload with FP8 adapters")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--with-base", default="none", choices=["none", "serial", "overlap"],
@@ -67,16 +69,17 @@ def parse_args(argv=None):
 # ---------------------------------------------------------------------------
 # Accounting (measurement, not the method): bytes and flops a call must move
 # ---------------------------------------------------------------------------
-def algorithmic_bytes(slot_ids, ranks, k, widths) -> int:
-    """Each active slot's A and B once (bf16), x rows of LoRA tokens once, their
-    y rows read and written (bf16).  Workspace, index and no-adapter rows excluded."""
+def algorithmic_bytes(slot_ids, ranks, k, widths, wbytes: int = 2) -> int:
+    """Each active slot's A and B once (wbytes per weight: 2 for bf16, 1 for
+    e4m3), x rows of LoRA tokens once, their y rows read and written (bf16).
+    Workspace, index and no-adapter rows excluded."""
     S, n, d = len(ranks), len(widths), int(sum(widths))
     ids = np.asarray(slot_ids)
     valid = (ids >= 0) & (ids < S)
     lora = np.zeros(len(ids), dtype=bool)
     lora[valid] = np.asarray(ranks)[ids[valid]] > 0
     n_l = int(lora.sum())
-    weights = sum(2 * int(ranks[s]) * (n * k + d) for s in np.unique(ids[lora]))
+    weights = sum(wbytes * int(ranks[s]) * (n * k + d) for s in np.unique(ids[lora]))
     return int(weights + 2 * k * n_l + 4 * d * n_l)
 
 
@@ -270,6 +273,12 @@ def run_ours(args):
     dev = torch.device("cuda", local)
 
     wl = _workload(args.config, args.requests)
+    if wl.weights == "e4m3":
+        if args.path == "auto":
+            args.path = "decode_direct_fp8"
+        if args.path != "decode_direct_fp8":
+            raise SystemExit(f"{args.config} holds FP8 adapters: only --path decode_direct_fp8 serves it")
+    wbytes = 1 if wl.weights == "e4m3" else 2
     mods = list(range(len(wl.modules)))
     # layer l uses projection mods[l % len(mods)] in its own buffers
     base = [ResidentProjection.from_workload(wl, m, device=dev) for m in mods]
@@ -370,7 +379,7 @@ def run_ours(args):
     value = job_throughput(units, elapsed_s, world, dev)
     ms_per_step = max_over_ranks(elapsed_s, dev) / args.steps * 1e3
 
-    bytes_per_call = [algorithmic_bytes(wl.slot_ids, wl.ranks, wl.modules[m].k, wl.modules[m].slice_widths)
+    bytes_per_call = [algorithmic_bytes(wl.slot_ids, wl.ranks, wl.modules[m].k, wl.modules[m].slice_widths, wbytes)
                       for m in mods]
     flops_per_call = [algorithmic_flops(wl.slot_ids, wl.ranks, wl.modules[m].k, wl.modules[m].slice_widths)
                       for m in mods]
@@ -405,7 +414,7 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "e4m3 (adapters; x rounded to e4m3, y bf16)" if wl.weights == "e4m3" else "bf16",
         "data": "synthetic (seeded: workloads.config)",
         "config": {
             "workload": wl.description if args.config != "decode_qkv" else
@@ -507,14 +516,19 @@ def run_e2e(args, wl, layers, index, slot_dev, ws_of, max_seg, dev, world):
 def _oracle_call(wl, rows):
     import oracle
     m = wl.modules[0]
+    fp8 = wl.weights == "e4m3"
     rule = oracle.slot_scales(wl.ranks, wl.alphas, wl.scale_rule, False)
+    premul = oracle.premultiply_e4m3 if fp8 else oracle.premultiply
     if wl.premultiplied:
-        B = [[(oracle.premultiply(b, rule[s]) if b is not None else None) for b in row] for s, row in enumerate(m.B)]
+        B = [[(premul(b, rule[s]) if b is not None else None) for b in row] for s, row in enumerate(m.B)]
         scales = np.ones(wl.S)
     else:
         B, scales = m.B, rule
     t0 = time.perf_counter()
-    oracle.apply(m.x, m.y_in, m.slice_widths, wl.slot_ids, wl.ranks, scales, m.A, B, rows=rows)
+    if fp8:
+        oracle.apply_e4m3(m.x, m.y_in, m.slice_widths, wl.slot_ids, wl.ranks, scales, m.A, B, rows=rows)
+    else:
+        oracle.apply(m.x, m.y_in, m.slice_widths, wl.slot_ids, wl.ranks, scales, m.A, B, rows=rows)
     return time.perf_counter() - t0
 
 

@@ -100,12 +100,26 @@ typedef enum {
                                     sharing every SM; needs T <= 2048, r_max <= 128, k % 16 == 0
                                     and tables that fit in shared memory (else
                                     LORA_ERR_UNSUPPORTED) */
-    LORA_PATH_DECODE_DIRECT = 6  /* two launches on warp-level MMA in which every warp streams its
+    LORA_PATH_DECODE_DIRECT = 6, /* two launches on warp-level MMA in which every warp streams its
                                     own byte-balanced share through a private cp.async ring (no
                                     barriers between warps): a split-K shrink adding into an fp32
                                     accumulator, then an expand launched as its programmatic
                                     dependent; needs T <= 2048, r_max <= 64, S <= 512 and
                                     S * n_slices <= 512 (else LORA_ERR_UNSUPPORTED) */
+    LORA_PATH_DECODE_DIRECT_FP8 = 7 /* LORA_PATH_DECODE_DIRECT with FP8 adapters (TensorRT-LLM LoRA
+                                    serving page, "第五步:FP8 特判" and the input-dtype check of the
+                                    forward pass): every A and B pointer of the slot table
+                                    addresses float8_e4m3fn codes in the same row-major layouts
+                                    (A_s,i [r][k], B_s,i [d_i][r], one byte each); x and y stay
+                                    bf16.  x is clamped to +-448 and rounded to e4m3 (nearest,
+                                    ties to even) inside the shrink, whose products are exact
+                                    and summed in fp32; the sums enter the expand rounded once
+                                    to f16 (|sum| <= 65504 assumed) against B converted exactly
+                                    to f16, and y = bf16(y + s * acc) as for bf16 adapters.
+                                    Scale B at load time with lora_premultiply on its bf16
+                                    values, then clamp and round to e4m3.  Same limits as
+                                    LORA_PATH_DECODE_DIRECT plus k % 16 == 0; never chosen by
+                                    LORA_PATH_AUTO, whose table is bf16 */
 } lora_path_t;
 
 #define LORA_DECODE_MAX_SEG 256
@@ -150,6 +164,16 @@ double lora_scale(double alpha, int32_t rank, int32_t rslora, double adapter_sca
  * slot is then used with scale 1.  w: device bf16, n elements, 2-byte aligned.
  */
 lora_status_t lora_premultiply(void *w, int64_t n, float scale, lora_stream_t stream);
+
+/*
+ * The same for an FP8 B (TensorRT-LLM LoRA serving page, "第五步:FP8 特判": FP8 has
+ * no scalar multiply, so the scale is applied in bf16 and the result clamped back
+ * into the FP8 range): w[e] = e4m3(clamp(bf16(value(w[e]) * scale), -448, 448)),
+ * the product exact (fp64) and rounded once to bf16, then rounded to the nearest
+ * e4m3 code with ties to even; NaN codes become 0x7F.  w: device float8_e4m3fn
+ * codes, n bytes, any alignment.  For LORA_PATH_DECODE_DIRECT_FP8 slots.
+ */
+lora_status_t lora_premultiply_e4m3(void *w, int64_t n, float scale, lora_stream_t stream);
 
 /*
  * Slot table: per slot s its rank r_s, runtime scale s_s and, per slice i, the

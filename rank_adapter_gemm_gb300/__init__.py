@@ -23,7 +23,7 @@ __all__ = [
     "LORA_ABI_VERSION", "LORA_MAX_RANK", "LORA_MAX_SLICES", "LORA_MAX_SLOTS", "LORA_DECODE_MAX_SEG",
     "LORA_NOALLOC_WS_BYTES",
     "LoraError", "lora_shape_t", "make_shape", "lora_abi_version", "lora_status_string", "lora_scale",
-    "lora_premultiply", "lora_slot_table_bytes", "lora_pack_slot_table", "lora_set_slot_table",
+    "lora_premultiply", "lora_premultiply_e4m3", "lora_slot_table_bytes", "lora_pack_slot_table", "lora_set_slot_table",
     "lora_build_index", "lora_build_index_seq", "lora_workspace_bytes", "lora_workspace_xa_offset", "lora_shrink", "lora_expand", "lora_apply", "lora_resolve_path",
     "lora_apply_noalloc", "lora_apply_overlap", "apply_with_base", "SlotTable", "TokenIndex", "Workspace",
 ]
@@ -103,6 +103,16 @@ def lora_premultiply(w, scale: float, stream=None) -> None:
     if not w.is_contiguous():
         raise ValueError("w must be contiguous")
     check(load().lora_premultiply(_p(w), w.numel(), float(scale), _stream(stream)), "lora_premultiply")
+
+
+def lora_premultiply_e4m3(w, scale: float, stream=None) -> None:
+    """In-place load-time scale of float8_e4m3fn codes (a uint8 or float8_e4m3fn tensor)."""
+    torch = _torch()
+    if not isinstance(w, torch.Tensor) or not w.is_cuda or w.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError("w must be a CUDA uint8 or float8_e4m3fn tensor")
+    if not w.is_contiguous():
+        raise ValueError("w must be contiguous")
+    check(load().lora_premultiply_e4m3(_p(w), w.numel(), float(scale), _stream(stream)), "lora_premultiply_e4m3")
 
 
 def lora_slot_table_bytes(S: int, n_slices: int) -> int:

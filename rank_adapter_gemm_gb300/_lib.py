@@ -33,7 +33,7 @@ STATUS = {
 globals().update({name: code for code, name in STATUS.items()})
 
 PATHS = {"auto": 0, "decode_fused": 1, "decode_split": 2, "prefill": 3, "decode_tc": 4, "decode_stream": 5,
-         "decode_direct": 6}
+         "decode_direct": 6, "decode_direct_fp8": 7}
 
 # Every function the header declares, for the export check.
 EXPORTED = (
@@ -41,7 +41,7 @@ EXPORTED = (
     "lora_slot_table_bytes", "lora_pack_slot_table", "lora_set_slot_table", "lora_build_index",
     "lora_workspace_bytes", "lora_shrink", "lora_expand", "lora_apply", "lora_apply_ex",
     "lora_resolve_path", "lora_apply_noalloc", "lora_workspace_xa_offset", "lora_build_index_seq",
-    "lora_apply_overlap",
+    "lora_apply_overlap", "lora_premultiply_e4m3",
 )
 
 
@@ -87,6 +87,7 @@ def load() -> ctypes.CDLL:
         "lora_status_string": (ctypes.c_char_p, [ST]),
         "lora_scale": (ctypes.c_double, [ctypes.c_double, I32, I32, ctypes.c_double]),
         "lora_premultiply": (ST, [P, I64, ctypes.c_float, P]),
+        "lora_premultiply_e4m3": (ST, [P, I64, ctypes.c_float, P]),
         "lora_slot_table_bytes": (SZ, [I32, I32]),
         "lora_pack_slot_table": (ST, [P, I32, I32, I32, P, P, P, P]),
         "lora_set_slot_table": (ST, [P, P, I32, I32, I32, P, P, P, P, P]),

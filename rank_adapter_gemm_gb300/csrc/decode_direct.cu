@@ -40,9 +40,21 @@
 //     into buffer g & 1 and clears buffer (g + 1) & 1, which the previous call
 //     used; the last expand CTA to finish advances g.  No CTA waits on another.
 //
+//   * FP8 adapters (LORA_PATH_DECODE_DIRECT_FP8; TensorRT-LLM LoRA serving
+//     page, "第五步:FP8 特判"): A and B are float8_e4m3fn codes.  The shrink
+//     copies 64-column blocks (a lane's 16 bytes of A are 16 columns), converts
+//     its x columns from bf16 to e4m3 in registers (clamped to +-448, nearest
+//     even) and runs mma.m16n8k32 e4m3 with the same shared k-permutation;
+//     token groups are 24 so that a block's 2 MT + 6 chunks fit a stage.  The
+//     expand copies [64][r] bytes of B, converts them exactly to f16 and feeds
+//     an f16 MMA with the sums rounded once to f16.
+//
 // Limits (the host routes other cases elsewhere): T <= 2048, r_max <= 64,
-// S * n_slices <= 512, S <= 512.
+// S * n_slices <= 512, S <= 512; FP8 also k % 16 == 0.
 #include <algorithm>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 
@@ -164,6 +176,64 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// ---------------------------------------------------------------------------
+// FP8 (float8_e4m3fn) operands
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint2 lds8(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+// Four bf16 values (two bf16x2 words, lowest column in the low half of lo) to
+// four e4m3 codes, lowest column in byte 0: clamped to the finite range
+// (+-448, satfinite) and rounded to nearest even, as x.clamp(-448, 448)
+// .to(float8_e4m3fn) does; bf16 -> f32 is exact, so this rounds once.
+__device__ __forceinline__ uint32_t e4m3x4_from_bf16x4(uint32_t lo, uint32_t hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 l, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 h, %4, %3;\n\t"
+        "mov.b32 %0, {l, h};\n\t}"
+        : "=r"(r)
+        : "f"(bf16lo_to_f32(lo)), "f"(bf16hi_to_f32(lo)), "f"(bf16lo_to_f32(hi)), "f"(bf16hi_to_f32(hi)));
+    return r;
+}
+// Two e4m3 codes (bits 0..15 of w; byte 0 -> low half) to f16x2, exactly:
+// every e4m3 value, subnormals included, is a normal f16.
+__device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t w) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 c;\n\t"
+        "cvt.u16.u32 c, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+        : "=r"(r) : "r"(w));
+    return r;
+}
+// Two fp32 -> packed f16x2 (lo in the low half), round-to-nearest-even.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// mma.m16n8k32 with e4m3 A and B, fp32 accumulate.  Lane 4g + q: a0 = (row g,
+// k 4q..4q+3), a1 = (row g+8, k 4q..), a2 = (row g, k 4q+16..), a3 = (row g+8,
+// k 4q+16..); b0 = (k 4q..4q+3, col g), b1 = (k 4q+16.., col g); the lowest k
+// in the lowest byte.  Accumulators as for m16n8k16.
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// mma.m16n8k16 with f16 A and B (fragments as for bf16), fp32 accumulate.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 
 // ---------------------------------------------------------------------------
 // Tables: one copy per CTA in shared memory, built by the prologue.
@@ -231,24 +301,24 @@ __device__ Tabs carve(unsigned char *base, int32_t S, int32_t n, int32_t T) {
 // of k: 2 MT chunks of A rows per token group of 32, one chunk of x rows per 8
 // tokens, and a fixed cost.
 __device__ __forceinline__ int32_t s_mt(int32_t r, int32_t rb) { return r - kRB * rb > 16 ? 2 : 1; }
-__device__ __forceinline__ int32_t s_block_w(int32_t r, int32_t L, int32_t rb) {
-    return 2 * s_mt(r, rb) * cdiv(L, kTGs) + cdiv(L, 8) + 1;
+__device__ __forceinline__ int32_t s_block_w(int32_t r, int32_t L, int32_t rb, int32_t tg, int32_t xf) {
+    return 2 * s_mt(r, rb) * cdiv(L, tg) + xf * cdiv(L, 8) + 1;
 }
-__device__ __forceinline__ long long s_slot_w(int32_t r, int32_t L, int32_t n, int32_t nkb) {
+__device__ __forceinline__ long long s_slot_w(int32_t r, int32_t L, int32_t n, int32_t nkb, int32_t tg, int32_t xf) {
     long long w = 0;
-    for (int32_t rb = 0; kRB * rb < r; ++rb) w += s_block_w(r, L, rb);
+    for (int32_t rb = 0; kRB * rb < r; ++rb) w += s_block_w(r, L, rb, tg, xf);
     return w * nkb * n;
 }
-// Expand: token group tg (16 tokens) of 64 output columns: 8 chunks of B rows
-// per 32 ranks, two chunks of y and 2 nkb chunks of sums per 8 tokens, and a
-// fixed cost.
-__device__ __forceinline__ int32_t e_unit_w(int32_t r, int32_t L, int32_t tg) {
+// Expand: token group tg (16 tokens) of 64 output columns: bw chunks of B rows
+// per 32 ranks (8 for bf16, 4 for e4m3), two chunks of y and 2 nkb chunks of
+// sums per 8 tokens, and a fixed cost.
+__device__ __forceinline__ int32_t e_unit_w(int32_t r, int32_t L, int32_t tg, int32_t bw) {
     const int32_t nt8 = min(2, cdiv(L - kTGe * tg, 8)), nkb = cdiv(r, 32);
-    return 8 * nkb + 2 * nt8 * (1 + nkb) + 2;
+    return bw * nkb + 2 * nt8 * (1 + nkb) + 2;
 }
-__device__ __forceinline__ int32_t e_cb_w(int32_t r, int32_t L) {
+__device__ __forceinline__ int32_t e_cb_w(int32_t r, int32_t L, int32_t bw) {
     const int32_t nkb = cdiv(r, 32);
-    return cdiv(L, kTGe) * (8 * nkb + 2) + 2 * cdiv(L, 8) * (1 + nkb);
+    return cdiv(L, kTGe) * (bw * nkb + 2) + 2 * cdiv(L, 8) * (1 + nkb);
 }
 
 __device__ __forceinline__ void cp4(void *dst, const void *src) {
@@ -260,8 +330,12 @@ __device__ __forceinline__ void cp8(void *dst, const void *src) {
 
 // Prologue: every table load of the CTA in flight at once, then the checks,
 // the per-active-slot records and their weight prefix.  Ends with a barrier.
+// Weight parameters, kept in misc[6] and misc[7]: for the shrink the token
+// group (tg), the x chunks per 8 tokens (xf) and the columns of k per block
+// (bc); for the expand tg is the B chunks per 32 ranks.
 template <bool kExpand>
-__device__ void build_tabs(const DArgs &a, const Shape &sh, const void *table, const Tabs &t) {
+__device__ void build_tabs(const DArgs &a, const Shape &sh, const void *table, const Tabs &t, int32_t tg,
+                           int32_t xf, int32_t bc) {
     const int32_t S = sh.S, n = sh.n, T = a.T;
     const int tid = threadIdx.x, nthr = blockDim.x, warp = tid >> 5, lane = tid & 31;
     const TableView tab(table, S, n);
@@ -271,6 +345,8 @@ __device__ void build_tabs(const DArgs &a, const Shape &sh, const void *table, c
         cp4(t.misc + 4, hdr + 1);
         cp4(t.misc + 5, hdr + 2);
         cp4(t.misc + 1, a.gen);
+        t.misc[6] = tg;
+        t.misc[7] = xf;
         int32_t c = 0, o = 0;
 #pragma unroll
         for (int i = 0; i <= LORA_MAX_SLICES; ++i) {
@@ -303,7 +379,7 @@ __device__ void build_tabs(const DArgs &a, const Shape &sh, const void *table, c
     const bool ok = t.misc[3] == kTableMagic && t.misc[4] == S && t.misc[5] == n && t.seg[S + 1] == T;
     if (!ok && tid == 0 && blockIdx.x == 0) report_error(a.err, LORA_ERR_INVALID_ARG);
     const int32_t NA = ok ? min(max(t.act[0], 0), S) : 0;
-    const int32_t nkb = cdiv(sh.k, 32), ncb = t.scb[LORA_MAX_SLICES];
+    const int32_t nkb = cdiv(sh.k, bc), ncb = t.scb[LORA_MAX_SLICES];
     for (int j = tid; j < NA; j += nthr) {
         const int32_t s = t.act[1 + j];
         int32_t r = 0, L = 0, p0 = 0;
@@ -327,7 +403,7 @@ __device__ void build_tabs(const DArgs &a, const Shape &sh, const void *table, c
         t.a_p0[j] = p0;
         t.a_len[j] = L;
         t.a_r[j] = r;
-        t.a_pre[j] = r == 0 ? 0 : (kExpand ? static_cast<long long>(ncb) * e_cb_w(r, L) : s_slot_w(r, L, n, nkb));
+        t.a_pre[j] = r == 0 ? 0 : (kExpand ? static_cast<long long>(ncb) * e_cb_w(r, L, tg) : s_slot_w(r, L, n, nkb, tg, xf));
     }
     __syncthreads();
     if (warp == 0) {
@@ -386,7 +462,7 @@ struct SGen {
     bool live;
 };
 
-__device__ __forceinline__ int32_t s_nt8(int32_t L, int32_t g) { return min(4, cdiv(L - kTGs * g, 8)); }
+__device__ __forceinline__ int32_t s_nt8(int32_t L, int32_t g, int32_t tg) { return min(tg / 8, cdiv(L - tg * g, 8)); }
 
 // Blocks of the current unit whose weight start is below R1.
 __device__ __forceinline__ void s_range(SGen &c, int32_t nkb) {
@@ -412,13 +488,13 @@ __device__ __forceinline__ void s_next_unit(SGen &c, const Tabs &t, int32_t n, i
             }
         }
     }
-    c.w = s_block_w(t.a_r[c.ja], t.a_len[c.ja], c.rb);
+    c.w = s_block_w(t.a_r[c.ja], t.a_len[c.ja], c.rb, t.misc[6], t.misc[7]);
     c.bs = 0;
     s_range(c, nkb);
 }
 
 __device__ __forceinline__ void s_next_seg(SGen &c, const Tabs &t, int32_t n, int32_t nkb) {
-    if (kTGs * (++c.g) >= t.a_len[c.ja]) s_next_unit(c, t, n, nkb);
+    if (t.misc[6] * (++c.g) >= t.a_len[c.ja]) s_next_unit(c, t, n, nkb);
 }
 
 __device__ __forceinline__ void s_first(SGen &c, const Tabs &t, int32_t n, int32_t nkb) {
@@ -433,19 +509,20 @@ __device__ __forceinline__ void s_first(SGen &c, const Tabs &t, int32_t n, int32
     c.ja = find_active(t.a_pre, NA, R0);
     const int32_t r = t.a_r[c.ja], L = t.a_len[c.ja];
     long long o = R0 - t.a_pre[c.ja];
-    const long long wslice = s_slot_w(r, L, 1, nkb);
+    const int32_t tg = t.misc[6], xf = t.misc[7];
+    const long long wslice = s_slot_w(r, L, 1, nkb, tg, xf);
     c.i = static_cast<int32_t>(o / wslice);
     o -= c.i * wslice;
     c.start = t.a_pre[c.ja] + c.i * wslice;
     c.rb = 0;
     while (true) {
-        const long long wu = static_cast<long long>(nkb) * s_block_w(r, L, c.rb);
+        const long long wu = static_cast<long long>(nkb) * s_block_w(r, L, c.rb, tg, xf);
         if (o < wu) break;
         o -= wu;
         c.start += wu;
         ++c.rb;
     }
-    c.w = s_block_w(r, L, c.rb);
+    c.w = s_block_w(r, L, c.rb, tg, xf);
     c.bs = static_cast<int32_t>((o + c.w - 1) / c.w);
     if (c.bs >= nkb) {
         s_next_unit(c, t, n, nkb);  // the share starts after this unit's last block start
@@ -457,7 +534,10 @@ __device__ __forceinline__ void s_first(SGen &c, const Tabs &t, int32_t n, int32
 // Copy walker: per-segment lane pointers at block 0, so a block costs one
 // 64-bit add per 16-byte copy.  Chunk c < 2 MT of a block is A row
 // 2 MT gq + c of the rank block; chunk 2 MT + nt is the x row of token
-// 32 g + 8 nt + gq; lane 4 gq + q copies columns 8q..8q+7 of each.
+// tg g + 8 nt + gq; lane 4 gq + q copies columns 8q..8q+7 of each.  With FP8
+// weights (kF8) a block is 64 columns: the lane's A chunk holds columns
+// 16q..16q+15 (one byte each) and its x row, still bf16, takes the two chunks
+// 2 MT + 2 nt and 2 MT + 2 nt + 1.
 struct SCopy {
     SGen gen;
     int32_t b, kb, cpb, mt, nt;
@@ -465,29 +545,31 @@ struct SCopy {
     const unsigned char *pa[4], *px[4];
 };
 
+template <bool kF8>
 __device__ __forceinline__ void s_copy_seg(SCopy &s, const Tabs &t, const Shape &sh, const DArgs &a, int lane) {
-    const int32_t gq = lane >> 2, q = lane & 3;
+    constexpr int32_t kEB = kF8 ? 1 : 2;  // bytes per weight
+    const int32_t gq = lane >> 2, q = lane & 3, tg = t.misc[6];
     const int32_t ja = s.gen.ja, r = t.a_r[ja], L = t.a_len[ja], p0 = t.a_p0[ja];
     s.mt = s_mt(r, s.gen.rb);
-    s.nt = s_nt8(L, s.gen.g);
-    s.cpb = 2 * s.mt + s.nt;
+    s.nt = s_nt8(L, s.gen.g, tg);
+    s.cpb = 2 * s.mt + (kF8 ? 2 : 1) * s.nt;
     s.kb = kSChunks / s.cpb;
     s.b = s.gen.bs;
     const int32_t rows = min(kRB, r - kRB * s.gen.rb);
     const unsigned char *A = reinterpret_cast<const unsigned char *>(t.aptr[t.a_slot[ja] * sh.n + s.gen.i]) +
-                             2 * (static_cast<int64_t>(kRB * s.gen.rb) * sh.k + 8 * q);
+                             kEB * static_cast<int64_t>(kRB * s.gen.rb) * sh.k + 16 * q;
     uint32_t vm = 0;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         const int32_t row = 2 * s.mt * gq + c;
         const bool v = c < 2 * s.mt && row < rows;
-        s.pa[c] = A + (v ? 2 * static_cast<int64_t>(row) * sh.k : 0);
+        s.pa[c] = A + (v ? kEB * static_cast<int64_t>(row) * sh.k : 0);
         vm |= v ? (1u << c) : 0u;
     }
-    const unsigned char *X = reinterpret_cast<const unsigned char *>(a.x) + 16 * q;
+    const unsigned char *X = reinterpret_cast<const unsigned char *>(a.x) + (kF8 ? 32 : 16) * q;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
-        const int32_t jt = kTGs * s.gen.g + 8 * nt + gq;
+        const int32_t jt = tg * s.gen.g + 8 * nt + gq;
         const int32_t tok = (nt < s.nt && jt < L) ? t.tok[p0 + jt] : -1;
         s.px[nt] = X + (tok >= 0 ? 2 * static_cast<int64_t>(tok) * a.ldx : 0);
         vm |= tok >= 0 ? (1u << (4 + nt)) : 0u;
@@ -497,6 +579,9 @@ __device__ __forceinline__ void s_copy_seg(SCopy &s, const Tabs &t, const Shape 
 
 // Issue the next stage of copies into `slot` (this lane's bytes) and commit
 // a group (an empty one once the walk is over).
+// kq = k minus the lane's first column in a block: a block's chunk is in range
+// when (columns per block) * blk < kq.
+template <bool kF8>
 __device__ __forceinline__ void s_copy_stage(SCopy &s, uint32_t slot, int32_t kq, const Tabs &t, const Shape &sh,
                                              const DArgs &a, int lane, int32_t nkb) {
     if (s.gen.live) {
@@ -505,7 +590,7 @@ __device__ __forceinline__ void s_copy_stage(SCopy &s, uint32_t slot, int32_t kq
         for (int j = 0; j < 4; ++j) {
             if (j < nb) {
                 const int32_t blk = s.b + j;
-                const bool cv = 32 * blk < kq;
+                const bool cv = (kF8 ? 64 : 32) * blk < kq;
                 const uint32_t dst = slot + j * s.cpb * kChunk;
                 const int64_t off = 64 * static_cast<int64_t>(blk);
 #pragma unroll
@@ -513,14 +598,22 @@ __device__ __forceinline__ void s_copy_stage(SCopy &s, uint32_t slot, int32_t kq
                     if (c < 2 * s.mt) cp16_ca(dst + c * kChunk, s.pa[c] + off, cv && ((s.vm >> c) & 1u));
                 const uint32_t dx = dst + 2 * s.mt * kChunk;
 #pragma unroll
-                for (int nt = 0; nt < 4; ++nt)
-                    if (nt < s.nt) cp16_cg(dx + nt * kChunk, s.px[nt] + off, cv && ((s.vm >> (4 + nt)) & 1u));
+                for (int nt = 0; nt < 4; ++nt) {
+                    if (nt >= s.nt) continue;
+                    const bool v = cv && ((s.vm >> (4 + nt)) & 1u);
+                    if (kF8) {
+                        cp16_cg(dx + 2 * nt * kChunk, s.px[nt] + 2 * off, v);
+                        cp16_cg(dx + (2 * nt + 1) * kChunk, s.px[nt] + 2 * off + 16, v);
+                    } else {
+                        cp16_cg(dx + nt * kChunk, s.px[nt] + off, v);
+                    }
+                }
             }
         }
         s.b += nb;
         if (s.b >= s.gen.be) {
             s_next_seg(s.gen, t, sh.n, nkb);
-            if (s.gen.live) s_copy_seg(s, t, sh, a, lane);
+            if (s.gen.live) s_copy_seg<kF8>(s, t, sh, a, lane);
         }
     }
     cp_commit();
@@ -532,16 +625,17 @@ __device__ __forceinline__ void s_reduce(const SGen &c, float *buf, const Tabs &
                                       int lane, const float (&acc)[2][4][4]) {
     const int32_t gq = lane >> 2, q = lane & 3;
     const int32_t r = t.a_r[c.ja], L = t.a_len[c.ja], p0 = t.a_p0[c.ja];
-    const int32_t MT = s_mt(r, c.rb), NT8 = s_nt8(L, c.g);
+    const int32_t tg = t.misc[6];
+    const int32_t MT = s_mt(r, c.rb), NT8 = s_nt8(L, c.g, tg);
     const int32_t rows = min(kRB, r - kRB * c.rb);
-    float *base = buf + (static_cast<int64_t>(c.i) * T + p0 + kTGs * c.g) * sh.r_max + kRB * c.rb;
+    float *base = buf + (static_cast<int64_t>(c.i) * T + p0 + tg * c.g) * sh.r_max + kRB * c.rb;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
         if (nt >= NT8) continue;
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int32_t jt = 8 * nt + 2 * q + e;
-            if (kTGs * c.g + jt >= L) continue;
+            if (tg * c.g + jt >= L) continue;
             float *p = base + static_cast<int64_t>(jt) * sh.r_max;
             if (MT == 2) {
                 if (4 * gq < rows) red_v4(p + 4 * gq, acc[0][nt][e], acc[0][nt][2 + e], acc[1][nt][e], acc[1][nt][2 + e]);
@@ -557,13 +651,14 @@ __device__ __forceinline__ void s_reduce(const SGen &c, float *buf, const Tabs &
 // token with an adapter, spread over all threads of the grid.  A warp issues
 // its share once its first stage has landed: the prefetches then fill the DRAM
 // time after the first burst of A instead of delaying it.
+template <bool kF8>
 __device__ __forceinline__ void prefetch_expand_inputs(const Tabs &t, const Shape &sh, const DArgs &a) {
     const int32_t NA = t.misc[0], G = gridDim.x, tid = threadIdx.x;
     for (int32_t e = blockIdx.x + G * tid; e < NA * sh.n; e += G * static_cast<int32_t>(blockDim.x)) {
         const int32_t ja = e / sh.n, i = e - ja * sh.n, r = t.a_r[ja];
         if (r == 0) continue;
         const unsigned char *B = reinterpret_cast<const unsigned char *>(t.bptr[t.a_slot[ja] * sh.n + i]);
-        const uint32_t bytes = 2u * static_cast<uint32_t>(t.soff[i + 1] - t.soff[i]) * r;
+        const uint32_t bytes = (kF8 ? 1u : 2u) * static_cast<uint32_t>(t.soff[i + 1] - t.soff[i]) * r;
         for (uint32_t o = 0; o < bytes; o += 65536u) bulk_prefetch_l2(B + o, min(65536u, bytes - o));
     }
     const uint32_t ybytes = 2u * static_cast<uint32_t>(t.soff[LORA_MAX_SLICES]);
@@ -578,13 +673,17 @@ size_t direct_shrink_smem(int32_t S, int32_t n, int32_t T) {
     return static_cast<size_t>(kSWarps) * kSStages * kSChunks * kChunk + tabs_bytes(S, n, T);
 }
 
+// kF8: A in e4m3, x converted to e4m3 in registers, 64-column blocks of k,
+// token groups of 24 (a stage of 2 MT + 6 chunks holds one block).
+template <bool kF8>
 __global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a, Shape sh, const void *table) {
+    constexpr int32_t kTG = kF8 ? 24 : kTGs, kXF = kF8 ? 2 : 1, kBC = kF8 ? 64 : 32;
     extern __shared__ __align__(128) unsigned char smem[];
     // the expand may start its prologue as soon as every CTA of this grid runs
     pdl_launch_dependents();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Tabs t = carve(smem + static_cast<size_t>(kSWarps) * kSStages * kSChunks * kChunk, sh.S, sh.n, a.T);
-    build_tabs<false>(a, sh, table, t);
+    build_tabs<false>(a, sh, table, t, kTG, kXF, kBC);
     const int32_t gen = t.misc[1];
     float *buf = (gen & 1) ? a.acc1 : a.acc0;
     {
@@ -595,26 +694,26 @@ __global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a,
              e += static_cast<int64_t>(gridDim.x) * blockDim.x)
             other[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const int32_t nkb = cdiv(sh.k, 32), kq = sh.k - 8 * (lane & 3);
+    const int32_t nkb = cdiv(sh.k, kBC), kq = sh.k - (kBC / 4) * (lane & 3);
     const uint32_t ring = sa(smem) + warp * (kSStages * kSChunks * kChunk) + 16 * lane;
     constexpr uint32_t kSlot = kSChunks * kChunk;
 
     SCopy cw;
     s_first(cw.gen, t, sh.n, nkb);
-    if (cw.gen.live) s_copy_seg(cw, t, sh, a, lane);
+    if (cw.gen.live) s_copy_seg<kF8>(cw, t, sh, a, lane);
     SGen cg = cw.gen;  // compute walker
 #pragma unroll
-    for (int s = 0; s < kSStages - 1; ++s) s_copy_stage(cw, ring + s * kSlot, kq, t, sh, a, lane, nkb);
+    for (int s = 0; s < kSStages - 1; ++s) s_copy_stage<kF8>(cw, ring + s * kSlot, kq, t, sh, a, lane, nkb);
 
-    if (!cg.live) prefetch_expand_inputs(t, sh, a);
+    if (!cg.live) prefetch_expand_inputs<kF8>(t, sh, a);
     bool prefetched = !cg.live;
     float acc[2][4][4];
     int32_t sc = 0, si = kSStages - 1;
     int32_t b = cg.bs, kb = 1, cpb = 1, MT = 1, NT = 1;
     if (cg.live) {
         MT = s_mt(t.a_r[cg.ja], cg.rb);
-        NT = s_nt8(t.a_len[cg.ja], cg.g);
-        cpb = 2 * MT + NT;
+        NT = s_nt8(t.a_len[cg.ja], cg.g, kTG);
+        cpb = 2 * MT + kXF * NT;
         kb = kSChunks / cpb;
     }
     bool first = true;
@@ -625,11 +724,11 @@ __global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a,
             cp_wait<0>();
             first = false;
         }
-        s_copy_stage(cw, ring + si * kSlot, kq, t, sh, a, lane, nkb);
+        s_copy_stage<kF8>(cw, ring + si * kSlot, kq, t, sh, a, lane, nkb);
         si = si + 1 == kSStages ? 0 : si + 1;
         cp_wait<kSStages - 1>();
         if (!prefetched) {
-            prefetch_expand_inputs(t, sh, a);
+            prefetch_expand_inputs<kF8>(t, sh, a);
             prefetched = true;
         }
         if (b == cg.bs) {
@@ -648,18 +747,36 @@ __global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a,
 #pragma unroll
             for (int c = 0; c < 4; ++c) av[c] = c < 2 * MT ? lds16(src + c * kChunk) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-                xv[nt] = nt < NT ? lds16(src + (2 * MT + nt) * kChunk) : make_uint4(0, 0, 0, 0);
+            for (int nt = 0; nt < 4; ++nt) {
+                if (kF8) {
+                    // columns 16q..16q+7 and 16q+8..16q+15 of the token's x row, to e4m3
+                    const bool v = nt < NT;
+                    const uint4 lo = v ? lds16(src + (2 * MT + 2 * nt) * kChunk) : make_uint4(0, 0, 0, 0);
+                    const uint4 hi = v ? lds16(src + (2 * MT + 2 * nt + 1) * kChunk) : make_uint4(0, 0, 0, 0);
+                    xv[nt] = make_uint4(e4m3x4_from_bf16x4(lo.x, lo.y), e4m3x4_from_bf16x4(lo.z, lo.w),
+                                        e4m3x4_from_bf16x4(hi.x, hi.y), e4m3x4_from_bf16x4(hi.z, hi.w));
+                } else {
+                    xv[nt] = nt < NT ? lds16(src + (2 * MT + nt) * kChunk) : make_uint4(0, 0, 0, 0);
+                }
+            }
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
                 if (mt >= MT) continue;
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt) {
                     if (nt >= NT) continue;
-                    mma_bf16_16816(acc[mt][nt], av[2 * mt].x, av[2 * mt + 1].x, av[2 * mt].y, av[2 * mt + 1].y,
-                                   xv[nt].x, xv[nt].y);
-                    mma_bf16_16816(acc[mt][nt], av[2 * mt].z, av[2 * mt + 1].z, av[2 * mt].w, av[2 * mt + 1].w,
-                                   xv[nt].z, xv[nt].w);
+                    if (kF8) {
+                        // columns 16q + 0..7 feed k {4q..4q+3, 4q+16..4q+19} of the first MMA, 16q + 8..15 the second
+                        mma_e4m3_16832(acc[mt][nt], av[2 * mt].x, av[2 * mt + 1].x, av[2 * mt].y, av[2 * mt + 1].y,
+                                       xv[nt].x, xv[nt].y);
+                        mma_e4m3_16832(acc[mt][nt], av[2 * mt].z, av[2 * mt + 1].z, av[2 * mt].w, av[2 * mt + 1].w,
+                                       xv[nt].z, xv[nt].w);
+                    } else {
+                        mma_bf16_16816(acc[mt][nt], av[2 * mt].x, av[2 * mt + 1].x, av[2 * mt].y, av[2 * mt + 1].y,
+                                       xv[nt].x, xv[nt].y);
+                        mma_bf16_16816(acc[mt][nt], av[2 * mt].z, av[2 * mt + 1].z, av[2 * mt].w, av[2 * mt + 1].w,
+                                       xv[nt].z, xv[nt].w);
+                    }
                 }
             }
         }
@@ -671,8 +788,8 @@ __global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a,
             if (cg.live) {
                 b = cg.bs;
                 MT = s_mt(t.a_r[cg.ja], cg.rb);
-                NT = s_nt8(t.a_len[cg.ja], cg.g);
-                cpb = 2 * MT + NT;
+                NT = s_nt8(t.a_len[cg.ja], cg.g, kTG);
+                cpb = 2 * MT + kXF * NT;
                 kb = kSChunks / cpb;
             }
         }
@@ -705,7 +822,7 @@ struct EGen {
 // units of a warp mostly share their tokens' sums, which stay in registers.
 __device__ __forceinline__ void e_advance(EGen &c, const Tabs &t, int32_t n) {
     const int32_t r = t.a_r[c.ja], L = t.a_len[c.ja];
-    c.start += e_unit_w(r, L, c.tg);
+    c.start += e_unit_w(r, L, c.tg, t.misc[6]);
     if (t.scb[c.i] + (++c.ci) == t.scb[c.i + 1]) {
         c.ci = 0;
         if (kTGe * (++c.tg) >= L) {
@@ -734,7 +851,8 @@ __device__ __forceinline__ void e_first(EGen &c, const Tabs &t, int32_t n) {
     c.ja = find_active(t.a_pre, NA, R0);
     const int32_t r = t.a_r[c.ja], L = t.a_len[c.ja];
     long long o = R0 - t.a_pre[c.ja];
-    const long long wcb = e_cb_w(r, L);
+    const int32_t bw = t.misc[6];
+    const long long wcb = e_cb_w(r, L, bw);
     c.start = t.a_pre[c.ja];
     while (o >= (t.scb[c.i + 1] - t.scb[c.i]) * wcb) {
         const long long ws = (t.scb[c.i + 1] - t.scb[c.i]) * wcb;
@@ -744,13 +862,13 @@ __device__ __forceinline__ void e_first(EGen &c, const Tabs &t, int32_t n) {
     }
     const int32_t nci = t.scb[c.i + 1] - t.scb[c.i];
     while (true) {
-        const long long wt = static_cast<long long>(nci) * e_unit_w(r, L, c.tg);
+        const long long wt = static_cast<long long>(nci) * e_unit_w(r, L, c.tg, bw);
         if (o < wt) break;
         o -= wt;
         c.start += wt;
         ++c.tg;
     }
-    const int32_t w = e_unit_w(r, L, c.tg);
+    const int32_t w = e_unit_w(r, L, c.tg, bw);
     c.ci = static_cast<int32_t>(o / w);
     c.start += static_cast<long long>(c.ci) * w;
     // the first unit whose start is >= R0
@@ -759,7 +877,9 @@ __device__ __forceinline__ void e_first(EGen &c, const Tabs &t, int32_t n) {
 }
 
 // Copies of the next unit into slot `slot` of this warp's ring (base `wslot`),
-// then a commit (an empty group once the walk is over).
+// then a commit (an empty group once the walk is over).  kF8: the B rows are
+// e4m3, r bytes each.
+template <bool kF8>
 __device__ __forceinline__ void e_copy_stage(EGen &g, uint32_t wslot, uint32_t bar, const Tabs &t, const Shape &sh,
                                              const DArgs &a, int lane, int32_t n) {
     if (g.live) {
@@ -768,9 +888,10 @@ __device__ __forceinline__ void e_copy_stage(EGen &g, uint32_t wslot, uint32_t b
         const int32_t o0 = t.soff[g.i], d = t.soff[g.i + 1] - o0;
         if (lane == 0) {
             const int32_t rows = min(kCB, d - kCB * g.ci);
-            const uint32_t bytes = 2u * static_cast<uint32_t>(rows * r);
+            constexpr int32_t kEB = kF8 ? 1 : 2;
+            const uint32_t bytes = kEB * static_cast<uint32_t>(rows * r);
             const unsigned char *src = reinterpret_cast<const unsigned char *>(t.bptr[t.a_slot[ja] * sh.n + g.i]) +
-                                       2 * static_cast<int64_t>(kCB * g.ci) * r;
+                                       kEB * static_cast<int64_t>(kCB * g.ci) * r;
             mbar_expect_tx(bar, bytes);
             bulk_copy(wslot, src, bytes, bar);
         }
@@ -819,6 +940,9 @@ __device__ __forceinline__ void e_load_xa(const EGen &g, const float *buf, const
     }
 }
 
+// kF8: B rows are e4m3 and enter an f16 MMA (exact conversion); the sums are
+// then rounded once to f16 instead of bf16.
+template <bool kF8>
 __device__ __forceinline__ void e_compute(const EGen &g, uint32_t wslot, const float4 (&X)[2][2][2], const Tabs &t,
                                           const DArgs &a, int lane) {
     const int32_t gq = lane >> 2, q = lane & 3;
@@ -837,22 +961,43 @@ __device__ __forceinline__ void e_compute(const EGen &g, uint32_t wslot, const f
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                bh[nt][h][0] = pack_bf16x2(X[nt][kb][h].x, X[nt][kb][h].y);
-                bh[nt][h][1] = pack_bf16x2(X[nt][kb][h].z, X[nt][kb][h].w);
+                if (kF8) {
+                    bh[nt][h][0] = pack_f16x2(X[nt][kb][h].x, X[nt][kb][h].y);
+                    bh[nt][h][1] = pack_f16x2(X[nt][kb][h].z, X[nt][kb][h].w);
+                } else {
+                    bh[nt][h][0] = pack_bf16x2(X[nt][kb][h].x, X[nt][kb][h].y);
+                    bh[nt][h][1] = pack_bf16x2(X[nt][kb][h].z, X[nt][kb][h].w);
+                }
             }
         const int32_t rc = 32 * kb + 8 * q;
         const bool vk = rc < r;
-        // B row 8 gq + 2 mt (+1) at ranks rc..rc+7: byte 2 (row r + rc) of the tile
-        const uint32_t brow = wslot + 2u * static_cast<uint32_t>(8 * gq * r + rc);
+        // B row 8 gq + 2 mt (+1) at ranks rc..rc+7: byte kEB (row r + rc) of the tile
+        constexpr uint32_t kEB = kF8 ? 1u : 2u;
+        const uint32_t brow = wslot + kEB * static_cast<uint32_t>(8 * gq * r + rc);
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
-            const uint4 c0 = vk ? lds16(brow + 2u * static_cast<uint32_t>(2 * mt * r)) : make_uint4(0, 0, 0, 0);
-            const uint4 c1 = vk ? lds16(brow + 2u * static_cast<uint32_t>((2 * mt + 1) * r)) : make_uint4(0, 0, 0, 0);
+            uint4 c0, c1;
+            if (kF8) {
+                const uint2 v0 = vk ? lds8(brow + static_cast<uint32_t>(2 * mt * r)) : make_uint2(0, 0);
+                const uint2 v1 = vk ? lds8(brow + static_cast<uint32_t>((2 * mt + 1) * r)) : make_uint2(0, 0);
+                c0 = make_uint4(f16x2_from_e4m3x2(v0.x), f16x2_from_e4m3x2(v0.x >> 16), f16x2_from_e4m3x2(v0.y),
+                                f16x2_from_e4m3x2(v0.y >> 16));
+                c1 = make_uint4(f16x2_from_e4m3x2(v1.x), f16x2_from_e4m3x2(v1.x >> 16), f16x2_from_e4m3x2(v1.y),
+                                f16x2_from_e4m3x2(v1.y >> 16));
+            } else {
+                c0 = vk ? lds16(brow + 2u * static_cast<uint32_t>(2 * mt * r)) : make_uint4(0, 0, 0, 0);
+                c1 = vk ? lds16(brow + 2u * static_cast<uint32_t>((2 * mt + 1) * r)) : make_uint4(0, 0, 0, 0);
+            }
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 if (nt >= NT8) continue;
-                mma_bf16_16816(acc[mt][nt], c0.x, c1.x, c0.y, c1.y, bh[nt][0][0], bh[nt][0][1]);
-                mma_bf16_16816(acc[mt][nt], c0.z, c1.z, c0.w, c1.w, bh[nt][1][0], bh[nt][1][1]);
+                if (kF8) {
+                    mma_f16_16816(acc[mt][nt], c0.x, c1.x, c0.y, c1.y, bh[nt][0][0], bh[nt][0][1]);
+                    mma_f16_16816(acc[mt][nt], c0.z, c1.z, c0.w, c1.w, bh[nt][1][0], bh[nt][1][1]);
+                } else {
+                    mma_bf16_16816(acc[mt][nt], c0.x, c1.x, c0.y, c1.y, bh[nt][0][0], bh[nt][0][1]);
+                    mma_bf16_16816(acc[mt][nt], c0.z, c1.z, c0.w, c1.w, bh[nt][1][0], bh[nt][1][1]);
+                }
             }
         }
     }
@@ -885,6 +1030,7 @@ size_t direct_expand_smem(int32_t S, int32_t n, int32_t T) {
     return static_cast<size_t>(kEWarps) * kEStages * kESlot + tabs_bytes(S, n, T);
 }
 
+template <bool kF8>
 __global__ void __launch_bounds__(32 * kEWarps, 1) direct_expand_kernel(DArgs a, Shape sh, const void *table) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t bars[kEWarps][kEStages];
@@ -895,14 +1041,14 @@ __global__ void __launch_bounds__(32 * kEWarps, 1) direct_expand_kernel(DArgs a,
     }
     const Tabs t = carve(smem + static_cast<size_t>(kEWarps) * kEStages * kESlot, sh.S, sh.n, a.T);
     // tables, B and y are not written by the shrink: read them before the wait
-    build_tabs<true>(a, sh, table, t);
+    build_tabs<true>(a, sh, table, t, kF8 ? 4 : 8, 1, 32);
     const float *buf = (t.misc[1] & 1) ? a.acc1 : a.acc0;
     const uint32_t wring = sa(smem) + warp * (kEStages * kESlot);
     EGen gi;
     e_first(gi, t, sh.n);
     EGen gc = gi;
 #pragma unroll
-    for (int s = 0; s < kEStages - 1; ++s) e_copy_stage(gi, wring + s * kESlot, sa(&bars[warp][s]), t, sh, a, lane, sh.n);
+    for (int s = 0; s < kEStages - 1; ++s) e_copy_stage<kF8>(gi, wring + s * kESlot, sa(&bars[warp][s]), t, sh, a, lane, sh.n);
     pdl_wait();
     float4 X[2][2][2];
     e_load_xa(gc, buf, t, sh, a.T, lane, X);
@@ -911,7 +1057,7 @@ __global__ void __launch_bounds__(32 * kEWarps, 1) direct_expand_kernel(DArgs a,
     while (gc.live) {
         const int32_t sn = (it + kEStages - 1) % kEStages, sc = it % kEStages;
         __syncwarp();  // every lane's reads of the slot refilled next are done
-        e_copy_stage(gi, wring + sn * kESlot, sa(&bars[warp][sn]), t, sh, a, lane, sh.n);
+        e_copy_stage<kF8>(gi, wring + sn * kESlot, sa(&bars[warp][sn]), t, sh, a, lane, sh.n);
         EGen gn = gc;
         e_advance(gn, t, sh.n);
         // the next unit's sums: the same registers while (slot, slice, token group) holds
@@ -923,7 +1069,7 @@ __global__ void __launch_bounds__(32 * kEWarps, 1) direct_expand_kernel(DArgs a,
             timed_out = true;
             if (lane == 0) report_error(a.err, LORA_ERR_TIMEOUT);
         }
-        e_compute(gc, wring + sc * kESlot, X, t, a, lane);
+        e_compute<kF8>(gc, wring + sc * kESlot, X, t, a, lane);
         if (!same) {
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
@@ -947,19 +1093,46 @@ __global__ void __launch_bounds__(32 * kEWarps, 1) direct_expand_kernel(DArgs a,
     }
 }
 
+// Load-time scale of an FP8 B (TensorRT-LLM LoRA serving page, "第五步:FP8 特判"):
+// w[e] = e4m3(clamp(bf16(value(w[e]) * scale), +-448)), the product exact in
+// fp64 and rounded once to bf16; NaN codes become 0x7F.
+__global__ void premultiply_e4m3_kernel(uint8_t *w, int64_t n, double scale) {
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint32_t h = f16x2_from_e4m3x2(w[e]);
+        const double v = static_cast<double>(__half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xffffu))));
+        const float b = __bfloat162float(__double2bfloat16(v * scale));
+        uint32_t c;
+        asm("{\n\t.reg .b16 p;\n\t"
+            "cvt.rn.satfinite.e4m3x2.f32 p, %1, %1;\n\t"
+            "cvt.u32.u16 %0, p;\n\t}"
+            : "=r"(c) : "f"(b));
+        w[e] = isnan(b) ? uint8_t(0x7F) : static_cast<uint8_t>(c & 0xffu);
+    }
+}
+
 }  // namespace
 
-bool decode_direct_supported(int32_t T, const Shape &sh) {
+cudaError_t launch_premultiply_e4m3(uint8_t *w, int64_t n, double scale, cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    const int64_t blocks = std::min<int64_t>((n + 255) / 256, 152 * 16);
+    premultiply_e4m3_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(w, n, scale);
+    return cudaGetLastError();
+}
+
+// fp8: A and B in float8_e4m3fn, whose rows of k bytes must stay 16-byte aligned.
+bool decode_direct_supported(int32_t T, const Shape &sh, bool fp8) {
     return T >= 1 && T <= kMaxTokens && sh.r_max <= kMaxRank && sh.S <= kMaxSlots && sh.S * sh.n <= kMaxPtrs &&
-           direct_shrink_smem(sh.S, sh.n, T) <= 227 * 1024 && direct_expand_smem(sh.S, sh.n, T) <= 227 * 1024;
+           (!fp8 || sh.k % 16 == 0) && direct_shrink_smem(sh.S, sh.n, T) <= 227 * 1024 &&
+           direct_expand_smem(sh.S, sh.n, T) <= 227 * 1024;
 }
 
 namespace {
 
 cudaError_t direct_args(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                         const int32_t *sorted_ids, const int32_t *seg, const int32_t *active, float *ws, int32_t T,
-                        int32_t *err, DArgs &a, int &num_sms) {
-    if (!decode_direct_supported(T, sh)) return cudaErrorNotSupported;
+                        int32_t *err, bool fp8, DArgs &a, int &num_sms) {
+    if (!decode_direct_supported(T, sh, fp8)) return cudaErrorNotSupported;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -987,16 +1160,18 @@ cudaError_t direct_args(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy
 }  // namespace
 
 // The x-only half: sums of x A^T into the call's buffer (reads x, A; writes the
-// workspace only).
+// workspace only).  fp8: A is e4m3 and x is rounded to e4m3 on the way in.
 cudaError_t launch_direct_shrink(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                  const void *table, const int32_t *sorted_ids, const int32_t *seg,
-                                 const int32_t *active, float *ws, int32_t T, int32_t *err, cudaStream_t stream) {
+                                 const int32_t *active, float *ws, int32_t T, int32_t *err, bool fp8,
+                                 cudaStream_t stream) {
     DArgs a;
     int num_sms = 0;
-    cudaError_t e = direct_args(x, ldx, y, ldy, sh, sorted_ids, seg, active, ws, T, err, a, num_sms);
+    cudaError_t e = direct_args(x, ldx, y, ldy, sh, sorted_ids, seg, active, ws, T, err, fp8, a, num_sms);
     if (e != cudaSuccess) return e;
     const size_t s_smem = direct_shrink_smem(sh.S, sh.n, T);
-    e = cudaFuncSetAttribute(direct_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s_smem));
+    auto kern = fp8 ? direct_shrink_kernel<true> : direct_shrink_kernel<false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s_smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(num_sms));
@@ -1004,22 +1179,23 @@ cudaError_t launch_direct_shrink(const uint16_t *x, int64_t ldx, uint16_t *y, in
     cfg.dynamicSmemBytes = s_smem;
     cfg.stream = stream;
     cfg.numAttrs = 0;
-    return cudaLaunchKernelEx(&cfg, direct_shrink_kernel, a, sh, table);
+    return cudaLaunchKernelEx(&cfg, kern, a, sh, table);
 }
 
-// The y half: y += s (x A^T) B^T from the buffer the shrink of this call filled.
-// `programmatic`: launched as a programmatic dependent of that shrink (it must
-// then directly follow it on the stream).
+// The y half: y += s (x A^T) B^T from the buffer the shrink of this call filled
+// (fp8: B is e4m3).  `programmatic`: launched as a programmatic dependent of
+// that shrink (it must then directly follow it on the stream).
 cudaError_t launch_direct_expand(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                  const void *table, const int32_t *sorted_ids, const int32_t *seg,
-                                 const int32_t *active, float *ws, int32_t T, int32_t *err, bool programmatic,
-                                 cudaStream_t stream) {
+                                 const int32_t *active, float *ws, int32_t T, int32_t *err, bool fp8,
+                                 bool programmatic, cudaStream_t stream) {
     DArgs a;
     int num_sms = 0;
-    cudaError_t e = direct_args(x, ldx, y, ldy, sh, sorted_ids, seg, active, ws, T, err, a, num_sms);
+    cudaError_t e = direct_args(x, ldx, y, ldy, sh, sorted_ids, seg, active, ws, T, err, fp8, a, num_sms);
     if (e != cudaSuccess) return e;
     const size_t e_smem = direct_expand_smem(sh.S, sh.n, T);
-    e = cudaFuncSetAttribute(direct_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(e_smem));
+    auto kern = fp8 ? direct_expand_kernel<true> : direct_expand_kernel<false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(e_smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(num_sms));
@@ -1031,15 +1207,16 @@ cudaError_t launch_direct_expand(const uint16_t *x, int64_t ldx, uint16_t *y, in
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = programmatic ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, direct_expand_kernel, a, sh, table);
+    return cudaLaunchKernelEx(&cfg, kern, a, sh, table);
 }
 
 cudaError_t launch_decode_direct(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                  const void *table, const int32_t *sorted_ids, const int32_t *seg,
-                                 const int32_t *active, float *ws, int32_t T, int32_t *err, cudaStream_t stream) {
-    cudaError_t e = launch_direct_shrink(x, ldx, y, ldy, sh, table, sorted_ids, seg, active, ws, T, err, stream);
+                                 const int32_t *active, float *ws, int32_t T, int32_t *err, bool fp8,
+                                 cudaStream_t stream) {
+    cudaError_t e = launch_direct_shrink(x, ldx, y, ldy, sh, table, sorted_ids, seg, active, ws, T, err, fp8, stream);
     if (e != cudaSuccess) return e;
-    return launch_direct_expand(x, ldx, y, ldy, sh, table, sorted_ids, seg, active, ws, T, err, true, stream);
+    return launch_direct_expand(x, ldx, y, ldy, sh, table, sorted_ids, seg, active, ws, T, err, fp8, true, stream);
 }
 
 }  // namespace lora

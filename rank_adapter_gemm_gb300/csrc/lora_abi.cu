@@ -21,6 +21,7 @@ cudaError_t launch_fused_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int
                                 const void *table, const int32_t *sorted_ids, const int32_t *seg,
                                 float *ws, int32_t T, int32_t *err, cudaStream_t stream);
 cudaError_t launch_premultiply(uint16_t *w, int64_t n, float scale, cudaStream_t stream);
+cudaError_t launch_premultiply_e4m3(uint8_t *w, int64_t n, double scale, cudaStream_t stream);
 bool prefill_supported(int32_t r_max);
 bool decode_tc_supported(int32_t T, const Shape &sh);
 bool decode_stream_supported(int32_t T, const Shape &sh);
@@ -31,17 +32,19 @@ cudaError_t launch_decode_tc(const uint16_t *x, int64_t ldx, uint16_t *y, int64_
                             const void *table, const int32_t *sorted_ids, const int32_t *seg, float *ws, int32_t T,
                             int32_t *err, cudaStream_t stream);
 bool fused_decode_supported(int32_t T, int32_t r_max, int32_t k);
-bool decode_direct_supported(int32_t T, const Shape &sh);
+bool decode_direct_supported(int32_t T, const Shape &sh, bool fp8);
 cudaError_t launch_direct_shrink(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                  const void *table, const int32_t *sorted_ids, const int32_t *seg,
-                                 const int32_t *active, float *ws, int32_t T, int32_t *err, cudaStream_t stream);
+                                 const int32_t *active, float *ws, int32_t T, int32_t *err, bool fp8,
+                                 cudaStream_t stream);
 cudaError_t launch_direct_expand(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                  const void *table, const int32_t *sorted_ids, const int32_t *seg,
-                                 const int32_t *active, float *ws, int32_t T, int32_t *err, bool programmatic,
-                                 cudaStream_t stream);
+                                 const int32_t *active, float *ws, int32_t T, int32_t *err, bool fp8,
+                                 bool programmatic, cudaStream_t stream);
 cudaError_t launch_decode_direct(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                  const void *table, const int32_t *sorted_ids, const int32_t *seg,
-                                 const int32_t *active, float *ws, int32_t T, int32_t *err, cudaStream_t stream);
+                                 const int32_t *active, float *ws, int32_t T, int32_t *err, bool fp8,
+                                 cudaStream_t stream);
 cudaError_t launch_prefill(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                            const void *table, const int32_t *sorted_ids, const int32_t *seg, float *ws,
                            int32_t T, int32_t *err, cudaStream_t stream);
@@ -114,7 +117,7 @@ lora_path_t resolve(lora_path_t path, int32_t T, int32_t max_seg_hint, const Sha
         // measured on GB300: the warp-streaming kernels lead from a few hundred
         // tokens up; at 64 tokens and fewer the split kernels' shorter prologue wins
         if (max_seg_hint > LORA_DECODE_MAX_SEG && lora::prefill_supported(sh.r_max)) path = LORA_PATH_PREFILL;
-        else if (T > kSmallDecodeT && lora::decode_direct_supported(T, sh)) path = LORA_PATH_DECODE_DIRECT;
+        else if (T > kSmallDecodeT && lora::decode_direct_supported(T, sh, false)) path = LORA_PATH_DECODE_DIRECT;
         else if (T > kSmallDecodeT && fused_ok(T, sh)) path = LORA_PATH_DECODE_FUSED;
         else path = LORA_PATH_DECODE_SPLIT;
     }
@@ -161,6 +164,12 @@ lora_status_t lora_premultiply(void *w, int64_t n, float scale, lora_stream_t st
     if ((reinterpret_cast<uintptr_t>(w) & 1u) != 0) return LORA_ERR_ALIGNMENT;
     return from_cuda(lora::launch_premultiply(static_cast<uint16_t *>(w), n, scale,
                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_premultiply_e4m3(void *w, int64_t n, float scale, lora_stream_t stream) {
+    if (n < 0 || (n > 0 && w == nullptr)) return LORA_ERR_INVALID_ARG;
+    return from_cuda(lora::launch_premultiply_e4m3(static_cast<uint8_t *>(w), n, static_cast<double>(scale),
+                                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t lora_slot_table_bytes(int32_t S, int32_t n_slices) {
@@ -331,9 +340,12 @@ lora_status_t lora_apply_ex(const void *x, int64_t ldx, void *y, int64_t ldy, in
         return from_cuda(lora::launch_decode_stream(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws, T,
                                                     err, s));
     case LORA_PATH_DECODE_DIRECT:
-        if (!lora::decode_direct_supported(T, sh)) return LORA_ERR_UNSUPPORTED;
+    case LORA_PATH_DECODE_DIRECT_FP8: {
+        const bool fp8 = path == LORA_PATH_DECODE_DIRECT_FP8;
+        if (!lora::decode_direct_supported(T, sh, fp8)) return LORA_ERR_UNSUPPORTED;
         return from_cuda(lora::launch_decode_direct(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, active,
-                                                    ws, T, err, s));
+                                                    ws, T, err, fp8, s));
+    }
     case LORA_PATH_DECODE_SPLIT: {
         float *xa = xa_of(ws, T, sh);
         cudaError_t e = lora::launch_shrink(xb, ldx, sh, dev_table, sorted_ids, seg_offsets, xa, T, err, true, s);
@@ -367,13 +379,15 @@ lora_status_t lora_apply_overlap(const void *x, int64_t ldx, void *y, int64_t ld
     const lora_path_t p = T == 0 ? LORA_PATH_DECODE_SPLIT : resolve(path, T, max_seg_hint, sh, nullptr);
     const uint16_t *xb = static_cast<const uint16_t *>(x);
     uint16_t *yb = static_cast<uint16_t *>(y);
-    if (T > 0 && p == LORA_PATH_DECODE_DIRECT && lora::decode_direct_supported(T, sh)) {
+    const bool fp8 = p == LORA_PATH_DECODE_DIRECT_FP8;
+    if (T > 0 && (p == LORA_PATH_DECODE_DIRECT || fp8)) {
+        if (!lora::decode_direct_supported(T, sh, fp8)) return LORA_ERR_UNSUPPORTED;
         if (lora::launch_direct_shrink(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, active, ws, T, err,
-                                       s) != cudaSuccess)
+                                       fp8, s) != cudaSuccess)
             return LORA_ERR_CUDA;
         if (ev != nullptr && cudaStreamWaitEvent(s, ev, 0) != cudaSuccess) return LORA_ERR_CUDA;
         return from_cuda(lora::launch_direct_expand(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, active,
-                                                    ws, T, err, false, s));
+                                                    ws, T, err, fp8, false, s));
     }
     if (T > 0 && p == LORA_PATH_DECODE_SPLIT) {
         float *xa = xa_of(ws, T, sh);

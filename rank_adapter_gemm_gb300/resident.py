@@ -1,9 +1,10 @@
 """Put one packed projection's adapters, activations and slot table on the device.
 
-Marshalling only: numpy bf16 bit patterns become torch bf16 device tensors,
-per-slot scales come from the library's lora_scale, a pre-multiplied scale is
-folded into B by the library's lora_premultiply kernel, and the pointer table
-is uploaded with lora_set_slot_table.
+Marshalling only: numpy bf16 bit patterns become torch bf16 device tensors
+(numpy uint8 float8_e4m3fn codes become torch uint8 tensors), per-slot scales
+come from the library's lora_scale, a pre-multiplied scale is folded into B by
+the library's lora_premultiply (or lora_premultiply_e4m3) kernel, and the
+pointer table is uploaded with lora_set_slot_table.
 """
 from __future__ import annotations
 
@@ -11,7 +12,7 @@ from typing import List, Optional, Sequence
 
 import numpy as np
 
-from . import SlotTable, lora_premultiply, lora_scale, make_shape
+from . import SlotTable, lora_premultiply, lora_premultiply_e4m3, lora_scale, make_shape
 
 
 def _to_dev(bits: np.ndarray, device):
@@ -20,11 +21,20 @@ def _to_dev(bits: np.ndarray, device):
     return t.to(device).view(torch.bfloat16)
 
 
+def _w_to_dev(w: np.ndarray, device):
+    """A weight matrix: bf16 bits (uint16) or e4m3 codes (uint8, kept as bytes)."""
+    if w.dtype == np.uint8:
+        import torch
+        return torch.from_numpy(np.ascontiguousarray(w)).to(device)
+    return _to_dev(w, device)
+
+
 class ResidentProjection:
     """Adapter weights of S slots for one projection plus its x and y rows.
 
-    A[s][i] is [r_s, k], B[s][i] is [d_i, r_s] (bf16 bit patterns); rank-0
-    slots have None.  ``scale_rule`` is "alpha_over_r" or "alpha_over_sqrt_r";
+    A[s][i] is [r_s, k], B[s][i] is [d_i, r_s] (bf16 bit patterns, or uint8
+    float8_e4m3fn codes for every matrix: then ``fp8`` is True and the table
+    serves the FP8 path); rank-0 slots have None.  ``scale_rule`` is "alpha_over_r" or "alpha_over_sqrt_r";
     with ``premultiplied`` the rule's scale is folded into B and the table
     carries scale 1.
     """
@@ -44,14 +54,17 @@ class ResidentProjection:
         self.B: List[List] = []
         a_ptrs = np.zeros(S * self.n, dtype=np.uint64)
         b_ptrs = np.zeros(S * self.n, dtype=np.uint64)
+        mats = [m for row in A for m in row if m is not None]
+        self.fp8 = bool(mats) and mats[0].dtype == np.uint8
+        premul = lora_premultiply_e4m3 if self.fp8 else lora_premultiply
         for s in range(S):
             rowA, rowB = [], []
             for i in range(self.n):
                 if self.ranks[s] > 0:
-                    ta = _to_dev(A[s][i], device)
-                    tb = _to_dev(B[s][i], device)
+                    ta = _w_to_dev(A[s][i], device)
+                    tb = _w_to_dev(B[s][i], device)
                     if premultiplied:
-                        lora_premultiply(tb, float(rule_scales[s]))
+                        premul(tb, float(rule_scales[s]))
                     a_ptrs[s * self.n + i] = ta.data_ptr()
                     b_ptrs[s * self.n + i] = tb.data_ptr()
                 else:

@@ -29,6 +29,21 @@ def oracle_y(wl, mod_idx=0, rows=None, y_in="module"):
     return y, st
 
 
+def oracle_y_e4m3(wl, mod_idx=0, rows=None):
+    """fp64 reference rows for FP8 adapters (A, B e4m3 codes; x rounded to e4m3),
+    a pre-multiplied B scaled in bf16 and clamped back to e4m3 as the pages say."""
+    m = wl.modules[mod_idx]
+    rule = oracle.slot_scales(wl.ranks, wl.alphas, wl.scale_rule, False)
+    if wl.premultiplied:
+        scales = np.ones(wl.S)
+        B = [[(oracle.premultiply_e4m3(b, rule[s]) if b is not None else None) for b in row]
+             for s, row in enumerate(m.B)]
+    else:
+        scales = rule
+        B = m.B
+    return oracle.apply_e4m3(m.x, m.y_in, m.slice_widths, wl.slot_ids, wl.ranks, scales, m.A, B, rows=rows)
+
+
 def gpu_apply(wl, mod_idx=0, path="auto", max_seg_hint=0, repeat=1):
     import torch
     import rank_adapter_gemm_gb300 as L

@@ -24,7 +24,7 @@ def L():
 def _declared():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(lora_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(lora_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declarations_are_exported(L):
@@ -32,7 +32,7 @@ def test_header_declarations_are_exported(L):
     declared = _declared()
     assert set(declared) == set(_lib.EXPORTED)
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.library_path()], capture_output=True, text=True).stdout
-    exported = set(re.findall(r" T (lora_[a-z_]+)$", out, flags=re.M))
+    exported = set(re.findall(r" T (lora_[a-z0-9_]+)$", out, flags=re.M))
     for name in declared:
         assert name in exported, name
     lib = _lib.load()

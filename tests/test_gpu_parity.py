@@ -584,3 +584,122 @@ def test_apply_with_base_on_aux_stream(path):
     assert int(idx.err.item()) == 0
     ref, _ = oracle_y(wl, y_in=base_bits)
     assert_y_close(to_host_bits(rp.y), ref, f"with base ({path})")
+
+
+# ---------------------------------------------------------------------------
+# FP8 adapters (LORA_PATH_DECODE_DIRECT_FP8) against the e4m3 oracle
+# ---------------------------------------------------------------------------
+def _small_fp8(seed, T, k, widths, S, ranks, frac_none=0.1, slot_dist="uniform", premultiplied=False):
+    wl = W.generate(name="case_fp8", seed=seed, T=T, S=S, rank=8, modules=[{"name": "m", "k": k, "slices": widths}],
+                    slot_dist=slot_dist, frac_none=frac_none, alpha=1.0 / 32.0, premultiplied=premultiplied,
+                    weights="e4m3")
+    rng = np.random.Generator(np.random.PCG64(seed + 7))
+    wl.ranks = np.asarray(ranks, dtype=np.int32)
+    wl.r_max = max(8, int(max(ranks)))
+    m = wl.modules[0]
+    m.A = [[(W._e4m3_codes(rng, (r, k)) if r > 0 else None) for _ in widths] for r in wl.ranks]
+    m.B = [[(W._e4m3_codes(rng, (w, r)) if r > 0 else None) for w in widths] for r in wl.ranks]
+    wl.alphas = np.full(S, 1.0 / 32.0)
+    return wl
+
+
+def _check_fp8(wl, what, repeat=1, overlap=False):
+    from _parity import oracle_y_e4m3
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import ResidentProjection, to_host_bits
+    rp = ResidentProjection.from_workload(wl)
+    assert rp.fp8
+    idx = L.TokenIndex(wl.T, wl.S)
+    idx.build(torch.from_numpy(np.ascontiguousarray(wl.slot_ids, dtype=np.int32)).cuda(), rp.table)
+    ws = L.Workspace(wl.T, rp.shape)
+    y0 = rp.y.clone()
+    ref, st = oracle_y_e4m3(wl)
+    assert st == 0
+    keep = untouched_rows(wl)
+    for _ in range(repeat):
+        rp.y.copy_(y0)
+        if overlap:
+            ev = torch.cuda.Event()
+            ev.record()
+            L.lora_apply_overlap(rp.x, rp.y, rp.shape, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active,
+                                 ws.buf, idx.err, y_ready=ev, path="decode_direct_fp8")
+        else:
+            L.lora_apply(rp.x, rp.y, rp.shape, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active, ws.buf,
+                         idx.err, path="decode_direct_fp8")
+        torch.cuda.synchronize()
+        assert int(idx.err.item()) == 0
+        y = to_host_bits(rp.y)
+        assert_y_close(y, ref, what)
+        np.testing.assert_array_equal(y[keep], wl.modules[0].y_in[keep])
+
+
+@pytest.mark.parametrize("y_init", ["zeros", "normal"])
+def test_apply_fp8_decode_qkv(y_init):
+    """Packed QKV decode (T=256, Llama-3-8B shapes, S=32, Zipf) with e4m3 adapters."""
+    _check_fp8(W.config(6, y_init=y_init), f"fp8 qkv {y_init}")
+
+
+def test_apply_fp8_repeat_and_overlap():
+    """The call counter and the two sum buffers stay consistent over calls, with
+    and without the y-ready event split."""
+    wl = W.config(6)
+    _check_fp8(wl, "fp8 repeat", repeat=3)
+    _check_fp8(wl, "fp8 overlap", repeat=2, overlap=True)
+
+
+FP8_RAGGED = [
+    # seed, T, k, widths, S, ranks
+    (61, 37, 256, [256], 3, [8, 16, 64]),
+    (62, 300, 4112, [4096, 1032, 520], 5, [64, 8, 0, 32, 24]),
+    (63, 1, 1024, [2048], 1, [64]),
+    (64, 700, 2048, [8, 136, 1000], 7, [8, 16, 24, 32, 40, 48, 56]),
+    (65, 2048, 512, [512], 2, [64, 16]),
+]
+
+
+@pytest.mark.parametrize("case", FP8_RAGGED, ids=[f"fp8ragged{c[0]}" for c in FP8_RAGGED])
+def test_apply_fp8_ragged(case):
+    """Token groups of 24 with ragged tails, k not a multiple of 64, slice widths
+    not multiples of 64, ranks 8..64, a single token and the 2048-token maximum."""
+    seed, T, k, widths, S, ranks = case
+    _check_fp8(_small_fp8(seed, T, k, widths, S, ranks), f"fp8 ragged {seed}")
+
+
+def test_apply_fp8_premultiplied_and_clamped_x():
+    """B scaled at load time by lora_premultiply_e4m3, and x entries beyond the
+    e4m3 range (clamped to +-448 before rounding).  A few saturated entries per
+    row: the sums enter the expand rounded to f16 (2^-11 of each sum), so rows
+    with dozens of them (sums in the thousands) and a cancelling y fall outside
+    the y tolerance by construction."""
+    wl = _small_fp8(66, 200, 1024, [1024, 256], 4, [16, 64, 32, 8], premultiplied=True)
+    x = wl.modules[0].x
+    x[::7, ::301] = np.uint16(0x447A)   # bf16 1000.0
+    x[3::7, 5::257] = np.uint16(0xC3E8)  # bf16 -464.0
+    _check_fp8(wl, "fp8 premultiplied, clamped x")
+
+
+def test_apply_fp8_rejects_k_not_multiple_of_16():
+    import rank_adapter_gemm_gb300 as L
+    wl = _small_fp8(67, 40, 1032, [256], 2, [16, 16])
+    with pytest.raises(L.LoraError) as e:
+        _check_fp8(wl, "fp8 k % 16")
+    assert e.value.status == 9
+
+
+def test_premultiply_e4m3_kernel_bit_exact():
+    """Every finite e4m3 code times scales that round, tie, clamp and underflow,
+    against the oracle bit for bit; NaN codes become 0x7F."""
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    for s in (2.0, 0.3, 1.0 / 256.0, 100.0, 0.0078125, 3.0, -1.5, 1e-3):
+        t = torch.from_numpy(np.tile(codes, 3)).cuda()
+        L.lora_premultiply_e4m3(t, s)
+        torch.cuda.synchronize()
+        want = oracle.premultiply_e4m3(np.tile(codes, 3), float(np.float32(s)))
+        np.testing.assert_array_equal(t.cpu().numpy(), want, err_msg=f"scale {s}")
+    t = torch.tensor([0x7F, 0xFF, 0x01], dtype=torch.uint8, device="cuda")
+    L.lora_premultiply_e4m3(t, 2.0)
+    torch.cuda.synchronize()
+    assert t.cpu().numpy().tolist()[:2] == [0x7F, 0x7F]

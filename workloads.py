@@ -7,7 +7,8 @@ product, no scale rule and no index here.  Ranks, alphas, the scale rule's name
 and the "pre-multiplied into B" flag are returned as plain data, and each
 consumer derives the per-slot scale (and any pre-multiplied B) with its own code.
 
-Layouts (PEFT orientation, row-major, bf16 stored as uint16 bit patterns):
+Layouts (PEFT orientation, row-major, bf16 stored as uint16 bit patterns; FP8
+weights as uint8 float8_e4m3fn codes):
   x    [T, k]        one row per token
   A    [r_s, k]      per slot s and output slice i (``mod.A[s][i]``)
   B    [d_i, r_s]    per slot s and output slice i (``mod.B[s][i]``)
@@ -17,7 +18,10 @@ Generation rules (all configs): numpy PCG64, seed ``1000 + config index``;
 draw order slot_ids, ranks, then per module x, A (slot-major, slice-minor),
 B (same order), y_in; values drawn in fp32 and rounded to bf16 with
 round-to-nearest-even.  A ~ N(0, 1/k) (variance 1/k), B ~ N(0, 0.02^2)
-(standard deviation 0.02), x ~ N(0, 1), y_in ~ N(0, 1) (or zeros).
+(standard deviation 0.02), x ~ N(0, 1), y_in ~ N(0, 1) (or zeros).  FP8
+weights (``weights="e4m3"``) are drawn as codes, not rounded from values: sign
+uniform, exponent field uniform in {3..7} (magnitudes 2^-4 .. 1.875), mantissa
+field uniform in {0..7}; the adapters' real magnitude then lives in the scale.
 """
 from __future__ import annotations
 
@@ -48,6 +52,14 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
+def _e4m3_codes(rng: np.random.Generator, shape: Sequence[int]) -> np.ndarray:
+    """float8_e4m3fn codes: sign, exponent field in {3..7}, mantissa field in {0..7}."""
+    sign = rng.integers(0, 2, size=shape, dtype=np.uint8)
+    expo = rng.integers(3, 8, size=shape, dtype=np.uint8)
+    mant = rng.integers(0, 8, size=shape, dtype=np.uint8)
+    return ((sign << np.uint8(7)) | (expo << np.uint8(3)) | mant).astype(np.uint8)
+
+
 def _normal_bf16(rng: np.random.Generator, shape: Sequence[int], std: float,
                  chunk_rows: int = 2048) -> np.ndarray:
     """Draw N(0, std^2) in fp32 row-chunk by row-chunk and round to bf16 bits."""
@@ -76,8 +88,8 @@ class Module:
     slice_widths: List[int]
     x: np.ndarray                                  # uint16 [T, k]
     y_in: np.ndarray                               # uint16 [T, d]
-    A: List[List[Optional[np.ndarray]]]            # [S][n] uint16 [r_s, k] (None if r_s == 0)
-    B: List[List[Optional[np.ndarray]]]            # [S][n] uint16 [d_i, r_s]
+    A: List[List[Optional[np.ndarray]]]            # [S][n] uint16 (uint8 for e4m3) [r_s, k] (None if r_s == 0)
+    B: List[List[Optional[np.ndarray]]]            # [S][n] uint16 (uint8 for e4m3) [d_i, r_s]
 
     @property
     def n_slices(self) -> int:
@@ -110,6 +122,7 @@ class Workload:
     seed: int
     description: str = ""
     tokens_per_seq: int = 1       # speculative decode: sequences of this many tokens, sequence-major
+    weights: str = "bf16"         # "bf16" or "e4m3" (A and B as float8_e4m3fn codes)
 
 
 # ----------------------------------------------------------------------------
@@ -149,7 +162,8 @@ def generate(*, name: str, seed: int, T: Optional[int], S: int,
              zipf_exponent: float = 1.1, alpha: Optional[float] = None,
              alpha_times_rank: Optional[float] = None, scale_rule: str = "alpha_over_r",
              premultiplied: bool = False, requests: Optional[Dict] = None,
-             y_init: str = "normal", description: str = "", tokens_per_seq: int = 1) -> Workload:
+             y_init: str = "normal", description: str = "", tokens_per_seq: int = 1,
+             weights: str = "bf16") -> Workload:
     """Draw one workload.
 
     ``modules`` is a list of ``{"name", "k", "slices"}`` dicts.  Slots get either
@@ -159,6 +173,7 @@ def generate(*, name: str, seed: int, T: Optional[int], S: int,
     prefill batch: lengths uniform in [min_len, max_len], one adapter per request
     drawn uniformly.  ``tokens_per_seq`` > 1 draws one slot per sequence of that
     many consecutive tokens (speculative decode; T must be a multiple).
+    ``weights="e4m3"`` draws A and B as float8_e4m3fn codes (module docstring).
     """
     rng = np.random.Generator(np.random.PCG64(seed))
     # 1. slot ids
@@ -189,10 +204,16 @@ def generate(*, name: str, seed: int, T: Optional[int], S: int,
         widths = [int(w) for w in m["slices"]]
         d = sum(widths)
         x = _normal_bf16(rng, (T, k), 1.0)
-        A = [[(_normal_bf16(rng, (int(ranks[s]), k), float(k) ** -0.5) if ranks[s] > 0 else None)
-              for _ in widths] for s in range(S)]
-        B = [[(_normal_bf16(rng, (w, int(ranks[s])), 0.02) if ranks[s] > 0 else None)
-              for w in widths] for s in range(S)]
+        if weights == "e4m3":
+            A = [[(_e4m3_codes(rng, (int(ranks[s]), k)) if ranks[s] > 0 else None)
+                  for _ in widths] for s in range(S)]
+            B = [[(_e4m3_codes(rng, (w, int(ranks[s]))) if ranks[s] > 0 else None)
+                  for w in widths] for s in range(S)]
+        else:
+            A = [[(_normal_bf16(rng, (int(ranks[s]), k), float(k) ** -0.5) if ranks[s] > 0 else None)
+                  for _ in widths] for s in range(S)]
+            B = [[(_normal_bf16(rng, (w, int(ranks[s])), 0.02) if ranks[s] > 0 else None)
+                  for w in widths] for s in range(S)]
         if y_init == "normal":
             y_in = _normal_bf16(rng, (T, d), 1.0)
         elif y_init == "zeros":
@@ -202,7 +223,8 @@ def generate(*, name: str, seed: int, T: Optional[int], S: int,
         mods.append(Module(name=m["name"], k=k, slice_widths=widths, x=x, y_in=y_in, A=A, B=B))
     return Workload(name=name, T=int(T), S=S, r_max=int(r_max), slot_ids=slot_ids, ranks=ranks,
                     alphas=alphas, scale_rule=scale_rule, premultiplied=premultiplied,
-                    modules=mods, seed=seed, description=description, tokens_per_seq=int(tokens_per_seq))
+                    modules=mods, seed=seed, description=description, tokens_per_seq=int(tokens_per_seq),
+                    weights=weights)
 
 
 # ----------------------------------------------------------------------------
@@ -215,11 +237,12 @@ LLAMA3_8B_LAYER = [
     {"name": "down", "k": 14336, "slices": [4096]},
 ]
 
-CONFIG_NAMES = ("tiny", "decode_q_proj", "decode_qkv", "prefill_mlp", "large_decode", "decode_qkv_spec")
+CONFIG_NAMES = ("tiny", "decode_q_proj", "decode_qkv", "prefill_mlp", "large_decode", "decode_qkv_spec",
+                "decode_qkv_fp8")
 
 
 def config(index: int, y_init: str = "normal", sweep: bool = False, n_requests: int = 16) -> Workload:
-    """Config ``index`` (0..5) of the benchmark suite, drawn at seed 1000+index.
+    """Config ``index`` (0..6) of the benchmark suite, drawn at seed 1000+index.
 
     0 tiny: T=8, k=d=256, one slice, S=2, r=8, slot ids uniform over {-1,0,1},
       alpha=16 (scale alpha/r applied at run time).
@@ -239,6 +262,8 @@ def config(index: int, y_init: str = "normal", sweep: bool = False, n_requests: 
     5 speculative decode, packed QKV (Llama-3-8B shapes): 64 sequences of 4
       tokens (one verified plus three draft tokens, T=256), one slot per sequence
       with Zipf(1.1) popularity over S=32, ranks from {8,16,32,64}, alpha=2r.
+    6 decode packed QKV with FP8 adapters: config 2's shapes and slot draw recipe,
+      A and B as float8_e4m3fn codes, alpha = r / 256 (scale 1/256 at run time).
     """
     seed = 1000 + index
     if index == 0:
@@ -278,4 +303,10 @@ def config(index: int, y_init: str = "normal", sweep: bool = False, n_requests: 
                         alpha_times_rank=2.0, y_init=y_init, tokens_per_seq=4,
                         description="64 sequences x 4 tokens (speculative decode), k=4096, "
                                     "slices 4096/1024/1024, S=32, r in {8,16,32,64}, Zipf(1.1) per sequence")
+    if index == 6:
+        return generate(name="decode_qkv_fp8", seed=seed, T=256, S=32, rank_choices=RANK_CHOICES,
+                        r_max=64, modules=[LLAMA3_8B_LAYER[0]], slot_dist="zipf",
+                        alpha_times_rank=1.0 / 256.0, y_init=y_init, weights="e4m3",
+                        description="T=256, k=4096, slices 4096/1024/1024, S=32, r in {8,16,32,64}, "
+                                    "Zipf(1.1), float8_e4m3fn adapters")
     raise IndexError(index)
