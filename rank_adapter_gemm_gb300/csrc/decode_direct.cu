@@ -77,6 +77,17 @@ constexpr int kTGs = 32;             // shrink token group
 constexpr int kCB = 64;              // expand output columns per unit
 constexpr int kTGe = 16;             // expand token group
 
+// Shrink and expand parameters of the bf16 (kF8 false) and e4m3 variants:
+// shrink token group, x chunks per 8 tokens, columns of k per block; expand B
+// chunks per 32 ranks.
+template <bool kF8>
+struct VP {
+    static constexpr int32_t TG = kF8 ? 24 : kTGs;
+    static constexpr int32_t XF = kF8 ? 2 : 1;
+    static constexpr int32_t BC = kF8 ? 64 : 32;
+    static constexpr int32_t BW = kF8 ? 4 : 8;
+};
+
 struct DArgs {
     const uint16_t *x;
     int64_t ldx;
@@ -330,9 +341,9 @@ __device__ __forceinline__ void cp8(void *dst, const void *src) {
 
 // Prologue: every table load of the CTA in flight at once, then the checks,
 // the per-active-slot records and their weight prefix.  Ends with a barrier.
-// Weight parameters, kept in misc[6] and misc[7]: for the shrink the token
-// group (tg), the x chunks per 8 tokens (xf) and the columns of k per block
-// (bc); for the expand tg is the B chunks per 32 ranks.
+// Weight parameters (VP): for the shrink the token group (tg), the x chunks per
+// 8 tokens (xf) and the columns of k per block (bc); for the expand tg is the B
+// chunks per 32 ranks.
 template <bool kExpand>
 __device__ void build_tabs(const DArgs &a, const Shape &sh, const void *table, const Tabs &t, int32_t tg,
                            int32_t xf, int32_t bc) {
@@ -345,8 +356,6 @@ __device__ void build_tabs(const DArgs &a, const Shape &sh, const void *table, c
         cp4(t.misc + 4, hdr + 1);
         cp4(t.misc + 5, hdr + 2);
         cp4(t.misc + 1, a.gen);
-        t.misc[6] = tg;
-        t.misc[7] = xf;
         int32_t c = 0, o = 0;
 #pragma unroll
         for (int i = 0; i <= LORA_MAX_SLICES; ++i) {
@@ -472,6 +481,7 @@ __device__ __forceinline__ void s_range(SGen &c, int32_t nkb) {
     if (c.be <= c.bs) c.live = false;
 }
 
+template <bool kF8>
 __device__ __forceinline__ void s_next_unit(SGen &c, const Tabs &t, int32_t n, int32_t nkb) {
     c.start += static_cast<long long>(nkb) * c.w;
     if (kRB * (++c.rb) >= t.a_r[c.ja]) {
@@ -488,15 +498,17 @@ __device__ __forceinline__ void s_next_unit(SGen &c, const Tabs &t, int32_t n, i
             }
         }
     }
-    c.w = s_block_w(t.a_r[c.ja], t.a_len[c.ja], c.rb, t.misc[6], t.misc[7]);
+    c.w = s_block_w(t.a_r[c.ja], t.a_len[c.ja], c.rb, VP<kF8>::TG, VP<kF8>::XF);
     c.bs = 0;
     s_range(c, nkb);
 }
 
+template <bool kF8>
 __device__ __forceinline__ void s_next_seg(SGen &c, const Tabs &t, int32_t n, int32_t nkb) {
-    if (t.misc[6] * (++c.g) >= t.a_len[c.ja]) s_next_unit(c, t, n, nkb);
+    if (VP<kF8>::TG * (++c.g) >= t.a_len[c.ja]) s_next_unit<kF8>(c, t, n, nkb);
 }
 
+template <bool kF8>
 __device__ __forceinline__ void s_first(SGen &c, const Tabs &t, int32_t n, int32_t nkb) {
     const int32_t NA = t.misc[0];
     c.ja = c.i = c.rb = c.g = c.bs = c.be = 0;  // defined fields for a warp without work
@@ -509,7 +521,7 @@ __device__ __forceinline__ void s_first(SGen &c, const Tabs &t, int32_t n, int32
     c.ja = find_active(t.a_pre, NA, R0);
     const int32_t r = t.a_r[c.ja], L = t.a_len[c.ja];
     long long o = R0 - t.a_pre[c.ja];
-    const int32_t tg = t.misc[6], xf = t.misc[7];
+    constexpr int32_t tg = VP<kF8>::TG, xf = VP<kF8>::XF;
     const long long wslice = s_slot_w(r, L, 1, nkb, tg, xf);
     c.i = static_cast<int32_t>(o / wslice);
     o -= c.i * wslice;
@@ -525,7 +537,7 @@ __device__ __forceinline__ void s_first(SGen &c, const Tabs &t, int32_t n, int32
     c.w = s_block_w(r, L, c.rb, tg, xf);
     c.bs = static_cast<int32_t>((o + c.w - 1) / c.w);
     if (c.bs >= nkb) {
-        s_next_unit(c, t, n, nkb);  // the share starts after this unit's last block start
+        s_next_unit<kF8>(c, t, n, nkb);  // the share starts after this unit's last block start
         return;
     }
     s_range(c, nkb);
@@ -548,7 +560,8 @@ struct SCopy {
 template <bool kF8>
 __device__ __forceinline__ void s_copy_seg(SCopy &s, const Tabs &t, const Shape &sh, const DArgs &a, int lane) {
     constexpr int32_t kEB = kF8 ? 1 : 2;  // bytes per weight
-    const int32_t gq = lane >> 2, q = lane & 3, tg = t.misc[6];
+    const int32_t gq = lane >> 2, q = lane & 3;
+    constexpr int32_t tg = VP<kF8>::TG;
     const int32_t ja = s.gen.ja, r = t.a_r[ja], L = t.a_len[ja], p0 = t.a_p0[ja];
     s.mt = s_mt(r, s.gen.rb);
     s.nt = s_nt8(L, s.gen.g, tg);
@@ -612,7 +625,7 @@ __device__ __forceinline__ void s_copy_stage(SCopy &s, uint32_t slot, int32_t kq
         }
         s.b += nb;
         if (s.b >= s.gen.be) {
-            s_next_seg(s.gen, t, sh.n, nkb);
+            s_next_seg<kF8>(s.gen, t, sh.n, nkb);
             if (s.gen.live) s_copy_seg<kF8>(s, t, sh, a, lane);
         }
     }
@@ -621,11 +634,12 @@ __device__ __forceinline__ void s_copy_stage(SCopy &s, uint32_t slot, int32_t kq
 
 // Lane 4 gq + q holds, for tokens 8 nt + 2q + e, the ranks 2 MT gq .. + 2 MT - 1
 // of the block: acc[mt][nt][e] is rank 2 MT gq + 2 mt, acc[mt][nt][2 + e] the next.
+template <bool kF8>
 __device__ __forceinline__ void s_reduce(const SGen &c, float *buf, const Tabs &t, const Shape &sh, int32_t T,
                                       int lane, const float (&acc)[2][4][4]) {
     const int32_t gq = lane >> 2, q = lane & 3;
     const int32_t r = t.a_r[c.ja], L = t.a_len[c.ja], p0 = t.a_p0[c.ja];
-    const int32_t tg = t.misc[6];
+    constexpr int32_t tg = VP<kF8>::TG;
     const int32_t MT = s_mt(r, c.rb), NT8 = s_nt8(L, c.g, tg);
     const int32_t rows = min(kRB, r - kRB * c.rb);
     float *base = buf + (static_cast<int64_t>(c.i) * T + p0 + tg * c.g) * sh.r_max + kRB * c.rb;
@@ -677,7 +691,7 @@ size_t direct_shrink_smem(int32_t S, int32_t n, int32_t T) {
 // token groups of 24 (a stage of 2 MT + 6 chunks holds one block).
 template <bool kF8>
 __global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a, Shape sh, const void *table) {
-    constexpr int32_t kTG = kF8 ? 24 : kTGs, kXF = kF8 ? 2 : 1, kBC = kF8 ? 64 : 32;
+    constexpr int32_t kTG = VP<kF8>::TG, kXF = VP<kF8>::XF, kBC = VP<kF8>::BC;
     extern __shared__ __align__(128) unsigned char smem[];
     // the expand may start its prologue as soon as every CTA of this grid runs
     pdl_launch_dependents();
@@ -699,7 +713,7 @@ __global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a,
     constexpr uint32_t kSlot = kSChunks * kChunk;
 
     SCopy cw;
-    s_first(cw.gen, t, sh.n, nkb);
+    s_first<kF8>(cw.gen, t, sh.n, nkb);
     if (cw.gen.live) s_copy_seg<kF8>(cw, t, sh, a, lane);
     SGen cg = cw.gen;  // compute walker
 #pragma unroll
@@ -783,8 +797,8 @@ __global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a,
         sc = sc + 1 == kSStages ? 0 : sc + 1;
         b += nb;
         if (b >= cg.be) {
-            s_reduce(cg, buf, t, sh, a.T, lane, acc);
-            s_next_seg(cg, t, sh.n, nkb);
+            s_reduce<kF8>(cg, buf, t, sh, a.T, lane, acc);
+            s_next_seg<kF8>(cg, t, sh.n, nkb);
             if (cg.live) {
                 b = cg.bs;
                 MT = s_mt(t.a_r[cg.ja], cg.rb);
@@ -820,9 +834,10 @@ struct EGen {
 
 // Units of a slot in the order (slice, token group, column block): consecutive
 // units of a warp mostly share their tokens' sums, which stay in registers.
+template <bool kF8>
 __device__ __forceinline__ void e_advance(EGen &c, const Tabs &t, int32_t n) {
     const int32_t r = t.a_r[c.ja], L = t.a_len[c.ja];
-    c.start += e_unit_w(r, L, c.tg, t.misc[6]);
+    c.start += e_unit_w(r, L, c.tg, VP<kF8>::BW);
     if (t.scb[c.i] + (++c.ci) == t.scb[c.i + 1]) {
         c.ci = 0;
         if (kTGe * (++c.tg) >= L) {
@@ -840,6 +855,7 @@ __device__ __forceinline__ void e_advance(EGen &c, const Tabs &t, int32_t n) {
     if (c.start >= c.R1) c.live = false;
 }
 
+template <bool kF8>
 __device__ __forceinline__ void e_first(EGen &c, const Tabs &t, int32_t n) {
     const int32_t NA = t.misc[0];
     c.ja = c.i = c.tg = c.ci = 0;  // defined fields for a warp without work
@@ -851,7 +867,7 @@ __device__ __forceinline__ void e_first(EGen &c, const Tabs &t, int32_t n) {
     c.ja = find_active(t.a_pre, NA, R0);
     const int32_t r = t.a_r[c.ja], L = t.a_len[c.ja];
     long long o = R0 - t.a_pre[c.ja];
-    const int32_t bw = t.misc[6];
+    constexpr int32_t bw = VP<kF8>::BW;
     const long long wcb = e_cb_w(r, L, bw);
     c.start = t.a_pre[c.ja];
     while (o >= (t.scb[c.i + 1] - t.scb[c.i]) * wcb) {
@@ -872,7 +888,7 @@ __device__ __forceinline__ void e_first(EGen &c, const Tabs &t, int32_t n) {
     c.ci = static_cast<int32_t>(o / w);
     c.start += static_cast<long long>(c.ci) * w;
     // the first unit whose start is >= R0
-    if (c.start < R0) e_advance(c, t, n);
+    if (c.start < R0) e_advance<kF8>(c, t, n);
     if (c.start >= c.R1) c.live = false;
 }
 
@@ -909,7 +925,7 @@ __device__ __forceinline__ void e_copy_stage(EGen &g, uint32_t wslot, uint32_t b
                 cp16_cg(ydst + (2 * nt + e) * kChunk, Y + (v ? 2 * static_cast<int64_t>(tok) * a.ldy : 0), v);
             }
         }
-        e_advance(g, t, n);
+        e_advance<kF8>(g, t, n);
     }
     cp_commit();
 }
@@ -1041,11 +1057,11 @@ __global__ void __launch_bounds__(32 * kEWarps, 1) direct_expand_kernel(DArgs a,
     }
     const Tabs t = carve(smem + static_cast<size_t>(kEWarps) * kEStages * kESlot, sh.S, sh.n, a.T);
     // tables, B and y are not written by the shrink: read them before the wait
-    build_tabs<true>(a, sh, table, t, kF8 ? 4 : 8, 1, 32);
+    build_tabs<true>(a, sh, table, t, VP<kF8>::BW, 1, 32);
     const float *buf = (t.misc[1] & 1) ? a.acc1 : a.acc0;
     const uint32_t wring = sa(smem) + warp * (kEStages * kESlot);
     EGen gi;
-    e_first(gi, t, sh.n);
+    e_first<kF8>(gi, t, sh.n);
     EGen gc = gi;
 #pragma unroll
     for (int s = 0; s < kEStages - 1; ++s) e_copy_stage<kF8>(gi, wring + s * kESlot, sa(&bars[warp][s]), t, sh, a, lane, sh.n);
@@ -1059,7 +1075,7 @@ __global__ void __launch_bounds__(32 * kEWarps, 1) direct_expand_kernel(DArgs a,
         __syncwarp();  // every lane's reads of the slot refilled next are done
         e_copy_stage<kF8>(gi, wring + sn * kESlot, sa(&bars[warp][sn]), t, sh, a, lane, sh.n);
         EGen gn = gc;
-        e_advance(gn, t, sh.n);
+        e_advance<kF8>(gn, t, sh.n);
         // the next unit's sums: the same registers while (slot, slice, token group) holds
         const bool same = gn.live && gn.ja == gc.ja && gn.i == gc.i && gn.tg == gc.tg;
         float4 Xn[2][2][2];
