@@ -111,10 +111,9 @@ typedef enum {
                                     forward pass): every A and B pointer of the slot table
                                     addresses float8_e4m3fn codes in the same row-major layouts
                                     (A_s,i [r][k], B_s,i [d_i][r], one byte each); x and y stay
-                                    bf16.  Three launches: x clamped to +-448 and rounded to
-                                    e4m3 (nearest, ties to even) into the workspace, then the
-                                    shrink (its programmatic dependent), whose products are
-                                    exact and summed in fp32, then the expand; the sums enter the expand rounded once
+                                    bf16.  x is clamped to +-448 and rounded to e4m3 (nearest,
+                                    ties to even) inside the shrink, whose products are exact
+                                    and summed in fp32; the sums enter the expand rounded once
                                     to f16 (|sum| <= 65504 assumed) against B converted exactly
                                     to f16, and y = bf16(y + s * acc) as for bf16 adapters.
                                     Scale B at load time with lora_premultiply on its bf16
@@ -262,9 +261,7 @@ lora_status_t lora_build_index_seq(const int32_t *seq_slot_ids, int32_t n_seq, i
  * or 64, the rank padded up); then, when r_max <= 128, two more fp32
  * accumulators the size of xa that LORA_PATH_DECODE_TC and
  * LORA_PATH_DECODE_STREAM use in turn (a call adds into one and clears the
- * other); last, when T <= 2048 and k % 16 == 0, x as e4m3 codes [T][k] (one
- * byte each), written by LORA_PATH_DECODE_DIRECT_FP8 before its shrink.
- * Regions start on 256-byte boundaries.  The whole buffer must be zero
+ * other).  Regions start on 256-byte boundaries.  The whole buffer must be zero
  * before the first call that uses it (e.g. one cudaMemsetAsync), and again after
  * a call whose error word reads LORA_ERR_TIMEOUT.  Otherwise every call leaves
  * what the next call of any path needs: the per-slot counters and the fused

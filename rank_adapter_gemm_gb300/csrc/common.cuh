@@ -56,11 +56,9 @@ __host__ __device__ inline int32_t tc_rank_pad(int32_t r_max) { return r_max <= 
 // fused decode kernel, which every call leaves zeroed for the next one, and
 // (r_max <= 64) the prefill path's xa as bf16 hi and lo parts, [n][T][RP] each
 // in sorted-token order.
-// Last (k given, T <= 2048 and k % 16 == 0): x as e4m3 codes [T][k] for the FP8
-// decode path.
 struct WorkspaceLayout {
-    size_t ctrl_bytes, xa_off, acc_off, hi_off, lo_off, acc2_off, acc3_off, x8_off, bytes;
-    __host__ __device__ WorkspaceLayout(int32_t T, int32_t n_slices, int32_t r_max, int32_t S, int32_t k = 0) {
+    size_t ctrl_bytes, xa_off, acc_off, hi_off, lo_off, acc2_off, acc3_off, bytes;
+    __host__ __device__ WorkspaceLayout(int32_t T, int32_t n_slices, int32_t r_max, int32_t S) {
         // two int32 counters per (slot, slice) + a few global words, rounded to 256 B
         ctrl_bytes = (sizeof(int32_t) * (2 * size_t(S) * LORA_MAX_SLICES + 64) + 255) & ~size_t(255);
         const size_t tt = size_t(T > 0 ? T : 0);
@@ -75,9 +73,7 @@ struct WorkspaceLayout {
         const size_t acc_tc = r_max <= 128 ? ((xa_bytes + 255) & ~size_t(255)) : 0;
         acc2_off = lo_off + ((hl_bytes + 255) & ~size_t(255));
         acc3_off = acc2_off + acc_tc;
-        x8_off = acc3_off + acc_tc;
-        const size_t x8_bytes = (T <= 2048 && k > 0 && k % 16 == 0) ? tt * size_t(k) : 0;
-        bytes = x8_off + ((x8_bytes + 255) & ~size_t(255));
+        bytes = acc3_off + acc_tc;
     }
 };
 

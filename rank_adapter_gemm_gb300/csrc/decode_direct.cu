@@ -41,14 +41,13 @@
 //     used; the last expand CTA to finish advances g.  No CTA waits on another.
 //
 //   * FP8 adapters (LORA_PATH_DECODE_DIRECT_FP8; TensorRT-LLM LoRA serving
-//     page, "第五步:FP8 特判"): A and B are float8_e4m3fn codes.  A first
-//     launch writes x as e4m3 codes (clamped to +-448, nearest even) into the
-//     workspace; the shrink, its programmatic dependent, builds its tables
-//     meanwhile and then streams 64-column blocks of A and of that copy (a
-//     lane's 16 bytes are 16 columns of either) into mma.m16n8k32 e4m3 with the
-//     same shared k-permutation.  The expand copies [64][r] bytes of B,
-//     converts them exactly to f16 and feeds an f16 MMA with the sums rounded
-//     once to f16.
+//     page, "第五步:FP8 特判"): A and B are float8_e4m3fn codes.  The shrink
+//     copies 64-column blocks (a lane's 16 bytes of A are 16 columns), converts
+//     its x columns from bf16 to e4m3 in registers (clamped to +-448, nearest
+//     even) and runs mma.m16n8k32 e4m3 with the same shared k-permutation;
+//     token groups are 24 so that a block's 2 MT + 6 chunks fit a stage.  The
+//     expand copies [64][r] bytes of B, converts them exactly to f16 and feeds
+//     an f16 MMA with the sums rounded once to f16.
 //
 // Limits (the host routes other cases elsewhere): T <= 2048, r_max <= 64,
 // S * n_slices <= 512, S <= 512; FP8 also k % 16 == 0.
@@ -83,8 +82,8 @@ constexpr int kTGe = 16;             // expand token group
 // chunks per 32 ranks.
 template <bool kF8>
 struct VP {
-    static constexpr int32_t TG = kTGs;
-    static constexpr int32_t XF = 1;
+    static constexpr int32_t TG = kF8 ? 24 : kTGs;
+    static constexpr int32_t XF = kF8 ? 2 : 1;
     static constexpr int32_t BC = kF8 ? 64 : 32;
     static constexpr int32_t BW = kF8 ? 4 : 8;
 };
@@ -92,7 +91,6 @@ struct VP {
 struct DArgs {
     const uint16_t *x;
     int64_t ldx;
-    const uint8_t *x8;   // FP8 path: x as e4m3 codes [T][k], written by quantize_x_kernel
     uint16_t *y;
     int64_t ldy;
     const int32_t *sorted_ids;
@@ -549,8 +547,9 @@ __device__ __forceinline__ void s_first(SGen &c, const Tabs &t, int32_t n, int32
 // 64-bit add per 16-byte copy.  Chunk c < 2 MT of a block is A row
 // 2 MT gq + c of the rank block; chunk 2 MT + nt is the x row of token
 // tg g + 8 nt + gq; lane 4 gq + q copies columns 8q..8q+7 of each.  With FP8
-// weights (kF8) a block is 64 columns and both A and x (the e4m3 copy x8) are
-// one byte per column: a lane's chunk holds columns 16q..16q+15.
+// weights (kF8) a block is 64 columns: the lane's A chunk holds columns
+// 16q..16q+15 (one byte each) and its x row, still bf16, takes the two chunks
+// 2 MT + 2 nt and 2 MT + 2 nt + 1.
 struct SCopy {
     SGen gen;
     int32_t b, kb, cpb, mt, nt;
@@ -566,7 +565,7 @@ __device__ __forceinline__ void s_copy_seg(SCopy &s, const Tabs &t, const Shape 
     const int32_t ja = s.gen.ja, r = t.a_r[ja], L = t.a_len[ja], p0 = t.a_p0[ja];
     s.mt = s_mt(r, s.gen.rb);
     s.nt = s_nt8(L, s.gen.g, tg);
-    s.cpb = 2 * s.mt + s.nt;
+    s.cpb = 2 * s.mt + (kF8 ? 2 : 1) * s.nt;
     s.kb = kSChunks / s.cpb;
     s.b = s.gen.bs;
     const int32_t rows = min(kRB, r - kRB * s.gen.rb);
@@ -580,13 +579,12 @@ __device__ __forceinline__ void s_copy_seg(SCopy &s, const Tabs &t, const Shape 
         s.pa[c] = A + (v ? kEB * static_cast<int64_t>(row) * sh.k : 0);
         vm |= v ? (1u << c) : 0u;
     }
-    const unsigned char *X = kF8 ? a.x8 + 16 * q : reinterpret_cast<const unsigned char *>(a.x) + 16 * q;
-    const int64_t xrow = kF8 ? static_cast<int64_t>(sh.k) : 2 * a.ldx;  // bytes per x row
+    const unsigned char *X = reinterpret_cast<const unsigned char *>(a.x) + (kF8 ? 32 : 16) * q;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
         const int32_t jt = tg * s.gen.g + 8 * nt + gq;
         const int32_t tok = (nt < s.nt && jt < L) ? t.tok[p0 + jt] : -1;
-        s.px[nt] = X + (tok >= 0 ? static_cast<int64_t>(tok) * xrow : 0);
+        s.px[nt] = X + (tok >= 0 ? 2 * static_cast<int64_t>(tok) * a.ldx : 0);
         vm |= tok >= 0 ? (1u << (4 + nt)) : 0u;
     }
     s.vm = vm;
@@ -613,8 +611,16 @@ __device__ __forceinline__ void s_copy_stage(SCopy &s, uint32_t slot, int32_t kq
                     if (c < 2 * s.mt) cp16_ca(dst + c * kChunk, s.pa[c] + off, cv && ((s.vm >> c) & 1u));
                 const uint32_t dx = dst + 2 * s.mt * kChunk;
 #pragma unroll
-                for (int nt = 0; nt < 4; ++nt)
-                    if (nt < s.nt) cp16_cg(dx + nt * kChunk, s.px[nt] + off, cv && ((s.vm >> (4 + nt)) & 1u));
+                for (int nt = 0; nt < 4; ++nt) {
+                    if (nt >= s.nt) continue;
+                    const bool v = cv && ((s.vm >> (4 + nt)) & 1u);
+                    if (kF8) {
+                        cp16_cg(dx + 2 * nt * kChunk, s.px[nt] + 2 * off, v);
+                        cp16_cg(dx + (2 * nt + 1) * kChunk, s.px[nt] + 2 * off + 16, v);
+                    } else {
+                        cp16_cg(dx + nt * kChunk, s.px[nt] + off, v);
+                    }
+                }
             }
         }
         s.b += nb;
@@ -681,9 +687,8 @@ size_t direct_shrink_smem(int32_t S, int32_t n, int32_t T) {
     return static_cast<size_t>(kSWarps) * kSStages * kSChunks * kChunk + tabs_bytes(S, n, T);
 }
 
-// kF8: A and x8 in e4m3, 64-column blocks of k; launched as a programmatic
-// dependent of quantize_x_kernel, whose x8 it reads only after
-// griddepcontrol.wait.
+// kF8: A in e4m3, x converted to e4m3 in registers, 64-column blocks of k,
+// token groups of 24 (a stage of 2 MT + 6 chunks holds one block).
 template <bool kF8>
 __global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a, Shape sh, const void *table) {
     constexpr int32_t kTG = VP<kF8>::TG, kXF = VP<kF8>::XF, kBC = VP<kF8>::BC;
@@ -706,7 +711,6 @@ __global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a,
     const int32_t nkb = cdiv(sh.k, kBC), kq = sh.k - (kBC / 4) * (lane & 3);
     const uint32_t ring = sa(smem) + warp * (kSStages * kSChunks * kChunk) + 16 * lane;
     constexpr uint32_t kSlot = kSChunks * kChunk;
-    if (kF8) pdl_wait();  // x8 is complete
 
     SCopy cw;
     s_first<kF8>(cw.gen, t, sh.n, nkb);
@@ -757,8 +761,18 @@ __global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a,
 #pragma unroll
             for (int c = 0; c < 4; ++c) av[c] = c < 2 * MT ? lds16(src + c * kChunk) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-                xv[nt] = nt < NT ? lds16(src + (2 * MT + nt) * kChunk) : make_uint4(0, 0, 0, 0);
+            for (int nt = 0; nt < 4; ++nt) {
+                if (kF8) {
+                    // columns 16q..16q+7 and 16q+8..16q+15 of the token's x row, to e4m3
+                    const bool v = nt < NT;
+                    const uint4 lo = v ? lds16(src + (2 * MT + 2 * nt) * kChunk) : make_uint4(0, 0, 0, 0);
+                    const uint4 hi = v ? lds16(src + (2 * MT + 2 * nt + 1) * kChunk) : make_uint4(0, 0, 0, 0);
+                    xv[nt] = make_uint4(e4m3x4_from_bf16x4(lo.x, lo.y), e4m3x4_from_bf16x4(lo.z, lo.w),
+                                        e4m3x4_from_bf16x4(hi.x, hi.y), e4m3x4_from_bf16x4(hi.z, hi.w));
+                } else {
+                    xv[nt] = nt < NT ? lds16(src + (2 * MT + nt) * kChunk) : make_uint4(0, 0, 0, 0);
+                }
+            }
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
                 if (mt >= MT) continue;
@@ -1095,24 +1109,6 @@ __global__ void __launch_bounds__(32 * kEWarps, 1) direct_expand_kernel(DArgs a,
     }
 }
 
-// x -> e4m3 codes for the FP8 shrink (the forward pass's dtype check on the
-// TensorRT-LLM LoRA serving page: a bf16 activation is clamped to the FP8 range
-// and converted): x8[t][c] = e4m3(clamp(x[t][c], -448, 448)), nearest even.  One
-// thread converts 16 columns (two 16-byte loads, one 16-byte store).
-__global__ void __launch_bounds__(256) quantize_x_kernel(const uint16_t *x, int64_t ldx, int32_t T, int32_t k,
-                                                         uint8_t *x8) {
-    pdl_launch_dependents();  // the shrink builds its tables meanwhile
-    const int64_t per_row = k / 16, total = static_cast<int64_t>(T) * per_row;
-    for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
-         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t t = e / per_row, c = 16 * (e - t * per_row);
-        const uint16_t *src = x + t * ldx + c;
-        const uint4 lo = ldg_cg(src), hi = ldg_cg(src + 8);
-        stg_u4(x8 + t * k + c, make_uint4(e4m3x4_from_bf16x4(lo.x, lo.y), e4m3x4_from_bf16x4(lo.z, lo.w),
-                                         e4m3x4_from_bf16x4(hi.x, hi.y), e4m3x4_from_bf16x4(hi.z, hi.w)));
-    }
-}
-
 // Load-time scale of an FP8 B (TensorRT-LLM LoRA serving page, "第五步:FP8 特判"):
 // w[e] = e4m3(clamp(bf16(value(w[e]) * scale), +-448)), the product exact in
 // fp64 and rounded once to bf16; NaN codes become 0x7F.
@@ -1158,7 +1154,7 @@ cudaError_t direct_args(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const WorkspaceLayout W(T, sh.n, sh.r_max, sh.S, sh.k);
+    const WorkspaceLayout W(T, sh.n, sh.r_max, sh.S);
     char *base = reinterpret_cast<char *>(ws);
     int32_t *ctrl = reinterpret_cast<int32_t *>(base);
     a.x = x;
@@ -1170,7 +1166,6 @@ cudaError_t direct_args(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy
     a.active = active;
     a.acc0 = reinterpret_cast<float *>(base + W.acc2_off);
     a.acc1 = reinterpret_cast<float *>(base + W.acc3_off);
-    a.x8 = fp8 ? reinterpret_cast<const uint8_t *>(base + W.x8_off) : nullptr;
     a.gen = ctrl + 2 * LORA_MAX_SLICES * static_cast<size_t>(sh.S);
     a.exits = a.gen + 1;
     a.err = err;
@@ -1181,8 +1176,7 @@ cudaError_t direct_args(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy
 }  // namespace
 
 // The x-only half: sums of x A^T into the call's buffer (reads x, A; writes the
-// workspace only).  fp8: A is e4m3; a first launch writes x as e4m3 codes into
-// the workspace and the shrink follows it as a programmatic dependent.
+// workspace only).  fp8: A is e4m3 and x is rounded to e4m3 on the way in.
 cudaError_t launch_direct_shrink(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                  const void *table, const int32_t *sorted_ids, const int32_t *seg,
                                  const int32_t *active, float *ws, int32_t T, int32_t *err, bool fp8,
@@ -1191,14 +1185,6 @@ cudaError_t launch_direct_shrink(const uint16_t *x, int64_t ldx, uint16_t *y, in
     int num_sms = 0;
     cudaError_t e = direct_args(x, ldx, y, ldy, sh, sorted_ids, seg, active, ws, T, err, fp8, a, num_sms);
     if (e != cudaSuccess) return e;
-    if (fp8) {
-        const int64_t items = static_cast<int64_t>(T) * (sh.k / 16);
-        const int64_t blocks = std::min<int64_t>((items + 255) / 256, static_cast<int64_t>(num_sms) * 8);
-        quantize_x_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            x, ldx, T, sh.k, const_cast<uint8_t *>(a.x8));
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
     const size_t s_smem = direct_shrink_smem(sh.S, sh.n, T);
     auto kern = fp8 ? direct_shrink_kernel<true> : direct_shrink_kernel<false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s_smem));
@@ -1208,11 +1194,7 @@ cudaError_t launch_direct_shrink(const uint16_t *x, int64_t ldx, uint16_t *y, in
     cfg.blockDim = dim3(32 * kSWarps);
     cfg.dynamicSmemBytes = s_smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = fp8 ? 1 : 0;
+    cfg.numAttrs = 0;
     return cudaLaunchKernelEx(&cfg, kern, a, sh, table);
 }
 

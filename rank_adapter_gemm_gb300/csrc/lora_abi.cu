@@ -95,7 +95,7 @@ lora_status_t check_rows(const void *p, int64_t ld, int32_t T, int32_t width) {
 }
 
 lora_status_t check_ws(const float *ws, size_t ws_bytes, int32_t T, const Shape &sh) {
-    const lora::WorkspaceLayout L(T, sh.n, sh.r_max, sh.S, sh.k);
+    const lora::WorkspaceLayout L(T, sh.n, sh.r_max, sh.S);
     if (ws == nullptr || ws_bytes < L.bytes) return LORA_ERR_WORKSPACE;
     if (!aligned16(ws)) return LORA_ERR_ALIGNMENT;
     return LORA_OK;
@@ -122,8 +122,7 @@ lora_path_t resolve(lora_path_t path, int32_t T, int32_t max_seg_hint, const Sha
         else path = LORA_PATH_DECODE_SPLIT;
     }
     if (launches != nullptr)
-        *launches = (path == LORA_PATH_DECODE_FUSED && lora::fused_decode_supported(T, sh.r_max, sh.k)) ? 1
-                    : path == LORA_PATH_DECODE_DIRECT_FP8 ? 3 : 2;
+        *launches = (path == LORA_PATH_DECODE_FUSED && lora::fused_decode_supported(T, sh.r_max, sh.k)) ? 1 : 2;
     return path;
 }
 
@@ -252,7 +251,7 @@ lora_status_t lora_workspace_bytes(int32_t T, const lora_shape_t *shape, size_t 
     if (bytes == nullptr || T < 0) return LORA_ERR_INVALID_ARG;
     const lora_status_t st = check_shape(shape, &sh);
     if (st != LORA_OK) return st;
-    *bytes = lora::WorkspaceLayout(T, sh.n, sh.r_max, sh.S, sh.k).bytes;
+    *bytes = lora::WorkspaceLayout(T, sh.n, sh.r_max, sh.S).bytes;
     return LORA_OK;
 }
 

@@ -87,23 +87,17 @@ def test_workspace_bytes(L):
     nbytes = L.lora_workspace_bytes(256, sh)
     xa = 3 * 256 * 64 * 4
     hl = 3 * 256 * 64 * 2  # prefill xa as bf16 hi and lo, rank padded to 64
-    x8 = 256 * 4096  # x as e4m3 codes for the FP8 path (T <= 2048, k % 16 == 0)
     # control block, the shrink output xa, the fused kernel's accumulator (same
-    # size as xa), the prefill path's hi/lo parts, the two accumulators the
-    # two-kernel decode paths use in turn, and x8
-    assert nbytes >= 4 * xa + 2 * hl + x8
-    assert nbytes - 4 * xa - 2 * hl - x8 < 4 * (2 * 32 * 4 + 64) + 7 * 256
+    # size as xa), the prefill path's hi/lo parts and the two accumulators the
+    # tensor-core decode kernels use in turn
+    assert nbytes >= 4 * xa + 2 * hl
+    assert nbytes - 4 * xa - 2 * hl < 4 * (2 * 32 * 4 + 64) + 6 * 256
     # ranks above 64 have no bf16 hi/lo regions; up to 128 they keep the two
     # accumulators of the two-kernel decode paths
     big = L.lora_workspace_bytes(256, L.make_shape(32, 128, 4096, [4096]))
-    assert 4 * 256 * 128 * 4 + x8 <= big < 4 * 256 * 128 * 4 + x8 + 4 * (2 * 32 * 4 + 64) + 7 * 256
+    assert 4 * 256 * 128 * 4 <= big < 4 * 256 * 128 * 4 + 4 * (2 * 32 * 4 + 64) + 6 * 256
     huge = L.lora_workspace_bytes(256, L.make_shape(32, 256, 4096, [4096]))
-    assert 2 * 256 * 256 * 4 + x8 <= huge < 2 * 256 * 256 * 4 + x8 + 4 * (2 * 32 * 4 + 64) + 7 * 256
-    # no x8 region past the FP8 path's token limit or for k % 16 != 0
-    long_t = L.lora_workspace_bytes(4096, L.make_shape(32, 256, 4096, [4096]))
-    assert long_t < 2 * 4096 * 256 * 4 + 4 * (2 * 32 * 4 + 64) + 7 * 256
-    odd_k = L.lora_workspace_bytes(256, L.make_shape(32, 256, 4104, [4096]))
-    assert odd_k < 2 * 256 * 256 * 4 + 4 * (2 * 32 * 4 + 64) + 7 * 256
+    assert 2 * 256 * 256 * 4 <= huge < 2 * 256 * 256 * 4 + 4 * (2 * 32 * 4 + 64) + 6 * 256
     with pytest.raises(L.LoraError) as e:
         L.lora_workspace_bytes(10, L.make_shape(0, 64, 4096, [4096]))
     assert e.value.status == 1
