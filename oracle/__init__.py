@@ -67,6 +67,8 @@ def configure(lib):
     lib.oracle_premultiply_e4m3.argtypes = [P, i64, f64, P]
     lib.oracle_apply_e4m3.restype = ctypes.c_int
     lib.oracle_apply_e4m3.argtypes = [P, i64, P, i64, i32, i32, P, P, i32, P, P, P, P, P, i32, P]
+    lib.oracle_apply_moe.restype = ctypes.c_int
+    lib.oracle_apply_moe.argtypes = [P, i64, i32, P, i64, i32, i32, P, P, P, i32, i32, i32, P, P, P, P, P, i32, P]
     return lib
 
 
@@ -180,6 +182,55 @@ def apply_e4m3(x: np.ndarray, y_in: Optional[np.ndarray], slice_widths: Sequence
                                    len(ranks), _ptr(ranks), _ptr(scales), ta, tb, _ptr(rows), len(rows), _ptr(out))
     del ka, kb
     return out, int(st)
+
+
+# ----------------------------------------------------------------------------
+# Routed-expert (MoE) LoRA
+# ----------------------------------------------------------------------------
+def apply_moe(x: np.ndarray, x_per_token: bool, y_in: Optional[np.ndarray], slice_widths: Sequence[int],
+              slot_ids: np.ndarray, expert_ids: np.ndarray, E: int, ranks: np.ndarray, scales: np.ndarray,
+              A: Sequence[Sequence[Optional[np.ndarray]]], B: Sequence[Sequence[Optional[np.ndarray]]],
+              rows: Optional[np.ndarray] = None):
+    """Rows (fp64) of the routed-expert branch for the pairs p = t K + j
+    (llama.cpp's build_lora_mm_id, TensorRT-LLM's per-expert layout).  A[s][i] is
+    [E, r_s, k] and B[s][i] [E, d_i, r_s]; expert_ids is [T, K]; y_in and the
+    result have one row per pair.  Returns (y[len(rows), d], status)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    slot_ids = np.ascontiguousarray(slot_ids, dtype=np.int32)
+    expert_ids = np.ascontiguousarray(expert_ids, dtype=np.int32)
+    ranks = np.ascontiguousarray(ranks, dtype=np.int32)
+    scales = np.ascontiguousarray(scales, dtype=np.float64)
+    T, K = expert_ids.shape
+    k = x.shape[1]
+    widths = [int(w) for w in slice_widths]
+    offs = np.zeros(len(widths) + 1, dtype=np.int32)
+    offs[1:] = np.cumsum(widths)
+    d = int(offs[-1])
+    if y_in is not None:
+        y_in = np.ascontiguousarray(y_in, dtype=np.uint16)
+    rows = np.arange(T * K, dtype=np.int32) if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+    out = np.zeros((len(rows), d), dtype=np.float64)
+    ta, ka = _ptr_table(A)
+    tb, kb = _ptr_table(B)
+    st = _load().oracle_apply_moe(_ptr(x), k, int(bool(x_per_token)), _ptr(y_in), d, k, len(widths), _ptr(offs),
+                                  _ptr(slot_ids), _ptr(expert_ids), int(K), int(E), len(ranks), _ptr(ranks),
+                                  _ptr(scales), ta, tb, _ptr(rows), len(rows), _ptr(out))
+    del ka, kb
+    return out, int(st)
+
+
+def moe_pair_slots(slot_ids: np.ndarray, expert_ids: np.ndarray, E: int, n_adapters: int) -> np.ndarray:
+    """Slot of each pair p = t K + j over n_adapters * E virtual slots: s E + e for
+    a token with adapter s routed to expert e, -1 without an adapter, and
+    n_adapters * E (out of range, reported) for an id outside its range."""
+    slot_ids = np.asarray(slot_ids, dtype=np.int64)
+    expert_ids = np.asarray(expert_ids, dtype=np.int64)
+    T, K = expert_ids.shape
+    s = np.repeat(slot_ids, K)
+    e = expert_ids.reshape(-1)
+    ok = (s >= 0) & (s < n_adapters) & (e >= 0) & (e < E)
+    bad = (s < -1) | (s >= n_adapters) | ((s >= 0) & ~ok)
+    return np.where(ok, s * E + e, np.where(bad, n_adapters * E, -1)).astype(np.int32)
 
 
 # ----------------------------------------------------------------------------

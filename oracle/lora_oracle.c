@@ -328,3 +328,66 @@ int oracle_apply_e4m3(const uint16_t *x, int64_t ldx, const uint16_t *y_in, int6
     free(xq);
     return status;
 }
+
+/*
+ * Routed-expert (MoE) LoRA.  llama.cpp LoRA adapter page, "MoE 专属的
+ * build_lora_mm_id": the A product and the B product are both routed by the
+ * token's expert ids, so every (token, chosen expert) pair uses that expert's
+ * A and B.  TensorRT-LLM LoRA serving page, "MoE LoRA": an adapter holds one
+ * (A, B) pair per expert, stored as A [E][r][k] and B [E][d_i][r], expert e's
+ * pair starting e * dim * rank elements into each.
+ *
+ * Pairs p = t K + j of T tokens with K choices each; token t has adapter
+ * slot_ids[t] (-1: none) and pair p expert expert_ids[p].  For each requested
+ * pair p (rows[]):
+ *   y_out[p][o_i + m] = y_in[p][o_i + m]
+ *                       + scale_s * sum_j B_{s,e,i}[m][j] sum_c x[row][c] A_{s,e,i}[j][c]
+ * with row = t when x_per_token (the layer input shared by the token's experts)
+ * and p otherwise.  A[s n + i] and B[s n + i] point at adapter s's [E][r_s][k]
+ * and [E][d_i][r_s] arrays.  A slot id outside [-1, S) or, for a token with an
+ * adapter, an expert id outside [0, E) sets ORACLE_ERR_SLOT_RANGE and leaves
+ * the pair's row unchanged.
+ */
+int oracle_apply_moe(const uint16_t *x, int64_t ldx, int32_t x_per_token, const uint16_t *y_in, int64_t ldy,
+                     int32_t k, int32_t n_slices, const int32_t *slice_offsets, const int32_t *slot_ids,
+                     const int32_t *expert_ids, int32_t K, int32_t E, int32_t S, const int32_t *ranks,
+                     const double *scales, const uint16_t *const *A, const uint16_t *const *B,
+                     const int32_t *rows, int32_t n_rows, double *y_out)
+{
+    int status = ORACLE_OK;
+    int32_t d = slice_offsets[n_slices];
+    for (int32_t q = 0; q < n_rows; ++q) {
+        int32_t p = rows[q];
+        int32_t t = p / K;
+        double *yo = y_out + (int64_t)q * d;
+        for (int32_t m = 0; m < d; ++m) yo[m] = y_in ? bf16_value(y_in[(int64_t)p * ldy + m]) : 0.0;
+        int32_t s = slot_ids[t];
+        if (s == -1) continue;
+        if (s < 0 || s >= S) { status = ORACLE_ERR_SLOT_RANGE; continue; }
+        int32_t e = expert_ids[p];
+        if (e < 0 || e >= E) { status = ORACLE_ERR_SLOT_RANGE; continue; }
+        int32_t r = ranks[s];
+        if (r <= 0) continue;
+        const uint16_t *xr = x + (int64_t)(x_per_token ? t : p) * ldx;
+        double *xa = (double *)malloc(sizeof(double) * (size_t)r);
+        for (int32_t i = 0; i < n_slices; ++i) {
+            int32_t o = slice_offsets[i];
+            int32_t di = slice_offsets[i + 1] - o;
+            /* expert e's pair: e * dim * rank elements into the adapter's arrays */
+            const uint16_t *a = A[(int64_t)s * n_slices + i] + (int64_t)e * k * r;
+            const uint16_t *b = B[(int64_t)s * n_slices + i] + (int64_t)e * di * r;
+            for (int32_t j = 0; j < r; ++j) {
+                double acc = 0.0;
+                for (int32_t c = 0; c < k; ++c) acc += bf16_value(xr[c]) * bf16_value(a[(int64_t)j * k + c]);
+                xa[j] = acc;
+            }
+            for (int32_t m = 0; m < di; ++m) {
+                double acc = 0.0;
+                for (int32_t j = 0; j < r; ++j) acc += xa[j] * bf16_value(b[(int64_t)m * r + j]);
+                yo[o + m] += scales[s] * acc;
+            }
+        }
+        free(xa);
+    }
+    return status;
+}

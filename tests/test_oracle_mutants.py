@@ -38,6 +38,13 @@ MUTANTS = {
     "fp8_x_not_quantized": ("xq[c] = oracle_e4m3_to_double(oracle_e4m3_round(bf16_value(x[(int64_t)t * ldx + c])));",
                             "xq[c] = bf16_value(x[(int64_t)t * ldx + c]);"),
     "e4m3_ties_to_odd": ("(c & 1) == 0 && (best & 1) == 1", "(c & 1) == 1 && (best & 1) == 0"),
+    "moe_A_offset_uses_d": ("A[(int64_t)s * n_slices + i] + (int64_t)e * k * r;",
+                            "A[(int64_t)s * n_slices + i] + (int64_t)e * di * r;"),
+    "moe_B_offset_uses_k": ("B[(int64_t)s * n_slices + i] + (int64_t)e * di * r;",
+                            "B[(int64_t)s * n_slices + i] + (int64_t)e * k * r;"),
+    "moe_x_row_per_pair": ("(int64_t)(x_per_token ? t : p) * ldx", "(int64_t)p * ldx"),
+    "moe_ignores_expert": ("int32_t e = expert_ids[p];", "int32_t e = 0;"),
+    "moe_expert_from_token": ("int32_t e = expert_ids[p];", "int32_t e = expert_ids[t];"),
 }
 
 PINS = [
@@ -60,6 +67,11 @@ PINS = [
     pins.test_e4m3_round_matches_library_clamp_and_convert,
     pins.test_e4m3_premultiply_matches_pages_expression,
     pins.test_fp8_branch_equals_bf16_branch_on_decoded_values,
+    lambda: pins.test_moe_one_hot_at_the_pages_expert_offset(True),
+    lambda: pins.test_moe_one_hot_at_the_pages_expert_offset(False),
+    pins.test_moe_single_expert_reduces_to_dense_branch,
+    pins.test_moe_choice_order_and_shared_rows,
+    pins.test_moe_out_of_range_ids_and_pair_slots,
 ]
 
 

@@ -522,3 +522,115 @@ def test_fp8_branch_equals_bf16_branch_on_decoded_values():
     B = [[bf16_of(b) if b is not None else None for b in row] for row in B8]
     ref, _, _ = oracle.apply(xq, y_in, widths, ids, ranks, scales, A, B)
     np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Routed-expert (MoE) LoRA: llama.cpp's build_lora_mm_id routes A and B by the
+# token's expert ids; TensorRT-LLM's per-expert layout is A [E, r, k], B [E, d, r]
+# with expert e's pair e * dim * rank elements in.
+# ---------------------------------------------------------------------------
+ONE_BF16 = np.uint16(0x3F80)
+
+
+def _moe_case(seed, T=6, K=2, E=3, k=16, widths=(8,), r=8, x_per_token=True):
+    rng = np.random.default_rng(seed)
+    x = W.f32_to_bf16_bits(rng.standard_normal((T if x_per_token else T * K, k), dtype=np.float32))
+    y_in = W.f32_to_bf16_bits(rng.standard_normal((T * K, sum(widths)), dtype=np.float32))
+    experts = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    return x, y_in, experts
+
+
+@pytest.mark.parametrize("x_per_token", [True, False])
+def test_moe_one_hot_at_the_pages_expert_offset(x_per_token):
+    """A single 1 in A at flat index e0*r*k + j0*k + c0 and in B at e0*d*r + m0*r + j0
+    (the pages' expert * dim * rank offset): pairs routed to e0 gain s * x[row][c0]
+    at column m0, exactly; every other entry keeps y."""
+    T, K, E, k, d, r = 6, 2, 3, 16, 8, 8
+    e0, j0, c0, m0, s = 1, 5, 11, 6, 0.5
+    x, y_in, experts = _moe_case(3, T, K, E, k, (d,), r, x_per_token)
+    A = np.zeros(E * r * k, np.uint16)
+    A[e0 * r * k + j0 * k + c0] = ONE_BF16
+    B = np.zeros(E * d * r, np.uint16)
+    B[e0 * d * r + m0 * r + j0] = ONE_BF16
+    slots = np.array([0, -1, 0, 0, 0, -1], np.int32)
+    y, st = oracle.apply_moe(x, x_per_token, y_in, [d], slots, experts, E, np.array([r]), np.array([s]),
+                             [[A]], [[B]])
+    assert st == 0
+    want = _f64(y_in).copy()
+    for p in range(T * K):
+        t = p // K
+        if slots[t] == 0 and experts[t, p % K] == e0:
+            want[p, m0] += s * _f64(x[t if x_per_token else p, c0])
+    np.testing.assert_array_equal(y, want)
+    assert any(slots[t] == 0 and e0 in experts[t] for t in range(T))
+
+
+def test_moe_single_expert_reduces_to_dense_branch():
+    """E = 1, K = 1 is the dense branch; K = 1 with every token on expert e is the
+    dense branch with each adapter's expert-e slices as its A and B."""
+    wl = _small_workload(seed=21, T=24, k=32, widths=(16, 8), S=3, ranks=(8, 16, 8))
+    mod = wl.modules[0]
+    scales = np.array([0.5, 2.0, 1.5])
+    dense, _, st0 = _run(wl, scales)
+    ids1 = np.zeros((wl.T, 1), np.int32)
+    y1, st1 = oracle.apply_moe(mod.x, True, mod.y_in, mod.slice_widths, wl.slot_ids, ids1, 1, wl.ranks, scales,
+                               mod.A, mod.B)
+    assert st0 == st1
+    np.testing.assert_array_equal(y1, dense)
+    E, e = 3, 2
+    rng = np.random.default_rng(5)
+    A3 = [[(W.f32_to_bf16_bits(rng.standard_normal((E, r, 32), dtype=np.float32)) if a is not None else None)
+           for a in row] for r, row in zip(wl.ranks, mod.A)]
+    B3 = [[(W.f32_to_bf16_bits(rng.standard_normal((E, w, r), dtype=np.float32) * np.float32(0.02))
+            if b is not None else None) for w, b in zip(mod.slice_widths, row)] for r, row in zip(wl.ranks, mod.B)]
+    ye, _ = oracle.apply_moe(mod.x, True, mod.y_in, mod.slice_widths, wl.slot_ids, np.full((wl.T, 1), e, np.int32),
+                             E, wl.ranks, scales, A3, B3)
+    Ae = [[(a[e] if a is not None else None) for a in row] for row in A3]
+    Be = [[(b[e] if b is not None else None) for b in row] for row in B3]
+    yd, _, _ = oracle.apply(mod.x, mod.y_in, mod.slice_widths, wl.slot_ids, wl.ranks, scales, Ae, Be)
+    np.testing.assert_array_equal(ye, yd)
+
+
+def test_moe_choice_order_and_shared_rows():
+    """Permuting a token's K choices permutes its K output rows; x shared per
+    token equals per-pair rows that repeat it; tokens without an adapter keep y."""
+    T, K, E, k, widths = 7, 3, 4, 24, (16, 8)
+    rng = np.random.default_rng(9)
+    x, y_in, experts = _moe_case(11, T, K, E, k, widths)
+    ranks = np.array([8, 16])
+    A = [[W.f32_to_bf16_bits(rng.standard_normal((E, r, k), dtype=np.float32)) for _ in widths] for r in ranks]
+    B = [[W.f32_to_bf16_bits(rng.standard_normal((E, w, r), dtype=np.float32)) for w in widths] for r in ranks]
+    slots = np.array([0, 1, -1, 1, 0, 0, -1], np.int32)
+    sc = np.array([0.25, 1.0])
+    y, st = oracle.apply_moe(x, True, y_in, widths, slots, experts, E, ranks, sc, A, B)
+    assert st == 0
+    perm = np.array([2, 0, 1])
+    y_in_p = y_in.reshape(T, K, -1)[:, perm].reshape(T * K, -1)
+    yp, _ = oracle.apply_moe(x, True, y_in_p, widths, slots, experts[:, perm], E, ranks, sc, A, B)
+    np.testing.assert_array_equal(yp.reshape(T, K, -1), y.reshape(T, K, -1)[:, perm])
+    yr, _ = oracle.apply_moe(np.repeat(x, K, axis=0), False, y_in, widths, slots, experts, E, ranks, sc, A, B)
+    np.testing.assert_array_equal(yr, y)
+    none = np.repeat(slots == -1, K)
+    np.testing.assert_array_equal(y[none], _f64(y_in[none]))
+    assert not np.array_equal(y[~none], _f64(y_in[~none]))
+
+
+def test_moe_out_of_range_ids_and_pair_slots():
+    """Pair slots of a hand-worked routing (E = 3, 2 adapters): s E + e, -1 without
+    an adapter, and 6 (out of range, reported) for a bad slot or expert id; the
+    branch leaves such pairs unchanged and reports them."""
+    slots = np.array([1, -1, 0, 5], np.int32)
+    experts = np.array([[2, 0], [1, 1], [0, 3], [0, 1]], np.int32)
+    np.testing.assert_array_equal(oracle.moe_pair_slots(slots, experts, 3, 2), [5, 3, -1, -1, 0, 6, 6, 6])
+    k, E = 8, 4
+    rng = np.random.default_rng(4)
+    x = W.f32_to_bf16_bits(rng.standard_normal((4, k), dtype=np.float32))
+    y_in = W.f32_to_bf16_bits(rng.standard_normal((8, 8), dtype=np.float32))
+    A = [[W.f32_to_bf16_bits(rng.standard_normal((E, 8, k), dtype=np.float32))] for _ in range(2)]
+    B = [[W.f32_to_bf16_bits(rng.standard_normal((E, 8, 8), dtype=np.float32))] for _ in range(2)]
+    bad_e = np.array([[0, 1], [2, 4], [0, -2], [3, 3]], np.int32)
+    y, st = oracle.apply_moe(x, True, y_in, [8], np.array([0, 1, 1, -1], np.int32), bad_e, E, np.array([8, 8]),
+                             np.ones(2), A, B)
+    assert st == oracle.ERR_SLOT_RANGE
+    np.testing.assert_array_equal(y[[3, 5, 6, 7]], _f64(y_in[[3, 5, 6, 7]]))
+    assert not np.array_equal(y[[0, 1, 2, 4]], _f64(y_in[[0, 1, 2, 4]]))
