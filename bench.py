@@ -51,7 +51,7 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--config", default="decode_qkv", choices=list(CONFIG_INDEX))
+    p.add_argument("--config", default="decode_qkv", choices=list(CONFIG_INDEX) + ["decode_moe"])
     p.add_argument("--layers", type=int, default=32)
     p.add_argument("--requests", type=int, default=16, help="prefill_mlp only: requests in the batch")
     p.add_argument("--path", default="auto", choices=["auto", "decode_fused", "decode_split", "prefill", "decode_tc", "decode_stream", "decode_direct",
@@ -237,6 +237,8 @@ class ClockSampler:
 # Our arm
 # ---------------------------------------------------------------------------
 def _workload(name, n_requests=16):
+    if name == "decode_moe":
+        return W.moe_config()
     idx = CONFIG_INDEX[name]
     return W.config(idx, y_init="normal", n_requests=n_requests)
 
@@ -260,6 +262,64 @@ def _build_index(index, slot_dev, table, tokens_per_seq):
         index.build_seq(slot_dev, tokens_per_seq, table)
     else:
         index.build(slot_dev, table)
+
+
+def time_steps(args, dev, local, index_part, apply_part):
+    """Capture a step's two parts (the per-step index, then the calls) in CUDA
+    graphs, warm up, and time ``args.steps`` replays with CUDA events on the
+    launching stream, sampling the SM clocks meanwhile.  Returns (elapsed s,
+    mean ms of the calls part, mean ms of the rest, clocks, peaks)."""
+    import torch
+    stream = torch.cuda.Stream(device=dev)
+    # eager warm-up (sets kernel attributes), then capture the two parts of a step
+    with torch.cuda.stream(stream):
+        index_part()
+        apply_part()
+    torch.cuda.synchronize()
+    g_index, g_apply = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_index, stream=stream):
+        index_part()
+    with torch.cuda.graph(g_apply, stream=stream):
+        apply_part()
+    torch.cuda.synchronize()
+
+    def replay(events=None):
+        g_index.replay()
+        if events is not None:
+            events[0].record()
+        g_apply.replay()
+        if events is not None:
+            events[1].record()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            replay()
+    torch.cuda.synchronize()
+
+    peaks = measured_peaks()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    w0 = time.time()
+    with torch.cuda.stream(stream):
+        t_start.record()
+        for k in range(args.steps):
+            replay(marks[k])
+        t_end.record()
+    torch.cuda.synchronize()
+    w1 = time.time()
+    barrier()
+    time.sleep(0.1)
+    sampler.stop()
+    elapsed_s = t_start.elapsed_time(t_end) / 1e3
+    apply_ms = [a.elapsed_time(b) for a, b in marks]          # the calls of every step
+    apply_ms_mean = float(np.mean(apply_ms))
+    index_ms_mean = (elapsed_s * 1e3 - float(np.sum(apply_ms))) / args.steps
+    return elapsed_s, apply_ms_mean, index_ms_mean, sampler.summary(w0, w1), peaks
 
 
 def run_ours(args):
@@ -313,8 +373,6 @@ def run_ours(args):
         L.lora_apply(lay.x, lay.y, lay.shape, lay.table.dev, index.sorted_ids, index.seg_offsets, index.active,
                      ws_of[l], index.err, max_seg_hint=max_seg, path=args.path)
 
-    stream = torch.cuda.Stream(device=dev)
-
     def index_part():
         layers[0].refresh_table()
         _build_index(index, slot_dev, layers[0].table, wl.tokens_per_seq)
@@ -323,56 +381,8 @@ def run_ours(args):
         for l in range(len(layers)):
             apply_layer(l)
 
-    # eager warm-up (sets kernel attributes), then capture the two parts of a step
-    with torch.cuda.stream(stream):
-        index_part()
-        apply_part()
-    torch.cuda.synchronize()
-    g_index, g_apply = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_index, stream=stream):
-        index_part()
-    with torch.cuda.graph(g_apply, stream=stream):
-        apply_part()
-    torch.cuda.synchronize()
-
-    def replay(events=None):
-        if events is None:
-            g_index.replay()
-            g_apply.replay()
-        else:
-            g_index.replay()
-            events[0].record()
-            g_apply.replay()
-            events[1].record()
-
-    with torch.cuda.stream(stream):
-        for _ in range(max(args.warmup, 3)):
-            replay()
-    torch.cuda.synchronize()
-
-    peak_gbs, peak_tf, peak_src = measured_peaks()
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    barrier()
-    torch.cuda.synchronize()
-    w0 = time.time()
-    with torch.cuda.stream(stream):
-        t_start.record()
-        for k in range(args.steps):
-            replay(marks[k])
-        t_end.record()
-    torch.cuda.synchronize()
-    w1 = time.time()
-    barrier()
-    time.sleep(0.1)
-    sampler.stop()
-    elapsed_s = t_start.elapsed_time(t_end) / 1e3
-    apply_ms = [a.elapsed_time(b) for a, b in marks]          # the L calls of every step
-    apply_ms_mean = float(np.mean(apply_ms))
-    index_ms_mean = (elapsed_s * 1e3 - float(np.sum(apply_ms))) / args.steps
+    elapsed_s, apply_ms_mean, index_ms_mean, clocks, (peak_gbs, peak_tf, peak_src) = \
+        time_steps(args, dev, local, index_part, apply_part)
     err = int(index.err.item())
 
     units = T * len(layers) * args.steps
@@ -402,7 +412,6 @@ def run_ours(args):
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         cpu = cpu_baseline(wl, args.cpu_seconds)
 
-    clocks = sampler.summary(w0, w1)
     out = {
         "metric": metric_name(args.config),
         "value": value,
@@ -513,8 +522,119 @@ def run_e2e(args, wl, layers, index, slot_dev, ws_of, max_seg, dev, world):
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
+def moe_algorithmic_bytes(wl, m) -> int:
+    """Routed-expert call: each (adapter, expert) pair in use reads its A and B
+    once (bf16), the x rows in use once (per token or per pair), and the y rows
+    of the pairs with an adapter are read and written (bf16)."""
+    mod = wl.modules[m]
+    n, k, d = len(mod.slice_widths), mod.k, mod.d
+    s = np.repeat(wl.slot_ids, wl.K)
+    e = wl.expert_ids.reshape(-1)
+    lora = s >= 0
+    lora[lora] = wl.ranks[s[lora]] > 0
+    used = np.unique(s[lora] * wl.E + e[lora])
+    weights = sum(2 * int(wl.ranks[v // wl.E]) * (n * k + d) for v in used)
+    x_rows = int(lora.reshape(wl.T, wl.K).any(axis=1).sum()) if mod.x_per_token else int(lora.sum())
+    return int(weights + 2 * k * x_rows + 4 * d * int(lora.sum()))
+
+
+def run_moe(args):
+    """The routed-expert workload: layer l runs module l % 2 (w1 with x per token,
+    w2 with x per pair) in its own buffers; one pair index per step."""
+    import torch
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import ResidentMoeProjection, clone_moe
+
+    rank, world = dist_init("nccl")
+    _, _, local = dist_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = W.moe_config()
+    mods = list(range(len(wl.modules)))
+    base = [ResidentMoeProjection(wl, m, device=dev) for m in mods]
+    layers = [base[l % len(base)] if l < len(base) else clone_moe(base[l % len(base)], device=dev)
+              for l in range(args.layers)]
+    P, V = wl.T * wl.K, wl.n_adapters * wl.E
+    index = L.TokenIndex(P, V, device=dev)
+    slot_dev = torch.from_numpy(wl.slot_ids).to(dev)
+    expert_dev = torch.from_numpy(wl.expert_ids.reshape(-1).copy()).to(dev)
+    ws = [L.Workspace(P, b.shape, device=dev) for b in base]
+
+    def index_part():
+        index.build_moe(slot_dev, expert_dev, wl.K, wl.E, layers[0].table)
+
+    def apply_part():
+        for l, lay in enumerate(layers):
+            L.lora_apply_moe(lay.x, lay.y, wl.K, lay.shape, lay.table.dev, index.sorted_ids, index.seg_offsets,
+                             index.active, ws[l % len(ws)].buf, index.err, x_per_token=lay.x_per_token)
+
+    elapsed_s, apply_ms_mean, index_ms_mean, clocks, (peak_gbs, peak_tf, peak_src) = \
+        time_steps(args, dev, local, index_part, apply_part)
+    err = int(index.err.item())
+    units = wl.T * len(layers) * args.steps
+    value = job_throughput(units, elapsed_s, world, dev)
+    ms_per_step = max_over_ranks(elapsed_s, dev) / args.steps * 1e3
+    per_layer_bytes = [moe_algorithmic_bytes(wl, l % len(mods)) for l in range(len(layers))]
+    call_s = apply_ms_mean / 1e3 / len(layers)
+    achieved_gbs = sum(per_layer_bytes) / len(layers) / call_s / 1e9
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        cpu = cpu_baseline(wl, args.cpu_seconds)
+    out = {
+        "metric": metric_name(args.config),
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded: workloads.moe_config)",
+        "config": {
+            "workload": wl.description,
+            "config": args.config,
+            "layers_per_step": len(layers),
+            "calls_per_step": len(layers),
+            "path": "lora_apply_moe (warp-streaming decode kernels over n_adapters * E virtual slots)",
+            "l2": f"inputs larger than L2: {len(layers)} distinct layer buffer sets, "
+                  f"{sum(per_layer_bytes) / 1e9:.2f} GB of algorithmic bytes per step",
+            "parallelism": f"replicas x{world}",
+        },
+        "gbs": achieved_gbs,
+        "roofline": {
+            "bound": "hbm",
+            "achieved": achieved_gbs,
+            "peak": peak_gbs,
+            "unit": "GB/s",
+            "frac": achieved_gbs / peak_gbs,
+            "traffic": None,
+            "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
+            "kernel": "lora_apply_moe (shrink + expand) per expert-projection call",
+            "bytes_per_call": sum(per_layer_bytes) / len(layers),
+            "us_per_call": call_s * 1e6,
+            "index_and_table_us": index_ms_mean * 1e3,
+        },
+        "gpu_launches": args.steps * (1 + 2 * len(layers)),
+        "clocks": clocks,
+        "device_error": err,
+    }
+    if cpu is not None:
+        out["cpu_baseline"] = cpu
+    return out, rank
+
+
 def _oracle_call(wl, rows):
     import oracle
+    if isinstance(wl, W.MoeWorkload):  # rows are (token, choice) pairs of the first module
+        m = wl.modules[0]
+        scales = oracle.slot_scales(wl.ranks, wl.alphas, wl.scale_rule, False)
+        t0 = time.perf_counter()
+        oracle.apply_moe(m.x, m.x_per_token, m.y_in, m.slice_widths, wl.slot_ids, wl.expert_ids, wl.E, wl.ranks,
+                         scales, m.A, m.B, rows=rows)
+        return time.perf_counter() - t0
     m = wl.modules[0]
     fp8 = wl.weights == "e4m3"
     rule = oracle.slot_scales(wl.ranks, wl.alphas, wl.scale_rule, False)
@@ -535,11 +655,12 @@ def _oracle_call(wl, rows):
 def cpu_baseline(wl, seconds: float):
     """The oracle as it stands, single-threaded, on repeated passes over the
     batch's rows until about ``seconds`` of CPU work (at least one pass)."""
-    rows = np.arange(wl.T, dtype=np.int32)
+    moe = isinstance(wl, W.MoeWorkload)  # rows are the T*K pairs, T tokens
+    rows = np.arange(wl.T * wl.K if moe else wl.T, dtype=np.int32)
     done, spent, passes = 0, 0.0, 0
     while passes == 0 or spent < seconds:
         spent += _oracle_call(wl, rows)
-        done += len(rows)
+        done += wl.T
         passes += 1
     return {"value": done / spent, "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"{passes} passes of the first projection over all {wl.T} tokens "
@@ -551,7 +672,8 @@ def run_reference(args):
     if rank != 0:
         return None, rank
     wl = _workload(args.config, args.requests)
-    rows = np.arange(wl.T, dtype=np.int32)
+    per_tok = wl.K if isinstance(wl, W.MoeWorkload) else 1  # MoE rows are (token, choice) pairs
+    rows = np.arange(wl.T * per_tok, dtype=np.int32)
     for _ in range(max(args.warmup, 0)):
         _oracle_call(wl, rows[:max(1, len(rows) // 8)])
     # each step: the branch for one projection call over a bounded sample of rows
@@ -562,7 +684,7 @@ def run_reference(args):
     t = 0.0
     for _ in range(args.steps):
         t += _oracle_call(wl, sample)
-    value = n_rows * args.steps / t
+    value = n_rows * args.steps / t / per_tok
     out = {
         "metric": metric_name(args.config),
         "value": value,
@@ -579,7 +701,8 @@ def run_reference(args):
         "config": {"workload": wl.description, "config": args.config},
         "impl": "reference",
         "cpu_baseline": {"kind": "oracle", "cores": 1, "value": value,
-                         "sample": f"{n_rows} of {wl.T} tokens of the first projection per step"},
+                         "sample": f"{n_rows} of {len(rows)} rows ({'token-expert pairs' if per_tok > 1 else 'tokens'}) "
+                                   "of the first projection per step"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     return out, rank
@@ -590,7 +713,7 @@ def main(argv=None):
     if args.impl == "reference":
         out, rank = run_reference(args)
     else:
-        out, rank = run_ours(args)
+        out, rank = run_moe(args) if args.config == "decode_moe" else run_ours(args)
     if rank == 0 and out is not None:
         print(json.dumps(out), flush=True)
     try:

@@ -383,6 +383,74 @@ lora_status_t lora_apply_noalloc(const void *x, int64_t ldx, void *y, int64_t ld
                                  const int32_t *sorted_ids, const int32_t *seg_offsets,
                                  const int32_t *active, int32_t *err, lora_stream_t stream);
 
+/*
+ * Routed-expert (MoE) LoRA.  llama.cpp LoRA adapter page, "MoE 专属的
+ * build_lora_mm_id": in an expert layer both the A and the B product are routed
+ * by the token's expert ids, like the base weights, so each (token, chosen
+ * expert) pair uses that expert's A and B; TensorRT-LLM LoRA serving page, "MoE
+ * LoRA: per-expert 布局": an adapter's expert weights are stored as
+ * A [E][r][k] and B [E][d_i][r], and expert e's pair starts e * dim * rank
+ * elements into each.
+ *
+ * The branch for pairs: with T tokens each routed to K experts, pair
+ * p = t K + j (token t, its j-th choice, expert e = expert_ids[p]) of a token
+ * with adapter s computes
+ *     y[p, o_i + m] = bf16( f32(y[p, o_i + m]) + scale_s * sum_j xa_j B_{s,e,i}[m, j] ),
+ *     xa_j = sum_c x[row(p), c] A_{s,e,i}[j, c],
+ * row(p) = t when the x rows are per token (x_per_token != 0, the layer's
+ * input shared by a token's experts) and p when they are per pair (the second
+ * projection of an expert MLP).  Pairs of tokens with slot -1 keep y.
+ *
+ * The library serves it as the batched branch over n_adapters * E virtual slots
+ * (slot s E + e) and T K rows: build the virtual table with
+ * lora_moe_slot_pointers and lora_set_slot_table (S = n_adapters * E), the
+ * index with lora_build_index_moe, and run lora_apply_moe.  The workspace is
+ * lora_workspace_bytes(T * K, shape).
+ */
+
+/*
+ * Virtual slot table entries (host only, no device access): for adapter a in
+ * [0, n_adapters) and expert e in [0, E), slot v = a E + e gets rank ranks[a],
+ * scale scales[a] and, for slice i, A_ptrs[v n + i] = A_base[a n + i] +
+ * e * r_a * k * elem_bytes and B_ptrs[v n + i] = B_base[a n + i] +
+ * e * d_i * r_a * elem_bytes (a zero base stays zero).  shape->S must equal
+ * n_adapters * E; elem_bytes is 2 (bf16).  Outputs: v_ranks and v_scales
+ * [n_adapters E], A_ptrs and B_ptrs [n_adapters E n_slices], caller-allocated.
+ * Errors: LORA_ERR_INVALID_ARG (null pointers, counts, S mismatch), the shape
+ * checks of lora_workspace_bytes.
+ */
+lora_status_t lora_moe_slot_pointers(int32_t n_adapters, int32_t E, const lora_shape_t *shape, int32_t elem_bytes,
+                                     const int32_t *ranks, const float *scales, const uint64_t *A_base,
+                                     const uint64_t *B_base, int32_t *v_ranks, float *v_scales, uint64_t *A_ptrs,
+                                     uint64_t *B_ptrs);
+
+/*
+ * Index over the T K (token, choice) pairs: slot_ids [T] (device int32, the
+ * token's adapter or -1), expert_ids [T K] (device int32, token-major: the K
+ * experts of token t at t K .. t K + K - 1).  Pair p is keyed by the virtual
+ * slot slot_ids[p / K] E + expert_ids[p]; outputs as lora_build_index with S
+ * the virtual slot count (a multiple of E, at most LORA_MAX_SLOTS) and T K
+ * items.  A slot id outside [-1, S / E) or an expert id outside [0, E) for a
+ * token with an adapter writes LORA_ERR_SLOT_RANGE to err and the pair keeps
+ * its y.
+ */
+lora_status_t lora_build_index_moe(const int32_t *slot_ids, const int32_t *expert_ids, int32_t T, int32_t K,
+                                   int32_t E, int32_t S, const void *dev_table, int32_t *sorted_ids,
+                                   int32_t *seg_offsets, int32_t *active, int32_t *err, lora_stream_t stream);
+
+/*
+ * The routed-expert branch on the warp-streaming decode kernels: y has T K rows
+ * (one per pair, ldy), x has T rows when x_per_token != 0 and T K rows
+ * otherwise (ldx); index from lora_build_index_moe; ws of
+ * lora_workspace_bytes(T * K, shape) bytes.  Needs T K <= 2048, r_max <= 64 and
+ * the virtual table within the limits of LORA_PATH_DECODE_DIRECT (else
+ * LORA_ERR_UNSUPPORTED).  Checks and errors otherwise as lora_apply.
+ */
+lora_status_t lora_apply_moe(const void *x, int64_t ldx, int32_t x_per_token, void *y, int64_t ldy, int32_t T,
+                             int32_t K, const lora_shape_t *shape, const void *dev_table, const int32_t *sorted_ids,
+                             const int32_t *seg_offsets, const int32_t *active, float *ws, size_t ws_bytes,
+                             int32_t *err, lora_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

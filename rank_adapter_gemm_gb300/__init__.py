@@ -25,7 +25,7 @@ __all__ = [
     "LoraError", "lora_shape_t", "make_shape", "lora_abi_version", "lora_status_string", "lora_scale",
     "lora_premultiply", "lora_premultiply_e4m3", "lora_slot_table_bytes", "lora_pack_slot_table", "lora_set_slot_table",
     "lora_build_index", "lora_build_index_seq", "lora_workspace_bytes", "lora_workspace_xa_offset", "lora_shrink", "lora_expand", "lora_apply", "lora_resolve_path",
-    "lora_apply_noalloc", "lora_apply_overlap", "apply_with_base", "SlotTable", "TokenIndex", "Workspace",
+    "lora_apply_noalloc", "lora_apply_overlap", "lora_moe_slot_pointers", "lora_build_index_moe", "lora_apply_moe", "apply_with_base", "SlotTable", "TokenIndex", "Workspace",
 ]
 
 
@@ -259,6 +259,56 @@ def lora_build_index_seq(seq_slot_ids, tokens_per_seq, S, dev_table, sorted_ids,
           "lora_build_index_seq")
 
 
+def lora_moe_slot_pointers(n_adapters: int, E: int, shape: lora_shape_t, ranks, scales, A_base, B_base,
+                           elem_bytes: int = 2):
+    """Virtual slot entries (rank, scale, A and B pointers) of n_adapters * E
+    routed-expert slots, from each adapter's [E][r][k] and [E][d_i][r] bases."""
+    ranks = np.ascontiguousarray(ranks, dtype=np.int32)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    A_base = np.ascontiguousarray(A_base, dtype=np.uint64)
+    B_base = np.ascontiguousarray(B_base, dtype=np.uint64)
+    V, n = int(n_adapters) * int(E), int(shape.n_slices)
+    v_ranks = np.zeros(V, np.int32)
+    v_scales = np.zeros(V, np.float32)
+    A_ptrs = np.zeros(V * n, np.uint64)
+    B_ptrs = np.zeros(V * n, np.uint64)
+    check(load().lora_moe_slot_pointers(int(n_adapters), int(E), ctypes.byref(shape), int(elem_bytes), _p(ranks),
+                                        _p(scales), _p(A_base), _p(B_base), _p(v_ranks), _p(v_scales), _p(A_ptrs),
+                                        _p(B_ptrs)), "lora_moe_slot_pointers")
+    return v_ranks, v_scales, A_ptrs, B_ptrs
+
+
+def lora_build_index_moe(slot_ids, expert_ids, K, E, S, dev_table, sorted_ids, seg_offsets, active, err,
+                         stream=None) -> None:
+    """Index of the T * K (token, choice) pairs over S = n_adapters * E virtual slots."""
+    torch = _torch()
+    _dev(slot_ids, "slot_ids", torch.int32)
+    _dev(expert_ids, "expert_ids", torch.int32)
+    T = int(slot_ids.numel())
+    if int(expert_ids.numel()) != T * int(K):
+        raise ValueError("expert_ids must hold K ids per token")
+    check(load().lora_build_index_moe(_p(slot_ids), _p(expert_ids), T, int(K), int(E), int(S), _p(dev_table),
+                                      _p(sorted_ids), _p(seg_offsets), _p(active), _p(err), _stream(stream)),
+          "lora_build_index_moe")
+
+
+def lora_apply_moe(x, y, K, shape, dev_table, sorted_ids, seg_offsets, active, ws, err, x_per_token: bool = True,
+                   stream=None) -> None:
+    """Routed-expert branch: y [T*K, d] per (token, choice) pair; x [T, k] shared
+    by a token's experts (x_per_token) or [T*K, k] per pair."""
+    ldx = _rows(x, "x")
+    ldy = _rows(y, "y")
+    P = int(y.shape[0])
+    if P % int(K) != 0:
+        raise ValueError("y must have T * K rows")
+    T = P // int(K)
+    if int(x.shape[0]) != (T if x_per_token else P):
+        raise ValueError("x must have T rows (x_per_token) or T * K rows")
+    check(load().lora_apply_moe(_p(x), ldx, int(bool(x_per_token)), _p(y), ldy, T, int(K), ctypes.byref(shape),
+                                _p(dev_table), _p(sorted_ids), _p(seg_offsets), _p(active), _p(ws),
+                                ws.numel() * ws.element_size(), _p(err), _stream(stream)), "lora_apply_moe")
+
+
 class SlotTable:
     """Device slot table plus the pinned staging buffer its upload copies from."""
 
@@ -293,6 +343,13 @@ class TokenIndex:
         """Index for T = len(seq_slot_ids) * tokens_per_seq tokens, sequence-major."""
         assert int(seq_slot_ids.numel()) * int(tokens_per_seq) == self.T
         lora_build_index_seq(seq_slot_ids, tokens_per_seq, self.S, table.dev, self.sorted_ids, self.seg_offsets,
+                             self.active, self.err, stream)
+
+
+    def build_moe(self, slot_ids, expert_ids, K: int, E: int, table: SlotTable, stream=None) -> None:
+        """Index of len(slot_ids) * K pairs over this index's S = n_adapters * E virtual slots."""
+        assert int(slot_ids.numel()) * int(K) == self.T
+        lora_build_index_moe(slot_ids, expert_ids, K, E, self.S, table.dev, self.sorted_ids, self.seg_offsets,
                              self.active, self.err, stream)
 
 

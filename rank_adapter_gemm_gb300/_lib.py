@@ -41,7 +41,8 @@ EXPORTED = (
     "lora_slot_table_bytes", "lora_pack_slot_table", "lora_set_slot_table", "lora_build_index",
     "lora_workspace_bytes", "lora_shrink", "lora_expand", "lora_apply", "lora_apply_ex",
     "lora_resolve_path", "lora_apply_noalloc", "lora_workspace_xa_offset", "lora_build_index_seq",
-    "lora_apply_overlap", "lora_premultiply_e4m3",
+    "lora_apply_overlap", "lora_premultiply_e4m3", "lora_moe_slot_pointers", "lora_build_index_moe",
+    "lora_apply_moe",
 )
 
 
@@ -102,6 +103,9 @@ def load() -> ctypes.CDLL:
         "lora_apply_overlap": (ST, [P, I64, P, I64, I32, SH, P, P, P, P, I32, ST, P, SZ, P, P, P]),
         "lora_resolve_path": (ST, [ST, I32, I32, ctypes.POINTER(I32)]),
         "lora_apply_noalloc": (ST, [P, I64, P, I64, I32, SH, P, P, P, P, P, P]),
+        "lora_moe_slot_pointers": (ST, [I32, I32, SH, I32, P, P, P, P, P, P, P, P]),
+        "lora_build_index_moe": (ST, [P, P, I32, I32, I32, I32, P, P, P, P, P, P]),
+        "lora_apply_moe": (ST, [P, I64, I32, P, I64, I32, I32, SH, P, P, P, P, P, SZ, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

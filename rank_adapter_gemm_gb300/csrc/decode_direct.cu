@@ -91,6 +91,7 @@ struct VP {
 struct DArgs {
     const uint16_t *x;
     int64_t ldx;
+    int32_t x_div;       // x row of sorted item p: p / x_div (routed experts sharing a token's row)
     uint16_t *y;
     int64_t ldy;
     const int32_t *sorted_ids;
@@ -584,7 +585,8 @@ __device__ __forceinline__ void s_copy_seg(SCopy &s, const Tabs &t, const Shape 
     for (int nt = 0; nt < 4; ++nt) {
         const int32_t jt = tg * s.gen.g + 8 * nt + gq;
         const int32_t tok = (nt < s.nt && jt < L) ? t.tok[p0 + jt] : -1;
-        s.px[nt] = X + (tok >= 0 ? 2 * static_cast<int64_t>(tok) * a.ldx : 0);
+        const int32_t xr = a.x_div == 1 ? tok : tok / a.x_div;
+        s.px[nt] = X + (tok >= 0 ? 2 * static_cast<int64_t>(xr) * a.ldx : 0);
         vm |= tok >= 0 ? (1u << (4 + nt)) : 0u;
     }
     s.vm = vm;
@@ -1147,7 +1149,7 @@ namespace {
 
 cudaError_t direct_args(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                         const int32_t *sorted_ids, const int32_t *seg, const int32_t *active, float *ws, int32_t T,
-                        int32_t *err, bool fp8, DArgs &a, int &num_sms) {
+                        int32_t *err, bool fp8, int32_t x_div, DArgs &a, int &num_sms) {
     if (!decode_direct_supported(T, sh, fp8)) return cudaErrorNotSupported;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1159,6 +1161,7 @@ cudaError_t direct_args(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy
     int32_t *ctrl = reinterpret_cast<int32_t *>(base);
     a.x = x;
     a.ldx = ldx;
+    a.x_div = x_div;
     a.y = y;
     a.ldy = ldy;
     a.sorted_ids = sorted_ids;
@@ -1180,10 +1183,10 @@ cudaError_t direct_args(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy
 cudaError_t launch_direct_shrink(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                  const void *table, const int32_t *sorted_ids, const int32_t *seg,
                                  const int32_t *active, float *ws, int32_t T, int32_t *err, bool fp8,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, int32_t x_div) {
     DArgs a;
     int num_sms = 0;
-    cudaError_t e = direct_args(x, ldx, y, ldy, sh, sorted_ids, seg, active, ws, T, err, fp8, a, num_sms);
+    cudaError_t e = direct_args(x, ldx, y, ldy, sh, sorted_ids, seg, active, ws, T, err, fp8, x_div, a, num_sms);
     if (e != cudaSuccess) return e;
     const size_t s_smem = direct_shrink_smem(sh.S, sh.n, T);
     auto kern = fp8 ? direct_shrink_kernel<true> : direct_shrink_kernel<false>;
@@ -1207,7 +1210,7 @@ cudaError_t launch_direct_expand(const uint16_t *x, int64_t ldx, uint16_t *y, in
                                  bool programmatic, cudaStream_t stream) {
     DArgs a;
     int num_sms = 0;
-    cudaError_t e = direct_args(x, ldx, y, ldy, sh, sorted_ids, seg, active, ws, T, err, fp8, a, num_sms);
+    cudaError_t e = direct_args(x, ldx, y, ldy, sh, sorted_ids, seg, active, ws, T, err, fp8, 1, a, num_sms);
     if (e != cudaSuccess) return e;
     const size_t e_smem = direct_expand_smem(sh.S, sh.n, T);
     auto kern = fp8 ? direct_expand_kernel<true> : direct_expand_kernel<false>;
@@ -1229,8 +1232,9 @@ cudaError_t launch_direct_expand(const uint16_t *x, int64_t ldx, uint16_t *y, in
 cudaError_t launch_decode_direct(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                  const void *table, const int32_t *sorted_ids, const int32_t *seg,
                                  const int32_t *active, float *ws, int32_t T, int32_t *err, bool fp8,
-                                 cudaStream_t stream) {
-    cudaError_t e = launch_direct_shrink(x, ldx, y, ldy, sh, table, sorted_ids, seg, active, ws, T, err, fp8, stream);
+                                 cudaStream_t stream, int32_t x_div) {
+    cudaError_t e =
+        launch_direct_shrink(x, ldx, y, ldy, sh, table, sorted_ids, seg, active, ws, T, err, fp8, stream, x_div);
     if (e != cudaSuccess) return e;
     return launch_direct_expand(x, ldx, y, ldy, sh, table, sorted_ids, seg, active, ws, T, err, fp8, true, stream);
 }

@@ -14,6 +14,14 @@
 // multiplied by tps and each sequence writes its tps token ids in a row.  With
 // tps = 1 this is the token-level sort.
 //
+// Routed-expert (MoE) LoRA (llama.cpp LoRA adapter page, "MoE 专属的
+// build_lora_mm_id": A and B are routed by the same expert ids as the base
+// weights; TensorRT-LLM LoRA serving page, "MoE LoRA": one (A, B) pair per
+// expert): the keys are (token, choice) pairs p = t K + j, pair p of a token
+// with adapter s routed to expert e = expert_ids[p] has the virtual slot
+// s E + e of a table of S = n_adapters E slots, and is keyed S when the token
+// has no adapter.
+//
 // One thread block does the whole sort: histogram in shared memory, an
 // exclusive scan into the segment offsets, then a pass over the tokens in
 // blockDim-sized chunks in token order.  Inside a chunk, a token's place among
@@ -26,10 +34,27 @@ namespace lora {
 
 namespace {
 
-__global__ void build_index_kernel(const int32_t *__restrict__ slot_ids, int32_t T, int32_t tps, int32_t S,
-                                   const void *table, int32_t *__restrict__ sorted_ids,
-                                   int32_t *__restrict__ seg_offsets, int32_t *__restrict__ active,
-                                   int32_t *err) {
+// Key of item t: its slot, or S for no adapter or an id out of range (bad).
+// With expert_ids, item t is the pair (t / K, t % K) and its key the virtual
+// slot slot_ids[t / K] * E + expert_ids[t].
+__device__ __forceinline__ int32_t index_key(const int32_t *__restrict__ slot_ids,
+                                             const int32_t *__restrict__ expert_ids, int32_t t, int32_t K,
+                                             int32_t E, int32_t S, bool &bad) {
+    if (expert_ids == nullptr) {
+        const int32_t s = slot_ids[t];
+        bad |= (s < -1 || s >= S);
+        return (s >= 0 && s < S) ? s : S;
+    }
+    const int32_t s = slot_ids[t / K], e = expert_ids[t], SA = S / E;
+    const bool ok = s >= 0 && s < SA && e >= 0 && e < E;
+    bad |= (s < -1 || s >= SA || (s >= 0 && !ok));
+    return ok ? s * E + e : S;
+}
+
+__global__ void build_index_kernel(const int32_t *__restrict__ slot_ids, const int32_t *__restrict__ expert_ids,
+                                   int32_t T, int32_t tps, int32_t K, int32_t E, int32_t S, const void *table,
+                                   int32_t *__restrict__ sorted_ids, int32_t *__restrict__ seg_offsets,
+                                   int32_t *__restrict__ active, int32_t *err) {
     extern __shared__ int32_t smem[];
     const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nw = nt >> 5;
@@ -49,12 +74,7 @@ __global__ void build_index_kernel(const int32_t *__restrict__ slot_ids, int32_t
 
     // 1. histogram
     bool bad = false;
-    for (int t = tid; t < T; t += nt) {
-        int32_t s = slot_ids[t];
-        int32_t key = (s >= 0 && s < S) ? s : S;
-        bad |= (s < -1 || s >= S);
-        atomicAdd(&cursor[key], tps);
-    }
+    for (int t = tid; t < T; t += nt) atomicAdd(&cursor[index_key(slot_ids, expert_ids, t, K, E, S, bad)], tps);
     if (bad) report_error(err, LORA_ERR_SLOT_RANGE);
     __syncthreads();
 
@@ -82,10 +102,8 @@ __global__ void build_index_kernel(const int32_t *__restrict__ slot_ids, int32_t
         const int t = base + tid;
         const bool valid = t < T;
         int32_t key = -1 - lane;  // unique per lane for invalid tokens: never matches
-        if (valid) {
-            int32_t s = slot_ids[t];
-            key = (s >= 0 && s < S) ? s : S;
-        }
+        bool unused = false;
+        if (valid) key = index_key(slot_ids, expert_ids, t, K, E, S, unused);
         const unsigned peers = __match_any_sync(0xffffffffu, key);
         const unsigned lower = peers & ((1u << lane) - 1u);
         const int in_warp = __popc(lower);
@@ -114,10 +132,11 @@ size_t index_smem_bytes(int32_t S, int threads) {
     return sizeof(int32_t) * (size_t(S + 1) + size_t(S) + size_t(S + 1) * nw + 33);
 }
 
-// T keys (tokens, or sequences of tps tokens each).
-cudaError_t launch_build_index(const int32_t *slot_ids, int32_t T, int32_t tps, int32_t S, const void *table,
-                               int32_t *sorted_ids, int32_t *seg_offsets, int32_t *active, int32_t *err,
-                               cudaStream_t stream) {
+// T keys (tokens, sequences of tps tokens each, or with expert_ids (K, E)
+// token-expert pairs).
+cudaError_t launch_build_index(const int32_t *slot_ids, const int32_t *expert_ids, int32_t T, int32_t tps, int32_t K,
+                               int32_t E, int32_t S, const void *table, int32_t *sorted_ids, int32_t *seg_offsets,
+                               int32_t *active, int32_t *err, cudaStream_t stream) {
     int threads = 1024;
     if (T < 1024) threads = ((T + 31) / 32) * 32;
     if (threads < 128) threads = 128;
@@ -133,8 +152,8 @@ cudaError_t launch_build_index(const int32_t *slot_ids, int32_t T, int32_t tps, 
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    build_index_kernel<<<1, threads, smem, stream>>>(slot_ids, T, tps, S, table, sorted_ids, seg_offsets,
-                                                     active, err);
+    build_index_kernel<<<1, threads, smem, stream>>>(slot_ids, expert_ids, T, tps, K, E, S, table, sorted_ids,
+                                                     seg_offsets, active, err);
     return cudaGetLastError();
 }
 

@@ -8,7 +8,8 @@
 #include "common.cuh"
 
 namespace lora {
-cudaError_t launch_build_index(const int32_t *slot_ids, int32_t T, int32_t tps, int32_t S, const void *table,
+cudaError_t launch_build_index(const int32_t *slot_ids, const int32_t *expert_ids, int32_t T, int32_t tps, int32_t K,
+                               int32_t E, int32_t S, const void *table,
                                int32_t *sorted_ids, int32_t *seg_offsets, int32_t *active, int32_t *err,
                                cudaStream_t stream);
 cudaError_t launch_shrink(const uint16_t *x, int64_t ldx, const Shape &sh, const void *table,
@@ -36,7 +37,7 @@ bool decode_direct_supported(int32_t T, const Shape &sh, bool fp8);
 cudaError_t launch_direct_shrink(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                  const void *table, const int32_t *sorted_ids, const int32_t *seg,
                                  const int32_t *active, float *ws, int32_t T, int32_t *err, bool fp8,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, int32_t x_div = 1);
 cudaError_t launch_direct_expand(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                  const void *table, const int32_t *sorted_ids, const int32_t *seg,
                                  const int32_t *active, float *ws, int32_t T, int32_t *err, bool fp8,
@@ -44,7 +45,7 @@ cudaError_t launch_direct_expand(const uint16_t *x, int64_t ldx, uint16_t *y, in
 cudaError_t launch_decode_direct(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                  const void *table, const int32_t *sorted_ids, const int32_t *seg,
                                  const int32_t *active, float *ws, int32_t T, int32_t *err, bool fp8,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, int32_t x_div = 1);
 cudaError_t launch_prefill(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                            const void *table, const int32_t *sorted_ids, const int32_t *seg, float *ws,
                            int32_t T, int32_t *err, cudaStream_t stream);
@@ -230,8 +231,8 @@ lora_status_t lora_build_index(const int32_t *slot_ids, int32_t T, int32_t S, co
     if (T > 0 && (slot_ids == nullptr || sorted_ids == nullptr)) return LORA_ERR_INVALID_ARG;
     if (dev_table == nullptr || seg_offsets == nullptr || active == nullptr) return LORA_ERR_INVALID_ARG;
     if (!aligned16(dev_table)) return LORA_ERR_ALIGNMENT;
-    return from_cuda(lora::launch_build_index(slot_ids, T, 1, S, dev_table, sorted_ids, seg_offsets, active, err,
-                                              reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(lora::launch_build_index(slot_ids, nullptr, T, 1, 1, 1, S, dev_table, sorted_ids, seg_offsets,
+                                              active, err, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 lora_status_t lora_build_index_seq(const int32_t *seq_slot_ids, int32_t n_seq, int32_t tokens_per_seq, int32_t S,
@@ -242,8 +243,51 @@ lora_status_t lora_build_index_seq(const int32_t *seq_slot_ids, int32_t n_seq, i
     if (n_seq > 0 && (seq_slot_ids == nullptr || sorted_ids == nullptr)) return LORA_ERR_INVALID_ARG;
     if (dev_table == nullptr || seg_offsets == nullptr || active == nullptr) return LORA_ERR_INVALID_ARG;
     if (!aligned16(dev_table)) return LORA_ERR_ALIGNMENT;
-    return from_cuda(lora::launch_build_index(seq_slot_ids, n_seq, tokens_per_seq, S, dev_table, sorted_ids,
+    return from_cuda(lora::launch_build_index(seq_slot_ids, nullptr, n_seq, tokens_per_seq, 1, 1, S, dev_table,
+                                              sorted_ids, seg_offsets, active, err,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_build_index_moe(const int32_t *slot_ids, const int32_t *expert_ids, int32_t T, int32_t K,
+                                   int32_t E, int32_t S, const void *dev_table, int32_t *sorted_ids,
+                                   int32_t *seg_offsets, int32_t *active, int32_t *err, lora_stream_t stream) {
+    if (T < 0 || K < 1 || E < 1 || S < 1 || S > LORA_MAX_SLOTS || S % E != 0) return LORA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(T) * K > INT32_MAX) return LORA_ERR_INVALID_ARG;
+    if (T > 0 && (slot_ids == nullptr || expert_ids == nullptr || sorted_ids == nullptr)) return LORA_ERR_INVALID_ARG;
+    if (dev_table == nullptr || seg_offsets == nullptr || active == nullptr) return LORA_ERR_INVALID_ARG;
+    if (!aligned16(dev_table)) return LORA_ERR_ALIGNMENT;
+    return from_cuda(lora::launch_build_index(slot_ids, expert_ids, T * K, 1, K, E, S, dev_table, sorted_ids,
                                               seg_offsets, active, err, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_moe_slot_pointers(int32_t n_adapters, int32_t E, const lora_shape_t *shape, int32_t elem_bytes,
+                                     const int32_t *ranks, const float *scales, const uint64_t *A_base,
+                                     const uint64_t *B_base, int32_t *v_ranks, float *v_scales, uint64_t *A_ptrs,
+                                     uint64_t *B_ptrs) {
+    Shape sh;
+    if (n_adapters < 1 || E < 1 || (elem_bytes != 1 && elem_bytes != 2)) return LORA_ERR_INVALID_ARG;
+    if (ranks == nullptr || scales == nullptr || A_base == nullptr || B_base == nullptr || v_ranks == nullptr ||
+        v_scales == nullptr || A_ptrs == nullptr || B_ptrs == nullptr)
+        return LORA_ERR_INVALID_ARG;
+    const lora_status_t st = check_shape(shape, &sh);
+    if (st != LORA_OK) return st;
+    if (static_cast<int64_t>(n_adapters) * E != sh.S) return LORA_ERR_INVALID_ARG;
+    for (int32_t a = 0; a < n_adapters; ++a) {
+        const int32_t r = ranks[a];
+        for (int32_t e = 0; e < E; ++e) {
+            const int32_t v = a * E + e;
+            v_ranks[v] = r;
+            v_scales[v] = scales[a];
+            for (int32_t i = 0; i < sh.n; ++i) {
+                const uint64_t ab = A_base[a * sh.n + i], bb = B_base[a * sh.n + i];
+                const uint64_t di = static_cast<uint64_t>(sh.off[i + 1] - sh.off[i]);
+                // expert e's slice starts expert * dim * rank elements in
+                A_ptrs[v * sh.n + i] = ab == 0 ? 0 : ab + static_cast<uint64_t>(e) * r * sh.k * elem_bytes;
+                B_ptrs[v * sh.n + i] = bb == 0 ? 0 : bb + static_cast<uint64_t>(e) * di * r * elem_bytes;
+            }
+        }
+    }
+    return LORA_OK;
 }
 
 lora_status_t lora_workspace_bytes(int32_t T, const lora_shape_t *shape, size_t *bytes) {
@@ -400,6 +444,26 @@ lora_status_t lora_apply_overlap(const void *x, int64_t ldx, void *y, int64_t ld
     if (ev != nullptr && cudaStreamWaitEvent(s, ev, 0) != cudaSuccess) return LORA_ERR_CUDA;
     return lora_apply_ex(x, ldx, y, ldy, T, shape, dev_table, sorted_ids, seg_offsets, active, max_seg_hint, p, ws,
                          ws_bytes, err, stream);
+}
+
+lora_status_t lora_apply_moe(const void *x, int64_t ldx, int32_t x_per_token, void *y, int64_t ldy, int32_t T,
+                             int32_t K, const lora_shape_t *shape, const void *dev_table, const int32_t *sorted_ids,
+                             const int32_t *seg_offsets, const int32_t *active, float *ws, size_t ws_bytes,
+                             int32_t *err, lora_stream_t stream) {
+    Shape sh;
+    lora_status_t st;
+    if (T < 0 || K < 1 || static_cast<int64_t>(T) * K > INT32_MAX) return LORA_ERR_INVALID_ARG;
+    const int32_t P = T * K;  // (token, choice) pairs: the rows of y
+    if ((st = check_shape(shape, &sh)) != LORA_OK) return st;
+    if ((st = check_index_ptrs(dev_table, sorted_ids, seg_offsets, active, P)) != LORA_OK) return st;
+    if ((st = check_rows(x, ldx, x_per_token ? T : P, sh.k)) != LORA_OK) return st;
+    if ((st = check_rows(y, ldy, P, sh.off[sh.n])) != LORA_OK) return st;
+    if ((st = check_ws(ws, ws_bytes, P, sh)) != LORA_OK) return st;
+    if (P == 0) return LORA_OK;
+    if (!lora::decode_direct_supported(P, sh, false)) return LORA_ERR_UNSUPPORTED;
+    return from_cuda(lora::launch_decode_direct(static_cast<const uint16_t *>(x), ldx, static_cast<uint16_t *>(y), ldy,
+                                                sh, dev_table, sorted_ids, seg_offsets, active, ws, P, err, false,
+                                                reinterpret_cast<cudaStream_t>(stream), x_per_token ? K : 1));
 }
 
 lora_status_t lora_apply(const void *x, int64_t ldx, void *y, int64_t ldy, int32_t T, const lora_shape_t *shape,

@@ -123,3 +123,52 @@ def to_host_bits(t) -> np.ndarray:
     """torch bf16 tensor -> numpy uint16 bit patterns."""
     import torch
     return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+class ResidentMoeProjection:
+    """One routed-expert projection on the device: each adapter's A [E, r, k] and
+    B [E, d_i, r] as one bf16 tensor per slice, the virtual slot table of
+    n_adapters * E slots (lora_moe_slot_pointers + lora_set_slot_table), x and
+    the per-pair y rows."""
+
+    def __init__(self, wl, module_index: int = 0, device="cuda"):
+        from . import lora_moe_slot_pointers
+        m = wl.modules[module_index]
+        self.K, self.E, self.n_adapters = wl.K, wl.E, wl.n_adapters
+        self.x_per_token = m.x_per_token
+        self.slice_widths = list(m.slice_widths)
+        n = len(self.slice_widths)
+        rslora = wl.scale_rule == "alpha_over_sqrt_r"
+        scales = np.array([lora_scale(wl.alphas[s], int(wl.ranks[s]), rslora) for s in range(wl.n_adapters)],
+                          dtype=np.float32)
+        self.A = [[_to_dev(a.reshape(-1), device) for a in row] for row in m.A]
+        self.B = [[_to_dev(b.reshape(-1), device) for b in row] for row in m.B]
+        a_base = np.array([t.data_ptr() for row in self.A for t in row], dtype=np.uint64)
+        b_base = np.array([t.data_ptr() for row in self.B for t in row], dtype=np.uint64)
+        V = wl.n_adapters * wl.E
+        self.shape = make_shape(V, wl.r_max, m.k, self.slice_widths)
+        v_ranks, v_scales, a_ptrs, b_ptrs = lora_moe_slot_pointers(wl.n_adapters, wl.E, self.shape, wl.ranks, scales,
+                                                                   a_base, b_base)
+        self.ranks, self.scales = np.asarray(wl.ranks, np.int32), scales
+        self.table = SlotTable(V, n, wl.r_max, device=device)
+        self.table.set(v_ranks, v_scales, a_ptrs, b_ptrs)
+        self.x = _to_dev(m.x, device)
+        self.y = _to_dev(m.y_in, device)
+
+
+def clone_moe(rp: ResidentMoeProjection, device="cuda") -> ResidentMoeProjection:
+    """Same values in fresh device buffers (weights, rows and virtual slot table)."""
+    import copy
+    from . import lora_moe_slot_pointers
+    other = copy.copy(rp)
+    other.A = [[t.clone() for t in row] for row in rp.A]
+    other.B = [[t.clone() for t in row] for row in rp.B]
+    a_base = np.array([t.data_ptr() for row in other.A for t in row], dtype=np.uint64)
+    b_base = np.array([t.data_ptr() for row in other.B for t in row], dtype=np.uint64)
+    v_ranks, v_scales, a_ptrs, b_ptrs = lora_moe_slot_pointers(rp.n_adapters, rp.E, rp.shape, rp.ranks, rp.scales,
+                                                               a_base, b_base)
+    other.table = SlotTable(rp.table.S, rp.table.n_slices, rp.table.r_max, device=device)
+    other.table.set(v_ranks, v_scales, a_ptrs, b_ptrs)
+    other.x = rp.x.clone()
+    other.y = rp.y.clone()
+    return other

@@ -104,3 +104,24 @@ def test_workspace_bytes(L):
     with pytest.raises(L.LoraError) as e:
         L.lora_workspace_bytes(10, L.make_shape(4, 64, 4095, [4096]))
     assert e.value.status == 2
+
+
+def test_moe_slot_pointers_follow_the_expert_offset(L):
+    """Virtual slot a E + e gets adapter a's rank and scale, and A and B bases moved
+    by e * dim * rank elements (TensorRT-LLM's per-expert layout), two bytes each."""
+    n_ad, E, k, widths = 3, 4, 4096, [4096, 1024]
+    sh = L.make_shape(n_ad * E, 64, k, widths)
+    ranks = [16, 64, 0]
+    a_base = [1 << 20, 2 << 20, 3 << 20, 4 << 20, 0, 0]
+    b_base = [5 << 20, 6 << 20, 7 << 20, 8 << 20, 0, 0]
+    vr, vs, ap, bp = L.lora_moe_slot_pointers(n_ad, E, sh, ranks, [0.5, 2.0, 1.0], a_base, b_base)
+    for a in range(n_ad):
+        for e in range(E):
+            v = a * E + e
+            assert vr[v] == ranks[a] and vs[v] == [0.5, 2.0, 1.0][a]
+            for i, w in enumerate(widths):
+                want_a = a_base[a * 2 + i] + e * ranks[a] * k * 2 if a_base[a * 2 + i] else 0
+                want_b = b_base[a * 2 + i] + e * w * ranks[a] * 2 if b_base[a * 2 + i] else 0
+                assert ap[v * 2 + i] == want_a and bp[v * 2 + i] == want_b
+    with pytest.raises(L.LoraError):
+        L.lora_moe_slot_pointers(n_ad, E + 1, sh, ranks, [1.0] * 3, a_base, b_base)

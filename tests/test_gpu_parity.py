@@ -703,3 +703,110 @@ def test_premultiply_e4m3_kernel_bit_exact():
     L.lora_premultiply_e4m3(t, 2.0)
     torch.cuda.synchronize()
     assert t.cpu().numpy().tolist()[:2] == [0x7F, 0x7F]
+
+
+# ---------------------------------------------------------------------------
+# Routed-expert (MoE) LoRA against the oracle's per-pair definition
+# ---------------------------------------------------------------------------
+def _gpu_moe_index(slot_ids, expert_ids, E, n_adapters, ranks):
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    T, K = expert_ids.shape
+    V = n_adapters * E
+    tab = L.SlotTable(V, 1, 256)
+    dummy = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
+    ptrs = np.full(V, dummy.data_ptr(), dtype=np.uint64)
+    tab.set(np.repeat(np.asarray(ranks, np.int32), E), np.ones(V, np.float32), ptrs, ptrs)
+    idx = L.TokenIndex(T * K, V)
+    idx.build_moe(torch.from_numpy(np.ascontiguousarray(slot_ids, np.int32)).cuda(),
+                  torch.from_numpy(np.ascontiguousarray(expert_ids, np.int32).reshape(-1)).cuda(), K, E, tab)
+    torch.cuda.synchronize()
+    return (idx.sorted_ids.cpu().numpy()[:T * K], idx.seg_offsets.cpu().numpy(), idx.active.cpu().numpy(),
+            int(idx.err.cpu().item()))
+
+
+@pytest.mark.parametrize("T,K,E,n_adapters,seed", [(128, 2, 8, 8, 1), (37, 3, 5, 2, 2), (1, 1, 1, 1, 3),
+                                                   (1000, 2, 64, 8, 4), (64, 8, 64, 4, 5)])
+def test_moe_index_bit_exact(T, K, E, n_adapters, seed):
+    """Pair index against the oracle's pair slots sorted by its comparison sort,
+    with no-adapter tokens, rank-0 adapters and out-of-range slot and expert ids."""
+    rng = np.random.default_rng(seed)
+    slots = rng.integers(-1, n_adapters, size=T).astype(np.int32)
+    experts = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    if T > 10:
+        slots[3] = n_adapters + 1
+        experts[5, 0] = E + 2 if slots[5] >= 0 else experts[5, 0]
+    ranks = rng.choice([0, 8, 16], size=n_adapters).astype(np.int32)
+    so, seg, act, err = _gpu_moe_index(slots, experts, E, n_adapters, ranks)
+    pair = oracle.moe_pair_slots(slots, experts, E, n_adapters)
+    so_r, seg_r, act_r, st_r = oracle.build_index(pair, n_adapters * E, np.repeat(ranks, E))
+    np.testing.assert_array_equal(so, so_r)
+    np.testing.assert_array_equal(seg, seg_r)
+    np.testing.assert_array_equal(act[:1 + act_r[0]], act_r[:1 + act_r[0]])
+    assert (err == 4) == (st_r == oracle.ERR_SLOT_RANGE)
+
+
+def _check_moe(wl, mod_idx, what, rows=None):
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import ResidentMoeProjection, to_host_bits
+    rp = ResidentMoeProjection(wl, mod_idx)
+    P = wl.T * wl.K
+    idx = L.TokenIndex(P, wl.n_adapters * wl.E)
+    idx.build_moe(torch.from_numpy(wl.slot_ids).cuda(), torch.from_numpy(wl.expert_ids.reshape(-1).copy()).cuda(),
+                  wl.K, wl.E, rp.table)
+    ws = L.Workspace(P, rp.shape)
+    L.lora_apply_moe(rp.x, rp.y, wl.K, rp.shape, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active, ws.buf,
+                     idx.err, x_per_token=rp.x_per_token)
+    torch.cuda.synchronize()
+    assert int(idx.err.item()) == 0
+    m = wl.modules[mod_idx]
+    scales = oracle.slot_scales(wl.ranks, wl.alphas, wl.scale_rule, False)
+    ref, st = oracle.apply_moe(m.x, m.x_per_token, m.y_in, m.slice_widths, wl.slot_ids, wl.expert_ids, wl.E,
+                               wl.ranks, scales, m.A, m.B, rows=rows)
+    assert st == 0
+    y = to_host_bits(rp.y)
+    sel = np.arange(P) if rows is None else rows
+    assert_y_close(y[sel], ref, what)
+    none = np.repeat(wl.slot_ids < 0, wl.K)
+    np.testing.assert_array_equal(y[none], m.y_in[none])
+
+
+@pytest.mark.parametrize("mod_idx", [0, 1], ids=["w1_x_per_token", "w2_x_per_pair"])
+def test_apply_moe_mixtral_decode(mod_idx):
+    """128 tokens routed top-2 of 8 experts (Mixtral-8x7B expert shapes), 8 adapters."""
+    _check_moe(W.moe_config(), mod_idx, f"moe module {mod_idx}")
+
+
+MOE_RAGGED = [
+    # seed, T, K, E, n_adapters, k, widths, ranks, x_per_token
+    (71, 37, 3, 5, 3, 264, [40, 16], [8, 24, 0], True),
+    (72, 50, 2, 16, 2, 512, [1032], [64, 8], False),
+    (73, 1, 1, 1, 1, 128, [64], [16], True),
+    (74, 256, 8, 32, 2, 1024, [256], [16, 32], True),
+]
+
+
+@pytest.mark.parametrize("case", MOE_RAGGED, ids=[f"moe{c[0]}" for c in MOE_RAGGED])
+def test_apply_moe_ragged(case):
+    seed, T, K, E, n_ad, k, widths, ranks, per_token = case
+    wl = W.generate_moe(name="moe_case", seed=seed, T=T, K=K, E=E, n_adapters=n_ad, rank=8,
+                        modules=[{"name": "m", "k": k, "slices": widths, "x_per_token": per_token}],
+                        slot_dist="uniform", frac_none=0.1)
+    rng = np.random.Generator(np.random.PCG64(seed + 7))
+    wl.ranks = np.asarray(ranks, np.int32)
+    wl.r_max = max(8, max(ranks))
+    wl.alphas = 2.0 * np.maximum(wl.ranks, 1)
+    m = wl.modules[0]
+    m.A = [[W._normal_bf16(rng, (E * r, k), k ** -0.5).reshape(E, r, k) for _ in widths] for r in wl.ranks]
+    m.B = [[W._normal_bf16(rng, (E * w, r), 0.02).reshape(E, w, r) for w in widths] for r in wl.ranks]
+    _check_moe(wl, 0, f"moe ragged {seed}")
+
+
+def test_apply_moe_rejects_too_many_pairs():
+    import rank_adapter_gemm_gb300 as L
+    wl = W.generate_moe(name="moe_big", seed=75, T=1100, K=2, E=4, n_adapters=1, rank=8,
+                        modules=[{"name": "m", "k": 128, "slices": [64], "x_per_token": True}])
+    with pytest.raises(L.LoraError) as e:
+        _check_moe(wl, 0, "moe too many pairs")
+    assert e.value.status == 9

@@ -310,3 +310,90 @@ def config(index: int, y_init: str = "normal", sweep: bool = False, n_requests: 
                         description="T=256, k=4096, slices 4096/1024/1024, S=32, r in {8,16,32,64}, "
                                     "Zipf(1.1), float8_e4m3fn adapters")
     raise IndexError(index)
+
+
+# ----------------------------------------------------------------------------
+# Routed-expert (MoE) LoRA workloads
+# ----------------------------------------------------------------------------
+@dataclasses.dataclass
+class MoeModule:
+    """One expert projection: per adapter and slice, A [E, r, k] and B [E, d_i, r]."""
+    name: str
+    k: int
+    slice_widths: List[int]
+    x_per_token: bool                              # x rows per token (shared by its experts) or per pair
+    x: np.ndarray                                  # uint16 [T, k] or [T*K, k]
+    y_in: np.ndarray                               # uint16 [T*K, d], one row per (token, choice) pair
+    A: List[List[Optional[np.ndarray]]]            # [n_adapters][n] uint16 [E, r_s, k]
+    B: List[List[Optional[np.ndarray]]]            # [n_adapters][n] uint16 [E, d_i, r_s]
+
+    @property
+    def d(self) -> int:
+        return int(sum(self.slice_widths))
+
+
+@dataclasses.dataclass
+class MoeWorkload:
+    name: str
+    T: int                        # tokens
+    K: int                        # experts per token
+    E: int                        # experts
+    n_adapters: int
+    r_max: int
+    slot_ids: np.ndarray          # int32 [T], adapter per token, -1 = none
+    expert_ids: np.ndarray        # int32 [T, K], distinct per token
+    ranks: np.ndarray             # int32 [n_adapters]
+    alphas: np.ndarray            # float64 [n_adapters]
+    scale_rule: str
+    modules: List[MoeModule]
+    seed: int
+    description: str = ""
+
+
+def generate_moe(*, name: str, seed: int, T: int, K: int, E: int, n_adapters: int, rank: int,
+                 modules: Sequence[Dict], slot_dist: str = "zipf", frac_none: float = 0.0,
+                 zipf_exponent: float = 1.1, alpha_times_rank: float = 2.0, y_init: str = "normal",
+                 description: str = "") -> MoeWorkload:
+    """Draw one routed-expert workload.  Draw order: adapter per token, K distinct
+    experts per token (uniform), then per module x, A (adapter-major, slice-minor;
+    each [E, r, k] ~ N(0, 1/k)), B ([E, d_i, r] ~ N(0, 0.02^2)), y_in.  ``modules``
+    holds ``{"name", "k", "slices", "x_per_token"}`` dicts."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    slot_ids = _draw_slot_ids(rng, T, n_adapters, slot_dist, frac_none, zipf_exponent).astype(np.int32)
+    expert_ids = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    ranks = np.full(n_adapters, int(rank), dtype=np.int32)
+    alphas = alpha_times_rank * ranks.astype(np.float64)
+    mods = []
+    for m in modules:
+        k = int(m["k"])
+        widths = [int(w) for w in m["slices"]]
+        per_token = bool(m["x_per_token"])
+        x = _normal_bf16(rng, (T if per_token else T * K, k), 1.0)
+        A = [[_normal_bf16(rng, (E * int(ranks[s]), k), float(k) ** -0.5).reshape(E, int(ranks[s]), k)
+              for _ in widths] for s in range(n_adapters)]
+        B = [[_normal_bf16(rng, (E * w, int(ranks[s])), 0.02).reshape(E, w, int(ranks[s])) for w in widths]
+             for s in range(n_adapters)]
+        d = sum(widths)
+        y_in = _normal_bf16(rng, (T * K, d), 1.0) if y_init == "normal" else np.zeros((T * K, d), np.uint16)
+        mods.append(MoeModule(name=m["name"], k=k, slice_widths=widths, x_per_token=per_token, x=x, y_in=y_in,
+                              A=A, B=B))
+    return MoeWorkload(name=name, T=int(T), K=int(K), E=int(E), n_adapters=int(n_adapters), r_max=int(rank),
+                       slot_ids=slot_ids, expert_ids=expert_ids, ranks=ranks, alphas=alphas,
+                       scale_rule="alpha_over_r", modules=mods, seed=seed, description=description)
+
+
+MIXTRAL_EXPERT = [
+    {"name": "w1", "k": 4096, "slices": [14336], "x_per_token": True},
+    {"name": "w2", "k": 14336, "slices": [4096], "x_per_token": False},
+]
+
+
+def moe_config(T: int = 128, y_init: str = "normal") -> MoeWorkload:
+    """Decode through one routed-expert layer with Mixtral-8x7B expert shapes: T
+    tokens (default 128) routed top-2 of 8 experts (T*2 pairs), 8 adapters with
+    Zipf(1.1) popularity, r = 16, alpha = 2r; modules w1 (hidden 4096 -> 14336,
+    x per token) and w2 (14336 -> 4096, x per pair); seed 1007."""
+    return generate_moe(name="decode_moe", seed=1007, T=T, K=2, E=8, n_adapters=8, rank=16,
+                        modules=MIXTRAL_EXPERT, y_init=y_init,
+                        description=f"routed-expert decode, Mixtral-8x7B expert shapes: T={T} tokens, top-2 of "
+                                    "8 experts, 8 adapters Zipf(1.1), r=16, w1 4096->14336 and w2 14336->4096")
