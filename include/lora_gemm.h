@@ -384,6 +384,24 @@ lora_status_t lora_apply_noalloc(const void *x, int64_t ldx, void *y, int64_t ld
                                  const int32_t *active, int32_t *err, lora_stream_t stream);
 
 /*
+ * Token index with activated-LoRA (aLoRA) enablement (llama.cpp LoRA adapter
+ * page, "aLoRA:让适配器在 prompt 中间生效": a request runs without its adapter
+ * before its invocation point and with it from there on).  Token t belongs to
+ * sequence q = seq_ids[t] (device int32 [T], in [0, n_seq)) at position
+ * positions[t] (device int32 [T]); its slot is seq_slot[q] (device int32
+ * [n_seq], -1 for none) when positions[t] >= invocation_start[q] (device int32
+ * [n_seq]) and -1 before it.  invocation_start 0 is a plain LoRA; a start past
+ * the sequence's last position leaves the sequence without its adapter (the
+ * pages' "invocation not found" case).  Outputs, limits and errors as
+ * lora_build_index; a sequence id outside [0, n_seq) is reported as
+ * LORA_ERR_SLOT_RANGE and the token keeps its y.
+ */
+lora_status_t lora_build_index_activated(const int32_t *seq_ids, const int32_t *positions, int32_t T,
+                                         const int32_t *seq_slot, const int32_t *invocation_start, int32_t n_seq,
+                                         int32_t S, const void *dev_table, int32_t *sorted_ids, int32_t *seg_offsets,
+                                         int32_t *active, int32_t *err, lora_stream_t stream);
+
+/*
  * Routed-expert (MoE) LoRA.  llama.cpp LoRA adapter page, "MoE 专属的
  * build_lora_mm_id": in an expert layer both the A and the B product are routed
  * by the token's expert ids, like the base weights, so each (token, chosen

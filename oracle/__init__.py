@@ -219,6 +219,25 @@ def apply_moe(x: np.ndarray, x_per_token: bool, y_in: Optional[np.ndarray], slic
     return out, int(st)
 
 
+def activated_token_slots(seq_ids: np.ndarray, positions: np.ndarray, seq_slot: np.ndarray,
+                          invocation_start: np.ndarray) -> np.ndarray:
+    """Per-token slots with activated LoRA (llama.cpp's aLoRA: no adapter before
+    the request's invocation point, its adapter from there on): token t of
+    sequence q gets seq_slot[q] at positions >= invocation_start[q], else -1; a
+    sequence id outside [0, n_seq) gives an out-of-range slot (reported)."""
+    seq_ids = np.asarray(seq_ids, dtype=np.int64)
+    positions = np.asarray(positions, dtype=np.int64)
+    seq_slot = np.asarray(seq_slot, dtype=np.int64)
+    start = np.asarray(invocation_start, dtype=np.int64)
+    out = np.empty(len(seq_ids), dtype=np.int64)
+    for t, q in enumerate(seq_ids):
+        if q < 0 or q >= len(seq_slot):
+            out[t] = np.iinfo(np.int32).max
+        else:
+            out[t] = seq_slot[q] if positions[t] >= start[q] else -1
+    return out.astype(np.int32)
+
+
 def moe_pair_slots(slot_ids: np.ndarray, expert_ids: np.ndarray, E: int, n_adapters: int) -> np.ndarray:
     """Slot of each pair p = t K + j over n_adapters * E virtual slots: s E + e for
     a token with adapter s routed to expert e, -1 without an adapter, and

@@ -25,7 +25,8 @@ __all__ = [
     "LoraError", "lora_shape_t", "make_shape", "lora_abi_version", "lora_status_string", "lora_scale",
     "lora_premultiply", "lora_premultiply_e4m3", "lora_slot_table_bytes", "lora_pack_slot_table", "lora_set_slot_table",
     "lora_build_index", "lora_build_index_seq", "lora_workspace_bytes", "lora_workspace_xa_offset", "lora_shrink", "lora_expand", "lora_apply", "lora_resolve_path",
-    "lora_apply_noalloc", "lora_apply_overlap", "lora_moe_slot_pointers", "lora_build_index_moe", "lora_apply_moe", "apply_with_base", "SlotTable", "TokenIndex", "Workspace",
+    "lora_apply_noalloc", "lora_apply_overlap", "lora_moe_slot_pointers", "lora_build_index_moe", "lora_apply_moe",
+    "lora_build_index_activated", "apply_with_base", "SlotTable", "TokenIndex", "Workspace",
 ]
 
 
@@ -278,6 +279,22 @@ def lora_moe_slot_pointers(n_adapters: int, E: int, shape: lora_shape_t, ranks, 
     return v_ranks, v_scales, A_ptrs, B_ptrs
 
 
+def lora_build_index_activated(seq_ids, positions, seq_slot, invocation_start, S, dev_table, sorted_ids,
+                               seg_offsets, active, err, stream=None) -> None:
+    """Token index with aLoRA enablement: token t takes its sequence's slot from
+    the sequence's invocation start on, and no adapter before it."""
+    torch = _torch()
+    for t, name in ((seq_ids, "seq_ids"), (positions, "positions"), (seq_slot, "seq_slot"),
+                    (invocation_start, "invocation_start")):
+        _dev(t, name, torch.int32)
+    T, n_seq = int(seq_ids.numel()), int(seq_slot.numel())
+    if int(positions.numel()) != T or int(invocation_start.numel()) != n_seq:
+        raise ValueError("positions must match seq_ids, invocation_start must match seq_slot")
+    check(load().lora_build_index_activated(_p(seq_ids), _p(positions), T, _p(seq_slot), _p(invocation_start), n_seq,
+                                            int(S), _p(dev_table), _p(sorted_ids), _p(seg_offsets), _p(active),
+                                            _p(err), _stream(stream)), "lora_build_index_activated")
+
+
 def lora_build_index_moe(slot_ids, expert_ids, K, E, S, dev_table, sorted_ids, seg_offsets, active, err,
                          stream=None) -> None:
     """Index of the T * K (token, choice) pairs over S = n_adapters * E virtual slots."""
@@ -345,6 +362,12 @@ class TokenIndex:
         lora_build_index_seq(seq_slot_ids, tokens_per_seq, self.S, table.dev, self.sorted_ids, self.seg_offsets,
                              self.active, self.err, stream)
 
+
+    def build_activated(self, seq_ids, positions, seq_slot, invocation_start, table: SlotTable,
+                        stream=None) -> None:
+        """Index of this index's T tokens with aLoRA enablement per sequence."""
+        lora_build_index_activated(seq_ids, positions, seq_slot, invocation_start, self.S, table.dev,
+                                   self.sorted_ids, self.seg_offsets, self.active, self.err, stream)
 
     def build_moe(self, slot_ids, expert_ids, K: int, E: int, table: SlotTable, stream=None) -> None:
         """Index of len(slot_ids) * K pairs over this index's S = n_adapters * E virtual slots."""

@@ -42,7 +42,7 @@ EXPORTED = (
     "lora_workspace_bytes", "lora_shrink", "lora_expand", "lora_apply", "lora_apply_ex",
     "lora_resolve_path", "lora_apply_noalloc", "lora_workspace_xa_offset", "lora_build_index_seq",
     "lora_apply_overlap", "lora_premultiply_e4m3", "lora_moe_slot_pointers", "lora_build_index_moe",
-    "lora_apply_moe",
+    "lora_apply_moe", "lora_build_index_activated",
 )
 
 
@@ -106,6 +106,7 @@ def load() -> ctypes.CDLL:
         "lora_moe_slot_pointers": (ST, [I32, I32, SH, I32, P, P, P, P, P, P, P, P]),
         "lora_build_index_moe": (ST, [P, P, I32, I32, I32, I32, P, P, P, P, P, P]),
         "lora_apply_moe": (ST, [P, I64, I32, P, I64, I32, I32, SH, P, P, P, P, P, SZ, P, P]),
+        "lora_build_index_activated": (ST, [P, P, I32, P, P, I32, I32, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -22,6 +22,12 @@
 // s E + e of a table of S = n_adapters E slots, and is keyed S when the token
 // has no adapter.
 //
+// Activated LoRA (llama.cpp LoRA adapter page, "aLoRA:让适配器在 prompt 中间生效":
+// a request runs without its adapter up to the invocation point and with it
+// from there on): with seq_ids given, token t of sequence q = seq_ids[t] at
+// position positions[t] is keyed seq_slot[q] when positions[t] >=
+// invocation_start[q] and S (no adapter) before it.
+//
 // One thread block does the whole sort: histogram in shared memory, an
 // exclusive scan into the segment offsets, then a pass over the tokens in
 // blockDim-sized chunks in token order.  Inside a chunk, a token's place among
@@ -34,12 +40,30 @@ namespace lora {
 
 namespace {
 
+// Per-token activation of aLoRA: sequence ids and positions of the tokens, the
+// sequences' slots and invocation starts.
+struct Activation {
+    const int32_t *seq_ids, *positions, *seq_slot, *invocation_start;
+    int32_t n_seq;
+};
+
 // Key of item t: its slot, or S for no adapter or an id out of range (bad).
 // With expert_ids, item t is the pair (t / K, t % K) and its key the virtual
-// slot slot_ids[t / K] * E + expert_ids[t].
+// slot slot_ids[t / K] * E + expert_ids[t].  With act.seq_ids, the slot of
+// token t is its sequence's from the invocation start on.
 __device__ __forceinline__ int32_t index_key(const int32_t *__restrict__ slot_ids,
-                                             const int32_t *__restrict__ expert_ids, int32_t t, int32_t K,
-                                             int32_t E, int32_t S, bool &bad) {
+                                             const int32_t *__restrict__ expert_ids, const Activation &act,
+                                             int32_t t, int32_t K, int32_t E, int32_t S, bool &bad) {
+    if (act.seq_ids != nullptr) {
+        const int32_t q = act.seq_ids[t];
+        if (q < 0 || q >= act.n_seq) {
+            bad = true;
+            return S;
+        }
+        const int32_t s = act.positions[t] >= act.invocation_start[q] ? act.seq_slot[q] : -1;
+        bad |= (s < -1 || s >= S);
+        return (s >= 0 && s < S) ? s : S;
+    }
     if (expert_ids == nullptr) {
         const int32_t s = slot_ids[t];
         bad |= (s < -1 || s >= S);
@@ -52,7 +76,8 @@ __device__ __forceinline__ int32_t index_key(const int32_t *__restrict__ slot_id
 }
 
 __global__ void build_index_kernel(const int32_t *__restrict__ slot_ids, const int32_t *__restrict__ expert_ids,
-                                   int32_t T, int32_t tps, int32_t K, int32_t E, int32_t S, const void *table,
+                                   Activation act, int32_t T, int32_t tps, int32_t K, int32_t E, int32_t S,
+                                   const void *table,
                                    int32_t *__restrict__ sorted_ids, int32_t *__restrict__ seg_offsets,
                                    int32_t *__restrict__ active, int32_t *err) {
     extern __shared__ int32_t smem[];
@@ -74,7 +99,7 @@ __global__ void build_index_kernel(const int32_t *__restrict__ slot_ids, const i
 
     // 1. histogram
     bool bad = false;
-    for (int t = tid; t < T; t += nt) atomicAdd(&cursor[index_key(slot_ids, expert_ids, t, K, E, S, bad)], tps);
+    for (int t = tid; t < T; t += nt) atomicAdd(&cursor[index_key(slot_ids, expert_ids, act, t, K, E, S, bad)], tps);
     if (bad) report_error(err, LORA_ERR_SLOT_RANGE);
     __syncthreads();
 
@@ -103,7 +128,7 @@ __global__ void build_index_kernel(const int32_t *__restrict__ slot_ids, const i
         const bool valid = t < T;
         int32_t key = -1 - lane;  // unique per lane for invalid tokens: never matches
         bool unused = false;
-        if (valid) key = index_key(slot_ids, expert_ids, t, K, E, S, unused);
+        if (valid) key = index_key(slot_ids, expert_ids, act, t, K, E, S, unused);
         const unsigned peers = __match_any_sync(0xffffffffu, key);
         const unsigned lower = peers & ((1u << lane) - 1u);
         const int in_warp = __popc(lower);
@@ -136,7 +161,10 @@ size_t index_smem_bytes(int32_t S, int threads) {
 // token-expert pairs).
 cudaError_t launch_build_index(const int32_t *slot_ids, const int32_t *expert_ids, int32_t T, int32_t tps, int32_t K,
                                int32_t E, int32_t S, const void *table, int32_t *sorted_ids, int32_t *seg_offsets,
-                               int32_t *active, int32_t *err, cudaStream_t stream) {
+                               int32_t *active, int32_t *err, cudaStream_t stream, const int32_t *seq_ids,
+                               const int32_t *positions, const int32_t *seq_slot, const int32_t *invocation_start,
+                               int32_t n_seq) {
+    const Activation act{seq_ids, positions, seq_slot, invocation_start, n_seq};
     int threads = 1024;
     if (T < 1024) threads = ((T + 31) / 32) * 32;
     if (threads < 128) threads = 128;
@@ -152,7 +180,7 @@ cudaError_t launch_build_index(const int32_t *slot_ids, const int32_t *expert_id
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    build_index_kernel<<<1, threads, smem, stream>>>(slot_ids, expert_ids, T, tps, K, E, S, table, sorted_ids,
+    build_index_kernel<<<1, threads, smem, stream>>>(slot_ids, expert_ids, act, T, tps, K, E, S, table, sorted_ids,
                                                      seg_offsets, active, err);
     return cudaGetLastError();
 }

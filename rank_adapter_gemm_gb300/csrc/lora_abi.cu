@@ -11,7 +11,9 @@ namespace lora {
 cudaError_t launch_build_index(const int32_t *slot_ids, const int32_t *expert_ids, int32_t T, int32_t tps, int32_t K,
                                int32_t E, int32_t S, const void *table,
                                int32_t *sorted_ids, int32_t *seg_offsets, int32_t *active, int32_t *err,
-                               cudaStream_t stream);
+                               cudaStream_t stream, const int32_t *seq_ids = nullptr,
+                               const int32_t *positions = nullptr, const int32_t *seq_slot = nullptr,
+                               const int32_t *invocation_start = nullptr, int32_t n_seq = 0);
 cudaError_t launch_shrink(const uint16_t *x, int64_t ldx, const Shape &sh, const void *table,
                           const int32_t *sorted_ids, const int32_t *seg, float *xa, int32_t T, int32_t *err,
                           bool trigger_dependents, cudaStream_t stream);
@@ -246,6 +248,20 @@ lora_status_t lora_build_index_seq(const int32_t *seq_slot_ids, int32_t n_seq, i
     return from_cuda(lora::launch_build_index(seq_slot_ids, nullptr, n_seq, tokens_per_seq, 1, 1, S, dev_table,
                                               sorted_ids, seg_offsets, active, err,
                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_build_index_activated(const int32_t *seq_ids, const int32_t *positions, int32_t T,
+                                         const int32_t *seq_slot, const int32_t *invocation_start, int32_t n_seq,
+                                         int32_t S, const void *dev_table, int32_t *sorted_ids, int32_t *seg_offsets,
+                                         int32_t *active, int32_t *err, lora_stream_t stream) {
+    if (T < 0 || n_seq < 0 || S < 1 || S > LORA_MAX_SLOTS) return LORA_ERR_INVALID_ARG;
+    if (T > 0 && (seq_ids == nullptr || positions == nullptr || sorted_ids == nullptr)) return LORA_ERR_INVALID_ARG;
+    if (n_seq > 0 && (seq_slot == nullptr || invocation_start == nullptr)) return LORA_ERR_INVALID_ARG;
+    if (dev_table == nullptr || seg_offsets == nullptr || active == nullptr) return LORA_ERR_INVALID_ARG;
+    if (!aligned16(dev_table)) return LORA_ERR_ALIGNMENT;
+    return from_cuda(lora::launch_build_index(seq_ids, nullptr, T, 1, 1, 1, S, dev_table, sorted_ids, seg_offsets,
+                                              active, err, reinterpret_cast<cudaStream_t>(stream), seq_ids,
+                                              positions, seq_slot, invocation_start, n_seq));
 }
 
 lora_status_t lora_build_index_moe(const int32_t *slot_ids, const int32_t *expert_ids, int32_t T, int32_t K,

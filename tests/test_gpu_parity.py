@@ -810,3 +810,88 @@ def test_apply_moe_rejects_too_many_pairs():
     with pytest.raises(L.LoraError) as e:
         _check_moe(wl, 0, "moe too many pairs")
     assert e.value.status == 9
+
+
+# ---------------------------------------------------------------------------
+# Activated LoRA (aLoRA) enablement in the index
+# ---------------------------------------------------------------------------
+def _activation_case(seed, n_seq, S, max_len=40):
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(1, max_len + 1, size=n_seq)
+    past = rng.integers(0, 100, size=n_seq)  # tokens already cached before this batch
+    seq_ids = np.repeat(np.arange(n_seq), lens).astype(np.int32)
+    positions = np.concatenate([p + np.arange(n) for p, n in zip(past, lens)]).astype(np.int32)
+    seq_slot = rng.integers(-1, S, size=n_seq).astype(np.int32)
+    start = rng.integers(0, 150, size=n_seq).astype(np.int32)
+    start[::5] = 0  # plain LoRA sequences
+    return seq_ids, positions, seq_slot, start
+
+
+def _gpu_activated_index(seq_ids, positions, seq_slot, start, S, ranks, table=None):
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    T = len(seq_ids)
+    if table is None:
+        table = L.SlotTable(S, 1, 256)
+        dummy = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
+        ptrs = np.full(S, dummy.data_ptr(), dtype=np.uint64)
+        table.set(np.asarray(ranks, np.int32), np.ones(S, np.float32), ptrs, ptrs)
+    idx = L.TokenIndex(T, S)
+    dev = [torch.from_numpy(np.ascontiguousarray(a, np.int32)).cuda() for a in (seq_ids, positions, seq_slot, start)]
+    idx.build_activated(*dev, table)
+    torch.cuda.synchronize()
+    return idx
+
+
+@pytest.mark.parametrize("n_seq,S,seed", [(20, 8, 1), (64, 32, 2), (1, 1, 3), (300, 128, 4)])
+def test_activated_index_bit_exact(n_seq, S, seed):
+    seq_ids, positions, seq_slot, start = _activation_case(seed, n_seq, S)
+    ranks = np.random.default_rng(seed).choice([0, 8, 16], size=S).astype(np.int32)
+    idx = _gpu_activated_index(seq_ids, positions, seq_slot, start, S, ranks)
+    T = len(seq_ids)
+    slots = oracle.activated_token_slots(seq_ids, positions, seq_slot, start)
+    so_r, seg_r, act_r, st_r = oracle.build_index(slots, S, ranks)
+    np.testing.assert_array_equal(idx.sorted_ids.cpu().numpy()[:T], so_r)
+    np.testing.assert_array_equal(idx.seg_offsets.cpu().numpy(), seg_r)
+    np.testing.assert_array_equal(idx.active.cpu().numpy()[:1 + act_r[0]], act_r[:1 + act_r[0]])
+    assert int(idx.err.item()) == 0 and st_r == 0
+
+
+def test_activated_index_reports_unknown_sequence():
+    seq_ids, positions, seq_slot, start = _activation_case(9, 10, 4)
+    seq_ids[7] = 10
+    idx = _gpu_activated_index(seq_ids, positions, seq_slot, start, 4, np.full(4, 8, np.int32))
+    slots = oracle.activated_token_slots(seq_ids, positions, seq_slot, start)
+    so_r, seg_r, _, st_r = oracle.build_index(slots, 4, np.full(4, 8, np.int32))
+    assert int(idx.err.item()) == 4 and st_r == oracle.ERR_SLOT_RANGE
+    np.testing.assert_array_equal(idx.sorted_ids.cpu().numpy()[:len(seq_ids)], so_r)
+
+
+def test_apply_activated_decode_qkv():
+    """Packed QKV shapes (config 2's weights and rows) for a batch of sequences of
+    which some invoke their adapter mid-batch: y against the oracle on the
+    per-token slots of the activation rule."""
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import ResidentProjection, to_host_bits
+    wl = W.config(2)
+    rng = np.random.default_rng(12)
+    lens = np.full(16, 16)
+    seq_ids = np.repeat(np.arange(16), lens).astype(np.int32)
+    positions = np.tile(np.arange(16), 16).astype(np.int32) + 200
+    seq_slot = rng.integers(-1, wl.S, size=16).astype(np.int32)
+    start = (200 + rng.integers(0, 20, size=16)).astype(np.int32)
+    rp = ResidentProjection.from_workload(wl)
+    idx = _gpu_activated_index(seq_ids, positions, seq_slot, start, wl.S, wl.ranks, table=rp.table)
+    ws = L.Workspace(wl.T, rp.shape)
+    L.lora_apply(rp.x, rp.y, rp.shape, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active, ws.buf, idx.err)
+    torch.cuda.synchronize()
+    assert int(idx.err.item()) == 0
+    wl.slot_ids = oracle.activated_token_slots(seq_ids, positions, seq_slot, start)
+    assert (wl.slot_ids == -1).sum() > 0 and (wl.slot_ids >= 0).sum() > 0
+    ref, st = oracle_y(wl)
+    assert st == 0
+    y = to_host_bits(rp.y)
+    assert_y_close(y, ref, "activated")
+    keep = untouched_rows(wl)
+    np.testing.assert_array_equal(y[keep], wl.modules[0].y_in[keep])

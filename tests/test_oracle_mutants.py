@@ -111,3 +111,24 @@ def test_pins_catch_planted_speculative_index_mistake(name, monkeypatch):
     monkeypatch.setattr(oracle, "build_index_seq", SEQ_MUTANTS[name])
     with pytest.raises(AssertionError):
         pins.test_speculative_index_matches_pages_expansion(2, 4)
+
+
+# Activated-LoRA enablement is a thin rule in oracle/__init__.py; plant the
+# plausible slips in it.
+ACT_MUTANTS = {
+    # the adapter starts one token late (strict comparison)
+    "strict_start": lambda seq, pos, slot, start: np.where(
+        np.asarray(pos) > np.asarray(start)[np.asarray(seq)], np.asarray(slot)[np.asarray(seq)], -1).astype(np.int32),
+    # the adapter applies before the invocation point instead of after it
+    "reversed": lambda seq, pos, slot, start: np.where(
+        np.asarray(pos) < np.asarray(start)[np.asarray(seq)], np.asarray(slot)[np.asarray(seq)], -1).astype(np.int32),
+    # the invocation start ignored
+    "always_on": lambda seq, pos, slot, start: np.asarray(slot)[np.asarray(seq)].astype(np.int32),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ACT_MUTANTS))
+def test_pins_catch_planted_activation_mistake(name, monkeypatch):
+    monkeypatch.setattr(oracle, "activated_token_slots", ACT_MUTANTS[name])
+    with pytest.raises((AssertionError, IndexError)):
+        pins.test_activated_slots_hand_worked()

@@ -634,3 +634,23 @@ def test_moe_out_of_range_ids_and_pair_slots():
     assert st == oracle.ERR_SLOT_RANGE
     np.testing.assert_array_equal(y[[3, 5, 6, 7]], _f64(y_in[[3, 5, 6, 7]]))
     assert not np.array_equal(y[[0, 1, 2, 4]], _f64(y_in[[0, 1, 2, 4]]))
+
+
+# ---------------------------------------------------------------------------
+# Activated LoRA (llama.cpp's aLoRA): no adapter before the invocation point
+# ---------------------------------------------------------------------------
+def test_activated_slots_hand_worked():
+    """Sequence 0 (slot 3) invoked at position 2, sequence 1 without an adapter,
+    sequence 2 (slot 1) invoked at 7, past its tokens (the pages' "not found" case):
+    worked out by hand.  Start 0 everywhere is the plain per-sequence slot; an
+    unknown sequence id gives an out-of-range slot."""
+    seq = np.array([0, 0, 0, 0, 1, 1, 2, 2, 0], np.int32)
+    pos = np.array([0, 1, 2, 3, 0, 1, 5, 6, 4], np.int32)
+    slot = np.array([3, -1, 1], np.int32)
+    start = np.array([2, 0, 7], np.int32)
+    np.testing.assert_array_equal(oracle.activated_token_slots(seq, pos, slot, start),
+                                  [-1, -1, 3, 3, -1, -1, -1, -1, 3])
+    np.testing.assert_array_equal(oracle.activated_token_slots(seq, pos, slot, np.zeros(3, np.int32)),
+                                  [3, 3, 3, 3, -1, -1, 1, 1, 3])
+    bad = oracle.activated_token_slots(np.array([3], np.int32), np.array([0], np.int32), slot, start)
+    assert bad[0] >= 3
