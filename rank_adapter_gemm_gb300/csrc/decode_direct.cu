@@ -1071,7 +1071,6 @@ __global__ void __launch_bounds__(32 * kEWarps, 1) direct_expand_kernel(DArgs a,
     float4 X[2][2][2];
     e_load_xa(gc, buf, t, sh, a.T, lane, X);
     int32_t it = 0;
-    bool timed_out = false;
     while (gc.live) {
         const int32_t sn = (it + kEStages - 1) % kEStages, sc = it % kEStages;
         __syncwarp();  // every lane's reads of the slot refilled next are done
@@ -1083,9 +1082,11 @@ __global__ void __launch_bounds__(32 * kEWarps, 1) direct_expand_kernel(DArgs a,
         float4 Xn[2][2][2];
         if (!same) e_load_xa(gn, buf, t, sh, a.T, lane, Xn);
         cp_wait<kEStages - 1>();
-        if (!mbar_wait(sa(&bars[warp][sc]), static_cast<uint32_t>(it / kEStages) & 1u) && !timed_out) {
-            timed_out = true;
+        // a B tile that never lands (only a broken memory system) ends the warp's
+        // walk: report it and issue nothing more into the ring
+        if (!__all_sync(0xffffffffu, mbar_wait(sa(&bars[warp][sc]), static_cast<uint32_t>(it / kEStages) & 1u))) {
             if (lane == 0) report_error(a.err, LORA_ERR_TIMEOUT);
+            break;
         }
         e_compute<kF8>(gc, wring + sc * kESlot, X, t, a, lane);
         if (!same) {
