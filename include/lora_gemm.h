@@ -57,7 +57,7 @@ typedef struct CUstream_st *lora_stream_t;
 
 #define LORA_ABI_VERSION 1
 #define LORA_MAX_SLICES 4
-#define LORA_MAX_RANK 256
+#define LORA_MAX_RANK 512
 #define LORA_MAX_SLOTS 1024
 
 typedef enum {
@@ -84,7 +84,11 @@ typedef enum {
                                     MMA; needs T <= 2048, r_max <= 128 and k % 16 == 0, else the
                                     tensor-core decode kernels when they apply (LORA_PATH_DECODE_TC),
                                     else LORA_ERR_UNSUPPORTED */
-    LORA_PATH_DECODE_SPLIT = 2,  /* two launches: shrink then expand (programmatic dependent launch) */
+    LORA_PATH_DECODE_SPLIT = 2,  /* two launches: shrink then expand (programmatic dependent launch);
+                                    any rank up to LORA_MAX_RANK; sums reduced in a fixed order, so
+                                    results are bit-identical over runs (the deterministic choice:
+                                    the other decode paths add split-K partials with fp32 atomics
+                                    whose order varies) */
     LORA_PATH_PREFILL = 3,       /* two launches: tcgen05/TMEM tensor-core shrink (split-K over a
                                     thread-block cluster) and expand, on 128-token tiles of
                                     one slot's segment; needs r_max <= 64

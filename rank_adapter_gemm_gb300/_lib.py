@@ -13,7 +13,7 @@ from . import build as _build
 
 LORA_ABI_VERSION = 1
 LORA_MAX_SLICES = 4
-LORA_MAX_RANK = 256
+LORA_MAX_RANK = 512
 LORA_MAX_SLOTS = 1024
 LORA_DECODE_MAX_SEG = 256
 LORA_NOALLOC_WS_BYTES = 4 << 20

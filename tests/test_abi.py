@@ -125,3 +125,13 @@ def test_moe_slot_pointers_follow_the_expert_offset(L):
                 assert ap[v * 2 + i] == want_a and bp[v * 2 + i] == want_b
     with pytest.raises(L.LoraError):
         L.lora_moe_slot_pointers(n_ad, E + 1, sh, ranks, [1.0] * 3, a_base, b_base)
+
+
+def test_rank_limit_is_512(L):
+    """Ranks up to 512 (multiples of 8) are accepted by every host check; above it,
+    LORA_ERR_RANK."""
+    assert L.LORA_MAX_RANK == 512
+    L.lora_workspace_bytes(64, L.make_shape(4, 512, 1024, [1024]))
+    with pytest.raises(L.LoraError) as e:
+        L.lora_workspace_bytes(64, L.make_shape(4, 520, 1024, [1024]))
+    assert e.value.status == 3

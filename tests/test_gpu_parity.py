@@ -895,3 +895,23 @@ def test_apply_activated_decode_qkv():
     assert_y_close(y, ref, "activated")
     keep = untouched_rows(wl)
     np.testing.assert_array_equal(y[keep], wl.modules[0].y_in[keep])
+
+
+
+@pytest.mark.parametrize("path", ["auto", "decode_split", "decode_fused", "decode_direct", "prefill"])
+def test_apply_ranks_up_to_512(path):
+    """Ranks 512 and 264 next to 8: the split kernels (AUTO's choice above rank 128)
+    take any rank in 64-wide chunks; the paths with a lower rank bound refuse."""
+    wl = _small(81, 100, 1024, [1024, 256], 3, [512, 264, 8])
+    if path in ("decode_fused", "decode_direct", "prefill"):
+        import rank_adapter_gemm_gb300 as L
+        with pytest.raises(L.LoraError) as e:
+            gpu_apply(wl, path=path)
+        assert e.value.status == 9
+        return
+    y, err, *_ = gpu_apply(wl, path=path)
+    assert err == 0
+    ref, _ = oracle_y(wl)
+    assert_y_close(y, ref, f"ranks to 512 ({path})")
+    keep = untouched_rows(wl)
+    np.testing.assert_array_equal(y[keep], wl.modules[0].y_in[keep])
