@@ -111,13 +111,8 @@ __host__ __device__ inline int32_t cdiv(int32_t a, int32_t b) { return (a + b - 
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t sa(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
-// 16 bytes global -> shared through L1 (re-read weights hit there), or 16 zero
-// bytes when !valid (src is not read then).
-__device__ __forceinline__ void cp16_ca(uint32_t dst, const void *src, bool valid) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(valid ? 16 : 0)
-                 : "memory");
-}
-// Same through L2 only (activations and y).
+// 16 bytes global -> shared through L2 only (A, x and y: nothing is re-read
+// from L1), or 16 zero bytes when !valid (src is not read then).
 __device__ __forceinline__ void cp16_cg(uint32_t dst, const void *src, bool valid) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(valid ? 16 : 0)
                  : "memory");
@@ -146,11 +141,8 @@ __device__ __forceinline__ float4 ldg_f4(const float *p) {
     return v;
 }
 
-// Bulk (TMA) copies and L2 prefetches of contiguous byte ranges (16-byte
-// aligned, sizes multiples of 16), completion of copies counted on an mbarrier.
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
-}
+// Bulk (TMA) copies of contiguous byte ranges (16-byte aligned, sizes
+// multiples of 16), completion counted on an mbarrier.
 __device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
@@ -610,7 +602,7 @@ __device__ __forceinline__ void s_copy_stage(SCopy &s, uint32_t slot, int32_t kq
                 const int64_t off = 64 * static_cast<int64_t>(blk);
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    if (c < 2 * s.mt) cp16_ca(dst + c * kChunk, s.pa[c] + off, cv && ((s.vm >> c) & 1u));
+                    if (c < 2 * s.mt) cp16_cg(dst + c * kChunk, s.pa[c] + off, cv && ((s.vm >> c) & 1u));
                 const uint32_t dx = dst + 2 * s.mt * kChunk;
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt) {
@@ -662,29 +654,6 @@ __device__ __forceinline__ void s_reduce(const SGen &c, float *buf, const Tabs &
     }
 }
 
-// Brings what the expand reads into L2 while the shrink streams A: the B
-// matrix of every (active slot, slice) in 64 KB pieces and the y row of every
-// token with an adapter, spread over all threads of the grid.  A warp issues
-// its share once its first stage has landed: the prefetches then fill the DRAM
-// time after the first burst of A instead of delaying it.
-template <bool kF8>
-__device__ __forceinline__ void prefetch_expand_inputs(const Tabs &t, const Shape &sh, const DArgs &a) {
-    const int32_t NA = t.misc[0], G = gridDim.x, tid = threadIdx.x;
-    for (int32_t e = blockIdx.x + G * tid; e < NA * sh.n; e += G * static_cast<int32_t>(blockDim.x)) {
-        const int32_t ja = e / sh.n, i = e - ja * sh.n, r = t.a_r[ja];
-        if (r == 0) continue;
-        const unsigned char *B = reinterpret_cast<const unsigned char *>(t.bptr[t.a_slot[ja] * sh.n + i]);
-        const uint32_t bytes = (kF8 ? 1u : 2u) * static_cast<uint32_t>(t.soff[i + 1] - t.soff[i]) * r;
-        for (uint32_t o = 0; o < bytes; o += 65536u) bulk_prefetch_l2(B + o, min(65536u, bytes - o));
-    }
-    const uint32_t ybytes = 2u * static_cast<uint32_t>(t.soff[LORA_MAX_SLICES]);
-    const int32_t npos = min(max(t.seg[sh.S], 0), a.T);
-    for (int32_t p = blockIdx.x + G * tid; p < npos; p += G * static_cast<int32_t>(blockDim.x)) {
-        const int32_t tok = t.tok[p];
-        if (tok >= 0) bulk_prefetch_l2(a.y + static_cast<int64_t>(tok) * a.ldy, ybytes);
-    }
-}
-
 size_t direct_shrink_smem(int32_t S, int32_t n, int32_t T) {
     return static_cast<size_t>(kSWarps) * kSStages * kSChunks * kChunk + tabs_bytes(S, n, T);
 }
@@ -721,8 +690,6 @@ __global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a,
 #pragma unroll
     for (int s = 0; s < kSStages - 1; ++s) s_copy_stage<kF8>(cw, ring + s * kSlot, kq, t, sh, a, lane, nkb);
 
-    if (!cg.live) prefetch_expand_inputs<kF8>(t, sh, a);
-    bool prefetched = !cg.live;
     float acc[2][4][4];
     int32_t sc = 0, si = kSStages - 1;
     int32_t b = cg.bs, kb = 1, cpb = 1, MT = 1, NT = 1;
@@ -732,21 +699,10 @@ __global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a,
         cpb = 2 * MT + kXF * NT;
         kb = kSChunks / cpb;
     }
-    bool first = true;
     while (cg.live) {
-        if (first) {
-            // the first stage of every warp lands before any second stage is asked
-            // for: the opening burst is half as long
-            cp_wait<0>();
-            first = false;
-        }
         s_copy_stage<kF8>(cw, ring + si * kSlot, kq, t, sh, a, lane, nkb);
         si = si + 1 == kSStages ? 0 : si + 1;
         cp_wait<kSStages - 1>();
-        if (!prefetched) {
-            prefetch_expand_inputs<kF8>(t, sh, a);
-            prefetched = true;
-        }
         if (b == cg.bs) {
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt)
@@ -1065,16 +1021,15 @@ __global__ void __launch_bounds__(32 * kEWarps, 1) direct_expand_kernel(DArgs a,
     EGen gi;
     e_first<kF8>(gi, t, sh.n);
     EGen gc = gi;
+    // the whole ring in flight before the wait: B and y need nothing of the shrink
 #pragma unroll
-    for (int s = 0; s < kEStages - 1; ++s) e_copy_stage<kF8>(gi, wring + s * kESlot, sa(&bars[warp][s]), t, sh, a, lane, sh.n);
+    for (int s = 0; s < kEStages; ++s) e_copy_stage<kF8>(gi, wring + s * kESlot, sa(&bars[warp][s]), t, sh, a, lane, sh.n);
     pdl_wait();
     float4 X[2][2][2];
     e_load_xa(gc, buf, t, sh, a.T, lane, X);
     int32_t it = 0;
     while (gc.live) {
-        const int32_t sn = (it + kEStages - 1) % kEStages, sc = it % kEStages;
-        __syncwarp();  // every lane's reads of the slot refilled next are done
-        e_copy_stage<kF8>(gi, wring + sn * kESlot, sa(&bars[warp][sn]), t, sh, a, lane, sh.n);
+        const int32_t sc = it % kEStages;
         EGen gn = gc;
         e_advance<kF8>(gn, t, sh.n);
         // the next unit's sums: the same registers while (slot, slice, token group) holds
@@ -1089,6 +1044,8 @@ __global__ void __launch_bounds__(32 * kEWarps, 1) direct_expand_kernel(DArgs a,
             break;
         }
         e_compute<kF8>(gc, wring + sc * kESlot, X, t, a, lane);
+        __syncwarp();  // every lane's reads of slot sc are done: refill it with unit it + kEStages
+        e_copy_stage<kF8>(gi, wring + sc * kESlot, sa(&bars[warp][sc]), t, sh, a, lane, sh.n);
         if (!same) {
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
