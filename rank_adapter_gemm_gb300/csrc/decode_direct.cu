@@ -62,8 +62,10 @@ namespace lora {
 
 namespace {
 
-constexpr int kSWarps = 12;          // shrink: 3 warps per SM sub-partition
-constexpr int kEWarps = 8;           // expand
+constexpr int kSCtas = 2;            // shrink CTAs per SM
+constexpr int kSWarps = 6;           // shrink warps per CTA (12 per SM, 3 per sub-partition)
+constexpr int kECtas = 2;            // expand CTAs per SM
+constexpr int kEWarps = 4;           // expand warps per CTA
 constexpr int kChunk = 512;          // 16 bytes per lane
 constexpr int kSChunks = 11;         // shrink stage: 11 chunks (5.5 KB)
 constexpr int kSStages = 3;          // shrink ring depth per warp
@@ -593,7 +595,7 @@ __device__ __forceinline__ void s_copy_stage(SCopy &s, uint32_t slot, int32_t kq
                                              const DArgs &a, int lane, int32_t nkb) {
     if (s.gen.live) {
         const int32_t nb = min(s.kb, s.gen.be - s.b);
-#pragma unroll
+#pragma unroll(kF8 ? 1 : 4)
         for (int j = 0; j < 4; ++j) {
             if (j < nb) {
                 const int32_t blk = s.b + j;
@@ -661,7 +663,7 @@ size_t direct_shrink_smem(int32_t S, int32_t n, int32_t T) {
 // kF8: A in e4m3, x converted to e4m3 in registers, 64-column blocks of k,
 // token groups of 24 (a stage of 2 MT + 6 chunks holds one block).
 template <bool kF8>
-__global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a, Shape sh, const void *table) {
+__global__ void __launch_bounds__(32 * kSWarps, kSCtas) direct_shrink_kernel(DArgs a, Shape sh, const void *table) {
     constexpr int32_t kTG = VP<kF8>::TG, kXF = VP<kF8>::XF, kBC = VP<kF8>::BC;
     extern __shared__ __align__(128) unsigned char smem[];
     // the expand may start its prologue as soon as every CTA of this grid runs
@@ -711,7 +713,7 @@ __global__ void __launch_bounds__(32 * kSWarps, 1) direct_shrink_kernel(DArgs a,
         }
         const int32_t nb = min(kb, cg.be - b);
         const uint32_t slot = ring + sc * kSlot;
-#pragma unroll
+#pragma unroll(kF8 ? 1 : 4)
         for (int j = 0; j < 4; ++j) {
             if (j >= nb) continue;
             const uint32_t src = slot + j * cpb * kChunk;
@@ -1005,7 +1007,7 @@ size_t direct_expand_smem(int32_t S, int32_t n, int32_t T) {
 }
 
 template <bool kF8>
-__global__ void __launch_bounds__(32 * kEWarps, 1) direct_expand_kernel(DArgs a, Shape sh, const void *table) {
+__global__ void __launch_bounds__(32 * kEWarps, kECtas) direct_expand_kernel(DArgs a, Shape sh, const void *table) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t bars[kEWarps][kEStages];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1100,7 +1102,7 @@ cudaError_t launch_premultiply_e4m3(uint8_t *w, int64_t n, double scale, cudaStr
 bool decode_direct_supported(int32_t T, const Shape &sh, bool fp8) {
     return T >= 1 && T <= kMaxTokens && sh.r_max <= kMaxRank && sh.S <= kMaxSlots && sh.S * sh.n <= kMaxPtrs &&
            (!fp8 || sh.k % 16 == 0) && direct_shrink_smem(sh.S, sh.n, T) <= 227 * 1024 &&
-           direct_expand_smem(sh.S, sh.n, T) <= 227 * 1024;
+           direct_expand_smem(sh.S, sh.n, T) <= 227 * 1024;  // past half an SM the grid runs in more waves
 }
 
 namespace {
@@ -1151,7 +1153,7 @@ cudaError_t launch_direct_shrink(const uint16_t *x, int64_t ldx, uint16_t *y, in
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s_smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(num_sms));
+    cfg.gridDim = dim3(static_cast<unsigned>(kSCtas * num_sms));
     cfg.blockDim = dim3(32 * kSWarps);
     cfg.dynamicSmemBytes = s_smem;
     cfg.stream = stream;
@@ -1175,7 +1177,7 @@ cudaError_t launch_direct_expand(const uint16_t *x, int64_t ldx, uint16_t *y, in
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(e_smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(num_sms));
+    cfg.gridDim = dim3(static_cast<unsigned>(kECtas * num_sms));
     cfg.blockDim = dim3(32 * kEWarps);
     cfg.dynamicSmemBytes = e_smem;
     cfg.stream = stream;
