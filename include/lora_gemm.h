@@ -317,9 +317,10 @@ lora_status_t lora_apply(const void *x, int64_t ldx, void *y, int64_t ldy, int32
                          float *ws, size_t ws_bytes, int32_t *err, lora_stream_t stream);
 
 /*
- * The path lora_apply takes for this max_seg_hint (and T) on this build, for
- * r_max <= 64 and k % 16 == 0: requested itself unless it is LORA_PATH_AUTO.  *launches receives the number
- * of kernel launches the path makes per call (may be null).  Host only.
+ * The path lora_apply takes for this max_seg_hint (and T) in this library
+ * version, for r_max <= 64 and k % 16 == 0: requested itself unless it is
+ * LORA_PATH_AUTO.  *launches receives the number of kernel launches the path
+ * makes per call (may be null).  Host only.
  */
 lora_path_t lora_resolve_path(lora_path_t requested, int32_t T, int32_t max_seg_hint, int32_t *launches);
 

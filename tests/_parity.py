@@ -7,7 +7,7 @@ import numpy as np
 import oracle
 import workloads as W
 
-# spec tolerance for bf16 y with fp32 accumulation: |gpu - ref| <= ATOL + RTOL |ref|,
+# tolerance for bf16 y with fp32 accumulation: |gpu - ref| <= ATOL + RTOL |ref|,
 # ref = the fp64 oracle value before rounding to bf16
 ATOL = 1e-2
 RTOL = 2e-2

@@ -1,6 +1,6 @@
 """GPU parity: the CUDA library against the CPU oracle on the same seeded inputs.
 
-Index outputs must match bit for bit; y must lie within the north-star
+Index outputs must match bit for bit; y must lie within the y
 tolerance |gpu - ref| <= 1e-2 + 2e-2 |ref| of the fp64 oracle; rows of tokens
 without an active slot must keep their exact input bits.  Every call goes
 through the C ABI (via the ctypes binding).
