@@ -915,3 +915,48 @@ def test_apply_ranks_up_to_512(path):
     assert_y_close(y, ref, f"ranks to 512 ({path})")
     keep = untouched_rows(wl)
     np.testing.assert_array_equal(y[keep], wl.modules[0].y_in[keep])
+
+
+# ---------------------------------------------------------------------------
+# Degenerate batches through the FP8, MoE and aLoRA entry points
+# ---------------------------------------------------------------------------
+def test_empty_batches_of_the_newer_entry_points():
+    """T = 0: the pair and activated indexes give zero offsets and no active slot,
+    and the MoE branch returns without touching anything."""
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    S = 8
+    tab = L.SlotTable(S, 1, 64)
+    dummy = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
+    ptrs = np.full(S, dummy.data_ptr(), dtype=np.uint64)
+    tab.set(np.full(S, 16, np.int32), np.ones(S, np.float32), ptrs, ptrs)
+    empty = torch.zeros(0, dtype=torch.int32, device="cuda")
+    idx = L.TokenIndex(0, S)
+    idx.seg_offsets.fill_(7)
+    idx.active.fill_(7)
+    idx.build_moe(empty, empty, 2, 4, tab)
+    torch.cuda.synchronize()
+    assert idx.seg_offsets.cpu().numpy().tolist() == [0] * (S + 2) and int(idx.active[0].item()) == 0
+    idx.seg_offsets.fill_(7)
+    idx.build_activated(empty, empty, torch.zeros(3, dtype=torch.int32, device="cuda"),
+                        torch.zeros(3, dtype=torch.int32, device="cuda"), tab)
+    torch.cuda.synchronize()
+    assert idx.seg_offsets.cpu().numpy().tolist() == [0] * (S + 2) and int(idx.err.item()) == 0
+    shape = L.make_shape(S, 64, 128, [64])
+    ws = L.Workspace(0, shape)
+    x = torch.zeros(0, 128, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(0, 64, dtype=torch.bfloat16, device="cuda")
+    L.lora_apply_moe(x, y, 2, shape, tab.dev, idx.sorted_ids, idx.seg_offsets, idx.active, ws.buf, idx.err)
+    torch.cuda.synchronize()
+
+
+def test_no_adapter_batches_keep_y_fp8_and_moe():
+    """Every token without an adapter: y keeps its input bits through the FP8 path
+    and through the MoE branch."""
+    wl = _small_fp8(91, 64, 256, [256], 2, [16, 8])
+    wl.slot_ids[:] = -1
+    _check_fp8(wl, "fp8 no adapter")
+    wm = W.generate_moe(name="moe_none", seed=92, T=40, K=2, E=4, n_adapters=2, rank=8,
+                        modules=[{"name": "m", "k": 128, "slices": [64], "x_per_token": True}])
+    wm.slot_ids[:] = -1
+    _check_moe(wm, 0, "moe no adapter")
