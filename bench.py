@@ -246,6 +246,14 @@ def _workload(name, n_requests=16):
 HEADLINE = "LoRA-branch tokens/sec and achieved HBM GB/s (% of peak), Llama-3-8B QKV decode"
 
 
+def workload_name(config, wl):
+    """The `config.workload` string both arms print."""
+    if config == "decode_qkv":
+        return ("decode packed QKV, Llama-3-8B shapes: T=256, k=4096, slices 4096/1024/1024, S=32, "
+                "r in {8,16,32,64} (r_max 64), Zipf(1.1) slot popularity, alpha=2r")
+    return wl.description
+
+
 def metric_name(config):
     return HEADLINE if config == "decode_qkv" else \
         f"LoRA-branch tokens/sec and achieved HBM GB/s (% of peak), {config}"
@@ -426,9 +434,7 @@ def run_ours(args):
         "dtype": "e4m3 (adapters; x rounded to e4m3, y bf16)" if wl.weights == "e4m3" else "bf16",
         "data": "synthetic (seeded: workloads.config)",
         "config": {
-            "workload": wl.description if args.config != "decode_qkv" else
-            "decode packed QKV, Llama-3-8B shapes: T=256, k=4096, slices 4096/1024/1024, S=32, "
-            "r in {8,16,32,64} (r_max 64), Zipf(1.1) slot popularity, alpha=2r",
+            "workload": workload_name(args.config, wl),
             "config": args.config,
             "layers_per_step": len(layers),
             "calls_per_step": len(layers),
@@ -594,7 +600,7 @@ def run_moe(args):
         "dtype": "bf16",
         "data": "synthetic (seeded: workloads.moe_config)",
         "config": {
-            "workload": wl.description,
+            "workload": workload_name(args.config, wl),
             "config": args.config,
             "layers_per_step": len(layers),
             "calls_per_step": len(layers),
@@ -698,7 +704,7 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded: workloads.config)",
-        "config": {"workload": wl.description, "config": args.config},
+        "config": {"workload": workload_name(args.config, wl), "config": args.config},
         "impl": "reference",
         "cpu_baseline": {"kind": "oracle", "cores": 1, "value": value,
                          "sample": f"{n_rows} of {len(rows)} rows ({'token-expert pairs' if per_tok > 1 else 'tokens'}) "
