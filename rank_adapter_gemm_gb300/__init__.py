@@ -25,7 +25,7 @@ __all__ = [
     "LoraError", "lora_shape_t", "make_shape", "lora_abi_version", "lora_status_string", "lora_scale",
     "lora_premultiply", "lora_premultiply_e4m3", "lora_slot_table_bytes", "lora_pack_slot_table", "lora_set_slot_table",
     "lora_build_index", "lora_build_index_seq", "lora_workspace_bytes", "lora_workspace_xa_offset", "lora_shrink", "lora_expand", "lora_apply", "lora_resolve_path",
-    "lora_apply_noalloc", "lora_apply_overlap", "lora_moe_slot_pointers", "lora_build_index_moe", "lora_apply_moe",
+    "apply", "lora_apply_noalloc", "lora_apply_overlap", "lora_moe_slot_pointers", "lora_build_index_moe", "lora_apply_moe",
     "lora_build_index_activated", "apply_with_base", "SlotTable", "TokenIndex", "Workspace",
 ]
 
@@ -187,6 +187,13 @@ def lora_apply(x, y, shape, dev_table, sorted_ids, seg_offsets, active, ws, err,
         check(load().lora_apply(*args, *tail), "lora_apply")
     else:
         check(load().lora_apply_ex(*args, PATHS[path], *tail), "lora_apply_ex")
+
+
+def apply(x, y, table, index, ws, shape, max_seg_hint: int = 0, path: str = "auto", stream=None) -> None:
+    """y += the branch for x, with a SlotTable, a built TokenIndex and a Workspace
+    (their device buffers passed to lora_apply / lora_apply_ex); raises on error."""
+    lora_apply(x, y, shape, table.dev, index.sorted_ids, index.seg_offsets, index.active, ws.buf, index.err,
+               max_seg_hint=max_seg_hint, path=path, stream=stream)
 
 
 def lora_apply_overlap(x, y, shape, dev_table, sorted_ids, seg_offsets, active, ws, err, y_ready=None,

@@ -960,3 +960,20 @@ def test_no_adapter_batches_keep_y_fp8_and_moe():
                         modules=[{"name": "m", "k": 128, "slices": [64], "x_per_token": True}])
     wm.slot_ids[:] = -1
     _check_moe(wm, 0, "moe no adapter")
+
+
+def test_object_level_apply():
+    """apply(x, y, table, index, ws, shape) is lora_apply on the objects' buffers."""
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import ResidentProjection, to_host_bits
+    wl = W.config(0)
+    rp = ResidentProjection.from_workload(wl)
+    idx = L.TokenIndex(wl.T, wl.S)
+    idx.build(torch.from_numpy(wl.slot_ids).cuda(), rp.table)
+    ws = L.Workspace(wl.T, rp.shape)
+    L.apply(rp.x, rp.y, rp.table, idx, ws, rp.shape)
+    torch.cuda.synchronize()
+    assert int(idx.err.item()) == 0
+    ref, _ = oracle_y(wl)
+    assert_y_close(to_host_bits(rp.y), ref, "object-level apply")
