@@ -59,6 +59,8 @@ def parse_args(argv=None):
                    help="auto takes decode_direct_fp8 for a workload with FP8 adapters")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-plan", action="store_true",
+                   help="warp-streaming paths: rebuild the tables in every call instead of per-step plans")
     p.add_argument("--with-base", default="none", choices=["none", "serial", "overlap"],
                    help="time the base projection y = x W0^T (bf16 library GEMM) with the branch: one after the "
                         "other on one stream, or the branch on an aux stream overlapping the GEMM")
@@ -369,9 +371,15 @@ def run_ours(args):
             d = int(sum(lay.widths)) if hasattr(lay, "widths") else int(lay.y.shape[1])
             w0.append((torch.randn(d, lay.x.shape[1], device=dev, generator=g) * 0.02).to(torch.bfloat16))
     aux = torch.cuda.Stream(device=dev)
+    resolved0, _ = L.lora_resolve_path(args.path, T, max_seg)
+    use_plan = not args.no_plan and args.with_base == "none" and resolved0 in ("decode_direct", "decode_direct_fp8")
+    plans = [L.Plan(T, lay.shape, resolved0, device=dev) for lay in layers] if use_plan else []
 
     def apply_layer(l):
         lay = layers[l]
+        if use_plan:
+            plans[l].apply(lay.x, lay.y, ws[l % len(ws)], index.err)
+            return
         if args.with_base == "overlap":
             L.apply_with_base(lay.x, w0[l], lay.y, lay.shape, lay.table.dev, index, ws_of[l], aux,
                               max_seg_hint=max_seg, path=args.path)
@@ -384,6 +392,9 @@ def run_ours(args):
     def index_part():
         layers[0].refresh_table()
         _build_index(index, slot_dev, layers[0].table, wl.tokens_per_seq)
+        if use_plan:  # one launch per shape: a plan per layer, each with its layer's weight pointers
+            for m in mods:
+                L.lora_build_plans(plans[m::len(mods)], [lay.table for lay in layers[m::len(mods)]], index)
 
     def apply_part():
         for l in range(len(layers)):
@@ -410,11 +421,11 @@ def run_ours(args):
     call_s = apply_ms_mean / 1e3 / len(layers)
     achieved_gbs = sum(per_layer_bytes) / len(layers) / call_s / 1e9
     resolved, launches_per_apply = L.lora_resolve_path(args.path, T, max_seg)
-    gpu_launches = args.steps * (1 + len(layers) * launches_per_apply)
+    gpu_launches = args.steps * (1 + len(layers) * launches_per_apply + (len(mods) if use_plan else 0))
 
     e2e = None
     if not args.no_e2e and args.with_base == "none":
-        e2e = run_e2e(args, wl, layers, index, slot_dev, ws_of, max_seg, dev, world)
+        e2e = run_e2e(args, wl, layers, index, slot_dev, ws_of, max_seg, dev, world, plans, mods, ws)
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
@@ -438,7 +449,7 @@ def run_ours(args):
             "config": args.config,
             "layers_per_step": len(layers),
             "calls_per_step": len(layers),
-            "path": resolved,
+            "path": resolved + (" with per-step plans" if use_plan else ""),
             "l2": f"inputs larger than L2: {len(layers)} distinct layer buffer sets, "
                   f"{sum(per_layer_bytes) / 1e9:.2f} GB of algorithmic bytes per step",
             "parallelism": f"replicas x{world}",
@@ -475,7 +486,7 @@ def run_ours(args):
     return out, rank
 
 
-def run_e2e(args, wl, layers, index, slot_dev, ws_of, max_seg, dev, world):
+def run_e2e(args, wl, layers, index, slot_dev, ws_of, max_seg, dev, world, plans=(), mods=(0,), ws=()):
     """Same metric with host buffers: every step copies slot ids and each layer's
     x and y from pinned host memory, runs the step, and reads every y back."""
     import torch
@@ -493,9 +504,15 @@ def run_e2e(args, wl, layers, index, slot_dev, ws_of, max_seg, dev, world):
             lay.x.copy_(hx, non_blocking=True)
             lay.y.copy_(hy, non_blocking=True)
         _build_index(index, slot_dev, layers[0].table, wl.tokens_per_seq)
+        if plans:
+            for m in mods:
+                L.lora_build_plans(plans[m::len(mods)], [lay.table for lay in layers[m::len(mods)]], index)
         for l, lay in enumerate(layers):
-            L.lora_apply(lay.x, lay.y, lay.shape, lay.table.dev, index.sorted_ids, index.seg_offsets,
-                         index.active, ws_of[l], index.err, max_seg_hint=max_seg, path=args.path)
+            if plans:
+                plans[l].apply(lay.x, lay.y, ws[l % len(ws)], index.err)
+            else:
+                L.lora_apply(lay.x, lay.y, lay.shape, lay.table.dev, index.sorted_ids, index.seg_offsets,
+                             index.active, ws_of[l], index.err, max_seg_hint=max_seg, path=args.path)
         for lay, ho in zip(layers, h_out):
             ho.copy_(lay.y, non_blocking=True)
 

@@ -407,6 +407,47 @@ lora_status_t lora_build_index_activated(const int32_t *seq_ids, const int32_t *
                                          int32_t *active, int32_t *err, lora_stream_t stream);
 
 /*
+ * A plan: the tables the two warp-streaming kernels otherwise build at the start
+ * of every call (the active slots, their token ranges and ranks, the split of
+ * the work over the warps), built once per batch and shape and then read by
+ * every call of that shape (one table image per kernel, loaded with one pass of
+ * 16-byte copies).  Rebuild it whenever the index or the slot table changes.
+ *
+ * lora_plan_bytes: the plan's size for T tokens and this shape (0 for T < 1 or
+ * a bad shape).
+ *
+ * lora_build_plan: one launch on `stream` that reads the slot table and the
+ * index (after lora_build_index) and writes the plan (device, 16-byte aligned,
+ * plan_bytes >= lora_plan_bytes).  path: LORA_PATH_DECODE_DIRECT or
+ * LORA_PATH_DECODE_DIRECT_FP8 (the kernels the plan is for; else
+ * LORA_ERR_UNSUPPORTED, also when those kernels do not take the shape).  Device
+ * data errors of the index are reported here, as lora_apply would.
+ *
+ * lora_apply_plan: lora_apply_ex on that path with the plan instead of the table
+ * and the index.  A plan built for another T, shape, slot count or path is
+ * reported as LORA_ERR_INVALID_ARG in err and the call leaves y unchanged.
+ * Other arguments, checks and errors as lora_apply_ex.
+ */
+size_t lora_plan_bytes(int32_t T, const lora_shape_t *shape);
+lora_status_t lora_build_plan(int32_t T, const lora_shape_t *shape, const void *dev_table, const int32_t *sorted_ids,
+                              const int32_t *seg_offsets, const int32_t *active, lora_path_t path, void *plan,
+                              size_t plan_bytes, int32_t *err, lora_stream_t stream);
+lora_status_t lora_apply_plan(const void *x, int64_t ldx, void *y, int64_t ldy, int32_t T, const lora_shape_t *shape,
+                              const void *plan, size_t plan_bytes, lora_path_t path, float *ws, size_t ws_bytes,
+                              int32_t *err, lora_stream_t stream);
+
+/*
+ * The plans of `count` slot tables that share the shape and the index (the
+ * layers of one step, each with its own weights), in one launch: dev_tables and
+ * plans are host arrays of `count` device pointers, each plan plan_bytes long.
+ * Checks and errors as lora_build_plan, for every table and plan.
+ */
+lora_status_t lora_build_plans(int32_t T, const lora_shape_t *shape, int32_t count, const void *const *dev_tables,
+                               void *const *plans, size_t plan_bytes, const int32_t *sorted_ids,
+                               const int32_t *seg_offsets, const int32_t *active, lora_path_t path, int32_t *err,
+                               lora_stream_t stream);
+
+/*
  * Routed-expert (MoE) LoRA.  llama.cpp LoRA adapter page, "MoE 专属的
  * build_lora_mm_id": in an expert layer both the A and the B product are routed
  * by the token's expert ids, like the base weights, so each (token, chosen

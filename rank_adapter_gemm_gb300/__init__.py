@@ -26,7 +26,7 @@ __all__ = [
     "lora_premultiply", "lora_premultiply_e4m3", "lora_slot_table_bytes", "lora_pack_slot_table", "lora_set_slot_table",
     "lora_build_index", "lora_build_index_seq", "lora_workspace_bytes", "lora_workspace_xa_offset", "lora_shrink", "lora_expand", "lora_apply", "lora_resolve_path",
     "apply", "lora_apply_noalloc", "lora_apply_overlap", "lora_moe_slot_pointers", "lora_build_index_moe", "lora_apply_moe",
-    "lora_build_index_activated", "apply_with_base", "SlotTable", "TokenIndex", "Workspace",
+    "lora_build_index_activated", "lora_plan_bytes", "lora_build_plan", "lora_apply_plan", "lora_build_plans", "Plan", "apply_with_base", "SlotTable", "TokenIndex", "Workspace",
 ]
 
 
@@ -331,6 +331,64 @@ def lora_apply_moe(x, y, K, shape, dev_table, sorted_ids, seg_offsets, active, w
     check(load().lora_apply_moe(_p(x), ldx, int(bool(x_per_token)), _p(y), ldy, T, int(K), ctypes.byref(shape),
                                 _p(dev_table), _p(sorted_ids), _p(seg_offsets), _p(active), _p(ws),
                                 ws.numel() * ws.element_size(), _p(err), _stream(stream)), "lora_apply_moe")
+
+
+def lora_plan_bytes(T: int, shape: lora_shape_t) -> int:
+    return int(load().lora_plan_bytes(int(T), ctypes.byref(shape)))
+
+
+def lora_build_plan(T, shape, dev_table, sorted_ids, seg_offsets, active, plan, err, path: str = "decode_direct",
+                    stream=None) -> None:
+    check(load().lora_build_plan(int(T), ctypes.byref(shape), _p(dev_table), _p(sorted_ids), _p(seg_offsets),
+                                 _p(active), PATHS[path], _p(plan), plan.numel() * plan.element_size(), _p(err),
+                                 _stream(stream)), "lora_build_plan")
+
+
+def lora_apply_plan(x, y, shape, plan, ws, err, path: str = "decode_direct", stream=None) -> None:
+    ldx = _rows(x, "x")
+    ldy = _rows(y, "y")
+    if x.shape[0] != y.shape[0]:
+        raise ValueError("x and y must have the same number of rows")
+    check(load().lora_apply_plan(_p(x), ldx, _p(y), ldy, int(x.shape[0]), ctypes.byref(shape), _p(plan),
+                                 plan.numel() * plan.element_size(), PATHS[path], _p(ws), ws.numel() * ws.element_size(),
+                                 _p(err), _stream(stream)), "lora_apply_plan")
+
+
+def lora_build_plans(plans, tables, index, stream=None) -> None:
+    """The plans of several slot tables of one shape and batch (e.g. every layer of
+    a step), in one launch; plans[j] is built for tables[j]."""
+    if len(plans) != len(tables):
+        raise ValueError("one table per plan")
+    if not plans:
+        return
+    p0 = plans[0]
+    if any(p.T != p0.T or p.path != p0.path or p.buf.numel() != p0.buf.numel() for p in plans):
+        raise ValueError("plans of one call share T, shape and path")
+    tabs = (ctypes.c_void_p * len(plans))(*[t.dev.data_ptr() for t in tables])
+    bufs = (ctypes.c_void_p * len(plans))(*[p.buf.data_ptr() for p in plans])
+    check(load().lora_build_plans(p0.T, ctypes.byref(p0.shape), len(plans), tabs, bufs, p0.buf.numel(),
+                                  _p(index.sorted_ids), _p(index.seg_offsets), _p(index.active), PATHS[p0.path],
+                                  _p(index.err), _stream(stream)), "lora_build_plans")
+
+
+class Plan:
+    """The tables of the warp-streaming kernels for one batch and shape, built once
+    (after the index) and used by every call of that shape."""
+
+    def __init__(self, T: int, shape: lora_shape_t, path: str = "decode_direct", device="cuda"):
+        torch = _torch()
+        nbytes = lora_plan_bytes(T, shape)
+        if nbytes == 0:
+            raise ValueError("no plan for this T and shape")
+        self.T, self.shape, self.path = int(T), shape, path
+        self.buf = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+
+    def build(self, index, table, stream=None) -> None:
+        lora_build_plan(self.T, self.shape, table.dev, index.sorted_ids, index.seg_offsets, index.active, self.buf,
+                        index.err, self.path, stream)
+
+    def apply(self, x, y, ws, err, stream=None) -> None:
+        lora_apply_plan(x, y, self.shape, self.buf, ws.buf, err, self.path, stream)
 
 
 class SlotTable:

@@ -42,7 +42,8 @@ EXPORTED = (
     "lora_workspace_bytes", "lora_shrink", "lora_expand", "lora_apply", "lora_apply_ex",
     "lora_resolve_path", "lora_apply_noalloc", "lora_workspace_xa_offset", "lora_build_index_seq",
     "lora_apply_overlap", "lora_premultiply_e4m3", "lora_moe_slot_pointers", "lora_build_index_moe",
-    "lora_apply_moe", "lora_build_index_activated",
+    "lora_apply_moe", "lora_build_index_activated", "lora_plan_bytes", "lora_build_plan", "lora_apply_plan",
+    "lora_build_plans",
 )
 
 
@@ -107,6 +108,10 @@ def load() -> ctypes.CDLL:
         "lora_build_index_moe": (ST, [P, P, I32, I32, I32, I32, P, P, P, P, P, P]),
         "lora_apply_moe": (ST, [P, I64, I32, P, I64, I32, I32, SH, P, P, P, P, P, SZ, P, P]),
         "lora_build_index_activated": (ST, [P, P, I32, P, P, I32, I32, P, P, P, P, P, P]),
+        "lora_plan_bytes": (SZ, [I32, SH]),
+        "lora_build_plan": (ST, [I32, SH, P, P, P, P, ST, P, SZ, P, P]),
+        "lora_apply_plan": (ST, [P, I64, P, I64, I32, SH, P, SZ, ST, P, SZ, P, P]),
+        "lora_build_plans": (ST, [I32, SH, I32, P, P, SZ, P, P, P, ST, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -104,6 +104,7 @@ struct DArgs {
     int32_t *exits;      // expand CTAs that finished this call
     int32_t *err;
     int32_t T;
+    const unsigned char *plan;  // this kernel's table image from a plan, or null: build the tables
 };
 
 __host__ __device__ inline int32_t cdiv(int32_t a, int32_t b) { return (a + b - 1) / b; }
@@ -350,7 +351,8 @@ __device__ void build_tabs(const DArgs &a, const Shape &sh, const void *table, c
         cp4(t.misc + 3, hdr);
         cp4(t.misc + 4, hdr + 1);
         cp4(t.misc + 5, hdr + 2);
-        cp4(t.misc + 1, a.gen);
+        if (a.gen != nullptr) cp4(t.misc + 1, a.gen);
+        else t.misc[1] = 0;
         int32_t c = 0, o = 0;
 #pragma unroll
         for (int i = 0; i <= LORA_MAX_SLICES; ++i) {
@@ -427,6 +429,31 @@ __device__ void build_tabs(const DArgs &a, const Shape &sh, const void *table, c
         if (lane == 0) {
             t.a_pre[NA] = carry;
             t.misc[0] = NA;
+        }
+    }
+    __syncthreads();
+}
+
+// Prologue from a plan: the table image a plan kernel built with build_tabs
+// for this shape and batch, copied in 16-byte pieces, then the call counter
+// read fresh.  An image for another batch size or table is reported and leaves
+// the call without work.  Ends with a barrier.
+template <bool kF8>
+__device__ void load_plan(const DArgs &a, const Shape &sh, const Tabs &t, size_t bytes) {
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    unsigned char *dst = reinterpret_cast<unsigned char *>(t.misc);
+    for (size_t o = 16 * static_cast<size_t>(tid); o < bytes; o += 16 * static_cast<size_t>(nthr))
+        cp16_cg(sa(dst + o), a.plan + o, true);
+    cp_commit();
+    cp_wait<0>();
+    __syncthreads();
+    if (tid == 0) {
+        t.misc[1] = *reinterpret_cast<volatile const int32_t *>(a.gen);
+        if (t.misc[2] != a.T || t.misc[3] != kTableMagic || t.misc[4] != sh.S || t.misc[5] != sh.n ||
+            t.misc[6] != (kF8 ? 1 : 0)) {
+            if (blockIdx.x == 0) report_error(a.err, LORA_ERR_INVALID_ARG);
+            t.misc[0] = 0;
+            t.a_pre[0] = 0;
         }
     }
     __syncthreads();
@@ -670,7 +697,8 @@ __global__ void __launch_bounds__(32 * kSWarps, kSCtas) direct_shrink_kernel(DAr
     pdl_launch_dependents();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Tabs t = carve(smem + static_cast<size_t>(kSWarps) * kSStages * kSChunks * kChunk, sh.S, sh.n, a.T);
-    build_tabs<false>(a, sh, table, t, kTG, kXF, kBC);
+    if (a.plan != nullptr) load_plan<kF8>(a, sh, t, tabs_bytes(sh.S, sh.n, a.T));
+    else build_tabs<false>(a, sh, table, t, kTG, kXF, kBC);
     const int32_t gen = t.misc[1];
     float *buf = (gen & 1) ? a.acc1 : a.acc0;
     {
@@ -1017,7 +1045,8 @@ __global__ void __launch_bounds__(32 * kEWarps, kECtas) direct_expand_kernel(DAr
     }
     const Tabs t = carve(smem + static_cast<size_t>(kEWarps) * kEStages * kESlot, sh.S, sh.n, a.T);
     // tables, B and y are not written by the shrink: read them before the wait
-    build_tabs<true>(a, sh, table, t, VP<kF8>::BW, 1, 32);
+    if (a.plan != nullptr) load_plan<kF8>(a, sh, t, tabs_bytes(sh.S, sh.n, a.T));
+    else build_tabs<true>(a, sh, table, t, VP<kF8>::BW, 1, 32);
     const float *buf = (t.misc[1] & 1) ? a.acc1 : a.acc0;
     const uint32_t wring = sa(smem) + warp * (kEStages * kESlot);
     EGen gi;
@@ -1069,6 +1098,38 @@ __global__ void __launch_bounds__(32 * kEWarps, kECtas) direct_expand_kernel(DAr
             atomicAdd(a.gen, 1);
         }
     }
+}
+
+// A plan: the tables both kernels of a call would build in their prologue,
+// built once for a batch (index) and shape by the same build_tabs and stored as
+// two images, the shrink's then the expand's.  misc[2] records T and misc[6]
+// the variant, which load_plan checks.  One launch builds the plans of up to
+// kMaxPlanJobs slot tables of the same shape and batch (the layers of a step):
+// block 2j + 0 / 2j + 1 writes the shrink / expand image of job j.
+constexpr int kMaxPlanJobs = 120;
+struct PlanJobs {
+    const void *table[kMaxPlanJobs];
+    unsigned char *plan[kMaxPlanJobs];
+};
+
+template <bool kF8>
+__global__ void __launch_bounds__(256) direct_plan_kernel(DArgs a, Shape sh, PlanJobs jobs) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int job = blockIdx.x >> 1, img = blockIdx.x & 1;
+    const void *table = jobs.table[job];
+    unsigned char *plan = jobs.plan[job];
+    const Tabs t = carve(smem, sh.S, sh.n, a.T);
+    if (img == 0) build_tabs<false>(a, sh, table, t, VP<kF8>::TG, VP<kF8>::XF, VP<kF8>::BC);
+    else build_tabs<true>(a, sh, table, t, VP<kF8>::BW, 1, 32);
+    if (threadIdx.x == 0) {
+        t.misc[2] = a.T;
+        t.misc[6] = kF8 ? 1 : 0;
+    }
+    __syncthreads();
+    const size_t bytes = tabs_bytes(sh.S, sh.n, a.T);
+    unsigned char *out = plan + img * bytes;
+    for (size_t o = 16 * static_cast<size_t>(threadIdx.x); o < bytes; o += 16 * static_cast<size_t>(blockDim.x))
+        *reinterpret_cast<uint4 *>(out + o) = *reinterpret_cast<const uint4 *>(smem + o);
 }
 
 // Load-time scale of an FP8 B (TensorRT-LLM LoRA serving page, "第五步:FP8 特判"):
@@ -1133,21 +1194,56 @@ cudaError_t direct_args(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy
     a.exits = a.gen + 1;
     a.err = err;
     a.T = T;
+    a.plan = nullptr;
     return cudaSuccess;
 }
 
 }  // namespace
+
+// A plan holds two table images (shrink, expand) of tabs_bytes each.
+size_t direct_plan_bytes(int32_t T, const Shape &sh) { return 2 * tabs_bytes(sh.S, sh.n, T); }
+
+// Builds the plans of `count` slot tables (one batch and shape) for the bf16 or
+// the FP8 kernels, kMaxPlanJobs per launch.
+cudaError_t launch_direct_plans(const Shape &sh, const void *const *tables, unsigned char *const *plans,
+                                int32_t count, const int32_t *sorted_ids, const int32_t *seg, const int32_t *active,
+                                int32_t T, bool fp8, int32_t *err, cudaStream_t stream) {
+    if (!decode_direct_supported(T, sh, fp8)) return cudaErrorNotSupported;
+    DArgs a = {};
+    a.sorted_ids = sorted_ids;
+    a.seg = seg;
+    a.active = active;
+    a.err = err;
+    a.T = T;
+    const size_t smem = tabs_bytes(sh.S, sh.n, T);
+    auto kern = fp8 ? direct_plan_kernel<true> : direct_plan_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    for (int32_t j0 = 0; j0 < count; j0 += kMaxPlanJobs) {
+        PlanJobs jobs = {};
+        const int32_t m = std::min(kMaxPlanJobs, count - j0);
+        for (int32_t j = 0; j < m; ++j) {
+            jobs.table[j] = tables[j0 + j];
+            jobs.plan[j] = plans[j0 + j];
+        }
+        kern<<<2 * m, 256, smem, stream>>>(a, sh, jobs);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
 
 // The x-only half: sums of x A^T into the call's buffer (reads x, A; writes the
 // workspace only).  fp8: A is e4m3 and x is rounded to e4m3 on the way in.
 cudaError_t launch_direct_shrink(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                  const void *table, const int32_t *sorted_ids, const int32_t *seg,
                                  const int32_t *active, float *ws, int32_t T, int32_t *err, bool fp8,
-                                 cudaStream_t stream, int32_t x_div) {
+                                 cudaStream_t stream, int32_t x_div, const unsigned char *plan) {
     DArgs a;
     int num_sms = 0;
     cudaError_t e = direct_args(x, ldx, y, ldy, sh, sorted_ids, seg, active, ws, T, err, fp8, x_div, a, num_sms);
     if (e != cudaSuccess) return e;
+    a.plan = plan;  // the shrink's image comes first
     const size_t s_smem = direct_shrink_smem(sh.S, sh.n, T);
     auto kern = fp8 ? direct_shrink_kernel<true> : direct_shrink_kernel<false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s_smem));
@@ -1167,11 +1263,12 @@ cudaError_t launch_direct_shrink(const uint16_t *x, int64_t ldx, uint16_t *y, in
 cudaError_t launch_direct_expand(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                  const void *table, const int32_t *sorted_ids, const int32_t *seg,
                                  const int32_t *active, float *ws, int32_t T, int32_t *err, bool fp8,
-                                 bool programmatic, cudaStream_t stream) {
+                                 bool programmatic, cudaStream_t stream, const unsigned char *plan) {
     DArgs a;
     int num_sms = 0;
     cudaError_t e = direct_args(x, ldx, y, ldy, sh, sorted_ids, seg, active, ws, T, err, fp8, 1, a, num_sms);
     if (e != cudaSuccess) return e;
+    a.plan = plan != nullptr ? plan + tabs_bytes(sh.S, sh.n, T) : nullptr;
     const size_t e_smem = direct_expand_smem(sh.S, sh.n, T);
     auto kern = fp8 ? direct_expand_kernel<true> : direct_expand_kernel<false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(e_smem));
@@ -1192,11 +1289,12 @@ cudaError_t launch_direct_expand(const uint16_t *x, int64_t ldx, uint16_t *y, in
 cudaError_t launch_decode_direct(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                  const void *table, const int32_t *sorted_ids, const int32_t *seg,
                                  const int32_t *active, float *ws, int32_t T, int32_t *err, bool fp8,
-                                 cudaStream_t stream, int32_t x_div) {
-    cudaError_t e =
-        launch_direct_shrink(x, ldx, y, ldy, sh, table, sorted_ids, seg, active, ws, T, err, fp8, stream, x_div);
+                                 cudaStream_t stream, int32_t x_div, const unsigned char *plan) {
+    cudaError_t e = launch_direct_shrink(x, ldx, y, ldy, sh, table, sorted_ids, seg, active, ws, T, err, fp8,
+                                         stream, x_div, plan);
     if (e != cudaSuccess) return e;
-    return launch_direct_expand(x, ldx, y, ldy, sh, table, sorted_ids, seg, active, ws, T, err, fp8, true, stream);
+    return launch_direct_expand(x, ldx, y, ldy, sh, table, sorted_ids, seg, active, ws, T, err, fp8, true, stream,
+                                plan);
 }
 
 }  // namespace lora

@@ -39,15 +39,19 @@ bool decode_direct_supported(int32_t T, const Shape &sh, bool fp8);
 cudaError_t launch_direct_shrink(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                  const void *table, const int32_t *sorted_ids, const int32_t *seg,
                                  const int32_t *active, float *ws, int32_t T, int32_t *err, bool fp8,
-                                 cudaStream_t stream, int32_t x_div = 1);
+                                 cudaStream_t stream, int32_t x_div = 1, const unsigned char *plan = nullptr);
 cudaError_t launch_direct_expand(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                  const void *table, const int32_t *sorted_ids, const int32_t *seg,
                                  const int32_t *active, float *ws, int32_t T, int32_t *err, bool fp8,
-                                 bool programmatic, cudaStream_t stream);
+                                 bool programmatic, cudaStream_t stream, const unsigned char *plan = nullptr);
 cudaError_t launch_decode_direct(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                  const void *table, const int32_t *sorted_ids, const int32_t *seg,
                                  const int32_t *active, float *ws, int32_t T, int32_t *err, bool fp8,
-                                 cudaStream_t stream, int32_t x_div = 1);
+                                 cudaStream_t stream, int32_t x_div = 1, const unsigned char *plan = nullptr);
+size_t direct_plan_bytes(int32_t T, const Shape &sh);
+cudaError_t launch_direct_plans(const Shape &sh, const void *const *tables, unsigned char *const *plans,
+                                int32_t count, const int32_t *sorted_ids, const int32_t *seg, const int32_t *active,
+                                int32_t T, bool fp8, int32_t *err, cudaStream_t stream);
 cudaError_t launch_prefill(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                            const void *table, const int32_t *sorted_ids, const int32_t *seg, float *ws,
                            int32_t T, int32_t *err, cudaStream_t stream);
@@ -480,6 +484,65 @@ lora_status_t lora_apply_moe(const void *x, int64_t ldx, int32_t x_per_token, vo
     return from_cuda(lora::launch_decode_direct(static_cast<const uint16_t *>(x), ldx, static_cast<uint16_t *>(y), ldy,
                                                 sh, dev_table, sorted_ids, seg_offsets, active, ws, P, err, false,
                                                 reinterpret_cast<cudaStream_t>(stream), x_per_token ? K : 1));
+}
+
+size_t lora_plan_bytes(int32_t T, const lora_shape_t *shape) {
+    Shape sh;
+    if (T < 1 || check_shape(shape, &sh) != LORA_OK) return 0;
+    return lora::direct_plan_bytes(T, sh);
+}
+
+lora_status_t lora_build_plans(int32_t T, const lora_shape_t *shape, int32_t count, const void *const *dev_tables,
+                               void *const *plans, size_t plan_bytes, const int32_t *sorted_ids,
+                               const int32_t *seg_offsets, const int32_t *active, lora_path_t path, int32_t *err,
+                               lora_stream_t stream) {
+    Shape sh;
+    lora_status_t st;
+    if (T < 1 || count < 0 || (count > 0 && (dev_tables == nullptr || plans == nullptr))) return LORA_ERR_INVALID_ARG;
+    if ((st = check_shape(shape, &sh)) != LORA_OK) return st;
+    if (path != LORA_PATH_DECODE_DIRECT && path != LORA_PATH_DECODE_DIRECT_FP8) return LORA_ERR_UNSUPPORTED;
+    const bool fp8 = path == LORA_PATH_DECODE_DIRECT_FP8;
+    if (!lora::decode_direct_supported(T, sh, fp8)) return LORA_ERR_UNSUPPORTED;
+    if (plan_bytes < lora::direct_plan_bytes(T, sh)) return LORA_ERR_WORKSPACE;
+    for (int32_t j = 0; j < count; ++j) {
+        if ((st = check_index_ptrs(dev_tables[j], sorted_ids, seg_offsets, active, T)) != LORA_OK) return st;
+        if (plans[j] == nullptr) return LORA_ERR_WORKSPACE;
+        if (!aligned16(plans[j])) return LORA_ERR_ALIGNMENT;
+    }
+    if (count == 0) return LORA_OK;
+    return from_cuda(lora::launch_direct_plans(sh, dev_tables, reinterpret_cast<unsigned char *const *>(plans), count,
+                                               sorted_ids, seg_offsets, active, T, fp8, err,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_build_plan(int32_t T, const lora_shape_t *shape, const void *dev_table, const int32_t *sorted_ids,
+                              const int32_t *seg_offsets, const int32_t *active, lora_path_t path, void *plan,
+                              size_t plan_bytes, int32_t *err, lora_stream_t stream) {
+    if (plan == nullptr) return LORA_ERR_WORKSPACE;
+    return lora_build_plans(T, shape, 1, &dev_table, &plan, plan_bytes, sorted_ids, seg_offsets, active, path, err,
+                            stream);
+}
+
+lora_status_t lora_apply_plan(const void *x, int64_t ldx, void *y, int64_t ldy, int32_t T, const lora_shape_t *shape,
+                              const void *plan, size_t plan_bytes, lora_path_t path, float *ws, size_t ws_bytes,
+                              int32_t *err, lora_stream_t stream) {
+    Shape sh;
+    lora_status_t st;
+    if (T < 0) return LORA_ERR_INVALID_ARG;
+    if ((st = check_shape(shape, &sh)) != LORA_OK) return st;
+    if ((st = check_rows(x, ldx, T, sh.k)) != LORA_OK) return st;
+    if ((st = check_rows(y, ldy, T, sh.off[sh.n])) != LORA_OK) return st;
+    if ((st = check_ws(ws, ws_bytes, T, sh)) != LORA_OK) return st;
+    if (T == 0) return LORA_OK;
+    if (path != LORA_PATH_DECODE_DIRECT && path != LORA_PATH_DECODE_DIRECT_FP8) return LORA_ERR_UNSUPPORTED;
+    const bool fp8 = path == LORA_PATH_DECODE_DIRECT_FP8;
+    if (!lora::decode_direct_supported(T, sh, fp8)) return LORA_ERR_UNSUPPORTED;
+    if (plan == nullptr || plan_bytes < lora::direct_plan_bytes(T, sh)) return LORA_ERR_WORKSPACE;
+    if (!aligned16(plan)) return LORA_ERR_ALIGNMENT;
+    return from_cuda(lora::launch_decode_direct(static_cast<const uint16_t *>(x), ldx, static_cast<uint16_t *>(y), ldy,
+                                                sh, nullptr, nullptr, nullptr, nullptr, ws, T, err, fp8,
+                                                reinterpret_cast<cudaStream_t>(stream), 1,
+                                                static_cast<const unsigned char *>(plan)));
 }
 
 lora_status_t lora_apply(const void *x, int64_t ldx, void *y, int64_t ldy, int32_t T, const lora_shape_t *shape,

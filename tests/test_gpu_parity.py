@@ -977,3 +977,113 @@ def test_object_level_apply():
     assert int(idx.err.item()) == 0
     ref, _ = oracle_y(wl)
     assert_y_close(to_host_bits(rp.y), ref, "object-level apply")
+
+
+# ---------------------------------------------------------------------------
+# Plans: the warp-streaming kernels' tables built once per batch and shape
+# ---------------------------------------------------------------------------
+def _plan_apply(wl, path="decode_direct", repeat=1, mod_idx=0):
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import ResidentProjection, to_host_bits
+    rp = ResidentProjection.from_workload(wl, mod_idx)
+    idx = L.TokenIndex(wl.T, wl.S)
+    idx.build(torch.from_numpy(np.ascontiguousarray(wl.slot_ids, dtype=np.int32)).cuda(), rp.table)
+    ws = L.Workspace(wl.T, rp.shape)
+    plan = L.Plan(wl.T, rp.shape, path)
+    plan.build(idx, rp.table)
+    y0 = rp.y.clone()
+    outs = []
+    for _ in range(repeat):
+        rp.y.copy_(y0)
+        plan.apply(rp.x, rp.y, ws, idx.err)
+        torch.cuda.synchronize()
+        outs.append(to_host_bits(rp.y))
+    return outs, int(idx.err.item()), (rp, idx, ws, plan)
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 4, 5])
+def test_apply_plan_configs(cfg):
+    """Every call of a plan against the oracle, three calls in a row on one workspace."""
+    wl = W.config(cfg)
+    outs, err, _ = _plan_apply(wl, repeat=3)
+    assert err == 0
+    rows = None if wl.T <= 512 else np.arange(0, wl.T, 3, dtype=np.int32)
+    ref, st = oracle_y(wl, rows=rows)
+    assert st == 0
+    for y in outs:
+        assert_y_close(y if rows is None else y[rows], ref, f"plan config {cfg}")
+
+
+@pytest.mark.parametrize("case", [c for c in RAGGED if max(c[5]) <= 64], ids=lambda c: f"plan_ragged{c[0]}")
+def test_apply_plan_ragged(case):
+    seed, T, k, widths, S, ranks = case
+    wl = _small(seed, T, k, widths, S, ranks)
+    outs, err, _ = _plan_apply(wl)
+    assert err == 0
+    ref, _ = oracle_y(wl)
+    assert_y_close(outs[0], ref, f"plan ragged {seed}")
+    keep = untouched_rows(wl)
+    np.testing.assert_array_equal(outs[0][keep], wl.modules[0].y_in[keep])
+
+
+def test_apply_plan_fp8():
+    from _parity import oracle_y_e4m3
+    wl = W.config(6)
+    outs, err, _ = _plan_apply(wl, path="decode_direct_fp8", repeat=2)
+    assert err == 0
+    ref, st = oracle_y_e4m3(wl)
+    assert st == 0
+    for y in outs:
+        assert_y_close(y, ref, "plan fp8")
+
+
+def test_plan_for_another_batch_or_variant_does_nothing_and_reports():
+    """A plan used with fewer tokens than it was built for, or for the other
+    variant, leaves y unchanged and writes LORA_ERR_INVALID_ARG."""
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import to_host_bits
+    wl = W.config(2)
+    _, err, (rp, idx, ws, plan) = _plan_apply(wl)
+    assert err == 0
+    x, y = rp.x[:128], rp.y[:128]
+    before = to_host_bits(y).copy()
+    idx.err.zero_()
+    L.lora_apply_plan(x, y, rp.shape, plan.buf, ws.buf, idx.err, path="decode_direct")
+    torch.cuda.synchronize()
+    assert int(idx.err.item()) == 1
+    np.testing.assert_array_equal(to_host_bits(y), before)
+    before = to_host_bits(rp.y).copy()
+    idx.err.zero_()
+    L.lora_apply_plan(rp.x, rp.y, rp.shape, plan.buf, ws.buf, idx.err, path="decode_direct_fp8")
+    torch.cuda.synchronize()
+    assert int(idx.err.item()) == 1
+    np.testing.assert_array_equal(to_host_bits(rp.y), before)
+
+
+def test_plans_of_several_layers_in_one_launch():
+    """lora_build_plans for three layers with their own weights (one index): each
+    layer's call through its plan matches the oracle on its own weights."""
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import ResidentProjection, to_host_bits
+    wls = [W.config(2), W.config(2), W.config(2)]
+    rng = np.random.default_rng(5)
+    for wl in wls[1:]:  # same slots and ranks, other weights
+        m = wl.modules[0]
+        m.A = [[(W._normal_bf16(rng, a.shape, a.shape[1] ** -0.5) if a is not None else None) for a in row]
+               for row in m.A]
+        m.B = [[(W._normal_bf16(rng, b.shape, 0.02) if b is not None else None) for b in row] for row in m.B]
+    rps = [ResidentProjection.from_workload(wl) for wl in wls]
+    idx = L.TokenIndex(wls[0].T, wls[0].S)
+    idx.build(torch.from_numpy(wls[0].slot_ids).cuda(), rps[0].table)
+    plans = [L.Plan(wls[0].T, rp.shape) for rp in rps]
+    L.lora_build_plans(plans, [rp.table for rp in rps], idx)
+    ws = L.Workspace(wls[0].T, rps[0].shape)
+    for wl, rp, plan in zip(wls, rps, plans):
+        plan.apply(rp.x, rp.y, ws, idx.err)
+        torch.cuda.synchronize()
+        assert int(idx.err.item()) == 0
+        ref, _ = oracle_y(wl)
+        assert_y_close(to_host_bits(rp.y), ref, "batched plans")
