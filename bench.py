@@ -582,14 +582,19 @@ def run_moe(args):
     slot_dev = torch.from_numpy(wl.slot_ids).to(dev)
     expert_dev = torch.from_numpy(wl.expert_ids.reshape(-1).copy()).to(dev)
     ws = [L.Workspace(P, b.shape, device=dev) for b in base]
+    plans = [] if args.no_plan else [L.Plan(P, lay.shape, device=dev) for lay in layers]
 
     def index_part():
         index.build_moe(slot_dev, expert_dev, wl.K, wl.E, layers[0].table)
+        if plans:  # one launch per module shape
+            for m in mods:
+                L.lora_build_plans(plans[m::len(mods)], [lay.table for lay in layers[m::len(mods)]], index)
 
     def apply_part():
         for l, lay in enumerate(layers):
             L.lora_apply_moe(lay.x, lay.y, wl.K, lay.shape, lay.table.dev, index.sorted_ids, index.seg_offsets,
-                             index.active, ws[l % len(ws)].buf, index.err, x_per_token=lay.x_per_token)
+                             index.active, ws[l % len(ws)].buf, index.err, x_per_token=lay.x_per_token,
+                             plan=plans[l] if plans else None)
 
     elapsed_s, apply_ms_mean, index_ms_mean, clocks, (peak_gbs, peak_tf, peak_src) = \
         time_steps(args, dev, local, index_part, apply_part)
@@ -621,7 +626,8 @@ def run_moe(args):
             "config": args.config,
             "layers_per_step": len(layers),
             "calls_per_step": len(layers),
-            "path": "lora_apply_moe (warp-streaming decode kernels over n_adapters * E virtual slots)",
+            "path": "lora_apply_moe (warp-streaming decode kernels over n_adapters * E virtual slots)"
+                    + (" with per-step plans" if plans else ""),
             "l2": f"inputs larger than L2: {len(layers)} distinct layer buffer sets, "
                   f"{sum(per_layer_bytes) / 1e9:.2f} GB of algorithmic bytes per step",
             "parallelism": f"replicas x{world}",
@@ -640,7 +646,7 @@ def run_moe(args):
             "us_per_call": call_s * 1e6,
             "index_and_table_us": index_ms_mean * 1e3,
         },
-        "gpu_launches": args.steps * (1 + 2 * len(layers)),
+        "gpu_launches": args.steps * (1 + 2 * len(layers) + (len(mods) if plans else 0)),
         "clocks": clocks,
         "device_error": err,
     }

@@ -515,6 +515,16 @@ lora_status_t lora_apply_moe(const void *x, int64_t ldx, int32_t x_per_token, vo
                              const int32_t *seg_offsets, const int32_t *active, float *ws, size_t ws_bytes,
                              int32_t *err, lora_stream_t stream);
 
+/*
+ * lora_apply_moe with a plan instead of the virtual table and the pair index: the
+ * plan built by lora_build_plan(s) for T * K rows, the virtual table and the
+ * pair index (path LORA_PATH_DECODE_DIRECT).  Checks and errors as
+ * lora_apply_moe and lora_apply_plan.
+ */
+lora_status_t lora_apply_moe_plan(const void *x, int64_t ldx, int32_t x_per_token, void *y, int64_t ldy, int32_t T,
+                                  int32_t K, const lora_shape_t *shape, const void *plan, size_t plan_bytes, float *ws,
+                                  size_t ws_bytes, int32_t *err, lora_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -317,9 +317,11 @@ def lora_build_index_moe(slot_ids, expert_ids, K, E, S, dev_table, sorted_ids, s
 
 
 def lora_apply_moe(x, y, K, shape, dev_table, sorted_ids, seg_offsets, active, ws, err, x_per_token: bool = True,
-                   stream=None) -> None:
+                   stream=None, plan=None) -> None:
     """Routed-expert branch: y [T*K, d] per (token, choice) pair; x [T, k] shared
-    by a token's experts (x_per_token) or [T*K, k] per pair."""
+    by a token's experts (x_per_token) or [T*K, k] per pair.  With `plan` (a Plan
+    built for T*K rows on the virtual table and the pair index) the table and
+    index arguments are not used."""
     ldx = _rows(x, "x")
     ldy = _rows(y, "y")
     P = int(y.shape[0])
@@ -328,6 +330,11 @@ def lora_apply_moe(x, y, K, shape, dev_table, sorted_ids, seg_offsets, active, w
     T = P // int(K)
     if int(x.shape[0]) != (T if x_per_token else P):
         raise ValueError("x must have T rows (x_per_token) or T * K rows")
+    if plan is not None:
+        check(load().lora_apply_moe_plan(_p(x), ldx, int(bool(x_per_token)), _p(y), ldy, T, int(K), ctypes.byref(shape),
+                                         _p(plan.buf), plan.buf.numel(), _p(ws), ws.numel() * ws.element_size(), _p(err),
+                                         _stream(stream)), "lora_apply_moe_plan")
+        return
     check(load().lora_apply_moe(_p(x), ldx, int(bool(x_per_token)), _p(y), ldy, T, int(K), ctypes.byref(shape),
                                 _p(dev_table), _p(sorted_ids), _p(seg_offsets), _p(active), _p(ws),
                                 ws.numel() * ws.element_size(), _p(err), _stream(stream)), "lora_apply_moe")

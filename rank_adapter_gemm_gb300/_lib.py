@@ -43,7 +43,7 @@ EXPORTED = (
     "lora_resolve_path", "lora_apply_noalloc", "lora_workspace_xa_offset", "lora_build_index_seq",
     "lora_apply_overlap", "lora_premultiply_e4m3", "lora_moe_slot_pointers", "lora_build_index_moe",
     "lora_apply_moe", "lora_build_index_activated", "lora_plan_bytes", "lora_build_plan", "lora_apply_plan",
-    "lora_build_plans",
+    "lora_build_plans", "lora_apply_moe_plan",
 )
 
 
@@ -112,6 +112,7 @@ def load() -> ctypes.CDLL:
         "lora_build_plan": (ST, [I32, SH, P, P, P, P, ST, P, SZ, P, P]),
         "lora_apply_plan": (ST, [P, I64, P, I64, I32, SH, P, SZ, ST, P, SZ, P, P]),
         "lora_build_plans": (ST, [I32, SH, I32, P, P, SZ, P, P, P, ST, P, P]),
+        "lora_apply_moe_plan": (ST, [P, I64, I32, P, I64, I32, I32, SH, P, SZ, P, SZ, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

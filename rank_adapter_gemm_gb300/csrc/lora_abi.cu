@@ -545,6 +545,27 @@ lora_status_t lora_apply_plan(const void *x, int64_t ldx, void *y, int64_t ldy, 
                                                 static_cast<const unsigned char *>(plan)));
 }
 
+lora_status_t lora_apply_moe_plan(const void *x, int64_t ldx, int32_t x_per_token, void *y, int64_t ldy, int32_t T,
+                                  int32_t K, const lora_shape_t *shape, const void *plan, size_t plan_bytes, float *ws,
+                                  size_t ws_bytes, int32_t *err, lora_stream_t stream) {
+    Shape sh;
+    lora_status_t st;
+    if (T < 0 || K < 1 || static_cast<int64_t>(T) * K > INT32_MAX) return LORA_ERR_INVALID_ARG;
+    const int32_t P = T * K;
+    if ((st = check_shape(shape, &sh)) != LORA_OK) return st;
+    if ((st = check_rows(x, ldx, x_per_token ? T : P, sh.k)) != LORA_OK) return st;
+    if ((st = check_rows(y, ldy, P, sh.off[sh.n])) != LORA_OK) return st;
+    if ((st = check_ws(ws, ws_bytes, P, sh)) != LORA_OK) return st;
+    if (P == 0) return LORA_OK;
+    if (!lora::decode_direct_supported(P, sh, false)) return LORA_ERR_UNSUPPORTED;
+    if (plan == nullptr || plan_bytes < lora::direct_plan_bytes(P, sh)) return LORA_ERR_WORKSPACE;
+    if (!aligned16(plan)) return LORA_ERR_ALIGNMENT;
+    return from_cuda(lora::launch_decode_direct(static_cast<const uint16_t *>(x), ldx, static_cast<uint16_t *>(y), ldy,
+                                                sh, nullptr, nullptr, nullptr, nullptr, ws, P, err, false,
+                                                reinterpret_cast<cudaStream_t>(stream), x_per_token ? K : 1,
+                                                static_cast<const unsigned char *>(plan)));
+}
+
 lora_status_t lora_apply(const void *x, int64_t ldx, void *y, int64_t ldy, int32_t T, const lora_shape_t *shape,
                          const void *dev_table, const int32_t *sorted_ids, const int32_t *seg_offsets,
                          const int32_t *active, int32_t max_seg_hint, float *ws, size_t ws_bytes, int32_t *err,

@@ -1087,3 +1087,34 @@ def test_plans_of_several_layers_in_one_launch():
         assert int(idx.err.item()) == 0
         ref, _ = oracle_y(wl)
         assert_y_close(to_host_bits(rp.y), ref, "batched plans")
+
+
+@pytest.mark.parametrize("mod_idx", [0, 1], ids=["w1_x_per_token", "w2_x_per_pair"])
+def test_apply_moe_with_plan(mod_idx):
+    """The routed-expert branch through a plan built on the virtual table and the
+    pair index (T*K rows)."""
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import ResidentMoeProjection, to_host_bits
+    wl = W.moe_config()
+    rp = ResidentMoeProjection(wl, mod_idx)
+    P = wl.T * wl.K
+    idx = L.TokenIndex(P, wl.n_adapters * wl.E)
+    idx.build_moe(torch.from_numpy(wl.slot_ids).cuda(), torch.from_numpy(wl.expert_ids.reshape(-1).copy()).cuda(),
+                  wl.K, wl.E, rp.table)
+    plan = L.Plan(P, rp.shape)
+    plan.build(idx, rp.table)
+    ws = L.Workspace(P, rp.shape)
+    for _ in range(2):
+        L.lora_apply_moe(rp.x, rp.y, wl.K, rp.shape, None, None, None, None, ws.buf, idx.err,
+                         x_per_token=rp.x_per_token, plan=plan)
+    torch.cuda.synchronize()
+    assert int(idx.err.item()) == 0
+    m = wl.modules[mod_idx]
+    scales = oracle.slot_scales(wl.ranks, wl.alphas, wl.scale_rule, False)
+    # two calls: y_in + 2 * branch
+    once, st = oracle.apply_moe(m.x, m.x_per_token, m.y_in, m.slice_widths, wl.slot_ids, wl.expert_ids, wl.E,
+                                wl.ranks, scales, m.A, m.B)
+    assert st == 0
+    ref = 2 * once - W.bf16_bits_to_f32(m.y_in).astype(np.float64)
+    assert_y_close(to_host_bits(rp.y), ref, f"moe plan {mod_idx}")
