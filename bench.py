@@ -487,34 +487,78 @@ def run_ours(args):
 
 
 def run_e2e(args, wl, layers, index, slot_dev, ws_of, max_seg, dev, world, plans=(), mods=(0,), ws=()):
-    """Same metric with host buffers: every step copies slot ids and each layer's
-    x and y from pinned host memory, runs the step, and reads every y back."""
+    """Same metric with host buffers: every step copies the slot ids and every
+    layer's x and y from pinned host memory, runs the step, and reads every y
+    back.  The layers of one shape keep their rows in one device buffer (a view
+    per layer); a step moves them in four chunks of layers per shape and
+    direction, the inputs of a chunk on one copy stream and its results on
+    another while the next chunk computes (events order them inside the graph)."""
     import torch
     import rank_adapter_gemm_gb300 as L
     T = wl.T
     h_slots = torch.from_numpy(_index_ids(wl)).pin_memory()
-    h_x = [lay.x.cpu().pin_memory() for lay in layers]
-    h_y = [lay.y.cpu().pin_memory() for lay in layers]
-    h_out = [torch.empty_like(h).pin_memory() for h in h_y]
+    groups = [list(range(m, len(layers), len(mods))) for m in mods]
+    d_x = [torch.stack([layers[l].x for l in g]) for g in groups]      # [layers of the shape, T, k]
+    d_y = [torch.stack([layers[l].y for l in g]) for g in groups]
+    h_x = [t.cpu().pin_memory() for t in d_x]
+    h_y = [t.cpu().pin_memory() for t in d_y]
+    h_out = [torch.empty_like(t).pin_memory() for t in h_y]
+    xv, yv = {}, {}
+    for gi, g in enumerate(groups):
+        for j, l in enumerate(g):
+            xv[l], yv[l] = d_x[gi][j], d_y[gi][j]
     stream = torch.cuda.Stream(device=dev)
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    n_chunks = 4  # inputs of chunk c+1 and results of chunk c-1 move while chunk c computes
+    parts = [[np.array_split(np.arange(len(g)), n_chunks)[c] for g in groups] for c in range(n_chunks)]
+
+    def rows(t, j):
+        return t[int(j[0]):int(j[-1]) + 1]
 
     def step():
-        slot_dev.copy_(h_slots, non_blocking=True)
-        for lay, hx, hy in zip(layers, h_x, h_y):
-            lay.x.copy_(hx, non_blocking=True)
-            lay.y.copy_(hy, non_blocking=True)
+        cur = torch.cuda.current_stream()
+        s_in.wait_stream(cur)
+        s_out.wait_stream(cur)
+        ev_in = []
+        with torch.cuda.stream(s_in):
+            slot_dev.copy_(h_slots, non_blocking=True)
+            ev_slots = torch.cuda.Event()
+            ev_slots.record(s_in)
+            for c in range(n_chunks):
+                for gi in range(len(groups)):
+                    j = parts[c][gi]
+                    if len(j):
+                        rows(d_x[gi], j).copy_(rows(h_x[gi], j), non_blocking=True)
+                        rows(d_y[gi], j).copy_(rows(h_y[gi], j), non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(s_in)
+                ev_in.append(ev)
+        cur.wait_event(ev_slots)
         _build_index(index, slot_dev, layers[0].table, wl.tokens_per_seq)
         if plans:
             for m in mods:
                 L.lora_build_plans(plans[m::len(mods)], [lay.table for lay in layers[m::len(mods)]], index)
-        for l, lay in enumerate(layers):
-            if plans:
-                plans[l].apply(lay.x, lay.y, ws[l % len(ws)], index.err)
-            else:
-                L.lora_apply(lay.x, lay.y, lay.shape, lay.table.dev, index.sorted_ids, index.seg_offsets,
-                             index.active, ws_of[l], index.err, max_seg_hint=max_seg, path=args.path)
-        for lay, ho in zip(layers, h_out):
-            ho.copy_(lay.y, non_blocking=True)
+        for c in range(n_chunks):
+            cur.wait_event(ev_in[c])
+            for gi, g in enumerate(groups):
+                for jj in parts[c][gi]:
+                    l = g[int(jj)]
+                    lay = layers[l]
+                    if plans:
+                        plans[l].apply(xv[l], yv[l], ws[l % len(ws)], index.err)
+                    else:
+                        L.lora_apply(xv[l], yv[l], lay.shape, lay.table.dev, index.sorted_ids, index.seg_offsets,
+                                     index.active, ws_of[l], index.err, max_seg_hint=max_seg, path=args.path)
+            ev = torch.cuda.Event()
+            ev.record(cur)
+            s_out.wait_event(ev)
+            with torch.cuda.stream(s_out):
+                for gi in range(len(groups)):
+                    j = parts[c][gi]
+                    if len(j):
+                        rows(h_out[gi], j).copy_(rows(d_y[gi], j), non_blocking=True)
+        cur.wait_stream(s_in)
+        cur.wait_stream(s_out)
 
     with torch.cuda.stream(stream):
         step()
