@@ -59,6 +59,8 @@ def parse_args(argv=None):
                    help="auto takes decode_direct_fp8 for a workload with FP8 adapters")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-chunks", type=int, default=8,
+                   help="e2e: chunks of layers whose copies overlap the compute of the previous chunk")
     p.add_argument("--no-plan", action="store_true",
                    help="warp-streaming paths: rebuild the tables in every call instead of per-step plans")
     p.add_argument("--with-base", default="none", choices=["none", "serial", "overlap"],
@@ -490,7 +492,7 @@ def run_e2e(args, wl, layers, index, slot_dev, ws_of, max_seg, dev, world, plans
     """Same metric with host buffers: every step copies the slot ids and every
     layer's x and y from pinned host memory, runs the step, and reads every y
     back.  The layers of one shape keep their rows in one device buffer (a view
-    per layer); a step moves them in four chunks of layers per shape and
+    per layer); a step moves them in chunks of layers (--e2e-chunks) per shape and
     direction, the inputs of a chunk on one copy stream and its results on
     another while the next chunk computes (events order them inside the graph)."""
     import torch
@@ -509,7 +511,7 @@ def run_e2e(args, wl, layers, index, slot_dev, ws_of, max_seg, dev, world, plans
             xv[l], yv[l] = d_x[gi][j], d_y[gi][j]
     stream = torch.cuda.Stream(device=dev)
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    n_chunks = 4  # inputs of chunk c+1 and results of chunk c-1 move while chunk c computes
+    n_chunks = max(1, min(args.e2e_chunks, min(len(g) for g in groups)))  # copies of c+1 / c-1 overlap chunk c
     parts = [[np.array_split(np.arange(len(g)), n_chunks)[c] for g in groups] for c in range(n_chunks)]
 
     def rows(t, j):
