@@ -411,7 +411,9 @@ lora_status_t lora_build_index_activated(const int32_t *seq_ids, const int32_t *
  * of every call (the active slots, their token ranges and ranks, the split of
  * the work over the warps), built once per batch and shape and then read by
  * every call of that shape (one table image per kernel, loaded with one pass of
- * 16-byte copies).  Rebuild it whenever the index or the slot table changes.
+ * 16-byte copies).  A plan holds the slot table's ranks, scales and weight
+ * pointers: build one per slot table (per layer), and rebuild it whenever the
+ * index or that table changes.
  *
  * lora_plan_bytes: the plan's size for T tokens and this shape (0 for T < 1 or
  * a bad shape).
@@ -424,9 +426,10 @@ lora_status_t lora_build_index_activated(const int32_t *seq_ids, const int32_t *
  * data errors of the index are reported here, as lora_apply would.
  *
  * lora_apply_plan: lora_apply_ex on that path with the plan instead of the table
- * and the index.  A plan built for another T, shape, slot count or path is
- * reported as LORA_ERR_INVALID_ARG in err and the call leaves y unchanged.
- * Other arguments, checks and errors as lora_apply_ex.
+ * and the index.  A plan built for another T, slot count, slice count or path is
+ * reported as LORA_ERR_INVALID_ARG in err and the call leaves y unchanged; the
+ * plan must also have been built with this shape's k and slice widths (not
+ * checked on the device).  Other arguments, checks and errors as lora_apply_ex.
  */
 size_t lora_plan_bytes(int32_t T, const lora_shape_t *shape);
 lora_status_t lora_build_plan(int32_t T, const lora_shape_t *shape, const void *dev_table, const int32_t *sorted_ids,
