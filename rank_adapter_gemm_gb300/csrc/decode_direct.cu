@@ -246,7 +246,8 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
 // Tables: one copy per CTA in shared memory, built by the prologue.
 // ---------------------------------------------------------------------------
 struct Tabs {
-    int32_t *misc;     // [0] active count NA, [1] call counter, [3..5] table header
+    int32_t *misc;     // [0] active count NA, [1] call counter, [3..5] table header; plans: [2] T,
+                       // [6] variant, [18] k, [19] r_max (misc[18], misc[19] follow scb)
     int32_t *soff;     // [LORA_MAX_SLICES + 1] slice offsets
     int32_t *scb;      // [LORA_MAX_SLICES + 1] exclusive prefix of 64-column blocks per slice
     int32_t *tok;      // [T] sorted token ids (-1 where invalid)
@@ -449,8 +450,13 @@ __device__ void load_plan(const DArgs &a, const Shape &sh, const Tabs &t, size_t
     __syncthreads();
     if (tid == 0) {
         t.misc[1] = *reinterpret_cast<volatile const int32_t *>(a.gen);
-        if (t.misc[2] != a.T || t.misc[3] != kTableMagic || t.misc[4] != sh.S || t.misc[5] != sh.n ||
-            t.misc[6] != (kF8 ? 1 : 0)) {
+        // everything that sets an address must match: batch, counts, variant, k, r_max, slice offsets
+        bool ok = t.misc[2] == a.T && t.misc[3] == kTableMagic && t.misc[4] == sh.S && t.misc[5] == sh.n &&
+                  t.misc[6] == (kF8 ? 1 : 0) && t.misc[18] == sh.k && t.misc[19] == sh.r_max;
+#pragma unroll
+        for (int i = 0; i <= LORA_MAX_SLICES; ++i)
+            if (i <= sh.n && t.soff[i] != sh.off[i]) ok = false;  // compile-time index into the shape
+        if (!ok) {
             if (blockIdx.x == 0) report_error(a.err, LORA_ERR_INVALID_ARG);
             t.misc[0] = 0;
             t.a_pre[0] = 0;
@@ -1102,8 +1108,9 @@ __global__ void __launch_bounds__(32 * kEWarps, kECtas) direct_expand_kernel(DAr
 
 // A plan: the tables both kernels of a call would build in their prologue,
 // built once for a batch (index) and shape by the same build_tabs and stored as
-// two images, the shrink's then the expand's.  misc[2] records T and misc[6]
-// the variant, which load_plan checks.  One launch builds the plans of up to
+// two images, the shrink's then the expand's.  misc[2] records T, misc[6] the
+// variant, misc[18] k and misc[19] r_max, which load_plan checks with the rest
+// of the shape.  One launch builds the plans of up to
 // kMaxPlanJobs slot tables of the same shape and batch (the layers of a step):
 // block 2j + 0 / 2j + 1 writes the shrink / expand image of job j.
 constexpr int kMaxPlanJobs = 120;
@@ -1124,6 +1131,8 @@ __global__ void __launch_bounds__(256) direct_plan_kernel(DArgs a, Shape sh, Pla
     if (threadIdx.x == 0) {
         t.misc[2] = a.T;
         t.misc[6] = kF8 ? 1 : 0;
+        t.misc[18] = sh.k;
+        t.misc[19] = sh.r_max;
     }
     __syncthreads();
     const size_t bytes = tabs_bytes(sh.S, sh.n, a.T);

@@ -1118,3 +1118,22 @@ def test_apply_moe_with_plan(mod_idx):
     assert st == 0
     ref = 2 * once - W.bf16_bits_to_f32(m.y_in).astype(np.float64)
     assert_y_close(to_host_bits(rp.y), ref, f"moe plan {mod_idx}")
+
+
+def test_plan_for_other_slice_widths_does_nothing_and_reports():
+    """A plan used with a shape of other slice widths (its offsets would place y
+    writes elsewhere) is refused on the device: y unchanged, LORA_ERR_INVALID_ARG."""
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import to_host_bits
+    wl = W.config(2)
+    _, err, (rp, idx, ws, plan) = _plan_apply(wl)
+    assert err == 0
+    other = L.make_shape(wl.S, wl.r_max, 4096, [4096, 1024, 512])
+    y = rp.y[:, :5632]
+    before = to_host_bits(rp.y).copy()
+    idx.err.zero_()
+    L.lora_apply_plan(rp.x, y, other, plan.buf, ws.buf, idx.err, path="decode_direct")
+    torch.cuda.synchronize()
+    assert int(idx.err.item()) == 1
+    np.testing.assert_array_equal(to_host_bits(rp.y), before)
