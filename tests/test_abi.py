@@ -135,3 +135,49 @@ def test_rank_limit_is_512(L):
     with pytest.raises(L.LoraError) as e:
         L.lora_workspace_bytes(64, L.make_shape(4, 520, 1024, [1024]))
     assert e.value.status == 3
+
+
+def test_host_checks_of_the_plan_moe_and_activated_entry_points(L):
+    """Argument errors are returned before anything is enqueued (no device is
+    touched): null pointers, counts, unsupported paths, short buffers."""
+    import ctypes
+    from rank_adapter_gemm_gb300 import _lib
+    lib = _lib.load()
+    sh = L.make_shape(32, 64, 4096, [4096, 1024, 1024])
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # never dereferenced: every call below fails its host checks first
+    paths = _lib.PATHS
+    # plan size: 0 for T < 1, two table images otherwise, growing with T
+    assert lib.lora_plan_bytes(0, ctypes.byref(sh)) == 0
+    b256, b512 = lib.lora_plan_bytes(256, ctypes.byref(sh)), lib.lora_plan_bytes(512, ctypes.byref(sh))
+    assert 0 < b256 < b512 and b256 % 32 == 0
+    # build: T < 1, unsupported path, short or null plan, misaligned plan
+    assert lib.lora_build_plan(0, ctypes.byref(sh), fake, fake, fake, fake, paths["decode_direct"], fake, b256,
+                               None, None) == 1
+    assert lib.lora_build_plan(256, ctypes.byref(sh), fake, fake, fake, fake, paths["decode_split"], fake, b256,
+                               None, None) == 9
+    assert lib.lora_build_plan(256, ctypes.byref(sh), fake, fake, fake, fake, paths["decode_direct"], fake, b256 - 16,
+                               None, None) == 6
+    assert lib.lora_build_plan(256, ctypes.byref(sh), fake, fake, fake, fake, paths["decode_direct"], None, b256,
+                               None, None) == 6
+    assert lib.lora_build_plan(256, ctypes.byref(sh), fake, fake, fake, fake, paths["decode_direct"],
+                               P((1 << 20) + 8), b256, None, None) == 2
+    # FP8 plans need k % 16 == 0
+    sh8 = L.make_shape(32, 64, 4104, [4096])
+    assert lib.lora_build_plan(256, ctypes.byref(sh8), fake, fake, fake, fake, paths["decode_direct_fp8"], fake,
+                               lib.lora_plan_bytes(256, ctypes.byref(sh8)), None, None) == 9
+    # batched build: negative count, null arrays
+    assert lib.lora_build_plans(256, ctypes.byref(sh), -1, None, None, b256, fake, fake, fake,
+                                paths["decode_direct"], None, None) == 1
+    assert lib.lora_build_plans(256, ctypes.byref(sh), 2, None, None, b256, fake, fake, fake,
+                                paths["decode_direct"], None, None) == 1
+    # MoE index: S not a multiple of E, T * K overflow
+    assert lib.lora_build_index_moe(fake, fake, 10, 2, 3, 8, fake, fake, fake, fake, None, None) == 1
+    assert lib.lora_build_index_moe(fake, fake, 1 << 30, 4, 2, 8, fake, fake, fake, fake, None, None) == 1
+    # aLoRA index: negative counts, missing sequence arrays
+    assert lib.lora_build_index_activated(fake, fake, -1, fake, fake, 2, 8, fake, fake, fake, fake, None, None) == 1
+    assert lib.lora_build_index_activated(fake, fake, 4, None, None, 2, 8, fake, fake, fake, fake, None, None) == 1
+    # MoE apply: K < 1; premultiply_e4m3: negative count
+    assert lib.lora_apply_moe(fake, 4096, 1, fake, 6144, 4, 0, ctypes.byref(sh), fake, fake, fake, fake, fake, 0,
+                              None, None) == 1
+    assert lib.lora_premultiply_e4m3(fake, -1, ctypes.c_float(1.0), None) == 1
