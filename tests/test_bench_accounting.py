@@ -30,3 +30,22 @@ def test_moe_bytes_count_each_used_expert_pair_once():
     down = 3 * 2 * 8 * (32 + 64) + 2 * 32 * 4 + 4 * 64 * 4     # x per pair (4)
     assert bench.moe_algorithmic_bytes(wl, 0) == up
     assert bench.moe_algorithmic_bytes(wl, 1) == down
+
+
+def test_reference_arm_prints_the_contract_line():
+    """bench.py --impl reference (the oracle on the host cores) prints one JSON line
+    with the keys the driver reads, on a config small enough for a unit test."""
+    import json
+    import subprocess
+    import sys
+    import os
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--config", "tiny", "--steps", "2",
+                          "--warmup", "1"], cwd=root, capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr[-500:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 2
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
