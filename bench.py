@@ -54,8 +54,8 @@ def parse_args(argv=None):
     p.add_argument("--config", default="decode_qkv", choices=list(CONFIG_INDEX) + ["decode_moe"])
     p.add_argument("--layers", type=int, default=32)
     p.add_argument("--requests", type=int, default=16, help="prefill_mlp only: requests in the batch")
-    p.add_argument("--path", default="auto", choices=["auto", "decode_fused", "decode_split", "prefill", "decode_tc", "decode_stream", "decode_direct",
-                            "decode_direct_fp8"],
+    p.add_argument("--path", default="auto", choices=["auto", "decode_fused", "decode_split", "prefill", "decode_direct",
+                                                        "decode_direct_fp8", "decode_tma"],
                    help="auto takes decode_direct_fp8 for a workload with FP8 adapters")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -118,6 +118,7 @@ def captured_traffic(kernel: str):
 TRAFFIC_KERNELS = {
     ("decode_qkv", "decode_fused"): ("fused_decode_kernel",),
     ("decode_qkv", "decode_direct"): ("direct_shrink_kernel", "direct_expand_kernel"),
+    ("decode_qkv", "decode_tma"): ("tma_decode_kernel",),
 }
 
 
@@ -374,7 +375,8 @@ def run_ours(args):
             w0.append((torch.randn(d, lay.x.shape[1], device=dev, generator=g) * 0.02).to(torch.bfloat16))
     aux = torch.cuda.Stream(device=dev)
     resolved0, _ = L.lora_resolve_path(args.path, T, max_seg)
-    use_plan = not args.no_plan and args.with_base == "none" and resolved0 in ("decode_direct", "decode_direct_fp8")
+    use_plan = not args.no_plan and args.with_base == "none" and resolved0 in ("decode_direct", "decode_direct_fp8",
+                                                                                "decode_tma")
     plans = [L.Plan(T, lay.shape, resolved0, device=dev) for lay in layers] if use_plan else []
 
     def apply_layer(l):
@@ -423,6 +425,8 @@ def run_ours(args):
     call_s = apply_ms_mean / 1e3 / len(layers)
     achieved_gbs = sum(per_layer_bytes) / len(layers) / call_s / 1e9
     resolved, launches_per_apply = L.lora_resolve_path(args.path, T, max_seg)
+    if use_plan and resolved == "decode_tma":
+        launches_per_apply = 1  # the plan replaces the per-call plan launch
     gpu_launches = args.steps * (1 + len(layers) * launches_per_apply + (len(mods) if use_plan else 0))
 
     e2e = None

@@ -81,9 +81,8 @@ typedef enum {
                                     shape, else the fused decode path when it does; otherwise
                                     the split decode kernels */
     LORA_PATH_DECODE_FUSED = 1,  /* one launch: shrink, per-(slot, slice) wait, expand, on warp-level
-                                    MMA; needs T <= 2048, r_max <= 128 and k % 16 == 0, else the
-                                    tensor-core decode kernels when they apply (LORA_PATH_DECODE_TC),
-                                    else LORA_ERR_UNSUPPORTED */
+                                    MMA; needs T <= 2048, r_max <= 128 and k % 16 == 0 (else
+                                    LORA_ERR_UNSUPPORTED) */
     LORA_PATH_DECODE_SPLIT = 2,  /* two launches: shrink then expand (programmatic dependent launch);
                                     any rank up to LORA_MAX_RANK; sums reduced in a fixed order, so
                                     results are bit-identical over runs (the deterministic choice:
@@ -93,37 +92,47 @@ typedef enum {
                                     thread-block cluster) and expand, on 128-token tiles of
                                     one slot's segment; needs r_max <= 64
                                     (else LORA_ERR_UNSUPPORTED) */
-    LORA_PATH_DECODE_TC = 4,     /* two launches, tcgen05/TMEM tensor cores: a split-K streaming
-                                    shrink adding into an fp32 accumulator, then a transposed
-                                    expand launched as its programmatic dependent; needs
-                                    T <= 2048, r_max <= 64 and tables that fit in shared memory
-                                    (else LORA_ERR_UNSUPPORTED) */
-    LORA_PATH_DECODE_STREAM = 5, /* two launches on warp-level MMA fed by bulk copies: a split-K
-                                    streaming shrink adding into an fp32 accumulator, then an
-                                    expand launched as its programmatic dependent, one CTA of each
-                                    sharing every SM; needs T <= 2048, r_max <= 128, k % 16 == 0
-                                    and tables that fit in shared memory (else
-                                    LORA_ERR_UNSUPPORTED) */
+    LORA_PATH_DECODE_TC = 4,     /* retired (slower than LORA_PATH_DECODE_DIRECT on every measured
+                                    shape): always LORA_ERR_UNSUPPORTED */
+    LORA_PATH_DECODE_STREAM = 5, /* retired, as LORA_PATH_DECODE_TC: always LORA_ERR_UNSUPPORTED */
     LORA_PATH_DECODE_DIRECT = 6, /* two launches on warp-level MMA in which every warp streams its
                                     own byte-balanced share through a private cp.async ring (no
                                     barriers between warps): a split-K shrink adding into an fp32
                                     accumulator, then an expand launched as its programmatic
                                     dependent; needs T <= 2048, r_max <= 64, S <= 512 and
                                     S * n_slices <= 512 (else LORA_ERR_UNSUPPORTED) */
-    LORA_PATH_DECODE_DIRECT_FP8 = 7 /* LORA_PATH_DECODE_DIRECT with FP8 adapters (TensorRT-LLM LoRA
+    LORA_PATH_DECODE_DIRECT_FP8 = 7, /* LORA_PATH_DECODE_DIRECT with FP8 adapters (TensorRT-LLM LoRA
                                     serving page, "第五步:FP8 特判" and the input-dtype check of the
                                     forward pass): every A and B pointer of the slot table
                                     addresses float8_e4m3fn codes in the same row-major layouts
                                     (A_s,i [r][k], B_s,i [d_i][r], one byte each); x and y stay
                                     bf16.  x is clamped to +-448 and rounded to e4m3 (nearest,
                                     ties to even) inside the shrink, whose products are exact
-                                    and summed in fp32; the sums enter the expand rounded once
-                                    to f16 (|sum| <= 65504 assumed) against B converted exactly
-                                    to f16, and y = bf16(y + s * acc) as for bf16 adapters.
+                                    and summed in fp32; the sums enter the expand as two bf16
+                                    parts (hi and the remainder, about 2^-17 of each sum, no
+                                    overflow) against B converted exactly to bf16, and
+                                    y = bf16(y + s * acc) as for bf16 adapters.
                                     Scale B at load time with lora_premultiply on its bf16
                                     values, then clamp and round to e4m3.  Same limits as
                                     LORA_PATH_DECODE_DIRECT plus k % 16 == 0; never chosen by
                                     LORA_PATH_AUTO, whose table is bf16 */
+    LORA_PATH_DECODE_TMA = 8     /* one persistent kernel per call (one CTA per SM): the adapter
+                                    tiles arrive as TMA boxes through the tensor maps of a table
+                                    set with lora_set_slot_table_tma, x and y rows are gathered
+                                    beside them, and the expand of a slot starts in the same
+                                    kernel once a per-slot counter says its shrink sums are
+                                    complete.  Launched as a programmatic dependent of the
+                                    previous kernel on the stream: it loads adapter weights (and
+                                    its plan) before that kernel has finished, so neither may be
+                                    written by the kernel directly before it.  Needs r_max <= 64,
+                                    n_slices * r_max <= 192 and k % 64 == 0 (else
+                                    LORA_ERR_UNSUPPORTED); every CTA of the call must be resident
+                                    at once (a slot whose sums are not complete within 200 ms is
+                                    reported as LORA_ERR_TIMEOUT).  Without a plan, lora_apply_ex
+                                    builds one in the workspace first (two launches); with
+                                    lora_build_plan(s) / lora_apply_plan it is one launch per call.
+                                    Never chosen by LORA_PATH_AUTO, whose table may lack the
+                                    tensor maps */
 } lora_path_t;
 
 #define LORA_DECODE_MAX_SEG 256
@@ -215,6 +224,29 @@ lora_status_t lora_set_slot_table(void *dev_table, void *host_staging, int32_t S
                                   lora_stream_t stream);
 
 /*
+ * Slot table with TMA tensor maps, for LORA_PATH_DECODE_TMA: the table of
+ * lora_set_slot_table (every path accepts it) followed by, for every slot s
+ * with rank r_s > 0 and slice i, a tensor map of A_s,i as [r_s][k] and one of
+ * B_s,i as [d_i][r_s] (bf16, 128-byte swizzle), encoded on the host with the
+ * driver's cuTensorMapEncodeTiled (no allocation; the CUDA runtime must be able
+ * to reach the driver).  The maps are tied to this shape's k and slice widths
+ * (a plan built with another shape is refused on the device).
+ *
+ * lora_slot_table_tma_bytes: the table's size for S slots and this shape (0 for
+ * a bad shape or S outside [1, LORA_MAX_SLOTS]).
+ *
+ * lora_set_slot_table_tma: checks as lora_pack_slot_table (with S and n_slices
+ * from the shape), dev_table 128-byte aligned (LORA_ERR_ALIGNMENT), then packs
+ * host_staging (lora_slot_table_tma_bytes bytes) and copies it to dev_table on
+ * `stream` as lora_set_slot_table does.  LORA_ERR_UNSUPPORTED if the driver's
+ * encoder is unavailable or rejects a map (e.g. a rank above 256).
+ */
+size_t lora_slot_table_tma_bytes(int32_t S, const lora_shape_t *shape);
+lora_status_t lora_set_slot_table_tma(void *dev_table, void *host_staging, const lora_shape_t *shape,
+                                      const int32_t *ranks, const float *scales, const uint64_t *A_ptrs,
+                                      const uint64_t *B_ptrs, lora_stream_t stream);
+
+/*
  * Per-step token index (TensorRT-LLM LoRA serving page, "a decode batch's
  * route", steps 2 and 4: sorted ids, bincount, cumsum with a final total; vLLM
  * book ch. 16, section 16.4.3, the LoRAKernelMeta tensors).  Device arrays:
@@ -263,14 +295,17 @@ lora_status_t lora_build_index_seq(const int32_t *seq_slot_ids, int32_t n_seq, i
  * accumulator (same size); and, when r_max <= 64, the prefill kernels' xa as two
  * bf16 parts hi + lo, each [n_slices][T][RP] in sorted-token order (RP = 16, 32
  * or 64, the rank padded up); then, when r_max <= 128, two more fp32
- * accumulators the size of xa that LORA_PATH_DECODE_TC and
- * LORA_PATH_DECODE_STREAM use in turn (a call adds into one and clears the
- * other).  Regions start on 256-byte boundaries.  The whole buffer must be zero
- * before the first call that uses it (e.g. one cudaMemsetAsync), and again after
- * a call whose error word reads LORA_ERR_TIMEOUT.  Otherwise every call leaves
- * what the next call of any path needs: the per-slot counters and the fused
- * accumulator zero, the call counter matching the clear accumulator of the
- * two-kernel decode paths.
+ * accumulators the size of xa that LORA_PATH_DECODE_DIRECT uses in turn (a call
+ * adds into one and clears the other); then, when r_max <= 64,
+ * LORA_PATH_DECODE_TMA's two fp32 sum sets (the size of xa, used in turn), its
+ * control block (2 S per-slot counters, a call counter and an exit counter) and
+ * room for the plan such a call without one builds.  Regions start on 256-byte
+ * boundaries, at offsets that depend on T and the shape: use one workspace for
+ * one (T, shape) pair.  The whole buffer must be zero before the first call that
+ * uses it (e.g. one cudaMemsetAsync), and again after a call whose error word
+ * reads LORA_ERR_TIMEOUT.  Otherwise every call leaves what the next call of any
+ * path needs: the per-slot counters and the fused accumulator zero, each call
+ * counter matching the clear accumulator or sum set of its path.
  */
 lora_status_t lora_workspace_bytes(int32_t T, const lora_shape_t *shape, size_t *bytes);
 
@@ -372,8 +407,10 @@ lora_status_t lora_apply_overlap(const void *x, int64_t ldx, void *y, int64_t ld
  *   - Limit: n_slices * T * r_max * 4 bytes must fit in LORA_NOALLOC_WS_BYTES,
  *     else the call returns LORA_ERR_WORKSPACE and enqueues nothing.
  *   - Set-up: the first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current and keeps it for the
+ *     process; make that first call before any stream capture.  The address
+ *     belongs to the device's context: do not reset the device
+ *     (cudaDeviceReset) between calls.
  *   - Sharing: every call on a device uses the same array, and the array keeps
  *     the last call's contents.  Calls whose kernels overlap on the GPU (calls
  *     on different streams, or from threads that do not order their streams)
@@ -415,15 +452,22 @@ lora_status_t lora_build_index_activated(const int32_t *seq_ids, const int32_t *
  * pointers: build one per slot table (per layer), and rebuild it whenever the
  * index or that table changes.
  *
- * lora_plan_bytes: the plan's size for T tokens and this shape (0 for T < 1 or
- * a bad shape).
+ * lora_plan_bytes: the plan's size for T tokens and this shape, enough for
+ * either kind of plan (0 for T < 1 or a bad shape).
  *
  * lora_build_plan: one launch on `stream` that reads the slot table and the
  * index (after lora_build_index) and writes the plan (device, 16-byte aligned,
- * plan_bytes >= lora_plan_bytes).  path: LORA_PATH_DECODE_DIRECT or
- * LORA_PATH_DECODE_DIRECT_FP8 (the kernels the plan is for; else
- * LORA_ERR_UNSUPPORTED, also when those kernels do not take the shape).  Device
- * data errors of the index are reported here, as lora_apply would.
+ * plan_bytes >= lora_plan_bytes).  path: LORA_PATH_DECODE_DIRECT,
+ * LORA_PATH_DECODE_DIRECT_FP8 or LORA_PATH_DECODE_TMA (the kernels the plan is
+ * for; else LORA_ERR_UNSUPPORTED, also when those kernels do not take the
+ * shape).  Device data errors of the index are reported here, as lora_apply
+ * would.  A LORA_PATH_DECODE_TMA plan holds, per active slot, its token groups
+ * and, per CTA, its share of the call's work (split by bytes moved) and a copy
+ * of sorted_ids; it needs a table from lora_set_slot_table_tma of this shape
+ * (else LORA_ERR_INVALID_ARG in err and a plan every call refuses), and is
+ * built for the current device's SM count.  The plan kernel is never launched
+ * as a programmatic dependent, so a LORA_PATH_DECODE_TMA call right after it
+ * (which reads the plan before waiting for its predecessor) sees it complete.
  *
  * lora_apply_plan: lora_apply_ex on that path with the plan instead of the table
  * and the index.  A plan built for another T, slot count, slice count or path is

@@ -24,6 +24,7 @@ __all__ = [
     "LORA_NOALLOC_WS_BYTES",
     "LoraError", "lora_shape_t", "make_shape", "lora_abi_version", "lora_status_string", "lora_scale",
     "lora_premultiply", "lora_premultiply_e4m3", "lora_slot_table_bytes", "lora_pack_slot_table", "lora_set_slot_table",
+    "lora_slot_table_tma_bytes", "lora_set_slot_table_tma",
     "lora_build_index", "lora_build_index_seq", "lora_workspace_bytes", "lora_workspace_xa_offset", "lora_shrink", "lora_expand", "lora_apply", "lora_resolve_path",
     "apply", "lora_apply_noalloc", "lora_apply_overlap", "lora_moe_slot_pointers", "lora_build_index_moe", "lora_apply_moe",
     "lora_build_index_activated", "lora_plan_bytes", "lora_build_plan", "lora_apply_plan", "lora_build_plans", "Plan", "apply_with_base", "SlotTable", "TokenIndex", "Workspace",
@@ -139,6 +140,22 @@ def lora_set_slot_table(dev_table, host_staging, S, n_slices, r_max, ranks, scal
     check(load().lora_set_slot_table(_p(dev_table), _p(host_staging), int(S), int(n_slices), int(r_max),
                                      _p(ranks), _p(scales), _p(A_ptrs), _p(B_ptrs), _stream(stream)),
           "lora_set_slot_table")
+
+
+def lora_slot_table_tma_bytes(S: int, shape: lora_shape_t) -> int:
+    return int(load().lora_slot_table_tma_bytes(int(S), ctypes.byref(shape)))
+
+
+def lora_set_slot_table_tma(dev_table, host_staging, shape, ranks, scales, A_ptrs, B_ptrs, stream=None) -> None:
+    """The slot table plus TMA tensor maps of every A and B (for path "decode_tma")."""
+    ranks = np.ascontiguousarray(ranks, dtype=np.int32)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    A_ptrs = np.ascontiguousarray(A_ptrs, dtype=np.uint64)
+    B_ptrs = np.ascontiguousarray(B_ptrs, dtype=np.uint64)
+    _dev(dev_table, "dev_table")
+    check(load().lora_set_slot_table_tma(_p(dev_table), _p(host_staging), ctypes.byref(shape), _p(ranks),
+                                         _p(scales), _p(A_ptrs), _p(B_ptrs), _stream(stream)),
+          "lora_set_slot_table_tma")
 
 
 def lora_build_index(slot_ids, S, dev_table, sorted_ids, seg_offsets, active, err, stream=None) -> None:
@@ -379,8 +396,10 @@ def lora_build_plans(plans, tables, index, stream=None) -> None:
 
 
 class Plan:
-    """The tables of the warp-streaming kernels for one batch and shape, built once
-    (after the index) and used by every call of that shape."""
+    """The per-step tables of the warp-streaming kernels ("decode_direct",
+    "decode_direct_fp8") or of the one-kernel TMA path ("decode_tma") for one
+    batch and shape, built once (after the index) and used by every call of that
+    shape."""
 
     def __init__(self, T: int, shape: lora_shape_t, path: str = "decode_direct", device="cuda"):
         torch = _torch()
@@ -399,18 +418,25 @@ class Plan:
 
 
 class SlotTable:
-    """Device slot table plus the pinned staging buffer its upload copies from."""
+    """Device slot table plus the pinned staging buffer its upload copies from.
+    With ``shape`` the table also carries the TMA tensor maps of every A and B
+    (lora_set_slot_table_tma), which path "decode_tma" needs; every path accepts it."""
 
-    def __init__(self, S: int, n_slices: int, r_max: int, device="cuda"):
+    def __init__(self, S: int, n_slices: int, r_max: int, device="cuda", shape: Optional[lora_shape_t] = None):
         torch = _torch()
-        self.S, self.n_slices, self.r_max = int(S), int(n_slices), int(r_max)
-        nbytes = lora_slot_table_bytes(S, n_slices)
+        self.S, self.n_slices, self.r_max, self.shape = int(S), int(n_slices), int(r_max), shape
+        nbytes = lora_slot_table_tma_bytes(S, shape) if shape is not None else lora_slot_table_bytes(S, n_slices)
+        if nbytes == 0:
+            raise ValueError("no slot table for this S and shape")
         self.dev = torch.zeros(nbytes, dtype=torch.uint8, device=device)
         self.staging = torch.zeros(nbytes, dtype=torch.uint8).pin_memory()
 
     def set(self, ranks, scales, A_ptrs, B_ptrs, stream=None) -> None:
-        lora_set_slot_table(self.dev, self.staging, self.S, self.n_slices, self.r_max, ranks, scales,
-                            A_ptrs, B_ptrs, stream)
+        if self.shape is not None:
+            lora_set_slot_table_tma(self.dev, self.staging, self.shape, ranks, scales, A_ptrs, B_ptrs, stream)
+        else:
+            lora_set_slot_table(self.dev, self.staging, self.S, self.n_slices, self.r_max, ranks, scales,
+                                A_ptrs, B_ptrs, stream)
 
 
 class TokenIndex:

@@ -33,7 +33,7 @@ STATUS = {
 globals().update({name: code for code, name in STATUS.items()})
 
 PATHS = {"auto": 0, "decode_fused": 1, "decode_split": 2, "prefill": 3, "decode_tc": 4, "decode_stream": 5,
-         "decode_direct": 6, "decode_direct_fp8": 7}
+         "decode_direct": 6, "decode_direct_fp8": 7, "decode_tma": 8}
 
 # Every function the header declares, for the export check.
 EXPORTED = (
@@ -43,7 +43,7 @@ EXPORTED = (
     "lora_resolve_path", "lora_apply_noalloc", "lora_workspace_xa_offset", "lora_build_index_seq",
     "lora_apply_overlap", "lora_premultiply_e4m3", "lora_moe_slot_pointers", "lora_build_index_moe",
     "lora_apply_moe", "lora_build_index_activated", "lora_plan_bytes", "lora_build_plan", "lora_apply_plan",
-    "lora_build_plans", "lora_apply_moe_plan",
+    "lora_build_plans", "lora_apply_moe_plan", "lora_slot_table_tma_bytes", "lora_set_slot_table_tma",
 )
 
 
@@ -113,6 +113,8 @@ def load() -> ctypes.CDLL:
         "lora_apply_plan": (ST, [P, I64, P, I64, I32, SH, P, SZ, ST, P, SZ, P, P]),
         "lora_build_plans": (ST, [I32, SH, I32, P, P, SZ, P, P, P, ST, P, P]),
         "lora_apply_moe_plan": (ST, [P, I64, I32, P, I64, I32, I32, SH, P, SZ, P, SZ, P, P]),
+        "lora_slot_table_tma_bytes": (SZ, [I32, SH]),
+        "lora_set_slot_table_tma": (ST, [P, P, SH, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -17,6 +17,10 @@ namespace lora {
 //   b_off              uint64 B[S * n_slices]
 // ---------------------------------------------------------------------------
 constexpr int32_t kTableMagic = 0x41526f4c;  // "LoRA"
+// Set in header word 3 (r_max, which no kernel reads) of a table whose tensor
+// maps follow it: the only reader of those maps checks this bit before it reads
+// anything past the plain table.
+constexpr int32_t kTableMapsFlag = 1 << 30;
 
 __host__ __device__ inline size_t pad16(size_t b) { return (b + 15) & ~size_t(15); }
 
@@ -51,13 +55,23 @@ struct TableView {
 // 32, 64 or 128 bytes, one swizzle span).
 __host__ __device__ inline int32_t tc_rank_pad(int32_t r_max) { return r_max <= 16 ? 16 : (r_max <= 32 ? 32 : 64); }
 
+// Plan of the one-kernel TMA decode path: a 128-byte header, 64 bytes per
+// slot, 32 bytes for each of up to 256 CTAs, then the T sorted token ids.
+__host__ __device__ inline size_t tma_plan_size(int32_t T, int32_t S) {
+    return (128 + 64 * size_t(S) + 256 * 32 + 4 * size_t(T > 0 ? T : 0) + 255) & ~size_t(255);
+}
+
 // Workspace: a control block of per-(slot, slice) counters, the fp32 xa that
 // lora_shrink writes (and lora_expand reads), the fp32 accumulator of the
 // fused decode kernel, which every call leaves zeroed for the next one, and
 // (r_max <= 64) the prefill path's xa as bf16 hi and lo parts, [n][T][RP] each
-// in sorted-token order.
+// in sorted-token order.  Then, for r_max <= 64, the one-kernel TMA decode
+// path's two fp32 sum sets (the size of xa, used in turn), its control block
+// (2 S per-slot counters, the call counter and the exit counter) and room for
+// the plan a call without one builds.
 struct WorkspaceLayout {
-    size_t ctrl_bytes, xa_off, acc_off, hi_off, lo_off, acc2_off, acc3_off, bytes;
+    size_t ctrl_bytes, xa_off, acc_off, hi_off, lo_off, acc2_off, acc3_off, tacc0_off, tacc1_off, tctrl_off,
+        tplan_off, bytes;
     __host__ __device__ WorkspaceLayout(int32_t T, int32_t n_slices, int32_t r_max, int32_t S) {
         // two int32 counters per (slot, slice) + a few global words, rounded to 256 B
         ctrl_bytes = (sizeof(int32_t) * (2 * size_t(S) * LORA_MAX_SLICES + 64) + 255) & ~size_t(255);
@@ -73,7 +87,12 @@ struct WorkspaceLayout {
         const size_t acc_tc = r_max <= 128 ? ((xa_bytes + 255) & ~size_t(255)) : 0;
         acc2_off = lo_off + ((hl_bytes + 255) & ~size_t(255));
         acc3_off = acc2_off + acc_tc;
-        bytes = acc3_off + acc_tc;
+        const size_t xa_r = (xa_bytes + 255) & ~size_t(255);
+        tacc0_off = acc3_off + acc_tc;
+        tacc1_off = tacc0_off + (tc ? xa_r : 0);
+        tctrl_off = tacc1_off + (tc ? xa_r : 0);
+        tplan_off = tctrl_off + (tc ? ((sizeof(int32_t) * (2 * size_t(S) + 2) + 255) & ~size_t(255)) : 0);
+        bytes = tplan_off + (tc ? tma_plan_size(T, S) : 0);
     }
 };
 

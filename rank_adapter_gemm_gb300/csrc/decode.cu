@@ -341,14 +341,10 @@ static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 cudaError_t launch_shrink(const uint16_t *x, int64_t ldx, const Shape &sh, const void *table,
                           const int32_t *sorted_ids, const int32_t *seg, float *xa, int32_t T, int32_t *err,
                           bool trigger_dependents, cudaStream_t stream) {
-    static bool attr_set = false;
     const size_t smem = shrink_smem(sh.S);
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(shrink_smem(LORA_MAX_SLOTS)));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    // per call: the attribute belongs to the current device's context
+    cudaError_t ea = cudaFuncSetAttribute(shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (ea != cudaSuccess) return ea;
     const int ks = shrink_cluster_size(sh.k);
     // upper bound on items: slices x rank groups x token groups (sum over slots
     // of ceil(n_s / 64) <= min(S, T) + T / 64)

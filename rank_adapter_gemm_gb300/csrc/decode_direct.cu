@@ -46,8 +46,9 @@
 //     its x columns from bf16 to e4m3 in registers (clamped to +-448, nearest
 //     even) and runs mma.m16n8k32 e4m3 with the same shared k-permutation;
 //     token groups are 24 so that a block's 2 MT + 6 chunks fit a stage.  The
-//     expand copies [64][r] bytes of B, converts them exactly to f16 and feeds
-//     an f16 MMA with the sums rounded once to f16.
+//     expand copies [64][r] bytes of B, converts them exactly to bf16 and feeds
+//     a bf16 MMA with the sums split into bf16 hi and lo parts (about 2^-17 of
+//     each sum, with fp32's exponent range).
 //
 // Limits (the host routes other cases elsewhere): T <= 2048, r_max <= 64,
 // S * n_slices <= 512, S <= 512; FP8 also k % 16 == 0.
@@ -215,11 +216,18 @@ __device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t w) {
         : "=r"(r) : "r"(w));
     return r;
 }
-// Two fp32 -> packed f16x2 (lo in the low half), round-to-nearest-even.
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-    uint32_t r;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
+// Two e4m3 codes (bits 0..15 of w; byte 0 -> low half) to bf16x2, exactly:
+// every e4m3 value has at most 4 significant bits and an exponent in bf16's
+// range, so the f16 values of the exact conversion above convert exactly too.
+__device__ __forceinline__ uint32_t bf16x2_from_e4m3x2(uint32_t w) {
+    const uint32_t h = f16x2_from_e4m3x2(w);
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, u;\n\t"
+        "mov.b32 {l, u}, %2;\n\t"
+        "cvt.f32.f16 %0, l;\n\t"
+        "cvt.f32.f16 %1, u;\n\t}"
+        : "=f"(lo), "=f"(hi) : "r"(h));
+    return pack_bf16x2(lo, hi);
 }
 // mma.m16n8k32 with e4m3 A and B, fp32 accumulate.  Lane 4g + q: a0 = (row g,
 // k 4q..4q+3), a1 = (row g+8, k 4q..), a2 = (row g, k 4q+16..), a3 = (row g+8,
@@ -228,14 +236,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 __device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                uint32_t b0, uint32_t b1) {
     asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-// mma.m16n8k16 with f16 A and B (fragments as for bf16), fp32 accumulate.
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -950,8 +950,10 @@ __device__ __forceinline__ void e_load_xa(const EGen &g, const float *buf, const
     }
 }
 
-// kF8: B rows are e4m3 and enter an f16 MMA (exact conversion); the sums are
-// then rounded once to f16 instead of bf16.
+// kF8: B rows are e4m3 and enter a bf16 MMA (exact conversion); the sums
+// enter it as two bf16 parts, hi = bf16(sum) and lo = bf16(sum - hi) (about
+// 2^-17 of each sum, and no overflow: bf16 has fp32's exponent range), one
+// MMA for each part.
 template <bool kF8>
 __device__ __forceinline__ void e_compute(const EGen &g, uint32_t wslot, const float4 (&X)[2][2][2], const Tabs &t,
                                           const DArgs &a, int lane) {
@@ -966,14 +968,15 @@ __device__ __forceinline__ void e_compute(const EGen &g, uint32_t wslot, const f
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
         if (32 * kb >= r) break;
-        uint32_t bh[2][2][2];  // [nt][half][pair]: the sums rounded to bf16 once
+        uint32_t bh[2][2][2];  // [nt][half][pair]: the sums rounded to bf16 once (kF8: the hi part)
+        uint32_t bl[2][2][2];  // kF8: the lo part
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 if (kF8) {
-                    bh[nt][h][0] = pack_f16x2(X[nt][kb][h].x, X[nt][kb][h].y);
-                    bh[nt][h][1] = pack_f16x2(X[nt][kb][h].z, X[nt][kb][h].w);
+                    split_bf16x2(X[nt][kb][h].x, X[nt][kb][h].y, bh[nt][h][0], bl[nt][h][0]);
+                    split_bf16x2(X[nt][kb][h].z, X[nt][kb][h].w, bh[nt][h][1], bl[nt][h][1]);
                 } else {
                     bh[nt][h][0] = pack_bf16x2(X[nt][kb][h].x, X[nt][kb][h].y);
                     bh[nt][h][1] = pack_bf16x2(X[nt][kb][h].z, X[nt][kb][h].w);
@@ -990,10 +993,10 @@ __device__ __forceinline__ void e_compute(const EGen &g, uint32_t wslot, const f
             if (kF8) {
                 const uint2 v0 = vk ? lds8(brow + static_cast<uint32_t>(2 * mt * r)) : make_uint2(0, 0);
                 const uint2 v1 = vk ? lds8(brow + static_cast<uint32_t>((2 * mt + 1) * r)) : make_uint2(0, 0);
-                c0 = make_uint4(f16x2_from_e4m3x2(v0.x), f16x2_from_e4m3x2(v0.x >> 16), f16x2_from_e4m3x2(v0.y),
-                                f16x2_from_e4m3x2(v0.y >> 16));
-                c1 = make_uint4(f16x2_from_e4m3x2(v1.x), f16x2_from_e4m3x2(v1.x >> 16), f16x2_from_e4m3x2(v1.y),
-                                f16x2_from_e4m3x2(v1.y >> 16));
+                c0 = make_uint4(bf16x2_from_e4m3x2(v0.x), bf16x2_from_e4m3x2(v0.x >> 16), bf16x2_from_e4m3x2(v0.y),
+                                bf16x2_from_e4m3x2(v0.y >> 16));
+                c1 = make_uint4(bf16x2_from_e4m3x2(v1.x), bf16x2_from_e4m3x2(v1.x >> 16), bf16x2_from_e4m3x2(v1.y),
+                                bf16x2_from_e4m3x2(v1.y >> 16));
             } else {
                 c0 = vk ? lds16(brow + 2u * static_cast<uint32_t>(2 * mt * r)) : make_uint4(0, 0, 0, 0);
                 c1 = vk ? lds16(brow + 2u * static_cast<uint32_t>((2 * mt + 1) * r)) : make_uint4(0, 0, 0, 0);
@@ -1002,8 +1005,10 @@ __device__ __forceinline__ void e_compute(const EGen &g, uint32_t wslot, const f
             for (int nt = 0; nt < 2; ++nt) {
                 if (nt >= NT8) continue;
                 if (kF8) {
-                    mma_f16_16816(acc[mt][nt], c0.x, c1.x, c0.y, c1.y, bh[nt][0][0], bh[nt][0][1]);
-                    mma_f16_16816(acc[mt][nt], c0.z, c1.z, c0.w, c1.w, bh[nt][1][0], bh[nt][1][1]);
+                    mma_bf16_16816(acc[mt][nt], c0.x, c1.x, c0.y, c1.y, bh[nt][0][0], bh[nt][0][1]);
+                    mma_bf16_16816(acc[mt][nt], c0.z, c1.z, c0.w, c1.w, bh[nt][1][0], bh[nt][1][1]);
+                    mma_bf16_16816(acc[mt][nt], c0.x, c1.x, c0.y, c1.y, bl[nt][0][0], bl[nt][0][1]);
+                    mma_bf16_16816(acc[mt][nt], c0.z, c1.z, c0.w, c1.w, bl[nt][1][0], bl[nt][1][1]);
                 } else {
                     mma_bf16_16816(acc[mt][nt], c0.x, c1.x, c0.y, c1.y, bh[nt][0][0], bh[nt][0][1]);
                     mma_bf16_16816(acc[mt][nt], c0.z, c1.z, c0.w, c1.w, bh[nt][1][0], bh[nt][1][1]);

@@ -711,11 +711,10 @@ bool fused_decode_supported(int32_t T, int32_t r_max, int32_t k) {
 cudaError_t launch_fused_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                 const void *table, const int32_t *sorted_ids, const int32_t *seg, float *ws,
                                 int32_t T, int32_t *err, cudaStream_t stream) {
-    static int num_sms = 0;
-    static bool attr_set = false;
     if (!fused_decode_supported(T, sh.r_max, sh.k)) return cudaErrorNotSupported;
-    if (!attr_set) {
-        int dev = 0;
+    // per call: the SM count and the attribute belong to the current device
+    int dev = 0, num_sms = 0;
+    {
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
         e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
@@ -723,11 +722,6 @@ cudaError_t launch_fused_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int
         const size_t max_smem = fused_smem_bytes(LORA_MAX_SLOTS, kMaxTokens);
         e = cudaFuncSetAttribute(fused_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(max_smem));
         if (e != cudaSuccess) return e;
-        int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_decode_kernel, kThreads, max_smem);
-        if (e != cudaSuccess) return e;
-        if (per_sm < 1) return cudaErrorInvalidConfiguration;
-        attr_set = true;
     }
     const WorkspaceLayout L(T, sh.n, sh.r_max, sh.S);
     char *base = reinterpret_cast<char *>(ws);

@@ -173,13 +173,10 @@ cudaError_t launch_build_index(const int32_t *slot_ids, const int32_t *expert_id
         threads /= 2;
         smem = index_smem_bytes(S, threads);
     }
-    static bool attr_set = false;  // once, outside any stream capture (the first call)
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(build_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             200 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    // per call: the attribute belongs to the current device's context
+    cudaError_t ea = cudaFuncSetAttribute(build_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          200 * 1024);
+    if (ea != cudaSuccess) return ea;
     build_index_kernel<<<1, threads, smem, stream>>>(slot_ids, expert_ids, act, T, tps, K, E, S, table, sorted_ids,
                                                      seg_offsets, active, err);
     return cudaGetLastError();

@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstring>
 
+#include "checks.cuh"
 #include "common.cuh"
 
 namespace lora {
@@ -26,14 +27,6 @@ cudaError_t launch_fused_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int
 cudaError_t launch_premultiply(uint16_t *w, int64_t n, float scale, cudaStream_t stream);
 cudaError_t launch_premultiply_e4m3(uint8_t *w, int64_t n, double scale, cudaStream_t stream);
 bool prefill_supported(int32_t r_max);
-bool decode_tc_supported(int32_t T, const Shape &sh);
-bool decode_stream_supported(int32_t T, const Shape &sh);
-cudaError_t launch_decode_stream(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
-                                 const void *table, const int32_t *sorted_ids, const int32_t *seg, float *ws,
-                                 int32_t T, int32_t *err, cudaStream_t stream);
-cudaError_t launch_decode_tc(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
-                            const void *table, const int32_t *sorted_ids, const int32_t *seg, float *ws, int32_t T,
-                            int32_t *err, cudaStream_t stream);
 bool fused_decode_supported(int32_t T, int32_t r_max, int32_t k);
 bool decode_direct_supported(int32_t T, const Shape &sh, bool fp8);
 cudaError_t launch_direct_shrink(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
@@ -55,51 +48,26 @@ cudaError_t launch_direct_plans(const Shape &sh, const void *const *tables, unsi
 cudaError_t launch_prefill(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                            const void *table, const int32_t *sorted_ids, const int32_t *seg, float *ws,
                            int32_t T, int32_t *err, cudaStream_t stream);
+size_t tma_table_bytes(int32_t S, int32_t n);
+bool encode_tma_table(void *host_buf, const Shape &sh, const int32_t *ranks, const uint64_t *A_ptrs,
+                      const uint64_t *B_ptrs);
+bool decode_tma_supported(int32_t T, const Shape &sh);
+size_t tma_plan_bytes(int32_t T, const Shape &sh);
+cudaError_t launch_tma_plans(const Shape &sh, const void *const *tables, unsigned char *const *plans, int32_t count,
+                             const int32_t *sorted_ids, const int32_t *seg, const int32_t *active, int32_t T,
+                             int32_t *err, cudaStream_t stream);
+cudaError_t launch_tma_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
+                              const unsigned char *plan, float *acc0, float *acc1, int32_t *ctrl, int32_t T,
+                              int32_t *err, cudaStream_t stream);
 }  // namespace lora
 
 using lora::Shape;
+using lora::aligned16;
+using lora::check_index_ptrs;
+using lora::check_rows;
+using lora::check_shape;
 
 namespace {
-
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-lora_status_t check_shape(const lora_shape_t *shape, Shape *out) {
-    if (shape == nullptr) return LORA_ERR_INVALID_ARG;
-    const lora_shape_t &s = *shape;
-    if (s.S < 1 || s.S > LORA_MAX_SLOTS) return LORA_ERR_INVALID_ARG;
-    if (s.n_slices < 1 || s.n_slices > LORA_MAX_SLICES) return LORA_ERR_INVALID_ARG;
-    if (s.k < 8) return LORA_ERR_INVALID_ARG;
-    if (s.k % 8 != 0) return LORA_ERR_ALIGNMENT;
-    if (s.r_max < 8 || s.r_max > LORA_MAX_RANK || s.r_max % 8 != 0) return LORA_ERR_RANK;
-    if (s.slice_offsets[0] != 0) return LORA_ERR_INVALID_ARG;
-    for (int i = 0; i < s.n_slices; ++i) {
-        const int32_t w = s.slice_offsets[i + 1] - s.slice_offsets[i];
-        if (w <= 0) return LORA_ERR_INVALID_ARG;
-        if (w % 8 != 0) return LORA_ERR_ALIGNMENT;
-    }
-    out->S = s.S;
-    out->r_max = s.r_max;
-    out->k = s.k;
-    out->n = s.n_slices;
-    for (int i = 0; i <= LORA_MAX_SLICES; ++i)
-        out->off[i] = i <= s.n_slices ? s.slice_offsets[i] : s.slice_offsets[s.n_slices];
-    return LORA_OK;
-}
-
-lora_status_t check_index_ptrs(const void *table, const int32_t *sorted_ids, const int32_t *seg,
-                               const int32_t *active, int32_t T) {
-    if (table == nullptr || seg == nullptr || active == nullptr) return LORA_ERR_INVALID_ARG;
-    if (T > 0 && sorted_ids == nullptr) return LORA_ERR_INVALID_ARG;
-    if (!aligned16(table)) return LORA_ERR_ALIGNMENT;
-    return LORA_OK;
-}
-
-lora_status_t check_rows(const void *p, int64_t ld, int32_t T, int32_t width) {
-    if (T > 0 && p == nullptr) return LORA_ERR_INVALID_ARG;
-    if (ld < width) return LORA_ERR_INVALID_ARG;
-    if (!aligned16(p) || ld % 8 != 0) return LORA_ERR_ALIGNMENT;
-    return LORA_OK;
-}
 
 lora_status_t check_ws(const float *ws, size_t ws_bytes, int32_t T, const Shape &sh) {
     const lora::WorkspaceLayout L(T, sh.n, sh.r_max, sh.S);
@@ -110,13 +78,9 @@ lora_status_t check_ws(const float *ws, size_t ws_bytes, int32_t T, const Shape 
 
 lora_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA; }
 
-// The fused decode path: the warp-level MMA kernel where it applies (faster
-// today on the decode shapes measured), else the tensor-core (tcgen05) one.
 constexpr int32_t kSmallDecodeT = 64;
 
-bool fused_ok(int32_t T, const Shape &sh) {
-    return lora::fused_decode_supported(T, sh.r_max, sh.k) || lora::decode_tc_supported(T, sh);
-}
+bool fused_ok(int32_t T, const Shape &sh) { return lora::fused_decode_supported(T, sh.r_max, sh.k); }
 
 lora_path_t resolve(lora_path_t path, int32_t T, int32_t max_seg_hint, const Shape &sh, int32_t *launches) {
     if (max_seg_hint <= 0 || max_seg_hint > T) max_seg_hint = T;
@@ -131,6 +95,17 @@ lora_path_t resolve(lora_path_t path, int32_t T, int32_t max_seg_hint, const Sha
     if (launches != nullptr)
         *launches = (path == LORA_PATH_DECODE_FUSED && lora::fused_decode_supported(T, sh.r_max, sh.k)) ? 1 : 2;
     return path;
+}
+
+// The one-kernel TMA decode call on a plan (its own or the workspace's).
+lora_status_t tma_call(const void *x, int64_t ldx, void *y, int64_t ldy, int32_t T, const Shape &sh,
+                       const unsigned char *plan, float *ws, int32_t *err, cudaStream_t s) {
+    const lora::WorkspaceLayout L(T, sh.n, sh.r_max, sh.S);
+    char *base = reinterpret_cast<char *>(ws);
+    return from_cuda(lora::launch_tma_decode(static_cast<const uint16_t *>(x), ldx, static_cast<uint16_t *>(y), ldy,
+                                             sh, plan, reinterpret_cast<float *>(base + L.tacc0_off),
+                                             reinterpret_cast<float *>(base + L.tacc1_off),
+                                             reinterpret_cast<int32_t *>(base + L.tctrl_off), T, err, s));
 }
 
 float *xa_of(float *ws, int32_t T, const Shape &sh) {
@@ -227,6 +202,27 @@ lora_status_t lora_set_slot_table(void *dev_table, void *host_staging, int32_t S
     const lora_status_t st = lora_pack_slot_table(host_staging, S, n_slices, r_max, ranks, scales, A_ptrs, B_ptrs);
     if (st != LORA_OK) return st;
     return from_cuda(cudaMemcpyAsync(dev_table, host_staging, lora::TableLayout(S, n_slices).bytes,
+                                     cudaMemcpyHostToDevice, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t lora_slot_table_tma_bytes(int32_t S, const lora_shape_t *shape) {
+    Shape sh;
+    if (S < 1 || S > LORA_MAX_SLOTS || check_shape(shape, &sh) != LORA_OK || sh.S != S) return 0;
+    return lora::tma_table_bytes(S, sh.n);
+}
+
+lora_status_t lora_set_slot_table_tma(void *dev_table, void *host_staging, const lora_shape_t *shape,
+                                      const int32_t *ranks, const float *scales, const uint64_t *A_ptrs,
+                                      const uint64_t *B_ptrs, lora_stream_t stream) {
+    Shape sh;
+    lora_status_t st;
+    if (dev_table == nullptr || host_staging == nullptr) return LORA_ERR_INVALID_ARG;
+    if ((st = check_shape(shape, &sh)) != LORA_OK) return st;
+    if ((reinterpret_cast<uintptr_t>(dev_table) & 127u) != 0) return LORA_ERR_ALIGNMENT;
+    if ((st = lora_pack_slot_table(host_staging, sh.S, sh.n, sh.r_max, ranks, scales, A_ptrs, B_ptrs)) != LORA_OK)
+        return st;
+    if (!lora::encode_tma_table(host_staging, sh, ranks, A_ptrs, B_ptrs)) return LORA_ERR_UNSUPPORTED;
+    return from_cuda(cudaMemcpyAsync(dev_table, host_staging, lora::tma_table_bytes(sh.S, sh.n),
                                      cudaMemcpyHostToDevice, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -389,20 +385,12 @@ lora_status_t lora_apply_ex(const void *x, int64_t ldx, void *y, int64_t ldy, in
     path = resolve(path, T, max_seg_hint, sh, nullptr);
     switch (path) {
     case LORA_PATH_DECODE_FUSED:
-        if (lora::fused_decode_supported(T, sh.r_max, sh.k))
-            return from_cuda(lora::launch_fused_decode(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws,
-                                                       T, err, s));
-        if (!lora::decode_tc_supported(T, sh)) return LORA_ERR_UNSUPPORTED;
-        return from_cuda(lora::launch_decode_tc(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws, T, err,
-                                               s));
+        if (!lora::fused_decode_supported(T, sh.r_max, sh.k)) return LORA_ERR_UNSUPPORTED;
+        return from_cuda(lora::launch_fused_decode(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws, T,
+                                                   err, s));
     case LORA_PATH_DECODE_TC:
-        if (!lora::decode_tc_supported(T, sh)) return LORA_ERR_UNSUPPORTED;
-        return from_cuda(lora::launch_decode_tc(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws, T, err,
-                                               s));
     case LORA_PATH_DECODE_STREAM:
-        if (!lora::decode_stream_supported(T, sh)) return LORA_ERR_UNSUPPORTED;
-        return from_cuda(lora::launch_decode_stream(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws, T,
-                                                    err, s));
+        return LORA_ERR_UNSUPPORTED;  // retired: slower than LORA_PATH_DECODE_DIRECT on every measured shape
     case LORA_PATH_DECODE_DIRECT:
     case LORA_PATH_DECODE_DIRECT_FP8: {
         const bool fp8 = path == LORA_PATH_DECODE_DIRECT_FP8;
@@ -419,6 +407,16 @@ lora_status_t lora_apply_ex(const void *x, int64_t ldx, void *y, int64_t ldy, in
     case LORA_PATH_PREFILL:
         if (!lora::prefill_supported(sh.r_max)) return LORA_ERR_UNSUPPORTED;
         return from_cuda(lora::launch_prefill(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, ws, T, err, s));
+    case LORA_PATH_DECODE_TMA: {
+        // a plan for this call in the workspace, then the call on it
+        if (!lora::decode_tma_supported(T, sh)) return LORA_ERR_UNSUPPORTED;
+        const lora::WorkspaceLayout L(T, sh.n, sh.r_max, sh.S);
+        unsigned char *plan = reinterpret_cast<unsigned char *>(ws) + L.tplan_off;
+        if (lora::launch_tma_plans(sh, &dev_table, &plan, 1, sorted_ids, seg_offsets, active, T, err, s) !=
+            cudaSuccess)
+            return LORA_ERR_CUDA;
+        return tma_call(x, ldx, y, ldy, T, sh, plan, ws, err, s);
+    }
     default:
         return LORA_ERR_INVALID_ARG;
     }
@@ -489,7 +487,7 @@ lora_status_t lora_apply_moe(const void *x, int64_t ldx, int32_t x_per_token, vo
 size_t lora_plan_bytes(int32_t T, const lora_shape_t *shape) {
     Shape sh;
     if (T < 1 || check_shape(shape, &sh) != LORA_OK) return 0;
-    return lora::direct_plan_bytes(T, sh);
+    return std::max(lora::direct_plan_bytes(T, sh), lora::tma_plan_bytes(T, sh));
 }
 
 lora_status_t lora_build_plans(int32_t T, const lora_shape_t *shape, int32_t count, const void *const *dev_tables,
@@ -500,6 +498,19 @@ lora_status_t lora_build_plans(int32_t T, const lora_shape_t *shape, int32_t cou
     lora_status_t st;
     if (T < 1 || count < 0 || (count > 0 && (dev_tables == nullptr || plans == nullptr))) return LORA_ERR_INVALID_ARG;
     if ((st = check_shape(shape, &sh)) != LORA_OK) return st;
+    if (path == LORA_PATH_DECODE_TMA) {
+        if (!lora::decode_tma_supported(T, sh)) return LORA_ERR_UNSUPPORTED;
+        if (plan_bytes < lora::tma_plan_bytes(T, sh)) return LORA_ERR_WORKSPACE;
+        for (int32_t j = 0; j < count; ++j) {
+            if ((st = check_index_ptrs(dev_tables[j], sorted_ids, seg_offsets, active, T)) != LORA_OK) return st;
+            if (plans[j] == nullptr) return LORA_ERR_WORKSPACE;
+            if (!aligned16(plans[j])) return LORA_ERR_ALIGNMENT;
+        }
+        if (count == 0) return LORA_OK;
+        return from_cuda(lora::launch_tma_plans(sh, dev_tables, reinterpret_cast<unsigned char *const *>(plans), count,
+                                                sorted_ids, seg_offsets, active, T, err,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+    }
     if (path != LORA_PATH_DECODE_DIRECT && path != LORA_PATH_DECODE_DIRECT_FP8) return LORA_ERR_UNSUPPORTED;
     const bool fp8 = path == LORA_PATH_DECODE_DIRECT_FP8;
     if (!lora::decode_direct_supported(T, sh, fp8)) return LORA_ERR_UNSUPPORTED;
@@ -534,6 +545,13 @@ lora_status_t lora_apply_plan(const void *x, int64_t ldx, void *y, int64_t ldy, 
     if ((st = check_rows(y, ldy, T, sh.off[sh.n])) != LORA_OK) return st;
     if ((st = check_ws(ws, ws_bytes, T, sh)) != LORA_OK) return st;
     if (T == 0) return LORA_OK;
+    if (path == LORA_PATH_DECODE_TMA) {
+        if (!lora::decode_tma_supported(T, sh)) return LORA_ERR_UNSUPPORTED;
+        if (plan == nullptr || plan_bytes < lora::tma_plan_bytes(T, sh)) return LORA_ERR_WORKSPACE;
+        if (!aligned16(plan)) return LORA_ERR_ALIGNMENT;
+        return tma_call(x, ldx, y, ldy, T, sh, static_cast<const unsigned char *>(plan), ws, err,
+                        reinterpret_cast<cudaStream_t>(stream));
+    }
     if (path != LORA_PATH_DECODE_DIRECT && path != LORA_PATH_DECODE_DIRECT_FP8) return LORA_ERR_UNSUPPORTED;
     const bool fp8 = path == LORA_PATH_DECODE_DIRECT_FP8;
     if (!lora::decode_direct_supported(T, sh, fp8)) return LORA_ERR_UNSUPPORTED;

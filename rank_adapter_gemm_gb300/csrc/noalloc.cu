@@ -9,6 +9,7 @@
 // device image, so it allocates nothing at all.
 #include <mutex>
 
+#include "checks.cuh"
 #include "common.cuh"
 
 namespace lora {
@@ -49,55 +50,36 @@ cudaError_t scratch_address(float **out) {
     return cudaSuccess;
 }
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 
 extern "C" lora_status_t lora_apply_noalloc(const void *x, int64_t ldx, void *y, int64_t ldy, int32_t T,
                                             const lora_shape_t *shape, const void *dev_table,
                                             const int32_t *sorted_ids, const int32_t *seg_offsets,
                                             const int32_t *active, int32_t *err, lora_stream_t stream) {
-    // argument checks: the same rules as lora_apply
-    if (shape == nullptr || T < 0) return LORA_ERR_INVALID_ARG;
+    // argument checks: the same rules (and the same code) as lora_apply
+    lora::Shape sh;
+    lora_status_t st;
+    if (T < 0) return LORA_ERR_INVALID_ARG;
+    if ((st = lora::check_shape(shape, &sh)) != LORA_OK) return st;
+    if ((st = lora::check_index_ptrs(dev_table, sorted_ids, seg_offsets, active, T)) != LORA_OK) return st;
+    if ((st = lora::check_rows(x, ldx, T, sh.k)) != LORA_OK) return st;
+    if ((st = lora::check_rows(y, ldy, T, sh.off[sh.n])) != LORA_OK) return st;
     const lora_shape_t &s = *shape;
-    if (s.S < 1 || s.S > LORA_MAX_SLOTS || s.n_slices < 1 || s.n_slices > LORA_MAX_SLICES || s.k < 8)
-        return LORA_ERR_INVALID_ARG;
-    if (s.k % 8 != 0) return LORA_ERR_ALIGNMENT;
-    if (s.r_max < 8 || s.r_max > LORA_MAX_RANK || s.r_max % 8 != 0) return LORA_ERR_RANK;
-    if (s.slice_offsets[0] != 0) return LORA_ERR_INVALID_ARG;
-    for (int i = 0; i < s.n_slices; ++i) {
-        const int32_t w = s.slice_offsets[i + 1] - s.slice_offsets[i];
-        if (w <= 0) return LORA_ERR_INVALID_ARG;
-        if (w % 8 != 0) return LORA_ERR_ALIGNMENT;
-    }
-    if (dev_table == nullptr || seg_offsets == nullptr || active == nullptr) return LORA_ERR_INVALID_ARG;
-    if (T > 0 && (sorted_ids == nullptr || x == nullptr || y == nullptr)) return LORA_ERR_INVALID_ARG;
-    if (ldx < s.k || ldy < s.slice_offsets[s.n_slices]) return LORA_ERR_INVALID_ARG;
-    if (!aligned16(dev_table) || !aligned16(x) || !aligned16(y) || ldx % 8 != 0 || ldy % 8 != 0)
-        return LORA_ERR_ALIGNMENT;
     // the fixed scratch bounds the problem size
     const size_t need = sizeof(float) * size_t(s.n_slices) * size_t(T) * size_t(s.r_max);
     if (need > LORA_NOALLOC_WS_BYTES) return LORA_ERR_WORKSPACE;
     if (T == 0) return LORA_OK;
 
-    lora::Shape sh;
-    sh.S = s.S;
-    sh.r_max = s.r_max;
-    sh.k = s.k;
-    sh.n = s.n_slices;
-    for (int i = 0; i <= LORA_MAX_SLICES; ++i)
-        sh.off[i] = i <= s.n_slices ? s.slice_offsets[i] : s.slice_offsets[s.n_slices];
-
     float *xa = nullptr;
     if (scratch_address(&xa) != cudaSuccess) return LORA_ERR_CUDA;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaStream_t strm = reinterpret_cast<cudaStream_t>(stream);
     // nothing in the scratch has to start at zero: the shrink writes every
     // entry the expand then reads
     if (lora::launch_shrink(static_cast<const uint16_t *>(x), ldx, sh, dev_table, sorted_ids, seg_offsets, xa, T,
-                            err, true, st) != cudaSuccess)
+                            err, true, strm) != cudaSuccess)
         return LORA_ERR_CUDA;
     if (lora::launch_expand(xa, static_cast<uint16_t *>(y), ldy, sh, dev_table, sorted_ids, seg_offsets, T, err,
-                            true, st) != cudaSuccess)
+                            true, strm) != cudaSuccess)
         return LORA_ERR_CUDA;
     return LORA_OK;
 }

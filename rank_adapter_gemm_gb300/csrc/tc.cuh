@@ -1,4 +1,4 @@
-// Helpers for the tensor-core (tcgen05 / TMEM) and TMA tensor kernels.
+// Helpers for the tensor-core (tcgen05 / TMEM) kernels.
 #pragma once
 
 #include <cuda.h>
@@ -106,29 +106,6 @@ __device__ __forceinline__ void cp_arrive_noinc(uint64_t *bar) {
 // Orders this thread's shared-memory writes (generic proxy, including its
 // completed cp.async copies) before later tensor-core reads (async proxy).
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-// ---------------------------------------------------------------------------
-// TMA: tiled tensor loads (2D box, or 4 gathered rows) and bulk copies
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int32_t x, int32_t y, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        :: "r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
-}
-
-// Rows y0..y3 (box of one row) to four consecutive box-sized slots at dst.
-__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *map, int32_t x, int32_t y0, int32_t y1,
-                                            int32_t y2, int32_t y3, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
-        :: "r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
-    asm volatile("prefetch.tensormap [%0];" :: "l"(map) : "memory");
-}
 
 // ---------------------------------------------------------------------------
 // tcgen05 (5th-generation tensor core, accumulator in tensor memory)

@@ -74,10 +74,10 @@ class ResidentProjection:
             self.A.append(rowA)
             self.B.append(rowB)
         self.scales = np.ones(S, dtype=np.float32) if premultiplied else rule_scales.astype(np.float32)
-        self.table = SlotTable(S, self.n, r_max, device=device)
+        self.shape = make_shape(S, r_max, k, self.slice_widths)
+        self.table = SlotTable(S, self.n, r_max, device=device, shape=self._table_shape())
         self.table.set(self.ranks, self.scales, a_ptrs, b_ptrs)
         self._ptrs = (a_ptrs, b_ptrs)
-        self.shape = make_shape(S, r_max, k, self.slice_widths)
         self.x = _to_dev(x, device) if x is not None else None
         self.y = _to_dev(y_in, device) if y_in is not None else None
 
@@ -95,12 +95,18 @@ class ResidentProjection:
                 if other.A[s][i] is not None:
                     a_ptrs[s * n + i] = other.A[s][i].data_ptr()
                     b_ptrs[s * n + i] = other.B[s][i].data_ptr()
-        other.table = SlotTable(self.S, n, self.r_max, device=device)
+        other.table = SlotTable(self.S, n, self.r_max, device=device, shape=self._table_shape())
         other.table.set(self.ranks, self.scales, a_ptrs, b_ptrs)
         other._ptrs = (a_ptrs, b_ptrs)
         other.x = self.x.clone() if self.x is not None else None
         other.y = self.y.clone() if self.y is not None else None
         return other
+
+    def _table_shape(self):
+        """bf16 adapters of a shape the one-kernel TMA path takes (r_max <= 64,
+        n_slices * r_max <= 192, k % 64 == 0) get the table with tensor maps."""
+        tma = not self.fp8 and self.r_max <= 64 and self.n * self.r_max <= 192 and self.k % 64 == 0
+        return self.shape if tma else None
 
     def refresh_table(self, stream=None) -> None:
         """Re-upload the slot table (what a change of slot ownership costs)."""

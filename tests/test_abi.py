@@ -90,8 +90,13 @@ def test_workspace_bytes(L):
     # control block, the shrink output xa, the fused kernel's accumulator (same
     # size as xa), the prefill path's hi/lo parts and the two accumulators the
     # tensor-core decode kernels use in turn
-    assert nbytes >= 4 * xa + 2 * hl
-    assert nbytes - 4 * xa - 2 * hl < 4 * (2 * 32 * 4 + 64) + 6 * 256
+    # then the one-kernel TMA path's two sum sets, its control block (2 S
+    # counters, the call and exit counters) and room for a plan (128-byte
+    # header, 64 bytes per slot, 32 per CTA for up to 256 CTAs, T token ids)
+    plan = (128 + 64 * 32 + 256 * 32 + 4 * 256 + 255) // 256 * 256
+    tma = 2 * xa + (4 * (2 * 32 + 2) + 255) // 256 * 256 + plan
+    assert nbytes >= 4 * xa + 2 * hl + tma
+    assert nbytes - 4 * xa - 2 * hl - tma < 4 * (2 * 32 * 4 + 64) + 6 * 256
     # ranks above 64 have no bf16 hi/lo regions; up to 128 they keep the two
     # accumulators of the two-kernel decode paths
     big = L.lora_workspace_bytes(256, L.make_shape(32, 128, 4096, [4096]))
@@ -156,7 +161,7 @@ def test_host_checks_of_the_plan_moe_and_activated_entry_points(L):
                                None, None) == 1
     assert lib.lora_build_plan(256, ctypes.byref(sh), fake, fake, fake, fake, paths["decode_split"], fake, b256,
                                None, None) == 9
-    assert lib.lora_build_plan(256, ctypes.byref(sh), fake, fake, fake, fake, paths["decode_direct"], fake, b256 - 16,
+    assert lib.lora_build_plan(256, ctypes.byref(sh), fake, fake, fake, fake, paths["decode_direct"], fake, 64,
                                None, None) == 6
     assert lib.lora_build_plan(256, ctypes.byref(sh), fake, fake, fake, fake, paths["decode_direct"], None, b256,
                                None, None) == 6
@@ -181,3 +186,48 @@ def test_host_checks_of_the_plan_moe_and_activated_entry_points(L):
     assert lib.lora_apply_moe(fake, 4096, 1, fake, 6144, 4, 0, ctypes.byref(sh), fake, fake, fake, fake, fake, 0,
                               None, None) == 1
     assert lib.lora_premultiply_e4m3(fake, -1, ctypes.c_float(1.0), None) == 1
+
+
+def test_host_checks_of_the_tma_entry_points(L):
+    """The tensor-map table and the one-kernel TMA path: sizes and the argument
+    errors returned before any device or driver call."""
+    import ctypes
+    from rank_adapter_gemm_gb300 import _lib
+    lib = _lib.load()
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # never dereferenced: every call below fails its host checks first
+    sh = L.make_shape(32, 64, 4096, [4096, 1024, 1024])
+    # the ordinary table, aligned to 128 bytes, a 128-byte block header, two
+    # 128-byte tensor maps per slot and slice
+    base = (L.lora_slot_table_bytes(32, 3) + 127) // 128 * 128
+    assert L.lora_slot_table_tma_bytes(32, sh) == base + 128 + 32 * 3 * 256
+    assert L.lora_slot_table_tma_bytes(31, sh) == 0  # S must match the shape
+    assert L.lora_slot_table_tma_bytes(32, L.make_shape(32, 64, 4095, [4096])) == 0
+    staging = np.zeros(L.lora_slot_table_tma_bytes(32, sh), np.uint8)
+    ranks = np.full(32, 16, np.int32)
+    scales = np.ones(32, np.float32)
+    ptrs = np.full(96, 1 << 20, np.uint64)
+
+    def setm(dev, rk=ranks, pa=ptrs):
+        return lib.lora_set_slot_table_tma(dev, P(staging.ctypes.data), ctypes.byref(sh), P(rk.ctypes.data),
+                                           P(scales.ctypes.data), P(pa.ctypes.data), P(pa.ctypes.data), None)
+
+    assert lib.lora_set_slot_table_tma(None, P(staging.ctypes.data), ctypes.byref(sh), None, None, None, None,
+                                       None) == 1
+    assert setm(P((1 << 20) + 16)) == 2                      # table not 128-byte aligned
+    assert setm(fake, rk=np.full(32, 12, np.int32)) == 3     # rank not a multiple of 8
+    assert setm(fake, pa=np.zeros(96, np.uint64)) == 5       # null weight of a rank>0 slot
+    # the path: unsupported shapes (rank above 64, n * r_max above 192, k % 64)
+    b = lib.lora_plan_bytes(256, ctypes.byref(sh))
+    assert b >= 128 + 64 * 32 + 256 * 32 + 4 * 256
+    for bad in (L.make_shape(32, 128, 4096, [4096]), L.make_shape(32, 64, 4096, [1024] * 4),
+                L.make_shape(32, 64, 4032 + 8, [4096])):
+        nb = lib.lora_plan_bytes(256, ctypes.byref(bad))
+        assert lib.lora_build_plan(256, ctypes.byref(bad), fake, fake, fake, fake, _lib.PATHS["decode_tma"], fake,
+                                   nb, None, None) == 9
+    assert lib.lora_build_plan(256, ctypes.byref(sh), fake, fake, fake, fake, _lib.PATHS["decode_tma"], fake,
+                               128, None, None) == 6
+    assert lib.lora_build_plan(256, ctypes.byref(sh), fake, fake, fake, fake, _lib.PATHS["decode_tma"],
+                               P((1 << 20) + 8), b, None, None) == 2
+    assert lib.lora_apply_plan(fake, 4096, fake, 6144, 256, ctypes.byref(sh), fake, 128, _lib.PATHS["decode_tma"],
+                               fake, 1 << 30, None, None) == 6

@@ -14,7 +14,13 @@ from _parity import assert_y_close, gpu_apply, oracle_y, untouched_rows
 
 pytestmark = pytest.mark.gpu
 
-DECODE_PATHS = ["decode_split", "decode_fused", "decode_tc", "decode_stream", "decode_direct"]
+DECODE_PATHS = ["decode_split", "decode_fused", "decode_direct", "decode_tma"]
+
+
+def tma_ok(wl, mod_idx=0):
+    """Shapes the one-kernel TMA decode path takes."""
+    m = wl.modules[mod_idx]
+    return wl.r_max <= 64 and len(m.slice_widths) * wl.r_max <= 192 and m.k % 64 == 0
 
 
 def _torch():
@@ -267,10 +273,9 @@ def test_apply_ragged(case, path):
             gpu_apply(wl, path=path)
         assert e.value.status == 9
         return
-    mma_ok = wl.r_max <= 128 and k % 16 == 0  # warp-MMA kernels (fused and streaming)
-    tc_ok = wl.r_max <= 64                     # tcgen05 decode kernels
-    if ((path == "decode_fused" and not (mma_ok or tc_ok)) or (path == "decode_tc" and not tc_ok)
-            or (path == "decode_stream" and not mma_ok) or (path == "decode_direct" and not tc_ok)):
+    mma_ok = wl.r_max <= 128 and k % 16 == 0  # the fused warp-MMA kernel
+    if ((path == "decode_fused" and not mma_ok) or (path == "decode_direct" and wl.r_max > 64)
+            or (path == "decode_tma" and not tma_ok(wl))):
         import rank_adapter_gemm_gb300 as L
         with pytest.raises(L.LoraError) as e:
             gpu_apply(wl, path=path)
@@ -367,7 +372,7 @@ def test_apply_is_deterministic():
         np.testing.assert_array_equal(y, ys[0])
 
 
-@pytest.mark.parametrize("path", ["decode_fused", "decode_tc", "decode_stream", "decode_direct"])
+@pytest.mark.parametrize("path", ["decode_fused", "decode_direct", "decode_tma"])
 def test_fused_repeat_stays_within_tolerance(path):
     """The fused kernels add split-k partials with fp32 reductions, whose order
     varies; every repetition must still match the oracle."""
@@ -379,12 +384,12 @@ def test_fused_repeat_stays_within_tolerance(path):
         assert_y_close(y, ref, "fused repeat")
 
 
-@pytest.mark.parametrize("path", ["decode_fused", "decode_tc", "decode_stream", "decode_direct"])
+@pytest.mark.parametrize("path", ["decode_fused", "decode_direct"])
 def test_decode_leaves_workspace_ready(path):
     """Each call leaves the workspace ready for the next one without a clearing
     launch: the fused kernel clears its accumulator rows and counters; the
-    two-kernel paths add into one of their two accumulators, clear the other
-    and advance the call counter g (the control word after the 8 S
+    warp-streaming kernels add into one of their two accumulators, clear the
+    other and advance the call counter g (the control word after the 8 S
     per-slot counters), so accumulator g & 1 is zero after every call."""
     torch = _torch()
     import rank_adapter_gemm_gb300 as L
@@ -414,7 +419,7 @@ def test_decode_leaves_workspace_ready(path):
         buf = ws.buf.cpu().numpy()
         ctrl = buf[:xa_off].view(np.int32).copy()
         assert not buf[acc_off:acc_off + xa_floats].any(), "fused accumulator not cleared"
-        if path in ("decode_tc", "decode_stream", "decode_direct"):
+        if path == "decode_direct":
             assert ctrl[gen_word] == call, "call counter not advanced"
             ctrl[gen_word] = 0
             nxt = acc2_off + (call & 1) * region
@@ -667,16 +672,26 @@ def test_apply_fp8_ragged(case):
 
 
 def test_apply_fp8_premultiplied_and_clamped_x():
-    """B scaled at load time by lora_premultiply_e4m3, and x entries beyond the
-    e4m3 range (clamped to +-448 before rounding).  A few saturated entries per
-    row: the sums enter the expand rounded to f16 (2^-11 of each sum), so rows
-    with dozens of them (sums in the thousands) and a cancelling y fall outside
-    the y tolerance by construction."""
+    """B scaled at load time by lora_premultiply_e4m3, and every x row heavily
+    saturated: 64 of its 1024 entries beyond the e4m3 range (bf16 +-1000 and
+    -464, clamped to +-448 before rounding; TensorRT-LLM LoRA serving page, the
+    forward pass's clamp of the activation).  One slot's A also holds codes at
+    +-448 in 32 of those columns, so its sums reach 32 * 448 * 448 (far past
+    the f16 range): the sums enter the expand as bf16 hi and lo parts and every
+    element must still meet the y tolerance."""
     wl = _small_fp8(66, 200, 1024, [1024, 256], 4, [16, 64, 32, 8], premultiplied=True)
     x = wl.modules[0].x
-    x[::7, ::301] = np.uint16(0x447A)   # bf16 1000.0
-    x[3::7, 5::257] = np.uint16(0xC3E8)  # bf16 -464.0
-    _check_fp8(wl, "fp8 premultiplied, clamped x")
+    rng = np.random.default_rng(66)
+    big = np.array([0x447A, 0xC47A, 0xC3E8], np.uint16)  # bf16 1000, -1000, -464
+    for t in range(wl.T):
+        cols = rng.choice(1024, size=64, replace=False)
+        x[t, cols] = big[rng.integers(0, 3, size=64)]
+    hot = np.arange(0, 1024, 32)  # the columns the large A codes sit in
+    x[:, hot] = np.uint16(0x447A)
+    for Ai in wl.modules[0].A[1]:  # slot 1 (rank 64): codes 0x7E / 0xFE = +-448
+        Ai[:, hot] = np.where(np.arange(Ai.shape[0])[:, None] % 2 == 0, 0x7E, 0xFE).astype(np.uint8)
+    assert (wl.slot_ids == 1).any()
+    _check_fp8(wl, "fp8 premultiplied, heavily clamped x, sums past 65504")
 
 
 def test_apply_fp8_rejects_k_not_multiple_of_16():
@@ -898,12 +913,12 @@ def test_apply_activated_decode_qkv():
 
 
 
-@pytest.mark.parametrize("path", ["auto", "decode_split", "decode_fused", "decode_direct", "prefill"])
+@pytest.mark.parametrize("path", ["auto", "decode_split", "decode_fused", "decode_direct", "prefill", "decode_tma"])
 def test_apply_ranks_up_to_512(path):
     """Ranks 512 and 264 next to 8: the split kernels (AUTO's choice above rank 128)
     take any rank in 64-wide chunks; the paths with a lower rank bound refuse."""
     wl = _small(81, 100, 1024, [1024, 256], 3, [512, 264, 8])
-    if path in ("decode_fused", "decode_direct", "prefill"):
+    if path in ("decode_fused", "decode_direct", "prefill", "decode_tma"):
         import rank_adapter_gemm_gb300 as L
         with pytest.raises(L.LoraError) as e:
             gpu_apply(wl, path=path)
@@ -1002,11 +1017,12 @@ def _plan_apply(wl, path="decode_direct", repeat=1, mod_idx=0):
     return outs, int(idx.err.item()), (rp, idx, ws, plan)
 
 
+@pytest.mark.parametrize("path", ["decode_direct", "decode_tma"])
 @pytest.mark.parametrize("cfg", [0, 1, 2, 4, 5])
-def test_apply_plan_configs(cfg):
+def test_apply_plan_configs(cfg, path):
     """Every call of a plan against the oracle, three calls in a row on one workspace."""
     wl = W.config(cfg)
-    outs, err, _ = _plan_apply(wl, repeat=3)
+    outs, err, _ = _plan_apply(wl, path=path, repeat=3)
     assert err == 0
     rows = None if wl.T <= 512 else np.arange(0, wl.T, 3, dtype=np.int32)
     ref, st = oracle_y(wl, rows=rows)
@@ -1137,3 +1153,176 @@ def test_plan_for_other_slice_widths_does_nothing_and_reports():
     torch.cuda.synchronize()
     assert int(idx.err.item()) == 1
     np.testing.assert_array_equal(to_host_bits(rp.y), before)
+
+
+# ---------------------------------------------------------------------------
+# The one-kernel TMA decode path
+# ---------------------------------------------------------------------------
+# k a multiple of 64 with ragged slice widths (not multiples of 64), ranks of
+# every multiple of 8 up to 64, slots with one token and slots with several
+# token groups (more than 64 or 128 tokens), four slices, T = 1 and T = 2048.
+TMA_RAGGED = [
+    # seed, T, k, widths, S, ranks
+    (41, 33, 64, [8, 24], 5, [8, 24, 0, 64, 8]),
+    (42, 1, 64, [8], 1, [8]),
+    (43, 300, 1024, [1000], 2, [64, 8]),
+    (44, 129, 512, [512, 16, 8, 24], 7, [8, 16, 24, 32, 40, 48, 8]),
+    (45, 700, 4096, [4096, 1024, 1024], 3, [64, 64, 32]),
+    (46, 2048, 2048, [136, 520], 4, [16, 8, 64, 40]),
+    (47, 90, 128, [72, 8, 528], 5, [16, 56, 40, 0, 24]),
+    (48, 200, 192, [200], 9, [8, 8, 16, 32, 64, 56, 8, 16, 24]),
+]
+
+
+@pytest.mark.parametrize("plan", [False, True], ids=["apply_ex", "plan"])
+@pytest.mark.parametrize("case", TMA_RAGGED, ids=[f"tma{c[0]}" for c in TMA_RAGGED])
+def test_tma_ragged(case, plan):
+    seed, T, k, widths, S, ranks = case
+    wl = _small(seed, T, k, widths, S, ranks)
+    assert tma_ok(wl)
+    if plan:
+        outs, err, _ = _plan_apply(wl, path="decode_tma", repeat=2)
+    else:
+        outs, err, *_ = gpu_apply(wl, path="decode_tma", repeat=2)
+    assert err == 0
+    ref, _ = oracle_y(wl)
+    keep = untouched_rows(wl)
+    for y in outs:
+        assert_y_close(y, ref, f"tma ragged {seed}")
+        np.testing.assert_array_equal(y[keep], wl.modules[0].y_in[keep])
+
+
+def test_tma_layer_plans_in_one_launch():
+    """Plans of three layers (own weights, one index) in one launch; each layer's
+    call through its plan matches the oracle, the calls back to back on one
+    workspace (each call's kernel may start before the previous one ends)."""
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import ResidentProjection, to_host_bits
+    wls = [W.config(2), W.config(2), W.config(2)]
+    rng = np.random.default_rng(15)
+    for wl in wls[1:]:
+        m = wl.modules[0]
+        m.A = [[(W._normal_bf16(rng, a.shape, a.shape[1] ** -0.5) if a is not None else None) for a in row]
+               for row in m.A]
+        m.B = [[(W._normal_bf16(rng, b.shape, 0.02) if b is not None else None) for b in row] for row in m.B]
+    rps = [ResidentProjection.from_workload(wl) for wl in wls]
+    idx = L.TokenIndex(wls[0].T, wls[0].S)
+    idx.build(torch.from_numpy(wls[0].slot_ids).cuda(), rps[0].table)
+    plans = [L.Plan(wls[0].T, rp.shape, "decode_tma") for rp in rps]
+    L.lora_build_plans(plans, [rp.table for rp in rps], idx)
+    ws = L.Workspace(wls[0].T, rps[0].shape)
+    for rp, plan in zip(rps, plans):
+        plan.apply(rp.x, rp.y, ws, idx.err)
+    torch.cuda.synchronize()
+    assert int(idx.err.item()) == 0
+    for wl, rp in zip(wls, rps):
+        ref, _ = oracle_y(wl)
+        assert_y_close(to_host_bits(rp.y), ref, "tma layer plans")
+
+
+def _tma_regions(L, T, shape):
+    """Float offsets of the TMA path's two sum sets and its control block (the
+    regions after the two-kernel decode paths' accumulators)."""
+    n, r_max, S = shape.n_slices, shape.r_max, shape.S
+    rp = 16 if r_max <= 16 else (32 if r_max <= 32 else 64)  # the prefill path's rank padding
+    region = (n * T * r_max + 63) // 64 * 64
+    hl_region = (n * T * rp * 2 // 4 + 63) // 64 * 64
+    xa_off = L.lora_workspace_xa_offset(shape) // 4
+    tacc0 = xa_off + region + region + 2 * hl_region + 2 * region
+    return tacc0, tacc0 + region, tacc0 + 2 * region, n * T * r_max
+
+
+def test_tma_leaves_workspace_ready():
+    """Call g adds into sum set g & 1, clears set (g + 1) & 1 and advances the
+    call counter (the word after the 2 S per-slot counters): after every call the
+    set the next call adds into and its counters are zero."""
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import ResidentProjection, to_host_bits
+    wl = W.config(2)
+    rp = ResidentProjection.from_workload(wl)
+    idx = L.TokenIndex(wl.T, wl.S)
+    idx.build(torch.from_numpy(wl.slot_ids).cuda(), rp.table)
+    ws = L.Workspace(wl.T, rp.shape)
+    ref, _ = oracle_y(wl)
+    y0 = rp.y.clone()
+    tacc0, tacc1, tctrl, nfl = _tma_regions(L, wl.T, rp.shape)
+    S = wl.S
+    for call in range(1, 5):
+        rp.y.copy_(y0)
+        L.lora_apply(rp.x, rp.y, rp.shape, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active, ws.buf,
+                     idx.err, path="decode_tma")
+        torch.cuda.synchronize()
+        assert int(idx.err.item()) == 0
+        assert_y_close(to_host_bits(rp.y), ref, "tma")
+        buf = ws.buf.cpu().numpy()
+        ctrl = buf[tctrl:tctrl + 2 * S + 2].view(np.int32)
+        assert ctrl[2 * S] == call, "call counter not advanced"
+        assert ctrl[2 * S + 1] == 0, "exit counter not reset"
+        nxt = call & 1
+        assert not ctrl[nxt * S:(nxt + 1) * S].any(), "next counters not cleared"
+        base = tacc1 if nxt else tacc0
+        assert not buf[base:base + nfl].any(), "next sum set not cleared"
+
+
+def test_tma_slot_wait_timeout_reports_error_and_device_stays_usable():
+    """Per-slot counters that can never reach their targets (a poisoned
+    workspace) make the expand's bounded wait give up: LORA_ERR_TIMEOUT in the
+    error word, the affected y rows unchanged, and a call on a clean workspace
+    afterwards is correct."""
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import ResidentProjection, to_host_bits
+    wl = W.config(0)
+    rp = ResidentProjection.from_workload(wl)
+    idx = L.TokenIndex(wl.T, wl.S)
+    idx.build(torch.from_numpy(wl.slot_ids).cuda(), rp.table)
+    ws = L.Workspace(wl.T, rp.shape)
+    y0 = rp.y.clone()
+    tacc0, tacc1, tctrl, nfl = _tma_regions(L, wl.T, rp.shape)
+    ws.buf[tctrl:tctrl + wl.S].view(torch.int32).fill_(-(1 << 30))  # call 0 counts into set 0
+    L.lora_apply(rp.x, rp.y, rp.shape, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active, ws.buf,
+                 idx.err, path="decode_tma")
+    torch.cuda.synchronize()
+    assert int(idx.err.item()) == 7  # LORA_ERR_TIMEOUT
+    np.testing.assert_array_equal(to_host_bits(rp.y), to_host_bits(y0))
+    ws.buf.zero_()
+    idx.err.zero_()
+    rp.y.copy_(y0)
+    L.lora_apply(rp.x, rp.y, rp.shape, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active, ws.buf,
+                 idx.err, path="decode_tma")
+    torch.cuda.synchronize()
+    assert int(idx.err.item()) == 0
+    ref, _ = oracle_y(wl)
+    assert_y_close(to_host_bits(rp.y), ref, "tma after a timed-out call")
+
+
+def test_tma_refuses_a_table_without_maps_and_a_foreign_plan():
+    """A table set without tensor maps, or a plan built for another T or for the
+    warp-streaming kernels: LORA_ERR_INVALID_ARG in err, y unchanged."""
+    torch = _torch()
+    import rank_adapter_gemm_gb300 as L
+    from rank_adapter_gemm_gb300.resident import ResidentProjection, to_host_bits
+    wl = W.config(2)
+    rp = ResidentProjection.from_workload(wl)
+    plain = L.SlotTable(wl.S, rp.n, wl.r_max)
+    plain.set(rp.ranks, rp.scales, *rp._ptrs)
+    idx = L.TokenIndex(wl.T, wl.S)
+    idx.build(torch.from_numpy(wl.slot_ids).cuda(), rp.table)
+    ws = L.Workspace(wl.T, rp.shape)
+    before = to_host_bits(rp.y).copy()
+    L.lora_apply(rp.x, rp.y, rp.shape, plain.dev, idx.sorted_ids, idx.seg_offsets, idx.active, ws.buf, idx.err,
+                 path="decode_tma")
+    torch.cuda.synchronize()
+    assert int(idx.err.item()) == 1
+    np.testing.assert_array_equal(to_host_bits(rp.y), before)
+    for path in ("decode_direct", "decode_tma"):
+        plan = L.Plan(wl.T, rp.shape, path)
+        plan.build(idx, rp.table)
+        idx.err.zero_()
+        x, y = (rp.x[:128], rp.y[:128]) if path == "decode_tma" else (rp.x, rp.y)
+        L.lora_apply_plan(x, y, rp.shape, plan.buf, ws.buf, idx.err, path="decode_tma")
+        torch.cuda.synchronize()
+        assert int(idx.err.item()) == 1
+        np.testing.assert_array_equal(to_host_bits(rp.y), before)
