@@ -54,9 +54,14 @@ def parse_args(argv=None):
     p.add_argument("--config", default="decode_qkv", choices=list(CONFIG_INDEX) + ["decode_moe"])
     p.add_argument("--layers", type=int, default=32)
     p.add_argument("--requests", type=int, default=16, help="prefill_mlp only: requests in the batch")
-    p.add_argument("--path", default="auto", choices=["auto", "decode_fused", "decode_split", "prefill", "decode_direct",
-                                                        "decode_direct_fp8", "decode_tma"],
-                   help="auto takes decode_direct_fp8 for a workload with FP8 adapters")
+    p.add_argument("--path", default="best", choices=["best", "auto", "decode_fused", "decode_split", "prefill",
+                                                        "decode_direct", "decode_direct_fp8", "decode_tma"],
+                   help="best: the library's fastest measured path for the workload (default_path); auto: "
+                        "LORA_PATH_AUTO (decode_direct_fp8 for a workload with FP8 adapters)")
+    p.add_argument("--configs", default="all",
+                   help="after the headline, one record per other workload: 'all', 'none' or a comma list of "
+                        + ", ".join(SUB_CONFIGS))
+    p.add_argument("--config-seconds", type=float, default=0.3, help="timed region of each per-workload record")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-chunks", type=int, default=8,
@@ -335,10 +340,100 @@ def time_steps(args, dev, local, index_part, apply_part):
     return elapsed_s, apply_ms_mean, index_ms_mean, sampler.summary(w0, w1), peaks
 
 
+class ProjectionBench:
+    """One workload of packed projections on the device for timing: layer l runs
+    projection l % len(modules) in its own buffers (weights, x, y, slot table),
+    one token index per step, per-step plans where the path has them."""
+
+    def __init__(self, wl, n_layers, path, dev, no_plan=False, with_base="none"):
+        import torch
+        import rank_adapter_gemm_gb300 as L
+        from rank_adapter_gemm_gb300.resident import ResidentProjection
+        self.L, self.wl, self.dev, self.with_base = L, wl, dev, with_base
+        self.wbytes = 1 if wl.weights == "e4m3" else 2
+        self.mods = list(range(len(wl.modules)))
+        n_layers = max(len(self.mods), n_layers // len(self.mods) * len(self.mods))
+        base = [ResidentProjection.from_workload(wl, m, device=dev) for m in self.mods]
+        self.layers = [base[l % len(base)] if l < len(base) else base[l % len(base)].clone(device=dev)
+                       for l in range(n_layers)]
+        self.T, self.S = wl.T, wl.S
+        counts = np.bincount(wl.slot_ids[wl.slot_ids >= 0], minlength=self.S)
+        self.max_seg = int(counts.max()) if counts.size else 0
+        self.slot_dev = torch.from_numpy(_index_ids(wl)).to(dev)
+        self.index = L.TokenIndex(self.T, self.S, device=dev)
+        self.ws = [L.Workspace(self.T, lay.shape, device=dev) for lay in self.layers[:len(base)]]
+        self.ws_of = [self.ws[l % len(self.ws)].buf for l in range(len(self.layers))]
+        self.w0 = []
+        if with_base != "none":
+            g = torch.Generator(device=dev).manual_seed(1234)
+            for lay in self.layers:
+                d = int(lay.y.shape[1])
+                self.w0.append((torch.randn(d, lay.x.shape[1], device=dev, generator=g) * 0.02).to(torch.bfloat16))
+        self.aux = torch.cuda.Stream(device=dev)
+        self.path = path
+        self.resolved, self.launches_per_apply = L.lora_resolve_path(path, self.T, self.max_seg)
+        self.use_plan = (not no_plan and with_base == "none" and
+                         self.resolved in ("decode_direct", "decode_direct_fp8", "decode_tma"))
+        if self.use_plan and self.resolved == "decode_tma":
+            self.launches_per_apply = 1  # the plan replaces the per-call plan launch
+        self.plans = ([L.Plan(self.T, lay.shape, self.resolved, device=dev) for lay in self.layers]
+                      if self.use_plan else [])
+        m = wl.modules
+        self.bytes_per_call = [algorithmic_bytes(wl.slot_ids, wl.ranks, m[j].k, m[j].slice_widths, self.wbytes)
+                               for j in self.mods]
+        self.flops_per_call = [algorithmic_flops(wl.slot_ids, wl.ranks, m[j].k, m[j].slice_widths) for j in self.mods]
+        if with_base != "none":  # the base GEMM's W0, x and y bytes too
+            self.bytes_per_call = [b + 2 * m[j].k * sum(m[j].slice_widths) + 2 * self.T * (m[j].k + sum(m[j].slice_widths))
+                                   for b, j in zip(self.bytes_per_call, self.mods)]
+
+    def apply_layer(self, l):
+        L, lay, torch = self.L, self.layers[l], __import__("torch")
+        if self.use_plan:
+            self.plans[l].apply(lay.x, lay.y, self.ws[l % len(self.ws)], self.index.err)
+            return
+        if self.with_base == "overlap":
+            L.apply_with_base(lay.x, self.w0[l], lay.y, lay.shape, lay.table.dev, self.index, self.ws_of[l], self.aux,
+                              max_seg_hint=self.max_seg, path=self.path)
+            return
+        if self.with_base == "serial":
+            torch.matmul(lay.x, self.w0[l].t(), out=lay.y)
+        L.lora_apply(lay.x, lay.y, lay.shape, lay.table.dev, self.index.sorted_ids, self.index.seg_offsets,
+                     self.index.active, self.ws_of[l], self.index.err, max_seg_hint=self.max_seg, path=self.path)
+
+    def index_part(self):
+        L = self.L
+        self.layers[0].refresh_table()
+        _build_index(self.index, self.slot_dev, self.layers[0].table, self.wl.tokens_per_seq)
+        if self.use_plan:  # one launch per shape: a plan per layer, each with its layer's weight pointers
+            n = len(self.mods)
+            for m in self.mods:
+                L.lora_build_plans(self.plans[m::n], [lay.table for lay in self.layers[m::n]], self.index)
+
+    def apply_part(self):
+        for l in range(len(self.layers)):
+            self.apply_layer(l)
+
+    def per_layer(self, values):
+        return [values[l % len(self.mods)] for l in range(len(self.layers))]
+
+
+def default_path(wl):
+    """The library's fastest measured path for a workload: the one-kernel TMA
+    decode path on per-step plans for bf16 decode batches, the FP8 variant of the
+    warp-streaming kernels for FP8 adapters, the tensor-core prefill kernels for
+    long segments."""
+    if wl.weights == "e4m3":
+        return "decode_direct_fp8"
+    counts = np.bincount(wl.slot_ids[wl.slot_ids >= 0], minlength=wl.S)
+    if counts.size and int(counts.max()) > 256:
+        return "auto"  # prefill
+    ok = all(wl.r_max <= 64 and len(m.slice_widths) * wl.r_max <= 192 and m.k % 64 == 0 for m in wl.modules)
+    return "decode_tma" if ok else "auto"
+
+
 def run_ours(args):
     import torch
     import rank_adapter_gemm_gb300 as L
-    from rank_adapter_gemm_gb300.resident import ResidentProjection
 
     rank, world = dist_init("nccl")
     _, _, local = dist_info()
@@ -346,96 +441,44 @@ def run_ours(args):
     dev = torch.device("cuda", local)
 
     wl = _workload(args.config, args.requests)
+    if args.path == "best":
+        args.path = default_path(wl)
     if wl.weights == "e4m3":
         if args.path == "auto":
             args.path = "decode_direct_fp8"
         if args.path != "decode_direct_fp8":
             raise SystemExit(f"{args.config} holds FP8 adapters: only --path decode_direct_fp8 serves it")
-    wbytes = 1 if wl.weights == "e4m3" else 2
-    mods = list(range(len(wl.modules)))
-    # layer l uses projection mods[l % len(mods)] in its own buffers
-    base = [ResidentProjection.from_workload(wl, m, device=dev) for m in mods]
-    layers = []
-    for l in range(args.layers):
-        src = base[l % len(base)]
-        layers.append(src if l < len(base) else src.clone(device=dev))
-    T, S = wl.T, wl.S
-    counts = np.bincount(wl.slot_ids[wl.slot_ids >= 0], minlength=S)
-    max_seg = int(counts.max()) if counts.size else 0
-    slot_dev = torch.from_numpy(_index_ids(wl)).to(dev)
-    index = L.TokenIndex(T, S, device=dev)
-    ws = [L.Workspace(T, lay.shape, device=dev) for lay in layers[:len(base)]]
-    ws_of = [ws[l % len(ws)].buf for l in range(len(layers))]
-
-    w0 = []
-    if args.with_base != "none":
-        g = torch.Generator(device=dev).manual_seed(1234)
-        for lay in layers:
-            d = int(sum(lay.widths)) if hasattr(lay, "widths") else int(lay.y.shape[1])
-            w0.append((torch.randn(d, lay.x.shape[1], device=dev, generator=g) * 0.02).to(torch.bfloat16))
-    aux = torch.cuda.Stream(device=dev)
-    resolved0, _ = L.lora_resolve_path(args.path, T, max_seg)
-    use_plan = not args.no_plan and args.with_base == "none" and resolved0 in ("decode_direct", "decode_direct_fp8",
-                                                                                "decode_tma")
-    plans = [L.Plan(T, lay.shape, resolved0, device=dev) for lay in layers] if use_plan else []
-
-    def apply_layer(l):
-        lay = layers[l]
-        if use_plan:
-            plans[l].apply(lay.x, lay.y, ws[l % len(ws)], index.err)
-            return
-        if args.with_base == "overlap":
-            L.apply_with_base(lay.x, w0[l], lay.y, lay.shape, lay.table.dev, index, ws_of[l], aux,
-                              max_seg_hint=max_seg, path=args.path)
-            return
-        if args.with_base == "serial":
-            torch.matmul(lay.x, w0[l].t(), out=lay.y)
-        L.lora_apply(lay.x, lay.y, lay.shape, lay.table.dev, index.sorted_ids, index.seg_offsets, index.active,
-                     ws_of[l], index.err, max_seg_hint=max_seg, path=args.path)
-
-    def index_part():
-        layers[0].refresh_table()
-        _build_index(index, slot_dev, layers[0].table, wl.tokens_per_seq)
-        if use_plan:  # one launch per shape: a plan per layer, each with its layer's weight pointers
-            for m in mods:
-                L.lora_build_plans(plans[m::len(mods)], [lay.table for lay in layers[m::len(mods)]], index)
-
-    def apply_part():
-        for l in range(len(layers)):
-            apply_layer(l)
+    pb = ProjectionBench(wl, args.layers, args.path, dev, no_plan=args.no_plan, with_base=args.with_base)
+    T, mods, layers = pb.T, pb.mods, pb.layers
 
     elapsed_s, apply_ms_mean, index_ms_mean, clocks, (peak_gbs, peak_tf, peak_src) = \
-        time_steps(args, dev, local, index_part, apply_part)
-    err = int(index.err.item())
+        time_steps(args, dev, local, pb.index_part, pb.apply_part)
+    err = int(pb.index.err.item())
 
     units = T * len(layers) * args.steps
     value = job_throughput(units, elapsed_s, world, dev)
     ms_per_step = max_over_ranks(elapsed_s, dev) / args.steps * 1e3
-
-    bytes_per_call = [algorithmic_bytes(wl.slot_ids, wl.ranks, wl.modules[m].k, wl.modules[m].slice_widths, wbytes)
-                      for m in mods]
-    flops_per_call = [algorithmic_flops(wl.slot_ids, wl.ranks, wl.modules[m].k, wl.modules[m].slice_widths)
-                      for m in mods]
-    if args.with_base != "none":  # the base GEMM's W0, x and y bytes too
-        bytes_per_call = [b + 2 * wl.modules[m].k * sum(wl.modules[m].slice_widths)
-                          + 2 * T * (wl.modules[m].k + sum(wl.modules[m].slice_widths))
-                          for b, m in zip(bytes_per_call, mods)]
-    per_layer_bytes = [bytes_per_call[l % len(mods)] for l in range(len(layers))]
-    per_layer_flops = [flops_per_call[l % len(mods)] for l in range(len(layers))]
+    per_layer_bytes = pb.per_layer(pb.bytes_per_call)
+    per_layer_flops = pb.per_layer(pb.flops_per_call)
     call_s = apply_ms_mean / 1e3 / len(layers)
     achieved_gbs = sum(per_layer_bytes) / len(layers) / call_s / 1e9
-    resolved, launches_per_apply = L.lora_resolve_path(args.path, T, max_seg)
-    if use_plan and resolved == "decode_tma":
-        launches_per_apply = 1  # the plan replaces the per-call plan launch
-    gpu_launches = args.steps * (1 + len(layers) * launches_per_apply + (len(mods) if use_plan else 0))
+    resolved = pb.resolved
+    gpu_launches = args.steps * (1 + len(layers) * pb.launches_per_apply + (len(mods) if pb.use_plan else 0))
 
     e2e = None
     if not args.no_e2e and args.with_base == "none":
-        e2e = run_e2e(args, wl, layers, index, slot_dev, ws_of, max_seg, dev, world, plans, mods, ws)
+        e2e = run_e2e(args, wl, layers, pb.index, pb.slot_dev, pb.ws_of, pb.max_seg, dev, world, pb.plans, mods,
+                      pb.ws)
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         cpu = cpu_baseline(wl, args.cpu_seconds)
+
+    configs = None
+    if args.configs != "none" and rank == 0 and world == 1:
+        del pb  # free the headline's buffers before the other workloads
+        torch.cuda.empty_cache()
+        configs = config_records(args, dev, local, peak_gbs)
 
     out = {
         "metric": metric_name(args.config),
@@ -453,9 +496,11 @@ def run_ours(args):
         "config": {
             "workload": workload_name(args.config, wl),
             "config": args.config,
+            "value_definition": "tokens through one projection call per second: T x calls per step / step time "
+                                "(one call = the branch of one packed projection of one layer)",
             "layers_per_step": len(layers),
             "calls_per_step": len(layers),
-            "path": resolved + (" with per-step plans" if use_plan else ""),
+            "path": resolved + (" with per-step plans" if pb_use_plan(resolved, args) else ""),
             "l2": f"inputs larger than L2: {len(layers)} distinct layer buffer sets, "
                   f"{sum(per_layer_bytes) / 1e9:.2f} GB of algorithmic bytes per step",
             "parallelism": f"replicas x{world}",
@@ -489,7 +534,14 @@ def run_ours(args):
         out["e2e"] = e2e
     if cpu is not None:
         out["cpu_baseline"] = cpu
+    if configs is not None:
+        out["configs"] = configs
     return out, rank
+
+
+def pb_use_plan(resolved, args):
+    return not args.no_plan and args.with_base == "none" and resolved in ("decode_direct", "decode_direct_fp8",
+                                                                          "decode_tma")
 
 
 def run_e2e(args, wl, layers, index, slot_dev, ws_of, max_seg, dev, world, plans=(), mods=(0,), ws=()):
@@ -611,48 +663,61 @@ def moe_algorithmic_bytes(wl, m) -> int:
     return int(weights + 2 * k * x_rows + 4 * d * int(lora.sum()))
 
 
+class MoeBench:
+    """The routed-expert workload on the device: layer l runs module l % 2 (w1
+    with x per token, w2 with x per pair) in its own buffers; one pair index per
+    step, per-step plans unless no_plan."""
+
+    def __init__(self, wl, n_layers, dev, no_plan=False):
+        import torch
+        import rank_adapter_gemm_gb300 as L
+        from rank_adapter_gemm_gb300.resident import ResidentMoeProjection, clone_moe
+        self.L, self.wl = L, wl
+        self.mods = list(range(len(wl.modules)))
+        base = [ResidentMoeProjection(wl, m, device=dev) for m in self.mods]
+        self.layers = [base[l % len(base)] if l < len(base) else clone_moe(base[l % len(base)], device=dev)
+                       for l in range(max(n_layers, len(base)))]
+        P, V = wl.T * wl.K, wl.n_adapters * wl.E
+        self.index = L.TokenIndex(P, V, device=dev)
+        self.slot_dev = torch.from_numpy(wl.slot_ids).to(dev)
+        self.expert_dev = torch.from_numpy(wl.expert_ids.reshape(-1).copy()).to(dev)
+        self.ws = [L.Workspace(P, b.shape, device=dev) for b in base]
+        self.plans = [] if no_plan else [L.Plan(P, lay.shape, device=dev) for lay in self.layers]
+        self.bytes_per_call = [moe_algorithmic_bytes(wl, m) for m in self.mods]
+
+    def index_part(self):
+        L, n, wl = self.L, len(self.mods), self.wl
+        self.index.build_moe(self.slot_dev, self.expert_dev, wl.K, wl.E, self.layers[0].table)
+        if self.plans:  # one launch per module shape
+            for m in self.mods:
+                L.lora_build_plans(self.plans[m::n], [lay.table for lay in self.layers[m::n]], self.index)
+
+    def apply_part(self):
+        L, wl = self.L, self.wl
+        for l, lay in enumerate(self.layers):
+            L.lora_apply_moe(lay.x, lay.y, wl.K, lay.shape, lay.table.dev, self.index.sorted_ids,
+                             self.index.seg_offsets, self.index.active, self.ws[l % len(self.ws)].buf, self.index.err,
+                             x_per_token=lay.x_per_token, plan=self.plans[l] if self.plans else None)
+
+
 def run_moe(args):
-    """The routed-expert workload: layer l runs module l % 2 (w1 with x per token,
-    w2 with x per pair) in its own buffers; one pair index per step."""
+    """The routed-expert workload as the headline line."""
     import torch
-    import rank_adapter_gemm_gb300 as L
-    from rank_adapter_gemm_gb300.resident import ResidentMoeProjection, clone_moe
 
     rank, world = dist_init("nccl")
     _, _, local = dist_info()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = W.moe_config()
-    mods = list(range(len(wl.modules)))
-    base = [ResidentMoeProjection(wl, m, device=dev) for m in mods]
-    layers = [base[l % len(base)] if l < len(base) else clone_moe(base[l % len(base)], device=dev)
-              for l in range(args.layers)]
-    P, V = wl.T * wl.K, wl.n_adapters * wl.E
-    index = L.TokenIndex(P, V, device=dev)
-    slot_dev = torch.from_numpy(wl.slot_ids).to(dev)
-    expert_dev = torch.from_numpy(wl.expert_ids.reshape(-1).copy()).to(dev)
-    ws = [L.Workspace(P, b.shape, device=dev) for b in base]
-    plans = [] if args.no_plan else [L.Plan(P, lay.shape, device=dev) for lay in layers]
-
-    def index_part():
-        index.build_moe(slot_dev, expert_dev, wl.K, wl.E, layers[0].table)
-        if plans:  # one launch per module shape
-            for m in mods:
-                L.lora_build_plans(plans[m::len(mods)], [lay.table for lay in layers[m::len(mods)]], index)
-
-    def apply_part():
-        for l, lay in enumerate(layers):
-            L.lora_apply_moe(lay.x, lay.y, wl.K, lay.shape, lay.table.dev, index.sorted_ids, index.seg_offsets,
-                             index.active, ws[l % len(ws)].buf, index.err, x_per_token=lay.x_per_token,
-                             plan=plans[l] if plans else None)
-
+    mb = MoeBench(wl, args.layers, dev, no_plan=args.no_plan)
     elapsed_s, apply_ms_mean, index_ms_mean, clocks, (peak_gbs, peak_tf, peak_src) = \
-        time_steps(args, dev, local, index_part, apply_part)
-    err = int(index.err.item())
+        time_steps(args, dev, local, mb.index_part, mb.apply_part)
+    err = int(mb.index.err.item())
+    layers = mb.layers
     units = wl.T * len(layers) * args.steps
     value = job_throughput(units, elapsed_s, world, dev)
     ms_per_step = max_over_ranks(elapsed_s, dev) / args.steps * 1e3
-    per_layer_bytes = [moe_algorithmic_bytes(wl, l % len(mods)) for l in range(len(layers))]
+    per_layer_bytes = [mb.bytes_per_call[l % len(mb.mods)] for l in range(len(layers))]
     call_s = apply_ms_mean / 1e3 / len(layers)
     achieved_gbs = sum(per_layer_bytes) / len(layers) / call_s / 1e9
     cpu = None
@@ -677,7 +742,7 @@ def run_moe(args):
             "layers_per_step": len(layers),
             "calls_per_step": len(layers),
             "path": "lora_apply_moe (warp-streaming decode kernels over n_adapters * E virtual slots)"
-                    + (" with per-step plans" if plans else ""),
+                    + (" with per-step plans" if mb.plans else ""),
             "l2": f"inputs larger than L2: {len(layers)} distinct layer buffer sets, "
                   f"{sum(per_layer_bytes) / 1e9:.2f} GB of algorithmic bytes per step",
             "parallelism": f"replicas x{world}",
@@ -696,13 +761,92 @@ def run_moe(args):
             "us_per_call": call_s * 1e6,
             "index_and_table_us": index_ms_mean * 1e3,
         },
-        "gpu_launches": args.steps * (1 + 2 * len(layers) + (len(mods) if plans else 0)),
+        "gpu_launches": args.steps * (1 + 2 * len(layers) + (len(mb.mods) if mb.plans else 0)),
         "clocks": clocks,
         "device_error": err,
     }
     if cpu is not None:
         out["cpu_baseline"] = cpu
     return out, rank
+
+
+# ---------------------------------------------------------------------------
+# One record per other workload, in the same run
+# ---------------------------------------------------------------------------
+SUB_CONFIGS = {
+    "decode_q_proj": {"index": 1},
+    "large_decode": {"index": 4},
+    "layer_sweep": {"index": 4, "sweep": True},
+    "prefill_mlp": {"index": 3},
+    "decode_qkv_spec": {"index": 5},
+    "decode_qkv_fp8": {"index": 6},
+    "decode_moe": {"moe": True},
+}
+L2_BYTES = 129e6
+
+
+def _timed(dev, local, index_part, apply_part, seconds):
+    """time_steps with about `seconds` of timed calls (a 3-step probe sizes it)."""
+    import types
+    probe = time_steps(types.SimpleNamespace(steps=3, warmup=3), dev, local, index_part, apply_part)
+    per_step = max(probe[1], 1e-3) / 1e3
+    steps = int(min(2000, max(5, seconds / per_step)))
+    return time_steps(types.SimpleNamespace(steps=steps, warmup=3), dev, local, index_part, apply_part), steps
+
+
+def config_records(args, dev, local, peak_gbs):
+    """Per-call time, algorithmic bytes and roofline fraction of every other
+    workload of the method (the driver's run sees all of them), each with the
+    oracle's one-core and all-core rates on a bounded sample."""
+    import torch
+    names = list(SUB_CONFIGS) if args.configs == "all" else [c for c in args.configs.split(",") if c]
+    out = {}
+    for name in names:
+        spec = SUB_CONFIGS[name]
+        t0 = time.time()
+        if spec.get("moe"):
+            wl = W.moe_config()
+            per_call = [moe_algorithmic_bytes(wl, m) for m in range(len(wl.modules))]
+            n_layers = len(per_call) * max(1, int(np.ceil(4 * L2_BYTES / sum(per_call))))
+            bench = MoeBench(wl, n_layers, dev)
+            path = "lora_apply_moe with per-step plans"
+            calls_per_step = len(bench.layers)
+        else:
+            wl = W.config(spec["index"], y_init="normal", sweep=spec.get("sweep", False))
+            path = default_path(wl)
+            wb = 1 if wl.weights == "e4m3" else 2
+            per_call = [algorithmic_bytes(wl.slot_ids, wl.ranks, m.k, m.slice_widths, wb) for m in wl.modules]
+            n_layers = len(per_call) * max(1, int(np.ceil(4 * L2_BYTES / sum(per_call))))
+            bench = ProjectionBench(wl, n_layers, path, dev)
+            path = bench.resolved + (" with per-step plans" if bench.use_plan else "")
+            calls_per_step = len(bench.layers)
+        (elapsed_s, apply_ms, index_ms, clocks, _), steps = _timed(dev, local, bench.index_part, bench.apply_part,
+                                                                   args.config_seconds)
+        err = int(bench.index.err.item())
+        per_layer = [per_call[l % len(per_call)] for l in range(calls_per_step)]
+        call_s = apply_ms / 1e3 / calls_per_step
+        gbs = sum(per_layer) / calls_per_step / call_s / 1e9
+        rec = {
+            "workload": wl.description,
+            "path": path,
+            "calls_per_step": calls_per_step,
+            "steps": steps,
+            "us_per_call": call_s * 1e6,
+            "bytes_per_call": sum(per_layer) / calls_per_step,
+            "tokens_per_call": int(wl.T),
+            "tokens_per_s": wl.T / call_s,
+            "gbs": gbs,
+            "frac": gbs / peak_gbs,
+            "index_and_plans_us": index_ms * 1e3,
+            "clocks": clocks,
+            "device_error": err,
+        }
+        del bench
+        torch.cuda.empty_cache()
+        rec["oracle"] = oracle_rates(wl, seconds=2.0)
+        rec["wall_s"] = round(time.time() - t0, 1)
+        out[name] = rec
+    return out
 
 
 def _oracle_call(wl, rows):
@@ -731,38 +875,78 @@ def _oracle_call(wl, rows):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(wl, seconds: float):
-    """The oracle as it stands, single-threaded, on repeated passes over the
-    batch's rows until about ``seconds`` of CPU work (at least one pass)."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _oracle_rows(wl):
     moe = isinstance(wl, W.MoeWorkload)  # rows are the T*K pairs, T tokens
-    rows = np.arange(wl.T * wl.K if moe else wl.T, dtype=np.int32)
-    done, spent, passes = 0, 0.0, 0
-    while passes == 0 or spent < seconds:
-        spent += _oracle_call(wl, rows)
-        done += wl.T
-        passes += 1
-    return {"value": done / spent, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{passes} passes of the first projection over all {wl.T} tokens "
-                      f"({done} token-calls, {spent:.1f} s, fp64 C oracle, one thread)"}
+    return np.arange(wl.T * wl.K if moe else wl.T, dtype=np.int32), (wl.K if moe else 1)
+
+
+def oracle_rates(wl, seconds: float):
+    """The oracle as it stands on the host: one thread, then every core (the
+    sample's rows split into one chunk per core, run on a thread pool: the C
+    oracle releases the GIL and keeps no state between calls), each the median
+    of three timed passes over a bounded sample of the batch's rows."""
+    import concurrent.futures as cf
+    rows, per_tok = _oracle_rows(wl)
+    cores = host_cores()
+    probe = max(1, min(len(rows), 8))
+    per_row = _oracle_call(wl, rows[:probe]) / probe
+    n = int(max(min(len(rows), cores), min(len(rows), seconds / 6 / max(per_row, 1e-9))))
+    sample = rows[:n]
+
+    def one():
+        return _oracle_call(wl, sample)
+
+    chunks = [c for c in np.array_split(sample, cores) if len(c)]
+    with cf.ThreadPoolExecutor(max_workers=len(chunks)) as ex:
+        def many():
+            t0 = time.perf_counter()
+            list(ex.map(lambda c: _oracle_call(wl, c), chunks))
+            return time.perf_counter() - t0
+        t1 = statistics.median(one() for _ in range(3))
+        tn = statistics.median(many() for _ in range(3))
+    return {"one_core": n / per_tok / t1, "all_cores": n / per_tok / tn, "cores": len(chunks), "unit": "tokens/s",
+            "sample": f"{n} of {len(rows)} rows of the first projection, median of 3 passes per leg"}
+
+
+def cpu_baseline(wl, seconds: float):
+    """The oracle as it stands on the host cores (oracle_rates): the all-core
+    rate is the value, the one-core rate beside it."""
+    r = oracle_rates(wl, seconds)
+    return {"value": r["all_cores"], "unit": "tokens/s", "cores": r["cores"], "kind": "oracle",
+            "one_core": r["one_core"],
+            "sample": r["sample"] + f"; fp64 C oracle on {r['cores']} threads (one core: {r['one_core']:.0f} tokens/s)"}
 
 
 def run_reference(args):
     rank, world, _ = dist_info()
     if rank != 0:
         return None, rank
+    import concurrent.futures as cf
     wl = _workload(args.config, args.requests)
-    per_tok = wl.K if isinstance(wl, W.MoeWorkload) else 1  # MoE rows are (token, choice) pairs
-    rows = np.arange(wl.T * per_tok, dtype=np.int32)
+    rows, per_tok = _oracle_rows(wl)  # MoE rows are (token, choice) pairs
+    cores = host_cores()
     for _ in range(max(args.warmup, 0)):
         _oracle_call(wl, rows[:max(1, len(rows) // 8)])
-    # each step: the branch for one projection call over a bounded sample of rows
+    # each step: the branch for one projection call over a bounded sample of rows,
+    # the rows split over every host core (the C oracle releases the GIL)
     budget_s = 150.0
     per_row = _oracle_call(wl, rows[:8]) / 8
-    n_rows = int(max(1, min(len(rows), budget_s / max(args.steps, 1) / max(per_row, 1e-9))))
+    n_rows = int(max(1, min(len(rows), cores * budget_s / max(args.steps, 1) / max(per_row, 1e-9))))
     sample = rows[:n_rows]
+    chunks = [c for c in np.array_split(sample, cores) if len(c)]
     t = 0.0
-    for _ in range(args.steps):
-        t += _oracle_call(wl, sample)
+    with cf.ThreadPoolExecutor(max_workers=len(chunks)) as ex:
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            list(ex.map(lambda c: _oracle_call(wl, c), chunks))
+            t += time.perf_counter() - t0
     value = n_rows * args.steps / t / per_tok
     out = {
         "metric": metric_name(args.config),
@@ -779,9 +963,9 @@ def run_reference(args):
         "data": "synthetic (seeded: workloads.config)",
         "config": {"workload": workload_name(args.config, wl), "config": args.config},
         "impl": "reference",
-        "cpu_baseline": {"kind": "oracle", "cores": 1, "value": value,
+        "cpu_baseline": {"kind": "oracle", "cores": len(chunks), "value": value,
                          "sample": f"{n_rows} of {len(rows)} rows ({'token-expert pairs' if per_tok > 1 else 'tokens'}) "
-                                   "of the first projection per step"},
+                                   f"of the first projection per step, split over {len(chunks)} threads"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     return out, rank

@@ -225,12 +225,18 @@ lora_status_t lora_set_slot_table(void *dev_table, void *host_staging, int32_t S
 
 /*
  * Slot table with TMA tensor maps, for LORA_PATH_DECODE_TMA: the table of
- * lora_set_slot_table (every path accepts it) followed by, for every slot s
- * with rank r_s > 0 and slice i, a tensor map of A_s,i as [r_s][k] and one of
- * B_s,i as [d_i][r_s] (bf16, 128-byte swizzle), encoded on the host with the
- * driver's cuTensorMapEncodeTiled (no allocation; the CUDA runtime must be able
- * to reach the driver).  The maps are tied to this shape's k and slice widths
- * (a plan built with another shape is refused on the device).
+ * lora_set_slot_table (every path accepts it), aligned to 128 bytes, then a
+ * 128-byte block header, S int32 slot flags (padded to 128 bytes) and eight
+ * 128-byte tensor maps per slot: for a slot s with rank r_s > 0, tensor maps
+ * of A (bf16, 128-byte swizzle, read in k-blocks of 64 columns) and of every
+ * B_s,i as [d_i][r_s], encoded on the host with the driver's
+ * cuTensorMapEncodeTiled (no allocation; the CUDA runtime must be able to
+ * reach the driver).  When the slot's A slices are one packed block
+ * (A_ptrs[s n + i] = A_ptrs[s n] + i r_s k 2 bytes for every i, n r_s <= 256)
+ * the A maps cover all n r_s rows and a stage of k-blocks takes one to four
+ * copies; otherwise each slice has its own map.  The maps are tied to this
+ * shape's k and slice widths (a plan built with another shape is refused on
+ * the device).
  *
  * lora_slot_table_tma_bytes: the table's size for S slots and this shape (0 for
  * a bad shape or S outside [1, LORA_MAX_SLOTS]).

@@ -15,24 +15,30 @@
 //     layer, so their first burst overlaps the previous call's tail.  Only x,
 //     y and the workspace wait for the previous grid.
 //   * Stages of up to 32 KB in a ring of three, one mbarrier each.  A shrink
-//     stage holds, for one slot, one group of its tokens and a run of 64-column
-//     k-blocks, every slice's A rows (TMA 2D boxes of [r][64] bf16, 128-byte
-//     swizzle, one per slice and k-block) and the group's x rows (16-byte
-//     cp.async copies, gathered through sorted_ids by a second warp into the
-//     same swizzled layout).  An expand stage holds a [64 columns][64 ranks]
-//     box of B (ranks past r are the tensor map's zero fill) and the group's y
-//     rows of those 64 columns.
-//   * Four warps run mma.m16n8k16 (bf16, fp32 accumulate) from the staged
-//     tiles with ldmatrix.  The shrink keeps its sums in registers across the
-//     k-blocks of a run and adds them into an fp32 buffer (red.global.add.v2)
-//     once per run; the split over k follows the byte-balanced partition
-//     (TensorRT-LLM LoRA serving page, "路径二:split-K 调优").  A per-slot
-//     counter of finished k-blocks (release / acquire) tells the expand of
-//     that slot, in the same kernel, that its sums are complete; the expand's
-//     B tiles are already streaming meanwhile.
-//   * The expand feeds the fp32 sums to its MMA rounded once to bf16 (2^-9
-//     relative, what serving engines' expand kernels take), accumulates in
-//     fp32 and writes y = bf16(y + s * acc), rounded once.
+//     stage holds, for one slot, one group of its tokens and a run of 64-wide
+//     k-blocks: the group's x rows (16-byte cp.async copies, gathered through
+//     sorted_ids by a second warp into the 128-byte swizzled layout), then
+//     every slice's A rows (TMA 2D boxes of [r][64] bf16, 128-byte swizzle, one
+//     per slice and k-block).  An expand stage holds up to `eu` units of one
+//     slice: [128 columns][rp ranks] boxes of B (rp = the rank rounded up to 16,
+//     32 or 64, with the matching swizzle; ranks past r are the tensor map's
+//     zero fill), then the group's y rows of those columns.
+//   * The 5th-generation tensor cores do the arithmetic (tcgen05.mma, bf16
+//     operands straight from the swizzled stage tiles, fp32 accumulators in
+//     tensor memory), issued by one thread: a shrink run (one slot, one token
+//     group, consecutive k-blocks) accumulates D[128 tokens][n r ranks] over
+//     its stages, each stage released by tcgen05.commit once its MMAs have read
+//     it; at the end of the run four warps read D and add it into an fp32
+//     buffer (red.global.add.v4) - the split over k follows the byte-balanced
+//     partition (TensorRT-LLM LoRA serving page, "路径二:split-K 调优").  A
+//     per-slot counter of finished k-blocks (release / acquire) tells the
+//     expand of that slot, in the same kernel, that its sums are complete; the
+//     expand's B tiles are already streaming meanwhile.
+//   * An expand unit is 128 output columns of one slice: D[128 columns][tokens]
+//     = B box x sums^T, the sums rounded once to bf16 (2^-9 relative, what
+//     serving engines' expand kernels take) in a swizzled tile, two tensor-
+//     memory buffers so that the next unit's MMAs overlap this unit's
+//     epilogue, which writes y = bf16(y + s * acc), rounded once.
 //   * The work of a call is described by a plan built once per batch and
 //     slot table (lora_build_plan(s)): the active slots with their token
 //     groups, and for every CTA its contiguous share of the shrink pieces
@@ -51,35 +57,51 @@
 #include <cuda.h>
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace lora {
 
 // ---------------------------------------------------------------------------
 // Slot table with tensor maps: the ordinary table (TableLayout), then a
-// 128-byte block header {magic, S, n, k, slice offsets}, then for every slot
-// s and slice i two CUtensorMaps of 128 bytes: A_s,i as [r][k] (box [r][64],
-// 128-byte swizzle) and B_s,i as [d_i][r] (box [64][64], 128-byte swizzle,
-// ranks past r zero-filled).
+// 128-byte block header {magic, S, n, k, slice offsets}, per-slot flags, and
+// for every slot eight CUtensorMaps of 128 bytes.  A is read as k-blocks of
+// 64 columns: a map over rows x k viewed as [k / 64][rows][64] (box of `depth`
+// k-blocks x rows x 64, 128-byte swizzle), which lands in shared memory as
+// `depth` consecutive [rows][64] tiles.  When the slot's slices are one
+// packed [n r][k] block (flag kSlotPackedA), maps 0..3 cover all n r rows with
+// depths 1, 2, 4 and 8, so a stage of k-blocks takes one to four copies;
+// otherwise map i covers slice i with depth 1.  Maps 4 + i: B_s,i as [d_i][r]
+// (box [128][rp], rp = r rounded up to 16, 32 or 64 with the 32-, 64- or
+// 128-byte swizzle, ranks past r zero-filled).
 // ---------------------------------------------------------------------------
 constexpr int32_t kTmaTableMagic = 0x4d414d54;
 
+constexpr int32_t kSlotPackedA = 1;
+constexpr int kMapsPerSlot = 8;
+
 struct TmaTableLayout {
-    size_t hdr, maps, bytes;
+    size_t hdr, flags, maps, bytes;
     __host__ __device__ TmaTableLayout(int32_t S, int32_t n) {
+        (void)n;
         hdr = (TableLayout(S, n).bytes + 127) & ~size_t(127);
-        maps = hdr + 128;
-        bytes = maps + size_t(S) * size_t(n) * 256;
+        flags = hdr + 128;
+        maps = flags + ((size_t(S) * 4 + 127) & ~size_t(127));
+        bytes = maps + size_t(S) * kMapsPerSlot * 128;
     }
 };
 
 namespace {
 
-constexpr int kThreads = 192;        // warp 0: TMA, warp 1: row gather, warps 2..5: MMA
+constexpr int kThreads = 192;        // warp 0: TMA, warp 1: row gather, warps 2..5: tensor cores
 constexpr int kMmaThreads = 128;
 constexpr int kStages = 3;
-constexpr int kStageBytes = 32768;
-constexpr int kXaBytes = 64 * 72 * 2;  // expand sums of 64 tokens x (64 + 8) ranks, bf16
+constexpr int kStageBytes = 32768;   // 256 rows of 128 bytes
+constexpr int kXaBytes = 64 * 64 * 2;  // expand sums of up to 64 tokens x 64 ranks, bf16
 constexpr int kSmemBytes = kStages * kStageBytes + kXaBytes + 1024;  // + alignment slack
+constexpr int kTmemCols = 256;       // shrink D (ranks 0..127 at column 0, 128.. at 128), then the expand's
+                                     // two 64-column buffers
+                                     // (two CTAs of 256 columns share an SM's 512)
+constexpr int kUnitCols = 128;       // expand unit: output columns
 constexpr int kMaxGrid = 256;
 constexpr int kMaxRank = 64;
 constexpr int kMaxNR = 192;          // n_slices * r_max
@@ -104,7 +126,8 @@ struct SlotRec {
     int32_t gs, ngs, cs;   // shrink: token group size, groups, k-blocks per stage
     int32_t ge, nge;       // expand: token group size, groups
     int32_t wps, wpe;      // weight of one shrink piece / expand unit (16-byte units)
-    int32_t pad[4];
+    int32_t rp, eu;        // B box width in ranks (16, 32 or 64), expand units per stage
+    int32_t pk, pad;       // A slices packed (one copy per stage covers every slice)
 };
 static_assert(sizeof(SlotRec) == 64, "slot record");
 
@@ -122,14 +145,23 @@ static_assert(sizeof(PlanHdr) + sizeof(CtaRec) * kMaxGrid == 128 + 256 * 32, "pl
 
 __host__ __device__ inline int32_t cdiv(int32_t a, int32_t b) { return (a + b - 1) / b; }
 __host__ __device__ inline int32_t pad16i(int32_t v) { return (v + 15) & ~15; }
+// Rows of an expand unit's y tile in the stage: the group rounded up to 8.
+__host__ __device__ inline int32_t ytile_rows(int32_t gsz) { return (gsz + 7) & ~7; }
+constexpr int32_t kGatherCost = 88;  // a four-row gather's fixed cost beyond its 512 bytes (16-byte units)
+constexpr int32_t kUnitCost = 384;   // an expand unit's fixed cost (16-byte units)
+// Width in ranks of a slot's B boxes (the rank rounded up to 16, 32 or 64;
+// ranks past r are the tensor map's zero fill).
+__host__ __device__ inline int32_t b_box_ranks(int32_t r) { return r <= 16 ? 16 : (r <= 32 ? 32 : 64); }
 
 struct TArgs {
+    // x as [T][k] (box [1][64], 128-byte swizzle) for the four-row gathers
+    CUtensorMap xmap;
     const uint16_t *x;
     int64_t ldx;
     uint16_t *y;
     int64_t ldy;
     const unsigned char *plan;
-    float *acc0, *acc1;        // [n][T][r_max] fp32 sums, set g & 1 this call
+    float *acc0, *acc1;        // [T][n r_max] fp32 sums (token-major), set g & 1 this call
     int32_t *done0, *done1;    // [S] finished k-blocks per slot
     int32_t *gen, *exits;      // call counter, CTAs that finished this call
     int32_t *err;
@@ -162,12 +194,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 // Bounded wait on a phase of a ring barrier; false after kRingLimitNs or once
 // another role has given up (*abort set), which only a broken device causes.
-__device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity, volatile int32_t *abort) {
+// The MMA warps poll without pause (they have nothing else to do and the
+// stage's data is what they wait for); the copy warps, whose waits end when an
+// MMA warp frees a slot, sleep `backoff_ns` between polls so that their
+// spinning takes no issue slots from the MMA warps of their sub-partitions.
+__device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity, volatile int32_t *abort,
+                                          uint32_t backoff_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        for (int i = 0; i < 64; ++i)
+        for (int i = 0; i < 16; ++i) {
             if (mbar_try_wait(bar, parity)) return true;
+            if (backoff_ns) __nanosleep(backoff_ns);
+        }
         if (*abort) return false;
         if (globaltimer_ns() - t0 > kRingLimitNs) {
             *abort = 1;
@@ -175,6 +214,8 @@ __device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity, volatil
         }
     }
 }
+constexpr uint32_t kCopyBackoffNs = 128;
+
 
 // 16 bytes global -> shared through L2, or 16 zero bytes when !valid.
 __device__ __forceinline__ void cp16(uint32_t dst, const void *src, bool valid) {
@@ -186,7 +227,22 @@ __device__ __forceinline__ void cp16(uint32_t dst, const void *src, bool valid) 
 __device__ __forceinline__ void cp_arrive_noinc(uint32_t bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
 }
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ void stg128(void *p, uint4 v) {
+    asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, int32_t x, int32_t y, int32_t z,
+                                            uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+        :: "r"(dst), "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy) : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, int32_t x, int32_t y, uint32_t bar,
                                             uint64_t policy) {
     asm volatile(
@@ -195,50 +251,48 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, int32
         :: "r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar), "l"(policy) : "memory");
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x2(uint32_t &r0, uint32_t &r1, uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
-}
-// Not volatile: the data was published by an mbarrier wait (a volatile asm
-// with a memory clobber) that precedes every use, so the compiler may hoist
-// these loads ahead of the stores that follow them.
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-    uint32_t v;
-    asm("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
-}
 __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared.b32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
 }
-__device__ __forceinline__ void red_v2(float *p, float a, float b) {
-    asm volatile("red.relaxed.gpu.global.add.v2.f32 [%0], {%1,%2};" :: "l"(p), "f"(a), "f"(b) : "memory");
-}
-__device__ __forceinline__ float2 ldcg_f2(const float *p) {
-    float2 v;
-    asm volatile("ld.global.cg.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
-    return v;
-}
-__device__ __forceinline__ void stg32(void *p, uint32_t v) {
-    asm volatile("st.global.b32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
-}
 __device__ __forceinline__ void mma_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Barrier of the four tensor-core warps that also ORs a predicate over them:
+// every decision that changes their control flow goes through it, so that
+// they always meet at the same barriers.
+__device__ __forceinline__ bool mma_any(bool p) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r) : "r"(p ? 1u : 0u) : "memory");
+    return r != 0;
+}
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// Byte offset of 16-byte chunk `ch` of row `row` in a tile of 128-byte rows
-// with the 128-byte swizzle (chunk index XOR row mod 8; tile 1024-aligned).
-__device__ __forceinline__ uint32_t swz(int row, int ch) {
-    return static_cast<uint32_t>(row) * 128u + (static_cast<uint32_t>(ch ^ (row & 7)) << 4);
+// Four rows (token ids rows.x .. rows.w) of a box one row high, stored as
+// four consecutive rows of the box width at dst.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *map, int32_t col, int4 rows, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+        :: "r"(dst), "l"(map), "r"(col), "r"(rows.x), "r"(rows.y), "r"(rows.z), "r"(rows.w), "r"(bar) : "memory");
 }
+// Token ids of rows 4 q .. 4 q + 3 of a group of gsz rows whose ids are in
+// shared memory; rows past the group repeat its last id (those tile rows are
+// never used).
+__device__ __forceinline__ int4 four_ids(const int32_t *ids, int32_t q, int32_t gsz) {
+    const int32_t r = 4 * q;
+    return make_int4(ids[min(r, gsz - 1)], ids[min(r + 1, gsz - 1)], ids[min(r + 2, gsz - 1)],
+                     ids[min(r + 3, gsz - 1)]);
+}
+
+
 
 // ---------------------------------------------------------------------------
 // Walking a CTA's share of the plan
 // ---------------------------------------------------------------------------
 struct Slot {
-    int32_t s, seg0, cnt, r, gs, ngs, cs, ge, nge;
+    int32_t s, seg0, cnt, r, gs, ngs, cs, ge, nge, rp, eu, pk;
     float scale;
 };
 
@@ -248,42 +302,34 @@ struct Slot {
 constexpr int kSlotCache = 32;
 
 __device__ __forceinline__ Slot load_slot(const unsigned char *plan, int32_t a, const int4 *cache, int32_t base) {
-    int4 v0, v1, v2;
+    int4 v[4];
+    const int4 *p = (a >= base && a < base + kSlotCache)
+                        ? cache + 4 * (a - base)
+                        : reinterpret_cast<const int4 *>(plan + plan_slots_off() + size_t(a) * sizeof(SlotRec));
     if (a >= base && a < base + kSlotCache) {
-        const int4 *p = cache + 4 * (a - base);
-        v0 = p[0];
-        v1 = p[1];
-        v2 = p[2];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] = p[q];
     } else {
-        const int4 *p = reinterpret_cast<const int4 *>(plan + plan_slots_off() + size_t(a) * sizeof(SlotRec));
-        v0 = __ldcg(p);
-        v1 = __ldcg(p + 1);
-        v2 = __ldcg(p + 2);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] = __ldcg(p + q);
     }
     Slot s;
-    s.s = v0.x;
-    s.seg0 = v0.y;
-    s.cnt = v0.z;
-    s.r = v0.w;
-    s.scale = __int_as_float(v1.x);
-    s.gs = v1.y;
-    s.ngs = v1.z;
-    s.cs = v1.w;
-    s.ge = v2.x;
-    s.nge = v2.y;
+    s.s = v[0].x;
+    s.seg0 = v[0].y;
+    s.cnt = v[0].z;
+    s.r = v[0].w;
+    s.scale = __int_as_float(v[1].x);
+    s.gs = v[1].y;
+    s.ngs = v[1].z;
+    s.cs = v[1].w;
+    s.ge = v[2].x;
+    s.nge = v[2].y;
+    s.rp = v[3].x;
+    s.eu = v[3].y;
+    s.pk = v[3].z;
     return s;
 }
 
-// A shrink stage: slot tile, token group g, k-blocks [kb, kb + nb); `first`
-// and `last` mark the ends of a run (same tile and group).
-struct SStage {
-    int32_t g, kb, nb;
-};
-
-// An expand unit: token group g, slice i, 64-column block cb of the slice.
-struct EUnit {
-    int32_t g, i, cb;
-};
 
 struct Ctx {
     int32_t T, n, k, r_max, nkb, ublk;
@@ -293,27 +339,12 @@ struct Ctx {
     const unsigned char *maps;
 };
 
-// Token ids of a group of up to 128 rows held by a warp: lane l keeps rows l,
-// l + 32, l + 64 and l + 96; id_of must be called by all 32 lanes with a
-// warp-uniform row >> 5.
-__device__ __forceinline__ void load_ids(const int32_t *ids, int32_t gsz, int32_t lane, int32_t (&idq)[4]) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int32_t r = q * 32 + lane;
-        idq[q] = r < gsz ? __ldcg(ids + r) : 0;
-    }
-}
-__device__ __forceinline__ int32_t id_of(const int32_t (&idq)[4], int32_t row) {
-    const int32_t q = row >> 5;
-    const int32_t v = q == 0 ? idq[0] : (q == 1 ? idq[1] : (q == 2 ? idq[2] : idq[3]));
-    return __shfl_sync(0xffffffffu, v, row & 31);
-}
 
 // Expand unit u (0 <= u < ublk) of a token group -> slice and column block.
 __device__ __forceinline__ void unit_slice(const Ctx &C, int32_t u, int32_t &i, int32_t &cb) {
     i = 0;
     while (true) {
-        const int32_t nb = cdiv(C.off[i + 1] - C.off[i], 64);
+        const int32_t nb = cdiv(C.off[i + 1] - C.off[i], kUnitCols);
         if (u < nb || i + 1 >= C.n) break;
         u -= nb;
         ++i;
@@ -322,146 +353,111 @@ __device__ __forceinline__ void unit_slice(const Ctx &C, int32_t u, int32_t &i, 
 }
 
 // ---------------------------------------------------------------------------
-// MMA roles
+// Tensor-core roles (tcgen05; warp 2 lane 0 issues, warps 2..5 read results)
 // ---------------------------------------------------------------------------
-// One shrink run (slot tile, token group g, run_len k-blocks): consumes its
-// stages from the ring, keeps the sums in registers and adds them into the
-// call's fp32 buffer at the end.  The M tiles (16 tokens) x N tiles (8 ranks)
-// of the run are spread over the four warps as a WM x WN grid, WM the
-// smallest of 1, 2, 4 that leaves each warp at most MTW M tiles: warp w takes
-// M tiles w % WM + WM i and N tiles w / WM + WN j.
-constexpr int kMTW = 2, kNTW = 12;
+__device__ __forceinline__ void red_f32(float *p, float v) {
+    asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" :: "l"(p), "f"(v) : "memory");
+}
+// Adds v to a per-slot counter with release semantics: the sums this CTA
+// added before (ordered by the barrier that precedes the call) are visible to
+// whoever acquires the new count.
+__device__ __forceinline__ void red_release_add(int32_t *p, int32_t v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
 
-__device__ __forceinline__ void shrink_run(const Ctx &C, const Slot &sl, int32_t g, int32_t run_len, uint32_t &c,
-                                           uint32_t ring, uint32_t bars, float *acc_buf, volatile int32_t *abort,
-                                           int32_t mw, int32_t lane) {
-    const int32_t nr = C.n * sl.r, ntt = nr >> 3;
-    const int32_t gsz = min(sl.gs, sl.cnt - g * sl.gs), gpad = pad16i(gsz), mtc = gpad >> 4;
-    const int32_t WM = mtc <= 2 ? 1 : (mtc <= 4 ? 2 : 4), WN = 4 / WM;
-    const int32_t wm = mw % WM, wn = mw / WM;
-    float acc[kMTW][kNTW][4];
+// Issues one shrink stage.  The stage holds the A rows of its nb k-blocks
+// (nb * nr rows) and then their x tiles (nb * gpad rows), both K-major with the
+// 128-byte swizzle; ranks go to tensor-memory lanes, tokens to columns.
+//   n r <= 128: one MMA per K=16 step covers every k-block of the stage:
+//     D[(kbl, rank)][(kbl', token)] (+)= A rows . x rows over the step's 16
+//     columns of each row's own block; only the diagonal blocks kbl = kbl'
+//     are products of matching columns, and the epilogue reads just those
+//     (the plan keeps nb * nr <= 128 and nb * gpad <= 256).  Four MMAs per
+//     stage however many k-blocks it holds.
+//   n r > 128 (nb = 1): ranks 0..127 into columns 0.., ranks 128.. into
+//     columns 128.. (a second MMA per step).
+// `first`: the run's first stage, whose first step overwrites D.
+__device__ __forceinline__ void shrink_mma_stage(uint32_t tmem, uint32_t sbase, int32_t nb, int32_t gpad, int32_t nr,
+                                                 bool first) {
+    const uint32_t xa = sbase + static_cast<uint32_t>(nb * nr) * 128u;
+    const uint32_t idesc = tc::idesc_bf16(128, nb * gpad);
 #pragma unroll
-    for (int im = 0; im < kMTW; ++im)
-#pragma unroll
-        for (int in = 0; in < kNTW; ++in)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[im][in][e] = 0.f;
-    int32_t done_pieces = 0;
-    while (done_pieces < run_len) {
-        const int32_t nb = min(sl.cs, run_len - done_pieces);
-        const uint32_t st = c % kStages;
-        const bool ok = ring_wait(bars + 8 * st, (c / kStages) & 1, abort);
-        if (ok) {
-            const uint32_t sbase = ring + st * kStageBytes;
-            const uint32_t xoff = static_cast<uint32_t>(nb * nr) * 128u;
-            for (int32_t kbl = 0; kbl < nb; ++kbl) {
-                const uint32_t abase = sbase + static_cast<uint32_t>(kbl * nr) * 128u;
-                const uint32_t xbase = sbase + xoff + static_cast<uint32_t>(kbl * gpad) * 128u;
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    uint32_t af[kMTW][4];
-#pragma unroll
-                    for (int im = 0; im < kMTW; ++im) {
-                        const int32_t mt = wm + WM * im;
-                        if (mt < mtc) ldsm_x4(af[im], xbase + swz(mt * 16 + (lane & 15), 2 * ks + (lane >> 4)));
-                    }
-#pragma unroll
-                    for (int in = 0; in < kNTW; ++in) {
-                        const int32_t nt = wn + WN * in;
-                        if (nt < ntt) {
-                            uint32_t b0, b1;
-                            ldsm_x2(b0, b1, abase + swz(nt * 8 + (lane & 7), 2 * ks + ((lane >> 3) & 1)));
-#pragma unroll
-                            for (int im = 0; im < kMTW; ++im)
-                                if (wm + WM * im < mtc)
-                                    mma_bf16_16816(acc[im][in], af[im][0], af[im][1], af[im][2], af[im][3], b0, b1);
-                        }
-                    }
-                }
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars + 8 * (kStages + st));
-        ++c;
-        done_pieces += nb;
-        if (!ok) return;
+    for (int kk = 0; kk < 4; ++kk) {
+        const bool acc = !(first && kk == 0);
+        const uint64_t xd = tc::smem_desc(xa + 32 * kk, 1024, tc::kLayoutSW128);
+        tc::mma_bf16(tmem, tc::smem_desc(sbase + 32 * kk, 1024, tc::kLayoutSW128), xd, idesc, acc);
+        if (nr > 128)
+            tc::mma_bf16(tmem + 128, tc::smem_desc(sbase + 128 * 128 + 32 * kk, 1024, tc::kLayoutSW128), xd, idesc,
+                         acc);
     }
-    // sums of this run -> acc_buf[i][p][j]
-    const int32_t gq = lane >> 2, q = lane & 3;
-    const int32_t p0 = sl.seg0 + g * sl.gs;
+}
+
+// Reads the run's D from tensor memory and adds it into the call's fp32 sums
+// acc_buf[p][i * r_max + j].  This warp's 32 lanes are D rows lane_base +
+// lane: for n r <= 128 row (kbl, rank) of the nbr k-blocks the run's stages
+// held, whose tokens sit in columns kbl * gpad..; for n r > 128 rank
+// 128 d + row of D_d.  Lanes holding the same rank for different k-blocks add
+// into the same sums; a warp's adds for one token cover consecutive ranks.
+__device__ __forceinline__ void shrink_epilogue(const Ctx &C, const Slot &sl, int32_t p0, int32_t gsz, int32_t gpad,
+                                                int32_t nbr, uint32_t tmem, int32_t lane_base, int32_t lane,
+                                                float *acc_buf) {
+    const int32_t nr = C.n * sl.r, NC = C.n * C.r_max;
+    const int32_t nd = nr > 128 ? 2 : 1, rows = nr > 128 ? nr : nbr * nr;
+    for (int32_t d = 0; d < nd; ++d) {
+        const int32_t row0 = 128 * d + lane_base;  // warp-uniform
+        if (row0 >= rows) continue;
+        const int32_t row = row0 + lane, kbl = nd == 2 ? 0 : row / nr, rank = nd == 2 ? row : row - kbl * nr;
+        const int32_t i = rank / sl.r, j = rank - i * sl.r;
+        const bool rv = row < rows;
+        float *dst = acc_buf + static_cast<size_t>(p0) * NC + i * C.r_max + j;
+        // the k-blocks whose rows this warp holds
+        const int32_t kb0 = nd == 2 ? 0 : row0 / nr, kb1 = nd == 2 ? 0 : min(row0 + 31, rows - 1) / nr;
+        for (int32_t kc = kb0; kc <= kb1; ++kc) {
+            const bool mine = rv && kbl == kc;
+            for (int32_t t0 = 0; t0 < gpad; t0 += 16) {
+                uint32_t r[16];
+                tc::tmem_ld16(tmem + (static_cast<uint32_t>(lane_base) << 16) +
+                                  static_cast<uint32_t>(128 * d + kc * gpad + t0),
+                              r);
+                if (mine) {
 #pragma unroll
-    for (int im = 0; im < kMTW; ++im) {
-        const int32_t mt = wm + WM * im;
-        if (mt >= mtc) continue;
-#pragma unroll
-        for (int in = 0; in < kNTW; ++in) {
-            const int32_t nt = wn + WN * in;
-            if (nt >= ntt) continue;
-            const int32_t col = nt * 8 + 2 * q;
-            const int32_t i = col / sl.r, j = col - i * sl.r;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int32_t tok = mt * 16 + gq + 8 * h;
-                if (tok < gsz)
-                    red_v2(acc_buf + (static_cast<size_t>(i) * C.T + p0 + tok) * C.r_max + j, acc[im][in][2 * h],
-                           acc[im][in][2 * h + 1]);
+                    for (int e = 0; e < 16; ++e)
+                        if (t0 + e < gsz) red_f32(dst + static_cast<size_t>(t0 + e) * NC, __uint_as_float(r[e]));
+                }
             }
         }
     }
 }
 
-// One expand unit from the ring: y rows of token group g (gsz tokens from
-// sorted position p0), slice i, columns [cb * 64, cb * 64 + 64) of the slice;
-// the sums are in the xa buffer (bf16, row stride xs elements).
-__device__ __forceinline__ void expand_unit(const Ctx &C, const Slot &sl, const int32_t *rows, int32_t gsz,
-                                            int32_t i, int32_t cb, uint32_t sbase, uint32_t xbuf, int32_t xs,
-                                            uint16_t *y, int64_t ldy, int32_t mw, int32_t lane) {
-    const int32_t mtc = pad16i(gsz) >> 4, ksteps = pad16i(sl.r) >> 4;
-    const uint32_t bbase = sbase, ybase = sbase + 8192;
-    float acc[4][2][4];
+// Issues one expand unit: D[128 columns][gpad tokens] = B box [128][rp] x
+// sums [gpad][rp]^T over the rank padded to 16 (K-major, swizzle by rp).
+__device__ __forceinline__ void expand_mma_unit(uint32_t tmem_d, uint32_t bbox, uint32_t xbuf, int32_t rp, int32_t r,
+                                                uint32_t idesc) {
+    const uint32_t layout = tc::layout_for_rowb(static_cast<uint32_t>(rp * 2));
+    const uint32_t sbo = static_cast<uint32_t>(16 * rp);  // 8 rows of rp ranks
+    const int32_t ksteps = pad16i(r) >> 4;
+    for (int32_t kk = 0; kk < ksteps; ++kk)
+        tc::mma_bf16(tmem_d, tc::smem_desc(bbox + 32 * kk, sbo, layout), tc::smem_desc(xbuf + 32 * kk, sbo, layout),
+                     idesc, kk > 0);
+}
+
+// One expand unit's epilogue, in shared memory: this warp's 32 lanes are
+// output columns lane_base + lane of the unit; the y tile ([yrows][128] bf16,
+// 256-byte rows) becomes y + s * acc rounded once to bf16, in place.  The rows
+// go to global memory afterwards.
+__device__ __forceinline__ void expand_epilogue(float scale, int32_t yrows, uint32_t tmem_d, unsigned char *ytile,
+                                                int32_t lane_base, int32_t lane) {
+    uint16_t *yc = reinterpret_cast<uint16_t *>(ytile) + lane_base + lane;
+    for (int32_t t0 = 0; t0 < yrows; t0 += 16) {
+        uint32_t r[16];
+        tc::tmem_ld16(tmem_d + (static_cast<uint32_t>(lane_base) << 16) + static_cast<uint32_t>(t0), r);
+        uint16_t yo[16];
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
+        for (int e = 0; e < 16; ++e) yo[e] = t0 + e < yrows ? yc[(t0 + e) * kUnitCols] : 0;
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[mt][t][e] = 0.f;
-    for (int32_t ks = 0; ks < ksteps; ++ks) {
-        uint32_t af[4][4];
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt)
-            if (mt < mtc)
-                ldsm_x4(af[mt], xbuf + static_cast<uint32_t>((mt * 16 + (lane & 15)) * xs * 2) +
-                                    static_cast<uint32_t>((2 * ks + (lane >> 4)) * 16));
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            const int32_t nt = 2 * mw + t;
-            uint32_t b0, b1;
-            ldsm_x2(b0, b1, bbase + swz(nt * 8 + (lane & 7), 2 * ks + ((lane >> 3) & 1)));
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt)
-                if (mt < mtc) mma_bf16_16816(acc[mt][t], af[mt][0], af[mt][1], af[mt][2], af[mt][3], b0, b1);
-        }
-    }
-    const int32_t gq = lane >> 2, q = lane & 3;
-    const int32_t di = C.off[i + 1] - C.off[i];
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-        if (mt >= mtc) continue;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int32_t tok = mt * 16 + gq + 8 * h;
-            if (tok >= gsz) continue;
-            const int64_t row = rows[tok];
-            uint16_t *yrow = y + row * ldy + C.off[i] + cb * 64;
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const int32_t cl = (2 * mw + t) * 8 + 2 * q;
-                if (cb * 64 + cl >= di) continue;
-                const uint32_t yv = lds32(ybase + swz(tok, cl >> 3) + static_cast<uint32_t>((cl & 7) * 2));
-                const float f0 = bf16lo_to_f32(yv) + sl.scale * acc[mt][t][2 * h];
-                const float f1 = bf16hi_to_f32(yv) + sl.scale * acc[mt][t][2 * h + 1];
-                stg32(yrow + cl, pack_bf16x2(f0, f1));
-            }
+        for (int e = 0; e < 16; ++e) {
+            const float v = bf16lo_to_f32(yo[e]) + scale * __uint_as_float(r[e]);
+            if (t0 + e < yrows) yc[(t0 + e) * kUnitCols] = static_cast<uint16_t>(pack_bf16x2(v, 0.f));
         }
     }
 }
@@ -469,11 +465,14 @@ __device__ __forceinline__ void expand_unit(const Ctx &C, const Slot &sl, const 
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(TArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(const __grid_constant__ TArgs a) {
     extern __shared__ unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t bars[2 * kStages];  // full[kStages], then empty[kStages]
+    // full[kStages], empty[kStages], run_done, acc_full
+    __shared__ __align__(8) uint64_t bars[2 * kStages + 2];
     __shared__ int32_t s_abort, s_flag;
-    __shared__ int32_t s_rows[kGe];                      // token ids of the expand run's group
+    __shared__ uint32_t s_tmem;
+    __shared__ int32_t s_rows[kGe];                      // token ids of the expand run's group (tensor-core warps)
+    __shared__ int32_t s_xids[128];                      // token ids of the gather warp's current group
     __shared__ int4 s_slots[4 * kSlotCache];              // slot records of tiles [slot_base, + kSlotCache)
 
     pdl_launch_dependents();
@@ -481,6 +480,10 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(TArgs a) {
     const int4 h0 = __ldcg(reinterpret_cast<const int4 *>(H)), h1 = __ldcg(reinterpret_cast<const int4 *>(H) + 1);
     const int4 h2 = __ldcg(reinterpret_cast<const int4 *>(H) + 2), h3 = __ldcg(reinterpret_cast<const int4 *>(H) + 3);
     const uint64_t table = __ldcg(&H->table);
+    // the CTA's record in the same round trip (a plan buffer is at least
+    // tma_plan_size(T, S) bytes, so the read is in bounds whatever it holds)
+    const CtaRec *cr = reinterpret_cast<const CtaRec *>(a.plan + plan_ctas_off(a.S)) + blockIdx.x;
+    const int4 crs = __ldcg(reinterpret_cast<const int4 *>(cr)), cre = __ldcg(reinterpret_cast<const int4 *>(cr) + 1);
     // h0 = magic, T, S, n; h1 = k, r_max, na, grid; h2 = off[0..3]; h3 = off[4], nkb, ublk, pad
     bool valid = h0.x == kPlanMagic && h0.y == a.T && h0.z == a.S && h0.w == a.n && h1.x == a.k &&
                  h1.y == a.r_max && h1.w == static_cast<int32_t>(gridDim.x) && table != 0;
@@ -505,9 +508,9 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(TArgs a) {
     const uint32_t ring = (sa(smem_raw) + 1023u) & ~1023u;
     const uint32_t xbuf = ring + kStages * kStageBytes;
     const uint32_t bar0 = sa(&bars[0]);  // full[st] at bar0 + 8 st, empty[st] at bar0 + 8 (kStages + st)
-    const CtaRec *cr = reinterpret_cast<const CtaRec *>(a.plan + plan_ctas_off(a.S)) + blockIdx.x;
-    const int4 crs = __ldcg(reinterpret_cast<const int4 *>(cr)), cre = __ldcg(reinterpret_cast<const int4 *>(cr) + 1);
+    const uint32_t bar_done = bar0 + 8 * (2 * kStages), bar_acc = bar_done + 8;
     const int32_t slot_base = min(crs.x, cre.x);
+    const int32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     {
         const int32_t na = h1.z;
         const int32_t e = threadIdx.x;  // 128 int4: four per cached record
@@ -517,15 +520,19 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(TArgs a) {
     }
     if (threadIdx.x == 0) {
         for (int st = 0; st < kStages; ++st) {
-            mbar_init(bar0 + 8 * st, 1 + 32);         // producer's expect_tx + 32 gather lanes
-            mbar_init(bar0 + 8 * (kStages + st), 4);  // one arrival per MMA warp
+            mbar_init(bar0 + 8 * st, 1 + 32);         // the producer's expect_tx + the 32 gather lanes
+            mbar_init(bar0 + 8 * (kStages + st), 1);  // a tcgen05.commit, or the expand's last epilogue
         }
+        mbar_init(bar_done, 1);
+        mbar_init(bar_acc, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_abort = 0;
     }
+    if (warp == 2) tc::tmem_alloc(&s_tmem, kTmemCols);  // whole warp
+    tc::fence_before_sync();
     __syncthreads();
-
-    const int32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    tc::fence_after_sync();
+    const uint32_t tmem = s_tmem;
     volatile int32_t *abort = &s_abort;
 
     if (warp == 0) {
@@ -541,17 +548,31 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(TArgs a) {
                     sl = load_slot(C.plan, tile, s_slots, slot_base);
                     cur = tile;
                 }
-                const int32_t kb = idx % C.nkb;
+                const int32_t g = idx / C.nkb, kb = idx % C.nkb;
                 const int32_t nb = min(min(sl.cs, C.nkb - kb), left);
+                const int32_t gpad = pad16i(min(sl.gs, sl.cnt - g * sl.gs));
                 const uint32_t st = c % kStages;
-                if (c >= kStages && !ring_wait(bar0 + 8 * (kStages + st), ((c / kStages) + 1) & 1, abort)) break;
-                const uint32_t full = bar0 + 8 * st, dst = ring + st * kStageBytes;
+                if (c >= kStages && !ring_wait(bar0 + 8 * (kStages + st), ((c / kStages) + 1) & 1, abort, kCopyBackoffNs))
+                    break;
+                const uint32_t full = bar0 + 8 * st;
+                const uint32_t dst = ring + st * kStageBytes;  // the A rows open the stage
                 mbar_expect_tx(full, static_cast<uint32_t>(nb * C.n * sl.r) * 128u);
-                for (int32_t kbl = 0; kbl < nb; ++kbl)
-                    for (int32_t i = 0; i < C.n; ++i)
-                        tma_load_2d(dst + static_cast<uint32_t>((kbl * C.n + i) * sl.r) * 128u,
-                                    C.maps + (static_cast<size_t>(sl.s) * C.n + i) * 256, (kb + kbl) * 64, 0, full,
-                                    policy);
+                const unsigned char *am = C.maps + static_cast<size_t>(sl.s) * (kMapsPerSlot * 128);
+                if (sl.pk) {
+                    // packed slices: blocks of depth 8, 4, 2, 1 (one copy each)
+                    const int32_t nr = C.n * sl.r;
+                    for (int32_t kbl = 0, d = 3; d >= 0; --d)
+                        if (nb & (1 << d)) {
+                            tma_load_3d(dst + static_cast<uint32_t>(kbl * nr) * 128u, am + d * 128, 0, 0, kb + kbl, full,
+                                        policy);
+                            kbl += 1 << d;
+                        }
+                } else {
+                    for (int32_t kbl = 0; kbl < nb; ++kbl)
+                        for (int32_t i = 0; i < C.n; ++i)
+                            tma_load_3d(dst + static_cast<uint32_t>((kbl * C.n + i) * sl.r) * 128u, am + i * 128, 0, 0,
+                                        kb + kbl, full, policy);
+                }
                 ++c;
                 idx += nb;
                 left -= nb;
@@ -571,15 +592,20 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(TArgs a) {
                 }
                 int32_t i, cb;
                 unit_slice(C, idx % C.ublk, i, cb);
+                const int32_t m = min(sl.eu, min(cdiv(C.off[i + 1] - C.off[i], kUnitCols) - cb, left));
                 const uint32_t st = c % kStages;
-                if (c >= kStages && !ring_wait(bar0 + 8 * (kStages + st), ((c / kStages) + 1) & 1, abort)) break;
-                const uint32_t full = bar0 + 8 * st;
-                mbar_expect_tx(full, 8192u);
-                tma_load_2d(ring + st * kStageBytes, C.maps + (static_cast<size_t>(sl.s) * C.n + i) * 256 + 128, 0,
-                            cb * 64, full, policy);
+                if (c >= kStages && !ring_wait(bar0 + 8 * (kStages + st), ((c / kStages) + 1) & 1, abort, kCopyBackoffNs))
+                    break;
+                const uint32_t full = bar0 + 8 * st, bbox = static_cast<uint32_t>(kUnitCols * sl.rp * 2);
+                mbar_expect_tx(full, static_cast<uint32_t>(m) * bbox);
+                for (int32_t u = 0; u < m; ++u)
+                    tma_load_2d(ring + st * kStageBytes + u * bbox,
+                                C.maps + static_cast<size_t>(sl.s) * (kMapsPerSlot * 128) + (4 + i) * 128, 0,
+                                (cb + u) * kUnitCols,
+                                full, policy);
                 ++c;
-                ++idx;
-                --left;
+                idx += m;
+                left -= m;
                 if (idx == sl.nge * C.ublk) {
                     ++tile;
                     idx = 0;
@@ -587,15 +613,14 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(TArgs a) {
             }
         }
     } else if (warp == 1) {
-        // ---- row gather: x rows of shrink stages, y rows of expand units.  The
-        // ids of the current token group stay in registers (lane l: rows l + 32 q),
-        // so a stage issues its copies without waiting on any global load.
+        // ---- row gathers through the tensor maps of x and y, four token rows
+        // per copy (lane l copies rows 4 l .. 4 l + 3 of the group); the ids of
+        // the current group are staged in shared memory
         pdl_wait();
         uint32_t c = 0;
         int32_t tile = crs.x, idx = crs.y, left = crs.z, cur = -1, cur_g = -1;
-        int32_t idq[4] = {0, 0, 0, 0};
         Slot sl{};
-        while (left > 0 && !*abort) {
+        while (left > 0 && !__any_sync(0xffffffffu, *abort != 0)) {
             if (tile != cur) {
                 sl = load_slot(C.plan, tile, s_slots, slot_base);
                 cur = tile;
@@ -603,23 +628,31 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(TArgs a) {
             }
             const int32_t g = idx / C.nkb, kb = idx % C.nkb;
             const int32_t nb = min(min(sl.cs, C.nkb - kb), left);
-            const int32_t gsz = min(sl.gs, sl.cnt - g * sl.gs), gpad = pad16i(gsz);
+            const int32_t gsz = min(sl.gs, sl.cnt - g * sl.gs), gpad = pad16i(gsz), nq = (gsz + 3) >> 2;
             if (g != cur_g) {
-                load_ids(C.ids + sl.seg0 + g * sl.gs, gsz, lane, idq);
+                __syncwarp();
+                for (int32_t r = lane; r < gsz; r += 32) s_xids[r] = __ldcg(C.ids + sl.seg0 + g * sl.gs + r);
+                __syncwarp();
                 cur_g = g;
             }
             const uint32_t st = c % kStages;
-            if (c >= kStages && !ring_wait(bar0 + 8 * (kStages + st), ((c / kStages) + 1) & 1, abort)) break;
-            const uint32_t xdst = ring + st * kStageBytes + static_cast<uint32_t>(nb * C.n * sl.r) * 128u;
-            const int32_t per_kb = gpad * 8;  // a multiple of 128: a warp's 32 elements share kbl and row >> 5
-            for (int32_t e0 = 0; e0 < nb * per_kb; e0 += 32) {
-                const int32_t e = e0 + lane;
-                const int32_t kbl = e / per_kb, rem = e - kbl * per_kb, row = rem >> 3, ch = rem & 7;
-                const int64_t tok = id_of(idq, row);
-                cp16(xdst + static_cast<uint32_t>(kbl * gpad) * 128u + swz(row, ch),
-                     a.x + tok * a.ldx + (kb + kbl) * 64 + ch * 8, row < gsz);
+            const bool free_ = c < kStages || ring_wait(bar0 + 8 * (kStages + st), ((c / kStages) + 1) & 1, abort,
+                                                        kCopyBackoffNs);
+            if (__any_sync(0xffffffffu, !free_)) break;
+            const uint32_t full = bar0 + 8 * st;
+            if (lane == 0)
+                mbar_expect_tx(full, static_cast<uint32_t>(nb * nq) * 512u);
+            else
+                mbar_arrive(full);
+            __syncwarp();
+            if (lane < nq) {
+                // x rows after the stage's A rows: [nb][gpad][64] bf16, 128-byte swizzle
+                const int4 rows = four_ids(s_xids, lane, gsz);
+                const uint32_t xdst = ring + st * kStageBytes + static_cast<uint32_t>(nb * sl.r * C.n) * 128u +
+                                      static_cast<uint32_t>(lane) * 512u;
+                for (int32_t kbl = 0; kbl < nb; ++kbl)
+                    tma_gather4(xdst + static_cast<uint32_t>(kbl * gpad) * 128u, &a.xmap, (kb + kbl) * 64, rows, full);
             }
-            cp_arrive_noinc(bar0 + 8 * st);
             ++c;
             idx += nb;
             left -= nb;
@@ -633,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(TArgs a) {
         left = cre.z;
         cur = -1;
         cur_g = -1;
-        while (left > 0 && !*abort) {
+        while (left > 0 && !__any_sync(0xffffffffu, *abort != 0)) {
             if (tile != cur) {
                 sl = load_slot(C.plan, tile, s_slots, slot_base);
                 cur = tile;
@@ -642,27 +675,34 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(TArgs a) {
             const int32_t g = idx / C.ublk;
             int32_t i, cb;
             unit_slice(C, idx % C.ublk, i, cb);
-            const int32_t gsz = min(sl.ge, sl.cnt - g * sl.ge), gpad = pad16i(gsz);
+            const int32_t gsz = min(sl.ge, sl.cnt - g * sl.ge);
             if (g != cur_g) {
-                load_ids(C.ids + sl.seg0 + g * sl.ge, gsz, lane, idq);
+                __syncwarp();
+                for (int32_t r = lane; r < gsz; r += 32) s_xids[r] = __ldcg(C.ids + sl.seg0 + g * sl.ge + r);
+                __syncwarp();
                 cur_g = g;
             }
             const int32_t di = C.off[i + 1] - C.off[i];
+            const int32_t m = min(sl.eu, min(cdiv(di, kUnitCols) - cb, left));
             const uint32_t st = c % kStages;
-            if (c >= kStages && !ring_wait(bar0 + 8 * (kStages + st), ((c / kStages) + 1) & 1, abort)) break;
-            const uint32_t ydst = ring + st * kStageBytes + 8192u;
-            for (int32_t e0 = 0; e0 < gpad * 8; e0 += 32) {
-                const int32_t e = e0 + lane;
-                const int32_t row = e >> 3, ch = e & 7;
-                const int32_t col = cb * 64 + ch * 8;
-                const bool v = row < gsz && col < di;
-                const int64_t tok = id_of(idq, row);
-                cp16(ydst + swz(row, ch), a.y + tok * a.ldy + C.off[i] + (v ? col : 0), v);
-            }
+            const bool free_ = c < kStages || ring_wait(bar0 + 8 * (kStages + st), ((c / kStages) + 1) & 1, abort,
+                                                        kCopyBackoffNs);
+            if (__any_sync(0xffffffffu, !free_)) break;
+            // y rows after the m B boxes: [m][gsz rounded to 8][128] bf16, 256-byte rows, 16-byte
+            // copies (a warp's 32 copies cover two rows); rows past the group are zeros
+            const uint32_t ydst = ring + st * kStageBytes + static_cast<uint32_t>(m * kUnitCols * sl.rp * 2);
+            const int32_t yrows = ytile_rows(gsz);
+            for (int32_t u = 0; u < m; ++u)
+                for (int32_t e = lane; e < yrows * 16; e += 32) {
+                    const int32_t row = e >> 4, ch = e & 15, col = (cb + u) * kUnitCols + ch * 8;
+                    const bool v = row < gsz && col < di;
+                    cp16(ydst + static_cast<uint32_t>(u * yrows * 256 + e * 16),
+                         a.y + static_cast<int64_t>(s_xids[v ? row : 0]) * a.ldy + C.off[i] + (v ? col : 0), v);
+                }
             cp_arrive_noinc(bar0 + 8 * st);
             ++c;
-            ++idx;
-            --left;
+            idx += m;
+            left -= m;
             if (idx == sl.nge * C.ublk) {
                 ++tile;
                 idx = 0;
@@ -670,9 +710,11 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(TArgs a) {
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
     } else {
-        // ---- MMA warps
+        // ---- tensor-core group: warps 2..5 (warp w reads tensor-memory lanes
+        // 32 (w % 4) ..); warp 2 lane 0 issues every tcgen05 instruction
         pdl_wait();
-        const int32_t mw = warp - 2, mtid = threadIdx.x - 64;
+        const int32_t mtid = threadIdx.x - 64, lane_base = 32 * (warp & 3);
+        const bool issuer = warp == 2 && lane == 0;
         const int32_t gen = __ldcg(a.gen);
         float *acc_buf = (gen & 1) ? a.acc1 : a.acc0;
         int32_t *done = (gen & 1) ? a.done1 : a.done0;
@@ -687,18 +729,45 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(TArgs a) {
                 reinterpret_cast<float4 *>(other)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int32_t s = blockIdx.x * kMmaThreads + mtid; s < a.S; s += gridDim.x * kMmaThreads) odone[s] = 0;
         }
-        uint32_t c = 0;
+        uint32_t c = 0, runs = 0, units = 0;
+        bool fail = false;  // the same in all four warps: every change of it goes through mma_any
         int32_t tile = crs.x, idx = crs.y, left = crs.z;
-        while (left > 0 && !*abort) {
+        while (left > 0 && !fail) {
             const Slot sl = load_slot(C.plan, tile, s_slots, slot_base);
             const int32_t g = idx / C.nkb, kb = idx % C.nkb;
             const int32_t run_len = min(C.nkb - kb, left);
-            shrink_run(C, sl, g, run_len, c, ring, bar0, acc_buf, abort, mw, lane);
-            mma_barrier();  // every warp's sums of the run are issued
-            if (mtid == 0) {
-                __threadfence();
-                atomicAdd(done + sl.s, run_len);
+            const int32_t nr = C.n * sl.r, gsz = min(sl.gs, sl.cnt - g * sl.gs), gpad = pad16i(gsz);
+            const int32_t nst = cdiv(run_len, sl.cs);  // the run's stages (the copy warps split it the same way)
+            bool bad = false;
+            if (issuer) {
+                for (int32_t q = 0, dp = 0; q < nst; ++q) {
+                    const int32_t nb = min(sl.cs, run_len - dp);
+                    const uint32_t st = (c + q) % kStages;
+                    if (!ring_wait(bar0 + 8 * st, ((c + q) / kStages) & 1, abort)) {
+                        bad = true;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    shrink_mma_stage(tmem, ring + st * kStageBytes, nb, gpad, nr, q == 0);
+                    tc::mma_commit(reinterpret_cast<uint64_t *>(&bars[kStages + st]));  // frees the stage
+                    dp += nb;
+                }
+                tc::mma_commit(reinterpret_cast<uint64_t *>(&bars[2 * kStages]));  // the run's D is complete
             }
+            __syncwarp();
+            c += nst;
+            const bool got = __all_sync(0xffffffffu, ring_wait(bar_done, runs & 1, abort));  // tcgen05.ld: whole warps
+            ++runs;
+            if (got) {
+                tc::fence_after_sync();
+                shrink_epilogue(C, sl, sl.seg0 + g * sl.gs, gsz, gpad, min(sl.cs, run_len), tmem, lane_base, lane,
+                                acc_buf);
+            }
+            tc::fence_before_sync();
+            // every warp's sums of the run are issued and D may be overwritten
+            fail = mma_any(bad || !got);
+            if (fail) break;
+            if (mtid == 0) red_release_add(done + sl.s, run_len);
             idx += run_len;
             left -= run_len;
             if (idx == sl.ngs * C.nkb) {
@@ -709,21 +778,21 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(TArgs a) {
         tile = cre.x;
         idx = cre.y;
         left = cre.z;
-        while (left > 0 && !*abort) {
+        while (left > 0 && !fail) {
             const Slot sl = load_slot(C.plan, tile, s_slots, slot_base);
             const int32_t g = idx / C.ublk;
             int32_t i, cb;
             unit_slice(C, idx % C.ublk, i, cb);
-            const int32_t blocks_i = cdiv(C.off[i + 1] - C.off[i], 64);
+            const int32_t blocks_i = cdiv(C.off[i + 1] - C.off[i], kUnitCols);
             const int32_t run_len = min(blocks_i - cb, left);
             const int32_t gsz = min(sl.ge, sl.cnt - g * sl.ge), gpad = pad16i(gsz);
             const int32_t p0 = sl.seg0 + g * sl.ge;
-            const int32_t r16 = pad16i(sl.r), xs = r16 + 8;
+            const int32_t r16 = pad16i(sl.r), rp = sl.rp;
             // the slot's sums are complete once every k-block of every group is in
             if (mtid == 0) {
                 const int32_t need = sl.ngs * C.nkb;
-                int32_t ok = 1;
-                if (ld_acquire(done + sl.s) < need) {
+                int32_t ok = *abort ? -1 : 1;
+                if (ok > 0 && ld_acquire(done + sl.s) < need) {
                     const uint64_t t0 = globaltimer_ns();
                     while (ld_acquire(done + sl.s) < need) {
                         if (globaltimer_ns() - t0 > kSlotLimitNs) {
@@ -737,12 +806,18 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(TArgs a) {
                 s_flag = ok;
             }
             mma_barrier();
-            const bool ok = s_flag != 0;
+            const int32_t flag = s_flag;
+            if (flag < 0) {  // the ring has given up
+                fail = true;
+                break;
+            }
+            const bool ok = flag != 0;  // false: the slot's y rows stay as they are, its stages still drain
             if (ok) {
-                // the group's sums -> bf16 in the xa buffer; every load of a thread is
-                // issued before its first store (at most 64 rows x 32 pairs / 128 threads)
+                // the group's sums -> bf16 [gpad][rp] tile with the swizzle of rp-rank rows
+                // (rows past the group repeat its last token; their results are never
+                // stored); every load of a thread is issued before its first store
                 if (mtid < gsz) s_rows[mtid] = __ldcg(C.ids + p0 + mtid);
-                const int32_t pairs = r16 >> 1, total = gpad * pairs;
+                const int32_t pairs = r16 >> 1, total = gpad * pairs, NC = C.n * C.r_max;
                 constexpr int kPer = kGe * 32 / kMmaThreads;
                 float2 v[kPer];
 #pragma unroll
@@ -750,29 +825,74 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(TArgs a) {
                     const int32_t e = mtid + u * kMmaThreads;
                     const int32_t row = e / pairs, j = 2 * (e - row * pairs);
                     v[u] = make_float2(0.f, 0.f);
-                    if (e < total && row < gsz && j < sl.r)
-                        v[u] = ldcg_f2(acc_buf + (static_cast<size_t>(i) * C.T + p0 + row) * C.r_max + j);
+                    if (e < total && j < sl.r)
+                        v[u] = __ldcg(reinterpret_cast<const float2 *>(
+                            acc_buf + static_cast<size_t>(p0 + min(row, gsz - 1)) * NC + i * C.r_max + j));
                 }
 #pragma unroll
                 for (int u = 0; u < kPer; ++u) {
                     const int32_t e = mtid + u * kMmaThreads;
                     const int32_t row = e / pairs, j = 2 * (e - row * pairs);
-                    if (e < total) sts32(xbuf + static_cast<uint32_t>((row * xs + j) * 2), pack_bf16x2(v[u].x, v[u].y));
+                    if (e < total)
+                        sts32(xbuf + tc::swz_offset(row, j >> 3, rp * 2) + static_cast<uint32_t>((j & 7) * 2),
+                              pack_bf16x2(v[u].x, v[u].y));
                 }
+                tc::fence_async_smem();  // the tile is read by the tensor cores (async proxy)
             }
             mma_barrier();
-            for (int32_t u = 0; u < run_len; ++u) {
-                const uint32_t st = c % kStages;
-                const bool got = ring_wait(bar0 + 8 * st, (c / kStages) & 1, abort);
-                if (got && ok)
-                    expand_unit(C, sl, s_rows, gsz, i, cb + u, ring + st * kStageBytes, xbuf, xs, a.y, a.ldy, mw,
-                                lane);
+            const uint32_t idesc = tc::idesc_bf16(128, gpad);
+            const uint32_t bbox = static_cast<uint32_t>(kUnitCols * rp * 2);
+            const int32_t di = C.off[i + 1] - C.off[i], yrows = ytile_rows(gsz);
+            for (int32_t u0 = 0; u0 < run_len && !fail;) {
+                // one stage: its m units' MMAs at once (unit u's D in columns u gpad ..),
+                // one commit, one epilogue pass, then the rows to global memory
+                const int32_t m = min(sl.eu, run_len - u0);
+                const uint32_t st = c % kStages, sbase = ring + st * kStageBytes;
+                fail = mma_any(!ring_wait(bar0 + 8 * st, (c / kStages) & 1, abort));
+                if (fail) break;
+                tc::fence_after_sync();
+                if (ok && issuer) {
+                    for (int32_t u = 0; u < m; ++u)
+                        expand_mma_unit(tmem + static_cast<uint32_t>(u * gpad), sbase + u * bbox, xbuf, rp, sl.r, idesc);
+                    tc::mma_commit(reinterpret_cast<uint64_t *>(&bars[2 * kStages + 1]));
+                }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar0 + 8 * (kStages + st));
+                bool got = true;
+                const uint32_t yt0 = sbase + static_cast<uint32_t>(m) * bbox;
+                if (ok) {
+                    got = __all_sync(0xffffffffu, ring_wait(bar_acc, units & 1, abort));
+                    ++units;
+                    if (got) {
+                        tc::fence_after_sync();
+                        for (int32_t u = 0; u < m; ++u)
+                            expand_epilogue(sl.scale, yrows, tmem + static_cast<uint32_t>(u * gpad),
+                                            smem_raw + (yt0 + static_cast<uint32_t>(u * yrows * 256) - sa(smem_raw)),
+                                            lane_base, lane);
+                    }
+                }
+                tc::fence_before_sync();
+                // the tiles' rows are final and tensor memory may be refilled
+                fail = mma_any(!got);
+                if (fail) break;
+                if (ok) {
+                    // the rows to global memory: 16-byte pieces, a row's 16 pieces by consecutive threads
+                    for (int32_t u = 0; u < m; ++u) {
+                        const int32_t col0 = (cb + u0 + u) * kUnitCols;
+                        const int32_t nch = min(kUnitCols, di - col0) >> 3;
+                        const uint32_t yt = yt0 + static_cast<uint32_t>(u * yrows * 256);
+                        for (int32_t e = mtid; e < gsz * 16; e += kMmaThreads) {
+                            const int32_t row = e >> 4, ch = e & 15;
+                            if (ch < nch)
+                                stg128(a.y + static_cast<int64_t>(s_rows[row]) * a.ldy + C.off[i] + col0 + ch * 8,
+                                       lds128(yt + static_cast<uint32_t>(row * 256 + ch * 16)));
+                        }
+                    }
+                }
+                mma_barrier();  // every read of the stage is done
+                if (mtid == 0) mbar_arrive(bar0 + 8 * (kStages + st));
                 ++c;
-                if (!got) break;
+                u0 += m;
             }
-            mma_barrier();  // the xa buffer is read by every warp before the next run rewrites it
             idx += run_len;
             left -= run_len;
             if (idx == sl.nge * C.ublk) {
@@ -780,16 +900,25 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(TArgs a) {
                 idx = 0;
             }
         }
+        if (fail && mtid == 0) *abort = 1;
     }
 
+    tc::fence_before_sync();
     __syncthreads();
+    const bool aborted = *abort != 0;  // nobody writes it past the barrier
+    if (aborted) {
+        // copies and MMAs that a stalled ring may still have in flight end
+        // within microseconds; wait well past that before the shared and
+        // tensor memory are given back
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
+    }
+    if (warp == 2) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
     if (threadIdx.x == 0) {
-        if (*abort) {
-            report_error(a.err, LORA_ERR_TIMEOUT);
-            // copies a stalled ring may still have in flight land within microseconds
-            const uint64_t t0 = globaltimer_ns();
-            while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
-        }
+        if (aborted) report_error(a.err, LORA_ERR_TIMEOUT);
         pdl_wait();
         __threadfence();
         if (atomicAdd(a.exits, 1) == static_cast<int32_t>(gridDim.x) - 1) {
@@ -869,9 +998,11 @@ __global__ void __launch_bounds__(512) tma_plan_kernel(PArgs pa, Shape sh, TmaPl
     const int32_t *hdr = static_cast<const int32_t *>(table);
     const TableView tab(table, S, sh.n);
     const int32_t *mh = reinterpret_cast<const int32_t *>(static_cast<const char *>(table) + TmaTableLayout(S, sh.n).hdr);
+    const int32_t *tflags =
+        reinterpret_cast<const int32_t *>(static_cast<const char *>(table) + TmaTableLayout(S, sh.n).flags);
     const int32_t n = sh.n, nkb = sh.k / 64;
     int32_t ublk = 0;
-    for (int i = 0; i < n; ++i) ublk += cdiv(sh.off[i + 1] - sh.off[i], 64);
+    for (int i = 0; i < n; ++i) ublk += cdiv(sh.off[i + 1] - sh.off[i], kUnitCols);
     if (threadIdx.x == 0) {
         // the maps block is read only once the header says the table has one
         bool ok = hdr[0] == kTableMagic && hdr[1] == S && hdr[2] == n && (hdr[3] & kTableMapsFlag) != 0 &&
@@ -918,7 +1049,12 @@ __global__ void __launch_bounds__(512) tma_plan_kernel(PArgs pa, Shape sh, TmaPl
         const int32_t nr = n * r;
         const int32_t gmax = nr <= 96 ? 128 : 64;
         const int32_t ngs = cdiv(cnt, gmax), gs = cdiv(cnt, ngs);
-        const int32_t cs = max(1, min(nkb, 256 / (nr + pad16i(gs))));
+        // k-blocks per stage: the A and x rows fit the stage's 256 rows; one MMA
+        // covers the stage (nb n r <= 128 D rows, nb gpad <= 256 columns); at
+        // most 15 (a packed stage is copied as blocks of 8, 4, 2 and 1)
+        const int32_t cs = nr > 128 ? 1
+                                    : max(1, min(min(min(nkb, 256 / (nr + pad16i(gs))), 128 / nr),
+                                                 min(256 / pad16i(gs), 15)));
         const int32_t nge = cdiv(cnt, kGe), ge = cdiv(cnt, nge);
         SlotRec rec;
         rec.s = s;
@@ -931,9 +1067,18 @@ __global__ void __launch_bounds__(512) tma_plan_kernel(PArgs pa, Shape sh, TmaPl
         rec.cs = cs;
         rec.ge = ge;
         rec.nge = nge;
-        rec.wps = (nr + gs) * 8;          // A rows and x rows of one k-block, 16-byte units
-        rec.wpe = 8 * r + 16 * ge;        // B tile [64][r] and y rows read + written
-        for (int q = 0; q < 4; ++q) rec.pad[q] = 0;
+        // weights in 16-byte units: the bytes a piece moves plus the fixed costs
+        // that bound small pieces (a four-row gather of x, an expand unit's
+        // share of its stage's tensor-core round trip, epilogue and barriers)
+        rec.wps = (nr + gs) * 8 + kGatherCost * ((gs + 3) >> 2);  // A and x rows of one k-block
+        rec.wpe = 16 * r + 32 * ge + kUnitCost;                   // B tile [128][r], y rows read + written
+        rec.rp = b_box_ranks(r);
+        // as many 128-column units of one run per stage as fit: the B boxes and
+        // their y rows (ge rounded up to 8) in the stage, their D in tensor memory
+        rec.eu = max(1, min(kStageBytes / (kUnitCols * rec.rp * 2 + ytile_rows(ge) * kUnitCols * 2),
+                            kTmemCols / pad16i(ge)));
+        rec.pk = (tflags[s] & kSlotPackedA) != 0;
+        rec.pad = 0;
         recs[a] = rec;
         wps[a] = rec.wps;
         wpe[a] = rec.wpe;
@@ -1060,27 +1205,45 @@ bool encode_tma_table(void *host_buf, const Shape &sh, const int32_t *ranks, con
     std::memset(p + L.hdr, 0, L.bytes - L.hdr);
     EncodeTiled enc = encode_fn();
     if (enc == nullptr) return false;
+    const cuuint32_t one[3] = {1, 1, 1};
+    // rows x k matrix at `base` viewed as [k / 64][rows][64]: the block index is
+    // the outer dimension with a 128-byte stride, rows stride k * 2 bytes
+    auto encode_a = [&](CUtensorMap *m, uint64_t base, int32_t rows, int32_t depth) {
+        const cuuint64_t dim[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(sh.k / 64)};
+        const cuuint64_t str[2] = {static_cast<cuuint64_t>(sh.k) * 2, 128};
+        const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), static_cast<cuuint32_t>(depth)};
+        return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, reinterpret_cast<void *>(base), dim, str, box, one,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    int32_t *flags = reinterpret_cast<int32_t *>(p + L.flags);
     for (int32_t s = 0; s < sh.S; ++s) {
         const int32_t r = ranks[s];
         if (r <= 0 || r > 256) continue;
+        CUtensorMap *maps = reinterpret_cast<CUtensorMap *>(p + L.maps + size_t(s) * kMapsPerSlot * 128);
+        const uint64_t a0 = A_ptrs[size_t(s) * sh.n];
+        const uint64_t slice_bytes = uint64_t(r) * uint64_t(sh.k) * 2;
+        bool packed = sh.n * r <= 256;
+        for (int32_t i = 1; i < sh.n; ++i) packed = packed && A_ptrs[size_t(s) * sh.n + i] == a0 + i * slice_bytes;
+        if (packed) {
+            flags[s] = kSlotPackedA;
+            for (int d = 0; d < 4; ++d)
+                if (!encode_a(maps + d, a0, sh.n * r, 1 << d)) return false;
+        } else {
+            for (int32_t i = 0; i < sh.n; ++i)
+                if (!encode_a(maps + i, A_ptrs[size_t(s) * sh.n + i], r, 1)) return false;
+        }
         for (int32_t i = 0; i < sh.n; ++i) {
-            CUtensorMap *ma = reinterpret_cast<CUtensorMap *>(p + L.maps + (size_t(s) * sh.n + i) * 256);
-            const cuuint64_t adim[2] = {static_cast<cuuint64_t>(sh.k), static_cast<cuuint64_t>(r)};
-            const cuuint64_t astr[1] = {static_cast<cuuint64_t>(sh.k) * 2};
-            const cuuint32_t abox[2] = {64, static_cast<cuuint32_t>(r)};
-            const cuuint32_t one[2] = {1, 1};
-            if (enc(ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, reinterpret_cast<void *>(A_ptrs[s * sh.n + i]), adim,
-                    astr, abox, one, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-                return false;
-            CUtensorMap *mb = ma + 1;
             const int32_t di = sh.off[i + 1] - sh.off[i];
             const cuuint64_t bdim[2] = {static_cast<cuuint64_t>(r), static_cast<cuuint64_t>(di)};
             const cuuint64_t bstr[1] = {static_cast<cuuint64_t>(r) * 2};
-            const cuuint32_t bbox[2] = {64, 64};
-            if (enc(mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, reinterpret_cast<void *>(B_ptrs[s * sh.n + i]), bdim,
-                    bstr, bbox, one, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            const int32_t rp = b_box_ranks(r);
+            const cuuint32_t bbox[2] = {static_cast<cuuint32_t>(rp), static_cast<cuuint32_t>(kUnitCols)};
+            const CUtensorMapSwizzle bsw = rp == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                    : (rp == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+            if (enc(maps + 4 + i, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, reinterpret_cast<void *>(B_ptrs[s * sh.n + i]),
+                    bdim, bstr, bbox, one, CU_TENSOR_MAP_INTERLEAVE_NONE, bsw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
                 return false;
         }
     }
@@ -1128,7 +1291,7 @@ cudaError_t launch_tma_plans(const Shape &sh, const void *const *tables, unsigne
 }
 
 // One call from a plan; ws_ctrl: [2 S] counters then gen, exits; acc0 / acc1:
-// the two fp32 sum sets of [n][T][r_max].
+// the two fp32 sum sets of [T][n r_max].
 cudaError_t launch_tma_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                               const unsigned char *plan, float *acc0, float *acc1, int32_t *ctrl, int32_t T,
                               int32_t *err, cudaStream_t stream) {
@@ -1137,7 +1300,20 @@ cudaError_t launch_tma_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int64
     cudaError_t e = static_cast<cudaError_t>(num_sms_now(num_sms));
     if (e != cudaSuccess) return e;
     if (num_sms > kMaxGrid) return cudaErrorNotSupported;
+    EncodeTiled enc = encode_fn();
+    if (enc == nullptr) return cudaErrorNotSupported;
     TArgs a;
+    memset(&a, 0, sizeof a);
+    {
+        // x: [T][k] rows of ldx elements, box [1][64], 128-byte swizzle (the shrink's x tiles)
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(sh.k), static_cast<cuuint64_t>(T)};
+        const cuuint64_t str[1] = {static_cast<cuuint64_t>(ldx) * 2};
+        const cuuint32_t box[2] = {64, 1}, one[2] = {1, 1};
+        if (enc(&a.xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims, str, box, one,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     a.x = x;
     a.ldx = ldx;
     a.y = y;

@@ -36,13 +36,16 @@ class ResidentProjection:
     float8_e4m3fn codes for every matrix: then ``fp8`` is True and the table
     serves the FP8 path); rank-0 slots have None.  ``scale_rule`` is "alpha_over_r" or "alpha_over_sqrt_r";
     with ``premultiplied`` the rule's scale is folded into B and the table
-    carries scale 1.
+    carries scale 1.  With ``pack_a`` (the default) a slot's A slices are views
+    of one [n, r_s, k] block, the layout the one-kernel TMA path copies with a
+    single tensor-map copy per stage.
     """
 
     def __init__(self, *, S: int, r_max: int, ranks: Sequence[int], alphas: Sequence[float], scale_rule: str,
                  premultiplied: bool, k: int, slice_widths: Sequence[int],
                  A: Sequence[Sequence[Optional[np.ndarray]]], B: Sequence[Sequence[Optional[np.ndarray]]],
-                 x: Optional[np.ndarray] = None, y_in: Optional[np.ndarray] = None, device="cuda"):
+                 x: Optional[np.ndarray] = None, y_in: Optional[np.ndarray] = None, device="cuda",
+                 pack_a: bool = True):
         self.S, self.r_max, self.k = int(S), int(r_max), int(k)
         self.slice_widths = [int(w) for w in slice_widths]
         self.n = len(self.slice_widths)
@@ -57,11 +60,14 @@ class ResidentProjection:
         mats = [m for row in A for m in row if m is not None]
         self.fp8 = bool(mats) and mats[0].dtype == np.uint8
         premul = lora_premultiply_e4m3 if self.fp8 else lora_premultiply
+        self.pack_a = pack_a
         for s in range(S):
             rowA, rowB = [], []
+            packed = (_w_to_dev(np.stack([np.asarray(A[s][i]) for i in range(self.n)]), device)
+                      if pack_a and self.ranks[s] > 0 else None)
             for i in range(self.n):
                 if self.ranks[s] > 0:
-                    ta = _w_to_dev(A[s][i], device)
+                    ta = packed[i] if packed is not None else _w_to_dev(A[s][i], device)
                     tb = _w_to_dev(B[s][i], device)
                     if premultiplied:
                         premul(tb, float(rule_scales[s]))
@@ -88,7 +94,14 @@ class ResidentProjection:
         n = self.n
         a_ptrs = np.zeros(self.S * n, dtype=np.uint64)
         b_ptrs = np.zeros(self.S * n, dtype=np.uint64)
-        other.A = [[(t.clone() if t is not None else None) for t in row] for row in self.A]
+        import torch
+
+        def clone_row(row):
+            if row and row[0] is not None and self.pack_a:
+                block = torch.stack(row)  # a fresh [n, r, k] block
+                return [block[i] for i in range(len(row))]
+            return [(t.clone() if t is not None else None) for t in row]
+        other.A = [clone_row(row) for row in self.A]
         other.B = [[(t.clone() if t is not None else None) for t in row] for row in self.B]
         for s in range(self.S):
             for i in range(n):
@@ -113,11 +126,11 @@ class ResidentProjection:
         self.table.set(self.ranks, self.scales, *self._ptrs, stream=stream)
 
     @classmethod
-    def from_workload(cls, wl, module_index: int = 0, device="cuda", with_rows: bool = True):
+    def from_workload(cls, wl, module_index: int = 0, device="cuda", with_rows: bool = True, pack_a: bool = True):
         m = wl.modules[module_index]
         return cls(S=wl.S, r_max=wl.r_max, ranks=wl.ranks, alphas=wl.alphas, scale_rule=wl.scale_rule,
                    premultiplied=wl.premultiplied, k=m.k, slice_widths=m.slice_widths, A=m.A, B=m.B,
-                   x=m.x if with_rows else None, y_in=m.y_in if with_rows else None, device=device)
+                   x=m.x if with_rows else None, y_in=m.y_in if with_rows else None, device=device, pack_a=pack_a)
 
 
 def to_device_bf16(bits: np.ndarray, device="cuda"):

@@ -44,11 +44,11 @@ def oracle_y_e4m3(wl, mod_idx=0, rows=None):
     return oracle.apply_e4m3(m.x, m.y_in, m.slice_widths, wl.slot_ids, wl.ranks, scales, m.A, B, rows=rows)
 
 
-def gpu_apply(wl, mod_idx=0, path="auto", max_seg_hint=0, repeat=1):
+def gpu_apply(wl, mod_idx=0, path="auto", max_seg_hint=0, repeat=1, pack_a=True):
     import torch
     import rank_adapter_gemm_gb300 as L
     from rank_adapter_gemm_gb300.resident import ResidentProjection, to_host_bits
-    rp = ResidentProjection.from_workload(wl, mod_idx)
+    rp = ResidentProjection.from_workload(wl, mod_idx, pack_a=pack_a)
     slot_dev = torch.from_numpy(np.ascontiguousarray(wl.slot_ids, dtype=np.int32)).cuda()
     idx = L.TokenIndex(wl.T, wl.S)
     idx.build(slot_dev, rp.table)

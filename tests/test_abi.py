@@ -197,10 +197,12 @@ def test_host_checks_of_the_tma_entry_points(L):
     P = ctypes.c_void_p
     fake = P(1 << 20)  # never dereferenced: every call below fails its host checks first
     sh = L.make_shape(32, 64, 4096, [4096, 1024, 1024])
-    # the ordinary table, aligned to 128 bytes, a 128-byte block header, two
-    # 128-byte tensor maps per slot and slice
+    # the ordinary table, aligned to 128 bytes, a 128-byte block header, the
+    # slot flags padded to 128 bytes, eight 128-byte tensor maps per slot
     base = (L.lora_slot_table_bytes(32, 3) + 127) // 128 * 128
-    assert L.lora_slot_table_tma_bytes(32, sh) == base + 128 + 32 * 3 * 256
+    assert L.lora_slot_table_tma_bytes(32, sh) == base + 128 + 128 + 32 * 8 * 128
+    assert L.lora_slot_table_tma_bytes(33, L.make_shape(33, 64, 4096, [4096, 1024, 1024])) == \
+        (L.lora_slot_table_bytes(33, 3) + 127) // 128 * 128 + 128 + 256 + 33 * 8 * 128
     assert L.lora_slot_table_tma_bytes(31, sh) == 0  # S must match the shape
     assert L.lora_slot_table_tma_bytes(32, L.make_shape(32, 64, 4095, [4096])) == 0
     staging = np.zeros(L.lora_slot_table_tma_bytes(32, sh), np.uint8)

@@ -60,7 +60,7 @@ def _canaries_intact(big, view, what):
     else:
         o = (view.data_ptr() - big.data_ptr()) // big.element_size()
         mask[o:o + view.shape[0]] = False
-    bits = big.view(torch.int16 if big.element_size() == 2 else torch.int32)
+    bits = big.view({1: torch.uint8, 2: torch.int16, 4: torch.int32}[big.element_size()])
     vals = bits[mask].cpu().numpy()
     first = vals[:1]
     assert vals.size == 0 or (vals == first).all(), f"{what}: canary changed"

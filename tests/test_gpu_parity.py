@@ -1174,6 +1174,30 @@ TMA_RAGGED = [
 ]
 
 
+@pytest.mark.parametrize("case", [TMA_RAGGED[0], TMA_RAGGED[3], TMA_RAGGED[4], TMA_RAGGED[6]],
+                         ids=lambda c: f"tma{c[0]}")
+def test_tma_separate_a_slices(case):
+    """A slot whose A slices are separate allocations (not one packed [n r][k]
+    block) is copied slice by slice: same results as the oracle."""
+    seed, T, k, widths, S, ranks = case
+    wl = _small(seed, T, k, widths, S, ranks)
+    outs, err, *_ = gpu_apply(wl, path="decode_tma", repeat=2, pack_a=False)
+    assert err == 0
+    ref, _ = oracle_y(wl)
+    for y in outs:
+        assert_y_close(y, ref, f"tma unpacked {seed}")
+
+
+def test_tma_separate_a_slices_packed_qkv():
+    """The packed QKV decode batch with every slot's A slices allocated apart."""
+    wl = W.config(2)
+    outs, err, *_ = gpu_apply(wl, path="decode_tma", repeat=2, pack_a=False)
+    assert err == 0
+    ref, _ = oracle_y(wl)
+    for y in outs:
+        assert_y_close(y, ref, "tma unpacked qkv")
+
+
 @pytest.mark.parametrize("plan", [False, True], ids=["apply_ex", "plan"])
 @pytest.mark.parametrize("case", TMA_RAGGED, ids=[f"tma{c[0]}" for c in TMA_RAGGED])
 def test_tma_ragged(case, plan):
