@@ -56,9 +56,9 @@ struct TableView {
 __host__ __device__ inline int32_t tc_rank_pad(int32_t r_max) { return r_max <= 16 ? 16 : (r_max <= 32 ? 32 : 64); }
 
 // Plan of the one-kernel TMA decode path: a 128-byte header, 64 bytes per
-// slot, 32 bytes for each of up to 256 CTAs, then the T sorted token ids.
+// slot, 32 bytes for each of up to 512 CTAs, then the T sorted token ids.
 __host__ __device__ inline size_t tma_plan_size(int32_t T, int32_t S) {
-    return (128 + 64 * size_t(S) + 256 * 32 + 4 * size_t(T > 0 ? T : 0) + 255) & ~size_t(255);
+    return (128 + 64 * size_t(S) + 512 * 32 + 4 * size_t(T > 0 ? T : 0) + 255) & ~size_t(255);
 }
 
 // Workspace: a control block of per-(slot, slice) counters, the fp32 xa that

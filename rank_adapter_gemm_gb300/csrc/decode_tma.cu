@@ -8,12 +8,14 @@
 // a call (launch, first burst, the shrink -> expand dependency, the tail) are
 // what separates it from the roofline.  The kernel is built around that:
 //
-//   * One CTA per SM, about 110 KB of shared memory, so that the CTA of the
-//     next call (launched as a programmatic dependent) fits beside it.  The
-//     next call's producer warp issues its first stages of adapter weights
-//     before griddepcontrol.wait: the weights never depend on the previous
-//     layer, so their first burst overlaps the previous call's tail.  Only x,
-//     y and the workspace wait for the previous grid.
+//   * Two CTAs per SM, about 110 KB of shared memory each: one CTA's loads
+//     stay in flight while the other waits on its tensor cores or writes y.
+//     The call is launched as a programmatic dependent, so a CTA of the next
+//     call takes an SM slot as soon as one of this call's CTAs there exits;
+//     its producer warp issues the first stages of adapter weights before
+//     griddepcontrol.wait (the weights never depend on the previous layer),
+//     so their first burst overlaps the previous call's tail.  Only x, y and
+//     the workspace wait for the previous grid.
 //   * Stages of up to 32 KB in a ring of three, one mbarrier each.  A shrink
 //     stage holds, for one slot, one group of its tokens and a run of 64-wide
 //     k-blocks: the group's x rows (16-byte cp.async copies, gathered through
@@ -102,7 +104,8 @@ constexpr int kTmemCols = 256;       // shrink D (ranks 0..127 at column 0, 128.
                                      // two 64-column buffers
                                      // (two CTAs of 256 columns share an SM's 512)
 constexpr int kUnitCols = 128;       // expand unit: output columns
-constexpr int kMaxGrid = 256;
+constexpr int kMaxGrid = 512;
+constexpr int kCtasPerSm = 2;      // two CTAs of a call share an SM (about 110 KB of shared memory each)
 constexpr int kMaxRank = 64;
 constexpr int kMaxNR = 192;          // n_slices * r_max
 constexpr int kGe = 64;              // expand token group
@@ -141,7 +144,7 @@ __host__ __device__ inline size_t plan_slots_off() { return sizeof(PlanHdr); }
 __host__ __device__ inline size_t plan_ctas_off(int32_t S) { return plan_slots_off() + size_t(S) * sizeof(SlotRec); }
 __host__ __device__ inline size_t plan_ids_off(int32_t S) { return plan_ctas_off(S) + size_t(kMaxGrid) * sizeof(CtaRec); }
 __host__ __device__ inline size_t plan_total(int32_t T, int32_t S) { return tma_plan_size(T, S); }
-static_assert(sizeof(PlanHdr) + sizeof(CtaRec) * kMaxGrid == 128 + 256 * 32, "plan layout matches tma_plan_size");
+static_assert(sizeof(PlanHdr) + sizeof(CtaRec) * kMaxGrid == 128 + 512 * 32, "plan layout matches tma_plan_size");
 
 __host__ __device__ inline int32_t cdiv(int32_t a, int32_t b) { return (a + b - 1) / b; }
 __host__ __device__ inline int32_t pad16i(int32_t v) { return (v + 15) & ~15; }
@@ -355,9 +358,6 @@ __device__ __forceinline__ void unit_slice(const Ctx &C, int32_t u, int32_t &i, 
 // ---------------------------------------------------------------------------
 // Tensor-core roles (tcgen05; warp 2 lane 0 issues, warps 2..5 read results)
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void red_f32(float *p, float v) {
-    asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" :: "l"(p), "f"(v) : "memory");
-}
 // Adds v to a per-slot counter with release semantics: the sums this CTA
 // added before (ordered by the barrier that precedes the call) are visible to
 // whoever acquires the new count.
@@ -392,38 +392,53 @@ __device__ __forceinline__ void shrink_mma_stage(uint32_t tmem, uint32_t sbase, 
     }
 }
 
+__device__ __forceinline__ void red_v4(float *p, float4 v) {
+    asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1,%2,%3,%4};" :: "l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w) : "memory");
+}
+
 // Reads the run's D from tensor memory and adds it into the call's fp32 sums
 // acc_buf[p][i * r_max + j].  This warp's 32 lanes are D rows lane_base +
 // lane: for n r <= 128 row (kbl, rank) of the nbr k-blocks the run's stages
 // held, whose tokens sit in columns kbl * gpad..; for n r > 128 rank
-// 128 d + row of D_d.  Lanes holding the same rank for different k-blocks add
-// into the same sums; a warp's adds for one token cover consecutive ranks.
+// 128 d + row of D_d.  Each 16-token load is turned around through the warp's
+// 2 KB of scratch (shared memory) so that a lane adds four consecutive ranks of
+// one token with one 16-byte add; rows holding the same rank for different
+// k-blocks add into the same sums.
 __device__ __forceinline__ void shrink_epilogue(const Ctx &C, const Slot &sl, int32_t p0, int32_t gsz, int32_t gpad,
                                                 int32_t nbr, uint32_t tmem, int32_t lane_base, int32_t lane,
-                                                float *acc_buf) {
+                                                float *acc_buf, float *scr) {
     const int32_t nr = C.n * sl.r, NC = C.n * C.r_max;
     const int32_t nd = nr > 128 ? 2 : 1, rows = nr > 128 ? nr : nbr * nr;
+    const int32_t rg = lane & 7, tq = lane >> 3;  // after the turn: ranks 4 rg .. 4 rg + 3, tokens tq + 4 k
     for (int32_t d = 0; d < nd; ++d) {
         const int32_t row0 = 128 * d + lane_base;  // warp-uniform
         if (row0 >= rows) continue;
-        const int32_t row = row0 + lane, kbl = nd == 2 ? 0 : row / nr, rank = nd == 2 ? row : row - kbl * nr;
-        const int32_t i = rank / sl.r, j = rank - i * sl.r;
-        const bool rv = row < rows;
-        float *dst = acc_buf + static_cast<size_t>(p0) * NC + i * C.r_max + j;
-        // the k-blocks whose rows this warp holds
+        // this lane's four rows after the turn (a group of four never crosses a
+        // slice or a k-block: r and n r are multiples of 8)
+        const int32_t grow = row0 + 4 * rg;
+        const int32_t gkbl = nd == 2 ? 0 : grow / nr, grank = nd == 2 ? grow : grow - gkbl * nr;
+        const int32_t gi = grank / sl.r, gj = grank - gi * sl.r;
+        float *dst = acc_buf + static_cast<size_t>(p0) * NC + gi * C.r_max + gj;
         const int32_t kb0 = nd == 2 ? 0 : row0 / nr, kb1 = nd == 2 ? 0 : min(row0 + 31, rows - 1) / nr;
         for (int32_t kc = kb0; kc <= kb1; ++kc) {
-            const bool mine = rv && kbl == kc;
-            for (int32_t t0 = 0; t0 < gpad; t0 += 16) {
+            const bool mine = grow < rows && gkbl == kc;
+            for (int32_t t0 = 0; t0 < gsz; t0 += 16) {
                 uint32_t r[16];
                 tc::tmem_ld16(tmem + (static_cast<uint32_t>(lane_base) << 16) +
                                   static_cast<uint32_t>(128 * d + kc * gpad + t0),
                               r);
-                if (mine) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        if (t0 + e < gsz) red_f32(dst + static_cast<size_t>(t0 + e) * NC, __uint_as_float(r[e]));
+                for (int e = 0; e < 16; ++e) scr[e * 32 + lane] = __uint_as_float(r[e]);
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int32_t t = tq + 4 * k;
+                    if (mine && t0 + t < gsz)
+                        red_v4(dst + static_cast<size_t>(t0 + t) * NC,
+                               *reinterpret_cast<const float4 *>(scr + t * 32 + 4 * rg));
                 }
+                __syncwarp();
             }
         }
     }
@@ -467,8 +482,8 @@ __device__ __forceinline__ void expand_epilogue(float scale, int32_t yrows, uint
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(const __grid_constant__ TArgs a) {
     extern __shared__ unsigned char smem_raw[];
-    // full[kStages], empty[kStages], run_done, acc_full
-    __shared__ __align__(8) uint64_t bars[2 * kStages + 2];
+    // full[kStages], empty[kStages], run_done, acc_full[2] (one per half of tensor memory)
+    __shared__ __align__(8) uint64_t bars[2 * kStages + 3];
     __shared__ int32_t s_abort, s_flag;
     __shared__ uint32_t s_tmem;
     __shared__ int32_t s_rows[kGe];                      // token ids of the expand run's group (tensor-core warps)
@@ -525,6 +540,7 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(const __grid_co
         }
         mbar_init(bar_done, 1);
         mbar_init(bar_acc, 1);
+        mbar_init(bar_acc + 8, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_abort = 0;
     }
@@ -729,6 +745,9 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(const __grid_co
                 reinterpret_cast<float4 *>(other)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int32_t s = blockIdx.x * kMmaThreads + mtid; s < a.S; s += gridDim.x * kMmaThreads) odone[s] = 0;
         }
+        // the shrink epilogue's scratch: 2 KB per warp in the expand's sum tile,
+        // which no expand run uses before this CTA's last shrink run
+        float *xscr = reinterpret_cast<float *>(smem_raw + (xbuf - sa(smem_raw))) + (warp & 3) * 512;
         uint32_t c = 0, runs = 0, units = 0;
         bool fail = false;  // the same in all four warps: every change of it goes through mma_any
         int32_t tile = crs.x, idx = crs.y, left = crs.z;
@@ -761,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(const __grid_co
             if (got) {
                 tc::fence_after_sync();
                 shrink_epilogue(C, sl, sl.seg0 + g * sl.gs, gsz, gpad, min(sl.cs, run_len), tmem, lane_base, lane,
-                                acc_buf);
+                                acc_buf, xscr);
             }
             tc::fence_before_sync();
             // every warp's sums of the run are issued and D may be overwritten
@@ -843,35 +862,51 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(const __grid_co
             const uint32_t idesc = tc::idesc_bf16(128, gpad);
             const uint32_t bbox = static_cast<uint32_t>(kUnitCols * rp * 2);
             const int32_t di = C.off[i + 1] - C.off[i], yrows = ytile_rows(gsz);
-            for (int32_t u0 = 0; u0 < run_len && !fail;) {
-                // one stage: its m units' MMAs at once (unit u's D in columns u gpad ..),
-                // one commit, one epilogue pass, then the rows to global memory
-                const int32_t m = min(sl.eu, run_len - u0);
-                const uint32_t st = c % kStages, sbase = ring + st * kStageBytes;
-                fail = mma_any(!ring_wait(bar0 + 8 * st, (c / kStages) & 1, abort));
+            const int32_t nstg = cdiv(run_len, sl.eu);
+            // Stage j of the run puts its m units' D in tensor-memory half (units + j) & 1
+            // (unit u at column u gpad of the half) and commits to acc_full of that half.
+            // The issuing thread starts stage j + 1's MMAs before stage j's epilogue
+            // when j + 1's data is already in, so the tensor cores overlap the
+            // epilogue and the stores.
+            int32_t issued = 0;  // stages whose MMAs are issued (issuing thread only)
+            auto issue_stage = [&](int32_t j) {
+                const uint32_t sb = ring + ((c + j) % kStages) * kStageBytes;
+                const int32_t mj = min(sl.eu, run_len - j * sl.eu);
+                const uint32_t half = static_cast<uint32_t>((units + j) & 1) * 128u;
+                for (int32_t u = 0; u < mj; ++u)
+                    expand_mma_unit(tmem + half + static_cast<uint32_t>(u * gpad), sb + u * bbox, xbuf, rp, sl.r, idesc);
+                tc::mma_commit(reinterpret_cast<uint64_t *>(&bars[2 * kStages + 1 + ((units + j) & 1)]));
+            };
+            for (int32_t j = 0; j < nstg && !fail; ++j) {
+                const int32_t u0 = j * sl.eu, m = min(sl.eu, run_len - u0);
+                const uint32_t st = (c + j) % kStages, sbase = ring + st * kStageBytes;
+                fail = mma_any(!ring_wait(bar0 + 8 * st, ((c + j) / kStages) & 1, abort));
                 if (fail) break;
                 tc::fence_after_sync();
                 if (ok && issuer) {
-                    for (int32_t u = 0; u < m; ++u)
-                        expand_mma_unit(tmem + static_cast<uint32_t>(u * gpad), sbase + u * bbox, xbuf, rp, sl.r, idesc);
-                    tc::mma_commit(reinterpret_cast<uint64_t *>(&bars[2 * kStages + 1]));
+                    if (issued == j) issue_stage(issued++);
+                    if (issued == j + 1 && j + 1 < nstg &&
+                        mbar_try_wait(bar0 + 8 * ((c + j + 1) % kStages), ((c + j + 1) / kStages) & 1)) {
+                        tc::fence_after_sync();
+                        issue_stage(issued++);
+                    }
                 }
                 __syncwarp();
                 bool got = true;
                 const uint32_t yt0 = sbase + static_cast<uint32_t>(m) * bbox;
                 if (ok) {
-                    got = __all_sync(0xffffffffu, ring_wait(bar_acc, units & 1, abort));
-                    ++units;
+                    const uint32_t U = units + j, half = (U & 1) * 128u;
+                    got = __all_sync(0xffffffffu, ring_wait(bar_acc + 8 * (U & 1), (U >> 1) & 1, abort));
                     if (got) {
                         tc::fence_after_sync();
                         for (int32_t u = 0; u < m; ++u)
-                            expand_epilogue(sl.scale, yrows, tmem + static_cast<uint32_t>(u * gpad),
+                            expand_epilogue(sl.scale, yrows, tmem + half + static_cast<uint32_t>(u * gpad),
                                             smem_raw + (yt0 + static_cast<uint32_t>(u * yrows * 256) - sa(smem_raw)),
                                             lane_base, lane);
                     }
                 }
                 tc::fence_before_sync();
-                // the tiles' rows are final and tensor memory may be refilled
+                // the tiles' rows are final and this half of tensor memory may be refilled
                 fail = mma_any(!got);
                 if (fail) break;
                 if (ok) {
@@ -890,9 +925,10 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(const __grid_co
                 }
                 mma_barrier();  // every read of the stage is done
                 if (mtid == 0) mbar_arrive(bar0 + 8 * (kStages + st));
-                ++c;
-                u0 += m;
             }
+            if (fail) break;
+            c += nstg;
+            if (ok) units += nstg;
             idx += run_len;
             left -= run_len;
             if (idx == sl.nge * C.ublk) {
@@ -1074,9 +1110,9 @@ __global__ void __launch_bounds__(512) tma_plan_kernel(PArgs pa, Shape sh, TmaPl
         rec.wpe = 16 * r + 32 * ge + kUnitCost;                   // B tile [128][r], y rows read + written
         rec.rp = b_box_ranks(r);
         // as many 128-column units of one run per stage as fit: the B boxes and
-        // their y rows (ge rounded up to 8) in the stage, their D in tensor memory
+        // their y rows (ge rounded up to 8) in the stage, their D in half of tensor memory
         rec.eu = max(1, min(kStageBytes / (kUnitCols * rec.rp * 2 + ytile_rows(ge) * kUnitCols * 2),
-                            kTmemCols / pad16i(ge)));
+                            (kTmemCols / 2) / pad16i(ge)));
         rec.pk = (tflags[s] & kSlotPackedA) != 0;
         rec.pad = 0;
         recs[a] = rec;
@@ -1166,6 +1202,14 @@ int num_sms_now(int &num_sms) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     return cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+}
+
+// The grid of one call: kCtasPerSm CTAs per SM of the current device.
+int tma_grid_now(int &grid) {
+    int num_sms = 0;
+    const int e = num_sms_now(num_sms);
+    grid = num_sms * kCtasPerSm;
+    return e;
 }
 
 // ---------------------------------------------------------------------------
@@ -1268,11 +1312,11 @@ cudaError_t launch_tma_plans(const Shape &sh, const void *const *tables, unsigne
                              const int32_t *sorted_ids, const int32_t *seg, const int32_t *active, int32_t T,
                              int32_t *err, cudaStream_t stream) {
     if (!decode_tma_supported(T, sh)) return cudaErrorNotSupported;
-    int num_sms = 0;
-    cudaError_t e = static_cast<cudaError_t>(num_sms_now(num_sms));
+    int grid = 0;
+    cudaError_t e = static_cast<cudaError_t>(tma_grid_now(grid));
     if (e != cudaSuccess) return e;
-    if (num_sms > kMaxGrid) return cudaErrorNotSupported;
-    PArgs pa{sorted_ids, seg, active, err, T, num_sms};
+    if (grid > kMaxGrid) return cudaErrorNotSupported;
+    PArgs pa{sorted_ids, seg, active, err, T, grid};
     const size_t smem = tma_plan_smem(sh.S);
     e = cudaFuncSetAttribute(tma_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -1296,10 +1340,10 @@ cudaError_t launch_tma_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int64
                               const unsigned char *plan, float *acc0, float *acc1, int32_t *ctrl, int32_t T,
                               int32_t *err, cudaStream_t stream) {
     if (!decode_tma_supported(T, sh)) return cudaErrorNotSupported;
-    int num_sms = 0;
-    cudaError_t e = static_cast<cudaError_t>(num_sms_now(num_sms));
+    int grid = 0;
+    cudaError_t e = static_cast<cudaError_t>(tma_grid_now(grid));
     if (e != cudaSuccess) return e;
-    if (num_sms > kMaxGrid) return cudaErrorNotSupported;
+    if (grid > kMaxGrid) return cudaErrorNotSupported;
     EncodeTiled enc = encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
     TArgs a;
@@ -1335,7 +1379,7 @@ cudaError_t launch_tma_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int64
     e = cudaFuncSetAttribute(tma_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(num_sms));
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;

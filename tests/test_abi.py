@@ -92,8 +92,8 @@ def test_workspace_bytes(L):
     # tensor-core decode kernels use in turn
     # then the one-kernel TMA path's two sum sets, its control block (2 S
     # counters, the call and exit counters) and room for a plan (128-byte
-    # header, 64 bytes per slot, 32 per CTA for up to 256 CTAs, T token ids)
-    plan = (128 + 64 * 32 + 256 * 32 + 4 * 256 + 255) // 256 * 256
+    # header, 64 bytes per slot, 32 per CTA for up to 512 CTAs, T token ids)
+    plan = (128 + 64 * 32 + 512 * 32 + 4 * 256 + 255) // 256 * 256
     tma = 2 * xa + (4 * (2 * 32 + 2) + 255) // 256 * 256 + plan
     assert nbytes >= 4 * xa + 2 * hl + tma
     assert nbytes - 4 * xa - 2 * hl - tma < 4 * (2 * 32 * 4 + 64) + 6 * 256
@@ -221,7 +221,7 @@ def test_host_checks_of_the_tma_entry_points(L):
     assert setm(fake, pa=np.zeros(96, np.uint64)) == 5       # null weight of a rank>0 slot
     # the path: unsupported shapes (rank above 64, n * r_max above 192, k % 64)
     b = lib.lora_plan_bytes(256, ctypes.byref(sh))
-    assert b >= 128 + 64 * 32 + 256 * 32 + 4 * 256
+    assert b >= 128 + 64 * 32 + 512 * 32 + 4 * 256
     for bad in (L.make_shape(32, 128, 4096, [4096]), L.make_shape(32, 64, 4096, [1024] * 4),
                 L.make_shape(32, 64, 4032 + 8, [4096])):
         nb = lib.lora_plan_bytes(256, ctypes.byref(bad))
