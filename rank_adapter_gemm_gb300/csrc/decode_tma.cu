@@ -1234,6 +1234,23 @@ EncodeTiled encode_fn() {
 
 }  // namespace
 
+// A tensor map of a bf16 matrix of `rows` rows of `cols` elements, `ld`
+// elements apart, read in boxes of box_rows x box_cols (box_cols * 2 bytes at
+// most 128 with the 128-byte swizzle); false if the driver's encoder is
+// unavailable or rejects the map.
+bool encode_bf16_rows_map(CUtensorMap *m, const void *base, int64_t ld, int32_t rows, int32_t cols, int32_t box_rows,
+                          int32_t box_cols, bool swizzle128) {
+    EncodeTiled enc = encode_fn();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t str[1] = {static_cast<cuuint64_t>(ld) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t one[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, str, box, one,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------------------
 // Entry points used by lora_abi.cu
 // ---------------------------------------------------------------------------

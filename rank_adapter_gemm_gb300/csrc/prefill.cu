@@ -31,6 +31,7 @@
 // thread), add it to y in fp32, round once to bf16 and write the rows back with
 // coalesced stores.
 #include <algorithm>
+#include <cstring>
 
 #include "common.cuh"
 #include "tc.cuh"
@@ -52,6 +53,13 @@ constexpr int kExpandThreads = 128 + 32 * kEpiWarps;  // warp 0 MMA, 1 operands,
 constexpr int kSmemLimit = 227 * 1024;
 
 struct PrefillArgs {
+    // x as [T][k] in boxes of 128 rows x 64 columns (128-byte swizzle): the
+    // shrink's x tile when the tile's 128 sorted positions are consecutive rows
+    CUtensorMap xmap;
+    // slice i of y as [T][d_i]: loads of 128 rows x 64 columns and stores of 32
+    // rows x 64 columns (128-byte swizzle), for units whose rows are consecutive
+    CUtensorMap yload[LORA_MAX_SLICES];
+    CUtensorMap ystore[LORA_MAX_SLICES];
     const uint16_t *x;
     int64_t ldx;
     uint16_t *y;
@@ -101,6 +109,15 @@ __device__ __forceinline__ void sts_f4(uint32_t addr, float a, float b, float c,
     asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" :: "r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
+// Tensor-map store of a 2-D box from shared memory, in this thread's bulk group.
+__device__ __forceinline__ void tma_store_2d(const void *map, int32_t x, int32_t y, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                 :: "l"(map), "r"(x), "r"(y), "r"(src) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // y (8 bf16 in v) + s * acc[0..8) in fp32, rounded once to bf16.
 __device__ __forceinline__ uint4 add_scaled(uint4 v, const uint32_t *acc, float s) {
     uint4 o;
@@ -123,8 +140,8 @@ __host__ __device__ constexpr uint32_t tmem_cols_for(int c) {
 // for each slice], all 128-byte swizzled K-major; then barriers and tables.  After
 // the main loop the stage area holds the fp32 partial [128][n*RP + 4].
 template <int RP>
-__global__ void __launch_bounds__(kShrinkThreads) tc_shrink_kernel(PrefillArgs a, Shape sh, const void *table,
-                                                                   int32_t stages) {
+__global__ void __launch_bounds__(kShrinkThreads) tc_shrink_kernel(const __grid_constant__ PrefillArgs a, Shape sh,
+                                                                   const void *table, int32_t stages) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
     unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -153,6 +170,11 @@ __global__ void __launch_bounds__(kShrinkThreads) tc_shrink_kernel(PrefillArgs a
     const int32_t nloc = static_cast<int32_t>((crank + 1) * nkb / KS) - kb_lo;
     const uint32_t tcols = tmem_cols_for(NC);
 
+    // A tile whose sorted positions hold consecutive rows of x (the tokens of
+    // one request in a prefill batch) takes its x rows as one tensor-map copy
+    // per k-block; other tiles gather them row by row.
+    const int32_t first = a.sorted_ids[ti.p0];
+    bool row_ok = true;
     if (threadIdx.x < kTile) {
         int32_t t = -1;
         if (static_cast<int32_t>(threadIdx.x) < ti.len) {
@@ -161,6 +183,7 @@ __global__ void __launch_bounds__(kShrinkThreads) tc_shrink_kernel(PrefillArgs a
                 report_error(a.err, LORA_ERR_INVALID_ARG);
                 t = -1;
             }
+            row_ok = t >= 0 && t == first + static_cast<int32_t>(threadIdx.x);
         }
         s_tok[threadIdx.x] = t;
     }
@@ -178,7 +201,7 @@ __global__ void __launch_bounds__(kShrinkThreads) tc_shrink_kernel(PrefillArgs a
         tc::tmem_alloc(tmem_slot, tcols);
         tc::fence_before_sync();
     }
-    __syncthreads();
+    const bool contig = __syncthreads_and(row_ok) != 0;
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const uint32_t sbase = tc::smem_u32(smem);
@@ -195,12 +218,22 @@ __global__ void __launch_bounds__(kShrinkThreads) tc_shrink_kernel(PrefillArgs a
             }
             const int32_t c0 = (kb_lo + it) * kKB;
             const uint32_t xs = sbase + st * stage_bytes;
+            if (contig) {
+                // rows past the tile are other tokens' x or the map's zero fill:
+                // their sums are never read
+                if (tid == 0) {
+                    tc::mbar_expect_tx(&full[st], kXStage);
+                    tc::tma_load_2d(xs, &a.xmap, c0, first, &full[st]);
+                }
+            } else {
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const int q = tid + kTile * m, row = q >> 3, c = q & 7;
-                const int32_t t = s_tok[row], col = c0 + 8 * c;
-                const bool v = t >= 0 && col < sh.k;
-                tc::cp16(xs + tc::swz_offset(row, c, 128), v ? a.x + static_cast<int64_t>(t) * a.ldx + col : a.x, v);
+                for (int m = 0; m < 8; ++m) {
+                    const int q = tid + kTile * m, row = q >> 3, c = q & 7;
+                    const int32_t t = s_tok[row], col = c0 + 8 * c;
+                    const bool v = t >= 0 && col < sh.k;
+                    tc::cp16(xs + tc::swz_offset(row, c, 128), v ? a.x + static_cast<int64_t>(t) * a.ldx + col : a.x,
+                             v);
+                }
             }
             for (int q = tid; q < NC * 8; q += kTile) {
                 const int i = q / (RP * 8), j = (q >> 3) % RP, c = q & 7;
@@ -337,8 +370,8 @@ __device__ __forceinline__ Unit unit_info(int64_t u, int32_t per_tile, const Chu
 // width), `ystages` (even) y buffers of 128 rows x 128 bytes (128-byte swizzle),
 // then barriers, the tile table and the segment offsets.
 template <int RP>
-__global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(PrefillArgs a, Shape sh, const void *table,
-                                                                      int32_t ystages) {
+__global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(const __grid_constant__ PrefillArgs a, Shape sh,
+                                                                      const void *table, int32_t ystages) {
     constexpr int rowb = RP * 2;
     constexpr uint32_t layout = rowb == 128 ? tc::kLayoutSW128 : (rowb == 64 ? tc::kLayoutSW64 : tc::kLayoutSW32);
     constexpr int xa_bytes = kTile * rowb;
@@ -461,10 +494,13 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(PrefillArg
     } else if (warp < 4) {
         // ---- y rows of the unit, 64 columns per buffer; the next unit's token
         // ids are fetched while this unit's copies are issued ----
+        // A unit whose rows are consecutive rows of y takes each buffer as one
+        // tensor-map copy (thread 0); otherwise 16-byte copies per row.
         const int yt = threadIdx.x - 64;  // 0..63
         int32_t yit = 0;
         bool stop = false;
         int32_t tok[16], tok_next[16];
+        int2 ends = make_int2(0, 0), ends_next;  // the unit's first and last token ids
         Unit un_next = unit_info(u_lo, per_tile, cp, sh, s_pref, s_seg);
         auto fetch = [&](const Unit &un, int32_t (&dst)[16]) {
 #pragma unroll
@@ -473,16 +509,22 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(PrefillArg
                 const int32_t t = row < un.len ? a.sorted_ids[un.p0 + row] : -1;
                 dst[m] = t < a.T ? t : -1;
             }
+            return make_int2(a.sorted_ids[un.p0], a.sorted_ids[un.p0 + un.len - 1]);
         };
-        fetch(un_next, tok_next);
+        ends_next = fetch(un_next, tok_next);
         for (int64_t u = u_lo; u < u_hi && !stop; ++u) {
             const Unit un = un_next;
+            ends = ends_next;
 #pragma unroll
             for (int m = 0; m < 16; ++m) tok[m] = tok_next[m];
             if (u + 1 < u_hi) {
                 un_next = unit_info(u + 1, per_tile, cp, sh, s_pref, s_seg);
-                fetch(un_next, tok_next);
+                ends_next = fetch(un_next, tok_next);
             }
+            // a slot's sorted positions hold strictly increasing token ids (the sort
+            // is stable), so first and last ids len - 1 apart mean consecutive rows
+            const int32_t first = ends.x;
+            const bool contig = ends.x >= 0 && ends.y < a.T && ends.y - ends.x == un.len - 1;
             const int nsub = (un.width + kSub - 1) / kSub;
             for (int q = 0; q < nsub; ++q, ++yit) {
                 const int yb = yit % ystages;
@@ -492,13 +534,22 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(PrefillArg
                     break;
                 }
                 const uint32_t dst = ybase + yb * kYBuf;
-                const int c = yt & 7, col = q * kSub + 8 * c;
-                const uint16_t *ycol = a.y + sh.off[un.i] + un.c0 + col;
+                if (contig) {
+                    // rows past the unit are other tokens' y or the map's zero fill: never stored
+                    if (yt == 0) {
+                        tc::mbar_expect_tx(&y_full[yb], kYBuf);
+                        tc::tma_load_2d(dst, &a.yload[un.i], un.c0 + q * kSub, first, &y_full[yb]);
+                    }
+                } else {
+                    const int c = yt & 7, col = q * kSub + 8 * c;
+                    const uint16_t *ycol = a.y + sh.off[un.i] + un.c0 + col;
 #pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const int row = (yt >> 3) + 8 * m;
-                    if (tok[m] >= 0 && col < un.width)
-                        tc::cp16(dst + tc::swz_offset(row, c, 128), ycol + static_cast<int64_t>(tok[m]) * a.ldy, true);
+                    for (int m = 0; m < 16; ++m) {
+                        const int row = (yt >> 3) + 8 * m;
+                        if (tok[m] >= 0 && col < un.width)
+                            tc::cp16(dst + tc::swz_offset(row, c, 128), ycol + static_cast<int64_t>(tok[m]) * a.ldy,
+                                     true);
+                    }
                 }
                 tc::cp_arrive_noinc(&y_full[yb]);
             }
@@ -527,6 +578,9 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(PrefillArg
             }
             tc::fence_after_sync();
             const float sc = tab.scale[un.s];
+            // this warp's 32 rows consecutive rows of y: one tensor-map store per buffer
+            const int32_t first_w = __shfl_sync(0xffffffffu, t, 0);
+            const bool wcontig = __all_sync(0xffffffffu, t >= 0 && t == first_w + lane);
             const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * eq) << 16) + b * kCols;
             uint16_t *yrow = a.y + sh.off[un.i] + un.c0;
             const int nsub = (un.width + kSub - 1) / kSub;
@@ -552,25 +606,38 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(PrefillArg
                         }
                     }
                 }
-                __syncwarp();
-                // coalesced write-back of this warp's 32 rows: 4 rows x 128 bytes per step
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const int rr = (lane >> 3) + 4 * m, c = lane & 7;
-                    const int32_t tr = __shfl_sync(0xffffffffu, t, rr);
-                    const int col = q * kSub + 8 * c;
-                    if (tr >= 0 && col < un.width) {
-                        const uint4 v = lds_u4(ys + tc::swz_offset(32 * eq + rr, c, 128));
-                        stg_u4(yrow + static_cast<int64_t>(tr) * a.ldy + col, v);
+                if (wcontig) {
+                    // columns past the slice are clipped by the slice's map
+                    tc::fence_async_smem();  // the rows (generic proxy) before the store reads them
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&a.ystore[un.i], un.c0 + q * kSub, first_w, ys + 32 * eq * 128);
+                        bulk_commit();
+                        bulk_wait_read();  // the buffer may be refilled once the store has read it
                     }
+                    __syncwarp();
+                } else {
+                    __syncwarp();
+                    // coalesced write-back of this warp's 32 rows: 4 rows x 128 bytes per step
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {
+                        const int rr = (lane >> 3) + 4 * m, c = lane & 7;
+                        const int32_t tr = __shfl_sync(0xffffffffu, t, rr);
+                        const int col = q * kSub + 8 * c;
+                        if (tr >= 0 && col < un.width) {
+                            const uint4 v = lds_u4(ys + tc::swz_offset(32 * eq + rr, c, 128));
+                            stg_u4(yrow + static_cast<int64_t>(tr) * a.ldy + col, v);
+                        }
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&y_empty[yb]);
             }
             if (stop) break;
             tc::fence_before_sync();
             if (lane == 0) tc::mbar_arrive(&acc_empty[b]);
         }
+        if (lane == 0) bulk_wait_all();  // the stores are complete before the CTA leaves
     }
     __syncthreads();
     if (warp == 0) {
@@ -660,6 +727,9 @@ cudaError_t launch_rp(const PrefillArgs &a, const Shape &sh, const void *table, 
 
 }  // namespace
 
+bool encode_bf16_rows_map(CUtensorMap *m, const void *base, int64_t ld, int32_t rows, int32_t cols, int32_t box_rows,
+                          int32_t box_cols, bool swizzle128);
+
 bool prefill_supported(int32_t r_max) { return r_max <= 64; }
 
 cudaError_t launch_prefill(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
@@ -668,8 +738,26 @@ cudaError_t launch_prefill(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t 
     if (!prefill_supported(sh.r_max)) return cudaErrorNotSupported;
     const WorkspaceLayout L(T, sh.n, sh.r_max, sh.S);
     char *w = reinterpret_cast<char *>(ws);
-    PrefillArgs a{x, ldx, y, ldy, sorted_ids, seg, reinterpret_cast<uint16_t *>(w + L.hi_off),
-                  reinterpret_cast<uint16_t *>(w + L.lo_off), T, err};
+    PrefillArgs a;
+    std::memset(&a, 0, sizeof a);
+    // (a map needs at least one row; with T = 0 no tile reads it)
+    if (!encode_bf16_rows_map(&a.xmap, x, ldx, std::max(T, 1), sh.k, kTile, kKB, true)) return cudaErrorNotSupported;
+    for (int i = 0; i < sh.n; ++i) {
+        const int32_t di = sh.off[i + 1] - sh.off[i];
+        if (!encode_bf16_rows_map(&a.yload[i], y + sh.off[i], ldy, std::max(T, 1), di, kTile, kSub, true) ||
+            !encode_bf16_rows_map(&a.ystore[i], y + sh.off[i], ldy, std::max(T, 1), di, 32, kSub, true))
+            return cudaErrorNotSupported;
+    }
+    a.x = x;
+    a.ldx = ldx;
+    a.y = y;
+    a.ldy = ldy;
+    a.sorted_ids = sorted_ids;
+    a.seg = seg;
+    a.xa_hi = reinterpret_cast<uint16_t *>(w + L.hi_off);
+    a.xa_lo = reinterpret_cast<uint16_t *>(w + L.lo_off);
+    a.T = T;
+    a.err = err;
     switch (tc_rank_pad(sh.r_max)) {
     case 16: return launch_rp<16>(a, sh, table, stream);
     case 32: return launch_rp<32>(a, sh, table, stream);
