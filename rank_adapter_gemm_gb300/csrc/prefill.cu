@@ -257,9 +257,11 @@ __global__ void __launch_bounds__(kShrinkThreads) tc_shrink_kernel(const __grid_
         tc::fence_async_smem();
         for (int32_t it = max(0, nloc - depth); it < nloc; ++it) tc::mbar_arrive(&full[it % stages]);
     } else {
-        // ---- MMA issuer: D[:, i*RP .. +RP) += x_tile A_i^T over this CTA's k range ----
+        // ---- MMA issuer: D[:, i*RP .. +RP) += x_tile A_i^T over this CTA's k range;
+        // the slices' A rows sit back to back in the stage, so one MMA of N = n RP
+        // covers them all ----
         if (lane == 0) {
-            const uint32_t idesc = tc::idesc_bf16(kTile, RP);
+            const uint32_t idesc = tc::idesc_bf16(kTile, NC);
             for (int32_t it = 0; it < nloc; ++it) {
                 const int st = it % stages;
                 if (!tc::mbar_wait(&full[st], (it / stages) & 1, abort_flag, kWaitNs)) {
@@ -269,13 +271,9 @@ __global__ void __launch_bounds__(kShrinkThreads) tc_shrink_kernel(const __grid_
                 tc::fence_after_sync();
                 const uint32_t xs = sbase + st * stage_bytes;
 #pragma unroll
-                for (int kk = 0; kk < kKB / 16; ++kk) {
-                    const uint64_t ad = tc::smem_desc(xs + 32 * kk, 1024, tc::kLayoutSW128);
-                    for (int i = 0; i < n; ++i) {
-                        const uint64_t bd = tc::smem_desc(xs + kXStage + i * RP * 128 + 32 * kk, 1024, tc::kLayoutSW128);
-                        tc::mma_bf16(tmem + i * RP, ad, bd, idesc, it > 0 || kk > 0);
-                    }
-                }
+                for (int kk = 0; kk < kKB / 16; ++kk)
+                    tc::mma_bf16(tmem, tc::smem_desc(xs + 32 * kk, 1024, tc::kLayoutSW128),
+                                 tc::smem_desc(xs + kXStage + 32 * kk, 1024, tc::kLayoutSW128), idesc, it > 0 || kk > 0);
                 tc::mma_commit(&empty[st]);
             }
             tc::mma_commit(done);  // arrives once every MMA issued above has completed
@@ -698,7 +696,7 @@ cudaError_t launch_rp(const PrefillArgs &a, const Shape &sh, const void *table, 
     const int64_t tiles_bound = ceil_div(a.T, kTile) + std::min<int64_t>(sh.S, a.T);
     const int64_t tiles_est = ceil_div(a.T, kTile);
     const int64_t nkb = ceil_div(sh.k, kKB);
-    int64_t ks = (2 * sms) / std::max<int64_t>(1, tiles_est);
+    int64_t ks = (4 * sms) / std::max<int64_t>(1, tiles_est);
     ks = std::max<int64_t>(1, std::min<int64_t>({ks, 8, std::max<int64_t>(1, nkb / 2)}));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(ks), static_cast<unsigned>(tiles_bound));
