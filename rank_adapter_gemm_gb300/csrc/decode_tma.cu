@@ -152,6 +152,7 @@ __host__ __device__ inline int32_t pad16i(int32_t v) { return (v + 15) & ~15; }
 __host__ __device__ inline int32_t ytile_rows(int32_t gsz) { return (gsz + 7) & ~7; }
 constexpr int32_t kGatherCost = 88;  // a four-row gather's fixed cost beyond its 512 bytes (16-byte units)
 constexpr int32_t kUnitCost = 384;   // an expand unit's fixed cost (16-byte units)
+constexpr int32_t kShrinkStageCost = 1600;  // a shrink stage's fixed cost, shared by its k-blocks (16-byte units)
 // Width in ranks of a slot's B boxes (the rank rounded up to 16, 32 or 64;
 // ranks past r are the tensor map's zero fill).
 __host__ __device__ inline int32_t b_box_ranks(int32_t r) { return r <= 16 ? 16 : (r <= 32 ? 32 : 64); }
@@ -1106,7 +1107,8 @@ __global__ void __launch_bounds__(512) tma_plan_kernel(PArgs pa, Shape sh, TmaPl
         // weights in 16-byte units: the bytes a piece moves plus the fixed costs
         // that bound small pieces (a four-row gather of x, an expand unit's
         // share of its stage's tensor-core round trip, epilogue and barriers)
-        rec.wps = (nr + gs) * 8 + kGatherCost * ((gs + 3) >> 2);  // A and x rows of one k-block
+        // A and x rows of one k-block, plus its share of the stage's fixed cost
+        rec.wps = (nr + gs) * 8 + kGatherCost * ((gs + 3) >> 2) + kShrinkStageCost / cs;
         rec.wpe = 16 * r + 32 * ge + kUnitCost;                   // B tile [128][r], y rows read + written
         rec.rp = b_box_ranks(r);
         // as many 128-column units of one run per stage as fit: the B boxes and
