@@ -151,7 +151,7 @@ __host__ __device__ inline int32_t pad16i(int32_t v) { return (v + 15) & ~15; }
 // Rows of an expand unit's y tile in the stage: the group rounded up to 8.
 __host__ __device__ inline int32_t ytile_rows(int32_t gsz) { return (gsz + 7) & ~7; }
 constexpr int32_t kGatherCost = 88;  // a four-row gather's fixed cost beyond its 512 bytes (16-byte units)
-constexpr int32_t kUnitCost = 384;   // an expand unit's fixed cost (16-byte units)
+constexpr int32_t kUnitCost = 1536;  // an expand unit's fixed cost (16-byte units)
 constexpr int32_t kShrinkStageCost = 1600;  // a shrink stage's fixed cost, shared by its k-blocks (16-byte units)
 // Width in ranks of a slot's B boxes (the rank rounded up to 16, 32 or 64;
 // ranks past r are the tensor map's zero fill).
