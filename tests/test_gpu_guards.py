@@ -195,3 +195,25 @@ def test_strided_rows_moe():
                                wl.ranks, scales, m.A, m.B)
     assert st == 0
     assert_y_close(to_host_bits(y.contiguous()), ref, "strided moe")
+
+
+def test_strided_rows_prefill_request_major_tma_tiles():
+    """Request-major prefill batch whose tiles mostly hold consecutive rows (the
+    tensor-map copies of x and y and the per-warp tensor-map stores): ragged
+    request lengths (tiles that end mid-buffer), adapters shared by several
+    requests (tiles that straddle two requests gather row by row), k not a
+    multiple of 64, slice widths not multiples of 64, x and y as column windows
+    with canary bands, two calls in a row."""
+    wl = W.generate(name="req_tma", seed=57, T=None, S=3, rank_choices=[16, 32, 64],
+                    modules=[{"name": "m", "k": 1000, "slices": [200, 72, 328]}],
+                    requests={"n": 7, "min_len": 100, "max_len": 700, "n_adapters": 3},
+                    alpha=16.0, y_init="normal")
+    assert wl.r_max <= 64
+    g = Guarded(wl)
+    ref, _ = oracle_y(wl)
+    for call in range(2):
+        g.y.copy_(g.y0)
+        g.L.lora_apply(g.x, g.y, g.rp.shape, g.rp.table.dev, g.sorted_ids, g.seg, g.active, g.ws, g.err,
+                       max_seg_hint=wl.T, path="prefill")
+        g.check(f"prefill request-major call {call}")
+        assert_y_close(g.y_bits(), ref, "strided request-major prefill")
