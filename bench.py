@@ -57,7 +57,8 @@ def parse_args(argv=None):
     p.add_argument("--path", default="best", choices=["best", "auto", "decode_fused", "decode_split", "prefill",
                                                         "decode_direct", "decode_direct_fp8", "decode_tma"],
                    help="best: the library's fastest measured path for the workload (default_path); auto: "
-                        "LORA_PATH_AUTO (decode_direct_fp8 for a workload with FP8 adapters)")
+                        "LORA_PATH_AUTO (decode_direct_fp8 for a workload with FP8 adapters); decode_moe takes "
+                        "decode_direct or decode_tma (best: decode_direct)")
     p.add_argument("--configs", default="all",
                    help="after the headline, one record per other workload: 'all', 'none' or a comma list of "
                         + ", ".join(SUB_CONFIGS))
@@ -668,7 +669,7 @@ class MoeBench:
     with x per token, w2 with x per pair) in its own buffers; one pair index per
     step, per-step plans unless no_plan."""
 
-    def __init__(self, wl, n_layers, dev, no_plan=False):
+    def __init__(self, wl, n_layers, dev, no_plan=False, path=None):
         import torch
         import rank_adapter_gemm_gb300 as L
         from rank_adapter_gemm_gb300.resident import ResidentMoeProjection, clone_moe
@@ -682,7 +683,12 @@ class MoeBench:
         self.slot_dev = torch.from_numpy(wl.slot_ids).to(dev)
         self.expert_dev = torch.from_numpy(wl.expert_ids.reshape(-1).copy()).to(dev)
         self.ws = [L.Workspace(P, b.shape, device=dev) for b in base]
-        self.plans = [] if no_plan else [L.Plan(P, lay.shape, device=dev) for lay in self.layers]
+        if path is None:
+            # measured on GB300 (Mixtral expert shapes, 32 interleaved w1/w2 calls): both paths take
+            # about 24.3 us per call, and the TMA plans cost 17 us more per step
+            path = "decode_direct"
+        self.path = path
+        self.plans = [] if no_plan else [L.Plan(P, lay.shape, path=path, device=dev) for lay in self.layers]
         self.bytes_per_call = [moe_algorithmic_bytes(wl, m) for m in self.mods]
 
     def index_part(self):
@@ -697,7 +703,7 @@ class MoeBench:
         for l, lay in enumerate(self.layers):
             L.lora_apply_moe(lay.x, lay.y, wl.K, lay.shape, lay.table.dev, self.index.sorted_ids,
                              self.index.seg_offsets, self.index.active, self.ws[l % len(self.ws)].buf, self.index.err,
-                             x_per_token=lay.x_per_token, plan=self.plans[l] if self.plans else None)
+                             x_per_token=lay.x_per_token, plan=self.plans[l] if self.plans else None, path=self.path)
 
 
 def run_moe(args):
@@ -709,7 +715,8 @@ def run_moe(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = W.moe_config()
-    mb = MoeBench(wl, args.layers, dev, no_plan=args.no_plan)
+    mb = MoeBench(wl, args.layers, dev, no_plan=args.no_plan,
+                  path=args.path if args.path in ("decode_direct", "decode_tma") else None)
     elapsed_s, apply_ms_mean, index_ms_mean, clocks, (peak_gbs, peak_tf, peak_src) = \
         time_steps(args, dev, local, mb.index_part, mb.apply_part)
     err = int(mb.index.err.item())
@@ -741,7 +748,7 @@ def run_moe(args):
             "config": args.config,
             "layers_per_step": len(layers),
             "calls_per_step": len(layers),
-            "path": "lora_apply_moe (warp-streaming decode kernels over n_adapters * E virtual slots)"
+            "path": f"lora_apply_moe on {mb.path} over n_adapters * E virtual slots"
                     + (" with per-step plans" if mb.plans else ""),
             "l2": f"inputs larger than L2: {len(layers)} distinct layer buffer sets, "
                   f"{sum(per_layer_bytes) / 1e9:.2f} GB of algorithmic bytes per step",
@@ -809,7 +816,7 @@ def config_records(args, dev, local, peak_gbs):
             per_call = [moe_algorithmic_bytes(wl, m) for m in range(len(wl.modules))]
             n_layers = len(per_call) * max(1, int(np.ceil(4 * L2_BYTES / sum(per_call))))
             bench = MoeBench(wl, n_layers, dev)
-            path = "lora_apply_moe with per-step plans"
+            path = f"lora_apply_moe on {bench.path} with per-step plans"
             calls_per_step = len(bench.layers)
         else:
             wl = W.config(spec["index"], y_init="normal", sweep=spec.get("sweep", False))

@@ -578,6 +578,33 @@ lora_status_t lora_apply_moe_plan(const void *x, int64_t ldx, int32_t x_per_toke
                                   int32_t K, const lora_shape_t *shape, const void *plan, size_t plan_bytes, float *ws,
                                   size_t ws_bytes, int32_t *err, lora_stream_t stream);
 
+/*
+ * lora_apply_moe on an explicit path: LORA_PATH_DECODE_DIRECT (what
+ * lora_apply_moe runs) or LORA_PATH_DECODE_TMA, the one-kernel tensor-map
+ * decode over the pairs.  The TMA path needs dev_table to be a table of
+ * lora_set_slot_table_tma over the virtual slots (the entries of
+ * lora_moe_slot_pointers), x 16-byte aligned with ldx a multiple of 8, and
+ * T K and the shape within the limits of LORA_PATH_DECODE_TMA in lora_apply_ex;
+ * it builds its plan in the workspace, like lora_apply_ex.  Any other path:
+ * LORA_ERR_UNSUPPORTED.  Checks and errors otherwise as lora_apply_moe.
+ */
+lora_status_t lora_apply_moe_ex(const void *x, int64_t ldx, int32_t x_per_token, void *y, int64_t ldy, int32_t T,
+                                int32_t K, const lora_shape_t *shape, const void *dev_table, const int32_t *sorted_ids,
+                                const int32_t *seg_offsets, const int32_t *active, lora_path_t path, float *ws,
+                                size_t ws_bytes, int32_t *err, lora_stream_t stream);
+
+/*
+ * lora_apply_moe_plan on an explicit path (LORA_PATH_DECODE_DIRECT or
+ * LORA_PATH_DECODE_TMA); the plan must have been built by lora_build_plan(s)
+ * for T * K rows with the same path (a TMA plan on a table of
+ * lora_set_slot_table_tma).  Checks and errors as lora_apply_moe_ex and
+ * lora_apply_plan.
+ */
+lora_status_t lora_apply_moe_plan_ex(const void *x, int64_t ldx, int32_t x_per_token, void *y, int64_t ldy,
+                                     int32_t T, int32_t K, const lora_shape_t *shape, const void *plan,
+                                     size_t plan_bytes, lora_path_t path, float *ws, size_t ws_bytes, int32_t *err,
+                                     lora_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -334,11 +334,13 @@ def lora_build_index_moe(slot_ids, expert_ids, K, E, S, dev_table, sorted_ids, s
 
 
 def lora_apply_moe(x, y, K, shape, dev_table, sorted_ids, seg_offsets, active, ws, err, x_per_token: bool = True,
-                   stream=None, plan=None) -> None:
+                   stream=None, plan=None, path: str = "decode_direct") -> None:
     """Routed-expert branch: y [T*K, d] per (token, choice) pair; x [T, k] shared
-    by a token's experts (x_per_token) or [T*K, k] per pair.  With `plan` (a Plan
-    built for T*K rows on the virtual table and the pair index) the table and
-    index arguments are not used."""
+    by a token's experts (x_per_token) or [T*K, k] per pair.  `path` is
+    "decode_direct" or "decode_tma" (dev_table then a tensor-map table of the
+    virtual slots).  With `plan` (a Plan built for T*K rows on the virtual table
+    and the pair index) the table and index arguments are not used and the
+    plan's path is run."""
     ldx = _rows(x, "x")
     ldy = _rows(y, "y")
     P = int(y.shape[0])
@@ -348,13 +350,14 @@ def lora_apply_moe(x, y, K, shape, dev_table, sorted_ids, seg_offsets, active, w
     if int(x.shape[0]) != (T if x_per_token else P):
         raise ValueError("x must have T rows (x_per_token) or T * K rows")
     if plan is not None:
-        check(load().lora_apply_moe_plan(_p(x), ldx, int(bool(x_per_token)), _p(y), ldy, T, int(K), ctypes.byref(shape),
-                                         _p(plan.buf), plan.buf.numel(), _p(ws), ws.numel() * ws.element_size(), _p(err),
-                                         _stream(stream)), "lora_apply_moe_plan")
+        check(load().lora_apply_moe_plan_ex(_p(x), ldx, int(bool(x_per_token)), _p(y), ldy, T, int(K),
+                                            ctypes.byref(shape), _p(plan.buf), plan.buf.numel(), PATHS[plan.path],
+                                            _p(ws), ws.numel() * ws.element_size(), _p(err), _stream(stream)),
+              "lora_apply_moe_plan_ex")
         return
-    check(load().lora_apply_moe(_p(x), ldx, int(bool(x_per_token)), _p(y), ldy, T, int(K), ctypes.byref(shape),
-                                _p(dev_table), _p(sorted_ids), _p(seg_offsets), _p(active), _p(ws),
-                                ws.numel() * ws.element_size(), _p(err), _stream(stream)), "lora_apply_moe")
+    check(load().lora_apply_moe_ex(_p(x), ldx, int(bool(x_per_token)), _p(y), ldy, T, int(K), ctypes.byref(shape),
+                                   _p(dev_table), _p(sorted_ids), _p(seg_offsets), _p(active), PATHS[path], _p(ws),
+                                   ws.numel() * ws.element_size(), _p(err), _stream(stream)), "lora_apply_moe_ex")
 
 
 def lora_plan_bytes(T: int, shape: lora_shape_t) -> int:

@@ -44,6 +44,7 @@ EXPORTED = (
     "lora_apply_overlap", "lora_premultiply_e4m3", "lora_moe_slot_pointers", "lora_build_index_moe",
     "lora_apply_moe", "lora_build_index_activated", "lora_plan_bytes", "lora_build_plan", "lora_apply_plan",
     "lora_build_plans", "lora_apply_moe_plan", "lora_slot_table_tma_bytes", "lora_set_slot_table_tma",
+    "lora_apply_moe_ex", "lora_apply_moe_plan_ex",
 )
 
 
@@ -115,6 +116,8 @@ def load() -> ctypes.CDLL:
         "lora_apply_moe_plan": (ST, [P, I64, I32, P, I64, I32, I32, SH, P, SZ, P, SZ, P, P]),
         "lora_slot_table_tma_bytes": (SZ, [I32, SH]),
         "lora_set_slot_table_tma": (ST, [P, P, SH, P, P, P, P, P]),
+        "lora_apply_moe_ex": (ST, [P, I64, I32, P, I64, I32, I32, SH, P, P, P, P, ST, P, SZ, P, P]),
+        "lora_apply_moe_plan_ex": (ST, [P, I64, I32, P, I64, I32, I32, SH, P, SZ, ST, P, SZ, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

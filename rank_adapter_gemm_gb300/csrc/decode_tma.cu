@@ -170,6 +170,7 @@ struct TArgs {
     int32_t *gen, *exits;      // call counter, CTAs that finished this call
     int32_t *err;
     int32_t T, S, n, k, r_max;
+    int32_t xdiv;              // x row of y row p: p / xdiv (routed experts sharing a token's x)
     int32_t off[LORA_MAX_SLICES + 1];
 };
 
@@ -648,7 +649,10 @@ __global__ void __launch_bounds__(kThreads, 2) tma_decode_kernel(const __grid_co
             const int32_t gsz = min(sl.gs, sl.cnt - g * sl.gs), gpad = pad16i(gsz), nq = (gsz + 3) >> 2;
             if (g != cur_g) {
                 __syncwarp();
-                for (int32_t r = lane; r < gsz; r += 32) s_xids[r] = __ldcg(C.ids + sl.seg0 + g * sl.gs + r);
+                for (int32_t r = lane; r < gsz; r += 32) {
+                    const int32_t p = __ldcg(C.ids + sl.seg0 + g * sl.gs + r);
+                    s_xids[r] = a.xdiv == 1 ? p : p / a.xdiv;
+                }
                 __syncwarp();
                 cur_g = g;
             }
@@ -1357,7 +1361,8 @@ cudaError_t launch_tma_plans(const Shape &sh, const void *const *tables, unsigne
 // the two fp32 sum sets of [T][n r_max].
 cudaError_t launch_tma_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                               const unsigned char *plan, float *acc0, float *acc1, int32_t *ctrl, int32_t T,
-                              int32_t *err, cudaStream_t stream) {
+                              int32_t *err, cudaStream_t stream, int32_t xdiv) {
+    if (xdiv < 1 || T % xdiv != 0) return cudaErrorInvalidValue;
     if (!decode_tma_supported(T, sh)) return cudaErrorNotSupported;
     int grid = 0;
     cudaError_t e = static_cast<cudaError_t>(tma_grid_now(grid));
@@ -1369,7 +1374,7 @@ cudaError_t launch_tma_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int64
     memset(&a, 0, sizeof a);
     {
         // x: [T][k] rows of ldx elements, box [1][64], 128-byte swizzle (the shrink's x tiles)
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(sh.k), static_cast<cuuint64_t>(T)};
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(sh.k), static_cast<cuuint64_t>(T / xdiv)};
         const cuuint64_t str[1] = {static_cast<cuuint64_t>(ldx) * 2};
         const cuuint32_t box[2] = {64, 1}, one[2] = {1, 1};
         if (enc(&a.xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims, str, box, one,
@@ -1390,6 +1395,7 @@ cudaError_t launch_tma_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int64
     a.exits = a.gen + 1;
     a.err = err;
     a.T = T;
+    a.xdiv = xdiv;
     a.S = sh.S;
     a.n = sh.n;
     a.k = sh.k;

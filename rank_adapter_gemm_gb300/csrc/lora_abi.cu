@@ -58,7 +58,7 @@ cudaError_t launch_tma_plans(const Shape &sh, const void *const *tables, unsigne
                              int32_t *err, cudaStream_t stream);
 cudaError_t launch_tma_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                               const unsigned char *plan, float *acc0, float *acc1, int32_t *ctrl, int32_t T,
-                              int32_t *err, cudaStream_t stream);
+                              int32_t *err, cudaStream_t stream, int32_t xdiv = 1);
 }  // namespace lora
 
 using lora::Shape;
@@ -99,13 +99,13 @@ lora_path_t resolve(lora_path_t path, int32_t T, int32_t max_seg_hint, const Sha
 
 // The one-kernel TMA decode call on a plan (its own or the workspace's).
 lora_status_t tma_call(const void *x, int64_t ldx, void *y, int64_t ldy, int32_t T, const Shape &sh,
-                       const unsigned char *plan, float *ws, int32_t *err, cudaStream_t s) {
+                       const unsigned char *plan, float *ws, int32_t *err, cudaStream_t s, int32_t xdiv = 1) {
     const lora::WorkspaceLayout L(T, sh.n, sh.r_max, sh.S);
     char *base = reinterpret_cast<char *>(ws);
     return from_cuda(lora::launch_tma_decode(static_cast<const uint16_t *>(x), ldx, static_cast<uint16_t *>(y), ldy,
                                              sh, plan, reinterpret_cast<float *>(base + L.tacc0_off),
                                              reinterpret_cast<float *>(base + L.tacc1_off),
-                                             reinterpret_cast<int32_t *>(base + L.tctrl_off), T, err, s));
+                                             reinterpret_cast<int32_t *>(base + L.tctrl_off), T, err, s, xdiv));
 }
 
 float *xa_of(float *ws, int32_t T, const Shape &sh) {
@@ -464,10 +464,10 @@ lora_status_t lora_apply_overlap(const void *x, int64_t ldx, void *y, int64_t ld
                          ws_bytes, err, stream);
 }
 
-lora_status_t lora_apply_moe(const void *x, int64_t ldx, int32_t x_per_token, void *y, int64_t ldy, int32_t T,
-                             int32_t K, const lora_shape_t *shape, const void *dev_table, const int32_t *sorted_ids,
-                             const int32_t *seg_offsets, const int32_t *active, float *ws, size_t ws_bytes,
-                             int32_t *err, lora_stream_t stream) {
+lora_status_t lora_apply_moe_ex(const void *x, int64_t ldx, int32_t x_per_token, void *y, int64_t ldy, int32_t T,
+                                int32_t K, const lora_shape_t *shape, const void *dev_table, const int32_t *sorted_ids,
+                                const int32_t *seg_offsets, const int32_t *active, lora_path_t path, float *ws,
+                                size_t ws_bytes, int32_t *err, lora_stream_t stream) {
     Shape sh;
     lora_status_t st;
     if (T < 0 || K < 1 || static_cast<int64_t>(T) * K > INT32_MAX) return LORA_ERR_INVALID_ARG;
@@ -477,11 +477,30 @@ lora_status_t lora_apply_moe(const void *x, int64_t ldx, int32_t x_per_token, vo
     if ((st = check_rows(x, ldx, x_per_token ? T : P, sh.k)) != LORA_OK) return st;
     if ((st = check_rows(y, ldy, P, sh.off[sh.n])) != LORA_OK) return st;
     if ((st = check_ws(ws, ws_bytes, P, sh)) != LORA_OK) return st;
+    if (path != LORA_PATH_DECODE_DIRECT && path != LORA_PATH_DECODE_TMA) return LORA_ERR_UNSUPPORTED;
     if (P == 0) return LORA_OK;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (path == LORA_PATH_DECODE_TMA) {
+        if (!lora::decode_tma_supported(P, sh)) return LORA_ERR_UNSUPPORTED;
+        const lora::WorkspaceLayout L(P, sh.n, sh.r_max, sh.S);
+        unsigned char *plan = reinterpret_cast<unsigned char *>(ws) + L.tplan_off;
+        if (lora::launch_tma_plans(sh, &dev_table, &plan, 1, sorted_ids, seg_offsets, active, P, err, s) !=
+            cudaSuccess)
+            return LORA_ERR_CUDA;
+        return tma_call(x, ldx, y, ldy, P, sh, plan, ws, err, s, x_per_token ? K : 1);
+    }
     if (!lora::decode_direct_supported(P, sh, false)) return LORA_ERR_UNSUPPORTED;
     return from_cuda(lora::launch_decode_direct(static_cast<const uint16_t *>(x), ldx, static_cast<uint16_t *>(y), ldy,
-                                                sh, dev_table, sorted_ids, seg_offsets, active, ws, P, err, false,
-                                                reinterpret_cast<cudaStream_t>(stream), x_per_token ? K : 1));
+                                                sh, dev_table, sorted_ids, seg_offsets, active, ws, P, err, false, s,
+                                                x_per_token ? K : 1));
+}
+
+lora_status_t lora_apply_moe(const void *x, int64_t ldx, int32_t x_per_token, void *y, int64_t ldy, int32_t T,
+                             int32_t K, const lora_shape_t *shape, const void *dev_table, const int32_t *sorted_ids,
+                             const int32_t *seg_offsets, const int32_t *active, float *ws, size_t ws_bytes,
+                             int32_t *err, lora_stream_t stream) {
+    return lora_apply_moe_ex(x, ldx, x_per_token, y, ldy, T, K, shape, dev_table, sorted_ids, seg_offsets, active,
+                             LORA_PATH_DECODE_DIRECT, ws, ws_bytes, err, stream);
 }
 
 size_t lora_plan_bytes(int32_t T, const lora_shape_t *shape) {
@@ -563,9 +582,10 @@ lora_status_t lora_apply_plan(const void *x, int64_t ldx, void *y, int64_t ldy, 
                                                 static_cast<const unsigned char *>(plan)));
 }
 
-lora_status_t lora_apply_moe_plan(const void *x, int64_t ldx, int32_t x_per_token, void *y, int64_t ldy, int32_t T,
-                                  int32_t K, const lora_shape_t *shape, const void *plan, size_t plan_bytes, float *ws,
-                                  size_t ws_bytes, int32_t *err, lora_stream_t stream) {
+lora_status_t lora_apply_moe_plan_ex(const void *x, int64_t ldx, int32_t x_per_token, void *y, int64_t ldy,
+                                     int32_t T, int32_t K, const lora_shape_t *shape, const void *plan,
+                                     size_t plan_bytes, lora_path_t path, float *ws, size_t ws_bytes, int32_t *err,
+                                     lora_stream_t stream) {
     Shape sh;
     lora_status_t st;
     if (T < 0 || K < 1 || static_cast<int64_t>(T) * K > INT32_MAX) return LORA_ERR_INVALID_ARG;
@@ -574,7 +594,15 @@ lora_status_t lora_apply_moe_plan(const void *x, int64_t ldx, int32_t x_per_toke
     if ((st = check_rows(x, ldx, x_per_token ? T : P, sh.k)) != LORA_OK) return st;
     if ((st = check_rows(y, ldy, P, sh.off[sh.n])) != LORA_OK) return st;
     if ((st = check_ws(ws, ws_bytes, P, sh)) != LORA_OK) return st;
+    if (path != LORA_PATH_DECODE_DIRECT && path != LORA_PATH_DECODE_TMA) return LORA_ERR_UNSUPPORTED;
     if (P == 0) return LORA_OK;
+    if (path == LORA_PATH_DECODE_TMA) {
+        if (!lora::decode_tma_supported(P, sh)) return LORA_ERR_UNSUPPORTED;
+        if (plan == nullptr || plan_bytes < lora::tma_plan_bytes(P, sh)) return LORA_ERR_WORKSPACE;
+        if (!aligned16(plan)) return LORA_ERR_ALIGNMENT;
+        return tma_call(x, ldx, y, ldy, P, sh, static_cast<const unsigned char *>(plan), ws, err,
+                        reinterpret_cast<cudaStream_t>(stream), x_per_token ? K : 1);
+    }
     if (!lora::decode_direct_supported(P, sh, false)) return LORA_ERR_UNSUPPORTED;
     if (plan == nullptr || plan_bytes < lora::direct_plan_bytes(P, sh)) return LORA_ERR_WORKSPACE;
     if (!aligned16(plan)) return LORA_ERR_ALIGNMENT;
@@ -582,6 +610,13 @@ lora_status_t lora_apply_moe_plan(const void *x, int64_t ldx, int32_t x_per_toke
                                                 sh, nullptr, nullptr, nullptr, nullptr, ws, P, err, false,
                                                 reinterpret_cast<cudaStream_t>(stream), x_per_token ? K : 1,
                                                 static_cast<const unsigned char *>(plan)));
+}
+
+lora_status_t lora_apply_moe_plan(const void *x, int64_t ldx, int32_t x_per_token, void *y, int64_t ldy, int32_t T,
+                                  int32_t K, const lora_shape_t *shape, const void *plan, size_t plan_bytes, float *ws,
+                                  size_t ws_bytes, int32_t *err, lora_stream_t stream) {
+    return lora_apply_moe_plan_ex(x, ldx, x_per_token, y, ldy, T, K, shape, plan, plan_bytes, LORA_PATH_DECODE_DIRECT,
+                                  ws, ws_bytes, err, stream);
 }
 
 lora_status_t lora_apply(const void *x, int64_t ldx, void *y, int64_t ldy, int32_t T, const lora_shape_t *shape,

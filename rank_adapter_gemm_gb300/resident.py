@@ -169,10 +169,17 @@ class ResidentMoeProjection:
         v_ranks, v_scales, a_ptrs, b_ptrs = lora_moe_slot_pointers(wl.n_adapters, wl.E, self.shape, wl.ranks, scales,
                                                                    a_base, b_base)
         self.ranks, self.scales = np.asarray(wl.ranks, np.int32), scales
-        self.table = SlotTable(V, n, wl.r_max, device=device)
+        self.table = SlotTable(V, n, wl.r_max, device=device, shape=self._table_shape())
         self.table.set(v_ranks, v_scales, a_ptrs, b_ptrs)
         self.x = _to_dev(m.x, device)
         self.y = _to_dev(m.y_in, device)
+
+    def _table_shape(self):
+        """Shapes the one-kernel TMA path takes (r_max <= 64, n_slices * r_max <= 192,
+        k % 64 == 0) get the virtual table with tensor maps."""
+        tma = (self.shape.r_max <= 64 and self.shape.n_slices * self.shape.r_max <= 192
+               and self.shape.k % 64 == 0)
+        return self.shape if tma else None
 
 
 def clone_moe(rp: ResidentMoeProjection, device="cuda") -> ResidentMoeProjection:
@@ -186,7 +193,7 @@ def clone_moe(rp: ResidentMoeProjection, device="cuda") -> ResidentMoeProjection
     b_base = np.array([t.data_ptr() for row in other.B for t in row], dtype=np.uint64)
     v_ranks, v_scales, a_ptrs, b_ptrs = lora_moe_slot_pointers(rp.n_adapters, rp.E, rp.shape, rp.ranks, rp.scales,
                                                                a_base, b_base)
-    other.table = SlotTable(rp.table.S, rp.table.n_slices, rp.table.r_max, device=device)
+    other.table = SlotTable(rp.table.S, rp.table.n_slices, rp.table.r_max, device=device, shape=rp._table_shape())
     other.table.set(v_ranks, v_scales, a_ptrs, b_ptrs)
     other.x = rp.x.clone()
     other.y = rp.y.clone()

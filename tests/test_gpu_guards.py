@@ -162,7 +162,8 @@ def test_strided_rows_prefill_long_segments():
     assert_y_close(g.y_bits(), ref, "strided prefill")
 
 
-def test_strided_rows_moe():
+@pytest.mark.parametrize("path", ["decode_direct", "decode_tma"])
+def test_strided_rows_moe(path):
     """Routed experts: y per (token, choice) pair in a column window, x per token
     in a column window, guarded pair index and workspace."""
     torch = _torch()
@@ -183,7 +184,7 @@ def test_strided_rows_moe():
                            torch.from_numpy(wl.expert_ids.reshape(-1).copy()).cuda(), wl.K, wl.E, V, rp.table.dev,
                            sorted_ids, seg, active, err)
     L.lora_apply_moe(x, y, wl.K, rp.shape, rp.table.dev, sorted_ids, seg, active, ws, err,
-                     x_per_token=rp.x_per_token)
+                     x_per_token=rp.x_per_token, path=path)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     for big, view, what in ((ybig, y, "y"), (xbig, x, "x"), (wbig, ws, "ws"), (sbig, sorted_ids, "sorted"),
@@ -194,7 +195,7 @@ def test_strided_rows_moe():
     ref, st = oracle.apply_moe(m.x, m.x_per_token, m.y_in, m.slice_widths, wl.slot_ids, wl.expert_ids, wl.E,
                                wl.ranks, scales, m.A, m.B)
     assert st == 0
-    assert_y_close(to_host_bits(y.contiguous()), ref, "strided moe")
+    assert_y_close(to_host_bits(y.contiguous()), ref, f"strided moe {path}")
 
 
 def test_strided_rows_prefill_request_major_tma_tiles():

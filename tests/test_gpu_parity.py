@@ -761,7 +761,7 @@ def test_moe_index_bit_exact(T, K, E, n_adapters, seed):
     assert (err == 4) == (st_r == oracle.ERR_SLOT_RANGE)
 
 
-def _check_moe(wl, mod_idx, what, rows=None):
+def _check_moe(wl, mod_idx, what, rows=None, path="decode_direct"):
     torch = _torch()
     import rank_adapter_gemm_gb300 as L
     from rank_adapter_gemm_gb300.resident import ResidentMoeProjection, to_host_bits
@@ -772,7 +772,7 @@ def _check_moe(wl, mod_idx, what, rows=None):
                   wl.K, wl.E, rp.table)
     ws = L.Workspace(P, rp.shape)
     L.lora_apply_moe(rp.x, rp.y, wl.K, rp.shape, rp.table.dev, idx.sorted_ids, idx.seg_offsets, idx.active, ws.buf,
-                     idx.err, x_per_token=rp.x_per_token)
+                     idx.err, x_per_token=rp.x_per_token, path=path)
     torch.cuda.synchronize()
     assert int(idx.err.item()) == 0
     m = wl.modules[mod_idx]
@@ -787,10 +787,14 @@ def _check_moe(wl, mod_idx, what, rows=None):
     np.testing.assert_array_equal(y[none], m.y_in[none])
 
 
+MOE_PATHS = ["decode_direct", "decode_tma"]
+
+
+@pytest.mark.parametrize("path", MOE_PATHS)
 @pytest.mark.parametrize("mod_idx", [0, 1], ids=["w1_x_per_token", "w2_x_per_pair"])
-def test_apply_moe_mixtral_decode(mod_idx):
+def test_apply_moe_mixtral_decode(mod_idx, path):
     """128 tokens routed top-2 of 8 experts (Mixtral-8x7B expert shapes), 8 adapters."""
-    _check_moe(W.moe_config(), mod_idx, f"moe module {mod_idx}")
+    _check_moe(W.moe_config(), mod_idx, f"moe module {mod_idx} {path}", path=path)
 
 
 MOE_RAGGED = [
@@ -802,8 +806,9 @@ MOE_RAGGED = [
 ]
 
 
+@pytest.mark.parametrize("path", MOE_PATHS)
 @pytest.mark.parametrize("case", MOE_RAGGED, ids=[f"moe{c[0]}" for c in MOE_RAGGED])
-def test_apply_moe_ragged(case):
+def test_apply_moe_ragged(case, path):
     seed, T, K, E, n_ad, k, widths, ranks, per_token = case
     wl = W.generate_moe(name="moe_case", seed=seed, T=T, K=K, E=E, n_adapters=n_ad, rank=8,
                         modules=[{"name": "m", "k": k, "slices": widths, "x_per_token": per_token}],
@@ -815,7 +820,14 @@ def test_apply_moe_ragged(case):
     m = wl.modules[0]
     m.A = [[W._normal_bf16(rng, (E * r, k), k ** -0.5).reshape(E, r, k) for _ in widths] for r in wl.ranks]
     m.B = [[W._normal_bf16(rng, (E * w, r), 0.02).reshape(E, w, r) for w in widths] for r in wl.ranks]
-    _check_moe(wl, 0, f"moe ragged {seed}")
+    if path == "decode_tma" and k % 64 != 0:
+        # the tensor-map path streams x and A in 64-column boxes: k must be a multiple of 64
+        import rank_adapter_gemm_gb300 as L
+        with pytest.raises(L.LoraError) as e:
+            _check_moe(wl, 0, f"moe ragged {seed} {path}", path=path)
+        assert e.value.status == 9
+        return
+    _check_moe(wl, 0, f"moe ragged {seed} {path}", path=path)
 
 
 def test_apply_moe_rejects_too_many_pairs():
@@ -1105,8 +1117,9 @@ def test_plans_of_several_layers_in_one_launch():
         assert_y_close(to_host_bits(rp.y), ref, "batched plans")
 
 
+@pytest.mark.parametrize("path", MOE_PATHS)
 @pytest.mark.parametrize("mod_idx", [0, 1], ids=["w1_x_per_token", "w2_x_per_pair"])
-def test_apply_moe_with_plan(mod_idx):
+def test_apply_moe_with_plan(mod_idx, path):
     """The routed-expert branch through a plan built on the virtual table and the
     pair index (T*K rows)."""
     torch = _torch()
@@ -1118,7 +1131,7 @@ def test_apply_moe_with_plan(mod_idx):
     idx = L.TokenIndex(P, wl.n_adapters * wl.E)
     idx.build_moe(torch.from_numpy(wl.slot_ids).cuda(), torch.from_numpy(wl.expert_ids.reshape(-1).copy()).cuda(),
                   wl.K, wl.E, rp.table)
-    plan = L.Plan(P, rp.shape)
+    plan = L.Plan(P, rp.shape, path=path)
     plan.build(idx, rp.table)
     ws = L.Workspace(P, rp.shape)
     for _ in range(2):
@@ -1133,7 +1146,7 @@ def test_apply_moe_with_plan(mod_idx):
                                 wl.ranks, scales, m.A, m.B)
     assert st == 0
     ref = 2 * once - W.bf16_bits_to_f32(m.y_in).astype(np.float64)
-    assert_y_close(to_host_bits(rp.y), ref, f"moe plan {mod_idx}")
+    assert_y_close(to_host_bits(rp.y), ref, f"moe plan {mod_idx} {path}")
 
 
 def test_plan_for_other_slice_widths_does_nothing_and_reports():
