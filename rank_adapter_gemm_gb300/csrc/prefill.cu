@@ -51,6 +51,7 @@ constexpr int kShrinkThreads = 160;             // warps 0-3 copy + epilogue, wa
 constexpr int kEpiWarps = 8;                    // expand epilogue: two groups of four warps
 constexpr int kExpandThreads = 128 + 32 * kEpiWarps;  // warp 0 MMA, 1 operands, 2-3 y, 4-11 epilogue
 constexpr int kSmemLimit = 227 * 1024;
+constexpr int kClaimRing = 8;                   // expand: ring of the CTA's claimed unit ids
 
 struct PrefillArgs {
     // x as [T][k] in boxes of 128 rows x 64 columns (128-byte swizzle): the
@@ -68,6 +69,7 @@ struct PrefillArgs {
     const int32_t *seg;
     uint16_t *xa_hi;  // [n][T][RP]
     uint16_t *xa_lo;
+    int32_t *claim;   // the expand's unit counter (a workspace word the shrink sets to 0)
     int32_t T;
     int32_t *err;
 };
@@ -142,6 +144,8 @@ __host__ __device__ constexpr uint32_t tmem_cols_for(int c) {
 template <int RP>
 __global__ void __launch_bounds__(kShrinkThreads) tc_shrink_kernel(const __grid_constant__ PrefillArgs a, Shape sh,
                                                                    const void *table, int32_t stages) {
+    // the expand of this call claims its units from a counter that starts at 0
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.claim = 0;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = tc::smem_u32(smem_raw);
     unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -209,8 +213,18 @@ __global__ void __launch_bounds__(kShrinkThreads) tc_shrink_kernel(const __grid_
     if (warp < 4) {
         // ---- producers: x rows (gathered) and the A rows of every slice ----
         const int tid = threadIdx.x;
+        // A stage is published (this thread's copies of it landed) before the
+        // thread waits for the slot it refills next, so the MMA of stage s
+        // waits for the MMA of stage s - 2 (or earlier), not s - 1
         const int depth = stages - 1;
+        int32_t issued = 0, published = 0;
         for (int32_t it = 0; it < nloc; ++it) {
+            if (it >= depth) {
+                tc::cp_wait_group_n(depth - 1);
+                tc::fence_async_smem();
+                tc::mbar_arrive(&full[(it - depth) % stages]);
+                published = it - depth + 1;
+            }
             const int st = it % stages;
             if (it >= stages && !tc::mbar_wait(&empty[st], ((it / stages) - 1) & 1, abort_flag, kWaitNs)) {
                 give_up(a.err, abort_flag);
@@ -244,18 +258,11 @@ __global__ void __launch_bounds__(kShrinkThreads) tc_shrink_kernel(const __grid_
                      v ? A + static_cast<int64_t>(j) * sh.k + col : a.x, v);
             }
             tc::cp_commit();
-            // stage it - depth has landed (this thread's part): publish it to
-            // the MMA thread.  The slot refilled next was published one
-            // iteration ago, so depth = stages - 1 keeps the ring full.
-            if (it >= depth) {
-                tc::cp_wait_group_n(depth);
-                tc::fence_async_smem();
-                tc::mbar_arrive(&full[(it - depth) % stages]);
-            }
+            issued = it + 1;
         }
         tc::cp_wait_all();
         tc::fence_async_smem();
-        for (int32_t it = max(0, nloc - depth); it < nloc; ++it) tc::mbar_arrive(&full[it % stages]);
+        for (int32_t it = published; it < issued; ++it) tc::mbar_arrive(&full[it % stages]);
     } else {
         // ---- MMA issuer: D[:, i*RP .. +RP) += x_tile A_i^T over this CTA's k range;
         // the slices' A rows sit back to back in the stage, so one MMA of N = n RP
@@ -389,6 +396,8 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(const __gr
     int32_t *s_pref = reinterpret_cast<int32_t *>(tmem_slot + 2);  // [S]
     int32_t *s_scr = s_pref + sh.S;                                // [40]
     int32_t *s_seg = s_scr + 40;                                   // [S + 1]
+    volatile int32_t *s_q = s_seg + sh.S + 1;                      // [kClaimRing] claimed unit ids
+    volatile int32_t *s_nq = s_q + kClaimRing;                     // ring entries published
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const TableView tab(table, sh.S, sh.n);
@@ -400,8 +409,33 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(const __gr
         cp.pre[i + 1] = cp.pre[i] + (i < sh.n ? (sh.off[i + 1] - sh.off[i] + kCols - 1) / kCols : 0);
     const int32_t per_tile = cp.pre[sh.n];
     const int64_t U = static_cast<int64_t>(ntiles) * per_tile;
-    const int64_t u_lo = U * blockIdx.x / gridDim.x, u_hi = U * (blockIdx.x + 1) / gridDim.x;
-    if (u_lo >= u_hi) return;
+    if (U >= (int64_t(1) << 30)) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) report_error(a.err, LORA_ERR_INVALID_ARG);
+        return;
+    }
+    // Units are claimed, not split up front: CTA b starts with unit b and then takes
+    // the next unclaimed one (gridDim.x + the counter), so an SM that streams faster
+    // does more of them.  The operand warp claims; entry j of the ring holds the
+    // CTA's j-th unit (-1 once none is left).  Every reader is at most four units
+    // behind the operand warp (its ring of operand stages, the MMA's two
+    // accumulators, the epilogue's release of them), so an entry is reused only
+    // after everyone has read it.
+    if (static_cast<int64_t>(blockIdx.x) >= U) return;
+    auto claimed = [&](int32_t j) -> int32_t {
+        if (*s_nq <= j) {
+            const uint64_t t0 = globaltimer_ns();
+            while (*s_nq <= j) {
+                if (*abort_flag) return -1;
+                if (globaltimer_ns() - t0 > kWaitNs) {
+                    give_up(a.err, abort_flag);
+                    return -1;
+                }
+                __nanosleep(32);
+            }
+        }
+        __threadfence_block();
+        return s_q[j % kClaimRing];
+    };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -417,6 +451,8 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(const __gr
                 tc::mbar_init(&y_empty[b], 4);
             }
             *abort_flag = 0;
+            s_q[0] = static_cast<int32_t>(blockIdx.x);
+            *s_nq = 1;
             tc::mbar_init_fence();
         }
         __syncwarp();
@@ -433,8 +469,8 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(const __gr
         // ---- MMA issuer: acc[b] = xa_hi B^T + xa_lo B^T ----
         if (lane == 0) {
             const uint32_t idesc = tc::idesc_bf16(kTile, kCols);
-            for (int64_t u = u_lo; u < u_hi; ++u) {
-                const int32_t it = static_cast<int32_t>(u - u_lo), b = it & 1;
+            for (int32_t it = 0; claimed(it) >= 0; ++it) {
+                const int32_t b = it & 1;
                 if (!tc::mbar_wait(&op_full[b], (it >> 1) & 1, abort_flag, kWaitNs) ||
                     (it >= 2 && !tc::mbar_wait(&acc_empty[b], ((it >> 1) - 1) & 1, abort_flag, kWaitNs))) {
                     give_up(a.err, abort_flag);
@@ -457,10 +493,17 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(const __gr
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ---- operands: xa hi/lo rows of the tile and the B rows of the chunk ----
-        for (int64_t u = u_lo; u < u_hi; ++u) {
-            const int32_t it = static_cast<int32_t>(u - u_lo), b = it & 1;
+        // ---- operands: xa hi/lo rows of the tile and the B rows of the chunk;
+        // lane 0 claims the next unit while this one's copies are in flight ----
+        int32_t u = static_cast<int32_t>(blockIdx.x);
+        for (int32_t it = 0; u >= 0; ++it) {
+            const int32_t b = it & 1;
             const Unit un = unit_info(u, per_tile, cp, sh, s_pref, s_seg);
+            int32_t nxt = -1;
+            if (lane == 0) {
+                const int64_t v = static_cast<int64_t>(atomicAdd(a.claim, 1)) + gridDim.x;
+                nxt = v < U ? static_cast<int32_t>(v) : -1;
+            }
             const int32_t r_s = tab.rank[un.s];
             const uint16_t *B = reinterpret_cast<const uint16_t *>(tab.b_ptr[un.s * sh.n + un.i]);
             if (it >= 2 && !tc::mbar_wait(&op_empty[b], ((it >> 1) - 1) & 1, abort_flag, kWaitNs)) {
@@ -486,7 +529,13 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(const __gr
             }
             tc::cp_wait_all();
             tc::fence_async_smem();
+            if (lane == 0) {
+                s_q[(it + 1) % kClaimRing] = nxt;
+                __threadfence_block();
+                *s_nq = it + 2;
+            }
             tc::mbar_arrive(&op_full[b]);
+            u = __shfl_sync(0xffffffffu, nxt, 0);
         }
         tc::cp_wait_all();
     } else if (warp < 4) {
@@ -498,8 +547,9 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(const __gr
         int32_t yit = 0;
         bool stop = false;
         int32_t tok[16], tok_next[16];
-        int2 ends = make_int2(0, 0), ends_next;  // the unit's first and last token ids
-        Unit un_next = unit_info(u_lo, per_tile, cp, sh, s_pref, s_seg);
+        int2 ends = make_int2(0, 0), ends_next = make_int2(0, 0);  // the unit's first and last token ids
+        int32_t u_next = claimed(0);
+        Unit un_next = unit_info(u_next >= 0 ? u_next : 0, per_tile, cp, sh, s_pref, s_seg);
         auto fetch = [&](const Unit &un, int32_t (&dst)[16]) {
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
@@ -509,16 +559,12 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(const __gr
             }
             return make_int2(a.sorted_ids[un.p0], a.sorted_ids[un.p0 + un.len - 1]);
         };
-        ends_next = fetch(un_next, tok_next);
-        for (int64_t u = u_lo; u < u_hi && !stop; ++u) {
+        if (u_next >= 0) ends_next = fetch(un_next, tok_next);
+        for (int32_t it = 0; u_next >= 0 && !stop; ++it) {
             const Unit un = un_next;
             ends = ends_next;
 #pragma unroll
             for (int m = 0; m < 16; ++m) tok[m] = tok_next[m];
-            if (u + 1 < u_hi) {
-                un_next = unit_info(u + 1, per_tile, cp, sh, s_pref, s_seg);
-                ends_next = fetch(un_next, tok_next);
-            }
             // a slot's sorted positions hold strictly increasing token ids (the sort
             // is stable), so first and last ids len - 1 apart mean consecutive rows
             const int32_t first = ends.x;
@@ -551,6 +597,12 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(const __gr
                 }
                 tc::cp_arrive_noinc(&y_full[yb]);
             }
+            // the next unit once this one's copies are issued
+            u_next = stop ? -1 : claimed(it + 1);
+            if (u_next >= 0) {
+                un_next = unit_info(u_next, per_tile, cp, sh, s_pref, s_seg);
+                ends_next = fetch(un_next, tok_next);
+            }
         }
         tc::cp_wait_all();
     } else {
@@ -560,14 +612,16 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(const __gr
         const int eq = warp & 3, grp = (warp - 4) >> 2, row = 32 * eq + lane;
         int32_t yit = 0;
         bool stop = false;
-        Unit un_next = unit_info(u_lo, per_tile, cp, sh, s_pref, s_seg);
-        int32_t t_next = row < un_next.len ? a.sorted_ids[un_next.p0 + row] : -1;
-        for (int64_t u = u_lo; u < u_hi && !stop; ++u) {
-            const int32_t it = static_cast<int32_t>(u - u_lo), b = it & 1;
+        int32_t u_next = claimed(0);
+        Unit un_next = unit_info(u_next >= 0 ? u_next : 0, per_tile, cp, sh, s_pref, s_seg);
+        int32_t t_next = u_next >= 0 && row < un_next.len ? a.sorted_ids[un_next.p0 + row] : -1;
+        for (int32_t it = 0; u_next >= 0 && !stop; ++it) {
+            const int32_t b = it & 1;
             const Unit un = un_next;
             const int32_t t = t_next < a.T ? t_next : -1;
-            if (u + 1 < u_hi) {
-                un_next = unit_info(u + 1, per_tile, cp, sh, s_pref, s_seg);
+            u_next = claimed(it + 1);
+            if (u_next >= 0) {
+                un_next = unit_info(u_next, per_tile, cp, sh, s_pref, s_seg);
                 t_next = row < un_next.len ? a.sorted_ids[un_next.p0 + row] : -1;
             }
             if (!__all_sync(0xffffffffu, tc::mbar_wait(&acc_full[b], (it >> 1) & 1, abort_flag, kWaitNs))) {
@@ -647,7 +701,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1) tc_expand_kernel(const __gr
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-size_t table_words(int32_t S) { return sizeof(int32_t) * (2 * static_cast<size_t>(S) + 48); }
+size_t table_words(int32_t S) { return sizeof(int32_t) * (2 * static_cast<size_t>(S) + 48 + kClaimRing + 8); }
 
 size_t shrink_smem(int RP, int n, int stages, int32_t S) {
     return 1024 + static_cast<size_t>(stages) * (kXStage + n * RP * kKB * 2) + 8 * (2 * stages + 1) + 8 +
@@ -754,6 +808,9 @@ cudaError_t launch_prefill(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t 
     a.seg = seg;
     a.xa_hi = reinterpret_cast<uint16_t *>(w + L.hi_off);
     a.xa_lo = reinterpret_cast<uint16_t *>(w + L.lo_off);
+    // a global word of the workspace's control area that no other path of a
+    // prefill call uses
+    a.claim = reinterpret_cast<int32_t *>(w) + 2 * LORA_MAX_SLICES * static_cast<size_t>(sh.S) + 8;
     a.T = T;
     a.err = err;
     switch (tc_rank_pad(sh.r_max)) {
