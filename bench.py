@@ -55,7 +55,8 @@ def parse_args(argv=None):
     p.add_argument("--layers", type=int, default=32)
     p.add_argument("--requests", type=int, default=16, help="prefill_mlp only: requests in the batch")
     p.add_argument("--path", default="best", choices=["best", "auto", "decode_fused", "decode_split", "prefill",
-                                                        "decode_direct", "decode_direct_fp8", "decode_tma"],
+                                                        "decode_direct", "decode_direct_fp8", "decode_tma",
+                                                        "decode_cluster"],
                    help="best: the library's fastest measured path for the workload (default_path); auto: "
                         "LORA_PATH_AUTO (decode_direct_fp8 for a workload with FP8 adapters); decode_moe takes "
                         "decode_direct or decode_tma (best: decode_direct)")
@@ -420,14 +421,16 @@ class ProjectionBench:
 
 def default_path(wl):
     """The library's fastest measured path for a workload: the one-kernel TMA
-    decode path on per-step plans for bf16 decode batches, the FP8 variant of the
-    warp-streaming kernels for FP8 adapters, the tensor-core prefill kernels for
-    long segments."""
+    decode path on per-step plans for bf16 decode batches, AUTO's one cluster per
+    slot for batches of 64 tokens and fewer, the FP8 variant of the warp-streaming
+    kernels for FP8 adapters, the tensor-core prefill kernels for long segments."""
     if wl.weights == "e4m3":
         return "decode_direct_fp8"
     counts = np.bincount(wl.slot_ids[wl.slot_ids >= 0], minlength=wl.S)
     if counts.size and int(counts.max()) > 256:
         return "auto"  # prefill
+    if wl.T <= 64:
+        return "auto"  # the one-cluster-per-slot kernel (LORA_PATH_DECODE_CLUSTER)
     ok = all(wl.r_max <= 64 and len(m.slice_widths) * wl.r_max <= 192 and m.k % 64 == 0 for m in wl.modules)
     return "decode_tma" if ok else "auto"
 

@@ -78,8 +78,9 @@ typedef enum {
     LORA_PATH_AUTO = 0,          /* the prefill kernels if max_seg_hint > LORA_DECODE_MAX_SEG and
                                     r_max <= 64; otherwise, above 64 tokens, the warp-streaming
                                     decode kernels (LORA_PATH_DECODE_DIRECT) when they take the
-                                    shape, else the fused decode path when it does; otherwise
-                                    the split decode kernels */
+                                    shape, else the fused decode path when it does; at 64 tokens
+                                    and fewer LORA_PATH_DECODE_CLUSTER when it takes the shape;
+                                    otherwise the split decode kernels */
     LORA_PATH_DECODE_FUSED = 1,  /* one launch: shrink, per-(slot, slice) wait, expand, on warp-level
                                     MMA; needs T <= 2048, r_max <= 128 and k % 16 == 0 (else
                                     LORA_ERR_UNSUPPORTED) */
@@ -132,7 +133,22 @@ typedef enum {
                                     builds one in the workspace first (two launches); with
                                     lora_build_plan(s) / lora_apply_plan it is one launch per call.
                                     Never chosen by LORA_PATH_AUTO, whose table may lack the
-                                    tensor maps */
+                                    tensor maps */,
+    LORA_PATH_DECODE_CLUSTER = 9 /* small batches in one launch: one thread-block cluster of 16
+                                    CTAs (8 where only those tiles fit) per slot.  Each CTA
+                                    multiplies the slot's x rows by A over 1/16 (1/8) of k
+                                    (warp MMA, fp32), the partial sums meet in distributed
+                                    shared memory (added in CTA-rank order), and each CTA
+                                    applies B to 1/16 (1/8) of every slice's columns, y read and
+                                    written once.  Tokens are taken 16 at a time.  Launched as a
+                                    programmatic dependent of the previous kernel on the stream:
+                                    it reads the slot table, the index and the adapter weights
+                                    before that kernel has finished (x and y after), so none of
+                                    those may be written by the kernel directly before it
+                                    (lora_build_index and the plan builders never start a
+                                    dependent early).  Needs k % 8 == 0, every slice offset % 8
+                                    == 0, r_max <= 256 and a CTA's tiles within 227 KB of shared
+                                    memory (else LORA_ERR_UNSUPPORTED).  Uses no workspace */
 } lora_path_t;
 
 #define LORA_DECODE_MAX_SEG 256

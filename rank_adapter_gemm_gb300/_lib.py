@@ -33,7 +33,7 @@ STATUS = {
 globals().update({name: code for code, name in STATUS.items()})
 
 PATHS = {"auto": 0, "decode_fused": 1, "decode_split": 2, "prefill": 3, "decode_tc": 4, "decode_stream": 5,
-         "decode_direct": 6, "decode_direct_fp8": 7, "decode_tma": 8}
+         "decode_direct": 6, "decode_direct_fp8": 7, "decode_tma": 8, "decode_cluster": 9}
 
 # Every function the header declares, for the export check.
 EXPORTED = (

@@ -59,6 +59,10 @@ cudaError_t launch_tma_plans(const Shape &sh, const void *const *tables, unsigne
 cudaError_t launch_tma_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                               const unsigned char *plan, float *acc0, float *acc1, int32_t *ctrl, int32_t T,
                               int32_t *err, cudaStream_t stream, int32_t xdiv = 1);
+bool cluster_decode_supported(int32_t T, const Shape &sh);
+cudaError_t launch_cluster_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
+                                  const void *table, const int32_t *sorted_ids, const int32_t *seg, int32_t T,
+                                  int32_t *err, cudaStream_t stream);
 }  // namespace lora
 
 using lora::Shape;
@@ -86,14 +90,19 @@ lora_path_t resolve(lora_path_t path, int32_t T, int32_t max_seg_hint, const Sha
     if (max_seg_hint <= 0 || max_seg_hint > T) max_seg_hint = T;
     if (path == LORA_PATH_AUTO) {
         // measured on GB300: the warp-streaming kernels lead from a few hundred
-        // tokens up; at 64 tokens and fewer the split kernels' shorter prologue wins
+        // tokens up; at 64 tokens and fewer the one-cluster-per-slot kernel (a
+        // 64-token q_proj call: 8.8 us against 11.0 for the split kernels)
         if (max_seg_hint > LORA_DECODE_MAX_SEG && lora::prefill_supported(sh.r_max)) path = LORA_PATH_PREFILL;
         else if (T > kSmallDecodeT && lora::decode_direct_supported(T, sh, false)) path = LORA_PATH_DECODE_DIRECT;
         else if (T > kSmallDecodeT && fused_ok(T, sh)) path = LORA_PATH_DECODE_FUSED;
+        else if (T <= kSmallDecodeT && lora::cluster_decode_supported(T, sh)) path = LORA_PATH_DECODE_CLUSTER;
         else path = LORA_PATH_DECODE_SPLIT;
     }
     if (launches != nullptr)
-        *launches = (path == LORA_PATH_DECODE_FUSED && lora::fused_decode_supported(T, sh.r_max, sh.k)) ? 1 : 2;
+        *launches = ((path == LORA_PATH_DECODE_FUSED && lora::fused_decode_supported(T, sh.r_max, sh.k)) ||
+                     path == LORA_PATH_DECODE_CLUSTER)
+                        ? 1
+                        : 2;
     return path;
 }
 
@@ -417,6 +426,10 @@ lora_status_t lora_apply_ex(const void *x, int64_t ldx, void *y, int64_t ldy, in
             return LORA_ERR_CUDA;
         return tma_call(x, ldx, y, ldy, T, sh, plan, ws, err, s);
     }
+    case LORA_PATH_DECODE_CLUSTER:
+        if (!lora::cluster_decode_supported(T, sh)) return LORA_ERR_UNSUPPORTED;
+        return from_cuda(lora::launch_cluster_decode(xb, ldx, yb, ldy, sh, dev_table, sorted_ids, seg_offsets, T, err,
+                                                     s));
     default:
         return LORA_ERR_INVALID_ARG;
     }

@@ -44,6 +44,29 @@ def oracle_y_e4m3(wl, mod_idx=0, rows=None):
     return oracle.apply_e4m3(m.x, m.y_in, m.slice_widths, wl.slot_ids, wl.ranks, scales, m.A, B, rows=rows)
 
 
+def cluster_ok(wl, mod_idx=0):
+    """Shapes the one-cluster-per-slot decode path takes: k and every slice offset
+    multiples of 8, r_max <= 256, and a CTA's tiles (A and x over 1/KS of k, the
+    partial and sums tiles, B and y over 1/KS of the columns) within 227 KB for a
+    cluster of 8 or 16 CTAs."""
+    m = wl.modules[mod_idx]
+    k, widths, n = m.k, list(m.slice_widths), len(m.slice_widths)
+    offs = np.concatenate([[0], np.cumsum(widths)])
+    if k % 8 or any(int(o) % 8 for o in offs) or wl.r_max > 256:
+        return False
+    rp8, rp16 = -(-wl.r_max // 8) * 8, -(-wl.r_max // 16) * 16
+    for ks in (8, 16):
+        kcw = -(-(k // 8) // ks) * 8
+        ars = -(-kcw // 16) * 16 + 8
+        ncol = sum(-(-(-(-w // ks)) // 8) * 8 for w in widths)
+        srs, yrs = n * rp16 + 8, ncol + 8
+        size = (n * rp8 * ars * 2 + 16 * ars * 2 + 16 * n * rp8 * 4 + 2 * 16 * srs * 2 + ncol * (rp16 + 8) * 2
+                + 16 * yrs * 2 + 16 * 4)
+        if size <= 227 * 1024:
+            return True
+    return False
+
+
 def gpu_apply(wl, mod_idx=0, path="auto", max_seg_hint=0, repeat=1, pack_a=True):
     import torch
     import rank_adapter_gemm_gb300 as L

@@ -106,7 +106,8 @@ class Guarded:
         return to_host_bits(self.y.contiguous())
 
 
-@pytest.mark.parametrize("path", ["decode_split", "decode_fused", "decode_direct", "decode_tma", "prefill", "auto"])
+@pytest.mark.parametrize("path", ["decode_split", "decode_fused", "decode_direct", "decode_tma", "decode_cluster",
+                                  "prefill", "auto"])
 def test_strided_rows_and_guard_bands(path):
     """The packed QKV decode config through every path, x and y column windows."""
     wl = W.config(2)

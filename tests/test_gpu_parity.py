@@ -10,11 +10,11 @@ import pytest
 
 import oracle
 import workloads as W
-from _parity import assert_y_close, gpu_apply, oracle_y, untouched_rows
+from _parity import assert_y_close, cluster_ok, gpu_apply, oracle_y, untouched_rows
 
 pytestmark = pytest.mark.gpu
 
-DECODE_PATHS = ["decode_split", "decode_fused", "decode_direct", "decode_tma"]
+DECODE_PATHS = ["decode_split", "decode_fused", "decode_direct", "decode_tma", "decode_cluster"]
 
 
 def tma_ok(wl, mod_idx=0):
@@ -181,6 +181,7 @@ def test_index_deterministic_over_runs():
 @pytest.mark.parametrize("y_init", ["zeros", "normal"])
 def test_apply_configs_full(cfg, y_init, path):
     wl = W.config(cfg, y_init=y_init)
+    assert path != "decode_cluster" or cluster_ok(wl)
     y, err, *_ = gpu_apply(wl, path=path)
     assert err == 0
     ref, st = oracle_y(wl)
@@ -194,6 +195,7 @@ def test_apply_configs_full(cfg, y_init, path):
 def test_apply_large_decode_sampled(path):
     """T=1024, k=d=8192, r=64, S=128: all rows checked (the oracle takes seconds)."""
     wl = W.config(4)
+    assert path != "decode_cluster" or cluster_ok(wl)
     y, err, *_ = gpu_apply(wl, path=path)
     assert err == 0
     rows = np.arange(wl.T, dtype=np.int32)
@@ -206,6 +208,12 @@ def test_apply_large_decode_sampled(path):
 def test_apply_layer_sweep_sampled(mod_idx, path):
     """The four packed projections of one Llama-3-8B layer at T=1024, r=64."""
     wl = W.config(4, sweep=True)
+    if path == "decode_cluster" and not cluster_ok(wl, mod_idx):
+        import rank_adapter_gemm_gb300 as L
+        with pytest.raises(L.LoraError) as e:  # a CTA's B and y tiles exceed its shared memory
+            gpu_apply(wl, mod_idx=mod_idx, path=path)
+        assert e.value.status == 9
+        return
     y, err, *_ = gpu_apply(wl, mod_idx=mod_idx, path=path)
     assert err == 0
     rng = np.random.default_rng(mod_idx)
@@ -275,7 +283,7 @@ def test_apply_ragged(case, path):
         return
     mma_ok = wl.r_max <= 128 and k % 16 == 0  # the fused warp-MMA kernel
     if ((path == "decode_fused" and not mma_ok) or (path == "decode_direct" and wl.r_max > 64)
-            or (path == "decode_tma" and not tma_ok(wl))):
+            or (path == "decode_tma" and not tma_ok(wl)) or (path == "decode_cluster" and not cluster_ok(wl))):
         import rank_adapter_gemm_gb300 as L
         with pytest.raises(L.LoraError) as e:
             gpu_apply(wl, path=path)
@@ -372,7 +380,7 @@ def test_apply_is_deterministic():
         np.testing.assert_array_equal(y, ys[0])
 
 
-@pytest.mark.parametrize("path", ["decode_fused", "decode_direct", "decode_tma"])
+@pytest.mark.parametrize("path", ["decode_fused", "decode_direct", "decode_tma", "decode_cluster"])
 def test_fused_repeat_stays_within_tolerance(path):
     """The fused kernels add split-k partials with fp32 reductions, whose order
     varies; every repetition must still match the oracle."""
@@ -925,12 +933,13 @@ def test_apply_activated_decode_qkv():
 
 
 
-@pytest.mark.parametrize("path", ["auto", "decode_split", "decode_fused", "decode_direct", "prefill", "decode_tma"])
+@pytest.mark.parametrize("path", ["auto", "decode_split", "decode_fused", "decode_direct", "prefill", "decode_tma",
+                                  "decode_cluster"])
 def test_apply_ranks_up_to_512(path):
     """Ranks 512 and 264 next to 8: the split kernels (AUTO's choice above rank 128)
     take any rank in 64-wide chunks; the paths with a lower rank bound refuse."""
     wl = _small(81, 100, 1024, [1024, 256], 3, [512, 264, 8])
-    if path in ("decode_fused", "decode_direct", "prefill", "decode_tma"):
+    if path in ("decode_fused", "decode_direct", "prefill", "decode_tma", "decode_cluster"):
         import rank_adapter_gemm_gb300 as L
         with pytest.raises(L.LoraError) as e:
             gpu_apply(wl, path=path)
