@@ -146,9 +146,10 @@ typedef enum {
                                     before that kernel has finished (x and y after), so none of
                                     those may be written by the kernel directly before it
                                     (lora_build_index and the plan builders never start a
-                                    dependent early).  Needs k % 8 == 0, every slice offset % 8
-                                    == 0, r_max <= 256 and a CTA's tiles within 227 KB of shared
-                                    memory (else LORA_ERR_UNSUPPORTED).  Uses no workspace */
+                                    dependent early).  Needs r_max <= 256 and a CTA's tiles
+                                    (A and x over its share of k, B and y over its share of the
+                                    columns) within 227 KB of shared memory (else
+                                    LORA_ERR_UNSUPPORTED).  Uses no workspace */
 } lora_path_t;
 
 #define LORA_DECODE_MAX_SEG 256

@@ -233,3 +233,37 @@ def test_host_checks_of_the_tma_entry_points(L):
                                P((1 << 20) + 8), b, None, None) == 2
     assert lib.lora_apply_plan(fake, 4096, fake, 6144, 256, ctypes.byref(sh), fake, 128, _lib.PATHS["decode_tma"],
                                fake, 1 << 30, None, None) == 6
+
+
+def test_host_checks_of_the_cluster_path(L):
+    """The one-cluster-per-slot decode path: AUTO's choice at 64 tokens and fewer,
+    one launch per call, and the shapes it refuses before any device call (k or
+    a slice offset not a multiple of 8, r_max above 256, tiles beyond a CTA's
+    shared memory)."""
+    import ctypes
+    from rank_adapter_gemm_gb300 import _lib
+    lib = _lib.load()
+    assert L.lora_resolve_path("auto", 1) == ("decode_cluster", 1)
+    assert L.lora_resolve_path("auto", 64) == ("decode_cluster", 1)
+    assert L.lora_resolve_path("auto", 65)[0] == "decode_direct"
+    assert L.lora_resolve_path("decode_cluster", 4096) == ("decode_cluster", 1)
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # never dereferenced: every call below fails its host checks first
+    cluster = _lib.PATHS["decode_cluster"]
+    # k or a slice width not a multiple of 8: every path's shape check (alignment)
+    for bad in (L.make_shape(8, 16, 4100, [4096]), L.make_shape(8, 16, 4096, [1028, 1020])):
+        d = int(bad.slice_offsets[bad.n_slices])
+        assert lib.lora_apply_ex(fake, 4104, fake, 4096, 64, ctypes.byref(bad), fake, fake, fake, fake, 0, cluster,
+                                 fake, 1 << 30, None, None) == 2
+    for bad in (L.make_shape(8, 264, 4096, [4096]),          # r_max above 256
+                L.make_shape(8, 64, 4096, [14336, 14336])):  # B and y tiles beyond 227 KB
+        d = int(bad.slice_offsets[bad.n_slices])
+        ws = L.lora_workspace_bytes(64, bad)
+        assert lib.lora_apply_ex(fake, bad.k, fake, d, 64, ctypes.byref(bad), fake, fake, fake, fake, 0, cluster,
+                                 fake, ws, None, None) == 9
+    # plans and the routed-expert entry points do not take it
+    sh = L.make_shape(8, 16, 4096, [4096])
+    assert lib.lora_build_plan(64, ctypes.byref(sh), fake, fake, fake, fake, cluster, fake,
+                               lib.lora_plan_bytes(64, ctypes.byref(sh)), None, None) == 9
+    assert lib.lora_apply_moe_ex(fake, 4096, 1, fake, 4096, 32, 2, ctypes.byref(sh), fake, fake, fake, fake, cluster,
+                                 fake, L.lora_workspace_bytes(64, sh), None, None) == 9
