@@ -691,7 +691,8 @@ class MoeBench:
             # about 24.3 us per call, and the TMA plans cost 17 us more per step
             path = "decode_direct"
         self.path = path
-        self.plans = [] if no_plan else [L.Plan(P, lay.shape, path=path, device=dev) for lay in self.layers]
+        self.plans = ([] if no_plan or path == "decode_cluster"  # the cluster kernel has no plan
+                      else [L.Plan(P, lay.shape, path=path, device=dev) for lay in self.layers])
         self.bytes_per_call = [moe_algorithmic_bytes(wl, m) for m in self.mods]
 
     def index_part(self):
@@ -719,7 +720,7 @@ def run_moe(args):
     dev = torch.device("cuda", local)
     wl = W.moe_config()
     mb = MoeBench(wl, args.layers, dev, no_plan=args.no_plan,
-                  path=args.path if args.path in ("decode_direct", "decode_tma") else None)
+                  path=args.path if args.path in ("decode_direct", "decode_tma", "decode_cluster") else None)
     elapsed_s, apply_ms_mean, index_ms_mean, clocks, (peak_gbs, peak_tf, peak_src) = \
         time_steps(args, dev, local, mb.index_part, mb.apply_part)
     err = int(mb.index.err.item())

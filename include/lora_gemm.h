@@ -597,8 +597,10 @@ lora_status_t lora_apply_moe_plan(const void *x, int64_t ldx, int32_t x_per_toke
 
 /*
  * lora_apply_moe on an explicit path: LORA_PATH_DECODE_DIRECT (what
- * lora_apply_moe runs) or LORA_PATH_DECODE_TMA, the one-kernel tensor-map
- * decode over the pairs.  The TMA path needs dev_table to be a table of
+ * lora_apply_moe runs), LORA_PATH_DECODE_TMA, the one-kernel tensor-map
+ * decode over the pairs, or LORA_PATH_DECODE_CLUSTER, one cluster per virtual
+ * slot (its limits as in lora_apply_ex; the workspace is not used).  The TMA
+ * path needs dev_table to be a table of
  * lora_set_slot_table_tma over the virtual slots (the entries of
  * lora_moe_slot_pointers), x 16-byte aligned with ldx a multiple of 8, and
  * T K and the shape within the limits of LORA_PATH_DECODE_TMA in lora_apply_ex;

@@ -88,6 +88,7 @@ struct CArgs {
     const int32_t *seg;
     int32_t *err;
     int32_t T;
+    int32_t xdiv;  // x row of y row t: t / xdiv (routed experts sharing a token's x row)
 };
 
 __device__ __forceinline__ uint32_t lds32(const uint16_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
@@ -219,8 +220,9 @@ __global__ void __launch_bounds__(kCThreads) cluster_decode_kernel(const CArgs a
             for (int32_t e = tid; e < kCTok * chunks; e += kCThreads) {
                 const int32_t row = e / chunks, ch = e % chunks, t = s_tok[row];
                 const bool v = t >= 0 && ch * 8 < kcw;
+                const int64_t xr = a.xdiv == 1 ? t : t / a.xdiv;
                 tc::cp16(base + L.x_off + static_cast<uint32_t>((row * L.ars + ch * 8) * 2),
-                         v ? a.x + static_cast<int64_t>(t) * a.ldx + kc0 + ch * 8 : static_cast<const void *>(a.x), v);
+                         v ? a.x + xr * a.ldx + kc0 + ch * 8 : static_cast<const void *>(a.x), v);
             }
             int32_t colbase = 0;
             for (int i = 0; i < sh.n; ++i) {
@@ -369,8 +371,8 @@ bool cluster_decode_supported(int32_t T, const Shape &sh) {
 
 cudaError_t launch_cluster_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                   const void *table, const int32_t *sorted_ids, const int32_t *seg, int32_t T,
-                                  int32_t *err, cudaStream_t stream) {
-    if (!cluster_decode_supported(T, sh)) return cudaErrorNotSupported;
+                                  int32_t *err, cudaStream_t stream, int32_t xdiv) {
+    if (!cluster_decode_supported(T, sh) || xdiv < 1 || T % xdiv != 0) return cudaErrorNotSupported;
     const int32_t KS = cluster_size_for(sh);
     const CLayout L = c_layout(sh, KS);
     cudaError_t e = cudaFuncSetAttribute(cluster_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -380,7 +382,7 @@ cudaError_t launch_cluster_decode(const uint16_t *x, int64_t ldx, uint16_t *y, i
         e = cudaFuncSetAttribute(cluster_decode_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
     }
-    CArgs a{x, ldx, y, ldy, table, sorted_ids, seg, err, T};
+    CArgs a{x, ldx, y, ldy, table, sorted_ids, seg, err, T, xdiv};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(KS), static_cast<unsigned>(sh.S));
     cfg.blockDim = dim3(kCThreads);

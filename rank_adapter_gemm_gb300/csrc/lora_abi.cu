@@ -62,7 +62,7 @@ cudaError_t launch_tma_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int64
 bool cluster_decode_supported(int32_t T, const Shape &sh);
 cudaError_t launch_cluster_decode(const uint16_t *x, int64_t ldx, uint16_t *y, int64_t ldy, const Shape &sh,
                                   const void *table, const int32_t *sorted_ids, const int32_t *seg, int32_t T,
-                                  int32_t *err, cudaStream_t stream);
+                                  int32_t *err, cudaStream_t stream, int32_t xdiv = 1);
 }  // namespace lora
 
 using lora::Shape;
@@ -490,9 +490,16 @@ lora_status_t lora_apply_moe_ex(const void *x, int64_t ldx, int32_t x_per_token,
     if ((st = check_rows(x, ldx, x_per_token ? T : P, sh.k)) != LORA_OK) return st;
     if ((st = check_rows(y, ldy, P, sh.off[sh.n])) != LORA_OK) return st;
     if ((st = check_ws(ws, ws_bytes, P, sh)) != LORA_OK) return st;
-    if (path != LORA_PATH_DECODE_DIRECT && path != LORA_PATH_DECODE_TMA) return LORA_ERR_UNSUPPORTED;
+    if (path != LORA_PATH_DECODE_DIRECT && path != LORA_PATH_DECODE_TMA && path != LORA_PATH_DECODE_CLUSTER)
+        return LORA_ERR_UNSUPPORTED;
     if (P == 0) return LORA_OK;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (path == LORA_PATH_DECODE_CLUSTER) {
+        if (!lora::cluster_decode_supported(P, sh)) return LORA_ERR_UNSUPPORTED;
+        return from_cuda(lora::launch_cluster_decode(static_cast<const uint16_t *>(x), ldx, static_cast<uint16_t *>(y),
+                                                     ldy, sh, dev_table, sorted_ids, seg_offsets, P, err, s,
+                                                     x_per_token ? K : 1));
+    }
     if (path == LORA_PATH_DECODE_TMA) {
         if (!lora::decode_tma_supported(P, sh)) return LORA_ERR_UNSUPPORTED;
         const lora::WorkspaceLayout L(P, sh.n, sh.r_max, sh.S);

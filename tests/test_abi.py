@@ -261,9 +261,9 @@ def test_host_checks_of_the_cluster_path(L):
         ws = L.lora_workspace_bytes(64, bad)
         assert lib.lora_apply_ex(fake, bad.k, fake, d, 64, ctypes.byref(bad), fake, fake, fake, fake, 0, cluster,
                                  fake, ws, None, None) == 9
-    # plans and the routed-expert entry points do not take it
+    # plans (also the routed-expert plan entry point) do not take it
     sh = L.make_shape(8, 16, 4096, [4096])
     assert lib.lora_build_plan(64, ctypes.byref(sh), fake, fake, fake, fake, cluster, fake,
                                lib.lora_plan_bytes(64, ctypes.byref(sh)), None, None) == 9
-    assert lib.lora_apply_moe_ex(fake, 4096, 1, fake, 4096, 32, 2, ctypes.byref(sh), fake, fake, fake, fake, cluster,
-                                 fake, L.lora_workspace_bytes(64, sh), None, None) == 9
+    assert lib.lora_apply_moe_plan_ex(fake, 4096, 1, fake, 4096, 32, 2, ctypes.byref(sh), fake, 1 << 20, cluster,
+                                      fake, L.lora_workspace_bytes(64, sh), None, None) == 9

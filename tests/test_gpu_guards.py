@@ -163,7 +163,7 @@ def test_strided_rows_prefill_long_segments():
     assert_y_close(g.y_bits(), ref, "strided prefill")
 
 
-@pytest.mark.parametrize("path", ["decode_direct", "decode_tma"])
+@pytest.mark.parametrize("path", ["decode_direct", "decode_tma", "decode_cluster"])
 def test_strided_rows_moe(path):
     """Routed experts: y per (token, choice) pair in a column window, x per token
     in a column window, guarded pair index and workspace."""

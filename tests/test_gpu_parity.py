@@ -795,7 +795,7 @@ def _check_moe(wl, mod_idx, what, rows=None, path="decode_direct"):
     np.testing.assert_array_equal(y[none], m.y_in[none])
 
 
-MOE_PATHS = ["decode_direct", "decode_tma"]
+MOE_PATHS = ["decode_direct", "decode_tma", "decode_cluster"]
 
 
 @pytest.mark.parametrize("path", MOE_PATHS)
@@ -1126,7 +1126,7 @@ def test_plans_of_several_layers_in_one_launch():
         assert_y_close(to_host_bits(rp.y), ref, "batched plans")
 
 
-@pytest.mark.parametrize("path", MOE_PATHS)
+@pytest.mark.parametrize("path", ["decode_direct", "decode_tma"])
 @pytest.mark.parametrize("mod_idx", [0, 1], ids=["w1_x_per_token", "w2_x_per_pair"])
 def test_apply_moe_with_plan(mod_idx, path):
     """The routed-expert branch through a plan built on the virtual table and the
