@@ -135,11 +135,10 @@ typedef enum {
                                     Never chosen by LORA_PATH_AUTO, whose table may lack the
                                     tensor maps */,
     LORA_PATH_DECODE_CLUSTER = 9 /* small batches in one launch: one thread-block cluster of 16
-                                    CTAs (8 where only those tiles fit) per slot.  Each CTA
-                                    multiplies the slot's x rows by A over 1/16 (1/8) of k
-                                    (warp MMA, fp32), the partial sums meet in distributed
-                                    shared memory (added in CTA-rank order), and each CTA
-                                    applies B to 1/16 (1/8) of every slice's columns, y read and
+                                    CTAs per slot.  Each CTA multiplies the slot's x rows by A
+                                    over 1/16 of k (warp MMA, fp32), the partial sums meet in
+                                    distributed shared memory (added in CTA-rank order), and
+                                    each CTA applies B to 1/16 of every slice's columns, y read and
                                     written once.  Tokens are taken 16 at a time.  Launched as a
                                     programmatic dependent of the previous kernel on the stream:
                                     it reads the slot table, the index and the adapter weights

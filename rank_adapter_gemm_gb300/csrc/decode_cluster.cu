@@ -5,7 +5,8 @@
 //     y[t, o_i + m] += scale_s * sum_j (sum_c x[t, c] A_{s,i}[j, c]) B_{s,i}[m, j].
 // With few tokens per slot the call moves a few megabytes and is bound by the
 // latency of its dependent steps.  This kernel keeps every step of a slot inside
-// one cluster of KS CTAs (16, or 8 where only those tiles fit a CTA):
+// one cluster of KS = 16 CTAs (a cluster size above the portable 8, which this
+// GPU allows):
 //   - CTA c reads A_{s,i} rows over its share of k and the slot's x rows for
 //     that share, and computes partial sums with warp MMAs (m16n8k16, bf16 in,
 //     fp32 out);
@@ -352,12 +353,11 @@ __global__ void __launch_bounds__(kCThreads) cluster_decode_kernel(const CArgs a
     }
 }
 
-// Cluster size: 16 CTAs (twice the copy streams of 8; measured faster on a
-// 64-token q_proj call), or 8 where only those tiles fit.
+// Cluster size: 16 CTAs (twice the copy streams of 8, measured faster on a
+// 64-token q_proj call; a CTA's tiles only shrink as the cluster grows, so a
+// shape that does not fit 16 fits no smaller cluster either); 0: unsupported.
 int32_t cluster_size_for(const Shape &sh) {
-    if (c_layout(sh, 16).bytes <= static_cast<uint32_t>(kCSmemLimit)) return 16;
-    if (c_layout(sh, 8).bytes <= static_cast<uint32_t>(kCSmemLimit)) return 8;
-    return 0;
+    return c_layout(sh, 16).bytes <= static_cast<uint32_t>(kCSmemLimit) ? 16 : 0;
 }
 
 }  // namespace

@@ -46,16 +46,15 @@ def oracle_y_e4m3(wl, mod_idx=0, rows=None):
 
 def cluster_ok(wl, mod_idx=0):
     """Shapes the one-cluster-per-slot decode path takes: k and every slice offset
-    multiples of 8, r_max <= 256, and a CTA's tiles (A and x over 1/KS of k, the
-    partial and sums tiles, B and y over 1/KS of the columns) within 227 KB for a
-    cluster of 8 or 16 CTAs."""
+    multiples of 8, r_max <= 256, and a CTA's tiles (A and x over 1/16 of k, the
+    partial and sums tiles, B and y over 1/16 of the columns) within 227 KB."""
     m = wl.modules[mod_idx]
     k, widths, n = m.k, list(m.slice_widths), len(m.slice_widths)
     offs = np.concatenate([[0], np.cumsum(widths)])
     if k % 8 or any(int(o) % 8 for o in offs) or wl.r_max > 256:
         return False
     rp8, rp16 = -(-wl.r_max // 8) * 8, -(-wl.r_max // 16) * 16
-    for ks in (8, 16):
+    for ks in (16,):
         kcw = -(-(k // 8) // ks) * 8
         ars = -(-kcw // 16) * 16 + 8
         ncol = sum(-(-(-(-w // ks)) // 8) * 8 for w in widths)
